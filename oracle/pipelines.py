@@ -1,0 +1,104 @@
+"""The five workloads end to end, step by step (oracle; test infrastructure).
+
+Each function follows the call order the pages give (SparseEngine "How it
+works": finish_step for SnapKV / H2O at the end of prefill, then the decode
+selection hooks; KARA Method section 3: periodic compression of the trailing
+window) and returns every intermediate so tests can compare stage by stage.
+``groups`` / ``seqs`` restrict the float work and the data movement to a
+sample of (sequence, KV head) pairs / sequences for full-size checks.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import attention, cache, quest, scoring, selection
+from .cache import Cache, values
+
+
+def to_f64(t) -> np.ndarray:
+    """Torch tensor (bf16 / fp32) or numpy array -> fp64 values."""
+    if hasattr(t, "detach"):
+        return values(cache._bits(t))
+    return np.asarray(t, dtype=np.float64)
+
+
+def snapkv(c: Cache, q_win, q_pos, q_dec, shape):
+    """SnapKV after the last prompt chunk: score, pool + top-k, compact, decode."""
+    B, ctx, w = c.B, int(c.ctx_len[0]), shape.window
+    scored = ctx - w
+    s = scoring.score_window(c, q_win, q_pos, [0] * B, [ctx] * B, [0] * B, [scored] * B,
+                             causal=True)
+    keep = [[selection.topk_keep(s[(b, h)], 0, shape.keep_topk, shape.pool_kernel, scored, ctx)
+             for h in range(c.Hkv)] for b in range(B)]
+    st = cache.compact(c, keep, [0] * B)
+    assert st == cache.SE_OK
+    o, _ = attention.decode_attention(c, to_f64(q_dec), "dense")
+    return dict(scores=s, keep=keep, o=o)
+
+
+def quest_step(c: Cache, kmin, kmax, q, top_pages: int, groups=None):
+    """One Quest decode step: page bound, top pages + current page, attention."""
+    qv = to_f64(q)
+    pairs = groups if groups is not None else [(b, g) for b in range(c.B) for g in range(c.Hkv)]
+    sel = {}
+    bounds = {}
+    for b, g in pairs:
+        sel[(b, g)], bounds[(b, g)] = quest.select_pages(c, kmin, kmax, qv[b], top_pages, b, g)
+    selb = {b: {g: sel[(b, g)] for (bb, g) in sel if bb == b} for b in {p[0] for p in pairs}}
+    o, _ = attention.decode_attention(c, qv, "pages", selb, groups=pairs)
+    return dict(sel=sel, bounds=bounds, o=o)
+
+
+def h2o_prefill(c: Cache, q_prompt, q_pos, shape, acc: np.ndarray):
+    """H2O at the end of prefill, reading (viii): causal scores of the whole
+    prompt become the initial running scores; keep the top ``heavy`` of the
+    non-recent prefix plus the ``recent`` last tokens."""
+    B, ctx = c.B, int(c.ctx_len[0])
+    s = scoring.score_window(c, q_prompt, q_pos, [0] * B, [ctx] * B, [0] * B, [ctx] * B,
+                             causal=True)
+    for (b, h), v in s.items():
+        acc[b, h, :ctx] = v
+    keep = [[selection.topk_keep(s[(b, h)][: ctx - shape.recent], 0, shape.heavy, 1,
+                                 ctx - shape.recent, ctx)
+             for h in range(c.Hkv)] for b in range(B)]
+    st = cache.compact(c, keep, [0] * B, aux=acc)
+    assert st == cache.SE_OK
+    return dict(scores=s, keep=keep)
+
+
+def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
+    """One H2O decode step: append, dense attention, add this step's
+    group-summed weights to the running scores, evict one if over budget."""
+    kb, vb = cache._bits(k_new), cache._bits(v_new)
+    st = cache.append(c, kb, vb, aux=acc)
+    assert st == cache.SE_OK
+    o, psums = attention.decode_attention(c, to_f64(q), "dense")
+    for (b, g), (slots, p) in psums.items():
+        acc[b, g, slots] += p
+    victim = np.full((c.B, c.Hkv), -1, dtype=np.int64)
+    for b in range(c.B):
+        recent_from = int(c.logical_len[b]) - shape.recent
+        for g in range(c.Hkv):
+            victim[b, g] = selection.h2o_victim(acc[b, g], c.slot_map[b, g], int(c.ctx_len[b]),
+                                                shape.budget, recent_from)
+    st = cache.move_last(c, victim, aux=acc)
+    assert st == cache.SE_OK
+    return dict(o=o, victim=victim)
+
+
+def kara_compress(c: Cache, q_win, q_pos, shape, groups=None, seqs=None):
+    """Kara periodic compression of the trailing window: bidirectional scores of
+    the compressible keys, Token2Chunk retention, compaction from the window."""
+    B = c.B
+    ctx = [int(x) for x in c.ctx_len]
+    win_lo = [x - shape.window for x in ctx]
+    prot_lo = [x - shape.protected for x in ctx]
+    s = scoring.score_window(c, q_win, q_pos, win_lo, ctx, win_lo, prot_lo, causal=False,
+                             groups=groups)
+    keep = [[None] * c.Hkv for _ in range(B)]
+    for b in range(B):
+        for h in range(c.Hkv):
+            if (b, h) in s:
+                keep[b][h] = selection.kara_keep(s[(b, h)], win_lo[b], shape.candidates,
+                                                 shape.budget, shape.chunk_coef, prot_lo[b], ctx[b])
+    return dict(scores=s, keep=keep, first_slot=win_lo)

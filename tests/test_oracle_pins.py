@@ -1,0 +1,604 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each pin uses an independent source: torch library routines (scaled dot
+product attention with V = I gives the attention probabilities, avg_pool1d),
+Python's ``sorted`` as a brute-force ranking, closed forms, invariants of the
+page accounting, and hand-worked fixtures under tests/golden/.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention, cache, pipelines, quest, scoring, selection
+from oracle.cache import values
+import se_workloads as W
+from tests.helpers import sdpa_out, sdpa_probs, tiny_cache, tiny_shape
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def oc(pc):
+    return cache.from_tensors(pc)
+
+
+# ---------------------------------------------------------------------------
+# O1 window scoring
+# ---------------------------------------------------------------------------
+
+
+def _set_identical_keys(pc):
+    """Every resident key of head h equal to one vector (per head)."""
+    for h in range(pc.Hkv):
+        kvec = torch.arange(pc.D, dtype=torch.float32) * 0.25 - 1.0 + h
+        pc.k_pool[:, h, :, :] = kvec.to(pc.k_pool.dtype)
+
+
+def test_scores_identical_keys_causal_closed_form():
+    # equal logits: each row spreads 1/(#visible) over its visible keys; a
+    # query at position t sees t+1 keys, so s_j = G * sum_{t_q >= j} 1/(t_q+1)
+    shape = tiny_shape(ctx=22)
+    pc = tiny_cache(shape)
+    _set_identical_keys(pc)
+    c = oc(pc)
+    w = 6
+    q = torch.randn(shape.B, w, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "q"))
+    q_pos = np.tile(np.arange(shape.ctx - w, shape.ctx), (shape.B, 1))
+    s = scoring.score_window(c, q.numpy(), q_pos, [0] * 2, [22] * 2, [0] * 2, [22] * 2, True)
+    G = shape.G
+    for (b, g), sv in s.items():
+        for j in range(22):
+            expect = G * sum(1.0 / (t + 1) for t in q_pos[b] if t >= j)
+            assert sv[j] == pytest.approx(expect, rel=1e-12)
+
+
+def test_scores_identical_keys_bidirectional_closed_form():
+    shape = tiny_shape(ctx=20)
+    pc = tiny_cache(shape)
+    _set_identical_keys(pc)
+    c = oc(pc)
+    w = 8
+    q = torch.randn(shape.B, w, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "qb"))
+    q_pos = np.tile(np.arange(12, 20), (shape.B, 1))
+    s = scoring.score_window(c, q.numpy(), q_pos, [12] * 2, [20] * 2, [12] * 2, [18] * 2, False)
+    for sv in s.values():
+        np.testing.assert_allclose(sv, shape.G * w / 8, rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_scores_match_library_attention_probabilities(causal):
+    # torch SDPA with V = identity returns the softmax matrix; its column sums
+    # over the group's heads and window queries are the scores
+    shape = tiny_shape(ctx=26, D=16)
+    pc = tiny_cache(shape)
+    c = oc(pc)
+    w = 5
+    q = torch.randn(shape.B, w, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "ql"))
+    q_pos = np.tile(np.arange(21, 26), (shape.B, 1))
+    lo, hi, olo, ohi = 3, 26, 4, 21
+    s = scoring.score_window(c, q.numpy(), q_pos, [lo] * 2, [hi] * 2, [olo] * 2, [ohi] * 2, causal)
+    for b in range(shape.B):
+        for g in range(shape.Hkv):
+            K = c.keys(b, g, range(lo, hi))
+            pos = c.slot_map[b, g, lo:hi]
+            total = np.zeros(hi - lo)
+            for h in range(g * shape.G, (g + 1) * shape.G):
+                Q = q[b, :, h, :].double().numpy()
+                mask = (pos[None, :] <= q_pos[b][:, None]) if causal else None
+                total += sdpa_probs(Q, K, mask).sum(axis=0)
+            np.testing.assert_allclose(s[(b, g)], total[olo - lo: ohi - lo], rtol=1e-12, atol=1e-15)
+
+
+def test_scores_rows_sum_to_one_and_single_key():
+    shape = tiny_shape(ctx=18)
+    pc = tiny_cache(shape)
+    c = oc(pc)
+    w = 4
+    q = torch.randn(shape.B, w, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "qr")) * 3
+    q_pos = np.tile(np.arange(14, 18), (shape.B, 1))
+    s = scoring.score_window(c, q.numpy(), q_pos, [0] * 2, [18] * 2, [0] * 2, [18] * 2, True)
+    for sv in s.values():
+        assert sv.sum() == pytest.approx(w * shape.G, rel=1e-12)
+    s1 = scoring.score_window(c, q.numpy(), q_pos, [5] * 2, [6] * 2, [5] * 2, [6] * 2, False)
+    for sv in s1.values():
+        assert sv[0] == pytest.approx(w * shape.G, rel=1e-12)
+
+
+def test_scores_causal_masks_future_keys():
+    shape = tiny_shape(ctx=20)
+    c = oc(tiny_cache(shape))
+    q = torch.randn(shape.B, 3, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "qf"))
+    q_pos = np.tile(np.array([10, 11, 12]), (shape.B, 1))
+    s = scoring.score_window(c, q.numpy(), q_pos, [0] * 2, [20] * 2, [0] * 2, [20] * 2, True)
+    for sv in s.values():
+        assert (sv[13:] == 0).all() and (sv[:13] > 0).all()
+
+
+# ---------------------------------------------------------------------------
+# O2 pooling
+# ---------------------------------------------------------------------------
+
+
+def test_pool_golden_hand_example():
+    g = golden("pool7_len8.json")
+    np.testing.assert_allclose(scoring.avg_pool(np.array(g["x"], float), g["kernel"]), g["expected"])
+
+
+def test_pool_matches_library_avg_pool1d():
+    x = torch.randn(97, generator=W.generator("cpu", "pin", "pool"), dtype=torch.float64)
+    lib = torch.nn.functional.avg_pool1d(x[None, None], 7, stride=1, padding=3,
+                                         count_include_pad=True)[0, 0].numpy()
+    np.testing.assert_allclose(scoring.avg_pool(x.numpy(), 7), lib, rtol=1e-14)
+    np.testing.assert_array_equal(scoring.avg_pool(x.numpy(), 1), x.numpy())
+
+
+def test_pool_constant_input():
+    out = scoring.avg_pool(np.full(20, 2.0), 7)
+    np.testing.assert_allclose(out[3:17], 2.0)
+    np.testing.assert_allclose(out[:3], [8 / 7, 10 / 7, 12 / 7])
+    np.testing.assert_allclose(out[17:], [12 / 7, 10 / 7, 8 / 7])
+
+
+# ---------------------------------------------------------------------------
+# O3 top-k with forced ranges
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_topk_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n, k = 40, 9
+    s = np.round(rng.random(n), 1)            # many ties
+    keep = selection.topk_keep(s, 10, k, 1, 45, 50)
+    cands = [j for j in range(10, 10 + n) if not 45 <= j < 50]   # forced slots are no candidates
+    ranked = sorted(cands, key=lambda j: (-s[j - 10], j))[:k]
+    assert list(keep) == sorted(ranked + list(range(45, 50)))
+
+
+def test_topk_with_pool_brute_force():
+    rng = np.random.default_rng(7)
+    s = rng.random(60)
+    pooled = torch.nn.functional.avg_pool1d(torch.tensor(s)[None, None], 7, 1, 3)[0, 0].numpy()
+    keep = selection.topk_keep(s, 0, 12, 7, 60, 64)
+    ranked = sorted(range(60), key=lambda j: (-pooled[j], j))[:12]
+    assert list(keep) == sorted(ranked) + [60, 61, 62, 63]
+
+
+def test_topk_all_equal_keeps_lowest_and_forced_overlap():
+    keep = selection.topk_keep(np.ones(30), 0, 5, 1, 30, 32)
+    assert list(keep) == [0, 1, 2, 3, 4, 30, 31]
+    # a forced range inside the candidate range is not a candidate
+    keep = selection.topk_keep(np.ones(30), 0, 5, 1, 2, 4)
+    assert list(keep) == [0, 1, 2, 3, 4, 5, 6]
+
+
+# ---------------------------------------------------------------------------
+# O4 Kara Token2Chunk
+# ---------------------------------------------------------------------------
+
+
+def test_kara_golden_hand_example():
+    g = golden("kara_token2chunk_hand.json")
+    keep = selection.kara_keep(np.array(g["scores"]), g["cand_lo"], g["n_cand"], g["budget"],
+                               g["coef"], g["force_lo"], g["force_hi"])
+    assert list(keep) == g["expected"]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_kara_invariants(seed):
+    rng = np.random.default_rng(100 + seed)
+    n, n_cand, budget = 224, 32, 64
+    s = rng.random(n) * rng.choice([1.0, 10.0])
+    keep = selection.kara_keep(s, 1000, n_cand, budget, 0.01, 1224, 1256)
+    body = keep[:-32]
+    assert list(keep[-32:]) == list(range(1224, 1256))
+    assert len(body) == budget and (np.diff(body) > 0).all()
+    top = sorted(range(n), key=lambda j: (-s[j], j))[:n_cand]
+    assert set(1000 + j for j in top) <= set(body)
+
+
+def test_kara_contiguous_candidates_reduce_to_topk():
+    # if the top candidates are contiguous every chunk interior is empty and
+    # the retained set is the top-`budget` by score (brute-force sorted)
+    rng = np.random.default_rng(3)
+    s = rng.random(224)
+    s[50:82] += 10.0                      # 32 contiguous best tokens
+    keep = selection.kara_keep(s, 0, 32, 64, 0.01, 224, 256)[:-32]
+    ranked = sorted(range(224), key=lambda j: (-s[j], j))[:64]
+    assert list(keep) == sorted(ranked)
+
+
+# ---------------------------------------------------------------------------
+# O5 H2O
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_h2o_victim_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    ctx = 30
+    acc = np.round(rng.random(40), 1)
+    pos = rng.permutation(100)[:40]
+    v = selection.h2o_victim(acc, pos, ctx, 29, 70)
+    elig = [j for j in range(ctx) if pos[j] < 70]
+    expect = sorted(elig, key=lambda j: (acc[j], -pos[j]))[0]
+    assert v == expect
+    assert selection.h2o_victim(acc, pos, ctx, 30, 70) == -1
+
+
+def _h2o_tiny(budget_heavy, recent, steps, prompt=24):
+    shape = W.h2o_decode(B=2, Hq=4, Hkv=2, D=16, ctx=prompt, heavy=budget_heavy, recent=recent,
+                         steps=steps, dtype=torch.float32, name="h2o_tiny")
+    inp = W.h2o_inputs(shape, "cpu")
+    return shape, inp
+
+
+def test_h2o_pipeline_invariants_and_acc_recomputation():
+    shape, inp = _h2o_tiny(8, 4, 10)
+    c = oc(inp["cache"])
+    orig = c.copy()
+    acc = np.zeros(c.slot_map.shape)
+    pipelines.h2o_prefill(c, inp["q_prompt"], inp["q_pos"].numpy(), shape, acc)
+    assert (c.ctx_len == shape.budget).all()
+    # independent running score per logical position, from library attention
+    run = {}
+    for b in range(c.B):
+        for g in range(c.Hkv):
+            K = orig.keys(b, g, range(shape.ctx))
+            tot = np.zeros(shape.ctx)
+            for h in range(g * shape.G, (g + 1) * shape.G):
+                Q = inp["q_prompt"][b, :, h].double().numpy()
+                mask = np.arange(shape.ctx)[None, :] <= np.arange(shape.ctx)[:, None]
+                tot += sdpa_probs(Q, K, mask).sum(axis=0)
+            run[(b, g)] = {p: tot[p] for p in range(shape.ctx)}
+    for t in range(shape.steps):
+        pipelines.h2o_step(c, acc, inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], shape)
+        for b in range(c.B):
+            L = int(c.logical_len[b])
+            assert c.ctx_len[b] == shape.budget
+            for g in range(c.Hkv):
+                pos = c.slot_map[b, g, : c.ctx_len[b]]
+                assert set(range(L - shape.recent, L)) <= set(pos.tolist())
+    # recompute acc for the survivors: prompt score + every step's group sum,
+    # replaying each step's attention with library SDPA over the entries that
+    # were resident at that step
+    c2 = oc(inp["cache"])
+    acc2 = np.zeros(c2.slot_map.shape)
+    pipelines.h2o_prefill(c2, inp["q_prompt"], inp["q_pos"].numpy(), shape, acc2)
+    for t in range(shape.steps):
+        kb, vb = cache._bits(inp["k_steps"][t]), cache._bits(inp["v_steps"][t])
+        cache.append(c2, kb, vb, aux=acc2)
+        q = inp["q_steps"][t].double().numpy()
+        for b in range(c2.B):
+            for g in range(c2.Hkv):
+                slots = np.arange(c2.ctx_len[b])
+                K, pos = c2.keys(b, g, slots), c2.slot_map[b, g, slots]
+                p = sum(sdpa_probs(q[b, h][None], K)[0] for h in range(g * shape.G, (g + 1) * shape.G))
+                for j, pp in zip(pos, p):
+                    run[(b, g)][int(j)] = run[(b, g)].get(int(j), 0.0) + pp
+        # same evictions as the oracle run (positions), to stay in lock-step
+        o, _ = attention.decode_attention(c2, q, "dense")
+        for (b, g), (slots, pp) in _.items():
+            acc2[b, g, slots] += pp
+        victim = np.full((c2.B, c2.Hkv), -1)
+        for b in range(c2.B):
+            for g in range(c2.Hkv):
+                victim[b, g] = selection.h2o_victim(acc2[b, g], c2.slot_map[b, g], int(c2.ctx_len[b]),
+                                                    shape.budget, int(c2.logical_len[b]) - shape.recent)
+        cache.move_last(c2, victim, aux=acc2)
+    for b in range(c.B):
+        for g in range(c.Hkv):
+            for s in range(c.ctx_len[b]):
+                assert acc[b, g, s] == pytest.approx(run[(b, g)][int(c.slot_map[b, g, s])], rel=1e-10)
+
+
+def test_h2o_no_eviction_when_budget_covers_context():
+    shape, inp = _h2o_tiny(100, 8, 4)
+    c = oc(inp["cache"])
+    acc = np.zeros(c.slot_map.shape)
+    pipelines.h2o_prefill(c, inp["q_prompt"], inp["q_pos"].numpy(), shape, acc)
+    for t in range(shape.steps):
+        r = pipelines.h2o_step(c, acc, inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], shape)
+        assert (r["victim"] == -1).all()
+        for b in range(c.B):
+            for g in range(c.Hkv):
+                slots = np.arange(c.ctx_len[b])
+                assert list(c.slot_map[b, g, slots]) == list(range(shape.ctx + t + 1))
+                q = inp["q_steps"][t][b, g * shape.G:(g + 1) * shape.G].double().numpy()
+                ref = sdpa_out(q, c.keys(b, g, slots), c.vals(b, g, slots))
+                np.testing.assert_allclose(r["o"][(b, g)], ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# O6 Quest
+# ---------------------------------------------------------------------------
+
+
+def _quest_tiny():
+    shape = W.quest_decode(B=2, Hq=4, Hkv=2, D=16, ctx=64, page_size=4, top_pages=5, steps=2,
+                           dtype=torch.bfloat16, name="quest_tiny")
+    return shape, W.quest_inputs(shape, "cpu")
+
+
+def test_quest_bound_is_upper_bound_and_meta_exact():
+    shape, inp = _quest_tiny()
+    c = oc(inp["cache"])
+    kmin, kmax = quest.build_meta(c)
+    q = values(cache._bits(inp["q_steps"][0]))
+    for b in range(c.B):
+        for blk in range(16):
+            page = c.block_table[b, blk]
+            for g in range(c.Hkv):
+                K = c.keys(b, g, range(blk * 4, blk * 4 + 4))
+                assert (kmin[page, g] <= K).all() and (K <= kmax[page, g]).all()
+                assert ((K == kmin[page, g]).any(axis=0)).all() and ((K == kmax[page, g]).any(axis=0)).all()
+                qg = q[b, g * 2:(g + 1) * 2]
+                U = quest.page_bound(qg, kmin[page, g], kmax[page, g])
+                for kv in K:
+                    assert U >= float((qg @ kv).sum()) - 1e-12
+                    for h in range(2):
+                        assert quest.page_bound(qg[h:h + 1], kmin[page, g], kmax[page, g]) >= qg[h] @ kv - 1e-12
+
+
+def test_quest_topk_brute_force_and_all_pages_dense():
+    shape, inp = _quest_tiny()
+    c = oc(inp["cache"])
+    kmin, kmax = quest.build_meta(c)
+    q = values(cache._bits(inp["q_steps"][1]))
+    for b in range(c.B):
+        for g in range(c.Hkv):
+            sel, U = quest.select_pages(c, kmin, kmax, q, 5, b, g)
+            ranked = sorted(range(15), key=lambda i: (-U[i], i))[:5]
+            assert list(sel) == sorted(ranked) + [15]
+    r = pipelines.quest_step(c, kmin, kmax, inp["q_steps"][1], 100)
+    for (b, g), o in r["o"].items():
+        slots = np.arange(64)
+        qg = q[b, g * 2:(g + 1) * 2]
+        np.testing.assert_allclose(o, sdpa_out(qg, c.keys(b, g, slots), c.vals(b, g, slots)),
+                                   rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# O7 / O8 compaction, move-last, append, prune
+# ---------------------------------------------------------------------------
+
+
+def _hand_cache(P, block_table, ctx, free_stack, num_pages, D=2):
+    B = len(block_table)
+    maxp = max(len(r) for r in block_table)
+    bt = np.full((B, maxp), -1, dtype=np.int64)
+    for b, r in enumerate(block_table):
+        bt[b, :len(r)] = r
+    k = np.zeros((num_pages, 1, P, D), dtype=np.uint32)
+    for p in range(num_pages):
+        for r in range(P):
+            k[p, 0, r, :] = 10 * p + r
+    sm = np.full((B, 1, maxp * P), -1, dtype=np.int64)
+    for b in range(B):
+        sm[b, 0, :ctx[b]] = np.arange(ctx[b])
+    fl = np.zeros(num_pages, dtype=np.int64)
+    fl[:len(free_stack)] = free_stack
+    refc = np.zeros(num_pages, dtype=np.int64)
+    for r in block_table:
+        for p in r:
+            if p >= 0:
+                refc[p] = 1
+    return cache.Cache(k=k, v=k.copy(), block_table=bt, slot_map=sm,
+                       ctx_len=np.array(ctx, dtype=np.int64), logical_len=np.array(ctx, dtype=np.int64),
+                       free_list=fl, free_top=len(free_stack), page_refcount=refc, page_size=P)
+
+
+def test_compact_golden_hand_example():
+    g = golden("compact_freelist_hand.json")
+    c = _hand_cache(g["page_size"], g["block_table"], g["ctx_len"], g["free_stack"], g["num_pages"])
+    keep = [[np.array(x)] for x in g["keep"]]
+    assert cache.compact(c, keep, g["first_slot"]) == cache.SE_OK
+    e = g["expected"]
+    assert c.block_table.tolist() == e["block_table"]
+    assert c.ctx_len.tolist() == e["ctx_len"]
+    assert c.free_list[: c.free_top].tolist() == e["free_stack"]
+    assert c.slot_map[:, 0, :].tolist() == e["slot_map"]
+    for page, rows in e["page_rows"].items():
+        assert c.k[int(page), 0, :3, 0].tolist() == rows
+    for page, rc in {**e["refcount_fresh"], **e["refcount_released"]}.items():
+        assert c.page_refcount[int(page)] == rc
+
+
+def _check_accounting(before, after):
+    num = before.k.shape[0]
+    in_tables = [int(p) for p in after.block_table.reshape(-1) if p >= 0]
+    free = [int(p) for p in after.free_list[: after.free_top]]
+    assert len(set(in_tables)) == len(in_tables)
+    assert not set(in_tables) & set(free)
+    assert sorted(in_tables + free) == list(range(num))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_compact_conserves_entries_and_pages(seed):
+    shape = tiny_shape(ctx=23, Hkv=3, Hq=6)
+    pc = tiny_cache(shape, num_pages=40, tag=f"cc{seed}")
+    c = oc(pc)
+    before = c.copy()
+    rng = np.random.default_rng(seed)
+    first = [int(rng.integers(0, 23)) for _ in range(shape.B)]
+    n_keep = [int(rng.integers(0, 23 - f + 1)) for f in first]
+    keep = [[np.sort(rng.choice(np.arange(first[b], 23), n_keep[b], replace=False))
+             for _ in range(3)] for b in range(shape.B)]
+    assert cache.compact(c, keep, first) == cache.SE_OK
+    _check_accounting(before, c)
+    assert (c.logical_len == before.logical_len).all()
+    for b in range(shape.B):
+        assert c.ctx_len[b] == first[b] + n_keep[b]
+        for h in range(3):
+            old_pos = before.slot_map[b, h, :23]
+            new_pos = c.slot_map[b, h, : c.ctx_len[b]]
+            expect = list(old_pos[: first[b]]) + [old_pos[s] for s in keep[b][h]]
+            assert list(new_pos) == expect
+            evicted = sorted(set(old_pos.tolist()) - set(new_pos.tolist()))
+            assert sorted(new_pos.tolist() + evicted) == sorted(old_pos.tolist())
+            for i, s in enumerate(list(range(first[b])) + list(keep[b][h])):
+                (p0,), (r0,) = before.where(b, [s])
+                (p1,), (r1,) = c.where(b, [i])
+                assert (before.k[p0, h, r0] == c.k[p1, h, r1]).all()
+                assert (before.v[p0, h, r0] == c.v[p1, h, r1]).all()
+
+
+def test_compact_out_of_pages_changes_nothing():
+    shape = tiny_shape(ctx=20)
+    c = oc(tiny_cache(shape, num_pages=10))
+    c.free_top = 1
+    before = c.copy()
+    keep = [[np.arange(0, 10)] * 2 for _ in range(2)]
+    assert cache.compact(c, keep, [0, 0]) == cache.SE_ERR_OUT_OF_PAGES
+    assert (c.block_table == before.block_table).all() and c.free_top == 1
+
+
+def test_move_last_and_append():
+    shape = tiny_shape(ctx=17, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=20, max_ctx=24))
+    before = c.copy()
+    victim = np.array([[3, 16], [0, 5]])
+    assert cache.move_last(c, victim) == cache.SE_OK
+    assert (c.ctx_len == 16).all()
+    assert c.slot_map[0, 0, 3] == 16 and c.slot_map[0, 1, 16] == -1
+    (p,), (r,) = before.where(0, [16])
+    (q,), (s,) = c.where(0, [3])
+    assert (c.k[q, 0, s] == before.k[p, 0, r]).all()
+    assert c.free_top == before.free_top + 2          # block 4 emptied in both sequences
+    _check_accounting(before, c)
+    kb = np.full((2, 2, shape.D), 7, dtype=np.uint32)
+    top = c.free_top
+    assert cache.append(c, kb, kb) == cache.SE_OK
+    assert c.free_top == top - 2 and (c.ctx_len == 17).all() and (c.logical_len == 18).all()
+    assert c.slot_map[1, 1, 16] == 17
+    _check_accounting(before, c)
+
+
+def _prune_hand(busy):
+    g = golden("prune_span_hand.json")
+    c = _hand_cache(g["page_size"], [g["block_table"]], [g["ctx"]], g["free_stack"], 9)
+    if busy:
+        c.page_refcount[3] = 2
+    st, nb = cache.prune(c, [g["L"]], [g["R"]], np.array([g["mask"]]))
+    assert st == cache.SE_OK
+    return g, c, nb
+
+
+def test_prune_golden_hand_example_idle_and_busy():
+    g, c, nb = _prune_hand(False)
+    e = g["expected_idle"]
+    assert c.slot_map[0, 0, : c.ctx_len[0]].tolist() == e["positions"]
+    assert c.block_table[0].tolist() == e["block_table"]
+    assert c.free_list[: c.free_top].tolist() == e["free_stack"]
+    g, c, nb = _prune_hand(True)
+    e = g["expected_busy"]
+    assert c.slot_map[0, 0, : c.ctx_len[0]].tolist() == e["positions"]
+    assert c.free_list[: c.free_top].tolist() == e["free_stack"]
+    assert c.page_refcount[3] == e["refcount_page3"] and nb == [e["busy_pages"]]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prune_set_identity(seed):
+    # Res' = (Res \ T) U I as Python sets, logical prefix unchanged
+    shape = tiny_shape(ctx=40, page_size=4, Hkv=2)
+    c = oc(tiny_cache(shape, num_pages=60, tag=f"pr{seed}"))
+    rng = np.random.default_rng(seed)
+    # first make head sets differ outside the span by an earlier compaction
+    keep = [[np.sort(rng.choice(np.arange(30, 40), 6, replace=False)) for _ in range(2)]
+            for _ in range(2)]
+    assert cache.compact(c, keep, [30, 30]) == cache.SE_OK
+    before = c.copy()
+    L, R = [5, 9], [21, 30]
+    mask = np.zeros((2, 25), dtype=np.uint8)
+    for b in range(2):
+        mask[b, rng.choice(R[b] - L[b], 4, replace=False)] = 1
+    st, _ = cache.prune(c, L, R, mask)
+    assert st == cache.SE_OK
+    _check_accounting(before, c)
+    assert (c.logical_len == before.logical_len).all()
+    for b in range(2):
+        T = set(range(L[b], R[b]))
+        I = {L[b] + i for i in range(R[b] - L[b]) if mask[b, i]}
+        for h in range(2):
+            res = set(before.slot_map[b, h, : before.ctx_len[b]].tolist())
+            new = c.slot_map[b, h, : c.ctx_len[b]].tolist()
+            assert set(new) == (res - T) | (I & res)
+            old_order = [p for p in before.slot_map[b, h, : before.ctx_len[b]].tolist() if p in set(new)]
+            assert new == old_order
+
+
+def test_prune_uneven_heads_is_rejected():
+    shape = tiny_shape(ctx=16, page_size=4, Hkv=2)
+    c = oc(tiny_cache(shape, num_pages=30))
+    keep = [[np.array([0, 1, 2, 3, 4, 5]), np.array([0, 1, 2, 3, 10, 11])] for _ in range(2)]
+    assert cache.compact(c, keep, [0, 0]) == cache.SE_OK
+    mask = np.zeros((2, 4), dtype=np.uint8)
+    st, _ = cache.prune(c, [2, 2], [6, 6], mask)
+    assert st == cache.SE_ERR_UNEVEN
+
+
+# ---------------------------------------------------------------------------
+# O9 decode attention and the end-to-end full-budget identity
+# ---------------------------------------------------------------------------
+
+
+def test_decode_attention_matches_library_on_all_views():
+    shape = tiny_shape(ctx=21, page_size=4)
+    c = oc(tiny_cache(shape))
+    q = torch.randn(2, shape.Hq, shape.D, generator=W.generator("cpu", "pin", "dq")).double().numpy()
+    sel_p = {b: {g: np.array([0, 2, 5]) for g in range(2)} for b in range(2)}
+    sel_t = {b: {g: np.array([1, 4, 9, 20]) for g in range(2)} for b in range(2)}
+    for view, sel, slots in [("dense", None, np.arange(21)),
+                             ("pages", sel_p, np.r_[0:4, 8:12, 20]),
+                             ("tokens", sel_t, np.array([1, 4, 9, 20]))]:
+        o, ps = attention.decode_attention(c, q, view, sel)
+        for (b, g), ob in o.items():
+            ref = sdpa_out(q[b, 2 * g:2 * g + 2], c.keys(b, g, slots), c.vals(b, g, slots))
+            np.testing.assert_allclose(ob, ref, rtol=1e-12, atol=1e-14)
+            assert ps[(b, g)][1].sum() == pytest.approx(2.0, rel=1e-12)
+
+
+def test_decode_attention_special_cases():
+    K = np.random.default_rng(0).standard_normal((1, 8))
+    V = np.random.default_rng(1).standard_normal((1, 8))
+    o, _ = attention.attend(np.ones((3, 8)), K, V)
+    np.testing.assert_allclose(o, np.repeat(V, 3, 0))
+    K = np.random.default_rng(2).standard_normal((9, 8))
+    o, _ = attention.attend(np.ones((2, 8)), K, np.full((9, 8), 0.5))
+    np.testing.assert_allclose(o, 0.5)
+
+
+def test_snapkv_full_budget_reproduces_dense_attention():
+    shape = W.snapkv_tiny(ctx=96, window=16, budget=96, heavy_count=3)
+    inp = W.snapkv_inputs(shape, "cpu")
+    c = oc(inp["cache"])
+    before = c.copy()
+    r = pipelines.snapkv(c, inp["q_win"], inp["q_pos"].numpy(), inp["q_dec"], shape)
+    assert all(len(k) == 96 for kb in r["keep"] for k in kb)
+    q = inp["q_dec"].double().numpy()
+    for (b, g), o in r["o"].items():
+        slots = np.arange(96)
+        ref = sdpa_out(q[b, 4 * g:4 * g + 4], before.keys(b, g, slots), before.vals(b, g, slots))
+        np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_snapkv_tiny_workload_shape_facts():
+    # the tiny SnapKV workload: budget 128 = top 96 + 32-token window, 8 fresh
+    # pages taken, 32 old pages returned
+    shape = W.snapkv_tiny()
+    inp = W.snapkv_inputs(shape, "cpu")
+    c = oc(inp["cache"])
+    top0 = c.free_top
+    r = pipelines.snapkv(c, inp["q_win"], inp["q_pos"].numpy(), inp["q_dec"], shape)
+    keep = r["keep"][0][0]
+    assert len(keep) == 128 and list(keep[-32:]) == list(range(480, 512))
+    assert c.ctx_len[0] == 128 and c.free_top == top0 - 8 + 32
+    assert (c.block_table[0, 8:] == -1).all()
