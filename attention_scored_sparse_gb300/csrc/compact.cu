@@ -1,0 +1,755 @@
+// Physical compaction, move-last eviction, append and prefix-span pruning.
+//
+// SparseEngine, "How it works": physical eviction rewrites the retained slot
+// mapping and the context length and returns discarded slots to the
+// allocator; the CacheManager allocates, writes, updates and frees.
+// SparseEngine, "How it differs": prefix pruning R' = (R \ T) U I on idle
+// blocks, logical prefix untouched.
+//
+// Every state change is split into a plan kernel (validation, page
+// accounting, prefix sums over sequences, free-list pops into the
+// workspace) and apply kernels that only run when the plan found no error,
+// so a call that reports a device error leaves the cache untouched.  Fresh
+// pages are popped from the top of the free-list stack in ascending
+// (sequence, block) order and old pages pushed afterwards in the same order;
+// the same order makes block tables and the free list deterministic.
+#include "se_common.cuh"
+
+namespace se {
+
+struct CompactCtrl {
+  int32_t abort;
+  int32_t top0;
+  int32_t total_new;
+  int32_t total_push;
+};
+
+struct CompactWs {
+  CompactCtrl* ctrl;
+  int32_t* pb;        // [B] first rewritten block
+  int32_t* n_new;     // [B] fresh pages
+  int32_t* old_blocks;// [B] blocks before the call
+  int32_t* new_ctx;   // [B]
+  int32_t* old_ctx;   // [B]
+  int32_t* off_new;   // [B] prefix of n_new
+  int32_t* off_push;  // [B] prefix of pushed pages
+  int32_t* newpage;   // [B * max_pages_per_seq]
+  int32_t* slot_tmp;  // [B][Hkv][row]  new slot_map values from pb*P on
+  float* aux_tmp;     // [B][Hkv][row]
+  int64_t row;        // max_keep + page_size
+};
+
+static CompactWs carve_compact(const se_paged_kv* kv, int32_t max_keep, void* ws, bool aux,
+                               size_t* bytes) {
+  WsCarver c(ws);
+  CompactWs w;
+  const int B = kv->B;
+  w.ctrl = c.take<CompactCtrl>(1);
+  w.pb = c.take<int32_t>(B);
+  w.n_new = c.take<int32_t>(B);
+  w.old_blocks = c.take<int32_t>(B);
+  w.new_ctx = c.take<int32_t>(B);
+  w.old_ctx = c.take<int32_t>(B);
+  w.off_new = c.take<int32_t>(B);
+  w.off_push = c.take<int32_t>(B);
+  w.newpage = c.take<int32_t>((size_t)B * kv->max_pages_per_seq);
+  w.row = (int64_t)max_keep + kv->page_size;
+  w.slot_tmp = c.take<int32_t>((size_t)B * kv->Hkv * w.row);
+  w.aux_tmp = aux ? c.take<float>((size_t)B * kv->Hkv * w.row) : nullptr;
+  if (!aux) c.take<float>((size_t)B * kv->Hkv * w.row);  // size does not depend on aux
+  *bytes = c.bytes();
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// FRESH_PAGES compaction
+// ---------------------------------------------------------------------------
+
+// One CTA: validation, page counts, prefix sums, pops into the workspace.
+__global__ void __launch_bounds__(1024) compact_plan_kernel(
+    se_paged_kv kv, const int32_t* __restrict__ n_keep, const int32_t* __restrict__ first_slot,
+    int32_t max_keep, const int32_t* __restrict__ abort_in, CompactWs w) {
+  __shared__ int tmp[33];
+  __shared__ int s_bad;
+  __shared__ int s_run_new, s_run_push;
+  const int tid = threadIdx.x;
+  const int P = kv.page_size;
+  if (tid == 0) {
+    s_bad = (abort_in != nullptr && *abort_in != 0) ? 1 : 0;
+    s_run_new = 0;
+    s_run_push = 0;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) w.ctrl->abort = 1;
+    return;
+  }
+  // per-sequence plan + prefix of fresh pages
+  for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
+    const int b = b0 + tid;
+    int nn = 0;
+    if (b < kv.B) {
+      const int ctx = kv.ctx_len[b];
+      const int fs = first_slot[b];
+      const int nk = n_keep[b];
+      const bool ok = fs >= 0 && fs <= ctx && nk >= 0 && nk <= ctx - fs && nk <= max_keep &&
+                      ctx <= kv.max_pages_per_seq * P;
+      if (!ok) {
+        set_status(kv.status, SE_ERR_BOUNDS);
+        atomicExch(&s_bad, 1);
+      }
+      const int pb = fs / P;
+      const int nctx = fs + nk;
+      nn = ok ? max(cdiv(nctx, P) - pb, 0) : 0;
+      w.pb[b] = pb;
+      w.n_new[b] = nn;
+      w.old_blocks[b] = cdiv(ctx, P);
+      w.new_ctx[b] = nctx;
+      w.old_ctx[b] = ctx;
+    }
+    int total;
+    int ex = block_exclusive_scan(nn, tmp, &total);
+    if (b < kv.B) w.off_new[b] = s_run_new + ex;
+    __syncthreads();
+    if (tid == 0) s_run_new += total;
+    __syncthreads();
+  }
+  // pushed pages per sequence: one warp per sequence
+  __shared__ int s_push[1024];
+  const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  for (int b0 = 0; b0 < kv.B; b0 += 1024) {
+    for (int bb = warp; bb < 1024 && b0 + bb < kv.B; bb += nw) {
+      const int b = b0 + bb;
+      const int pb = w.pb[b], ob = w.old_blocks[b];
+      int cnt = 0;
+      if (kv.page_refcount == nullptr) {
+        cnt = lane == 0 ? max(ob - pb, 0) : 0;
+      } else {
+        for (int blk = pb + lane; blk < ob; blk += 32) {
+          const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
+          cnt += (page >= 0 && kv.page_refcount[page] <= 1) ? 1 : 0;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (lane == 0) s_push[bb] = cnt;
+    }
+    __syncthreads();
+    const int b = b0 + tid;
+    const int v = (b < kv.B) ? s_push[tid] : 0;
+    int total;
+    int ex = block_exclusive_scan(v, tmp, &total);
+    if (b < kv.B) w.off_push[b] = s_run_push + ex;
+    __syncthreads();
+    if (tid == 0) s_run_push += total;
+    __syncthreads();
+  }
+  const int top0 = *kv.free_top;
+  const int total_new = s_run_new;
+  if (tid == 0) {
+    w.ctrl->top0 = top0;
+    w.ctrl->total_new = total_new;
+    w.ctrl->total_push = s_run_push;
+    int bad = s_bad;
+    if (!bad && total_new > top0) {
+      set_status(kv.status, SE_ERR_OUT_OF_PAGES);
+      bad = 1;
+    }
+    w.ctrl->abort = bad;
+  }
+  if (s_bad || total_new > top0) return;
+  for (int i = tid; i < total_new; i += blockDim.x) w.newpage[i] = kv.free_list[top0 - 1 - i];
+}
+
+// Copies the surviving entries into the fresh pages (K, V) and stages their
+// slot_map / aux values.  grid: (entry chunks, Hkv, B).
+template <int CHUNKS>  // 16-byte chunks per entry row
+__global__ void __launch_bounds__(256) compact_gather_kernel(
+    se_paged_kv kv, const int32_t* __restrict__ keep_idx, int32_t keep_stride,
+    const int32_t* __restrict__ first_slot, const float* __restrict__ aux, int64_t aux_stride,
+    CompactWs w, int entries_per_cta) {
+  if (w.ctrl->abort) return;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int P = kv.page_size;
+  const int pb = w.pb[b];
+  const int fs = first_slot[b];
+  const int head = fs - pb * P;
+  const int total = head + (w.new_ctx[b] - fs);
+  const int e0 = blockIdx.x * entries_per_cta;
+  if (e0 >= total) return;
+  const int e1 = min(e0 + entries_per_cta, total);
+  const int old_ctx = w.old_ctx[b];
+  const int32_t* keep = keep_idx + ((int64_t)b * kv.Hkv + h) * keep_stride;
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  const int esz = (int)elem_size(kv.dtype);
+  const int64_t row_bytes = (int64_t)kv.D * esz;          // = CHUNKS * 16
+  const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
+  const char* kp = static_cast<const char*>(kv.k_pool);
+  const char* vp = static_cast<const char*>(kv.v_pool);
+  char* kpw = static_cast<char*>(kv.k_pool);
+  char* vpw = static_cast<char*>(kv.v_pool);
+  constexpr int EPP = 256 / CHUNKS;  // entries per pass
+  const int sub = threadIdx.x / CHUNKS, ch = threadIdx.x % CHUNKS;
+  const int64_t tmp_base = ((int64_t)b * kv.Hkv + h) * w.row;
+  for (int i = e0 + sub; i < e1; i += EPP) {
+    int src;
+    if (i < head) {
+      src = pb * P + i;
+    } else {
+      src = keep[i - head];
+      const bool ok = src >= fs && src < old_ctx && (i == head || src > keep[i - head - 1]);
+      if (!ok) {
+        if (ch == 0) {
+          set_status(kv.status, SE_ERR_BOUNDS);
+          atomicExch(&w.ctrl->abort, 1);
+        }
+        continue;
+      }
+    }
+    const int sp = bt[src / P];
+    const int dp = w.newpage[w.off_new[b] + i / P];
+    if (sp < 0 || sp >= kv.num_pages || dp < 0 || dp >= kv.num_pages) {
+      if (ch == 0) {
+        set_status(kv.status, SE_ERR_BOUNDS);
+        atomicExch(&w.ctrl->abort, 1);
+      }
+      continue;
+    }
+    const int64_t so = (int64_t)sp * page_bytes + ((int64_t)h * P + src % P) * row_bytes + ch * 16;
+    const int64_t dof = (int64_t)dp * page_bytes + ((int64_t)h * P + i % P) * row_bytes + ch * 16;
+    const uint4 kv4 = ldg_nc_v4(kp + so);
+    const uint4 vv4 = ldg_nc_v4(vp + so);
+    stg_v4(kpw + dof, kv4);
+    stg_v4(vpw + dof, vv4);
+    if (ch == 0) {
+      w.slot_tmp[tmp_base + i] = kv.slot_map[((int64_t)b * kv.Hkv + h) *
+                                                 ((int64_t)kv.max_pages_per_seq * P) + src];
+      if (aux != nullptr && w.aux_tmp != nullptr)
+        w.aux_tmp[tmp_base + i] = aux[((int64_t)b * kv.Hkv + h) * aux_stride + src];
+    }
+  }
+}
+
+// Commits block tables, slot maps, lengths, refcounts and pushes.  grid: B.
+__global__ void __launch_bounds__(256) compact_finalize_kernel(se_paged_kv kv, float* aux,
+                                                               int64_t aux_stride, CompactWs w) {
+  __shared__ int tmp[33];
+  if (w.ctrl->abort) return;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int P = kv.page_size;
+  const int pb = w.pb[b], nn = w.n_new[b], ob = w.old_blocks[b];
+  const int nctx = w.new_ctx[b], octx = w.old_ctx[b];
+  const int top0 = w.ctrl->top0, total_new = w.ctrl->total_new;
+  const int push_base = top0 - total_new + w.off_push[b];
+  int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  const int end = max(ob, pb + nn);
+  int running = 0;
+  for (int c0 = pb; c0 < end; c0 += blockDim.x) {
+    const int blk = c0 + tid;
+    int old = -1;
+    bool busy = false, push = false;
+    if (blk < ob) {
+      old = bt[blk];
+      busy = old >= 0 && kv.page_refcount != nullptr && kv.page_refcount[old] > 1;
+      push = old >= 0 && !busy;
+    }
+    int total;
+    const int pos = block_exclusive_scan(push ? 1 : 0, tmp, &total);
+    if (blk < end) {
+      if (blk < pb + nn) {
+        const int np = w.newpage[w.off_new[b] + blk - pb];
+        bt[blk] = np;
+        if (kv.page_refcount) kv.page_refcount[np] = 1;
+      } else {
+        bt[blk] = -1;
+      }
+    }
+    if (push && push_base + running + pos < kv.num_pages) {
+      kv.free_list[push_base + running + pos] = old;
+      if (kv.page_refcount) kv.page_refcount[old] = 0;
+    }
+    if (busy) kv.page_refcount[old] -= 1;
+    running += total;
+  }
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  const int n_rows = nctx - pb * P;
+  for (int h = 0; h < kv.Hkv; ++h) {
+    int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+    const int64_t tb = ((int64_t)b * kv.Hkv + h) * w.row;
+    for (int i = tid; i < n_rows; i += blockDim.x) sm[pb * P + i] = w.slot_tmp[tb + i];
+    for (int s = nctx + tid; s < octx; s += blockDim.x) sm[s] = -1;
+    if (aux != nullptr) {
+      float* ar = aux + ((int64_t)b * kv.Hkv + h) * aux_stride;
+      for (int i = tid; i < n_rows; i += blockDim.x) ar[pb * P + i] = w.aux_tmp[tb + i];
+      for (int s = nctx + tid; s < octx; s += blockDim.x) ar[s] = 0.f;
+    }
+  }
+  if (tid == 0) {
+    kv.ctx_len[b] = nctx;
+    if (b == 0) *kv.free_top = top0 - total_new + w.ctrl->total_push;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MOVE_LAST eviction (H2O)
+// ---------------------------------------------------------------------------
+
+struct MoveWs {
+  CompactCtrl* ctrl;
+  int32_t* act;       // [B] 1 = evict one
+  int32_t* off_push;  // [B]
+  int32_t* ctx;       // [B] snapshot
+};
+
+static MoveWs carve_move(const se_paged_kv* kv, void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  MoveWs w;
+  w.ctrl = c.take<CompactCtrl>(1);
+  w.act = c.take<int32_t>(kv->B);
+  w.off_push = c.take<int32_t>(kv->B);
+  w.ctx = c.take<int32_t>(kv->B);
+  *bytes = c.bytes();
+  return w;
+}
+
+__global__ void __launch_bounds__(1024) move_last_plan_kernel(se_paged_kv kv,
+                                                              const int32_t* __restrict__ victim,
+                                                              MoveWs w) {
+  __shared__ int tmp[33];
+  __shared__ int s_bad, s_run;
+  const int tid = threadIdx.x;
+  if (tid == 0) { s_bad = 0; s_run = 0; }
+  __syncthreads();
+  for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
+    const int b = b0 + tid;
+    int freed = 0;
+    if (b < kv.B) {
+      const int ctx = kv.ctx_len[b];
+      int n_neg = 0, n_ok = 0;
+      for (int h = 0; h < kv.Hkv; ++h) {
+        const int v = victim[b * kv.Hkv + h];
+        n_neg += v < 0;
+        n_ok += (v >= 0 && v < ctx);
+      }
+      int act = 0;
+      if (n_neg == kv.Hkv) {
+        act = 0;
+      } else if (n_ok == kv.Hkv) {
+        act = 1;
+      } else {
+        set_status(kv.status, n_neg > 0 ? SE_ERR_UNEVEN : SE_ERR_BOUNDS);
+        atomicExch(&s_bad, 1);
+      }
+      w.act[b] = act;
+      w.ctx[b] = ctx;
+      freed = act && ((ctx - 1) % kv.page_size == 0);
+    }
+    int total;
+    const int ex = block_exclusive_scan(freed, tmp, &total);
+    if (b < kv.B) w.off_push[b] = s_run + ex;
+    __syncthreads();
+    if (tid == 0) s_run += total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    w.ctrl->abort = s_bad;
+    w.ctrl->top0 = *kv.free_top;
+    w.ctrl->total_push = s_run;
+  }
+}
+
+// grid: B; one warp per KV head.
+__global__ void __launch_bounds__(256) move_last_apply_kernel(se_paged_kv kv,
+                                                              const int32_t* __restrict__ victim,
+                                                              float* aux, int64_t aux_stride,
+                                                              MoveWs w) {
+  if (w.ctrl->abort) return;
+  const int b = blockIdx.x;
+  if (!w.act[b]) return;
+  const int P = kv.page_size;
+  const int last = w.ctx[b] - 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int esz = (int)elem_size(kv.dtype);
+  const int64_t row_bytes = (int64_t)kv.D * esz;
+  const int chunks = (int)(row_bytes / 16);
+  const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  for (int h = warp; h < kv.Hkv; h += blockDim.x >> 5) {
+    const int v = victim[b * kv.Hkv + h];
+    if (v != last) {
+      const int64_t so = (int64_t)bt[last / P] * page_bytes + ((int64_t)h * P + last % P) * row_bytes;
+      const int64_t dof = (int64_t)bt[v / P] * page_bytes + ((int64_t)h * P + v % P) * row_bytes;
+      for (int c = lane; c < chunks; c += 32) {
+        const uint4 k4 = ldg_v4(static_cast<const char*>(kv.k_pool) + so + c * 16);
+        const uint4 v4 = ldg_v4(static_cast<const char*>(kv.v_pool) + so + c * 16);
+        stg_v4(static_cast<char*>(kv.k_pool) + dof + c * 16, k4);
+        stg_v4(static_cast<char*>(kv.v_pool) + dof + c * 16, v4);
+      }
+    }
+    if (lane == 0) {
+      int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+      const int pos = sm[last];
+      sm[v] = pos;
+      sm[last] = -1;
+      if (aux != nullptr) {
+        float* ar = aux + ((int64_t)b * kv.Hkv + h) * aux_stride;
+        const float a = ar[last];
+        ar[v] = a;
+        ar[last] = 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    kv.ctx_len[b] = last;
+    if (last % P == 0) {
+      const int page = bt[last / P];
+      kv.block_table[(int64_t)b * kv.max_pages_per_seq + last / P] = -1;
+      if (kv.page_refcount) kv.page_refcount[page] = 0;
+      kv.free_list[w.ctrl->top0 + w.off_push[b]] = page;
+    }
+    if (b == 0) *kv.free_top = w.ctrl->top0 + w.ctrl->total_push;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Append (CacheManager write)
+// ---------------------------------------------------------------------------
+
+struct AppendWs {
+  CompactCtrl* ctrl;
+  int32_t* page;     // [B] page receiving the new slot
+  int32_t* fresh;    // [B] 1 = popped
+  int32_t* ctx;      // [B] snapshot
+  int32_t* logical;  // [B] snapshot
+};
+
+static AppendWs carve_append(const se_paged_kv* kv, void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  AppendWs w;
+  w.ctrl = c.take<CompactCtrl>(1);
+  w.page = c.take<int32_t>(kv->B);
+  w.fresh = c.take<int32_t>(kv->B);
+  w.ctx = c.take<int32_t>(kv->B);
+  w.logical = c.take<int32_t>(kv->B);
+  *bytes = c.bytes();
+  return w;
+}
+
+__global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, AppendWs w) {
+  __shared__ int tmp[33];
+  __shared__ int s_bad, s_run;
+  const int tid = threadIdx.x;
+  const int P = kv.page_size;
+  if (tid == 0) { s_bad = 0; s_run = 0; }
+  __syncthreads();
+  const int top0 = *kv.free_top;
+  // pass 1: counts and bounds
+  for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
+    const int b = b0 + tid;
+    int need = 0;
+    if (b < kv.B) {
+      const int ctx = kv.ctx_len[b];
+      if (ctx < 0 || ctx >= kv.max_pages_per_seq * P) {
+        set_status(kv.status, SE_ERR_BOUNDS);
+        atomicExch(&s_bad, 1);
+      }
+      need = (ctx % P == 0) ? 1 : 0;
+      w.ctx[b] = ctx;
+      w.logical[b] = kv.logical_len[b];
+      w.fresh[b] = need;
+    }
+    int total;
+    const int ex = block_exclusive_scan(need, tmp, &total);
+    if (b < kv.B) w.page[b] = need ? -(s_run + ex) - 1 : 0;  // encoded pop rank
+    __syncthreads();
+    if (tid == 0) s_run += total;
+    __syncthreads();
+  }
+  const bool bad = s_bad || s_run > top0;
+  if (tid == 0) {
+    if (!s_bad && s_run > top0) set_status(kv.status, SE_ERR_OUT_OF_PAGES);
+    w.ctrl->abort = bad ? 1 : 0;
+    w.ctrl->top0 = top0;
+    w.ctrl->total_new = s_run;
+  }
+  if (bad) return;
+  for (int b = tid; b < kv.B; b += blockDim.x) {
+    const int ctx = w.ctx[b];
+    if (w.fresh[b]) {
+      const int rank = -w.page[b] - 1;
+      w.page[b] = kv.free_list[top0 - 1 - rank];
+    } else {
+      w.page[b] = kv.block_table[(int64_t)b * kv.max_pages_per_seq + ctx / P];
+    }
+  }
+}
+
+// grid: B
+__global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
+                                                           const void* __restrict__ k_new,
+                                                           const void* __restrict__ v_new,
+                                                           float* aux, int64_t aux_stride,
+                                                           AppendWs w) {
+  if (w.ctrl->abort) return;
+  const int b = blockIdx.x;
+  const int P = kv.page_size;
+  const int s = w.ctx[b];
+  const int page = w.page[b];
+  const int esz = (int)elem_size(kv.dtype);
+  const int64_t row_bytes = (int64_t)kv.D * esz;
+  const int chunks = (int)(row_bytes / 16);
+  const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
+  for (int t = threadIdx.x; t < kv.Hkv * chunks; t += blockDim.x) {
+    const int h = t / chunks, c = t % chunks;
+    const int64_t so = ((int64_t)b * kv.Hkv + h) * row_bytes + c * 16;
+    const int64_t dof = (int64_t)page * page_bytes + ((int64_t)h * P + s % P) * row_bytes + c * 16;
+    stg_v4(static_cast<char*>(kv.k_pool) + dof, ldg_v4(static_cast<const char*>(k_new) + so));
+    stg_v4(static_cast<char*>(kv.v_pool) + dof, ldg_v4(static_cast<const char*>(v_new) + so));
+  }
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  for (int h = threadIdx.x; h < kv.Hkv; h += blockDim.x) {
+    kv.slot_map[((int64_t)b * kv.Hkv + h) * smax + s] = w.logical[b];
+    if (aux != nullptr) aux[((int64_t)b * kv.Hkv + h) * aux_stride + s] = 0.f;
+  }
+  if (threadIdx.x == 0) {
+    if (w.fresh[b]) {
+      kv.block_table[(int64_t)b * kv.max_pages_per_seq + s / P] = page;
+      if (kv.page_refcount) kv.page_refcount[page] = 1;
+    }
+    kv.ctx_len[b] = s + 1;
+    kv.logical_len[b] = w.logical[b] + 1;
+    if (b == 0) *kv.free_top = w.ctrl->top0 - w.ctrl->total_new;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Prefix-span pruning plan
+// ---------------------------------------------------------------------------
+
+struct PruneWs {
+  int32_t* abort;    // [1]
+  int32_t* keep;     // [B][Hkv][smax]
+  int32_t* n_keep;   // [B]
+  int32_t* first;    // [B]
+  void* compact_ws;
+  size_t compact_bytes;
+};
+
+static PruneWs carve_prune(const se_paged_kv* kv, void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  PruneWs w;
+  const int64_t smax = (int64_t)kv->max_pages_per_seq * kv->page_size;
+  w.abort = c.take<int32_t>(1);
+  w.keep = c.take<int32_t>((size_t)kv->B * kv->Hkv * smax);
+  w.n_keep = c.take<int32_t>(kv->B);
+  w.first = c.take<int32_t>(kv->B);
+  size_t cb = 0;
+  carve_compact(kv, (int32_t)smax, nullptr, true, &cb);
+  char* cws = c.take<char>(cb);
+  w.compact_ws = cws;
+  w.compact_bytes = cb;
+  *bytes = c.bytes();
+  return w;
+}
+
+// grid: B, 1024 threads.  Builds per-head keep lists for R' = (R \ T) U I.
+__global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
+                                                          const int32_t* __restrict__ Lp,
+                                                          const int32_t* __restrict__ Rp,
+                                                          const uint8_t* __restrict__ mask,
+                                                          int32_t mask_stride, int32_t* n_busy,
+                                                          PruneWs w) {
+  __shared__ int tmp[33];
+  __shared__ int s_first, s_busy, s_count0, s_bad;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int P = kv.page_size;
+  const int ctx = kv.ctx_len[b];
+  const int L = Lp[b], R = Rp[b];
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  if (tid == 0) { s_first = ctx; s_busy = 0; s_count0 = -1; s_bad = 0; }
+  __syncthreads();
+  for (int h = 0; h < kv.Hkv; ++h) {
+    const int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+    for (int s = tid; s < ctx; s += blockDim.x)
+      if (sm[s] >= L) atomicMin(&s_first, s);
+  }
+  __syncthreads();
+  const int fs = s_first;
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  if (kv.page_refcount != nullptr) {
+    int cnt = 0;
+    for (int blk = fs / P + tid; blk < cdiv(ctx, P); blk += blockDim.x)
+      cnt += kv.page_refcount[bt[blk]] > 1;
+    if (cnt) atomicAdd(&s_busy, cnt);
+  }
+  for (int h = 0; h < kv.Hkv; ++h) {
+    const int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+    int32_t* keep = w.keep + ((int64_t)b * kv.Hkv + h) * smax;
+    int running = 0;
+    for (int c0 = fs; c0 < ctx; c0 += blockDim.x) {
+      const int s = c0 + tid;
+      int k = 0;
+      if (s < ctx) {
+        const int pos = sm[s];
+        const bool in_T = pos >= L && pos < R;
+        bool leaves = false;
+        if (in_T) {
+          if (pos - L >= mask_stride) {
+            set_status(kv.status, SE_ERR_BOUNDS);
+            atomicExch(w.abort, 1);
+          }
+          const bool in_I = pos - L < mask_stride && mask[(int64_t)b * mask_stride + (pos - L)] != 0;
+          const bool busy = kv.page_refcount != nullptr && kv.page_refcount[bt[s / P]] > 1;
+          leaves = !in_I && !busy;
+        }
+        k = leaves ? 0 : 1;
+      }
+      int total;
+      const int ex = block_exclusive_scan(k, tmp, &total);
+      if (k) keep[running + ex] = s;
+      running += total;
+    }
+    if (tid == 0) {
+      if (h == 0) s_count0 = running;
+      else if (running != s_count0) s_bad = 1;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    w.first[b] = fs;
+    w.n_keep[b] = s_count0 < 0 ? 0 : s_count0;
+    if (n_busy) n_busy[b] = s_busy;
+    if (s_bad) {
+      set_status(kv.status, SE_ERR_UNEVEN);
+      atomicExch(w.abort, 1);
+    }
+  }
+}
+
+__global__ void zero_int_kernel(int32_t* p) { *p = 0; }
+
+}  // namespace se
+
+using namespace se;
+
+// ---------------------------------------------------------------------------
+// Host entry points
+// ---------------------------------------------------------------------------
+
+static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
+                                int32_t keep_stride, const int32_t* n_keep,
+                                const int32_t* first_slot, int32_t max_keep, float* aux,
+                                int64_t aux_stride, void* ws, size_t ws_bytes,
+                                const int32_t* abort_in, cudaStream_t st) {
+  size_t need = 0;
+  CompactWs w = carve_compact(kv, max_keep, ws, aux != nullptr, &need);
+  if (ws == nullptr || ws_bytes < need) return SE_ERR_INVALID_ARG;
+  compact_plan_kernel<<<1, 1024, 0, st>>>(*kv, n_keep, first_slot, max_keep, abort_in, w);
+  const int row_bytes = kv->D * (int)elem_size(kv->dtype);
+  const int chunks = row_bytes / 16;
+  const int epc = 64;
+  const int max_entries = max_keep + kv->page_size;
+  dim3 grid(cdiv(max_entries, epc), kv->Hkv, kv->B);
+  switch (chunks) {
+    case 8:
+      compact_gather_kernel<8><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
+                                                      aux_stride, w, epc);
+      break;
+    case 16:
+      compact_gather_kernel<16><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
+                                                       aux_stride, w, epc);
+      break;
+    case 32:
+      compact_gather_kernel<32><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
+                                                       aux_stride, w, epc);
+      break;
+    default:
+      return SE_ERR_UNSUPPORTED;
+  }
+  compact_finalize_kernel<<<kv->B, 256, 0, st>>>(*kv, aux, aux_stride, w);
+  return se_last_launch_status();
+}
+
+extern "C" size_t se_compact_evict_workspace_size(const se_paged_kv* kv, int32_t max_keep) {
+  if (kv == nullptr) return 0;
+  size_t a = 0, b = 0;
+  carve_compact(kv, max_keep, nullptr, true, &a);
+  carve_move(kv, nullptr, &b);
+  return a > b ? a : b;
+}
+
+extern "C" se_status se_compact_evict(const se_paged_kv* kv, int32_t mode,
+                                      const int32_t* keep_idx, int32_t keep_stride,
+                                      const int32_t* n_keep, const int32_t* first_slot,
+                                      int32_t max_keep, float* aux, int64_t aux_stride,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (keep_idx == nullptr || workspace == nullptr) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode == SE_COMPACT_FRESH_PAGES) {
+    if (n_keep == nullptr || first_slot == nullptr || max_keep < 0 || keep_stride < max_keep)
+      return SE_ERR_INVALID_ARG;
+    return launch_compact(kv, keep_idx, keep_stride, n_keep, first_slot, max_keep, aux,
+                          aux_stride, workspace, workspace_bytes, nullptr, st);
+  }
+  if (mode == SE_COMPACT_MOVE_LAST) {
+    size_t need = 0;
+    MoveWs w = carve_move(kv, workspace, &need);
+    if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+    move_last_plan_kernel<<<1, 1024, 0, st>>>(*kv, keep_idx, w);
+    move_last_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, keep_idx, aux, aux_stride, w);
+    return se_last_launch_status();
+  }
+  return SE_ERR_INVALID_ARG;
+}
+
+extern "C" size_t se_append_kv_workspace_size(const se_paged_kv* kv) {
+  if (kv == nullptr) return 0;
+  size_t b = 0;
+  carve_append(kv, nullptr, &b);
+  return b;
+}
+
+extern "C" se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
+                                  float* aux, int64_t aux_stride, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (k_new == nullptr || v_new == nullptr || workspace == nullptr) return SE_ERR_INVALID_ARG;
+  size_t need = 0;
+  AppendWs w = carve_append(kv, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  append_plan_kernel<<<1, 1024, 0, st>>>(*kv, w);
+  append_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, k_new, v_new, aux, aux_stride, w);
+  return se_last_launch_status();
+}
+
+extern "C" size_t se_prune_span_workspace_size(const se_paged_kv* kv) {
+  if (kv == nullptr) return 0;
+  size_t b = 0;
+  carve_prune(kv, nullptr, &b);
+  return b;
+}
+
+extern "C" se_status se_prune_span(const se_paged_kv* kv, const int32_t* L, const int32_t* R,
+                                   const uint8_t* mask, int32_t mask_stride, int32_t* n_busy,
+                                   float* aux, int64_t aux_stride, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (L == nullptr || R == nullptr || mask == nullptr || workspace == nullptr || mask_stride < 0)
+    return SE_ERR_INVALID_ARG;
+  size_t need = 0;
+  PruneWs w = carve_prune(kv, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t smax = kv->max_pages_per_seq * kv->page_size;
+  zero_int_kernel<<<1, 1, 0, st>>>(w.abort);
+  prune_plan_kernel<<<kv->B, 1024, 0, st>>>(*kv, L, R, mask, mask_stride, n_busy, w);
+  return launch_compact(kv, w.keep, smax, w.n_keep, w.first, smax, aux, aux_stride, w.compact_ws,
+                        w.compact_bytes, w.abort, st);
+}

@@ -1,0 +1,343 @@
+// Decode attention over a view of the paged cache.
+//
+// SparseEngine "How it works" (AttentionView): View = BuildView(C, I),
+// o = Attention(q, View) -- the view is every resident entry, the resident
+// slots of a list of blocks (Quest pages) or a list of slots.
+//
+// Bandwidth-bound design (each K/V byte is used by the G query heads of its
+// group and nothing else): split-K over the view ("chunks" of entries, one
+// CTA each, sized so the grid fills the 152 SMs several times), one half-warp
+// per entry with 16-byte row loads (a 256-byte bf16 row is one coalesced
+// half-warp load), the group's G queries pre-scaled by log2(e)/sqrt(D) in
+// registers, a 4-step xor butterfly for the dot products and a base-2 online
+// softmax per half-warp.  Half-warp states merge in shared memory; a second
+// kernel merges the chunks and, for H2O, adds sum_h p_{h,j} to the running
+// scores from the logits the first kernel stored.
+#include "se_common.cuh"
+
+namespace se {
+
+template <typename T, int V>
+SE_DEV void load_row(const T* p, float* f) {
+  if constexpr (sizeof(T) == 2 && V == 8) {
+    unpack8_bf16(ldg_nc_v4(p), f);
+  } else if constexpr (sizeof(T) == 2 && V == 4) {
+    uint2 u;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(u.x), "=r"(u.y) : "l"(p));
+    f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  } else if constexpr (sizeof(T) == 4 && V == 4) {
+    const uint4 u = ldg_nc_v4(p);
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  } else {
+    static_assert(sizeof(T) == 4 && V == 8, "row layout");
+    const uint4 u = ldg_nc_v4(p);
+    const uint4 w = ldg_nc_v4(p + 4);
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    f[4] = __uint_as_float(w.x); f[5] = __uint_as_float(w.y);
+    f[6] = __uint_as_float(w.z); f[7] = __uint_as_float(w.w);
+  }
+}
+
+SE_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct DecodeArgs {
+  se_paged_kv kv;
+  const void* q;
+  int view;
+  const int32_t* sel;
+  int32_t sel_stride;
+  int32_t n_sel;
+  int chunk;     // view entries per CTA
+  int n_chunks;
+  float* part;   // [B][Hkv][n_chunks][G][D + 2]
+  float* logits; // [B][Hkv][max_entries][G] or null
+  int max_entries;
+};
+
+// Resident slot of view entry e of (b, g), or -1.
+SE_DEV int view_slot(const DecodeArgs& a, int b, int g, int e, int ctx) {
+  if (a.view == SE_VIEW_DENSE) return e < ctx ? e : -1;
+  const int32_t* sel = a.sel + ((int64_t)b * a.kv.Hkv + g) * a.sel_stride;
+  if (a.view == SE_VIEW_PAGES) {
+    const int P = a.kv.page_size;
+    const int i = e / P;
+    if (i >= a.n_sel) return -1;
+    const int blk = sel[i];
+    const int s = blk * P + e % P;
+    return (blk >= 0 && s < ctx) ? s : -1;
+  }
+  if (e >= a.n_sel) return -1;
+  const int s = sel[e];
+  return (s >= 0 && s < ctx) ? s : -1;
+}
+
+SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
+  if (a.view == SE_VIEW_DENSE) return ctx;
+  if (a.view == SE_VIEW_PAGES) return a.n_sel * a.kv.page_size;
+  return a.n_sel;
+}
+
+// grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
+  constexpr int V = D / 16;  // elements per lane
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ float s_o[8][G][D];
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const se_paged_kv& kv = a.kv;
+  const int P = kv.page_size;
+  const int ctx = kv.ctx_len[b];
+  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int n_view = min(view_entries(a, ctx), a.max_entries);
+  const int e_begin = c * a.chunk;
+  const int e_end = min(e_begin + a.chunk, n_view);
+
+  const float qscale = kLog2e * rsqrtf((float)D);
+  float q[G][V];
+  const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+    for (int i = 0; i < V; ++i) q[j][i] *= qscale;
+  }
+  float m[G], l[G], o[G][V];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) o[j][i] = 0.f;
+  }
+  const T* kp = static_cast<const T*>(kv.k_pool);
+  const T* vp = static_cast<const T*>(kv.v_pool);
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
+
+  constexpr int U = 4;  // entries in flight per half-warp
+  // Every lane of a warp runs the same iterations (the xor shuffles below
+  // need both half-warps); invalid entries are predicated off.
+  for (int base = e_begin; base < e_end; base += 8 * U) {
+    float kf[U][V], vf[U][V];
+    int slot[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = base + hw + 8 * u;
+      slot[u] = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
+      if (slot[u] >= 0) {
+        const int64_t off = (((int64_t)bt[slot[u] / P] * kv.Hkv + g) * P + slot[u] % P) * D + t * V;
+        load_row<T, V>(kp + off, kf[u]);
+        load_row<T, V>(vp + off, vf[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) { kf[u][i] = 0.f; vf[u][i] = 0.f; }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float s[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[u][i], acc);
+        s[j] = acc;
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+        for (int j = 0; j < G; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], off);
+      if (slot[u] < 0) continue;  // uniform within the half-warp
+      if (lg != nullptr && t < G) {
+        float sv = s[0];
+#pragma unroll
+        for (int j = 1; j < G; ++j) sv = (t == j) ? s[j] : sv;
+        lg[(int64_t)(base + hw + 8 * u) * G + t] = sv;
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float mn = fmaxf(m[j], s[j]);
+        const float sc = ex2(m[j] - mn);
+        const float p = ex2(s[j] - mn);
+        l[j] = fmaf(l[j], sc, p);
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[j][i] = fmaf(o[j][i], sc, p * vf[u][i]);
+        m[j] = mn;
+      }
+    }
+  }
+  // merge the 8 half-warp states
+  if (t == 0) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) { s_m[hw][j] = m[j]; s_l[hw][j] = l[j]; }
+  }
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int i = 0; i < V; ++i) s_o[hw][j][t * V + i] = o[j][i];
+  __syncthreads();
+  float* part = a.part + (((int64_t)b * kv.Hkv + g) * a.n_chunks + c) * G * (D + 2);
+  for (int x = threadIdx.x; x < G * D; x += 128) {
+    const int j = x / D, d = x % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w][j]);
+    float acc = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float f = ex2(s_m[w][j] - M);
+        acc = fmaf(s_o[w][j][d], f, acc);
+        L = fmaf(s_l[w][j], f, L);
+      }
+    }
+    part[j * (D + 2) + d] = acc;
+    if (d == 0) {
+      part[j * (D + 2) + D] = M;
+      part[j * (D + 2) + D + 1] = L;
+    }
+  }
+}
+
+// grid: (Hkv, B); 128 threads.  Merges chunks, writes o, updates acc.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a, T* out, float* acc,
+                                                             int64_t acc_stride) {
+  __shared__ float s_M[G], s_invL[G];
+  const int g = blockIdx.x, b = blockIdx.y;
+  const se_paged_kv& kv = a.kv;
+  const float* part = a.part + ((int64_t)b * kv.Hkv + g) * a.n_chunks * G * (D + 2);
+  if (threadIdx.x < G) {
+    const int j = threadIdx.x;
+    float M = -INFINITY;
+    for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, part[(c * G + j) * (D + 2) + D]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int c = 0; c < a.n_chunks; ++c) {
+        const float* pc = part + (c * G + j) * (D + 2);
+        L = fmaf(pc[D + 1], ex2(pc[D] - M), L);
+      }
+    s_M[j] = M;
+    s_invL[j] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
+    const int j = x / D, d = x % D;
+    const float M = s_M[j];
+    float v = 0.f;
+    if (M != -INFINITY)
+      for (int c = 0; c < a.n_chunks; ++c) {
+        const float* pc = part + (c * G + j) * (D + 2);
+        v = fmaf(pc[d], ex2(pc[D] - M), v);
+      }
+    v *= s_invL[j];
+    T* op = out + ((int64_t)b * kv.Hq + g * G + j) * D + d;
+    if constexpr (sizeof(T) == 2) *op = __float2bfloat16_rn(v);
+    else *op = v;
+  }
+  if (acc != nullptr && a.logits != nullptr) {
+    const int ctx = kv.ctx_len[b];
+    const int n_view = min(view_entries(a, ctx), a.max_entries);
+    const float* lg = a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G;
+    float* ar = acc + ((int64_t)b * kv.Hkv + g) * acc_stride;
+    for (int e = threadIdx.x; e < n_view; e += blockDim.x) {
+      const int s = view_slot(a, b, g, e, ctx);
+      if (s < 0) continue;
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < G; ++j) ps += ex2(lg[(int64_t)e * G + j] - s_M[j]) * s_invL[j];
+      ar[s] += ps;
+    }
+  }
+}
+
+struct DecodeWs {
+  float* part;
+  float* logits;
+};
+
+static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, int n_chunks, void* ws,
+                             size_t* bytes) {
+  WsCarver c(ws);
+  DecodeWs w;
+  const int G = kv->Hq / kv->Hkv;
+  w.part = c.take<float>((size_t)kv->B * kv->Hkv * n_chunks * G * (kv->D + 2));
+  w.logits = c.take<float>((size_t)kv->B * kv->Hkv * max_entries * G);
+  *bytes = c.bytes();
+  return w;
+}
+
+// Entries per CTA: enough CTAs to fill the GPU several times over.
+static int pick_chunk(const se_paged_kv* kv, int max_entries) {
+  const int64_t units = (int64_t)kv->B * kv->Hkv;
+  int chunk = 1024;
+  while (chunk > 64 && units * cdiv(max_entries, chunk) < 152 * 8) chunk >>= 1;
+  return chunk;
+}
+
+template <typename T, int D, int G>
+static void launch_decode_t(const DecodeArgs& a, void* o, float* acc, int64_t acc_stride,
+                            cudaStream_t st) {
+  decode_partial_kernel<T, D, G><<<dim3(a.n_chunks, a.kv.Hkv, a.kv.B), 128, 0, st>>>(a);
+  decode_combine_kernel<T, D, G><<<dim3(a.kv.Hkv, a.kv.B), 128, 0, st>>>(a, static_cast<T*>(o),
+                                                                          acc, acc_stride);
+}
+
+template <typename T, int D>
+static se_status launch_decode_d(const DecodeArgs& a, int G, void* o, float* acc,
+                                 int64_t acc_stride, cudaStream_t st) {
+  switch (G) {
+    case 1: launch_decode_t<T, D, 1>(a, o, acc, acc_stride, st); return SE_OK;
+    case 2: launch_decode_t<T, D, 2>(a, o, acc, acc_stride, st); return SE_OK;
+    case 4: launch_decode_t<T, D, 4>(a, o, acc, acc_stride, st); return SE_OK;
+    case 8: launch_decode_t<T, D, 8>(a, o, acc, acc_stride, st); return SE_OK;
+    default: return SE_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace se
+
+using namespace se;
+
+extern "C" size_t se_sparse_decode_attn_workspace_size(const se_paged_kv* kv, int32_t max_entries) {
+  if (kv == nullptr || max_entries < 0) return 0;
+  const int chunk = pick_chunk(kv, max_entries);
+  size_t b = 0;
+  carve_decode(kv, max_entries, cdiv(max(max_entries, 1), chunk), nullptr, &b);
+  return b;
+}
+
+extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
+                                           const int32_t* sel, int32_t sel_stride, int32_t n_sel,
+                                           int32_t max_entries, void* o, float* acc_scores,
+                                           int64_t acc_stride, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (q == nullptr || o == nullptr || workspace == nullptr || max_entries < 1) return SE_ERR_INVALID_ARG;
+  if (view != SE_VIEW_DENSE && (sel == nullptr || n_sel < 0 || sel_stride < n_sel))
+    return SE_ERR_INVALID_ARG;
+  if (view < SE_VIEW_DENSE || view > SE_VIEW_TOKENS) return SE_ERR_INVALID_ARG;
+  const int chunk = pick_chunk(kv, max_entries);
+  const int n_chunks = cdiv(max_entries, chunk);
+  size_t need = 0;
+  DecodeWs w = carve_decode(kv, max_entries, n_chunks, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  DecodeArgs a{*kv, q, view, sel, sel_stride, n_sel, chunk, n_chunks, w.part,
+               acc_scores ? w.logits : nullptr, max_entries};
+  const int G = kv->Hq / kv->Hkv;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (kv->dtype == SE_BF16 && kv->D == 128) s = launch_decode_d<__nv_bfloat16, 128>(a, G, o, acc_scores, acc_stride, st);
+  else if (kv->dtype == SE_BF16 && kv->D == 64) s = launch_decode_d<__nv_bfloat16, 64>(a, G, o, acc_scores, acc_stride, st);
+  else if (kv->dtype == SE_F32 && kv->D == 128) s = launch_decode_d<float, 128>(a, G, o, acc_scores, acc_stride, st);
+  else if (kv->dtype == SE_F32 && kv->D == 64) s = launch_decode_d<float, 64>(a, G, o, acc_scores, acc_stride, st);
+  else return SE_ERR_UNSUPPORTED;
+  if (s != SE_OK) return s;
+  return se_last_launch_status();
+}

@@ -1,0 +1,249 @@
+// Quest page metadata and query-dependent page selection.
+//
+// SparseEngine "How it works" (build_decode_selection performs Quest's
+// query-dependent page selection; metadata persists beside the KV state) and
+// "How it differs" (Quest keeps the full KV history).  The bound per page p
+// and KV group g is sum_{h in g} sum_d max(q_hd * kmax_pd, q_hd * kmin_pd).
+//
+// Both kernels stream HBM: the metadata build reads every resident key once
+// (16-byte loads, one CTA per page, 16 threads per head row); the bound
+// kernel reads 2*D elements per (page, group) with one half-warp per page and
+// the group's queries held in registers, writes one float per page, and the
+// shared block radix top-k then picks the pages.
+#include "se_common.cuh"
+
+namespace se {
+
+se_status launch_topk_select_pages(int B, int Hkv, const float* U, int64_t stride,
+                                   const int32_t* cand_lo, const int32_t* cand_hi,
+                                   const int32_t* force_lo,
+                                   const int32_t* force_hi, int32_t* out, int32_t out_stride,
+                                   int32_t* n_sel, int32_t* status, int top, int n_max,
+                                   cudaStream_t st);
+
+// grid: (blocks of a sequence, B); threads: Hkv * (row_bytes/16) <= 1024
+template <typename T>
+__global__ void quest_meta_kernel(se_paged_kv kv, T* kmin, T* kmax) {
+  const int blk = blockIdx.x, b = blockIdx.y;
+  const int P = kv.page_size;
+  const int ctx = kv.ctx_len[b];
+  if (blk * P >= ctx) return;
+  const int rows = min(P, ctx - blk * P);
+  const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
+  constexpr int EPC = 16 / sizeof(T);  // elements per 16-byte chunk
+  const int chunks = kv.D / EPC;
+  const int t = threadIdx.x;
+  if (t >= kv.Hkv * chunks) return;
+  const int h = t / chunks, c = t % chunks;
+  const T* base = static_cast<const T*>(kv.k_pool) + (((int64_t)page * kv.Hkv + h) * P) * kv.D + c * EPC;
+  float mn[EPC], mx[EPC];
+#pragma unroll
+  for (int i = 0; i < EPC; ++i) { mn[i] = INFINITY; mx[i] = -INFINITY; }
+  for (int r = 0; r < rows; ++r) {
+    const uint4 u = ldg_nc_v4(base + (int64_t)r * kv.D);
+    float f[EPC];
+    if constexpr (sizeof(T) == 2) {
+      unpack8_bf16(u, f);
+    } else {
+      f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+      f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+#pragma unroll
+    for (int i = 0; i < EPC; ++i) { mn[i] = fminf(mn[i], f[i]); mx[i] = fmaxf(mx[i], f[i]); }
+  }
+  const int64_t o = ((int64_t)page * kv.Hkv + h) * kv.D + c * EPC;
+#pragma unroll
+  for (int i = 0; i < EPC; ++i) {
+    if constexpr (sizeof(T) == 2) {
+      kmin[o + i] = __float2bfloat16_rn(mn[i]);  // exact: a bf16 value
+      kmax[o + i] = __float2bfloat16_rn(mx[i]);
+    } else {
+      kmin[o + i] = mn[i];
+      kmax[o + i] = mx[i];
+    }
+  }
+}
+
+// Page bound U for every full block.  grid: (cdiv(max_blocks, 16), Hkv, B),
+// 256 threads = 8 warps x 2 half-warps, one block per half-warp.
+// D = 128 bf16: lane t of the half-warp owns dims [8t, 8t+8).
+template <int G>
+__global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
+                                                               const __nv_bfloat16* __restrict__ kmin,
+                                                               const __nv_bfloat16* __restrict__ kmax,
+                                                               const __nv_bfloat16* __restrict__ q,
+                                                               float* __restrict__ U,
+                                                               int64_t u_stride) {
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int P = kv.page_size;
+  const int nb = cdiv(kv.ctx_len[b], P);
+  const int half = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int blk = blockIdx.x * 16 + half;
+  float qv[G][8];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const uint4 u = ldg_nc_v4(q + ((int64_t)b * kv.Hq + g * G + j) * kv.D + t * 8);
+    unpack8_bf16(u, qv[j]);
+  }
+  float acc = 0.f;
+  const bool active = blk < nb - 1 && blk < u_stride;
+  if (active) {
+    const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
+    const int64_t o = ((int64_t)page * kv.Hkv + g) * kv.D + t * 8;
+    float mn[8], mx[8];
+    unpack8_bf16(ldg_nc_v4(kmin + o), mn);
+    unpack8_bf16(ldg_nc_v4(kmax + o), mx);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) part += fmaxf(qv[j][i] * mx[i], qv[j][i] * mn[i]);
+      acc += part;
+    }
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (active && t == 0) U[((int64_t)b * kv.Hkv + g) * u_stride + blk] = acc;
+}
+
+// Generic bound (any D, fp32 or bf16): one thread per (block, group).
+template <typename T>
+__global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const T* kmax,
+                                           const T* q, float* U, int64_t u_stride) {
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int blk = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nb = cdiv(kv.ctx_len[b], kv.page_size);
+  if (blk >= nb - 1 || blk >= u_stride) return;
+  const int G = kv.Hq / kv.Hkv;
+  const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
+  const int64_t o = ((int64_t)page * kv.Hkv + g) * kv.D;
+  float acc = 0.f;
+  for (int j = 0; j < G; ++j) {
+    const T* qh = q + ((int64_t)b * kv.Hq + g * G + j) * kv.D;
+    float part = 0.f;
+    for (int d = 0; d < kv.D; ++d) {
+      const float x = (float)qh[d];
+      part += fmaxf(x * (float)kmax[o + d], x * (float)kmin[o + d]);
+    }
+    acc += part;
+  }
+  U[((int64_t)b * kv.Hkv + g) * u_stride + blk] = acc;
+}
+
+// cand_hi = nblocks - 1, forced = [nblocks - 1, nblocks)
+__global__ void quest_ranges_kernel(const int32_t* ctx_len, int B, int P, int max_blocks,
+                                    int32_t* status, int32_t* cand_hi, int32_t* flo,
+                                    int32_t* fhi) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int nb = cdiv(ctx_len[b], P);
+  if (nb > max_blocks) {  // bound buffer too short: select among the first max_blocks
+    set_status(status, SE_ERR_BOUNDS);
+    nb = max_blocks;
+  }
+  cand_hi[b] = max(nb - 1, 0);
+  flo[b] = max(nb - 1, 0);
+  fhi[b] = nb;
+}
+
+struct QuestWs {
+  float* U;
+  int32_t* cand_lo;
+  int32_t* cand_hi;
+  int32_t* flo;
+  int32_t* fhi;
+  int64_t u_stride;
+};
+
+static QuestWs carve_quest(const se_paged_kv* kv, int32_t max_blocks, void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  QuestWs w;
+  w.u_stride = max_blocks;
+  w.U = c.take<float>((size_t)kv->B * kv->Hkv * max_blocks);
+  w.cand_lo = c.take<int32_t>(kv->B);
+  w.cand_hi = c.take<int32_t>(kv->B);
+  w.flo = c.take<int32_t>(kv->B);
+  w.fhi = c.take<int32_t>(kv->B);
+  *bytes = c.bytes();
+  return w;
+}
+
+}  // namespace se
+
+using namespace se;
+
+extern "C" se_status se_quest_build_meta(const se_paged_kv* kv, void* kmin, void* kmax,
+                                         void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (kmin == nullptr || kmax == nullptr) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int threads = kv->Hkv * kv->D * (int)elem_size(kv->dtype) / 16;
+  if (threads > 1024) return SE_ERR_UNSUPPORTED;
+  dim3 grid(kv->max_pages_per_seq, kv->B);
+  if (kv->dtype == SE_BF16)
+    quest_meta_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+        *kv, static_cast<__nv_bfloat16*>(kmin), static_cast<__nv_bfloat16*>(kmax));
+  else
+    quest_meta_kernel<float><<<grid, threads, 0, st>>>(*kv, static_cast<float*>(kmin),
+                                                       static_cast<float*>(kmax));
+  return se_last_launch_status();
+}
+
+extern "C" size_t se_quest_page_select_workspace_size(const se_paged_kv* kv, int32_t max_blocks) {
+  if (kv == nullptr) return 0;
+  size_t b = 0;
+  carve_quest(kv, max_blocks, nullptr, &b);
+  return b;
+}
+
+__global__ void se_fill_zero_i32(int32_t* p, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0;
+}
+
+extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmin,
+                                          const void* kmax, const void* q, int32_t top_pages,
+                                          int32_t max_blocks, int32_t* page_idx, int32_t* n_sel,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (kmin == nullptr || kmax == nullptr || q == nullptr || page_idx == nullptr ||
+      workspace == nullptr || top_pages < 0 || max_blocks < 1 ||
+      max_blocks > kv->max_pages_per_seq)
+    return SE_ERR_INVALID_ARG;
+  size_t need = 0;
+  QuestWs w = carve_quest(kv, max_blocks, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int G = kv->Hq / kv->Hkv;
+  dim3 grid(cdiv(max_blocks, 16), kv->Hkv, kv->B);
+  if (kv->dtype == SE_BF16 && kv->D == 128 && (G == 1 || G == 2 || G == 4 || G == 8)) {
+    auto km = static_cast<const __nv_bfloat16*>(kmin);
+    auto kx = static_cast<const __nv_bfloat16*>(kmax);
+    auto qq = static_cast<const __nv_bfloat16*>(q);
+    if (G == 1) quest_bound_bf16_kernel<1><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 2) quest_bound_bf16_kernel<2><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 4) quest_bound_bf16_kernel<4><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 8) quest_bound_bf16_kernel<8><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
+  } else {
+    dim3 g2(cdiv(max_blocks, 128), kv->Hkv, kv->B);
+    if (kv->dtype == SE_BF16)
+      quest_bound_generic_kernel<__nv_bfloat16><<<g2, 128, 0, st>>>(
+          *kv, static_cast<const __nv_bfloat16*>(kmin), static_cast<const __nv_bfloat16*>(kmax),
+          static_cast<const __nv_bfloat16*>(q), w.U, w.u_stride);
+    else
+      quest_bound_generic_kernel<float><<<g2, 128, 0, st>>>(
+          *kv, static_cast<const float*>(kmin), static_cast<const float*>(kmax),
+          static_cast<const float*>(q), w.U, w.u_stride);
+  }
+  se_fill_zero_i32<<<cdiv(kv->B, 256), 256, 0, st>>>(w.cand_lo, kv->B);
+  quest_ranges_kernel<<<cdiv(kv->B, 256), 256, 0, st>>>(kv->ctx_len, kv->B, kv->page_size,
+                                                        max_blocks, kv->status, w.cand_hi, w.flo,
+                                                        w.fhi);
+  s = launch_topk_select_pages(kv->B, kv->Hkv, w.U, w.u_stride, w.cand_lo, w.cand_hi, w.flo,
+                               w.fhi, page_idx, top_pages + 1, n_sel, kv->status, top_pages,
+                               max_blocks, st);
+  if (s != SE_OK) return s;
+  return se_last_launch_status();
+}

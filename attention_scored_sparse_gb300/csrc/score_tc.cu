@@ -1,0 +1,724 @@
+// Window scoring on the 5th-generation tensor cores (bf16, D = 128).
+//
+// SparseEngine "How it works" (SnapKV / H2O: attention of the window queries
+// over the cached keys) and KARA Method 1 (bidirectional window scoring):
+//     s[b, g, j] = sum_{h in g} sum_{q in window} softmax_j(q . k_j / sqrt(D))
+// Rows of a group are (window query, head in group); the softmax of a row is
+// needed before its column can be summed, so there are two sweeps:
+//
+//   pass 1 (rowstats)  S = Q_rows K_tile^T with the 256 rows of a chunk on
+//       TMEM lanes (two M=128 accumulators), N = 128 keys; each epilogue
+//       thread owns one row and keeps a base-2 running max / sum over its
+//       CTA's key range.  Partials per key split go to the workspace.
+//   rowinfo            the CUDA-core kernel merges the splits: lse2 per row
+//       (plus the row's query position for causal masking).
+//   pass 2 (colsum)    S^T = K_tile Q_rows^T with the 128 keys of a tile on
+//       TMEM lanes (M=128), N = 256 rows; each epilogue thread owns one key
+//       and sums exp2(t - lse2_r) over the rows in registers -- no cross-
+//       thread reduction -- and writes its column sum.
+//
+// Both passes: one producer warp issues TMA loads (K pages as 16-row boxes
+// gathered through the block table, 128-byte swizzle; Q via a 4-D map over
+// [B][w][Hq][D]; key positions and row info as 1-D bulk copies), one warp
+// issues tcgen05.mma from shared-memory descriptors into double-buffered TMEM
+// accumulators, eight warps run the softmax epilogue from tcgen05.ld.  Every
+// mbarrier wait is bounded by %globaltimer: on expiry the CTA records
+// SE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "tc_primitives.cuh"
+
+namespace se {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kKeyTile = 128;       // keys per tile (M of pass 2, N of pass 1)
+constexpr int kRowChunk = 256;      // rows per chunk (2 x M=128 in pass 1, N of pass 2)
+constexpr int kKTileBytes = kKeyTile * kD * 2;   // 32 KB
+constexpr int kQChunkBytes = kRowChunk * kD * 2; // 64 KB
+constexpr int kStages1 = 4;         // K-tile ring depth, pass 1
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
+
+struct TcArgs {
+  int B, Hq, Hkv, G, w, P, rows, RC;  // RC: row chunks of 256
+  int max_pages_per_seq, num_pages;
+  const int32_t* block_table;
+  const int32_t* slot_map;
+  int64_t smax;                       // slot-map row length
+  const int32_t* q_pos;
+  const int32_t* attn_lo;
+  const int32_t* attn_hi;
+  const int32_t* out_lo;
+  const int32_t* out_hi;
+  int causal, accumulate, n_max;
+  float* scores;
+  int64_t scores_stride;
+  float* part;      // [groups][RC*256][n_splits][2]
+  float2* rowinfo;  // [groups][RC*256] {lse2, qpos bits}
+  int n_splits, tiles_per_split, tiles_per_cta2;
+  int32_t* status;
+  float scale;      // log2(e) / sqrt(D)
+};
+
+// Key-tile geometry of one (sequence, group): tiles start at the page that
+// holds attn_lo; tile t covers slots [base + 128 t, base + 128 t + 128).
+struct TileGeom {
+  int lo, hi, base, n_tiles, end_block;
+  SE_DEV static TileGeom make(const TcArgs& a, int b) {
+    TileGeom t;
+    t.lo = a.attn_lo[b];
+    t.hi = a.attn_hi[b];
+    t.base = (t.lo / a.P) * a.P;
+    t.n_tiles = t.hi > t.lo ? cdiv(t.hi - t.base, kKeyTile) : 0;
+    t.end_block = cdiv(t.hi, a.P);
+    return t;
+  }
+  SE_DEV int pages_in(int tile, int P) const {
+    const int first = base / P + tile * (kKeyTile / P);
+    return max(0, min(kKeyTile / P, end_block - first));
+  }
+};
+
+SE_DEV bool geom_ok(const TcArgs& a, const TileGeom& t) {
+  return t.lo >= 0 && t.hi >= t.lo && t.hi - t.lo <= a.n_max &&
+         (int64_t)t.hi <= a.smax;
+}
+
+// Issues the TMA loads of K tile `tile` of (b, g) into `dst` (2 column halves
+// of 128 rows x 128 bytes) and, when `pos` is set, the tile's key positions.
+// Returns the bytes the loads will deliver.
+SE_DEV uint32_t load_k_tile(const TcArgs& a, const CUtensorMap* kmap, const TileGeom& tg, int b,
+                            int g, int tile, uint8_t* dst, int32_t* pos, uint64_t* bar) {
+  const int P = a.P;
+  const int np = tg.pages_in(tile, P);
+  const int blk0 = tg.base / P + tile * (kKeyTile / P);
+  uint32_t bytes = (uint32_t)np * P * kD * 2;
+  if (pos != nullptr) {
+    const int s0 = tg.base + tile * kKeyTile;
+    const int cnt = (int)(a.smax - s0 < kKeyTile ? a.smax - s0 : kKeyTile);
+    bytes += (uint32_t)cnt * 4;
+  }
+  tc::mbar_arrive_expect_tx(bar, bytes);
+  const int32_t* bt = a.block_table + (int64_t)b * a.max_pages_per_seq;
+  for (int i = 0; i < np; ++i) {
+    const int page = bt[blk0 + i];
+    const int y = (page * a.Hkv + g) * P;
+    tc::tma_load_2d(dst + i * P * 128, kmap, bar, 0, y);
+    tc::tma_load_2d(dst + kKTileBytes / 2 + i * P * 128, kmap, bar, 64, y);
+  }
+  if (pos != nullptr) {
+    const int s0 = tg.base + tile * kKeyTile;
+    const int cnt = (int)(a.smax - s0 < kKeyTile ? a.smax - s0 : kKeyTile);
+    const int32_t* src = a.slot_map + ((int64_t)b * a.Hkv + g) * a.smax + s0;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(tc::smem_u32(pos)), "l"(src), "r"(cnt * 4), "r"(tc::smem_u32(bar))
+        : "memory");
+  }
+  return bytes;
+}
+
+SE_DEV void load_q_chunk(const TcArgs& a, const CUtensorMap* qmap, int b, int g, int rc,
+                         uint8_t* dst, uint64_t* bar) {
+  const int qpc = kRowChunk / a.G;  // queries per chunk
+  tc::mbar_arrive_expect_tx(bar, kQChunkBytes);
+  tc::tma_load_4d(dst, qmap, bar, 0, g * a.G, rc * qpc, b);
+  tc::tma_load_4d(dst + kQChunkBytes / 2, qmap, bar, 64, g * a.G, rc * qpc, b);
+}
+
+SE_DEV bool aborted(const int* flag) { return *reinterpret_cast<const volatile int*>(flag) != 0; }
+
+SE_DEV void record_timeout(const TcArgs& a, int* s_abort) {
+  set_status(a.status, SE_ERR_TIMEOUT);
+  atomicExch(s_abort, 1);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 320 threads.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                  TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;                                   // 64 KB
+  uint8_t* k_s = q_s + kQChunkBytes;                     // kStages1 x 32 KB
+  int32_t* pos_s = reinterpret_cast<int32_t*>(k_s + kStages1 * kKTileBytes);  // [S][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pos_s + kStages1 * kKeyTile);
+  uint64_t* full = bars;                   // [S]  TMA -> MMA / epilogue
+  uint64_t* empty = bars + kStages1;       // [S]  MMA done reading K
+  uint64_t* pos_free = bars + 2 * kStages1;  // [S] epilogue done with positions
+  uint64_t* acc_full = bars + 3 * kStages1;  // [2]
+  uint64_t* acc_free = acc_full + 2;         // [2]
+  uint64_t* q_full = acc_free + 2;
+  uint64_t* done = q_full + 1;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, rc = blockIdx.y, bg = blockIdx.z;
+  const int b = bg / a.Hkv, g = bg % a.Hkv;
+  const TileGeom tg = TileGeom::make(a, b);
+  const bool ok = geom_ok(a, tg);
+  const int t_begin = split * a.tiles_per_split;
+  const int t_end = ok ? min(t_begin + a.tiles_per_split, tg.n_tiles) : 0;
+  const int n_my = max(t_end - t_begin, 0);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    if (!ok) set_status(a.status, SE_ERR_BOUNDS);
+    for (int s = 0; s < kStages1; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&pos_free[s], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_free[i], kEpiWarps);
+    }
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
+      if (n_my > 0) load_q_chunk(a, &qmap, b, g, rc, q_s, q_full);
+      int issued = 0;
+      for (int i = 0; i < n_my && !aborted(&s_abort); ++i) {
+        const int s = i % kStages1;
+        const uint32_t par = ((i / kStages1) & 1) ^ 1;
+        if (i >= kStages1) {
+          if (!tc::mbar_wait(&empty[s], par, kTimeoutNs) ||
+              !tc::mbar_wait(&pos_free[s], par, kTimeoutNs)) {
+            record_timeout(a, &s_abort);
+            break;
+          }
+        }
+        load_k_tile(a, &kmap, tg, b, g, t_begin + i, k_s + s * kKTileBytes,
+                    a.causal ? pos_s + s * kKeyTile : nullptr, &full[s]);
+        issued = i + 1;
+      }
+      // drain: every issued load must land before the CTA can exit
+      for (int i = max(0, issued - kStages1); i < issued; ++i)
+        tc::mbar_wait(&full[i % kStages1], (i / kStages1) & 1, kTimeoutNs);
+      if (n_my > 0) tc::mbar_wait(q_full, 0, kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (tc::elect_one()) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, kKeyTile);
+      bool go = n_my > 0 && tc::mbar_wait(q_full, 0, kTimeoutNs);
+      if (n_my > 0 && !go) record_timeout(a, &s_abort);
+      for (int i = 0; go && i < n_my && !aborted(&s_abort); ++i) {
+        const int s = i % kStages1;
+        const int acc = i & 1;
+        if (!tc::mbar_wait(&full[s], (i / kStages1) & 1, kTimeoutNs) ||
+            (i >= 2 && !tc::mbar_wait(&acc_free[acc], ((i >> 1) & 1) ^ 1, kTimeoutNs))) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t kbase = tc::smem_u32(k_s + s * kKTileBytes);
+        const uint32_t qbase = tc::smem_u32(q_s);
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = tc::smem_desc_sw128(qbase + (k >> 2) * (kQChunkBytes / 2) +
+                                                    mb * (128 * 128) + (k & 3) * 32);
+            const uint64_t bd = tc::smem_desc_sw128(kbase + (k >> 2) * (kKTileBytes / 2) + (k & 3) * 32);
+            tc::mma_bf16(tmem + acc * 256 + mb * 128, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&acc_full[acc]);
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0, kTimeoutNs);
+    }
+  } else {
+    // ---------------- epilogue: one row per thread ----------------
+    const int e = warp - 2;
+    const int mb = e / 4;                 // row block (accumulator half)
+    const int quarter = warp & 3;         // TMEM lane quarter this warp may read
+    const int r = mb * 128 + quarter * 32 + lane;  // row in chunk
+    const int row = rc * kRowChunk + r;
+    const bool row_ok = row < a.rows;
+    const int qpos = row_ok ? a.q_pos[(int64_t)b * a.w + row / a.G] : -1;
+    float m = -INFINITY, l = 0.f;
+    for (int i = 0; i < n_my; ++i) {
+      const int s = i % kStages1;
+      const int acc = i & 1;
+      if (!tc::mbar_wait(&acc_full[acc], (i >> 1) & 1, kTimeoutNs) ||
+          (a.causal && !tc::mbar_wait(&full[s], (i / kStages1) & 1, kTimeoutNs))) {
+        record_timeout(a, &s_abort);
+        break;
+      }
+      tc::tc_fence_after();
+      const int tile = t_begin + i;
+      const int key0 = tg.base + tile * kKeyTile;
+      const int32_t* pos = pos_s + s * kKeyTile;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 32, v);
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int key = key0 + c * 32 + j;
+          bool vis = row_ok && key >= tg.lo && key < tg.hi;
+          if (a.causal) vis = vis && pos[c * 32 + j] <= qpos;
+          v[j] = vis ? v[j] * a.scale : -INFINITY;
+          cm = fmaxf(cm, v[j]);
+        }
+        if (cm != -INFINITY) {
+          const float mn = fmaxf(m, cm);
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum += tc::ex2(v[j] - mn);
+          l = l * tc::ex2(m - mn) + sum;
+          m = mn;
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&acc_free[acc]);
+        tc::mbar_arrive(&pos_free[s]);
+      }
+    }
+    if (row_ok) {
+      float* p = a.part + (((int64_t)bg * a.RC * kRowChunk + row) * a.n_splits + split) * 2;
+      p[0] = m;
+      p[1] = l;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row info: lse2 per row (+inf when the row sees nothing) and query position.
+// grid (cdiv(RC*256, 256), B*Hkv)
+// ---------------------------------------------------------------------------
+__global__ void score_rowinfo_tc(TcArgs a) {
+  const int bg = blockIdx.y, b = bg / a.Hkv;
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  const int padded = a.RC * kRowChunk;
+  if (row >= padded) return;
+  float lse = INFINITY;
+  int qpos = -1;
+  if (row < a.rows) {
+    const float* p = a.part + ((int64_t)bg * padded + row) * a.n_splits * 2;
+    float M = -INFINITY;
+    for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, p[2 * s]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int s = 0; s < a.n_splits; ++s) L += p[2 * s + 1] * exp2f(p[2 * s] - M);
+    if (L > 0.f) lse = M + log2f(L);
+    qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
+  }
+  a.rowinfo[(int64_t)bg * padded + row] = make_float2(lse, __int_as_float(qpos));
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: column sums.  grid (cdiv(n_tiles_max, tiles_per_cta2), B*Hkv).
+// Key tiles are taken in pairs (2p, 2p+1); for each row chunk rc the pair is
+// multiplied by the same Q chunk, tile 2p into TMEM buffer 0 and tile 2p+1
+// into buffer 1.  Epilogue warps 2-5 own even tiles, warps 6-9 odd tiles, so
+// each thread sums one key over every row chunk in registers.  When the rows
+// fit one chunk the Q chunk stays resident and K tiles stream through four
+// stages; otherwise Q chunks stream through two stages (once per pair) and K
+// uses two stages.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int RC = a.RC;
+  const bool q_resident = RC == 1;
+  const int QS = q_resident ? 1 : 2;       // Q stages
+  const int KS = q_resident ? 4 : 2;       // K stages
+  uint8_t* q_s = smem;
+  uint8_t* k_s = q_s + QS * kQChunkBytes;
+  int32_t* pos_s = reinterpret_cast<int32_t*>(k_s + KS * kKTileBytes);   // [KS][128]
+  float2* info_s = reinterpret_cast<float2*>(pos_s + KS * kKeyTile);     // [QS][256]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(info_s + QS * kRowChunk);
+  uint64_t* kfull = bars;                 // [KS]
+  uint64_t* kempty = bars + 4;            // [KS] MMA done with the K tile
+  uint64_t* pfree = bars + 8;             // [KS] epilogue done with its positions
+  uint64_t* qfull = bars + 12;            // [QS]
+  uint64_t* qempty = bars + 14;           // [QS] MMA done with the Q chunk
+  uint64_t* ifree = bars + 16;            // [QS] epilogue done with the row info
+  uint64_t* acc_full = bars + 18;         // [2]
+  uint64_t* acc_free = bars + 20;         // [2]
+  uint64_t* done = bars + 22;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg % a.Hkv;
+  const TileGeom tg = TileGeom::make(a, b);
+  const bool ok = geom_ok(a, tg);
+  const int t_begin = blockIdx.x * a.tiles_per_cta2;
+  const int t_end = ok ? min(t_begin + a.tiles_per_cta2, tg.n_tiles) : 0;
+  const int n_my = max(t_end - t_begin, 0);
+  const int n_pairs = cdiv(n_my, 2);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    if (!ok) set_status(a.status, SE_ERR_BOUNDS);
+    for (int s = 0; s < KS; ++s) {
+      tc::mbar_init(&kfull[s], 1);
+      tc::mbar_init(&kempty[s], 1);
+      tc::mbar_init(&pfree[s], 4);
+    }
+    for (int i = 0; i < QS; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1);
+      tc::mbar_init(&ifree[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_free[i], 4);
+    }
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const float2* info_g = a.rowinfo + (int64_t)bg * RC * kRowChunk;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
+      int k_issued = 0, q_issued = 0;
+      bool stop = false;
+      for (int p = 0; p < n_pairs && !stop && !aborted(&s_abort); ++p) {
+        for (int rc = 0; rc < RC && !stop; ++rc) {
+          if (rc == 0) {
+            for (int t = 2 * p; t < min(2 * p + 2, n_my); ++t) {
+              const int s = t % KS;
+              const uint32_t par = ((t / KS) & 1) ^ 1;
+              if (t >= KS && (!tc::mbar_wait(&kempty[s], par, kTimeoutNs) ||
+                              !tc::mbar_wait(&pfree[s], par, kTimeoutNs))) {
+                record_timeout(a, &s_abort);
+                stop = true;
+                break;
+              }
+              load_k_tile(a, &kmap, tg, b, g, t_begin + t, k_s + s * kKTileBytes,
+                          a.causal ? pos_s + s * kKeyTile : nullptr, &kfull[s]);
+              k_issued = t + 1;
+            }
+            if (stop) break;
+          }
+          if (q_resident && q_issued > 0) continue;
+          const int qs = q_issued % QS;
+          const uint32_t par = ((q_issued / QS) & 1) ^ 1;
+          if (q_issued >= QS && (!tc::mbar_wait(&qempty[qs], par, kTimeoutNs) ||
+                                 !tc::mbar_wait(&ifree[qs], par, kTimeoutNs))) {
+            record_timeout(a, &s_abort);
+            stop = true;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&qfull[qs], kQChunkBytes + kRowChunk * 8);
+          const int qpc = kRowChunk / a.G;
+          tc::tma_load_4d(q_s + qs * kQChunkBytes, &qmap, &qfull[qs], 0, g * a.G, rc * qpc, b);
+          tc::tma_load_4d(q_s + qs * kQChunkBytes + kQChunkBytes / 2, &qmap, &qfull[qs], 64,
+                          g * a.G, rc * qpc, b);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+              ::"r"(tc::smem_u32(info_s + qs * kRowChunk)), "l"(info_g + rc * kRowChunk),
+              "r"(kRowChunk * 8), "r"(tc::smem_u32(&qfull[qs]))
+              : "memory");
+          q_issued++;
+        }
+      }
+      for (int t = max(0, k_issued - KS); t < k_issued; ++t)
+        tc::mbar_wait(&kfull[t % KS], (t / KS) & 1, kTimeoutNs);
+      for (int j = max(0, q_issued - QS); j < q_issued; ++j)
+        tc::mbar_wait(&qfull[j % QS], (j / QS) & 1, kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (tc::elect_one()) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, kRowChunk);
+      int q_used = 0;
+      int uses[2] = {0, 0};
+      bool stop = false;
+      for (int p = 0; p < n_pairs && !stop && !aborted(&s_abort); ++p) {
+        for (int rc = 0; rc < RC && !stop; ++rc) {
+          const int qs = q_used % QS;
+          if (!q_resident || q_used == 0) {
+            if (!(q_resident && q_used > 0) &&
+                !tc::mbar_wait(&qfull[qs], (q_used / QS) & 1, kTimeoutNs)) {
+              record_timeout(a, &s_abort);
+              stop = true;
+              break;
+            }
+          }
+          const int t1 = min(2 * p + 2, n_my);
+          for (int t = 2 * p; t < t1; ++t) {
+            const int s = t % KS;
+            const int buf = t & 1;
+            bool w_ok = true;
+            if (rc == 0) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
+            if (w_ok && uses[buf] > 0)
+              w_ok = tc::mbar_wait(&acc_free[buf], (uses[buf] - 1) & 1, kTimeoutNs);
+            if (!w_ok) {
+              record_timeout(a, &s_abort);
+              stop = true;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t kbase = tc::smem_u32(k_s + s * kKTileBytes);
+            const uint32_t qbase = tc::smem_u32(q_s + qs * kQChunkBytes);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = tc::smem_desc_sw128(kbase + (k >> 2) * (kKTileBytes / 2) + (k & 3) * 32);
+              const uint64_t bd = tc::smem_desc_sw128(qbase + (k >> 2) * (kQChunkBytes / 2) + (k & 3) * 32);
+              tc::mma_bf16(tmem + buf * 256, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            if (rc == RC - 1) tc::mma_commit(&kempty[s]);
+            tc::mma_commit(&acc_full[buf]);
+            uses[buf]++;
+          }
+          if (stop) break;
+          if (!q_resident) tc::mma_commit(&qempty[qs]);
+          q_used++;
+        }
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0, kTimeoutNs);
+    }
+  } else {
+    // ---------------- epilogue: one key per thread, tiles of one parity ----------------
+    const int set = (warp - 2) / 4;       // 0: even tiles (buffer 0), 1: odd tiles
+    const int quarter = warp & 3;
+    const int kl = quarter * 32 + lane;   // key within its tile
+    int use = 0;
+    bool stop = false;
+    for (int p = 0; p < n_pairs && !stop; ++p) {
+      const int t = 2 * p + set;
+      const int s = t % KS;
+      if (t >= n_my) {
+        // no tile of this parity in the last pair: still release each streamed
+        // Q chunk after it has landed, so the pair's row-info stage frees up
+        if (!q_resident) {
+          for (int rc = 0; rc < RC; ++rc) {
+            const int qn = p * RC + rc;
+            if (!tc::mbar_wait(&qfull[qn % QS], (qn / QS) & 1, kTimeoutNs)) {
+              record_timeout(a, &s_abort);
+              stop = true;
+              break;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ifree[qn % QS]);
+          }
+        }
+        break;
+      }
+      float colsum = 0.f;
+      int kpos = 0;
+      for (int rc = 0; rc < RC; ++rc) {
+        const int qn = p * RC + rc;          // Q chunk load number (0 when resident)
+        const int qs = q_resident ? 0 : qn % QS;
+        bool w_ok = tc::mbar_wait(&acc_full[set], use & 1, kTimeoutNs);
+        if (w_ok && rc == 0 && a.causal) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
+        if (w_ok) w_ok = tc::mbar_wait(&qfull[qs], q_resident ? 0 : ((qn / QS) & 1), kTimeoutNs);
+        if (!w_ok) {
+          record_timeout(a, &s_abort);
+          stop = true;
+          break;
+        }
+        tc::tc_fence_after();
+        if (rc == 0 && a.causal) kpos = pos_s[s * kKeyTile + kl];
+        const float2* info = info_s + qs * kRowChunk;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float v[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float2 ri = info[c * 32 + j];
+            float pv = tc::ex2(fmaf(v[j], a.scale, -ri.x));
+            if (a.causal && kpos > __float_as_int(ri.y)) pv = 0.f;
+            colsum += pv;
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&acc_free[set]);
+          if (!q_resident) tc::mbar_arrive(&ifree[qs]);
+          if (rc == RC - 1) tc::mbar_arrive(&pfree[s]);
+        }
+        use++;
+      }
+      if (stop) break;
+      const int key = tg.base + (t_begin + t) * kKeyTile + kl;
+      if (key >= a.out_lo[b] && key < a.out_hi[b] && key >= tg.lo && key < tg.hi &&
+          key < a.scores_stride) {
+        float* out = a.scores + (int64_t)bg * a.scores_stride + key;
+        *out = a.accumulate ? *out + colsum : colsum;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+constexpr size_t kSmem1 = 1024 + kQChunkBytes + kStages1 * kKTileBytes + kStages1 * kKeyTile * 4 + 256;
+constexpr size_t kSmem2 = 1024 + 2 * kQChunkBytes + 2 * kKTileBytes + 4 * kKeyTile * 4 +
+                          2 * kRowChunk * 8 + 256;
+constexpr size_t kSmem2Resident = 1024 + kQChunkBytes + 4 * kKTileBytes + 4 * kKeyTile * 4 +
+                                  kRowChunk * 8 + 256;
+
+struct TcPlan {
+  int RC, n_splits, tiles_per_split, tiles_per_cta2, n_tiles_max;
+};
+
+TcPlan plan(const se_paged_kv* kv, int w, int n_max) {
+  TcPlan p;
+  const int G = kv->Hq / kv->Hkv;
+  p.RC = cdiv(w * G, kRowChunk);
+  // one extra tile when attn_lo is not page aligned
+  p.n_tiles_max = cdiv(n_max + kv->page_size, kKeyTile);
+  p.tiles_per_split = 16;
+  p.n_splits = cdiv(p.n_tiles_max, p.tiles_per_split);
+  p.tiles_per_cta2 = p.RC == 1 ? 16 : 2;
+  return p;
+}
+
+}  // namespace
+
+bool score_tc_supported(const se_paged_kv* kv) {
+  const int G = kv->Hq / kv->Hkv;
+  return kv->dtype == SE_BF16 && kv->D == kD && (G == 1 || G == 2 || G == 4 || G == 8) &&
+         (kv->page_size == 16 || kv->page_size == 32 || kv->page_size == 64) &&
+         (int64_t)kv->num_pages * kv->Hkv * kv->page_size < (int64_t)1 << 31;
+}
+
+size_t score_tc_ws(const se_paged_kv* kv, int w, int n_max) {
+  const TcPlan p = plan(kv, w, n_max);
+  WsCarver c(nullptr);
+  c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * p.n_splits * 2);
+  c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
+  return c.bytes();
+}
+
+se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const int32_t* q_pos,
+                          const int32_t* attn_lo, const int32_t* attn_hi, const int32_t* out_lo,
+                          const int32_t* out_hi, int causal, int accumulate, int n_max,
+                          float* scores, int64_t scores_stride, void* ws, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return SE_ERR_CUDA;
+  const int G = kv->Hq / kv->Hkv;
+  const TcPlan p = plan(kv, w, n_max);
+  CUtensorMap kmap, qmap;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)kv->num_pages * kv->Hkv * kv->page_size};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kv->page_size};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv->k_pool, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SE_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kv->Hq, (cuuint64_t)w, (cuuint64_t)kv->B};
+    cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kv->Hq * kD * 2,
+                             (cuuint64_t)w * kv->Hq * kD * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(kRowChunk / G), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q_win), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SE_ERR_CUDA;
+  }
+  TcArgs a{};
+  a.B = kv->B; a.Hq = kv->Hq; a.Hkv = kv->Hkv; a.G = G; a.w = w; a.P = kv->page_size;
+  a.rows = w * G; a.RC = p.RC;
+  a.max_pages_per_seq = kv->max_pages_per_seq; a.num_pages = kv->num_pages;
+  a.block_table = kv->block_table; a.slot_map = kv->slot_map;
+  a.smax = (int64_t)kv->max_pages_per_seq * kv->page_size;
+  a.q_pos = q_pos; a.attn_lo = attn_lo; a.attn_hi = attn_hi; a.out_lo = out_lo; a.out_hi = out_hi;
+  a.causal = causal; a.accumulate = accumulate; a.n_max = n_max;
+  a.scores = scores; a.scores_stride = scores_stride;
+  WsCarver c(ws);
+  a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * p.n_splits * 2);
+  a.rowinfo = c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
+  a.n_splits = p.n_splits; a.tiles_per_split = p.tiles_per_split;
+  a.tiles_per_cta2 = p.tiles_per_cta2;
+  a.status = kv->status;
+  a.scale = kLog2e / sqrtf((float)kD);
+  static bool attrs = false;
+  if (!attrs) {
+    if (cudaFuncSetAttribute(score_rowstats_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem1) != cudaSuccess ||
+        cudaFuncSetAttribute(score_colsum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem2) != cudaSuccess)
+      return SE_ERR_CUDA;
+    attrs = true;
+  }
+  const int groups = kv->B * kv->Hkv;
+  score_rowstats_tc<<<dim3(p.n_splits, p.RC, groups), kThreads, kSmem1, st>>>(kmap, qmap, a);
+  score_rowinfo_tc<<<dim3(cdiv(p.RC * kRowChunk, 256), groups), 256, 0, st>>>(a);
+  const size_t smem2 = p.RC == 1 ? kSmem2Resident : kSmem2;
+  score_colsum_tc<<<dim3(cdiv(p.n_tiles_max, p.tiles_per_cta2), groups), kThreads, smem2, st>>>(
+      kmap, qmap, a);
+  return SE_OK;
+}
+
+}  // namespace se

@@ -1,0 +1,120 @@
+// Shared device/host helpers of the sm_103a kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "se.h"
+
+#define SE_DEV __device__ __forceinline__
+#define SE_HD __host__ __device__ __forceinline__
+
+namespace se {
+
+SE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
+SE_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// First-writer-wins device error word.
+SE_DEV void set_status(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// bf16 pair (packed in a uint32) -> two floats, exact.
+SE_DEV float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+SE_DEV float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// 8 consecutive elements (16 bytes for bf16) -> floats.
+SE_DEV void unpack8_bf16(const uint4& u, float* f) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+SE_DEV uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+SE_DEV uint4 ldg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+SE_DEV void stg_v4(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Order-preserving float -> uint32 key (larger float -> larger key).
+SE_DEV uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024,
+// multiple of 32).  `tmp` must hold 33 ints of shared memory.  Returns the
+// exclusive prefix; *total receives the block sum.  Contains __syncthreads.
+SE_DEV int block_exclusive_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarps) tmp[lane] = w;  // inclusive warp totals
+    if (lane == 31) tmp[32] = w;
+  }
+  __syncthreads();
+  int base = warp > 0 ? tmp[warp - 1] : 0;
+  int t = tmp[32];
+  __syncthreads();
+  if (total) *total = t;
+  return base + x - v;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bump allocator over a caller-provided workspace (host side).
+struct WsCarver {
+  char* base;
+  size_t off = 0;
+  explicit WsCarver(void* p) : base(static_cast<char*>(p)) {}
+  template <typename T>
+  T* take(size_t n) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+  size_t bytes() const { return align_up(off, 256); }
+};
+
+SE_HD size_t elem_size(int32_t dtype) { return dtype == SE_BF16 ? 2 : 4; }
+
+}  // namespace se
+
+// Host-side launch helpers shared by the translation units.
+se_status se_check_kv(const se_paged_kv* kv);
+se_status se_last_launch_status();

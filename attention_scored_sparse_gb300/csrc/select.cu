@@ -1,0 +1,478 @@
+// Per-KV-head selection of the entries to retain.
+//
+// TOPK        SparseEngine "How it works" (SnapKV keeps the top entries per
+//             KV head after the last prompt chunk; H2O heavy hitters; Quest
+//             top pages): avg-pool over the candidate range, rank by (score
+//             desc, slot asc), keep k plus a forced range.  One CTA per
+//             (sequence, head): scores staged in shared memory, pooled into
+//             order-preserving integer keys held in registers, an 8-bit
+//             4-pass block radix select finds the k-th key, and two block
+//             scans emit the kept slots in ascending order.
+// KARA_CHUNK  KARA Method 1-2 (top-K candidates, Token2Chunk): one warp per
+//             (sequence, head); candidates, chunk scores, greedy fill and
+//             top-up are warp argmax rounds over registers.
+// EVICT_ONE   SparseEngine "What it is" (H2O persistent scores + physical
+//             eviction): one warp per (sequence, head) argmin.
+#include "se_common.cuh"
+
+namespace se {
+
+struct SelectArgs {
+  int B, Hkv;
+  const float* scores;
+  int64_t stride;
+  const int32_t* cand_lo;
+  const int32_t* cand_hi;
+  const int32_t* force_lo;
+  const int32_t* force_hi;
+  int32_t* keep;
+  int32_t keep_stride;
+  int32_t* n_keep;
+  int32_t* status;
+};
+
+template <int ITEMS>
+SE_DEV int padded(int e) { return e + e / ITEMS; }
+
+// grid: (Hkv, B), 1024 threads, dynamic smem (1024*(ITEMS+1)+64) floats.
+template <int ITEMS>
+__global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, int k) {
+  extern __shared__ float s_sc[];
+  __shared__ int tmp[33];
+  __shared__ int hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  __shared__ int s_before_force;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int lo = a.cand_lo[b], hi = a.cand_hi[b];
+  const int flo = a.force_lo ? a.force_lo[b] : 0;
+  const int fhi = a.force_hi ? a.force_hi[b] : 0;
+  const int n = hi - lo;
+  const int nf = max(fhi - flo, 0);
+  if (n < 0 || n > 1024 * ITEMS) {
+    if (tid == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  const float* row = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
+  for (int e = tid; e < n; e += 1024) s_sc[padded<ITEMS>(e)] = row[lo + e];
+  if (tid == 0) s_before_force = 0;
+  __syncthreads();
+
+  uint32_t key[ITEMS];
+  const int r = pool / 2;
+  const float inv_div = (float)pool;
+  int n_forced_in = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int e = tid * ITEMS + i;
+    key[i] = 0u;
+    if (e < n) {
+      const int slot = lo + e;
+      if (slot >= flo && slot < fhi) {
+        n_forced_in++;
+      } else {
+        float v;
+        if (pool > 1) {
+          float acc = 0.f;
+          for (int d = -r; d <= r; ++d) {
+            const int x = e + d;
+            if (x >= 0 && x < n) acc += s_sc[padded<ITEMS>(x)];
+          }
+          v = acc / inv_div;
+        } else {
+          v = s_sc[padded<ITEMS>(e)];
+        }
+        key[i] = float_key(v);
+      }
+    }
+  }
+  int forced_in_total;
+  block_exclusive_scan(n_forced_in, tmp, &forced_in_total);
+  const int ncand = n - forced_in_total;
+  const int kk = min(max(k, 0), ncand);
+
+  // 4 rounds of 8-bit radix select for the kk-th largest key.
+  uint32_t prefix = 0, pmask = 0;
+  int remaining = kk;
+  if (kk > 0) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += 1024) hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i)
+        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+      __syncthreads();
+      if (tid < 32) {
+        // lane l owns bins [8l, 8l+8); suffix sums from the top bin down
+        int cnt[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { cnt[j] = hist[tid * 8 + j]; tot += cnt[j]; }
+        int suf = tot;  // inclusive suffix over lanes >= tid
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, suf, o);
+          if (tid + o < 32) suf += y;
+        }
+        const int above = suf - tot;  // elements in higher lanes' bins
+        const bool mine = above < remaining && suf >= remaining;
+        if (mine) {
+          int acc = above;
+          for (int j = 7; j >= 0; --j) {
+            if (acc + cnt[j] >= remaining) {
+              s_prefix = prefix | ((uint32_t)(tid * 8 + j) << shift);
+              s_remaining = remaining - acc;
+              break;
+            }
+            acc += cnt[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      remaining = s_remaining;
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+  }
+  const uint32_t T = kk > 0 ? prefix : 0xffffffffu;
+  const int need_eq = kk > 0 ? remaining : 0;
+
+  int c_eq = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
+  int dummy;
+  int eq_rank = block_exclusive_scan(c_eq, tmp, &dummy);
+  bool sel[ITEMS];
+  int c_sel = 0, c_sel_before_force = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    sel[i] = false;
+    if (key[i] != 0u) {
+      if (key[i] > T) {
+        sel[i] = true;
+      } else if (key[i] == T) {
+        sel[i] = eq_rank < need_eq;
+        eq_rank++;
+      }
+    }
+    c_sel += sel[i];
+    c_sel_before_force += (sel[i] && lo + tid * ITEMS + i < flo) ? 1 : 0;
+  }
+  int total_sel;
+  int pos = block_exclusive_scan(c_sel, tmp, &total_sel);
+  if (total_sel + nf > a.keep_stride) {  // output row too short: report, write nothing
+    if (tid == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  if (c_sel_before_force) atomicAdd(&s_before_force, c_sel_before_force);
+  __syncthreads();
+  const int before_force = s_before_force;
+  int32_t* out = a.keep + ((int64_t)b * a.Hkv + h) * a.keep_stride;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    if (sel[i]) {
+      const int slot = lo + tid * ITEMS + i;
+      out[pos + (slot >= fhi && nf > 0 ? nf : 0)] = slot;
+      pos++;
+    }
+  }
+  for (int f = tid; f < nf; f += 1024) out[before_force + f] = flo + f;
+  for (int p = total_sel + nf + tid; p < a.keep_stride; p += 1024) out[p] = -1;
+  if (h == 0 && tid == 0 && a.n_keep) a.n_keep[b] = total_sel + nf;
+}
+
+// --------------------------------------------------------------------------
+// Kara Token2Chunk: one warp per (b, h); compressible window <= 32*IT slots.
+// --------------------------------------------------------------------------
+
+struct ArgBest {
+  float s;
+  int idx;  // element index (tie: smaller wins)
+};
+
+SE_DEV ArgBest warp_argmax(ArgBest v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgBest w;
+    w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
+    w.idx = __shfl_xor_sync(0xffffffffu, v.idx, o);
+    if (w.s > v.s || (w.s == v.s && w.idx < v.idx)) v = w;
+  }
+  return v;
+}
+
+// j-th set bit (0-based) of a little-endian multi-word mask, -1 if none.
+template <int IT>
+SE_DEV int select_bit(const uint32_t* words, int j) {
+#pragma unroll
+  for (int w = 0; w < IT; ++w) {
+    const int c = __popc(words[w]);
+    if (j < c) {
+      uint32_t x = words[w];
+      for (int t = 0; t < j; ++t) x &= x - 1;
+      return w * 32 + (__ffs(x) - 1);
+    }
+    j -= c;
+  }
+  return -1;
+}
+
+template <int IT>
+__global__ void __launch_bounds__(256) kara_chunk_kernel(SelectArgs a, int n_cand, int budget,
+                                                         float coef) {
+  __shared__ float s_sc[8][32 * IT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int inst = blockIdx.x * 8 + warp;
+  if (inst >= a.B * a.Hkv) return;
+  const int b = inst / a.Hkv, h = inst % a.Hkv;
+  const int lo = a.cand_lo[b], hi = a.cand_hi[b];
+  const int flo = a.force_lo ? a.force_lo[b] : 0;
+  const int fhi = a.force_hi ? a.force_hi[b] : 0;
+  const int nf = max(fhi - flo, 0);
+  const int n = hi - lo;
+  if (n < 0 || n > 32 * IT || n_cand > 32) {
+    if (lane == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  const float* row = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
+  float* sc = s_sc[warp];
+  float s[IT];
+  bool cand_ok[IT], is_c[IT], ret[IT];
+#pragma unroll
+  for (int i = 0; i < IT; ++i) {
+    const int e = i * 32 + lane;
+    const int slot = lo + e;
+    const bool inr = e < n && !(slot >= flo && slot < fhi);
+    s[i] = e < n ? row[lo + e] : 0.f;
+    if (e < 32 * IT) sc[e] = s[i];
+    cand_ok[i] = inr;
+    is_c[i] = false;
+    ret[i] = false;
+  }
+  __syncwarp();
+  int n_avail = 0;
+#pragma unroll
+  for (int i = 0; i < IT; ++i) n_avail += __popc(__ballot_sync(0xffffffffu, cand_ok[i]));
+  const int kc = min(n_cand, n_avail);
+  const int bud = min(budget, n_avail);
+  // 1) top-kc discrete candidates by (score desc, index asc)
+  for (int r = 0; r < kc; ++r) {
+    ArgBest v{-INFINITY, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+      const int e = i * 32 + lane;
+      if (cand_ok[i] && !is_c[i] && (s[i] > v.s || (s[i] == v.s && e < v.idx))) v = ArgBest{s[i], e};
+    }
+    v = warp_argmax(v);
+    if ((v.idx & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < IT; ++i)
+        if (i == (v.idx >> 5)) is_c[i] = true;
+    }
+  }
+  uint32_t words[IT];
+#pragma unroll
+  for (int i = 0; i < IT; ++i) {
+    words[i] = __ballot_sync(0xffffffffu, is_c[i]);
+    ret[i] = is_c[i];
+  }
+  int count = kc;
+  // 2) chunk between consecutive candidates j, j+1 (lane j)
+  const int n_chunks = max(kc - 1, 0);
+  float csc = -INFINITY;
+  int ca = 0, cb = 0;
+  if (lane < n_chunks) {
+    ca = select_bit<IT>(words, lane);
+    cb = select_bit<IT>(words, lane + 1);
+    csc = (sc[ca] + sc[cb]) * 0.5f - coef * (float)(cb - ca);
+  }
+  bool visited = lane >= n_chunks;
+  for (int r = 0; r < n_chunks; ++r) {
+    ArgBest v{-INFINITY, 0x7fffffff};
+    if (!visited) v = ArgBest{csc, ca};
+    v = warp_argmax(v);
+    // the winner is the chunk starting at v.idx
+    const bool win = !visited && ca == v.idx;
+    const unsigned wm = __ballot_sync(0xffffffffu, win);
+    const int wl = __ffs(wm) - 1;
+    const int a0 = __shfl_sync(0xffffffffu, ca, wl);
+    const int b0 = __shfl_sync(0xffffffffu, cb, wl);
+    if (lane == wl) visited = true;
+    const int interior = b0 - a0 - 1;
+    if (interior > 0 && count + interior <= bud) {
+      count += interior;
+#pragma unroll
+      for (int i = 0; i < IT; ++i) {
+        const int e = i * 32 + lane;
+        if (e > a0 && e < b0) ret[i] = true;
+      }
+    }
+  }
+  // 3) top up with the best remaining single tokens
+  while (count < bud) {
+    ArgBest v{-INFINITY, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+      const int e = i * 32 + lane;
+      if (cand_ok[i] && !ret[i] && (s[i] > v.s || (s[i] == v.s && e < v.idx))) v = ArgBest{s[i], e};
+    }
+    v = warp_argmax(v);
+    if ((v.idx & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < IT; ++i)
+        if (i == (v.idx >> 5)) ret[i] = true;
+    }
+    count++;
+  }
+  // 4) emit retained slots ascending, forced range in slot order
+  if (count + nf > a.keep_stride) {
+    if (lane == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  int32_t* out = a.keep + ((int64_t)b * a.Hkv + h) * a.keep_stride;
+  int before_force = 0;
+#pragma unroll
+  for (int i = 0; i < IT; ++i) {
+    const uint32_t m = __ballot_sync(0xffffffffu, ret[i] && lo + i * 32 + lane < flo);
+    before_force += __popc(m);
+  }
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < IT; ++i) {
+    const uint32_t m = __ballot_sync(0xffffffffu, ret[i]);
+    if (ret[i]) {
+      const int slot = lo + i * 32 + lane;
+      const int p = base + __popc(m & ((1u << lane) - 1u));
+      out[p + (slot >= fhi && nf > 0 ? nf : 0)] = slot;
+    }
+    base += __popc(m);
+  }
+  for (int f = lane; f < nf; f += 32) out[before_force + f] = flo + f;
+  if (h == 0 && lane == 0 && a.n_keep) a.n_keep[b] = count + nf;
+}
+
+// --------------------------------------------------------------------------
+// H2O evict-one: one warp per (b, h).
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) evict_one_kernel(SelectArgs a, const int32_t* ctx_len,
+                                                        const int32_t* logical_len,
+                                                        const int32_t* slot_map, int64_t smax,
+                                                        int budget, int recent) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int inst = blockIdx.x * 8 + warp;
+  if (inst >= a.B * a.Hkv) return;
+  const int b = inst / a.Hkv, h = inst % a.Hkv;
+  const int ctx = ctx_len[b];
+  int32_t* out = a.keep + (int64_t)b * a.Hkv + h;
+  if (ctx <= budget) {
+    if (lane == 0) *out = -1;
+    return;
+  }
+  const int recent_from = logical_len[b] - recent;
+  const float* acc = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
+  const int32_t* sm = slot_map + ((int64_t)b * a.Hkv + h) * smax;
+  float best = INFINITY;
+  int bpos = -1, bslot = -1;
+  for (int s = lane; s < ctx; s += 32) {
+    const int pos = sm[s];
+    if (pos < recent_from) {
+      const float v = acc[s];
+      if (bslot < 0 || v < best || (v == best && pos > bpos)) { best = v; bpos = pos; bslot = s; }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v = __shfl_xor_sync(0xffffffffu, best, o);
+    const int p = __shfl_xor_sync(0xffffffffu, bpos, o);
+    const int s = __shfl_xor_sync(0xffffffffu, bslot, o);
+    if (s >= 0 && (bslot < 0 || v < best || (v == best && p > bpos))) { best = v; bpos = p; bslot = s; }
+  }
+  if (lane == 0) *out = bslot;
+}
+
+template <int ITEMS>
+static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_t st) {
+  const size_t smem = (size_t)(1024 * (ITEMS + 1) + 64) * sizeof(float);
+  static bool attr_set = false;  // per device is enough here: set before first launch
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_kernel<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return SE_ERR_CUDA;
+    attr_set = true;
+  }
+  topk_kernel<ITEMS><<<dim3(a.Hkv, a.B), 1024, smem, st>>>(a, pool, k);
+  return SE_OK;
+}
+
+se_status launch_topk(const SelectArgs& a, int pool, int k, int n_max, cudaStream_t st) {
+  const int items = cdiv(max(n_max, 1), 1024);
+  if (items <= 1) return launch_topk_t<1>(a, pool, k, st);
+  if (items <= 2) return launch_topk_t<2>(a, pool, k, st);
+  if (items <= 4) return launch_topk_t<4>(a, pool, k, st);
+  if (items <= 8) return launch_topk_t<8>(a, pool, k, st);
+  if (items <= 16) return launch_topk_t<16>(a, pool, k, st);
+  if (items <= 32) return launch_topk_t<32>(a, pool, k, st);
+  if (items <= 48) return launch_topk_t<48>(a, pool, k, st);
+  return SE_ERR_UNSUPPORTED;
+}
+
+se_status launch_topk_select_pages(int B, int Hkv, const float* U, int64_t stride,
+                                   const int32_t* cand_lo, const int32_t* cand_hi,
+                                   const int32_t* force_lo, const int32_t* force_hi, int32_t* out,
+                                   int32_t out_stride, int32_t* n_sel, int32_t* status, int top,
+                                   int n_max, cudaStream_t st) {
+  SelectArgs a{B, Hkv, U, stride, cand_lo, cand_hi, force_lo, force_hi, out, out_stride, n_sel,
+               status};
+  return launch_topk(a, 1, top, n_max, st);
+}
+
+}  // namespace se
+
+using namespace se;
+
+extern "C" se_status se_topk_select(const se_paged_kv* kv, const float* scores,
+                                    int64_t scores_stride, const se_select_params* params,
+                                    const int32_t* cand_lo, const int32_t* cand_hi,
+                                    const int32_t* force_lo, const int32_t* force_hi,
+                                    int32_t* keep_idx, int32_t keep_stride, int32_t* n_keep,
+                                    void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (params == nullptr || scores == nullptr || keep_idx == nullptr) return SE_ERR_INVALID_ARG;
+  if ((force_lo == nullptr) != (force_hi == nullptr)) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SelectArgs a{kv->B, kv->Hkv, scores, scores_stride, cand_lo, cand_hi, force_lo, force_hi,
+               keep_idx, keep_stride, n_keep, kv->status};
+  const se_select_params& p = *params;
+  if (p.mode == SE_SELECT_TOPK) {
+    if (cand_lo == nullptr || cand_hi == nullptr || p.pool_kernel < 1 || p.pool_kernel % 2 == 0 ||
+        p.k < 0 || p.n_max < 0)
+      return SE_ERR_INVALID_ARG;
+    s = launch_topk(a, p.pool_kernel, p.k, p.n_max, st);
+    if (s != SE_OK) return s;
+    return se_last_launch_status();
+  }
+  if (p.mode == SE_SELECT_KARA_CHUNK) {
+    if (cand_lo == nullptr || cand_hi == nullptr || p.k < 1 || p.k > 32 || p.chunk_budget < 0 ||
+        p.n_max < 0)
+      return SE_ERR_INVALID_ARG;
+    const int blocks = cdiv(kv->B * kv->Hkv, 8);
+    if (p.n_max <= 256) {
+      kara_chunk_kernel<8><<<blocks, 256, 0, st>>>(a, p.k, p.chunk_budget, p.chunk_coef);
+    } else if (p.n_max <= 512) {
+      kara_chunk_kernel<16><<<blocks, 256, 0, st>>>(a, p.k, p.chunk_budget, p.chunk_coef);
+    } else {
+      return SE_ERR_UNSUPPORTED;
+    }
+    return se_last_launch_status();
+  }
+  if (p.mode == SE_SELECT_EVICT_ONE) {
+    if (p.budget < 0 || p.recent < 0) return SE_ERR_INVALID_ARG;
+    const int blocks = cdiv(kv->B * kv->Hkv, 8);
+    evict_one_kernel<<<blocks, 256, 0, st>>>(a, kv->ctx_len, kv->logical_len, kv->slot_map,
+                                             (int64_t)kv->max_pages_per_seq * kv->page_size,
+                                             p.budget, p.recent);
+    return se_last_launch_status();
+  }
+  return SE_ERR_INVALID_ARG;
+}

@@ -1,0 +1,226 @@
+"""Workload pipelines: the C-ABI calls in the order the methods use them.
+
+Each class preallocates every buffer it needs (scores, kept indices,
+workspaces) at construction, so a step launches kernels only and can be
+captured in a CUDA graph.  Call order follows the pages: SparseEngine "How it
+works" (SnapKV / H2O selection at the end of prefill via finish_step, Quest
+selection per decode step via build_decode_selection, physical eviction,
+AttentionView) and KARA Method 3 (periodic compression of the trailing
+window); SparseEngine "How it differs" (prefix-span pruning).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (SE_COMPACT_FRESH_PAGES, SE_COMPACT_MOVE_LAST, SE_SELECT_EVICT_ONE,
+               SE_SELECT_KARA_CHUNK, SE_SELECT_TOPK, SE_VIEW_DENSE, SE_VIEW_PAGES, kv_desc,
+               se_append_kv, se_compact_evict, se_prune_span, se_quest_build_meta,
+               se_quest_page_select, se_score_window, se_sparse_decode_attn, se_topk_select,
+               workspace_sizes)
+
+
+def _i32(vals, device):
+    return torch.as_tensor(vals, dtype=torch.int32).to(device)
+
+
+class _Base:
+    def __init__(self, cache, Hq):
+        self.cache = cache
+        self.Hq = Hq
+        self.kv = kv_desc(cache, Hq)
+        self.device = cache.k_pool.device
+        self.B = cache.block_table.shape[0]
+        self.Hkv = cache.k_pool.shape[1]
+        self.P = cache.page_size
+        self.max_slots = cache.slot_map.shape[-1]
+
+    def _ws(self, nbytes):
+        return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+
+
+class SnapKV(_Base):
+    """SnapKV after the last prompt chunk: causal window scores, avg-pool +
+    top-k per KV head with the window forced, compaction into fresh pages,
+    then decode attention over the retained entries."""
+
+    def __init__(self, cache, Hq, *, ctx, window, budget, pool_kernel):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.ctx, self.window, self.budget, self.pool = ctx, window, budget, pool_kernel
+        scored = ctx - window
+        self.zero = _i32([0] * B, dev)
+        self.ctx_t = _i32([ctx] * B, dev)
+        self.scored_t = _i32([scored] * B, dev)
+        self.scores = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
+        self.keep = torch.empty((B, self.Hkv, budget), dtype=torch.int32, device=dev)
+        self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+        sz = workspace_sizes(self.kv, w=window, n_max=ctx, max_keep=budget, max_entries=budget)
+        self.ws_score = self._ws(sz["score_window"])
+        self.ws_compact = self._ws(sz["compact_evict"])
+        self.ws_decode = self._ws(sz["sparse_decode_attn"])
+
+    def score(self, q_win, q_pos, stream=None):
+        se_score_window(self.kv, q_win, q_pos, self.zero, self.ctx_t, self.zero, self.scored_t,
+                        causal=True, accumulate=False, n_max=self.ctx, scores=self.scores,
+                        workspace=self.ws_score, stream=stream)
+
+    def select(self, stream=None):
+        se_topk_select(self.kv, self.scores, mode=SE_SELECT_TOPK, cand_lo=self.zero,
+                       cand_hi=self.scored_t, force_lo=self.scored_t, force_hi=self.ctx_t,
+                       keep_idx=self.keep, n_keep=self.n_keep, pool_kernel=self.pool,
+                       k=self.budget - self.window, n_max=self.ctx - self.window, stream=stream)
+
+    def compact(self, stream=None):
+        se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
+                         first_slot=self.zero, max_keep=self.budget, workspace=self.ws_compact,
+                         stream=stream)
+
+    def decode(self, q, o, stream=None):
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.budget,
+                              workspace=self.ws_decode, stream=stream)
+
+    def step(self, q_win, q_pos, q_dec, o, stream=None):
+        self.score(q_win, q_pos, stream)
+        self.select(stream)
+        self.compact(stream)
+        self.decode(q_dec, o, stream)
+
+
+class QuestDecode(_Base):
+    """Quest: per-page key min/max once, then per decode step the page bound,
+    top pages + current page, and attention over those pages."""
+
+    def __init__(self, cache, Hq, *, ctx, top_pages):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.top = top_pages
+        self.nblocks = (ctx + self.P - 1) // self.P
+        shape = (cache.k_pool.shape[0], self.Hkv, cache.k_pool.shape[3])
+        self.kmin = torch.empty(shape, dtype=cache.k_pool.dtype, device=dev)
+        self.kmax = torch.empty(shape, dtype=cache.k_pool.dtype, device=dev)
+        self.page_idx = torch.empty((B, self.Hkv, top_pages + 1), dtype=torch.int32, device=dev)
+        self.n_sel = torch.empty(B, dtype=torch.int32, device=dev)
+        sz = workspace_sizes(self.kv, max_blocks=self.nblocks,
+                             max_entries=(top_pages + 1) * self.P)
+        self.ws_sel = self._ws(sz["quest_page_select"])
+        self.ws_decode = self._ws(sz["sparse_decode_attn"])
+
+    def build_meta(self, stream=None):
+        se_quest_build_meta(self.kv, self.kmin, self.kmax, stream=stream)
+
+    def select(self, q, stream=None):
+        se_quest_page_select(self.kv, self.kmin, self.kmax, q, top_pages=self.top,
+                             max_blocks=self.nblocks, page_idx=self.page_idx, n_sel=self.n_sel,
+                             workspace=self.ws_sel, stream=stream)
+
+    def decode(self, q, o, stream=None):
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_PAGES, o=o, sel=self.page_idx,
+                              n_sel=self.top + 1, max_entries=(self.top + 1) * self.P,
+                              workspace=self.ws_decode, stream=stream)
+
+    def step(self, q, o, stream=None):
+        self.select(q, stream)
+        self.decode(q, o, stream)
+
+
+class H2O(_Base):
+    """H2O: causal scores of the whole prompt seed the running scores and pick
+    the initial heavy hitters (plus the recent tokens); each decode step
+    appends, attends over every resident entry while adding its weights to
+    the running scores, and evicts the lowest-scoring non-recent entry."""
+
+    def __init__(self, cache, Hq, *, prompt, heavy, recent):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.prompt, self.heavy, self.recent = prompt, heavy, recent
+        self.budget = heavy + recent
+        self.zero = _i32([0] * B, dev)
+        self.ctx_t = _i32([prompt] * B, dev)
+        self.cand_t = _i32([prompt - recent] * B, dev)
+        self.acc = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
+        self.keep = torch.empty((B, self.Hkv, self.budget), dtype=torch.int32, device=dev)
+        self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+        self.victim = torch.empty((B, self.Hkv), dtype=torch.int32, device=dev)
+        sz = workspace_sizes(self.kv, w=prompt, n_max=prompt, max_keep=self.budget,
+                             max_entries=self.budget + 1)
+        self.ws_score = self._ws(sz["score_window"])
+        self.ws_compact = self._ws(sz["compact_evict"])
+        self.ws_decode = self._ws(sz["sparse_decode_attn"])
+        self.ws_append = self._ws(sz["append_kv"])
+
+    def prefill(self, q_prompt, q_pos, stream=None):
+        se_score_window(self.kv, q_prompt, q_pos, self.zero, self.ctx_t, self.zero, self.ctx_t,
+                        causal=True, accumulate=False, n_max=self.prompt, scores=self.acc,
+                        workspace=self.ws_score, stream=stream)
+        se_topk_select(self.kv, self.acc, mode=SE_SELECT_TOPK, cand_lo=self.zero,
+                       cand_hi=self.cand_t, force_lo=self.cand_t, force_hi=self.ctx_t,
+                       keep_idx=self.keep, n_keep=self.n_keep, pool_kernel=1, k=self.heavy,
+                       n_max=self.prompt - self.recent, stream=stream)
+        se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
+                         first_slot=self.zero, max_keep=self.budget, aux=self.acc,
+                         workspace=self.ws_compact, stream=stream)
+
+    def step(self, q, k_new, v_new, o, stream=None):
+        se_append_kv(self.kv, k_new, v_new, aux=self.acc, workspace=self.ws_append, stream=stream)
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.budget + 1,
+                              acc_scores=self.acc, workspace=self.ws_decode, stream=stream)
+        se_topk_select(self.kv, self.acc, mode=SE_SELECT_EVICT_ONE, keep_idx=self.victim,
+                       budget=self.budget, recent=self.recent, stream=stream)
+        se_compact_evict(self.kv, SE_COMPACT_MOVE_LAST, self.victim, aux=self.acc,
+                         workspace=self.ws_compact, stream=stream)
+
+
+class Kara(_Base):
+    """Kara periodic compression of the trailing window (bidirectional scores
+    of the compressible keys, Token2Chunk, compaction from the window start),
+    prefix-span pruning, and decode attention over the result."""
+
+    def __init__(self, cache, Hq, *, ctx, window, protected, candidates, budget, chunk_coef):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.ctx, self.window, self.protected = ctx, window, protected
+        self.candidates, self.budget, self.coef = candidates, budget, chunk_coef
+        self.win_lo = _i32([ctx - window] * B, dev)
+        self.prot_lo = _i32([ctx - protected] * B, dev)
+        self.ctx_t = _i32([ctx] * B, dev)
+        self.scores = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
+        self.keep = torch.empty((B, self.Hkv, budget + protected), dtype=torch.int32, device=dev)
+        self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+        self.n_busy = torch.empty(B, dtype=torch.int32, device=dev)
+        sz = workspace_sizes(self.kv, w=window, n_max=window, max_keep=budget + protected,
+                             max_entries=ctx)
+        self.ws_score = self._ws(sz["score_window"])
+        self.ws_compact = self._ws(sz["compact_evict"])
+        self.ws_prune = self._ws(sz["prune_span"])
+        self.ws_decode = self._ws(sz["sparse_decode_attn"])
+
+    def score(self, q_win, q_pos, stream=None):
+        se_score_window(self.kv, q_win, q_pos, self.win_lo, self.ctx_t, self.win_lo,
+                        self.prot_lo, causal=False, accumulate=False, n_max=self.window,
+                        scores=self.scores, workspace=self.ws_score, stream=stream)
+
+    def select(self, stream=None):
+        se_topk_select(self.kv, self.scores, mode=SE_SELECT_KARA_CHUNK, cand_lo=self.win_lo,
+                       cand_hi=self.prot_lo, force_lo=self.prot_lo, force_hi=self.ctx_t,
+                       keep_idx=self.keep, n_keep=self.n_keep, k=self.candidates,
+                       chunk_budget=self.budget, chunk_coef=self.coef,
+                       n_max=self.window - self.protected, stream=stream)
+
+    def compact(self, stream=None):
+        se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
+                         first_slot=self.win_lo, max_keep=self.budget + self.protected,
+                         workspace=self.ws_compact, stream=stream)
+
+    def compress(self, q_win, q_pos, stream=None):
+        self.score(q_win, q_pos, stream)
+        self.select(stream)
+        self.compact(stream)
+
+    def prune(self, L, R, mask, stream=None):
+        se_prune_span(self.kv, L, R, mask, n_busy=self.n_busy, workspace=self.ws_prune,
+                      stream=stream)
+
+    def decode(self, q, o, max_entries=None, stream=None):
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o,
+                              max_entries=max_entries or self.ctx, workspace=self.ws_decode,
+                              stream=stream)

@@ -1,0 +1,592 @@
+#!/usr/bin/env python
+"""Benchmark of the attention-scored sparse KV path on GB300.
+
+Default workload (the headline metric "KV tokens scored+compacted/s"): the
+Llama-3.1-8B-shaped layer at the end of prefill -- 4 sequences x 32,768
+tokens, 32 query / 8 KV heads, d=128, bf16, SnapKV window of 64 queries,
+pooling 7, budget 2048 per KV head.  One step = the whole path on one batch:
+window scoring -> pooled top-k -> compaction into fresh pages -> decode
+attention over the retained view.  Inputs are synthetic (seeded N(0,1) with
+1% of keys offset by 3 sigma along a random direction) and resident in HBM;
+the KV cache (570 MB) is larger than L2, so no flush is needed between steps.
+Before each step the cache's metadata (block table, slot map, lengths, free
+list, refcounts) is restored so that every step compresses the same input;
+the restore sits outside the device-timed region (it does not touch K/V: the
+compaction writes only fresh pages).
+
+Other workloads (--workload): snapkv_tiny, quest_decode, h2o_decode,
+kara_prune -- each prints its own line with its own dominant kernel.
+
+--impl reference times the CPU oracle (the slow, plain fp64 reference) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for k in FALLBACK_PEAKS:
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[k] = float(v) if v is not None else None
+        if all(v is not None for v in out.values()):
+            return out, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+
+def oracle_prepare(workload: str, groups: int):
+    """Builds a bounded sample of the workload for the oracle; returns a
+    function that runs the oracle once on a fresh copy of it and reports
+    (token-equivalents processed, seconds, description)."""
+    import numpy as np
+    import se_workloads as W
+    from oracle import attention as oattn
+    from oracle import cache as ocache
+    from oracle import pipelines as opipe
+    from oracle import quest as oquest
+    from oracle import scoring as oscore
+    from oracle import selection as osel
+
+    if workload in ("snapkv_llama8b", "snapkv_tiny"):
+        full = W.WORKLOADS[workload]()
+        shape = W.WORKLOADS[workload](B=1)
+        inp = W.snapkv_inputs(shape, "cpu")
+        c0 = ocache.from_tensors(inp["cache"])
+        heads = list(range(min(groups, shape.Hkv)))
+        q_pos = inp["q_pos"].numpy()
+        q_dec = opipe.to_f64(inp["q_dec"])
+        desc = (f"1 of {full.B} sequences, {len(heads)} of {shape.Hkv} KV heads ({shape.ctx} "
+                "tokens): score + pool/top-k + compact + decode")
+
+        def run():
+            c = c0.copy()
+            t0 = time.perf_counter()
+            s = oscore.score_window(c, inp["q_win"], q_pos, [0], [shape.ctx], [0],
+                                    [shape.scored], True, groups=[(0, h) for h in heads])
+            keep = [[osel.topk_keep(s[(0, h)], 0, shape.keep_topk, shape.pool_kernel,
+                                    shape.scored, shape.ctx) if h in heads
+                     else np.arange(shape.ctx - shape.budget, shape.ctx)
+                     for h in range(shape.Hkv)]]
+            ocache.compact(c, keep, [0])
+            oattn.decode_attention(c, q_dec, "dense", groups=[(0, h) for h in heads])
+            return shape.ctx * len(heads) / shape.Hkv, time.perf_counter() - t0, desc
+        return run
+    if workload == "quest_decode":
+        shape = W.quest_decode(B=1, ctx=16 * 1024)
+        inp = W.quest_inputs(shape, "cpu")
+        c = ocache.from_tensors(inp["cache"])
+        kmin, kmax = oquest.build_meta(c)
+        g = [(0, h) for h in range(min(groups, shape.Hkv))]
+        desc = (f"1 sequence, {len(g)} KV heads, 16384-token context (1023 candidate pages): "
+                "page bound + top-128 + decode")
+
+        def run():
+            t0 = time.perf_counter()
+            opipe.quest_step(c, kmin, kmax, inp["q_steps"][0], shape.top_pages, groups=g)
+            return len(g) / shape.Hkv, time.perf_counter() - t0, desc
+        return run
+    if workload == "h2o_decode":
+        shape = W.h2o_decode(B=1, ctx=1152)
+        inp = W.h2o_inputs(shape, "cpu", steps=2)
+        c0 = ocache.from_tensors(inp["cache"])
+        acc0 = np.random.default_rng(0).random(c0.slot_map.shape)
+        desc = "1 sequence at the 1152-token budget: append + attention + acc + evict"
+
+        def run():
+            c, acc = c0.copy(), acc0.copy()
+            t0 = time.perf_counter()
+            opipe.h2o_step(c, acc, inp["q_steps"][0], inp["k_steps"][0], inp["v_steps"][0], shape)
+            return 1.0, time.perf_counter() - t0, desc
+        return run
+    if workload == "kara_prune":
+        shape = W.kara_prune(B=1)
+        inp = W.kara_inputs(shape, "cpu")
+        c0 = ocache.from_tensors(inp["cache"])
+        q_pos = inp["q_pos"].numpy()
+        mask = inp["prune_mask"].numpy()
+        desc = "1 of 128 sequences (16384 tokens): Kara compress + prune"
+
+        def run():
+            c = c0.copy()
+            t0 = time.perf_counter()
+            r = opipe.kara_compress(c, inp["q_win"], q_pos, shape)
+            ocache.compact(c, r["keep"], r["first_slot"])
+            ocache.prune(c, [shape.prune_L], [shape.prune_R], mask)
+            return shape.ctx, time.perf_counter() - t0, desc
+        return run
+    raise ValueError(workload)
+
+
+def oracle_runs(workload: str, groups: int, n: int):
+    run = oracle_prepare(workload, groups)
+    return [run() for _ in range(n)]
+
+
+def oracle_subprocess(workload: str, groups: int, n: int = 1):
+    """Oracle samples in a child process pinned to one BLAS / OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench.oracle_runs({workload!r}, {groups}, {n})))")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------
+# GPU workloads
+# ---------------------------------------------------------------------------
+
+METRIC = "KV tokens scored+compacted/s"
+
+
+class Events:
+    def __init__(self, torch, names):
+        self.torch = torch
+        self.names = names
+        self.ev = {n: [] for n in names}
+
+    def mark(self, name):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.ev[name].append(e)
+
+    def durations(self, a, b):
+        return [x.elapsed_time(y) for x, y in zip(self.ev[a], self.ev[b])]
+
+
+def run_snapkv(args, torch, rank, world):
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    shape = W.WORKLOADS[args.workload]()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.snapkv_inputs(shape, dev)
+    pc = inp["cache"]
+    pipe = P.SnapKV(pc, shape.Hq, ctx=shape.ctx, window=shape.window, budget=shape.budget,
+                    pool_kernel=shape.pool_kernel)
+    o = torch.empty_like(inp["q_dec"])
+    meta = {n: getattr(pc, n).clone() for n in
+            ["block_table", "slot_map", "ctx_len", "free_list", "free_top", "page_refcount"]}
+
+    def restore():
+        for n, t in meta.items():
+            getattr(pc, n).copy_(t)
+
+    stages = ["s0", "s1", "s2", "s3", "s4"]
+    ev = Events(torch, stages)
+
+    def step(timed):
+        restore()
+        if timed: ev.mark("s0")
+        pipe.score(inp["q_win"], inp["q_pos"])
+        if timed: ev.mark("s1")
+        pipe.select()
+        if timed: ev.mark("s2")
+        pipe.compact()
+        if timed: ev.mark("s3")
+        pipe.decode(inp["q_dec"], o)
+        if timed: ev.mark("s4")
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    assert int(pc.status.item()) == 0
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    score_ms = ev.durations("s0", "s1")
+    sel_ms = ev.durations("s1", "s2")
+    comp_ms = ev.durations("s2", "s3")
+    dec_ms = ev.durations("s3", "s4")
+    step_ms = [a + b + c + d for a, b, c, d in zip(score_ms, sel_ms, comp_ms, dec_ms)]
+    ms = statistics.mean(step_ms)
+    G, D, B, Hkv = shape.G, shape.D, shape.B, shape.Hkv
+    rows = shape.window * G
+    flops = 2.0 * D * rows * shape.ctx * B * Hkv          # one sweep over the attention range
+    entry = 2 * D * (2 if shape.dtype == torch.bfloat16 else 4)  # K + V bytes of one entry
+    comp_bytes = 2.0 * B * Hkv * shape.budget * entry            # read + write
+    dec_bytes = B * Hkv * shape.budget * entry
+    tokens = B * shape.ctx
+    # e2e: host buffers, copies inside the timed region
+    e2e = run_e2e_snapkv(torch, pipe, inp, restore, args.steps)
+    detail = {
+        "score_ms": statistics.mean(score_ms), "select_ms": statistics.mean(sel_ms),
+        "compact_ms": statistics.mean(comp_ms), "decode_ms": statistics.mean(dec_ms),
+        "score_tflops": flops / (statistics.mean(score_ms) * 1e-3) / 1e12,
+        "compact_gbs": comp_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9,
+        "decode_gbs": dec_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9,
+    }
+    roof = dict(bound="tensor", achieved=detail["score_tflops"], unit="TFLOP/s",
+                kernel="se_score_window", per_launch=f"{flops:.4g} FLOP (one QK^T sweep)")
+    launches = 3 + 1 + 3 + 2
+    cfg = {"workload": f"{shape.name}: B={B} x {shape.ctx} tokens, Hq={shape.Hq}/Hkv={Hkv}, "
+                       f"d={D}, window {shape.window}, pool {shape.pool_kernel}, budget "
+                       f"{shape.budget}", "l2": "inputs larger than L2 (KV cache 570 MB)"}
+    return dict(tokens=tokens, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
+                launches=launches, cfg=cfg, e2e=e2e, dtype="bf16" if shape.dtype == torch.bfloat16 else "f32")
+
+
+def run_e2e_snapkv(torch, pipe, inp, restore, steps):
+    """Same metric through the public API with host-resident per-step inputs:
+    each step copies q_win, q_pos, q_dec from pinned host memory and reads the
+    decode output and the kept indices back."""
+    hq = {k: inp[k].cpu().pin_memory() for k in ("q_win", "q_pos", "q_dec")}
+    dq = {k: torch.empty_like(inp[k]) for k in hq}
+    o = torch.empty_like(inp["q_dec"])
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hk = torch.empty(pipe.keep.shape, dtype=pipe.keep.dtype, pin_memory=True)
+    total = []
+    for i in range(steps + 2):
+        restore()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in hq:
+            dq[k].copy_(hq[k], non_blocking=True)
+        pipe.step(dq["q_win"], dq["q_pos"], dq["q_dec"], o)
+        ho.copy_(o, non_blocking=True)
+        hk.copy_(pipe.keep, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            total.append(e0.elapsed_time(e1))
+    bi = sum(t.numel() * t.element_size() for t in hq.values())
+    bo = ho.numel() * ho.element_size() + hk.numel() * hk.element_size()
+    return statistics.mean(total), bi, bo
+
+
+def run_quest(args, torch, rank, world):
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    shape = W.quest_decode()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.quest_inputs(shape, dev)
+    pipe = P.QuestDecode(inp["cache"], shape.Hq, ctx=shape.ctx, top_pages=shape.top_pages)
+    pipe.build_meta()
+    o = torch.empty_like(inp["q_steps"][0])
+    ev = Events(torch, ["s0", "s1", "s2"])
+    it = [0]
+
+    def step(timed):
+        q = inp["q_steps"][it[0] % shape.steps]
+        it[0] += 1
+        if timed: ev.mark("s0")
+        pipe.select(q)
+        if timed: ev.mark("s1")
+        pipe.decode(q, o)
+        if timed: ev.mark("s2")
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    sel = ev.durations("s0", "s1")
+    dec = ev.durations("s1", "s2")
+    ms = statistics.mean([a + b for a, b in zip(sel, dec)])
+    nb = shape.ctx // shape.page_size
+    meta_bytes = shape.B * shape.Hkv * (nb - 1) * 2 * shape.D * 2
+    kv_bytes = shape.B * shape.Hkv * (shape.top_pages + 1) * shape.page_size * 2 * shape.D * 2
+    detail = {"select_ms": statistics.mean(sel), "decode_ms": statistics.mean(dec),
+              "select_gbs": meta_bytes / (statistics.mean(sel) * 1e-3) / 1e9,
+              "decode_gbs": kv_bytes / (statistics.mean(dec) * 1e-3) / 1e9,
+              "step_gbs": (meta_bytes + kv_bytes) / (ms * 1e-3) / 1e9}
+    roof = dict(bound="hbm", achieved=detail["step_gbs"], unit="GB/s", kernel="quest step",
+                per_launch=f"{meta_bytes + kv_bytes:.4g} B")
+    return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
+                launches=2 + 3 + 2, metric="decode tokens/s", e2e=None,
+                cfg={"workload": "quest_decode: B=2 x 131072 tokens, top 128 pages + current, "
+                                 "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
+                dtype="bf16")
+
+
+def run_h2o(args, torch, rank, world):
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    shape = W.h2o_decode()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    nsteps = max(args.steps + args.warmup + 2, 16)
+    inp = W.h2o_inputs(shape, dev, steps=nsteps)
+    pipe = P.H2O(inp["cache"], shape.Hq, prompt=shape.ctx, heavy=shape.heavy, recent=shape.recent)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    pipe.prefill(inp["q_prompt"], inp["q_pos"])
+    t1.record()
+    torch.cuda.synchronize()
+    prefill_ms = t0.elapsed_time(t1)
+    o = torch.empty_like(inp["q_steps"][0])
+    ev = Events(torch, ["s0", "s1"])
+    it = [0]
+
+    def step(timed):
+        t = it[0] % nsteps
+        it[0] += 1
+        if timed: ev.mark("s0")
+        pipe.step(inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], o)
+        if timed: ev.mark("s1")
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    ms = statistics.mean(ev.durations("s0", "s1"))
+    kv_bytes = shape.B * shape.Hkv * (shape.budget + 1) * 2 * shape.D * 2
+    detail = {"prefill_ms": prefill_ms, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9}
+    roof = dict(bound="hbm", achieved=detail["step_gbs"], unit="GB/s", kernel="h2o step",
+                per_launch=f"{kv_bytes:.4g} B")
+    return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
+                launches=2 + 2 + 1 + 2, metric="decode tokens/s", e2e=None,
+                cfg={"workload": "h2o_decode: B=64, 4096-token prompt, budget 1024+128, "
+                                 "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
+                dtype="bf16")
+
+
+def run_kara(args, torch, rank, world):
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    shape = W.kara_prune()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.kara_inputs(shape, dev)
+    pc = inp["cache"]
+    pipe = P.Kara(pc, shape.Hq, ctx=shape.ctx, window=shape.window, protected=shape.protected,
+                  candidates=shape.candidates, budget=shape.budget, chunk_coef=shape.chunk_coef)
+    meta = {n: getattr(pc, n).clone() for n in
+            ["block_table", "slot_map", "ctx_len", "free_list", "free_top", "page_refcount"]}
+    L = torch.full((shape.B,), shape.prune_L, dtype=torch.int32, device=dev)
+    R = torch.full((shape.B,), shape.prune_R, dtype=torch.int32, device=dev)
+    o = torch.empty_like(inp["q_dec"])
+    new_ctx = shape.prune_L + shape.prune_keep + (shape.ctx - shape.window - shape.prune_R) + \
+        shape.budget + shape.protected
+
+    def restore():
+        for n, t in meta.items():
+            getattr(pc, n).copy_(t)
+
+    ev = Events(torch, ["s0", "s1", "s2", "s3"])
+
+    def step(timed):
+        restore()
+        if timed: ev.mark("s0")
+        pipe.compress(inp["q_win"], inp["q_pos"])
+        if timed: ev.mark("s1")
+        pipe.prune(L, R, inp["prune_mask"])
+        if timed: ev.mark("s2")
+        pipe.decode(inp["q_dec"], o, max_entries=new_ctx)
+        if timed: ev.mark("s3")
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    assert int(pc.status.item()) == 0
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    comp = ev.durations("s0", "s1")
+    prn = ev.durations("s1", "s2")
+    dec = ev.durations("s2", "s3")
+    ms = statistics.mean([a + b + c for a, b, c in zip(comp, prn, dec)])
+    entry = 2 * shape.D * 2
+    moved = shape.prune_keep + (shape.ctx - shape.window - shape.prune_R) + shape.budget + shape.protected
+    prune_bytes = 2.0 * shape.B * shape.Hkv * moved * entry
+    dec_bytes = shape.B * shape.Hkv * new_ctx * entry
+    detail = {"compress_ms": statistics.mean(comp), "prune_ms": statistics.mean(prn),
+              "decode_ms": statistics.mean(dec),
+              "prune_gbs": prune_bytes / (statistics.mean(prn) * 1e-3) / 1e9,
+              "decode_gbs": dec_bytes / (statistics.mean(dec) * 1e-3) / 1e9}
+    roof = dict(bound="hbm", achieved=detail["prune_gbs"], unit="GB/s", kernel="se_prune_span",
+                per_launch=f"{prune_bytes:.4g} B (moved entries, read + write)")
+    return dict(tokens=shape.B * shape.ctx, ms=ms, wall=t_wall, clocks=clocks, detail=detail,
+                roof=roof, launches=3 + 1 + 3 + 5 + 2, e2e=None,
+                cfg={"workload": "kara_prune: B=128 x 16384 tokens, window 256 (32 protected), "
+                                 "chunk budget 64, prune [2048,6144) keep 20%",
+                     "l2": "inputs larger than L2"}, dtype="bf16")
+
+
+def timed_loop(args, torch, rank, world, fn):
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as cs:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            fn()
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    return t1 - t0, cs.summary()
+
+
+RUNNERS = {"snapkv_llama8b": run_snapkv, "snapkv_tiny": run_snapkv, "quest_decode": run_quest,
+           "h2o_decode": run_h2o, "kara_prune": run_kara}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="snapkv_llama8b", choices=sorted(RUNNERS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        runs = oracle_subprocess(args.workload, 1, args.warmup + args.steps)[args.warmup:]
+        per = [r[0] for r in runs]
+        times = [r[1] for r in runs]
+        desc = runs[0][2]
+        value = sum(per) / sum(times)
+        unit = "KV tokens/s" if args.workload.startswith(("snapkv", "kara")) else "decode tokens/s"
+        line = {"impl": "reference", "metric": METRIC if unit == "KV tokens/s" else "decode tokens/s",
+                "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "sample": desc},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import attention_scored_sparse_gb300  # noqa: F401  (fails loudly without the library)
+
+    r = RUNNERS[args.workload](args, torch, rank, world)
+    ms = r["ms"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = r["tokens"] * world / (ms * 1e-3)
+    pk, src = peaks()
+    peak = pk["bf16_tflops"] if r["roof"]["bound"] == "tensor" else pk["hbm_gbs"]
+    metric = r.get("metric", METRIC)
+    unit = "KV tokens/s" if metric == METRIC else "decode tokens/s"
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
+        "config": dict(r["cfg"], parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": r["roof"]["bound"], "achieved": r["roof"]["achieved"], "peak": peak,
+                     "unit": r["roof"]["unit"], "frac": r["roof"]["achieved"] / peak,
+                     "traffic": None, "kernel": r["roof"]["kernel"],
+                     "per_launch": r["roof"]["per_launch"], "peak_source": src},
+        "clocks": r["clocks"], "gpu_launches": r["launches"] * args.steps, "detail": r["detail"],
+        "wall_s_timed_region": r["wall"],
+    }
+    if r.get("e2e"):
+        e2e_ms, bi, bo = r["e2e"]
+        line["e2e"] = {"value": r["tokens"] * world / (e2e_ms * 1e-3), "unit": unit,
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            tokens, dt, desc = oracle_subprocess(args.workload, 2)[0]
+            line["cpu_baseline"] = {"value": tokens / dt, "unit": unit, "cores": 1,
+                                    "kind": "oracle", "sample": desc}
+        except Exception as exc:  # reported, not hidden
+            line["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

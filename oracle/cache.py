@@ -119,12 +119,13 @@ def _ints(t):
     return t.detach().cpu().numpy().astype(np.int64)
 
 
-def from_tensors(pc, seqs: Optional[Sequence[int]] = None) -> Cache:
+def from_tensors(pc, seqs: Optional[Sequence[int]] = None, blocks=None) -> Cache:
     """Snapshot a ``se_workloads.PagedCache`` (torch tensors) as an oracle Cache.
 
-    With ``seqs`` only the pages of those sequences are copied; the other
-    pages stay zero (lazily allocated), which is enough for checks restricted
-    to those sequences.
+    With ``seqs`` only the pages of those sequences are copied (plus, for
+    every sequence, the pages of the block range ``blocks`` = (lo, hi)); the
+    other pages stay zero (lazily allocated), which is enough for checks
+    restricted to those sequences / blocks.
     """
     bt = _ints(pc.block_table)
     if seqs is None:
@@ -134,12 +135,17 @@ def from_tensors(pc, seqs: Optional[Sequence[int]] = None) -> Cache:
         dt = np.uint16 if str(pc.k_pool.dtype) == "torch.bfloat16" else np.uint32
         k = np.zeros(shape, dtype=dt)
         v = np.zeros(shape, dtype=dt)
-        for b in seqs:
-            pages = bt[b][bt[b] >= 0]
-            import torch
-            idx = torch.as_tensor(pages, device=pc.k_pool.device)
-            k[pages] = _bits(pc.k_pool.index_select(0, idx))
-            v[pages] = _bits(pc.v_pool.index_select(0, idx))
+        import torch
+        want = [bt[b][bt[b] >= 0] for b in seqs]
+        if blocks is not None:
+            want += [bt[b, blocks[0]:blocks[1]] for b in range(bt.shape[0])]
+        pages = np.unique(np.concatenate(want))
+        pages = pages[pages >= 0]
+        for i in range(0, len(pages), 4096):
+            part = pages[i:i + 4096]
+            idx = torch.as_tensor(part, device=pc.k_pool.device)
+            k[part] = _bits(pc.k_pool.index_select(0, idx))
+            v[part] = _bits(pc.v_pool.index_select(0, idx))
     return Cache(k=k, v=v, block_table=bt, slot_map=_ints(pc.slot_map),
                  ctx_len=_ints(pc.ctx_len), logical_len=_ints(pc.logical_len),
                  free_list=_ints(pc.free_list), free_top=int(pc.free_top.reshape(-1)[0]),

@@ -75,6 +75,7 @@ def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
     o, psums = attention.decode_attention(c, to_f64(q), "dense")
     for (b, g), (slots, p) in psums.items():
         acc[b, g, slots] += p
+    acc_pre = acc.copy()
     victim = np.full((c.B, c.Hkv), -1, dtype=np.int64)
     for b in range(c.B):
         recent_from = int(c.logical_len[b]) - shape.recent
@@ -83,7 +84,7 @@ def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
                                                 shape.budget, recent_from)
     st = cache.move_last(c, victim, aux=acc)
     assert st == cache.SE_OK
-    return dict(o=o, victim=victim)
+    return dict(o=o, victim=victim, acc_pre=acc_pre)
 
 
 def kara_compress(c: Cache, q_win, q_pos, shape, groups=None, seqs=None):
