@@ -262,8 +262,10 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     for (int i = 0; i < n_my; ++i) {
       const int s = i % kStages1;
       const int acc = i & 1;
-      if (!tc::mbar_wait(&acc_full[acc], (i >> 1) & 1, kTimeoutNs) ||
-          (a.causal && !tc::mbar_wait(&full[s], (i / kStages1) & 1, kTimeoutNs))) {
+      bool w_ok = tc::mbar_wait(&acc_full[acc], (i >> 1) & 1, kTimeoutNs);
+      if (w_ok && a.causal) w_ok = tc::mbar_wait(&full[s], (i / kStages1) & 1, kTimeoutNs);
+      // warp-uniform decision: tcgen05.ld below is a warp-collective
+      if (!__all_sync(0xffffffffu, w_ok)) {
         record_timeout(a, &s_abort);
         break;
       }
@@ -528,7 +530,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         if (!q_resident) {
           for (int rc = 0; rc < RC; ++rc) {
             const int qn = p * RC + rc;
-            if (!tc::mbar_wait(&qfull[qn % QS], (qn / QS) & 1, kTimeoutNs)) {
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[qn % QS], (qn / QS) & 1, kTimeoutNs))) {
               record_timeout(a, &s_abort);
               stop = true;
               break;
@@ -547,7 +549,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         bool w_ok = tc::mbar_wait(&acc_full[set], use & 1, kTimeoutNs);
         if (w_ok && rc == 0 && a.causal) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
         if (w_ok) w_ok = tc::mbar_wait(&qfull[qs], q_resident ? 0 : ((qn / QS) & 1), kTimeoutNs);
-        if (!w_ok) {
+        if (!__all_sync(0xffffffffu, w_ok)) {  // tcgen05.ld below is a warp-collective
           record_timeout(a, &s_abort);
           stop = true;
           break;

@@ -72,7 +72,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -346,16 +346,32 @@ def run_quest(args, torch, rank, world):
     pipe = P.QuestDecode(inp["cache"], shape.Hq, ctx=shape.ctx, top_pages=shape.top_pages)
     pipe.build_meta()
     o = torch.empty_like(inp["q_steps"][0])
+    sq = torch.empty_like(inp["q_steps"][0])
+    sq.copy_(inp["q_steps"][0])
+    graphs = None
+    if not args.no_graph:
+        pipe.step(sq, o)
+        torch.cuda.synchronize()
+        graphs = []
+        for part in (pipe.select, lambda q: pipe.decode(q, o)):
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                part(sq)
+            graphs.append(g_)
+        torch.cuda.synchronize()
     ev = Events(torch, ["s0", "s1", "s2"])
     it = [0]
 
     def step(timed):
         q = inp["q_steps"][it[0] % shape.steps]
         it[0] += 1
+        sq.copy_(q)
         if timed: ev.mark("s0")
-        pipe.select(q)
+        if graphs: graphs[0].replay()
+        else: pipe.select(sq)
         if timed: ev.mark("s1")
-        pipe.decode(q, o)
+        if graphs: graphs[1].replay()
+        else: pipe.decode(sq, o)
         if timed: ev.mark("s2")
 
     for _ in range(args.warmup):
@@ -397,6 +413,25 @@ def run_h2o(args, torch, rank, world):
     torch.cuda.synchronize()
     prefill_ms = t0.elapsed_time(t1)
     o = torch.empty_like(inp["q_steps"][0])
+    # the step (append, attention + running scores, evict-one, move-last) is
+    # captured once in a CUDA graph over static input buffers; each step
+    # copies its q, k, v in and replays the graph
+    sq = torch.empty_like(inp["q_steps"][0])
+    sk = torch.empty_like(inp["k_steps"][0])
+    sv = torch.empty_like(inp["v_steps"][0])
+    sq.copy_(inp["q_steps"][0]); sk.copy_(inp["k_steps"][0]); sv.copy_(inp["v_steps"][0])
+    graph = None
+    if not args.no_graph:
+        s_cap = torch.cuda.Stream()
+        s_cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_cap):
+            pipe.step(sq, sk, sv, o)          # warm: kernel attributes, first launches
+        torch.cuda.current_stream().wait_stream(s_cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            pipe.step(sq, sk, sv, o)
+        torch.cuda.synchronize()
     ev = Events(torch, ["s0", "s1"])
     it = [0]
 
@@ -404,7 +439,11 @@ def run_h2o(args, torch, rank, world):
         t = it[0] % nsteps
         it[0] += 1
         if timed: ev.mark("s0")
-        pipe.step(inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], o)
+        sq.copy_(inp["q_steps"][t]); sk.copy_(inp["k_steps"][t]); sv.copy_(inp["v_steps"][t])
+        if graph is not None:
+            graph.replay()
+        else:
+            pipe.step(sq, sk, sv, o)
         if timed: ev.mark("s1")
 
     for _ in range(args.warmup):
@@ -498,6 +537,22 @@ def timed_loop(args, torch, rank, world, fn):
     return t1 - t0, cs.summary()
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's step time (every rank runs its own replica)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units processed by all ranks per second of the slowest rank."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 RUNNERS = {"snapkv_llama8b": run_snapkv, "snapkv_tiny": run_snapkv, "quest_decode": run_quest,
            "h2o_decode": run_h2o, "kara_prune": run_kara}
 
@@ -505,11 +560,12 @@ RUNNERS = {"snapkv_llama8b": run_snapkv, "snapkv_tiny": run_snapkv, "quest_decod
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="snapkv_llama8b", choices=sorted(RUNNERS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch decode steps eagerly")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -547,13 +603,8 @@ def main():
     import attention_scored_sparse_gb300  # noqa: F401  (fails loudly without the library)
 
     r = RUNNERS[args.workload](args, torch, rank, world)
-    ms = r["ms"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = r["tokens"] * world / (ms * 1e-3)
+    ms = max_over_ranks(r["ms"], world, "cuda")
+    value = whole_job_rate(r["tokens"], world, ms)
     pk, src = peaks()
     peak = pk["bf16_tflops"] if r["roof"]["bound"] == "tensor" else pk["hbm_gbs"]
     metric = r.get("metric", METRIC)

@@ -17,8 +17,8 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from attention_scored_sparse_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 

@@ -182,7 +182,7 @@ def _prune_case(se, seed, busy_pages=0):
         page = int(c.block_table[i % 3, 3 + i])
         c.page_refcount[page] = 2
         pc.page_refcount[page] = 2
-    L, R = [20, 33, 5], [120, 101, 160]
+    L, R = [20, 33, 5], [120, 101, 140]   # spans stay below the per-head tail at 150
     mask = np.zeros((3, 160), dtype=np.uint8)
     for b in range(3):
         mask[b, rng.choice(R[b] - L[b], (R[b] - L[b]) // 5, replace=False)] = 1

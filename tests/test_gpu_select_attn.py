@@ -45,7 +45,7 @@ def test_topk_matches_oracle(cuda_lib, n, k, pool, flo, fhi):
     B, Hkv = 3, 2
     pc, kv = _desc_dims(se, B, Hkv)
     g = W.generator("cpu", "topk", n, k)
-    scores = torch.rand((B, Hkv, fhi + 8), generator=g)
+    scores = torch.rand((B, Hkv, max(n, fhi) + 8), generator=g)
     scores[0, 0, : n // 2] = torch.round(scores[0, 0, : n // 2] * 8) / 8   # exact ties
     sc = scores.cuda()
     keep = torch.full((B, Hkv, k + (fhi - flo) + 4), -7, dtype=torch.int32, device="cuda")
