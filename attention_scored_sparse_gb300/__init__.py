@@ -31,6 +31,7 @@ SE_BF16, SE_F32 = 0, 1
 SE_SELECT_TOPK, SE_SELECT_KARA_CHUNK, SE_SELECT_EVICT_ONE = 0, 1, 2
 SE_COMPACT_FRESH_PAGES, SE_COMPACT_MOVE_LAST = 0, 1
 SE_VIEW_DENSE, SE_VIEW_PAGES, SE_VIEW_TOKENS = 0, 1, 2
+SE_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 EXPORTED = [
     "se_score_window", "se_score_window_workspace_size",
@@ -39,6 +40,7 @@ EXPORTED = [
     "se_prune_span", "se_prune_span_workspace_size",
     "se_quest_build_meta", "se_quest_page_select", "se_quest_page_select_workspace_size",
     "se_sparse_decode_attn", "se_sparse_decode_attn_workspace_size",
+    "se_sparse_decode_attn_static",
     "se_append_kv", "se_append_kv_workspace_size",
     "se_status_string", "se_version",
 ]
@@ -95,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "se_sparse_decode_attn": [P, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
                                   c_void_p, c_void_p, c_int64, c_void_p, c_size_t, c_void_p],
         "se_sparse_decode_attn_workspace_size": [P, c_int32],
+        "se_sparse_decode_attn_static": [P, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
+                                         c_void_p, c_void_p, c_int64, c_void_p],
         "se_append_kv": [P, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_size_t, c_void_p],
         "se_append_kv_workspace_size": [P],
         "se_status_string": [c_int32],
@@ -250,6 +254,16 @@ def se_sparse_decode_attn(kv, q, *, view, o, max_entries, sel=None, n_sel=0, acc
     _check("se_sparse_decode_attn", _lib.se_sparse_decode_attn(
         d, _ptr(q), view, _ptr(sel), sel_stride, n_sel, max_entries, _ptr(o), _ptr(acc_scores),
         acc_scores.shape[-1] if acc_scores is not None else 0, _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def se_sparse_decode_attn_static(kv, q, *, view, o, max_entries, sel=None, n_sel=0,
+                                 acc_scores=None, stream=None):
+    """Decode attention with the library's fixed device scratch (no workspace)."""
+    sel_stride = sel.shape[-1] if sel is not None else 0
+    _check("se_sparse_decode_attn_static", _lib.se_sparse_decode_attn_static(
+        ctypes.byref(kv), _ptr(q), view, _ptr(sel), sel_stride, n_sel, max_entries, _ptr(o),
+        _ptr(acc_scores), acc_scores.shape[-1] if acc_scores is not None else 0,
         _stream(stream)))
 
 

@@ -341,3 +341,54 @@ extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q,
   if (s != SE_OK) return s;
   return se_last_launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: scratch in a fixed device array owned by the
+// library (see se_sparse_decode_attn_static in se.h for who needs it).
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_decode_static_scratch[SE_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (cudaGetSymbolAddress, with that device current).  The host-side
+// name of the array is only a stand-in and must never reach a kernel.
+se_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_static_scratch) != cudaSuccess || p == nullptr)
+      return SE_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SE_OK;
+}
+
+}  // namespace
+
+extern "C" se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const void* q,
+                                                  int32_t view, const int32_t* sel,
+                                                  int32_t sel_stride, int32_t n_sel,
+                                                  int32_t max_entries, void* o, float* acc_scores,
+                                                  int64_t acc_stride, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (max_entries < 1) return SE_ERR_INVALID_ARG;
+  if (se_sparse_decode_attn_workspace_size(kv, max_entries) > SE_DECODE_STATIC_SCRATCH_BYTES)
+    return SE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  s = static_scratch(&scratch);
+  if (s != SE_OK) return s;
+  return se_sparse_decode_attn(kv, q, view, sel, sel_stride, n_sel, max_entries, o, acc_scores,
+                               acc_stride, scratch, SE_DECODE_STATIC_SCRATCH_BYTES, stream);
+}

@@ -286,6 +286,39 @@ se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q, int32_t vi
                                 void* stream);
 size_t se_sparse_decode_attn_workspace_size(const se_paged_kv* kv, int32_t max_entries);
 
+/*
+ * se_sparse_decode_attn_static -- the same decode attention as
+ * se_sparse_decode_attn, for callers that cannot allocate device memory at
+ * the point where they call it: code that runs inside a framework's own
+ * allocator-free region (plugins of an inference engine that owns every
+ * buffer, hooks that run while a memory pool is locked), embedded runtimes
+ * with a fixed memory budget, or callers without a device allocator at all.
+ * The pages have no counterpart of this call; it is a deployment variant.
+ *
+ * Instead of a caller-provided workspace it uses one scratch array of
+ * SE_DECODE_STATIC_SCRATCH_BYTES (16 MiB) that the library defines in
+ * device memory; every GPU that loads the library holds that array until the
+ * process exits.  Arguments are those of se_sparse_decode_attn without the
+ * workspace; the caller still owns q, o, sel and acc_scores.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture on the device.
+ *   - Calls share the array, which keeps the previous call's contents.
+ *     Nothing in it needs to start at zero (each call writes every value it
+ *     reads first), but calls that overlap on the GPU -- on different
+ *     streams, or on one stream from different host threads without ordering
+ *     -- race on it.  Serialize them.
+ *   - Returns SE_ERR_UNSUPPORTED, launching nothing, when the call needs more
+ *     scratch than the array holds (se_sparse_decode_attn_workspace_size
+ *     gives the amount for the same arguments).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define SE_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const void* q, int32_t view,
+                                       const int32_t* sel, int32_t sel_stride, int32_t n_sel,
+                                       int32_t max_entries, void* o, float* acc_scores,
+                                       int64_t acc_stride, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Helpers                                                                    */
 /* ------------------------------------------------------------------------ */
