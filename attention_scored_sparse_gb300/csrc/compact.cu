@@ -32,7 +32,7 @@ struct CompactWs {
   int32_t* new_ctx;   // [B]
   int32_t* old_ctx;   // [B]
   int32_t* off_new;   // [B] prefix of n_new
-  int32_t* off_push;  // [B] prefix of pushed pages
+  int32_t* push_count;// [B] old pages of the sequence that go back to the free list
   int32_t* newpage;   // [B * max_pages_per_seq]
   int32_t* slot_tmp;  // [B][Hkv][row]  new slot_map values from pb*P on
   float* aux_tmp;     // [B][Hkv][row]
@@ -51,7 +51,7 @@ static CompactWs carve_compact(const se_paged_kv* kv, int32_t max_keep, void* ws
   w.new_ctx = c.take<int32_t>(B);
   w.old_ctx = c.take<int32_t>(B);
   w.off_new = c.take<int32_t>(B);
-  w.off_push = c.take<int32_t>(B);
+  w.push_count = c.take<int32_t>(B);
   w.newpage = c.take<int32_t>((size_t)B * kv->max_pages_per_seq);
   w.row = (int64_t)max_keep + kv->page_size;
   w.slot_tmp = c.take<int32_t>((size_t)B * kv->Hkv * w.row);
@@ -71,13 +71,12 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
     int32_t max_keep, const int32_t* __restrict__ abort_in, CompactWs w) {
   __shared__ int tmp[33];
   __shared__ int s_bad;
-  __shared__ int s_run_new, s_run_push;
+  __shared__ int s_run_new;
   const int tid = threadIdx.x;
   const int P = kv.page_size;
   if (tid == 0) {
     s_bad = (abort_in != nullptr && *abort_in != 0) ? 1 : 0;
     s_run_new = 0;
-    s_run_push = 0;
   }
   __syncthreads();
   if (s_bad) {
@@ -114,42 +113,11 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
     if (tid == 0) s_run_new += total;
     __syncthreads();
   }
-  // pushed pages per sequence: one warp per sequence
-  __shared__ int s_push[1024];
-  const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  for (int b0 = 0; b0 < kv.B; b0 += 1024) {
-    for (int bb = warp; bb < 1024 && b0 + bb < kv.B; bb += nw) {
-      const int b = b0 + bb;
-      const int pb = w.pb[b], ob = w.old_blocks[b];
-      int cnt = 0;
-      if (kv.page_refcount == nullptr) {
-        cnt = lane == 0 ? max(ob - pb, 0) : 0;
-      } else {
-        for (int blk = pb + lane; blk < ob; blk += 32) {
-          const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
-          cnt += (page >= 0 && kv.page_refcount[page] <= 1) ? 1 : 0;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      if (lane == 0) s_push[bb] = cnt;
-    }
-    __syncthreads();
-    const int b = b0 + tid;
-    const int v = (b < kv.B) ? s_push[tid] : 0;
-    int total;
-    int ex = block_exclusive_scan(v, tmp, &total);
-    if (b < kv.B) w.off_push[b] = s_run_push + ex;
-    __syncthreads();
-    if (tid == 0) s_run_push += total;
-    __syncthreads();
-  }
   const int top0 = *kv.free_top;
   const int total_new = s_run_new;
   if (tid == 0) {
     w.ctrl->top0 = top0;
     w.ctrl->total_new = total_new;
-    w.ctrl->total_push = s_run_push;
     int bad = s_bad;
     if (!bad && total_new > top0) {
       set_status(kv.status, SE_ERR_OUT_OF_PAGES);
@@ -157,8 +125,6 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
     }
     w.ctrl->abort = bad;
   }
-  if (s_bad || total_new > top0) return;
-  for (int i = tid; i < total_new; i += blockDim.x) w.newpage[i] = kv.free_list[top0 - 1 - i];
 }
 
 // Copies the surviving entries into the fresh pages (K, V) and stages their
@@ -173,6 +139,26 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   const int P = kv.page_size;
   const int pb = w.pb[b];
   const int fs = first_slot[b];
+  const int top0 = w.ctrl->top0;
+  const int pop0 = top0 - 1 - w.off_new[b];   // free_list index of this sequence's first fresh page
+  if (blockIdx.x == 0 && h == 0) {
+    // record the fresh pages for the commit kernel, count the old pages that
+    // return to the free list (busy pages only lose a reference)
+    __shared__ int s_cnt;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < w.n_new[b]; i += blockDim.x)
+      w.newpage[w.off_new[b] + i] = kv.free_list[pop0 - i];
+    const int32_t* btb = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    int cnt = 0;
+    for (int blk = pb + threadIdx.x; blk < w.old_blocks[b]; blk += blockDim.x) {
+      const int page = btb[blk];
+      cnt += (page >= 0 && (kv.page_refcount == nullptr || kv.page_refcount[page] <= 1)) ? 1 : 0;
+    }
+    if (cnt) atomicAdd(&s_cnt, cnt);
+    __syncthreads();
+    if (threadIdx.x == 0) w.push_count[b] = s_cnt;
+  }
   const int head = fs - pb * P;
   const int total = head + (w.new_ctx[b] - fs);
   const int e0 = blockIdx.x * entries_per_cta;
@@ -207,7 +193,7 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
       }
     }
     const int sp = bt[src / P];
-    const int dp = w.newpage[w.off_new[b] + i / P];
+    const int dp = kv.free_list[pop0 - i / P];
     if (sp < 0 || sp >= kv.num_pages || dp < 0 || dp >= kv.num_pages) {
       if (ch == 0) {
         set_status(kv.status, SE_ERR_BOUNDS);
@@ -230,17 +216,26 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   }
 }
 
-// Commits block tables, slot maps, lengths, refcounts and pushes.  grid: B.
-__global__ void __launch_bounds__(256) compact_finalize_kernel(se_paged_kv kv, float* aux,
-                                                               int64_t aux_stride, CompactWs w) {
+// Commits block tables, lengths, refcounts and free-list pushes.  grid: B.
+__global__ void __launch_bounds__(256) compact_finalize_pages_kernel(se_paged_kv kv, CompactWs w) {
   __shared__ int tmp[33];
   if (w.ctrl->abort) return;
   const int b = blockIdx.x, tid = threadIdx.x;
-  const int P = kv.page_size;
   const int pb = w.pb[b], nn = w.n_new[b], ob = w.old_blocks[b];
-  const int nctx = w.new_ctx[b], octx = w.old_ctx[b];
   const int top0 = w.ctrl->top0, total_new = w.ctrl->total_new;
-  const int push_base = top0 - total_new + w.off_push[b];
+  __shared__ int s_off, s_total;
+  if (tid == 0) {
+    int off = 0, total = 0;
+    for (int bb = 0; bb < kv.B; ++bb) {
+      const int cnt = w.push_count[bb];
+      off += bb < b ? cnt : 0;
+      total += cnt;
+    }
+    s_off = off;
+    s_total = total;
+  }
+  __syncthreads();
+  const int push_base = top0 - total_new + s_off;
   int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   const int end = max(ob, pb + nn);
   int running = 0;
@@ -268,25 +263,41 @@ __global__ void __launch_bounds__(256) compact_finalize_kernel(se_paged_kv kv, f
       kv.free_list[push_base + running + pos] = old;
       if (kv.page_refcount) kv.page_refcount[old] = 0;
     }
-    if (busy) kv.page_refcount[old] -= 1;
+    if (busy) atomicSub(&kv.page_refcount[old], 1);
     running += total;
   }
-  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
-  const int n_rows = nctx - pb * P;
-  for (int h = 0; h < kv.Hkv; ++h) {
-    int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
-    const int64_t tb = ((int64_t)b * kv.Hkv + h) * w.row;
-    for (int i = tid; i < n_rows; i += blockDim.x) sm[pb * P + i] = w.slot_tmp[tb + i];
-    for (int s = nctx + tid; s < octx; s += blockDim.x) sm[s] = -1;
-    if (aux != nullptr) {
-      float* ar = aux + ((int64_t)b * kv.Hkv + h) * aux_stride;
-      for (int i = tid; i < n_rows; i += blockDim.x) ar[pb * P + i] = w.aux_tmp[tb + i];
-      for (int s = nctx + tid; s < octx; s += blockDim.x) ar[s] = 0.f;
-    }
-  }
   if (tid == 0) {
-    kv.ctx_len[b] = nctx;
-    if (b == 0) *kv.free_top = top0 - total_new + w.ctrl->total_push;
+    kv.ctx_len[b] = w.new_ctx[b];
+    if (b == 0) *kv.free_top = top0 - total_new + s_total;
+  }
+}
+
+// Commits slot maps (and aux) from the staged values; slots past the new
+// length become -1 (aux 0).  grid: (slot chunks of 1024, Hkv, B).
+__global__ void __launch_bounds__(256) compact_finalize_slots_kernel(se_paged_kv kv, float* aux,
+                                                                     int64_t aux_stride,
+                                                                     CompactWs w) {
+  if (w.ctrl->abort) return;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int P = kv.page_size;
+  const int base = w.pb[b] * P;
+  const int nctx = w.new_ctx[b], octx = w.old_ctx[b];
+  const int s_end = max(nctx, octx);
+  const int s0 = base + blockIdx.x * 1024;
+  if (s0 >= s_end) return;
+  const int s1 = min(s0 + 1024, s_end);
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+  const int64_t tb = ((int64_t)b * kv.Hkv + h) * w.row;
+  float* ar = aux != nullptr ? aux + ((int64_t)b * kv.Hkv + h) * aux_stride : nullptr;
+  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+    if (s < nctx) {
+      sm[s] = w.slot_tmp[tb + (s - base)];
+      if (ar) ar[s] = w.aux_tmp[tb + (s - base)];
+    } else {
+      sm[s] = -1;
+      if (ar) ar[s] = 0.f;
+    }
   }
 }
 
@@ -668,7 +679,10 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
     default:
       return SE_ERR_UNSUPPORTED;
   }
-  compact_finalize_kernel<<<kv->B, 256, 0, st>>>(*kv, aux, aux_stride, w);
+  compact_finalize_pages_kernel<<<kv->B, 256, 0, st>>>(*kv, w);
+  const int max_span = kv->max_pages_per_seq * kv->page_size;
+  compact_finalize_slots_kernel<<<dim3(cdiv(max_span, 1024), kv->Hkv, kv->B), 256, 0, st>>>(
+      *kv, aux, aux_stride, w);
   return se_last_launch_status();
 }
 

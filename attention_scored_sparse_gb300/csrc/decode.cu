@@ -6,13 +6,13 @@
 //
 // Bandwidth-bound design (each K/V byte is used by the G query heads of its
 // group and nothing else): split-K over the view ("chunks" of entries, one
-// CTA each, sized so the grid fills the 152 SMs several times), one half-warp
-// per entry with 16-byte row loads (a 256-byte bf16 row is one coalesced
-// half-warp load), the group's G queries pre-scaled by log2(e)/sqrt(D) in
-// registers, a 4-step xor butterfly for the dot products and a base-2 online
-// softmax per half-warp.  Half-warp states merge in shared memory; a second
-// kernel merges the chunks and, for H2O, adds sum_h p_{h,j} to the running
-// scores from the logits the first kernel stored.
+// CTA each, about four CTAs per SM), a half-warp per group of 16/G entries
+// with 16-byte row loads (a 256-byte bf16 row is one coalesced half-warp
+// load), the group's G queries pre-scaled by log2(e)/sqrt(D) in registers, an
+// xor reduce-scatter of the partial dot products, one exponential per
+// (entry, head) and a base-2 online softmax.  Half-warp states merge in
+// shared memory; a second kernel merges the chunks and, for H2O, adds
+// sum_h p_{h,j} to the running scores from the logits the first kernel stored.
 #include "se_common.cuh"
 
 namespace se {
@@ -84,9 +84,23 @@ SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
 }
 
 // grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps.
+//
+// A half-warp takes E = 16/G consecutive view entries per iteration; lane t
+// owns dims [V t, V t + V) of K, V, q and o (V = D/16).  The E x G partial dot
+// products of a lane are reduced across the 16 lanes by a 4-step xor
+// reduce-scatter that leaves lane t with the complete logit of
+// (entry t / G, head t % G): 15 shuffles per iteration instead of 4 G per
+// entry.  Each lane then runs the base-2 online softmax for its own logit
+// (one exponential), the per-head maxima are exchanged among the lanes of a
+// head, the probabilities are all-gathered through shared memory, and every
+// lane accumulates p * v for its dims.  o is rescaled only when a head's
+// maximum grows.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
-  constexpr int V = D / 16;  // elements per lane
+  constexpr int V = D / 16;        // dims per lane
+  constexpr int E = 16 / G;        // entries per half-warp iteration
+  static_assert(E * G == 16, "G must divide 16");
+  __shared__ float s_p[8][16];
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ float s_o[8][G][D];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -94,6 +108,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
   const int P = kv.page_size;
   const int ctx = kv.ctx_len[b];
   const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int my_e = t / G, my_h = t % G;   // the logit this lane holds after the reduction
   const int n_view = min(view_entries(a, ctx), a.max_entries);
   const int e_begin = c * a.chunk;
   const int e_end = min(e_begin + a.chunk, n_view);
@@ -107,31 +122,31 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) q[j][i] *= qscale;
   }
-  float m[G], l[G], o[G][V];
+  float m[G], o[G][V];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     m[j] = -INFINITY;
-    l[j] = 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) o[j][i] = 0.f;
   }
+  float l_own = 0.f;                 // running sum of this lane's head, own entries
   const T* kp = static_cast<const T*>(kv.k_pool);
   const T* vp = static_cast<const T*>(kv.v_pool);
   const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
+  const unsigned full = 0xffffffffu;
 
-  constexpr int U = 4;  // entries in flight per half-warp
-  // Every lane of a warp runs the same iterations (the xor shuffles below
-  // need both half-warps); invalid entries are predicated off.
-  for (int base = e_begin; base < e_end; base += 8 * U) {
-    float kf[U][V], vf[U][V];
-    int slot[U];
+  for (int base = e_begin; base < e_end; base += 8 * E) {
+    const int e0 = base + hw * E;
+    float kf[E][V], vf[E][V];
+    bool valid[E];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int e = base + hw + 8 * u;
-      slot[u] = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
-      if (slot[u] >= 0) {
-        const int64_t off = (((int64_t)bt[slot[u] / P] * kv.Hkv + g) * P + slot[u] % P) * D + t * V;
+    for (int u = 0; u < E; ++u) {
+      const int e = e0 + u;
+      const int slot = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
+      valid[u] = slot >= 0;
+      if (valid[u]) {
+        const int64_t off = (((int64_t)bt[slot / P] * kv.Hkv + g) * P + slot % P) * D + t * V;
         load_row<T, V>(kp + off, kf[u]);
         load_row<T, V>(vp + off, vf[u]);
       } else {
@@ -139,43 +154,86 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
         for (int i = 0; i < V; ++i) { kf[u][i] = 0.f; vf[u][i] = 0.f; }
       }
     }
+    // partial dots, value index u * G + j
+    float part[16];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float s[G];
+    for (int u = 0; u < E; ++u)
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[u][i], acc);
-        s[j] = acc;
+        part[u * G + j] = acc;
       }
+    // reduce-scatter: the lane keeps the upper half where its bit is set, so
+    // after 4 steps lane t holds value t
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1)
+    for (int step = 0; step < 4; ++step) {
+      const int off = 8 >> step;
+      const int n = 8 >> step;
+      const bool upper = (t & off) != 0;
 #pragma unroll
-        for (int j = 0; j < G; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], off);
-      if (slot[u] < 0) continue;  // uniform within the half-warp
-      if (lg != nullptr && t < G) {
-        float sv = s[0];
-#pragma unroll
-        for (int j = 1; j < G; ++j) sv = (t == j) ? s[j] : sv;
-        lg[(int64_t)(base + hw + 8 * u) * G + t] = sv;
-      }
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float mn = fmaxf(m[j], s[j]);
-        const float sc = ex2(m[j] - mn);
-        const float p = ex2(s[j] - mn);
-        l[j] = fmaf(l[j], sc, p);
-#pragma unroll
-        for (int i = 0; i < V; ++i) o[j][i] = fmaf(o[j][i], sc, p * vf[u][i]);
-        m[j] = mn;
+      for (int i = 0; i < n; ++i) {
+        const float lo = part[i], hi = part[i + n];
+        part[i] = (upper ? hi : lo) + __shfl_xor_sync(full, upper ? lo : hi, off);
       }
     }
-  }
-  // merge the 8 half-warp states
-  if (t == 0) {
+    bool ok = false;
 #pragma unroll
-    for (int j = 0; j < G; ++j) { s_m[hw][j] = m[j]; s_l[hw][j] = l[j]; }
+    for (int u = 0; u < E; ++u) ok = (u == my_e) ? valid[u] : ok;
+    const float sv = ok ? part[0] : -INFINITY;
+    if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+    // maximum of this head over the iteration's entries: lanes of one head
+    // differ in the bits above log2(G)
+    float tmax = sv;
+#pragma unroll
+    for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full, tmax, off));
+    float m_mine = m[0];             // running max of my head before this iteration
+#pragma unroll
+    for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+    const float mn_mine = fmaxf(m_mine, tmax);
+    const float alpha_mine = (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+    const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+    l_own = fmaf(l_own, alpha_mine, p);
+    s_p[hw][t] = p;
+    // every lane needs every head's new maximum / rescale factor
+    bool grew = false;
+    float alpha[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float mj = __shfl_sync(full, mn_mine, (threadIdx.x & 16) + j);
+      alpha[j] = __shfl_sync(full, alpha_mine, (threadIdx.x & 16) + j);
+      grew |= mj != m[j];
+      m[j] = mj;
+    }
+    __syncwarp();
+    if (grew) {
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[j][i] *= alpha[j];
+    }
+#pragma unroll
+    for (int u = 0; u < E; ++u) {
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float pu = s_p[hw][u * G + j];
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[j][i] = fmaf(pu, vf[u][i], o[j][i]);
+      }
+    }
+    __syncwarp();
+  }
+  // running sums of each head: lanes of a head add up their own entries
+  float lsum = l_own;
+#pragma unroll
+  for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full, lsum, off);
+  if (t < G) {
+    float mt = m[0];
+#pragma unroll
+    for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+    s_m[hw][t] = mt;
+    s_l[hw][t] = lsum;
   }
 #pragma unroll
   for (int j = 0; j < G; ++j)
@@ -273,11 +331,13 @@ static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, int n_chunk
   return w;
 }
 
-// Entries per CTA: enough CTAs to fill the GPU several times over.
+// Entries per CTA: about four CTAs per SM of the 152, at least 128 entries
+// (64 KB of K/V) per CTA so that per-CTA set-up and the partial write stay
+// small next to the stream, at most 1024.
 static int pick_chunk(const se_paged_kv* kv, int max_entries) {
   const int64_t units = (int64_t)kv->B * kv->Hkv;
   int chunk = 1024;
-  while (chunk > 64 && units * cdiv(max_entries, chunk) < 152 * 8) chunk >>= 1;
+  while (chunk > 128 && units * cdiv(max_entries, chunk) < 152 * 4) chunk >>= 1;
   return chunk;
 }
 

@@ -273,25 +273,58 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       const int tile = t_begin + i;
       const int key0 = tg.base + tile * kKeyTile;
       const int32_t* pos = pos_s + s * kKeyTile;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 32, v);
-        float cm = -INFINITY;
+      // fast path: every key of the tile is in range and visible to this row
+      bool fast = row_ok && key0 >= tg.lo && key0 + kKeyTile <= tg.hi;
+      if (a.causal) {
+        const int4 p4 = reinterpret_cast<const int4*>(pos)[lane];
+        int mx = max(max(p4.x, p4.y), max(p4.z, p4.w));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = key0 + c * 32 + j;
-          bool vis = row_ok && key >= tg.lo && key < tg.hi;
-          if (a.causal) vis = vis && pos[c * 32 + j] <= qpos;
-          v[j] = vis ? v[j] * a.scale : -INFINITY;
-          cm = fmaxf(cm, v[j]);
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        fast = fast && mx <= qpos;
+      }
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float v[64];
+        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 64, v);
+        if (fast) {
+          float c0 = v[0], c1 = v[1], c2 = v[2], c3 = v[3];
+#pragma unroll
+          for (int j = 4; j < 64; j += 4) {
+            c0 = fmaxf(c0, v[j]); c1 = fmaxf(c1, v[j + 1]);
+            c2 = fmaxf(c2, v[j + 2]); c3 = fmaxf(c3, v[j + 3]);
+          }
+          const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * a.scale);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            s0 += tc::ex2(fmaf(v[j], a.scale, -mn));
+            s1 += tc::ex2(fmaf(v[j + 1], a.scale, -mn));
+            s2 += tc::ex2(fmaf(v[j + 2], a.scale, -mn));
+            s3 += tc::ex2(fmaf(v[j + 3], a.scale, -mn));
+          }
+          l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
+          m = mn;
+          continue;
         }
+        float c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int key = key0 + c * 64 + j;
+          bool vis = row_ok && key >= tg.lo && key < tg.hi;
+          if (a.causal) vis = vis && pos[c * 64 + j] <= qpos;
+          v[j] = vis ? v[j] * a.scale : -INFINITY;
+          if (j & 1) c1 = fmaxf(c1, v[j]); else c0 = fmaxf(c0, v[j]);
+        }
+        const float cm = fmaxf(c0, c1);
         if (cm != -INFINITY) {
           const float mn = fmaxf(m, cm);
-          float sum = 0.f;
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum += tc::ex2(v[j] - mn);
-          l = l * tc::ex2(m - mn) + sum;
+          for (int j = 0; j < 64; j += 2) {
+            s0 += tc::ex2(v[j] - mn);
+            s1 += tc::ex2(v[j + 1] - mn);
+          }
+          l = l * tc::ex2(m - mn) + (s0 + s1);
           m = mn;
         }
       }
@@ -325,7 +358,7 @@ __global__ void score_rowinfo_tc(TcArgs a) {
   const int padded = a.RC * kRowChunk;
   if (row >= padded) return;
   float lse = INFINITY;
-  int qpos = -1;
+  int qpos = 0x7fffffff;   // padded rows: lse = +inf already makes p = 0
   if (row < a.rows) {
     const float* p = a.part + ((int64_t)bg * padded + row) * a.n_splits * 2;
     float M = -INFINITY;
@@ -336,7 +369,10 @@ __global__ void score_rowinfo_tc(TcArgs a) {
     if (L > 0.f) lse = M + log2f(L);
     qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
   }
-  a.rowinfo[(int64_t)bg * padded + row] = make_float2(lse, __int_as_float(qpos));
+  // per 256-row chunk: 256 lse2 values, then 256 query positions
+  float* chunk = reinterpret_cast<float*>(a.rowinfo + (int64_t)bg * padded + (row / kRowChunk) * kRowChunk);
+  chunk[row % kRowChunk] = lse;
+  chunk[kRowChunk + row % kRowChunk] = __int_as_float(qpos);
 }
 
 // ---------------------------------------------------------------------------
@@ -556,19 +592,45 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         }
         tc::tc_fence_after();
         if (rc == 0 && a.causal) kpos = pos_s[s * kKeyTile + kl];
-        const float2* info = info_s + qs * kRowChunk;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float v[32];
-          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 32, v);
+        const float* lse_s = reinterpret_cast<const float*>(info_s + qs * kRowChunk);
+        const int* qp_s = reinterpret_cast<const int*>(lse_s + kRowChunk);
+        // fast path: this key is visible to every row of the chunk
+        bool fast = !a.causal;
+        if (a.causal) {
+          const int4 q4a = reinterpret_cast<const int4*>(qp_s)[lane * 2];
+          const int4 q4b = reinterpret_cast<const int4*>(qp_s)[lane * 2 + 1];
+          int mn = min(min(min(q4a.x, q4a.y), min(q4a.z, q4a.w)), min(min(q4b.x, q4b.y), min(q4b.z, q4b.w)));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float2 ri = info[c * 32 + j];
-            float pv = tc::ex2(fmaf(v[j], a.scale, -ri.x));
-            if (a.causal && kpos > __float_as_int(ri.y)) pv = 0.f;
-            colsum += pv;
+          for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          fast = kpos <= mn;
+        }
+        float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[64];
+          tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 64, v);
+          if (fast) {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c * 64 + j);
+              cs0 += tc::ex2(fmaf(v[j], a.scale, -l4.x));
+              cs1 += tc::ex2(fmaf(v[j + 1], a.scale, -l4.y));
+              cs2 += tc::ex2(fmaf(v[j + 2], a.scale, -l4.z));
+              cs3 += tc::ex2(fmaf(v[j + 3], a.scale, -l4.w));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              float p0 = tc::ex2(fmaf(v[j], a.scale, -lse_s[c * 64 + j]));
+              float p1 = tc::ex2(fmaf(v[j + 1], a.scale, -lse_s[c * 64 + j + 1]));
+              if (kpos > qp_s[c * 64 + j]) p0 = 0.f;
+              if (kpos > qp_s[c * 64 + j + 1]) p1 = 0.f;
+              cs0 += p0;
+              cs1 += p1;
+            }
           }
         }
+        colsum += (cs0 + cs1) + (cs2 + cs3);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {

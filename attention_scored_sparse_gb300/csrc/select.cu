@@ -98,9 +98,15 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += 1024) hist[i] = 0;
       __syncthreads();
+      // warp-aggregated histogram: lanes holding the same digit add once
+      // (scores cluster in a few exponents, so plain atomics would serialise)
 #pragma unroll
-      for (int i = 0; i < ITEMS; ++i)
-        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+      for (int i = 0; i < ITEMS; ++i) {
+        const bool in = key[i] != 0u && (key[i] & pmask) == prefix;
+        const uint32_t bin = in ? ((key[i] >> shift) & 255u) : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (in && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+      }
       __syncthreads();
       if (tid < 32) {
         // lane l owns bins [8l, 8l+8); suffix sums from the top bin down
