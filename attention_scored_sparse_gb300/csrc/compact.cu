@@ -175,9 +175,17 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   char* kpw = static_cast<char*>(kv.k_pool);
   char* vpw = static_cast<char*>(kv.v_pool);
   constexpr int EPP = 256 / CHUNKS;  // entries per pass
+  constexpr int PASSES = 4;          // entries_per_cta == EPP * PASSES
   const int sub = threadIdx.x / CHUNKS, ch = threadIdx.x % CHUNKS;
   const int64_t tmp_base = ((int64_t)b * kv.Hkv + h) * w.row;
-  for (int i = e0 + sub; i < e1; i += EPP) {
+  // all loads of this thread first (PASSES x (K, V) 16-byte rows in flight), then the stores
+  uint4 kbuf[PASSES], vbuf[PASSES];
+  int64_t dst[PASSES];
+#pragma unroll
+  for (int pss = 0; pss < PASSES; ++pss) {
+    const int i = e0 + sub + pss * EPP;
+    dst[pss] = -1;
+    if (i >= e1) continue;
     int src;
     if (i < head) {
       src = pb * P + i;
@@ -202,11 +210,9 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
       continue;
     }
     const int64_t so = (int64_t)sp * page_bytes + ((int64_t)h * P + src % P) * row_bytes + ch * 16;
-    const int64_t dof = (int64_t)dp * page_bytes + ((int64_t)h * P + i % P) * row_bytes + ch * 16;
-    const uint4 kv4 = ldg_nc_v4(kp + so);
-    const uint4 vv4 = ldg_nc_v4(vp + so);
-    stg_v4(kpw + dof, kv4);
-    stg_v4(vpw + dof, vv4);
+    dst[pss] = (int64_t)dp * page_bytes + ((int64_t)h * P + i % P) * row_bytes + ch * 16;
+    kbuf[pss] = ldg_nc_v4(kp + so);
+    vbuf[pss] = ldg_nc_v4(vp + so);
     if (ch == 0) {
       w.slot_tmp[tmp_base + i] = kv.slot_map[((int64_t)b * kv.Hkv + h) *
                                                  ((int64_t)kv.max_pages_per_seq * P) + src];
@@ -214,10 +220,16 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
         w.aux_tmp[tmp_base + i] = aux[((int64_t)b * kv.Hkv + h) * aux_stride + src];
     }
   }
+#pragma unroll
+  for (int pss = 0; pss < PASSES; ++pss) {
+    if (dst[pss] < 0) continue;
+    stg_v4(kpw + dst[pss], kbuf[pss]);
+    stg_v4(vpw + dst[pss], vbuf[pss]);
+  }
 }
 
 // Commits block tables, lengths, refcounts and free-list pushes.  grid: B.
-__global__ void __launch_bounds__(256) compact_finalize_pages_kernel(se_paged_kv kv, CompactWs w) {
+__global__ void __launch_bounds__(1024) compact_finalize_pages_kernel(se_paged_kv kv, CompactWs w) {
   __shared__ int tmp[33];
   if (w.ctrl->abort) return;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -660,26 +672,31 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
   compact_plan_kernel<<<1, 1024, 0, st>>>(*kv, n_keep, first_slot, max_keep, abort_in, w);
   const int row_bytes = kv->D * (int)elem_size(kv->dtype);
   const int chunks = row_bytes / 16;
-  const int epc = 64;
   const int max_entries = max_keep + kv->page_size;
-  dim3 grid(cdiv(max_entries, epc), kv->Hkv, kv->B);
+  // entries per CTA = (256 / chunks) rows per pass x 4 passes
   switch (chunks) {
-    case 8:
-      compact_gather_kernel<8><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
-                                                      aux_stride, w, epc);
+    case 8: {
+      const int epc = 4 * (256 / 8);
+      compact_gather_kernel<8><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+          *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
-    case 16:
-      compact_gather_kernel<16><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
-                                                       aux_stride, w, epc);
+    }
+    case 16: {
+      const int epc = 4 * (256 / 16);
+      compact_gather_kernel<16><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+          *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
-    case 32:
-      compact_gather_kernel<32><<<grid, 256, 0, st>>>(*kv, keep_idx, keep_stride, first_slot, aux,
-                                                       aux_stride, w, epc);
+    }
+    case 32: {
+      const int epc = 4 * (256 / 32);
+      compact_gather_kernel<32><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+          *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
+    }
     default:
       return SE_ERR_UNSUPPORTED;
   }
-  compact_finalize_pages_kernel<<<kv->B, 256, 0, st>>>(*kv, w);
+  compact_finalize_pages_kernel<<<kv->B, 1024, 0, st>>>(*kv, w);
   const int max_span = kv->max_pages_per_seq * kv->page_size;
   compact_finalize_slots_kernel<<<dim3(cdiv(max_span, 1024), kv->Hkv, kv->B), 256, 0, st>>>(
       *kv, aux, aux_stride, w);

@@ -13,7 +13,7 @@
 // (entry, head) and a base-2 online softmax.  Half-warp states merge in
 // shared memory; a second kernel merges the chunks and, for H2O, adds
 // sum_h p_{h,j} to the running scores from the logits the first kernel stored.
-#include "se_common.cuh"
+#include "tc_primitives.cuh"
 
 namespace se {
 
@@ -96,7 +96,7 @@ SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
 // lane accumulates p * v for its dims.  o is rescaled only when a head's
 // maximum grows.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) {
   constexpr int V = D / 16;        // dims per lane
   constexpr int E = 16 / G;        // entries per half-warp iteration
   static_assert(E * G == 16, "G must divide 16");
@@ -263,6 +263,283 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
   }
 }
 
+
+// Bulk copy global -> shared (the TMA engine, no tensor map), completing on
+// an mbarrier; the byte count is added to the barrier's expected total first.
+SE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+template <typename T, int D, int G>
+struct StagedGeom {
+  static constexpr int V = D / 16;                 // dims per lane
+  static constexpr int E = 16 / G;                 // entries per half-warp per stage
+  static constexpr int SE = 8 * E;                 // entries per stage
+  static constexpr int RB = D * (int)sizeof(T);    // bytes per K (or V) row
+  static constexpr int STAGE_BYTES = SE * RB * 2;
+  static constexpr int STAGES = STAGE_BYTES <= 16384 ? 4 : (STAGE_BYTES <= 32768 ? 2 : 0);
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+};
+
+// Issues the copies of stage `it` (view entries [s0, s0 + SE)) of (b, g):
+// runs of consecutive rows inside one page become one K and one V copy.
+template <typename T, int D, int G>
+SE_DEV void issue_stage(const DecodeArgs& a, int b, int g, int ctx, int s0, int e_end,
+                        uint8_t* dst, uint64_t* bar) {
+  using Gm = StagedGeom<T, D, G>;
+  const se_paged_kv& kv = a.kv;
+  const int P = kv.page_size;
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  const char* kp = static_cast<const char*>(kv.k_pool);
+  const char* vp = static_cast<const char*>(kv.v_pool);
+  int u = 0;
+  while (u < Gm::SE) {
+    const int e = s0 + u;
+    const int slot = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
+    if (slot < 0) { ++u; continue; }
+    // extend the run while the next entries are the next rows of the same page
+    int len = 1;
+    if (a.view != SE_VIEW_TOKENS) {
+      while (u + len < Gm::SE && (slot % P) + len < P && e + len < e_end) {
+        const int nxt = view_slot(a, b, g, e + len, ctx);
+        if (nxt != slot + len) break;
+        ++len;
+      }
+    }
+    const int page = bt[slot / P];
+    if (page >= 0 && page < kv.num_pages) {
+      const int64_t off = (((int64_t)page * kv.Hkv + g) * P + slot % P) * Gm::RB;
+      bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
+      bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
+    }
+    u += len;
+  }
+  tc::mbar_arrive(bar);
+}
+
+// grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps; dynamic smem
+// StagedGeom::SMEM.  Lane 0 of warp 0 keeps STAGES-1 stages of copies in
+// flight; every half-warp reads its E rows of each stage from shared memory
+// (16 lanes x 16 bytes = one 256-byte row, conflict-free) and runs the same
+// reduce-scatter / online-softmax arithmetic as the register kernel above.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
+  using Gm = StagedGeom<T, D, G>;
+  constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[4], empty[4];
+  __shared__ float s_p[8][16];
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ int s_abort;
+  static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const se_paged_kv& kv = a.kv;
+  const int ctx = kv.ctx_len[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int my_e = t / G, my_h = t % G;
+  const int n_view = min(view_entries(a, ctx), a.max_entries);
+  const int e_begin = c * a.chunk;
+  const int e_end = min(e_begin + a.chunk, n_view);
+  const int n_it = e_end > e_begin ? cdiv(e_end - e_begin, SE) : 0;
+  const unsigned full_mask = 0xffffffffu;
+  constexpr uint64_t kLimit = 2000000000ull;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 4);
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  const bool producer = threadIdx.x == 0;
+  if (producer)
+    for (int i = 0; i < min(S - 1, n_it); ++i)
+      issue_stage<T, D, G>(a, b, g, ctx, e_begin + i * SE, e_end, stages + i * Gm::STAGE_BYTES, &full[i]);
+
+  const float qscale = kLog2e * rsqrtf((float)D);
+  float q[G][V];
+  const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+    for (int i = 0; i < V; ++i) q[j][i] *= qscale;
+  }
+  float m[G], o[G][V];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) o[j][i] = 0.f;
+  }
+  float l_own = 0.f;
+  float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
+  int issued = min(S - 1, n_it);
+
+  for (int it = 0; it < n_it; ++it) {
+    const int s = it % S;
+    if (producer && issued < n_it) {
+      // refill the stage consumed in the previous iteration
+      const int ps = issued % S;
+      if (issued < S || tc::mbar_wait(&empty[ps], ((issued / S) - 1) & 1, kLimit)) {
+        issue_stage<T, D, G>(a, b, g, ctx, e_begin + issued * SE, e_end,
+                             stages + ps * Gm::STAGE_BYTES, &full[ps]);
+        ++issued;
+      } else {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(&s_abort, 1);
+      }
+    }
+    const bool ok_wait = tc::mbar_wait(&full[s], (it / S) & 1, kLimit);
+    if (!__all_sync(full_mask, ok_wait)) {
+      if (lane == 0) {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(&s_abort, 1);
+      }
+      break;
+    }
+    const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
+    const uint8_t* vst = kst + SE * RB;
+    const int e0 = e_begin + it * SE + hw * E;
+    float kf[E][V], vf[E][V];
+    bool valid[E];
+#pragma unroll
+    for (int u = 0; u < E; ++u) {
+      const int e = e0 + u;
+      valid[u] = e < e_end && view_slot(a, b, g, e, ctx) >= 0;
+      if (valid[u]) {
+        const T* kr = reinterpret_cast<const T*>(kst + (hw * E + u) * RB) + t * V;
+        const T* vr = reinterpret_cast<const T*>(vst + (hw * E + u) * RB) + t * V;
+        if constexpr (sizeof(T) == 2 && V == 8) {
+          unpack8_bf16(*reinterpret_cast<const uint4*>(kr), kf[u]);
+          unpack8_bf16(*reinterpret_cast<const uint4*>(vr), vf[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) { kf[u][i] = (float)kr[i]; vf[u][i] = (float)vr[i]; }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) { kf[u][i] = 0.f; vf[u][i] = 0.f; }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[s]);   // rows are in registers now
+    float part[16];
+#pragma unroll
+    for (int u = 0; u < E; ++u)
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[u][i], acc);
+        part[u * G + j] = acc;
+      }
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+      const int off = 8 >> step;
+      const int n = 8 >> step;
+      const bool upper = (t & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n; ++i) {
+        const float lo = part[i], hi = part[i + n];
+        part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
+      }
+    }
+    bool ok = false;
+#pragma unroll
+    for (int u = 0; u < E; ++u) ok = (u == my_e) ? valid[u] : ok;
+    const float sv = ok ? part[0] : -INFINITY;
+    if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+    float tmax = sv;
+#pragma unroll
+    for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
+    float m_mine = m[0];
+#pragma unroll
+    for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+    const float mn_mine = fmaxf(m_mine, tmax);
+    const float alpha_mine = (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+    const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+    l_own = fmaf(l_own, alpha_mine, p);
+    s_p[hw][t] = p;
+    bool grew = false;
+    float alpha[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
+      alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
+      grew |= mj != m[j];
+      m[j] = mj;
+    }
+    __syncwarp();
+    if (grew) {
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[j][i] *= alpha[j];
+    }
+#pragma unroll
+    for (int u = 0; u < E; ++u) {
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float pu = s_p[hw][u * G + j];
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[j][i] = fmaf(pu, vf[u][i], o[j][i]);
+      }
+    }
+    __syncwarp();
+  }
+  // drain copies still in flight (only after a timeout)
+  if (producer)
+    for (int i = 0; i < issued; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
+  float lsum = l_own;
+#pragma unroll
+  for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
+  if (t < G) {
+    float mt = m[0];
+#pragma unroll
+    for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+    s_m[hw][t] = mt;
+    s_l[hw][t] = lsum;
+  }
+  __syncthreads();   // every stage has been read: reuse the stage memory
+  float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int i = 0; i < V; ++i) s_o[hw][j][t * V + i] = o[j][i];
+  __syncthreads();
+  float* part = a.part + (((int64_t)b * kv.Hkv + g) * a.n_chunks + c) * G * (D + 2);
+  for (int x = threadIdx.x; x < G * D; x += 128) {
+    const int j = x / D, d = x % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w][j]);
+    float acc = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float f = ex2(s_m[w][j] - M);
+        acc = fmaf(s_o[w][j][d], f, acc);
+        L = fmaf(s_l[w][j], f, L);
+      }
+    }
+    part[j * (D + 2) + d] = acc;
+    if (d == 0) {
+      part[j * (D + 2) + D] = M;
+      part[j * (D + 2) + D + 1] = L;
+    }
+  }
+}
+
 // grid: (Hkv, B); 128 threads.  Merges chunks, writes o, updates acc.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a, T* out, float* acc,
@@ -344,7 +621,20 @@ static int pick_chunk(const se_paged_kv* kv, int max_entries) {
 template <typename T, int D, int G>
 static void launch_decode_t(const DecodeArgs& a, void* o, float* acc, int64_t acc_stride,
                             cudaStream_t st) {
-  decode_partial_kernel<T, D, G><<<dim3(a.n_chunks, a.kv.Hkv, a.kv.B), 128, 0, st>>>(a);
+  using Gm = StagedGeom<T, D, G>;
+  const dim3 grid(a.n_chunks, a.kv.Hkv, a.kv.B);
+  bool staged = Gm::STAGES > 0;
+  if constexpr (Gm::STAGES > 0) {
+    static bool attr = false;
+    if (!attr) {
+      attr = cudaFuncSetAttribute(decode_partial_kernel<T, D, G>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Gm::SMEM) == cudaSuccess;
+      staged = attr;
+    }
+    if (staged) decode_partial_kernel<T, D, G><<<grid, 128, Gm::SMEM, st>>>(a);
+  }
+  if (!staged) decode_partial_regs_kernel<T, D, G><<<grid, 128, 0, st>>>(a);
   decode_combine_kernel<T, D, G><<<dim3(a.kv.Hkv, a.kv.B), 128, 0, st>>>(a, static_cast<T*>(o),
                                                                           acc, acc_stride);
 }

@@ -26,6 +26,8 @@
 // SE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "tc_primitives.cuh"
 
 namespace se {
@@ -300,7 +302,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             s0 += tc::ex2(fmaf(v[j], a.scale, -mn));
             s1 += tc::ex2(fmaf(v[j + 1], a.scale, -mn));
             s2 += tc::ex2(fmaf(v[j + 2], a.scale, -mn));
-            s3 += tc::ex2(fmaf(v[j + 3], a.scale, -mn));
+            s3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -mn));   // 1 in 4 on the FMA pipe
           }
           l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
           m = mn;
@@ -616,7 +618,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
               cs0 += tc::ex2(fmaf(v[j], a.scale, -l4.x));
               cs1 += tc::ex2(fmaf(v[j + 1], a.scale, -l4.y));
               cs2 += tc::ex2(fmaf(v[j + 2], a.scale, -l4.z));
-              cs3 += tc::ex2(fmaf(v[j + 3], a.scale, -l4.w));
+              cs3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -l4.w));   // 1 in 4 on the FMA pipe
             }
           } else {
 #pragma unroll
@@ -656,6 +658,566 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
 }
 
+
+SE_DEV int group_tiles(const TcArgs& a, int bg) {
+  const TileGeom tg = TileGeom::make(a, bg / a.Hkv);
+  return geom_ok(a, tg) ? tg.n_tiles : 0;
+}
+
+// Position of global tile index x: group and tile within it.
+SE_DEV void locate(const TcArgs& a, int x, int& bg, int& tile) {
+  bg = 0;
+  int base = 0;
+  const int groups = a.B * a.Hkv;
+  while (bg < groups) {
+    const int n = group_tiles(a, bg);
+    if (x < base + n) break;
+    base += n;
+    ++bg;
+  }
+  tile = x - base;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1, persistent form for one row chunk (RC == 1).  grid = the number of
+// SMs; CTA c takes tiles [c T / C, (c+1) T / C) of the global (group, tile)
+// sequence.  Each epilogue thread keeps its row's running max / sum per group
+// and writes it, when the group ends in this CTA, to the partial slot of this
+// CTA: part[(group * 256 + row) * C + c].  score_rowinfo_persistent merges the
+// slots of the CTAs whose ranges meet the group.
+// ---------------------------------------------------------------------------
+SE_DEV int total_tiles(const TcArgs& a) {
+  int total = 0;
+  for (int bg = 0; bg < a.B * a.Hkv; ++bg) total += group_tiles(a, bg);
+  return total;
+}
+
+// The CTA whose range [c T / C, (c+1) T / C) holds tile x.
+SE_DEV int cta_of(int64_t x, int64_t T, int64_t C) { return (int)(((x + 1) * C - 1) / T); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap qmap, TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int KS = kStages1;
+  uint8_t* q_s = smem;
+  uint8_t* k_s = q_s + kQChunkBytes;
+  int32_t* pos_s = reinterpret_cast<int32_t*>(k_s + KS * kKTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pos_s + KS * kKeyTile);
+  uint64_t* full = bars;             // [KS]
+  uint64_t* empty = bars + 4;        // [KS]
+  uint64_t* pos_free = bars + 8;     // [KS]
+  uint64_t* acc_full = bars + 12;    // [2]
+  uint64_t* acc_free = bars + 14;    // [2]
+  uint64_t* q_full = bars + 16;
+  uint64_t* q_done = bars + 17;
+  uint64_t* done = bars + 18;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_range[2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    const int total = total_tiles(a);
+    s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
+    s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    for (int i = 0; i < KS; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&pos_free[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_free[i], kEpiWarps);
+    }
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_done, 1);
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int x0 = s_range[0], x1 = s_range[1];
+  const int n_my = x1 - x0;
+
+  if (warp == 0) {
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
+      int bg = 0, tile = 0;
+      locate(a, x0, bg, tile);
+      int cur = -1, gi = 0, issued = 0;
+      for (int i = 0; i < n_my && !aborted(&s_abort); ++i) {
+        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        const int b = bg / a.Hkv, g = bg % a.Hkv;
+        if (bg != cur) {
+          if (gi > 0 && !tc::mbar_wait(q_done, (gi - 1) & 1, kTimeoutNs)) {
+            record_timeout(a, &s_abort);
+            break;
+          }
+          load_q_chunk(a, &qmap, b, g, 0, q_s, q_full);
+          cur = bg;
+          ++gi;
+        }
+        const int s = i % KS;
+        const uint32_t par = ((i / KS) & 1) ^ 1;
+        if (i >= KS && (!tc::mbar_wait(&empty[s], par, kTimeoutNs) ||
+                        !tc::mbar_wait(&pos_free[s], par, kTimeoutNs))) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        const TileGeom tg = TileGeom::make(a, b);
+        load_k_tile(a, &kmap, tg, b, g, tile, k_s + s * kKTileBytes,
+                    a.causal ? pos_s + s * kKeyTile : nullptr, &full[s]);
+        issued = i + 1;
+        ++tile;
+      }
+      for (int i = max(0, issued - KS); i < issued; ++i)
+        tc::mbar_wait(&full[i % KS], (i / KS) & 1, kTimeoutNs);
+      if (gi > 0) tc::mbar_wait(q_full, (gi - 1) & 1, kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    if (tc::elect_one()) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, kKeyTile);
+      int bg = 0, tile = 0;
+      locate(a, x0, bg, tile);
+      int cur = -1, gi = 0;
+      for (int i = 0; i < n_my && !aborted(&s_abort); ++i) {
+        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        if (bg != cur) {
+          if (gi > 0) tc::mma_commit(q_done);
+          if (!tc::mbar_wait(q_full, gi & 1, kTimeoutNs)) {
+            record_timeout(a, &s_abort);
+            break;
+          }
+          cur = bg;
+          ++gi;
+        }
+        const int s = i % KS;
+        const int acc = i & 1;
+        if (!tc::mbar_wait(&full[s], (i / KS) & 1, kTimeoutNs) ||
+            (i >= 2 && !tc::mbar_wait(&acc_free[acc], ((i >> 1) & 1) ^ 1, kTimeoutNs))) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t kbase = tc::smem_u32(k_s + s * kKTileBytes);
+        const uint32_t qbase = tc::smem_u32(q_s);
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = tc::smem_desc_sw128(qbase + (k >> 2) * (kQChunkBytes / 2) +
+                                                    mb * (128 * 128) + (k & 3) * 32);
+            const uint64_t bd = tc::smem_desc_sw128(kbase + (k >> 2) * (kKTileBytes / 2) + (k & 3) * 32);
+            tc::mma_bf16(tmem + acc * 256 + mb * 128, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&acc_full[acc]);
+        ++tile;
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0, kTimeoutNs);
+    }
+  } else {
+    const int e = warp - 2;
+    const int mb = e / 4;
+    const int quarter = warp & 3;
+    const int r = mb * 128 + quarter * 32 + lane;   // row of the group
+    const bool row_ok = r < a.rows;
+    int bg = 0, tile = 0;
+    locate(a, x0, bg, tile);
+    int cur = -1, qpos = -1;
+    float m = -INFINITY, l = 0.f;
+    for (int i = 0; i < n_my; ++i) {
+      while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+      const int b = bg / a.Hkv;
+      if (bg != cur) {
+        if (cur >= 0 && row_ok) {
+          float* p = a.part + (((int64_t)cur * kRowChunk + r) * gridDim.x + blockIdx.x) * 2;
+          p[0] = m;
+          p[1] = l;
+        }
+        m = -INFINITY;
+        l = 0.f;
+        qpos = row_ok ? a.q_pos[(int64_t)b * a.w + r / a.G] : -1;
+        cur = bg;
+      }
+      const int s = i % KS;
+      const int acc = i & 1;
+      bool w_ok = tc::mbar_wait(&acc_full[acc], (i >> 1) & 1, kTimeoutNs);
+      if (w_ok && a.causal) w_ok = tc::mbar_wait(&full[s], (i / KS) & 1, kTimeoutNs);
+      if (!__all_sync(0xffffffffu, w_ok)) {
+        record_timeout(a, &s_abort);
+        break;
+      }
+      tc::tc_fence_after();
+      const TileGeom tg = TileGeom::make(a, b);
+      const int key0 = tg.base + tile * kKeyTile;
+      const int32_t* pos = pos_s + s * kKeyTile;
+      bool fast = row_ok && key0 >= tg.lo && key0 + kKeyTile <= tg.hi;
+      if (a.causal) {
+        const int4 p4 = reinterpret_cast<const int4*>(pos)[lane];
+        int mx = max(max(p4.x, p4.y), max(p4.z, p4.w));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        fast = fast && mx <= qpos;
+      }
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float v[64];
+        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 64, v);
+        if (fast) {
+          float c0 = v[0], c1 = v[1], c2 = v[2], c3 = v[3];
+#pragma unroll
+          for (int j = 4; j < 64; j += 4) {
+            c0 = fmaxf(c0, v[j]); c1 = fmaxf(c1, v[j + 1]);
+            c2 = fmaxf(c2, v[j + 2]); c3 = fmaxf(c3, v[j + 3]);
+          }
+          const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * a.scale);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            s0 += tc::ex2(fmaf(v[j], a.scale, -mn));
+            s1 += tc::ex2(fmaf(v[j + 1], a.scale, -mn));
+            s2 += tc::ex2(fmaf(v[j + 2], a.scale, -mn));
+            s3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -mn));   // 1 in 4 on the FMA pipe
+          }
+          l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
+          m = mn;
+          continue;
+        }
+        float c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int key = key0 + c * 64 + j;
+          bool vis = row_ok && key >= tg.lo && key < tg.hi;
+          if (a.causal) vis = vis && pos[c * 64 + j] <= qpos;
+          v[j] = vis ? v[j] * a.scale : -INFINITY;
+          if (j & 1) c1 = fmaxf(c1, v[j]); else c0 = fmaxf(c0, v[j]);
+        }
+        const float cm = fmaxf(c0, c1);
+        if (cm != -INFINITY) {
+          const float mn = fmaxf(m, cm);
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            s0 += tc::ex2(v[j] - mn);
+            s1 += tc::ex2(v[j + 1] - mn);
+          }
+          l = l * tc::ex2(m - mn) + (s0 + s1);
+          m = mn;
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&acc_free[acc]);
+        tc::mbar_arrive(&pos_free[s]);
+      }
+      ++tile;
+    }
+    if (cur >= 0 && row_ok) {
+      float* p = a.part + (((int64_t)cur * kRowChunk + r) * gridDim.x + blockIdx.x) * 2;
+      p[0] = m;
+      p[1] = l;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Row info for the persistent passes: merges the partial slots of the CTAs
+// whose tile ranges meet the group.  grid (1, B*Hkv), 256 threads.
+__global__ void score_rowinfo_persistent_tc(TcArgs a, int n_ctas) {
+  const int bg = blockIdx.y, b = bg / a.Hkv;
+  const int row = threadIdx.x;
+  __shared__ int s_first, s_last;
+  if (threadIdx.x == 0) {
+    int64_t T = 0, gstart = 0;
+    for (int x = 0; x < a.B * a.Hkv; ++x) {
+      const int n = group_tiles(a, x);
+      if (x < bg) gstart += n;
+      T += n;
+    }
+    const int n = group_tiles(a, bg);
+    s_first = (n > 0 && T > 0) ? cta_of(gstart, T, n_ctas) : 0;
+    s_last = (n > 0 && T > 0) ? cta_of(gstart + n - 1, T, n_ctas) : -1;
+  }
+  __syncthreads();
+  float lse = INFINITY;
+  int qpos = 0x7fffffff;
+  if (row < a.rows) {
+    const float* p = a.part + ((int64_t)bg * kRowChunk + row) * n_ctas * 2;
+    float M = -INFINITY;
+    for (int c = s_first; c <= s_last; ++c) M = fmaxf(M, p[2 * c]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int c = s_first; c <= s_last; ++c) L += p[2 * c + 1] * exp2f(p[2 * c] - M);
+    if (L > 0.f) lse = M + log2f(L);
+    qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
+  }
+  float* chunk = reinterpret_cast<float*>(a.rowinfo + (int64_t)bg * kRowChunk);
+  chunk[row] = lse;
+  chunk[kRowChunk + row] = __int_as_float(qpos);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2, persistent form for one row chunk (RC == 1: w * G <= 256 rows).
+// grid = the number of SMs; CTA c takes an equal contiguous share of the
+// global sequence of (group, key tile) pairs, so the last wave is full and the
+// pipeline runs across tiles of consecutive groups without refilling.  The Q
+// chunk and row info of a group are loaded when the group changes (after the
+// MMA and both epilogue sets are done with the previous ones).  Epilogue warps
+// 2-5 take the CTA's even local tiles (TMEM buffer 0), warps 6-9 the odd ones.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap qmap, TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int KS = 4;
+  uint8_t* q_s = smem;
+  uint8_t* k_s = q_s + kQChunkBytes;
+  int32_t* pos_s = reinterpret_cast<int32_t*>(k_s + KS * kKTileBytes);   // [KS][128]
+  float2* info_s = reinterpret_cast<float2*>(pos_s + KS * kKeyTile);     // [256]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(info_s + kRowChunk);
+  uint64_t* kfull = bars;            // [KS]
+  uint64_t* kempty = bars + 4;       // [KS]
+  uint64_t* pfree = bars + 8;        // [KS]
+  uint64_t* qfull = bars + 12;
+  uint64_t* qdone = bars + 13;       // MMA done with the group's Q
+  uint64_t* ifree = bars + 14;       // both epilogue sets done with the group's row info
+  uint64_t* acc_full = bars + 15;    // [2]
+  uint64_t* acc_free = bars + 17;    // [2]
+  uint64_t* done = bars + 19;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_range[2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    int total = 0;
+    for (int bg = 0; bg < a.B * a.Hkv; ++bg) total += group_tiles(a, bg);
+    s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
+    s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    for (int i = 0; i < KS; ++i) {
+      tc::mbar_init(&kfull[i], 1);
+      tc::mbar_init(&kempty[i], 1);
+      tc::mbar_init(&pfree[i], 4);
+    }
+    tc::mbar_init(qfull, 1);
+    tc::mbar_init(qdone, 1);
+    tc::mbar_init(ifree, kEpiWarps);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_free[i], 4);
+    }
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int x0 = s_range[0], x1 = s_range[1];
+  const int n_my = x1 - x0;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
+      int bg = 0, tile = 0;
+      locate(a, x0, bg, tile);
+      int cur = -1, gi = 0, issued = 0;
+      for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
+        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        const int b = bg / a.Hkv, g = bg % a.Hkv;
+        if (bg != cur) {
+          if (gi > 0 && (!tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs) ||
+                         !tc::mbar_wait(ifree, (gi - 1) & 1, kTimeoutNs))) {
+            record_timeout(a, &s_abort);
+            break;
+          }
+          tc::mbar_arrive_expect_tx(qfull, kQChunkBytes + kRowChunk * 8);
+          const int qpc = kRowChunk / a.G;
+          (void)qpc;
+          tc::tma_load_4d(q_s, &qmap, qfull, 0, g * a.G, 0, b);
+          tc::tma_load_4d(q_s + kQChunkBytes / 2, &qmap, qfull, 64, g * a.G, 0, b);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+              ::"r"(tc::smem_u32(info_s)), "l"(a.rowinfo + (int64_t)bg * kRowChunk),
+              "r"(kRowChunk * 8), "r"(tc::smem_u32(qfull))
+              : "memory");
+          cur = bg;
+          ++gi;
+        }
+        const int s = lt % KS;
+        const uint32_t par = ((lt / KS) & 1) ^ 1;
+        if (lt >= KS && (!tc::mbar_wait(&kempty[s], par, kTimeoutNs) ||
+                         !tc::mbar_wait(&pfree[s], par, kTimeoutNs))) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        const TileGeom tg = TileGeom::make(a, b);
+        load_k_tile(a, &kmap, tg, b, g, tile, k_s + s * kKTileBytes,
+                    a.causal ? pos_s + s * kKeyTile : nullptr, &kfull[s]);
+        issued = lt + 1;
+        ++tile;
+      }
+      for (int i = max(0, issued - KS); i < issued; ++i)
+        tc::mbar_wait(&kfull[i % KS], (i / KS) & 1, kTimeoutNs);
+      if (gi > 0) tc::mbar_wait(qfull, (gi - 1) & 1, kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (tc::elect_one()) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, kRowChunk);
+      int bg = 0, tile = 0;
+      locate(a, x0, bg, tile);
+      int cur = -1, gi = 0;
+      int uses[2] = {0, 0};
+      for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
+        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        if (bg != cur) {
+          if (gi > 0) tc::mma_commit(qdone);       // previous group's MMAs read its Q
+          if (!tc::mbar_wait(qfull, gi & 1, kTimeoutNs)) {
+            record_timeout(a, &s_abort);
+            break;
+          }
+          cur = bg;
+          ++gi;
+        }
+        const int s = lt % KS;
+        const int buf = lt & 1;
+        bool w_ok = tc::mbar_wait(&kfull[s], (lt / KS) & 1, kTimeoutNs);
+        if (w_ok && uses[buf] > 0) w_ok = tc::mbar_wait(&acc_free[buf], (uses[buf] - 1) & 1, kTimeoutNs);
+        if (!w_ok) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t kbase = tc::smem_u32(k_s + s * kKTileBytes);
+        const uint32_t qbase = tc::smem_u32(q_s);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ad = tc::smem_desc_sw128(kbase + (k >> 2) * (kKTileBytes / 2) + (k & 3) * 32);
+          const uint64_t bd = tc::smem_desc_sw128(qbase + (k >> 2) * (kQChunkBytes / 2) + (k & 3) * 32);
+          tc::mma_bf16(tmem + buf * 256, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&kempty[s]);
+        tc::mma_commit(&acc_full[buf]);
+        uses[buf]++;
+        ++tile;
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0, kTimeoutNs);
+    }
+  } else {
+    // ---------------- epilogue: one key per thread ----------------
+    const int set = (warp - 2) / 4;
+    const int quarter = warp & 3;
+    const int kl = quarter * 32 + lane;
+    int bg = 0, tile = 0;
+    locate(a, x0, bg, tile);
+    int cur = -1, gi = 0, use = 0;
+    for (int lt = 0; lt < n_my; ++lt) {
+      while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+      if (bg != cur) {
+        // leaving a group: both sets release its row info
+        if (gi > 0) {
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(ifree);
+        }
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(qfull, gi & 1, kTimeoutNs))) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        cur = bg;
+        ++gi;
+      }
+      if ((lt & 1) != set) { ++tile; continue; }
+      const int b = bg / a.Hkv;
+      const int s = lt % KS;
+      bool w_ok = tc::mbar_wait(&acc_full[set], use & 1, kTimeoutNs);
+      if (w_ok && a.causal) w_ok = tc::mbar_wait(&kfull[s], (lt / KS) & 1, kTimeoutNs);
+      if (!__all_sync(0xffffffffu, w_ok)) {
+        record_timeout(a, &s_abort);
+        break;
+      }
+      tc::tc_fence_after();
+      const int kpos = a.causal ? pos_s[s * kKeyTile + kl] : 0;
+      const float* lse_s = reinterpret_cast<const float*>(info_s);
+      const int* qp_s = reinterpret_cast<const int*>(lse_s + kRowChunk);
+      bool fast = !a.causal;
+      if (a.causal) {
+        const int4 q4a = reinterpret_cast<const int4*>(qp_s)[lane * 2];
+        const int4 q4b = reinterpret_cast<const int4*>(qp_s)[lane * 2 + 1];
+        int mn = min(min(min(q4a.x, q4a.y), min(q4a.z, q4a.w)), min(min(q4b.x, q4b.y), min(q4b.z, q4b.w)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        fast = kpos <= mn;
+      }
+      float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[64];
+        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 64, v);
+        if (fast) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c * 64 + j);
+            cs0 += tc::ex2(fmaf(v[j], a.scale, -l4.x));
+            cs1 += tc::ex2(fmaf(v[j + 1], a.scale, -l4.y));
+            cs2 += tc::ex2(fmaf(v[j + 2], a.scale, -l4.z));
+            cs3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -l4.w));   // 1 in 4 on the FMA pipe
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            float p0 = tc::ex2(fmaf(v[j], a.scale, -lse_s[c * 64 + j]));
+            float p1 = tc::ex2(fmaf(v[j + 1], a.scale, -lse_s[c * 64 + j + 1]));
+            if (kpos > qp_s[c * 64 + j]) p0 = 0.f;
+            if (kpos > qp_s[c * 64 + j + 1]) p1 = 0.f;
+            cs0 += p0;
+            cs1 += p1;
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&acc_free[set]);
+        tc::mbar_arrive(&pfree[s]);
+      }
+      ++use;
+      const TileGeom tg = TileGeom::make(a, b);
+      const int key = tg.base + tile * kKeyTile + kl;
+      const float colsum = (cs0 + cs1) + (cs2 + cs3);
+      if (key >= a.out_lo[b] && key < a.out_hi[b] && key >= tg.lo && key < tg.hi &&
+          key < a.scores_stride) {
+        float* out = a.scores + (int64_t)bg * a.scores_stride + key;
+        *out = a.accumulate ? *out + colsum : colsum;
+      }
+      ++tile;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -713,10 +1275,13 @@ bool score_tc_supported(const se_paged_kv* kv) {
          (int64_t)kv->num_pages * kv->Hkv * kv->page_size < (int64_t)1 << 31;
 }
 
+constexpr int kMaxPersistentCTAs = 256;   // partial slots per row of the persistent pass 1
+
 size_t score_tc_ws(const se_paged_kv* kv, int w, int n_max) {
   const TcPlan p = plan(kv, w, n_max);
   WsCarver c(nullptr);
-  c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * p.n_splits * 2);
+  const int slots = p.RC == 1 ? std::max(p.n_splits, kMaxPersistentCTAs) : p.n_splits;
+  c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
   return c.bytes();
 }
@@ -761,7 +1326,8 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
   a.causal = causal; a.accumulate = accumulate; a.n_max = n_max;
   a.scores = scores; a.scores_stride = scores_stride;
   WsCarver c(ws);
-  a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * p.n_splits * 2);
+  const int slots = p.RC == 1 ? std::max(p.n_splits, kMaxPersistentCTAs) : p.n_splits;
+  a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   a.rowinfo = c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
   a.n_splits = p.n_splits; a.tiles_per_split = p.tiles_per_split;
   a.tiles_per_cta2 = p.tiles_per_cta2;
@@ -772,15 +1338,35 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
     if (cudaFuncSetAttribute(score_rowstats_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmem1) != cudaSuccess ||
         cudaFuncSetAttribute(score_colsum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem2) != cudaSuccess)
+                             (int)kSmem2) != cudaSuccess ||
+        cudaFuncSetAttribute(score_colsum_persistent_tc,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem2Resident) != cudaSuccess ||
+        cudaFuncSetAttribute(score_rowstats_persistent_tc,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem1) != cudaSuccess)
       return SE_ERR_CUDA;
     attrs = true;
   }
   const int groups = kv->B * kv->Hkv;
+  if (p.RC == 1) {
+    // one row chunk: persistent CTAs, one per SM, over the (group, tile) sequence
+    static int n_sm = 0;
+    if (n_sm == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SE_ERR_CUDA;
+    }
+    const int ctas = std::min(std::min(n_sm, kMaxPersistentCTAs), groups * p.n_tiles_max);
+    score_rowstats_persistent_tc<<<ctas, kThreads, kSmem1, st>>>(kmap, qmap, a);
+    score_rowinfo_persistent_tc<<<dim3(1, groups), kRowChunk, 0, st>>>(a, ctas);
+    score_colsum_persistent_tc<<<ctas, kThreads, kSmem2Resident, st>>>(kmap, qmap, a);
+    return SE_OK;
+  }
   score_rowstats_tc<<<dim3(p.n_splits, p.RC, groups), kThreads, kSmem1, st>>>(kmap, qmap, a);
   score_rowinfo_tc<<<dim3(cdiv(p.RC * kRowChunk, 256), groups), 256, 0, st>>>(a);
-  const size_t smem2 = p.RC == 1 ? kSmem2Resident : kSmem2;
-  score_colsum_tc<<<dim3(cdiv(p.n_tiles_max, p.tiles_per_cta2), groups), kThreads, smem2, st>>>(
+  score_colsum_tc<<<dim3(cdiv(p.n_tiles_max, p.tiles_per_cta2), groups), kThreads, kSmem2, st>>>(
       kmap, qmap, a);
   return SE_OK;
 }

@@ -5,14 +5,16 @@
 //             top pages): avg-pool over the candidate range, rank by (score
 //             desc, slot asc), keep k plus a forced range.  One CTA per
 //             (sequence, head): scores staged in shared memory, pooled into
-//             order-preserving integer keys held in registers, an 8-bit
-//             4-pass block radix select finds the k-th key, and two block
-//             scans emit the kept slots in ascending order.
+//             order-preserving integer keys held in registers, a 3-pass
+//             (11/11/10-bit) block radix select finds the k-th key, and two
+//             block scans emit the kept slots in ascending order.
 // KARA_CHUNK  KARA Method 1-2 (top-K candidates, Token2Chunk): one warp per
 //             (sequence, head); candidates, chunk scores, greedy fill and
 //             top-up are warp argmax rounds over registers.
 // EVICT_ONE   SparseEngine "What it is" (H2O persistent scores + physical
 //             eviction): one warp per (sequence, head) argmin.
+#include <cooperative_groups.h>
+
 #include "se_common.cuh"
 
 namespace se {
@@ -39,7 +41,7 @@ template <int ITEMS>
 __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, int k) {
   extern __shared__ float s_sc[];
   __shared__ int tmp[33];
-  __shared__ int hist[256];
+  __shared__ int hist[2048];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   __shared__ int s_before_force;
@@ -91,52 +93,51 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   const int ncand = n - forced_in_total;
   const int kk = min(max(k, 0), ncand);
 
-  // 4 rounds of 8-bit radix select for the kk-th largest key.
+  // 3 rounds of radix select (digits of 11, 11 and 10 bits, top first) for
+  // the kk-th largest key.  Wide digits spread scores that share an exponent.
   uint32_t prefix = 0, pmask = 0;
   int remaining = kk;
   if (kk > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += 1024) hist[i] = 0;
+#pragma unroll 1
+    for (int round = 0; round < 3; ++round) {
+      const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+      const int nbins = round == 2 ? 1024 : 2048;
+      const uint32_t dmask = (uint32_t)nbins - 1u;
+      for (int i = tid; i < nbins; i += 1024) hist[i] = 0;
       __syncthreads();
-      // warp-aggregated histogram: lanes holding the same digit add once
-      // (scores cluster in a few exponents, so plain atomics would serialise)
 #pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const bool in = key[i] != 0u && (key[i] & pmask) == prefix;
-        const uint32_t bin = in ? ((key[i] >> shift) & 255u) : 256u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (in && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
-      }
+      for (int i = 0; i < ITEMS; ++i)
+        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
       __syncthreads();
       if (tid < 32) {
-        // lane l owns bins [8l, 8l+8); suffix sums from the top bin down
-        int cnt[8], tot = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { cnt[j] = hist[tid * 8 + j]; tot += cnt[j]; }
+        // lane l owns bins [l*per, (l+1)*per); suffix sums from the top bin down
+        const int per = nbins / 32;
+        int tot = 0;
+        for (int j = 0; j < per; ++j) tot += hist[tid * per + j];
         int suf = tot;  // inclusive suffix over lanes >= tid
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_down_sync(0xffffffffu, suf, o);
           if (tid + o < 32) suf += y;
         }
-        const int above = suf - tot;  // elements in higher lanes' bins
-        const bool mine = above < remaining && suf >= remaining;
-        if (mine) {
+        const int above = suf - tot;
+        if (above < remaining && suf >= remaining) {
           int acc = above;
-          for (int j = 7; j >= 0; --j) {
-            if (acc + cnt[j] >= remaining) {
-              s_prefix = prefix | ((uint32_t)(tid * 8 + j) << shift);
+          for (int j = per - 1; j >= 0; --j) {
+            const int cnt = hist[tid * per + j];
+            if (acc + cnt >= remaining) {
+              s_prefix = prefix | ((uint32_t)(tid * per + j) << shift);
               s_remaining = remaining - acc;
               break;
             }
-            acc += cnt[j];
+            acc += cnt;
           }
         }
       }
       __syncthreads();
       prefix = s_prefix;
       remaining = s_remaining;
-      pmask |= 255u << shift;
+      pmask |= dmask << shift;
       __syncthreads();
     }
   }
@@ -185,6 +186,203 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   for (int f = tid; f < nf; f += 1024) out[before_force + f] = flo + f;
   for (int p = total_sel + nf + tid; p < a.keep_stride; p += 1024) out[p] = -1;
   if (h == 0 && tid == 0 && a.n_keep) a.n_keep[b] = total_sel + nf;
+}
+
+// --------------------------------------------------------------------------
+// Same selection split over a cluster of 4 CTAs per (sequence, head): CTA
+// rank r owns a quarter of the candidate range (plus a pooling halo), keeps
+// its keys in registers, and the cluster combines radix histograms, equal-key
+// ranks and output offsets through distributed shared memory.  Four times the
+// SMs of the one-CTA kernel for the few-instance, long-range case.
+// grid: (4 * Hkv, B), cluster (4, 1, 1), 1024 threads.
+// --------------------------------------------------------------------------
+constexpr int kClusterCTAs = 4;
+
+template <int ITEMS>
+__global__ void __cluster_dims__(kClusterCTAs, 1, 1) __launch_bounds__(1024, 1)
+topk_cluster_kernel(SelectArgs a, int pool, int k) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ float s_sc[];
+  __shared__ int tmp[33];
+  __shared__ int hist[2048];
+  __shared__ int s_cnt[4];        // forced-in-range, equal-to-T, selected, selected-before-force
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int rank = (int)cluster.block_rank();
+  const int h = blockIdx.x / kClusterCTAs, b = blockIdx.y, tid = threadIdx.x;
+  const int lo = a.cand_lo[b], hi = a.cand_hi[b];
+  const int flo = a.force_lo ? a.force_lo[b] : 0;
+  const int fhi = a.force_hi ? a.force_hi[b] : 0;
+  const int n = hi - lo;
+  const int nf = max(fhi - flo, 0);
+  const int per = cdiv(max(n, 1), kClusterCTAs);
+  const bool bad = n < 0 || per > 1024 * ITEMS;    // same for the whole cluster
+  const int r0 = min(rank * per, max(n, 0)), r1 = min(r0 + per, max(n, 0));
+  const int halo = pool / 2;
+  const float* row = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
+  // local smem index x <-> element r0 - halo + x
+  const int x1 = bad ? 0 : (r1 + halo) - (r0 - halo);
+  for (int x = tid; x < x1; x += 1024) {
+    const int e = r0 - halo + x;
+    s_sc[padded<ITEMS>(x)] = (e >= 0 && e < n) ? row[lo + e] : 0.f;
+  }
+  if (tid < 4) s_cnt[tid] = 0;
+  __syncthreads();
+
+  uint32_t key[ITEMS];
+  int n_forced_in = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int e = r0 + tid * ITEMS + i;
+    key[i] = 0u;
+    if (!bad && e < r1) {
+      const int slot = lo + e;
+      if (slot >= flo && slot < fhi) {
+        n_forced_in++;
+      } else {
+        const int x = e - r0 + halo;
+        float v;
+        if (pool > 1) {
+          float acc = 0.f;
+          for (int d = -halo; d <= halo; ++d) {
+            const int ee = e + d;
+            if (ee >= 0 && ee < n) acc += s_sc[padded<ITEMS>(x + d)];
+          }
+          v = acc / (float)pool;
+        } else {
+          v = s_sc[padded<ITEMS>(x)];
+        }
+        key[i] = float_key(v);
+      }
+    }
+  }
+  if (n_forced_in) atomicAdd(&s_cnt[0], n_forced_in);
+  cluster.sync();
+  int forced_in_total = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) forced_in_total += *cluster.map_shared_rank(&s_cnt[0], r);
+  const int ncand = n - forced_in_total;
+  const int kk = bad ? 0 : min(max(k, 0), ncand);
+
+  uint32_t prefix = 0, pmask = 0;
+  int remaining = kk;
+  if (kk > 0) {
+#pragma unroll 1
+    for (int round = 0; round < 3; ++round) {
+      const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+      const int nbins = round == 2 ? 1024 : 2048;
+      const uint32_t dmask = (uint32_t)nbins - 1u;
+      for (int i = tid; i < nbins; i += 1024) hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i)
+        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+      cluster.sync();                    // every CTA's histogram is complete
+      int tot_local[2] = {0, 0};
+      // each thread sums up to two bins over the cluster into registers
+      for (int j = 0; j < 2; ++j) {
+        const int bin = tid + j * 1024;
+        if (bin < nbins)
+          for (int r = 0; r < kClusterCTAs; ++r) tot_local[j] += *cluster.map_shared_rank(&hist[bin], r);
+      }
+      cluster.sync();                    // peers have read my histogram
+      for (int j = 0; j < 2; ++j)
+        if (tid + j * 1024 < nbins) hist[tid + j * 1024] = tot_local[j];
+      __syncthreads();
+      if (tid < 32) {
+        const int perl = nbins / 32;
+        int tot = 0;
+        for (int j = 0; j < perl; ++j) tot += hist[tid * perl + j];
+        int suf = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, suf, o);
+          if (tid + o < 32) suf += y;
+        }
+        const int above = suf - tot;
+        if (above < remaining && suf >= remaining) {
+          int acc = above;
+          for (int j = perl - 1; j >= 0; --j) {
+            const int cnt = hist[tid * perl + j];
+            if (acc + cnt >= remaining) {
+              s_prefix = prefix | ((uint32_t)(tid * perl + j) << shift);
+              s_remaining = remaining - acc;
+              break;
+            }
+            acc += cnt;
+          }
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      remaining = s_remaining;
+      pmask |= dmask << shift;
+      __syncthreads();
+    }
+  }
+  const uint32_t T = kk > 0 ? prefix : 0xffffffffu;
+  const int need_eq = kk > 0 ? remaining : 0;
+
+  // equal keys: cluster-wide rank in element order
+  int c_eq = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
+  int my_eq_total;
+  int eq_rank = block_exclusive_scan(c_eq, tmp, &my_eq_total);
+  if (tid == 0) s_cnt[1] = my_eq_total;
+  cluster.sync();
+  for (int r = 0; r < rank; ++r) eq_rank += *cluster.map_shared_rank(&s_cnt[1], r);
+  bool sel[ITEMS];
+  int c_sel = 0, c_sel_before_force = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    sel[i] = false;
+    if (key[i] != 0u) {
+      if (key[i] > T) {
+        sel[i] = true;
+      } else if (key[i] == T) {
+        sel[i] = eq_rank < need_eq;
+        eq_rank++;
+      }
+    }
+    c_sel += sel[i];
+    c_sel_before_force += (sel[i] && lo + r0 + tid * ITEMS + i < flo) ? 1 : 0;
+  }
+  int my_sel_total;
+  int pos = block_exclusive_scan(c_sel, tmp, &my_sel_total);
+  if (c_sel_before_force) atomicAdd(&s_cnt[3], c_sel_before_force);
+  if (tid == 0) s_cnt[2] = my_sel_total;
+  cluster.sync();
+  int total_sel = 0, before_force = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    const int cs = *cluster.map_shared_rank(&s_cnt[2], r);
+    if (r < rank) pos += cs;
+    total_sel += cs;
+    before_force += *cluster.map_shared_rank(&s_cnt[3], r);
+  }
+  cluster.sync();                        // no CTA leaves while peers read its counters
+  if (bad) {
+    if (rank == 0 && tid == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  if (total_sel + nf > a.keep_stride) {
+    if (rank == 0 && tid == 0) set_status(a.status, SE_ERR_BOUNDS);
+    return;
+  }
+  int32_t* out = a.keep + ((int64_t)b * a.Hkv + h) * a.keep_stride;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    if (sel[i]) {
+      const int slot = lo + r0 + tid * ITEMS + i;
+      out[pos + (slot >= fhi && nf > 0 ? nf : 0)] = slot;
+      pos++;
+    }
+  }
+  if (rank == 0) {
+    for (int f = tid; f < nf; f += 1024) out[before_force + f] = flo + f;
+    for (int p = total_sel + nf + tid; p < a.keep_stride; p += 1024) out[p] = -1;
+    if (h == 0 && tid == 0 && a.n_keep) a.n_keep[b] = total_sel + nf;
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -410,7 +608,32 @@ static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_
   return SE_OK;
 }
 
+template <int ITEMS>
+static se_status launch_topk_cluster_t(const SelectArgs& a, int pool, int k, cudaStream_t st) {
+  const size_t smem = (size_t)(1024 * (ITEMS + 1) + 64) * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_cluster_kernel<ITEMS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SE_ERR_CUDA;
+    attr_set = true;
+  }
+  topk_cluster_kernel<ITEMS><<<dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st>>>(a, pool, k);
+  return SE_OK;
+}
+
 se_status launch_topk(const SelectArgs& a, int pool, int k, int n_max, cudaStream_t st) {
+  // long candidate ranges: four CTAs per (sequence, head) in a cluster
+  if (n_max > 2048) {
+    const int items = cdiv(cdiv(n_max, kClusterCTAs) + 8, 1024);
+    if (items <= 2) return launch_topk_cluster_t<2>(a, pool, k, st);
+    if (items <= 4) return launch_topk_cluster_t<4>(a, pool, k, st);
+    if (items <= 8) return launch_topk_cluster_t<8>(a, pool, k, st);
+    if (items <= 16) return launch_topk_cluster_t<16>(a, pool, k, st);
+    if (items <= 32) return launch_topk_cluster_t<32>(a, pool, k, st);
+    if (items <= 48) return launch_topk_cluster_t<48>(a, pool, k, st);
+    return SE_ERR_UNSUPPORTED;
+  }
   const int items = cdiv(max(n_max, 1), 1024);
   if (items <= 1) return launch_topk_t<1>(a, pool, k, st);
   if (items <= 2) return launch_topk_t<2>(a, pool, k, st);

@@ -344,7 +344,17 @@ def run_quest(args, torch, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.quest_inputs(shape, dev)
     pipe = P.QuestDecode(inp["cache"], shape.Hq, ctx=shape.ctx, top_pages=shape.top_pages)
+    pipe.build_meta()                    # warm
+    m0 = torch.cuda.Event(enable_timing=True)
+    m1 = torch.cuda.Event(enable_timing=True)
+    m0.record()
     pipe.build_meta()
+    m1.record()
+    torch.cuda.synchronize()
+    meta_ms = m0.elapsed_time(m1)
+    # metadata build reads every resident key once and writes 2 x D per (page, head)
+    meta_build_bytes = shape.B * shape.ctx * shape.Hkv * shape.D * 2 + \
+        shape.B * (shape.ctx // shape.page_size) * shape.Hkv * 2 * shape.D * 2
     o = torch.empty_like(inp["q_steps"][0])
     sq = torch.empty_like(inp["q_steps"][0])
     sq.copy_(inp["q_steps"][0])
@@ -384,7 +394,8 @@ def run_quest(args, torch, rank, world):
     nb = shape.ctx // shape.page_size
     meta_bytes = shape.B * shape.Hkv * (nb - 1) * 2 * shape.D * 2
     kv_bytes = shape.B * shape.Hkv * (shape.top_pages + 1) * shape.page_size * 2 * shape.D * 2
-    detail = {"select_ms": statistics.mean(sel), "decode_ms": statistics.mean(dec),
+    detail = {"meta_build_ms": meta_ms, "meta_build_gbs": meta_build_bytes / (meta_ms * 1e-3) / 1e9,
+              "select_ms": statistics.mean(sel), "decode_ms": statistics.mean(dec),
               "select_gbs": meta_bytes / (statistics.mean(sel) * 1e-3) / 1e9,
               "decode_gbs": kv_bytes / (statistics.mean(dec) * 1e-3) / 1e9,
               "step_gbs": (meta_bytes + kv_bytes) / (ms * 1e-3) / 1e9}
