@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
                                                            const void* __restrict__ k_new,
                                                            const void* __restrict__ v_new,
                                                            float* aux, int64_t aux_stride,
-                                                           AppendWs w) {
+                                                           void* kmin, void* kmax, AppendWs w) {
   if (w.ctrl->abort) return;
   const int b = blockIdx.x;
   const int P = kv.page_size;
@@ -530,6 +530,29 @@ __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
     const int64_t dof = (int64_t)page * page_bytes + ((int64_t)h * P + s % P) * row_bytes + c * 16;
     stg_v4(static_cast<char*>(kv.k_pool) + dof, ldg_v4(static_cast<const char*>(k_new) + so));
     stg_v4(static_cast<char*>(kv.v_pool) + dof, ldg_v4(static_cast<const char*>(v_new) + so));
+  }
+  if (kmin != nullptr) {
+    // Quest metadata: a fresh page starts at the key, an old page widens
+    const bool fresh = (s % P) == 0;
+    for (int x = threadIdx.x; x < kv.Hkv * kv.D; x += blockDim.x) {
+      const int h = x / kv.D, d = x % kv.D;
+      const int64_t mo = ((int64_t)page * kv.Hkv + h) * kv.D + d;
+      const int64_t ko = ((int64_t)b * kv.Hkv + h) * kv.D + d;
+      if (kv.dtype == SE_BF16) {
+        const __nv_bfloat16 k = static_cast<const __nv_bfloat16*>(k_new)[ko];
+        __nv_bfloat16* mn = static_cast<__nv_bfloat16*>(kmin) + mo;
+        __nv_bfloat16* mx = static_cast<__nv_bfloat16*>(kmax) + mo;
+        const float kf = __bfloat162float(k);
+        *mn = fresh || kf < __bfloat162float(*mn) ? k : *mn;
+        *mx = fresh || kf > __bfloat162float(*mx) ? k : *mx;
+      } else {
+        const float k = static_cast<const float*>(k_new)[ko];
+        float* mn = static_cast<float*>(kmin) + mo;
+        float* mx = static_cast<float*>(kmax) + mo;
+        *mn = fresh ? k : fminf(*mn, k);
+        *mx = fresh ? k : fmaxf(*mx, k);
+      }
+    }
   }
   const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
   for (int h = threadIdx.x; h < kv.Hkv; h += blockDim.x) {
@@ -745,17 +768,18 @@ extern "C" size_t se_append_kv_workspace_size(const se_paged_kv* kv) {
 }
 
 extern "C" se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
-                                  float* aux, int64_t aux_stride, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+                                  float* aux, int64_t aux_stride, void* kmin, void* kmax,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   se_status s = se_check_kv(kv);
   if (s != SE_OK) return s;
   if (k_new == nullptr || v_new == nullptr || workspace == nullptr) return SE_ERR_INVALID_ARG;
+  if ((kmin == nullptr) != (kmax == nullptr)) return SE_ERR_INVALID_ARG;
   size_t need = 0;
   AppendWs w = carve_append(kv, workspace, &need);
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   append_plan_kernel<<<1, 1024, 0, st>>>(*kv, w);
-  append_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, k_new, v_new, aux, aux_stride, w);
+  append_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, k_new, v_new, aux, aux_stride, kmin, kmax, w);
   return se_last_launch_status();
 }
 

@@ -140,6 +140,99 @@ SE_DEV void record_timeout(const TcArgs& a, int* s_abort) {
 
 }  // namespace
 
+constexpr int kMaxTilesPerSplit = 64;
+
+// Largest query position of row chunk rc of sequence b (rows are (query, head)).
+SE_DEV int chunk_max_qpos(const TcArgs& a, int b, int rc, int lane) {
+  const int q0 = rc * (kRowChunk / a.G);
+  const int q1 = min(q0 + kRowChunk / a.G, a.w);
+  int mx = INT_MIN;
+  for (int q = q0 + lane; q < q1; q += 32) mx = max(mx, a.q_pos[(int64_t)b * a.w + q]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  return mx;
+}
+
+// Smallest position among the keys of tile `tile` (slots in [lo, hi)).
+SE_DEV int tile_min_pos(const TcArgs& a, const TileGeom& tg, int b, int g, int tile, int lane) {
+  const int32_t* sm = a.slot_map + ((int64_t)b * a.Hkv + g) * a.smax;
+  int mn = INT_MAX;
+  for (int j = lane; j < kKeyTile; j += 32) {
+    const int slot = tg.base + tile * kKeyTile + j;
+    if (slot >= tg.lo && slot < tg.hi) mn = min(mn, sm[slot]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  return mn;
+}
+
+// Fills list[0 .. *n) with the tiles of [t0, t0 + count) that at least one
+// row of chunk rc can see (every tile when not causal).  Called by all
+// threads of the CTA; the caller syncs before reading the list.
+SE_DEV void active_tiles(const TcArgs& a, const TileGeom& tg, int b, int g, int rc, int t0,
+                         int count, int* list, int* n) {
+  __shared__ int s_keep[kMaxTilesPerSplit];
+  __shared__ int s_qmax;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  count = min(count, kMaxTilesPerSplit);
+  if (!a.causal) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < count; ++i) list[i] = t0 + i;
+      *n = count;
+    }
+    return;
+  }
+  if (warp == 0) {
+    const int qm = chunk_max_qpos(a, b, rc, lane);
+    if (lane == 0) s_qmax = qm;
+  }
+  __syncthreads();
+  for (int i = warp; i < count; i += nw) {
+    const int mn = tile_min_pos(a, tg, b, g, t0 + i, lane);
+    if (lane == 0) s_keep[i] = mn <= s_qmax ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int k = 0;
+    for (int i = 0; i < count; ++i)
+      if (s_keep[i]) list[k++] = t0 + i;
+    *n = k;
+  }
+}
+
+constexpr int kMaxRowChunkList = 1024;
+
+// Fills list[0 .. *n) with the row chunks of [0, RC) in which some query can
+// see some key of tiles [t0, t0 + count) (a chunk is dropped only when all its
+// queries precede all those keys).  Returns false, leaving the list unused,
+// when every chunk is kept anyway (not causal, or RC above the list size).
+// Called by all threads of the CTA; the caller syncs before reading.
+SE_DEV bool active_row_chunks(const TcArgs& a, const TileGeom& tg, int b, int g, int RC, int t0,
+                              int count, int* list, int* n) {
+  if (!a.causal || RC > kMaxRowChunkList) return false;
+  __shared__ int s_kmin;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) s_kmin = INT_MAX;
+  __syncthreads();
+  for (int i = warp; i < count; i += nw) {
+    const int mn = tile_min_pos(a, tg, b, g, t0 + i, lane);
+    if (lane == 0) atomicMin(&s_kmin, mn);
+  }
+  __syncthreads();
+  for (int rc = warp; rc < RC; rc += nw) {
+    const int qm = chunk_max_qpos(a, b, rc, lane);
+    if (lane == 0) list[rc] = qm >= s_kmin ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int k = 0;
+    for (int rc = 0; rc < RC; ++rc)
+      if (list[rc]) list[k++] = rc;
+    *n = k;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 320 threads.
 // ---------------------------------------------------------------------------
@@ -169,7 +262,9 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const bool ok = geom_ok(a, tg);
   const int t_begin = split * a.tiles_per_split;
   const int t_end = ok ? min(t_begin + a.tiles_per_split, tg.n_tiles) : 0;
-  const int n_my = max(t_end - t_begin, 0);
+  const int n_range = max(t_end - t_begin, 0);
+  __shared__ int s_tiles[kMaxTilesPerSplit];   // tiles of the range that some row sees
+  __shared__ int s_n;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -188,9 +283,12 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc::fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  // causal: drop key tiles whose every key lies after the chunk's last query
+  active_tiles(a, tg, b, g, rc, t_begin, n_range, s_tiles, &s_n);
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = s_tmem;
+  const int n_my = s_n;
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -209,7 +307,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             break;
           }
         }
-        load_k_tile(a, &kmap, tg, b, g, t_begin + i, k_s + s * kKTileBytes,
+        load_k_tile(a, &kmap, tg, b, g, s_tiles[i], k_s + s * kKTileBytes,
                     a.causal ? pos_s + s * kKeyTile : nullptr, &full[s]);
         issued = i + 1;
       }
@@ -272,7 +370,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         break;
       }
       tc::tc_fence_after();
-      const int tile = t_begin + i;
+      const int tile = s_tiles[i];
       const int key0 = tg.base + tile * kKeyTile;
       const int32_t* pos = pos_s + s * kKeyTile;
       // fast path: every key of the tile is in range and visible to this row
@@ -421,6 +519,8 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const int t_end = ok ? min(t_begin + a.tiles_per_cta2, tg.n_tiles) : 0;
   const int n_my = max(t_end - t_begin, 0);
   const int n_pairs = cdiv(n_my, 2);
+  __shared__ int s_rcs[kMaxRowChunkList];   // row chunks that see some key of this CTA
+  __shared__ int s_nrc;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -443,9 +543,12 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     tc::fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  // causal: drop row chunks whose every query precedes every key of this CTA
+  const bool rc_list = active_row_chunks(a, tg, b, g, RC, t_begin, n_my, s_rcs, &s_nrc);
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = s_tmem;
+  const int n_rc = rc_list ? s_nrc : RC;
   const float2* info_g = a.rowinfo + (int64_t)bg * RC * kRowChunk;
 
   if (warp == 0) {
@@ -456,8 +559,9 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       int k_issued = 0, q_issued = 0;
       bool stop = false;
       for (int p = 0; p < n_pairs && !stop && !aborted(&s_abort); ++p) {
-        for (int rc = 0; rc < RC && !stop; ++rc) {
-          if (rc == 0) {
+        for (int ri = 0; ri < n_rc && !stop; ++ri) {
+          const int rc = rc_list ? s_rcs[ri] : ri;
+          if (ri == 0) {
             for (int t = 2 * p; t < min(2 * p + 2, n_my); ++t) {
               const int s = t % KS;
               const uint32_t par = ((t / KS) & 1) ^ 1;
@@ -508,7 +612,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       int uses[2] = {0, 0};
       bool stop = false;
       for (int p = 0; p < n_pairs && !stop && !aborted(&s_abort); ++p) {
-        for (int rc = 0; rc < RC && !stop; ++rc) {
+        for (int ri = 0; ri < n_rc && !stop; ++ri) {
           const int qs = q_used % QS;
           if (!q_resident || q_used == 0) {
             if (!(q_resident && q_used > 0) &&
@@ -523,7 +627,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const int s = t % KS;
             const int buf = t & 1;
             bool w_ok = true;
-            if (rc == 0) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
+            if (ri == 0) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
             if (w_ok && uses[buf] > 0)
               w_ok = tc::mbar_wait(&acc_free[buf], (uses[buf] - 1) & 1, kTimeoutNs);
             if (!w_ok) {
@@ -540,7 +644,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
               const uint64_t bd = tc::smem_desc_sw128(qbase + (k >> 2) * (kQChunkBytes / 2) + (k & 3) * 32);
               tc::mma_bf16(tmem + buf * 256, ad, bd, idesc, k > 0 ? 1u : 0u);
             }
-            if (rc == RC - 1) tc::mma_commit(&kempty[s]);
+            if (ri == n_rc - 1) tc::mma_commit(&kempty[s]);
             tc::mma_commit(&acc_full[buf]);
             uses[buf]++;
           }
@@ -566,8 +670,8 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         // no tile of this parity in the last pair: still release each streamed
         // Q chunk after it has landed, so the pair's row-info stage frees up
         if (!q_resident) {
-          for (int rc = 0; rc < RC; ++rc) {
-            const int qn = p * RC + rc;
+          for (int ri = 0; ri < n_rc; ++ri) {
+            const int qn = p * n_rc + ri;
             if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[qn % QS], (qn / QS) & 1, kTimeoutNs))) {
               record_timeout(a, &s_abort);
               stop = true;
@@ -581,11 +685,11 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       }
       float colsum = 0.f;
       int kpos = 0;
-      for (int rc = 0; rc < RC; ++rc) {
-        const int qn = p * RC + rc;          // Q chunk load number (0 when resident)
+      for (int ri = 0; ri < n_rc; ++ri) {
+        const int qn = p * n_rc + ri;        // Q chunk load number (0 when resident)
         const int qs = q_resident ? 0 : qn % QS;
         bool w_ok = tc::mbar_wait(&acc_full[set], use & 1, kTimeoutNs);
-        if (w_ok && rc == 0 && a.causal) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
+        if (w_ok && ri == 0 && a.causal) w_ok = tc::mbar_wait(&kfull[s], (t / KS) & 1, kTimeoutNs);
         if (w_ok) w_ok = tc::mbar_wait(&qfull[qs], q_resident ? 0 : ((qn / QS) & 1), kTimeoutNs);
         if (!__all_sync(0xffffffffu, w_ok)) {  // tcgen05.ld below is a warp-collective
           record_timeout(a, &s_abort);
@@ -593,7 +697,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           break;
         }
         tc::tc_fence_after();
-        if (rc == 0 && a.causal) kpos = pos_s[s * kKeyTile + kl];
+        if (ri == 0 && a.causal) kpos = pos_s[s * kKeyTile + kl];
         const float* lse_s = reinterpret_cast<const float*>(info_s + qs * kRowChunk);
         const int* qp_s = reinterpret_cast<const int*>(lse_s + kRowChunk);
         // fast path: this key is visible to every row of the chunk
@@ -638,7 +742,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         if (lane == 0) {
           tc::mbar_arrive(&acc_free[set]);
           if (!q_resident) tc::mbar_arrive(&ifree[qs]);
-          if (rc == RC - 1) tc::mbar_arrive(&pfree[s]);
+          if (ri == n_rc - 1) tc::mbar_arrive(&pfree[s]);
         }
         use++;
       }
@@ -1260,7 +1364,7 @@ TcPlan plan(const se_paged_kv* kv, int w, int n_max) {
   p.RC = cdiv(w * G, kRowChunk);
   // one extra tile when attn_lo is not page aligned
   p.n_tiles_max = cdiv(n_max + kv->page_size, kKeyTile);
-  p.tiles_per_split = 16;
+  p.tiles_per_split = 16;   // <= kMaxTilesPerSplit
   p.n_splits = cdiv(p.n_tiles_max, p.tiles_per_split);
   p.tiles_per_cta2 = p.RC == 1 ? 16 : 2;
   return p;

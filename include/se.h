@@ -327,11 +327,14 @@ se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const void* q, int
  * token per sequence at slot ctx_len[b] with position logical_len[b]; a
  * sequence whose last page is full pops a fresh page (ascending b).
  * k_new, v_new [B][Hkv][D]; aux (optional) gets 0 at the new slot.
+ * kmin, kmax (optional, both or neither) [num_pages][Hkv][D] Quest page
+ * metadata kept current: the new key starts a fresh page's min / max and
+ * widens an existing page's elementwise.
  * Device error: SE_ERR_OUT_OF_PAGES (nothing written).
  */
 se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
-                       float* aux, int64_t aux_stride, void* workspace,
-                       size_t workspace_bytes, void* stream);
+                       float* aux, int64_t aux_stride, void* kmin, void* kmax,
+                       void* workspace, size_t workspace_bytes, void* stream);
 size_t se_append_kv_workspace_size(const se_paged_kv* kv);
 
 /* Human-readable name of a status code (static string). */

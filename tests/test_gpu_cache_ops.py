@@ -145,6 +145,28 @@ def test_append_matches_oracle(cuda_lib, dtype, D):
         np.testing.assert_array_equal(aux.cpu().double().numpy(), aux_o)
 
 
+def test_append_keeps_quest_metadata_current(cuda_lib):
+    # appending with kmin / kmax equals rebuilding the metadata from scratch
+    se = cuda_lib
+    from oracle import quest as oquest
+    shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=29, max_ctx=60, tag="apq")
+    kv = se.kv_desc(pc, shape.Hq)
+    kmin = torch.empty_like(pc.k_pool[:, :, 0, :])
+    kmax = torch.empty_like(kmin)
+    se.se_quest_build_meta(kv, kmin, kmax)
+    for step in range(20):                # crosses the page boundaries at 32 and 48
+        k = W.normal((3, 2, 128), torch.bfloat16, "cuda", "apq", "k", step)
+        se.se_append_kv(kv, k, k, kmin=kmin, kmax=kmax)
+    torch.cuda.synchronize()
+    assert H.status(pc) == 0
+    c = ocache.from_tensors(pc)
+    omin, omax = oquest.build_meta(c)
+    for b in range(3):
+        pages = c.block_table[b, : W.cdiv(int(c.ctx_len[b]), 16)]
+        np.testing.assert_array_equal(kmin[pages].double().cpu().numpy(), omin[pages])
+        np.testing.assert_array_equal(kmax[pages].double().cpu().numpy(), omax[pages])
+
+
 def test_append_out_of_pages(cuda_lib):
     se = cuda_lib
     shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=32, max_ctx=48, tag="apo")

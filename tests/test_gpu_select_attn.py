@@ -277,6 +277,33 @@ def test_score_window_matches_oracle(cuda_lib, dtype, D, G, causal):
         assert (sg[b, g, :out_lo[b]] == -5.0).all() and (sg[b, g, out_hi[b]:] == -5.0).all()
 
 
+@pytest.mark.parametrize("G", [4, 8])
+def test_score_long_causal_window_matches_oracle(cuda_lib, G):
+    """Several row chunks (w G > 256): causal skipping of key tiles (pass 1)
+    and row chunks (pass 2) must not change any score.  Sequence 0 is a
+    prompt scored against itself (positions ascending), sequence 1 a window
+    of scattered positions in descending order."""
+    se = cuda_lib
+    B, Hkv, D, w, ctx = 2, 2, 128, 600, 1400
+    dtype = torch.bfloat16
+    shape = W.Shape(name="scl", B=B, Hq=Hkv * G, Hkv=Hkv, D=D, page_size=16, ctx=ctx, dtype=dtype)
+    pc = W.build_paged_cache(shape, num_pages=B * 88 + 2, max_ctx=ctx, device="cuda", tag="scl")
+    q_win = W.normal((B, w, shape.Hq, D), dtype, "cuda", "scl", "q", D, G)
+    gen = torch.Generator().manual_seed(7)
+    scattered = torch.randperm(ctx, generator=gen)[:w].sort(descending=True).values
+    q_pos = torch.stack([torch.arange(ctx - w, ctx), scattered]).to(torch.int32)
+    z, n = H.ranges(B, 0, ctx)
+    scores = torch.full((B, Hkv, ctx), -5.0, device="cuda")
+    se.se_score_window(se.kv_desc(pc, shape.Hq), q_win, q_pos.cuda(), z, n, z, n, causal=True,
+                       accumulate=False, n_max=ctx, scores=scores)
+    torch.cuda.synchronize()
+    c = ocache.from_tensors(pc)
+    os_ = oscore.score_window(c, q_win, q_pos.numpy(), [0] * B, [ctx] * B, [0] * B, [ctx] * B, True)
+    sg = scores.cpu().double().numpy()
+    for (b, g), row in os_.items():
+        H.assert_scores_close(sg[b, g], row, dtype, w, G)
+
+
 def test_score_window_accumulates(cuda_lib):
     se = cuda_lib
     B, Hkv, G, w, ctx = 1, 1, 4, 8, 100

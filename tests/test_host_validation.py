@@ -35,7 +35,7 @@ def kv(**kw):
 def test_descriptor_checks(bad, code):
     d, _ = kv(**bad)
     assert L.se_quest_build_meta(d, FAKE, FAKE, None) == code
-    assert L.se_append_kv(d, FAKE, FAKE, None, 0, FAKE, 1 << 20, None) == code
+    assert L.se_append_kv(d, FAKE, FAKE, None, 0, None, None, FAKE, 1 << 20, None) == code
 
 
 def test_null_pointers_rejected():
@@ -110,6 +110,12 @@ def test_static_scratch_variant_checks_size_before_anything():
     assert L.se_sparse_decode_attn_static(d, FAKE, 0, None, 0, 0, 1 << 22, FAKE, None, 0, None) == \
         se.SE_ERR_UNSUPPORTED
     assert L.se_sparse_decode_attn_static(d, FAKE, 0, None, 0, 0, 0, FAKE, None, 0, None) == \
+        se.SE_ERR_INVALID_ARG
+
+
+def test_append_meta_pointers_come_in_pairs():
+    d, _ = kv()
+    assert L.se_append_kv(d, FAKE, FAKE, None, 0, FAKE, None, FAKE, 1 << 20, None) == \
         se.SE_ERR_INVALID_ARG
 
 
