@@ -99,8 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "se_sparse_decode_attn_workspace_size": [P, c_int32],
         "se_sparse_decode_attn_static": [P, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
                                          c_void_p, c_void_p, c_int64, c_void_p],
-        "se_append_kv": [P, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
-                         c_size_t, c_void_p],
+        "se_append_kv": [P, c_void_p, c_void_p, c_int32, c_void_p, c_int64, c_void_p, c_void_p,
+                         c_void_p, c_size_t, c_void_p],
         "se_append_kv_workspace_size": [P],
         "se_status_string": [c_int32],
         "se_version": [],
@@ -270,11 +270,13 @@ def se_sparse_decode_attn_static(kv, q, *, view, o, max_entries, sel=None, n_sel
 
 def se_append_kv(kv, k_new, v_new, *, aux=None, kmin=None, kmax=None, workspace=None,
                  stream=None):
+    """k_new, v_new: [B][Hkv][D] (one token per sequence) or [B][n][Hkv][D]."""
     d = ctypes.byref(kv)
+    n_new = 1 if k_new.dim() == 3 else k_new.shape[1]
     need = _lib.se_append_kv_workspace_size(d)
     ws = _ws(workspace, need, k_new.device)
     _check("se_append_kv", _lib.se_append_kv(
-        d, _ptr(k_new), _ptr(v_new), _ptr(aux), aux.shape[-1] if aux is not None else 0,
+        d, _ptr(k_new), _ptr(v_new), n_new, _ptr(aux), aux.shape[-1] if aux is not None else 0,
         _ptr(kmin), _ptr(kmax), _ptr(ws), ws.numel(), _stream(stream)))
 
 

@@ -442,8 +442,7 @@ __global__ void __launch_bounds__(256) move_last_apply_kernel(se_paged_kv kv,
 
 struct AppendWs {
   CompactCtrl* ctrl;
-  int32_t* page;     // [B] page receiving the new slot
-  int32_t* fresh;    // [B] 1 = popped
+  int32_t* base;     // [B] pop rank of the sequence's first fresh page
   int32_t* ctx;      // [B] snapshot
   int32_t* logical;  // [B] snapshot
 };
@@ -452,15 +451,16 @@ static AppendWs carve_append(const se_paged_kv* kv, void* ws, size_t* bytes) {
   WsCarver c(ws);
   AppendWs w;
   w.ctrl = c.take<CompactCtrl>(1);
-  w.page = c.take<int32_t>(kv->B);
-  w.fresh = c.take<int32_t>(kv->B);
+  w.base = c.take<int32_t>(kv->B);
   w.ctx = c.take<int32_t>(kv->B);
   w.logical = c.take<int32_t>(kv->B);
   *bytes = c.bytes();
   return w;
 }
 
-__global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, AppendWs w) {
+// 1 CTA: bounds, fresh pages per sequence (blocks cdiv(ctx, P) ..
+// cdiv(ctx + n, P) - 1), pop ranks in ascending (b, block), capacity.
+__global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, int n, AppendWs w) {
   __shared__ int tmp[33];
   __shared__ int s_bad, s_run;
   const int tid = threadIdx.x;
@@ -468,104 +468,115 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, Appen
   if (tid == 0) { s_bad = 0; s_run = 0; }
   __syncthreads();
   const int top0 = *kv.free_top;
-  // pass 1: counts and bounds
   for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
     const int b = b0 + tid;
     int need = 0;
     if (b < kv.B) {
       const int ctx = kv.ctx_len[b];
-      if (ctx < 0 || ctx >= kv.max_pages_per_seq * P) {
+      if (ctx < 0 || (int64_t)ctx + n > (int64_t)kv.max_pages_per_seq * P) {
         set_status(kv.status, SE_ERR_BOUNDS);
         atomicExch(&s_bad, 1);
+      } else {
+        need = cdiv(ctx + n, P) - cdiv(ctx, P);
       }
-      need = (ctx % P == 0) ? 1 : 0;
       w.ctx[b] = ctx;
       w.logical[b] = kv.logical_len[b];
-      w.fresh[b] = need;
     }
     int total;
     const int ex = block_exclusive_scan(need, tmp, &total);
-    if (b < kv.B) w.page[b] = need ? -(s_run + ex) - 1 : 0;  // encoded pop rank
+    if (b < kv.B) w.base[b] = s_run + ex;
     __syncthreads();
     if (tid == 0) s_run += total;
     __syncthreads();
   }
-  const bool bad = s_bad || s_run > top0;
   if (tid == 0) {
+    const bool bad = s_bad || s_run > top0;
     if (!s_bad && s_run > top0) set_status(kv.status, SE_ERR_OUT_OF_PAGES);
     w.ctrl->abort = bad ? 1 : 0;
     w.ctrl->top0 = top0;
     w.ctrl->total_new = s_run;
   }
-  if (bad) return;
-  for (int b = tid; b < kv.B; b += blockDim.x) {
-    const int ctx = w.ctx[b];
-    if (w.fresh[b]) {
-      const int rank = -w.page[b] - 1;
-      w.page[b] = kv.free_list[top0 - 1 - rank];
-    } else {
-      w.page[b] = kv.block_table[(int64_t)b * kv.max_pages_per_seq + ctx / P];
-    }
-  }
 }
 
-// grid: B
+// grid: (cdiv(n + P - 1, P), B), 256 threads.  CTA (j, b) fills block
+// ctx / P + j of sequence b: K/V rows, slot map, aux, Quest bounds, and the
+// block-table entry of a fresh page.  CTA (0, b) commits the lengths.
 __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
                                                            const void* __restrict__ k_new,
-                                                           const void* __restrict__ v_new,
+                                                           const void* __restrict__ v_new, int n,
                                                            float* aux, int64_t aux_stride,
                                                            void* kmin, void* kmax, AppendWs w) {
   if (w.ctrl->abort) return;
-  const int b = blockIdx.x;
+  const int b = blockIdx.y;
   const int P = kv.page_size;
-  const int s = w.ctx[b];
-  const int page = w.page[b];
-  const int esz = (int)elem_size(kv.dtype);
-  const int64_t row_bytes = (int64_t)kv.D * esz;
-  const int chunks = (int)(row_bytes / 16);
-  const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
-  for (int t = threadIdx.x; t < kv.Hkv * chunks; t += blockDim.x) {
-    const int h = t / chunks, c = t % chunks;
-    const int64_t so = ((int64_t)b * kv.Hkv + h) * row_bytes + c * 16;
-    const int64_t dof = (int64_t)page * page_bytes + ((int64_t)h * P + s % P) * row_bytes + c * 16;
-    stg_v4(static_cast<char*>(kv.k_pool) + dof, ldg_v4(static_cast<const char*>(k_new) + so));
-    stg_v4(static_cast<char*>(kv.v_pool) + dof, ldg_v4(static_cast<const char*>(v_new) + so));
-  }
-  if (kmin != nullptr) {
-    // Quest metadata: a fresh page starts at the key, an old page widens
-    const bool fresh = (s % P) == 0;
-    for (int x = threadIdx.x; x < kv.Hkv * kv.D; x += blockDim.x) {
-      const int h = x / kv.D, d = x % kv.D;
-      const int64_t mo = ((int64_t)page * kv.Hkv + h) * kv.D + d;
-      const int64_t ko = ((int64_t)b * kv.Hkv + h) * kv.D + d;
-      if (kv.dtype == SE_BF16) {
-        const __nv_bfloat16 k = static_cast<const __nv_bfloat16*>(k_new)[ko];
-        __nv_bfloat16* mn = static_cast<__nv_bfloat16*>(kmin) + mo;
-        __nv_bfloat16* mx = static_cast<__nv_bfloat16*>(kmax) + mo;
-        const float kf = __bfloat162float(k);
-        *mn = fresh || kf < __bfloat162float(*mn) ? k : *mn;
-        *mx = fresh || kf > __bfloat162float(*mx) ? k : *mx;
-      } else {
-        const float k = static_cast<const float*>(k_new)[ko];
-        float* mn = static_cast<float*>(kmin) + mo;
-        float* mx = static_cast<float*>(kmax) + mo;
-        *mn = fresh ? k : fminf(*mn, k);
-        *mx = fresh ? k : fmaxf(*mx, k);
+  const int ctx = w.ctx[b];
+  const int blk = ctx / P + blockIdx.x;
+  const int s0 = max(ctx, blk * P), s1 = min(ctx + n, (blk + 1) * P);   // slots filled here
+  const int64_t mps = kv.max_pages_per_seq;
+  if (s0 < s1) {
+    const bool fresh = blk * P >= ctx;   // the block held nothing before
+    const int page = fresh ? kv.free_list[w.ctrl->top0 - 1 - (w.base[b] + blk - cdiv(ctx, P))]
+                           : kv.block_table[b * mps + blk];
+    const int esz = (int)elem_size(kv.dtype);
+    const int64_t row_bytes = (int64_t)kv.D * esz;
+    const int chunks = (int)(row_bytes / 16);
+    const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
+    const int rows = (s1 - s0) * kv.Hkv;
+    for (int t = threadIdx.x; t < rows * chunks; t += blockDim.x) {
+      const int r = t / chunks, c = t % chunks;
+      const int slot = s0 + r / kv.Hkv, h = r % kv.Hkv;
+      const int64_t so = (((int64_t)b * n + (slot - ctx)) * kv.Hkv + h) * row_bytes + c * 16;
+      const int64_t dof = (int64_t)page * page_bytes + ((int64_t)h * P + slot % P) * row_bytes + c * 16;
+      stg_v4(static_cast<char*>(kv.k_pool) + dof, ldg_v4(static_cast<const char*>(k_new) + so));
+      stg_v4(static_cast<char*>(kv.v_pool) + dof, ldg_v4(static_cast<const char*>(v_new) + so));
+    }
+    if (kmin != nullptr) {
+      // Quest bounds: a fresh page starts from its first key, an old page widens
+      for (int x = threadIdx.x; x < kv.Hkv * kv.D; x += blockDim.x) {
+        const int h = x / kv.D, d = x % kv.D;
+        const int64_t mo = ((int64_t)page * kv.Hkv + h) * kv.D + d;
+        if (kv.dtype == SE_BF16) {
+          const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(k_new);
+          __nv_bfloat16* mn = static_cast<__nv_bfloat16*>(kmin) + mo;
+          __nv_bfloat16* mx = static_cast<__nv_bfloat16*>(kmax) + mo;
+          __nv_bfloat16 lo = fresh ? kn[(((int64_t)b * n + (s0 - ctx)) * kv.Hkv + h) * kv.D + d] : *mn;
+          __nv_bfloat16 hi = fresh ? lo : *mx;
+          for (int slot = s0; slot < s1; ++slot) {
+            const __nv_bfloat16 k = kn[(((int64_t)b * n + (slot - ctx)) * kv.Hkv + h) * kv.D + d];
+            if (__bfloat162float(k) < __bfloat162float(lo)) lo = k;
+            if (__bfloat162float(k) > __bfloat162float(hi)) hi = k;
+          }
+          *mn = lo;
+          *mx = hi;
+        } else {
+          const float* kn = static_cast<const float*>(k_new);
+          float* mn = static_cast<float*>(kmin) + mo;
+          float* mx = static_cast<float*>(kmax) + mo;
+          float lo = fresh ? INFINITY : *mn, hi = fresh ? -INFINITY : *mx;
+          for (int slot = s0; slot < s1; ++slot) {
+            const float k = kn[(((int64_t)b * n + (slot - ctx)) * kv.Hkv + h) * kv.D + d];
+            lo = fminf(lo, k);
+            hi = fmaxf(hi, k);
+          }
+          *mn = lo;
+          *mx = hi;
+        }
       }
     }
-  }
-  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
-  for (int h = threadIdx.x; h < kv.Hkv; h += blockDim.x) {
-    kv.slot_map[((int64_t)b * kv.Hkv + h) * smax + s] = w.logical[b];
-    if (aux != nullptr) aux[((int64_t)b * kv.Hkv + h) * aux_stride + s] = 0.f;
-  }
-  if (threadIdx.x == 0) {
-    if (w.fresh[b]) {
-      kv.block_table[(int64_t)b * kv.max_pages_per_seq + s / P] = page;
+    const int64_t smax = mps * P;
+    for (int x = threadIdx.x; x < (s1 - s0) * kv.Hkv; x += blockDim.x) {
+      const int slot = s0 + x / kv.Hkv, h = x % kv.Hkv;
+      kv.slot_map[((int64_t)b * kv.Hkv + h) * smax + slot] = w.logical[b] + (slot - ctx);
+      if (aux != nullptr) aux[((int64_t)b * kv.Hkv + h) * aux_stride + slot] = 0.f;
+    }
+    if (threadIdx.x == 0 && fresh) {
+      kv.block_table[b * mps + blk] = page;
       if (kv.page_refcount) kv.page_refcount[page] = 1;
     }
-    kv.ctx_len[b] = s + 1;
-    kv.logical_len[b] = w.logical[b] + 1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    kv.ctx_len[b] = ctx + n;
+    kv.logical_len[b] = w.logical[b] + n;
     if (b == 0) *kv.free_top = w.ctrl->top0 - w.ctrl->total_new;
   }
 }
@@ -768,18 +779,24 @@ extern "C" size_t se_append_kv_workspace_size(const se_paged_kv* kv) {
 }
 
 extern "C" se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
-                                  float* aux, int64_t aux_stride, void* kmin, void* kmax,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+                                  int32_t n_new, float* aux, int64_t aux_stride, void* kmin,
+                                  void* kmax, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
   se_status s = se_check_kv(kv);
   if (s != SE_OK) return s;
-  if (k_new == nullptr || v_new == nullptr || workspace == nullptr) return SE_ERR_INVALID_ARG;
+  if (k_new == nullptr || v_new == nullptr || workspace == nullptr || n_new < 0)
+    return SE_ERR_INVALID_ARG;
   if ((kmin == nullptr) != (kmax == nullptr)) return SE_ERR_INVALID_ARG;
+  if ((int64_t)n_new > (int64_t)kv->max_pages_per_seq * kv->page_size) return SE_ERR_INVALID_ARG;
   size_t need = 0;
   AppendWs w = carve_append(kv, workspace, &need);
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  if (n_new == 0) return SE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  append_plan_kernel<<<1, 1024, 0, st>>>(*kv, w);
-  append_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, k_new, v_new, aux, aux_stride, kmin, kmax, w);
+  append_plan_kernel<<<1, 1024, 0, st>>>(*kv, n_new, w);
+  const dim3 grid(cdiv(n_new + kv->page_size - 1, kv->page_size), kv->B);
+  append_apply_kernel<<<grid, 256, 0, st>>>(*kv, k_new, v_new, n_new, aux, aux_stride, kmin, kmax,
+                                            w);
   return se_last_launch_status();
 }
 

@@ -286,40 +286,50 @@ struct StagedGeom {
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
 };
 
-// Issues the copies of stage `it` (view entries [s0, s0 + SE)) of (b, g):
-// runs of consecutive rows inside one page become one K and one V copy.
+// Issues the copies of one stage (view entries [s0, s0 + SE)) of (b, g);
+// called by all 32 lanes of one warp.  Lane i resolves entry i of each group
+// of 32 (slot, page); a maximal run of entries that are consecutive rows of
+// one page becomes one K and one V copy, issued by the lane that starts it.
+// valid[u] records whether entry u has a row (read by the consumers after the
+// stage's barrier completes).  Lane 0 arrives on the barrier last.
 template <typename T, int D, int G>
 SE_DEV void issue_stage(const DecodeArgs& a, int b, int g, int ctx, int s0, int e_end,
-                        uint8_t* dst, uint64_t* bar) {
+                        uint8_t* dst, uint64_t* bar, int8_t* valid, int lane) {
   using Gm = StagedGeom<T, D, G>;
   const se_paged_kv& kv = a.kv;
   const int P = kv.page_size;
   const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   const char* kp = static_cast<const char*>(kv.k_pool);
   const char* vp = static_cast<const char*>(kv.v_pool);
-  int u = 0;
-  while (u < Gm::SE) {
+  uint32_t n_valid = 0;
+#pragma unroll
+  for (int u0 = 0; u0 < Gm::SE; u0 += 32) {
+    const int u = u0 + lane;
     const int e = s0 + u;
-    const int slot = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
-    if (slot < 0) { ++u; continue; }
-    // extend the run while the next entries are the next rows of the same page
-    int len = 1;
-    if (a.view != SE_VIEW_TOKENS) {
-      while (u + len < Gm::SE && (slot % P) + len < P && e + len < e_end) {
-        const int nxt = view_slot(a, b, g, e + len, ctx);
-        if (nxt != slot + len) break;
-        ++len;
-      }
-    }
-    const int page = bt[slot / P];
-    if (page >= 0 && page < kv.num_pages) {
+    int slot = (u < Gm::SE && e < e_end) ? view_slot(a, b, g, e, ctx) : -1;
+    int page = slot >= 0 ? bt[slot / P] : -1;
+    if (page < 0 || page >= kv.num_pages) slot = -1;
+    const bool ok = slot >= 0;
+    if (u < Gm::SE) valid[u] = ok ? 1 : 0;
+    // a run continues when this entry is the next row of the previous one's page
+    const int prev = __shfl_up_sync(0xffffffffu, slot, 1);
+    const bool cont = ok && lane > 0 && prev >= 0 && prev + 1 == slot && slot % P != 0;
+    const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+    const uint32_t starts = __ballot_sync(0xffffffffu, ok && !cont);
+    n_valid += __popc(okm);
+    if (ok && !cont) {
+      const uint32_t above = lane == 31 ? 0u : (~0u << (lane + 1));
+      const uint32_t stop = (starts | ~okm) & above;
+      const int end = stop ? __ffs(stop) - 1 : 32;
+      const int len = end - lane;
       const int64_t off = (((int64_t)page * kv.Hkv + g) * P + slot % P) * Gm::RB;
       bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
       bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
     }
-    u += len;
   }
-  tc::mbar_arrive(bar);
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(bar);
+  (void)n_valid;
 }
 
 // grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps; dynamic smem
@@ -334,6 +344,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[4], empty[4];
+  __shared__ int8_t s_valid[4][SE];
   __shared__ float s_p[8][16];
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ int s_abort;
@@ -360,10 +371,11 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     tc::fence_barrier_init();
   }
   __syncthreads();
-  const bool producer = threadIdx.x == 0;
+  const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
   if (producer)
     for (int i = 0; i < min(S - 1, n_it); ++i)
-      issue_stage<T, D, G>(a, b, g, ctx, e_begin + i * SE, e_end, stages + i * Gm::STAGE_BYTES, &full[i]);
+      issue_stage<T, D, G>(a, b, g, ctx, e_begin + i * SE, e_end, stages + i * Gm::STAGE_BYTES,
+                           &full[i], s_valid[i], lane);
 
   const float qscale = kLog2e * rsqrtf((float)D);
   float q[G][V];
@@ -390,11 +402,12 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     if (producer && issued < n_it) {
       // refill the stage consumed in the previous iteration
       const int ps = issued % S;
-      if (issued < S || tc::mbar_wait(&empty[ps], ((issued / S) - 1) & 1, kLimit)) {
+      const bool free_ok = issued < S || tc::mbar_wait(&empty[ps], ((issued / S) - 1) & 1, kLimit);
+      if (__all_sync(full_mask, free_ok)) {
         issue_stage<T, D, G>(a, b, g, ctx, e_begin + issued * SE, e_end,
-                             stages + ps * Gm::STAGE_BYTES, &full[ps]);
+                             stages + ps * Gm::STAGE_BYTES, &full[ps], s_valid[ps], lane);
         ++issued;
-      } else {
+      } else if (lane == 0) {
         set_status(kv.status, SE_ERR_TIMEOUT);
         atomicExch(&s_abort, 1);
       }
@@ -415,7 +428,8 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
 #pragma unroll
     for (int u = 0; u < E; ++u) {
       const int e = e0 + u;
-      valid[u] = e < e_end && view_slot(a, b, g, e, ctx) >= 0;
+      valid[u] = s_valid[s][hw * E + u] != 0;
+      (void)e;
       if (valid[u]) {
         const T* kr = reinterpret_cast<const T*>(kst + (hw * E + u) * RB) + t * V;
         const T* vr = reinterpret_cast<const T*>(vst + (hw * E + u) * RB) + t * V;
@@ -497,9 +511,10 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     }
     __syncwarp();
   }
-  // drain copies still in flight (only after a timeout)
-  if (producer)
-    for (int i = 0; i < issued; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
+  // drain: after a timeout, copies of the last stages may still be in flight
+  // (each earlier stage was waited on before its buffer was refilled)
+  if (producer && lane == 0)
+    for (int i = max(0, issued - S); i < issued; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
   float lsum = l_own;
 #pragma unroll
   for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
@@ -615,7 +630,9 @@ static int pick_chunk(const se_paged_kv* kv, int max_entries) {
   const int64_t units = (int64_t)kv->B * kv->Hkv;
   int chunk = 1024;
   while (chunk > 128 && units * cdiv(max_entries, chunk) < 152 * 4) chunk >>= 1;
-  return chunk;
+  // same number of chunks, evened out (multiples of 128 entries)
+  const int n = cdiv(max(max_entries, 1), chunk);
+  return min(chunk, cdiv(cdiv(max(max_entries, 1), n), 128) * 128);
 }
 
 template <typename T, int D, int G>

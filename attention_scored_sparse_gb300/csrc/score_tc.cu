@@ -233,6 +233,104 @@ SE_DEV bool active_row_chunks(const TcArgs& a, const TileGeom& tg, int b, int g,
   return true;
 }
 
+// One 64-column block of a row for the online base-2 softmax statistics
+// (m, l) of pass 1.  fast: every key of the tile is in range and visible.
+SE_DEV void rowstats_block(const uint32_t (&r)[64], bool fast, bool row_ok, int key0,
+                           const TileGeom& tg, bool causal, const int32_t* pos, int qpos,
+                           float scale, float& m, float& l) {
+  if (fast) {
+    float c0 = __uint_as_float(r[0]), c1 = __uint_as_float(r[1]);
+    float c2 = __uint_as_float(r[2]), c3 = __uint_as_float(r[3]);
+#pragma unroll
+    for (int j = 4; j < 64; j += 4) {
+      c0 = fmaxf(c0, __uint_as_float(r[j])); c1 = fmaxf(c1, __uint_as_float(r[j + 1]));
+      c2 = fmaxf(c2, __uint_as_float(r[j + 2])); c3 = fmaxf(c3, __uint_as_float(r[j + 3]));
+    }
+    const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * scale);
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      s0 += tc::ex2(fmaf(__uint_as_float(r[j]), scale, -mn));
+      s1 += tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -mn));
+      s2 += tc::ex2(fmaf(__uint_as_float(r[j + 2]), scale, -mn));
+      s3 += tc::exp2_poly(fmaf(__uint_as_float(r[j + 3]), scale, -mn));   // 1 in 4 on the FMA pipe
+    }
+    l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
+    m = mn;
+    return;
+  }
+  float v[64];
+  float c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int key = key0 + j;
+    bool vis = row_ok && key >= tg.lo && key < tg.hi;
+    if (causal) vis = vis && pos[j] <= qpos;
+    v[j] = vis ? __uint_as_float(r[j]) * scale : -INFINITY;
+    if (j & 1) c1 = fmaxf(c1, v[j]); else c0 = fmaxf(c0, v[j]);
+  }
+  const float cm = fmaxf(c0, c1);
+  if (cm != -INFINITY) {
+    const float mn = fmaxf(m, cm);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; j += 2) {
+      s0 += tc::ex2(v[j] - mn);
+      s1 += tc::ex2(v[j + 1] - mn);
+    }
+    l = l * tc::ex2(m - mn) + (s0 + s1);
+    m = mn;
+  }
+}
+
+// One 32-row block of a key's column sum in pass 2: adds
+// exp2(logit * scale - lse2) over the rows that see the key.  fast: every row
+// of the chunk sees it.
+SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const float* lse,
+                         const int* qp, float scale, float& cs0, float& cs1, float& cs2,
+                         float& cs3) {
+  if (fast) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(lse + j);
+      cs0 += tc::ex2(fmaf(__uint_as_float(r[j]), scale, -l4.x));
+      cs1 += tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -l4.y));
+      cs2 += tc::ex2(fmaf(__uint_as_float(r[j + 2]), scale, -l4.z));
+      cs3 += tc::exp2_poly(fmaf(__uint_as_float(r[j + 3]), scale, -l4.w));   // 1 in 4 on the FMA pipe
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float p0 = tc::ex2(fmaf(__uint_as_float(r[j]), scale, -lse[j]));
+    float p1 = tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -lse[j + 1]));
+    if (kpos > qp[j]) p0 = 0.f;
+    if (kpos > qp[j + 1]) p1 = 0.f;
+    cs0 += p0;
+    cs1 += p1;
+  }
+}
+
+// Column sum of one key over the 256 rows of a chunk held in TMEM at tb
+// (lane = key, columns = rows): eight 32-row blocks, each loaded while the
+// previous one is summed.
+SE_DEV void colsum_tile(uint32_t tb, bool fast, int kpos, const float* lse_s, const int* qp_s,
+                        float scale, float& cs0, float& cs1, float& cs2, float& cs3) {
+  uint32_t ra[32], rb[32];
+  tc::tmem_ld32_async(tb, ra);
+  tc::tmem_wait32(ra);
+#pragma unroll 1
+  for (int c = 0; c < 8; c += 2) {
+    tc::tmem_ld32_async(tb + (c + 1) * 32, rb);
+    colsum_block(ra, fast, kpos, lse_s + c * 32, qp_s + c * 32, scale, cs0, cs1, cs2, cs3);
+    tc::tmem_wait32(rb);
+    if (c + 2 < 8) tc::tmem_ld32_async(tb + (c + 2) * 32, ra);
+    colsum_block(rb, fast, kpos, lse_s + (c + 1) * 32, qp_s + (c + 1) * 32, scale, cs0, cs1, cs2,
+                 cs3);
+    if (c + 2 < 8) tc::tmem_wait32(ra);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 320 threads.
 // ---------------------------------------------------------------------------
@@ -382,51 +480,16 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         fast = fast && mx <= qpos;
       }
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[64];
-        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 64, v);
-        if (fast) {
-          float c0 = v[0], c1 = v[1], c2 = v[2], c3 = v[3];
-#pragma unroll
-          for (int j = 4; j < 64; j += 4) {
-            c0 = fmaxf(c0, v[j]); c1 = fmaxf(c1, v[j + 1]);
-            c2 = fmaxf(c2, v[j + 2]); c3 = fmaxf(c3, v[j + 3]);
-          }
-          const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * a.scale);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            s0 += tc::ex2(fmaf(v[j], a.scale, -mn));
-            s1 += tc::ex2(fmaf(v[j + 1], a.scale, -mn));
-            s2 += tc::ex2(fmaf(v[j + 2], a.scale, -mn));
-            s3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -mn));   // 1 in 4 on the FMA pipe
-          }
-          l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
-          m = mn;
-          continue;
-        }
-        float c0 = -INFINITY, c1 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int key = key0 + c * 64 + j;
-          bool vis = row_ok && key >= tg.lo && key < tg.hi;
-          if (a.causal) vis = vis && pos[c * 64 + j] <= qpos;
-          v[j] = vis ? v[j] * a.scale : -INFINITY;
-          if (j & 1) c1 = fmaxf(c1, v[j]); else c0 = fmaxf(c0, v[j]);
-        }
-        const float cm = fmaxf(c0, c1);
-        if (cm != -INFINITY) {
-          const float mn = fmaxf(m, cm);
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            s0 += tc::ex2(v[j] - mn);
-            s1 += tc::ex2(v[j + 1] - mn);
-          }
-          l = l * tc::ex2(m - mn) + (s0 + s1);
-          m = mn;
-        }
+      {
+        // two 64-column blocks; the second loads while the first is reduced
+        uint32_t ra[64], rb[64];
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128;
+        tc::tmem_ld64_async(tb, ra);
+        tc::tmem_wait64(ra);
+        tc::tmem_ld64_async(tb + 64, rb);
+        rowstats_block(ra, fast, row_ok, key0, tg, a.causal, pos, qpos, a.scale, m, l);
+        tc::tmem_wait64(rb);
+        rowstats_block(rb, fast, row_ok, key0 + 64, tg, a.causal, pos + 64, qpos, a.scale, m, l);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -711,31 +774,8 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           fast = kpos <= mn;
         }
         float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[64];
-          tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 64, v);
-          if (fast) {
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c * 64 + j);
-              cs0 += tc::ex2(fmaf(v[j], a.scale, -l4.x));
-              cs1 += tc::ex2(fmaf(v[j + 1], a.scale, -l4.y));
-              cs2 += tc::ex2(fmaf(v[j + 2], a.scale, -l4.z));
-              cs3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -l4.w));   // 1 in 4 on the FMA pipe
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-              float p0 = tc::ex2(fmaf(v[j], a.scale, -lse_s[c * 64 + j]));
-              float p1 = tc::ex2(fmaf(v[j + 1], a.scale, -lse_s[c * 64 + j + 1]));
-              if (kpos > qp_s[c * 64 + j]) p0 = 0.f;
-              if (kpos > qp_s[c * 64 + j + 1]) p1 = 0.f;
-              cs0 += p0;
-              cs1 += p1;
-            }
-          }
-        }
+        colsum_tile(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256, fast, kpos, lse_s, qp_s,
+                    a.scale, cs0, cs1, cs2, cs3);
         colsum += (cs0 + cs1) + (cs2 + cs3);
         tc::tc_fence_before();
         __syncwarp();
@@ -972,51 +1012,16 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         fast = fast && mx <= qpos;
       }
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[64];
-        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + c * 64, v);
-        if (fast) {
-          float c0 = v[0], c1 = v[1], c2 = v[2], c3 = v[3];
-#pragma unroll
-          for (int j = 4; j < 64; j += 4) {
-            c0 = fmaxf(c0, v[j]); c1 = fmaxf(c1, v[j + 1]);
-            c2 = fmaxf(c2, v[j + 2]); c3 = fmaxf(c3, v[j + 3]);
-          }
-          const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * a.scale);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            s0 += tc::ex2(fmaf(v[j], a.scale, -mn));
-            s1 += tc::ex2(fmaf(v[j + 1], a.scale, -mn));
-            s2 += tc::ex2(fmaf(v[j + 2], a.scale, -mn));
-            s3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -mn));   // 1 in 4 on the FMA pipe
-          }
-          l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
-          m = mn;
-          continue;
-        }
-        float c0 = -INFINITY, c1 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int key = key0 + c * 64 + j;
-          bool vis = row_ok && key >= tg.lo && key < tg.hi;
-          if (a.causal) vis = vis && pos[c * 64 + j] <= qpos;
-          v[j] = vis ? v[j] * a.scale : -INFINITY;
-          if (j & 1) c1 = fmaxf(c1, v[j]); else c0 = fmaxf(c0, v[j]);
-        }
-        const float cm = fmaxf(c0, c1);
-        if (cm != -INFINITY) {
-          const float mn = fmaxf(m, cm);
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            s0 += tc::ex2(v[j] - mn);
-            s1 += tc::ex2(v[j + 1] - mn);
-          }
-          l = l * tc::ex2(m - mn) + (s0 + s1);
-          m = mn;
-        }
+      {
+        // two 64-column blocks; the second loads while the first is reduced
+        uint32_t ra[64], rb[64];
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128;
+        tc::tmem_ld64_async(tb, ra);
+        tc::tmem_wait64(ra);
+        tc::tmem_ld64_async(tb + 64, rb);
+        rowstats_block(ra, fast, row_ok, key0, tg, a.causal, pos, qpos, a.scale, m, l);
+        tc::tmem_wait64(rb);
+        rowstats_block(rb, fast, row_ok, key0 + 64, tg, a.causal, pos + 64, qpos, a.scale, m, l);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -1273,31 +1278,8 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         fast = kpos <= mn;
       }
       float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[64];
-        tc::tmem_ld64(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + c * 64, v);
-        if (fast) {
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c * 64 + j);
-            cs0 += tc::ex2(fmaf(v[j], a.scale, -l4.x));
-            cs1 += tc::ex2(fmaf(v[j + 1], a.scale, -l4.y));
-            cs2 += tc::ex2(fmaf(v[j + 2], a.scale, -l4.z));
-            cs3 += tc::exp2_poly(fmaf(v[j + 3], a.scale, -l4.w));   // 1 in 4 on the FMA pipe
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            float p0 = tc::ex2(fmaf(v[j], a.scale, -lse_s[c * 64 + j]));
-            float p1 = tc::ex2(fmaf(v[j + 1], a.scale, -lse_s[c * 64 + j + 1]));
-            if (kpos > qp_s[c * 64 + j]) p0 = 0.f;
-            if (kpos > qp_s[c * 64 + j + 1]) p1 = 0.f;
-            cs0 += p0;
-            cs1 += p1;
-          }
-        }
-      }
+      colsum_tile(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256, fast, kpos, lse_s, qp_s,
+                  a.scale, cs0, cs1, cs2, cs3);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -170,6 +170,63 @@ class H2O(_Base):
                          workspace=self.ws_compact, stream=stream)
 
 
+class H2OChunkedPrefill(_Base):
+    """H2O chunk-wise prefill eviction: each prompt chunk is written to the
+    cache, its queries score every resident entry causally into the running
+    scores (new entries start at 0), and once more than heavy + recent
+    entries are resident the top ``heavy`` of the older ones plus the last
+    ``recent`` are compacted from slot 0, the scores moving with them."""
+
+    def __init__(self, cache, Hq, *, chunk, heavy, recent):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.chunk, self.heavy, self.recent = chunk, heavy, recent
+        self.budget = heavy + recent
+        self.zero = _i32([0] * B, dev)
+        self.acc = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
+        self.keep = torch.empty((B, self.Hkv, self.budget), dtype=torch.int32, device=dev)
+        self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+        self.n_max = self.budget + chunk
+        sz = workspace_sizes(self.kv, w=chunk, n_max=self.n_max, max_keep=self.budget)
+        self.ws_score = self._ws(sz["score_window"])
+        self.ws_compact = self._ws(sz["compact_evict"])
+        self.ws_append = self._ws(sz["append_kv"])
+        self._lens = {}
+
+    def _len(self, n):
+        if n not in self._lens:
+            self._lens[n] = _i32([n] * self.B, self.device)
+        return self._lens[n]
+
+    def chunk_step(self, resident, q_chunk, q_pos, k_chunk, v_chunk, stream=None):
+        """One chunk on top of ``resident`` entries per sequence; returns the
+        resident count afterwards (known on the host, no sync)."""
+        ctx = resident + self.chunk
+        ctx_t = self._len(ctx)
+        se_append_kv(self.kv, k_chunk, v_chunk, aux=self.acc, workspace=self.ws_append,
+                     stream=stream)
+        se_score_window(self.kv, q_chunk, q_pos, self.zero, ctx_t, self.zero, ctx_t, causal=True,
+                        accumulate=True, n_max=ctx, scores=self.acc, workspace=self.ws_score,
+                        stream=stream)
+        if ctx <= self.budget:
+            return ctx
+        cand = self._len(ctx - self.recent)
+        se_topk_select(self.kv, self.acc, mode=SE_SELECT_TOPK, cand_lo=self.zero, cand_hi=cand,
+                       force_lo=cand, force_hi=ctx_t, keep_idx=self.keep, n_keep=self.n_keep,
+                       pool_kernel=1, k=self.heavy, n_max=ctx - self.recent, stream=stream)
+        se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
+                         first_slot=self.zero, max_keep=self.budget, aux=self.acc,
+                         workspace=self.ws_compact, stream=stream)
+        return self.budget
+
+    def run(self, q_chunks, q_pos, k_chunks, v_chunks, stream=None):
+        resident = 0
+        for i in range(q_chunks.shape[0]):
+            resident = self.chunk_step(resident, q_chunks[i], q_pos[i], k_chunks[i], v_chunks[i],
+                                       stream=stream)
+        return resident
+
+
 class Kara(_Base):
     """Kara periodic compression of the trailing window (bidirectional scores
     of the compressible keys, Token2Chunk, compaction from the window start),

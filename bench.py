@@ -464,6 +464,7 @@ def run_h2o(args, torch, rank, world):
     ms = statistics.mean(ev.durations("s0", "s1"))
     kv_bytes = shape.B * shape.Hkv * (shape.budget + 1) * 2 * shape.D * 2
     detail = {"prefill_ms": prefill_ms, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9}
+    detail.update(time_h2o_chunked(torch, shape, 512, dev))
     roof = dict(bound="hbm", achieved=detail["step_gbs"], unit="GB/s", kernel="h2o step",
                 per_launch=f"{kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
@@ -471,6 +472,37 @@ def run_h2o(args, torch, rank, world):
                 cfg={"workload": "h2o_decode: B=64, 4096-token prompt, budget 1024+128, "
                                  "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
                 dtype="bf16")
+
+
+def time_h2o_chunked(torch, shape, chunk, dev, reps=3):
+    """Chunk-wise H2O prefill eviction of the same prompt shape (chunks of
+    ``chunk`` tokens appended, scored into the running scores, evicted to the
+    budget); the cache metadata is restored between runs, outside the events."""
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    inp = W.h2o_chunked_inputs(shape, chunk, dev)
+    pc = inp["cache"]
+    meta = ["block_table", "slot_map", "ctx_len", "logical_len", "free_list", "free_top",
+            "page_refcount", "status"]
+    snap = {m: getattr(pc, m).clone() for m in meta}
+    pipe = P.H2OChunkedPrefill(pc, shape.Hq, chunk=chunk, heavy=shape.heavy, recent=shape.recent)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    for r in range(reps + 1):
+        for m in meta:
+            getattr(pc, m).copy_(snap[m])
+        torch.cuda.synchronize()
+        t0.record()
+        pipe.run(inp["q_chunks"], inp["q_pos"], inp["k_chunks"], inp["v_chunks"])
+        t1.record()
+        torch.cuda.synchronize()
+        if r > 0:
+            times.append(t0.elapsed_time(t1))
+    if int(pc.status.item()) != 0:
+        raise RuntimeError(f"chunked prefill failed with device status {int(pc.status.item())}")
+    del inp, pipe
+    return {"chunked_prefill_ms": statistics.mean(times), "chunked_prefill_chunk": chunk}
 
 
 def run_kara(args, torch, rank, world):

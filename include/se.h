@@ -323,17 +323,21 @@ se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const void* q, int
 /* Helpers                                                                    */
 /* ------------------------------------------------------------------------ */
 /*
- * se_append_kv -- SparseEngine "How it works" (CacheManager write): one new
- * token per sequence at slot ctx_len[b] with position logical_len[b]; a
- * sequence whose last page is full pops a fresh page (ascending b).
- * k_new, v_new [B][Hkv][D]; aux (optional) gets 0 at the new slot.
- * kmin, kmax (optional, both or neither) [num_pages][Hkv][D] Quest page
- * metadata kept current: the new key starts a fresh page's min / max and
- * widens an existing page's elementwise.
- * Device error: SE_ERR_OUT_OF_PAGES (nothing written).
+ * se_append_kv -- SparseEngine "How it works" (CacheManager write): n_new
+ * tokens per sequence at slots ctx_len[b] .. ctx_len[b] + n_new - 1 with
+ * positions logical_len[b] onward (a decode step is n_new = 1, a prefill
+ * chunk is n_new > 1).  Blocks that were empty take fresh pages popped from
+ * the free-list top in ascending (b, block) order.  Both lengths grow by
+ * n_new.  k_new, v_new [B][n_new][Hkv][D] in the cache dtype (device).
+ * aux (optional, [B][Hkv][aux_stride] fp32) gets 0 at the new slots.  kmin,
+ * kmax (optional, both or neither) [num_pages][Hkv][D] Quest page bounds kept
+ * current: a fresh page starts from its keys, an existing page widens.
+ * Host errors: SE_ERR_INVALID_ARG (null buffers, n_new < 0, workspace too
+ * small).  Device errors (nothing written): SE_ERR_BOUNDS (a sequence would
+ * exceed max_pages_per_seq pages), SE_ERR_OUT_OF_PAGES.
  */
 se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
-                       float* aux, int64_t aux_stride, void* kmin, void* kmax,
+                       int32_t n_new, float* aux, int64_t aux_stride, void* kmin, void* kmax,
                        void* workspace, size_t workspace_bytes, void* stream);
 size_t se_append_kv_workspace_size(const se_paged_kv* kv);
 

@@ -41,6 +41,7 @@ import numpy as np
 SE_OK = 0
 SE_ERR_OUT_OF_PAGES = 3
 SE_ERR_UNEVEN = 4
+SE_ERR_BOUNDS = 7
 
 
 def cdiv(a: int, b: int) -> int:
@@ -306,6 +307,45 @@ def append(c: Cache, k_bits: np.ndarray, v_bits: np.ndarray,
             aux[b, :, s] = 0.0
         c.ctx_len[b] = s + 1
         c.logical_len[b] += 1
+    return SE_OK
+
+
+def append_tokens(c: Cache, k_bits: np.ndarray, v_bits: np.ndarray,
+                  aux: Optional[np.ndarray] = None) -> int:
+    """CacheManager "write" of n tokens per sequence (a prefill chunk).
+
+    k_bits, v_bits: [B][n][Hkv][D] raw bits.  Token i of sequence b goes to
+    slot ctx_len[b] + i with logical position logical_len[b] + i.  Every block
+    that was empty before takes a fresh page; all fresh pages are popped from
+    the free-list top in ascending (sequence, block) order, as compaction
+    pops them (reading xii).  For one sequence this is the same as n
+    single-token appends.  Nothing changes on an error.
+    """
+    P = c.page_size
+    n = int(k_bits.shape[1])
+    cap = c.block_table.shape[1] * P
+    if any(int(c.ctx_len[b]) + n > cap for b in range(c.B)):
+        return SE_ERR_BOUNDS
+    need = sum(cdiv(int(c.ctx_len[b]) + n, P) - cdiv(int(c.ctx_len[b]), P) for b in range(c.B))
+    if need > c.free_top:
+        return SE_ERR_OUT_OF_PAGES
+    for b in range(c.B):
+        ctx = int(c.ctx_len[b])
+        for blk in range(cdiv(ctx, P), cdiv(ctx + n, P)):
+            c.free_top -= 1
+            page = int(c.free_list[c.free_top])
+            c.block_table[b, blk] = page
+            c.page_refcount[page] = 1
+        for i in range(n):
+            s = ctx + i
+            page = int(c.block_table[b, s // P])
+            c.k[page, :, s % P, :] = k_bits[b, i]
+            c.v[page, :, s % P, :] = v_bits[b, i]
+            c.slot_map[b, :, s] = c.logical_len[b] + i
+            if aux is not None:
+                aux[b, :, s] = 0.0
+        c.ctx_len[b] = ctx + n
+        c.logical_len[b] += n
     return SE_OK
 
 

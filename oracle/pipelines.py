@@ -66,6 +66,36 @@ def h2o_prefill(c: Cache, q_prompt, q_pos, shape, acc: np.ndarray):
     return dict(scores=s, keep=keep)
 
 
+def h2o_prefill_chunk(c: Cache, acc: np.ndarray, q_chunk, q_pos, k_chunk, v_chunk,
+                      heavy: int, recent: int):
+    """One chunk of H2O chunk-wise prefill eviction (SparseEngine "How it
+    works": H2O evicts during prefill, chunk by chunk, on accumulated scores).
+
+    Reading (xviii): the chunk's keys and values are written first; its
+    queries then attend causally to every resident entry (earlier survivors
+    and the chunk itself) and their group-summed weights are added to the
+    running scores (new entries start at 0); when more than heavy + recent
+    entries are resident, the top ``heavy`` of the non-recent ones by
+    running score (lower slot first on ties) and the last ``recent`` are
+    kept and compacted from slot 0, the scores moving with their entries.
+    """
+    st = cache.append_tokens(c, cache._bits(k_chunk), cache._bits(v_chunk), aux=acc)
+    assert st == cache.SE_OK
+    B, ctx = c.B, int(c.ctx_len[0])
+    s = scoring.score_window(c, q_chunk, q_pos, [0] * B, [ctx] * B, [0] * B, [ctx] * B,
+                             causal=True)
+    for (b, h), v in s.items():
+        acc[b, h, :ctx] += v
+    acc_pre = acc.copy()
+    keep = None
+    if ctx > heavy + recent:
+        keep = [[selection.topk_keep(acc[b, h, : ctx - recent], 0, heavy, 1, ctx - recent, ctx)
+                 for h in range(c.Hkv)] for b in range(B)]
+        st = cache.compact(c, keep, [0] * B, aux=acc)
+        assert st == cache.SE_OK
+    return dict(acc_pre=acc_pre, keep=keep)
+
+
 def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
     """One H2O decode step: append, dense attention, add this step's
     group-summed weights to the running scores, evict one if over budget."""

@@ -402,6 +402,29 @@ def h2o_inputs(shape: H2O, device, *, steps: Optional[int] = None):
                 k_steps=k_steps, v_steps=v_steps)
 
 
+def h2o_chunked_inputs(shape: H2O, chunk: int, device):
+    """Chunk-wise prefill of the H2O prompt: an empty cache, and the prompt's
+    queries, keys and values laid out chunk-major ([n_chunks][B][chunk]...),
+    so that each chunk is one contiguous block.  The pool holds the largest
+    resident set (budget + chunk) plus the fresh pages of one compaction."""
+    if shape.ctx % chunk:
+        raise ValueError("the prompt must be a whole number of chunks")
+    P = shape.page_size
+    n = shape.ctx // chunk
+    per_seq = cdiv(shape.budget + chunk, P) + cdiv(shape.budget, P) + 1
+    cache = build_paged_cache(shape, num_pages=per_seq * shape.B,
+                              max_ctx=shape.budget + chunk, device=device, ctx=0,
+                              tag="chunked")
+    q = normal((n, shape.B, chunk, shape.Hq, shape.D), shape.dtype, device, shape.name,
+               "chunked", "q")
+    k = normal((n, shape.B, chunk, shape.Hkv, shape.D), shape.dtype, device, shape.name,
+               "chunked", "k")
+    v = normal((n, shape.B, chunk, shape.Hkv, shape.D), shape.dtype, device, shape.name,
+               "chunked", "v")
+    pos = torch.arange(shape.ctx, dtype=torch.int32).view(n, 1, chunk).repeat(1, shape.B, 1)
+    return dict(cache=cache, q_chunks=q, k_chunks=k, v_chunks=v, q_pos=pos.to(device))
+
+
 def kara_inputs(shape: Kara, device):
     P = shape.page_size
     per_seq = cdiv(shape.ctx, P)

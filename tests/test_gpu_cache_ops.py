@@ -167,6 +167,49 @@ def test_append_keeps_quest_metadata_current(cuda_lib):
         np.testing.assert_array_equal(kmax[pages].double().cpu().numpy(), omax[pages])
 
 
+@pytest.mark.parametrize("dtype,D,n", [(torch.bfloat16, 128, 37), (torch.float32, 64, 5),
+                                         (torch.bfloat16, 128, 16)])
+def test_append_chunk_matches_oracle(cuda_lib, dtype, D, n):
+    """n tokens per sequence in one call (a prefill chunk), from a ragged
+    start, with aux and Quest bounds kept current."""
+    se = cuda_lib
+    from oracle import quest as oquest
+    shape, pc = _cache(dtype, D, B=3, Hkv=2, ctx=29, max_ctx=29 + 3 * n + 16, tag="apc")
+    kv = se.kv_desc(pc, shape.Hq)
+    c = ocache.from_tensors(pc)
+    aux = torch.ones(c.slot_map.shape, device="cuda")
+    aux_o = aux.double().cpu().numpy()
+    kmin = torch.empty_like(pc.k_pool[:, :, 0, :])
+    kmax = torch.empty_like(kmin)
+    se.se_quest_build_meta(kv, kmin, kmax)
+    for step in range(3):
+        k = W.normal((3, n, 2, D), dtype, "cuda", "apc", "k", step)
+        v = W.normal((3, n, 2, D), dtype, "cuda", "apc", "v", step)
+        assert ocache.append_tokens(c, ocache._bits(k), ocache._bits(v), aux=aux_o) == ocache.SE_OK
+        se.se_append_kv(kv, k, v, aux=aux, kmin=kmin, kmax=kmax)
+        torch.cuda.synchronize()
+        assert H.status(pc) == 0
+        H.assert_cache_equal(pc, c)
+        np.testing.assert_array_equal(aux.cpu().double().numpy(), aux_o)
+    omin, omax = oquest.build_meta(c)
+    for b in range(3):
+        pages = c.block_table[b, : W.cdiv(int(c.ctx_len[b]), 16)]
+        np.testing.assert_array_equal(kmin[pages].double().cpu().numpy(), omin[pages])
+        np.testing.assert_array_equal(kmax[pages].double().cpu().numpy(), omax[pages])
+
+
+def test_append_chunk_beyond_capacity_changes_nothing(cuda_lib):
+    se = cuda_lib
+    shape, pc = _cache(torch.bfloat16, 128, B=2, Hkv=2, ctx=20, max_ctx=48, tag="apb")
+    before = pc.clone()
+    k = W.normal((2, 29, 2, 128), torch.bfloat16, "cuda", "apb", "k")
+    se.se_append_kv(se.kv_desc(pc, shape.Hq), k, k)
+    torch.cuda.synchronize()
+    assert H.status(pc) == se.SE_ERR_BOUNDS
+    assert torch.equal(pc.ctx_len, before.ctx_len) and torch.equal(pc.block_table, before.block_table)
+    assert torch.equal(pc.free_top, before.free_top)
+
+
 def test_append_out_of_pages(cuda_lib):
     se = cuda_lib
     shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=32, max_ctx=48, tag="apo")

@@ -238,6 +238,62 @@ def test_h2o_full_decode_lockstep_from_generated_state(cuda_lib):
         _check_out(o, r["o"], shape.dtype, shape.G)
 
 
+def _h2o_chunked(cuda_lib, shape, chunk):
+    """Chunk-wise prefill eviction in lock-step with the oracle: running
+    scores after every chunk, the kept sets (near-ties of the oracle's k-th
+    score re-synchronised to the GPU's choice) and the cache bit for bit."""
+    inp = W.h2o_chunked_inputs(shape, chunk, "cuda")
+    pc = inp["cache"]
+    c = ocache.from_tensors(pc)
+    acc_o = np.zeros(c.slot_map.shape)
+    pipe = P.H2OChunkedPrefill(pc, shape.Hq, chunk=chunk, heavy=shape.heavy, recent=shape.recent)
+    resident, resynced = 0, 0
+    for i in range(inp["q_chunks"].shape[0]):
+        ctx = resident + chunk
+        resident = pipe.chunk_step(resident, inp["q_chunks"][i], inp["q_pos"][i],
+                                   inp["k_chunks"][i], inp["v_chunks"][i])
+        torch.cuda.synchronize()
+        assert H.status(pc) == 0
+        assert ocache.append_tokens(c, ocache._bits(inp["k_chunks"][i]),
+                                    ocache._bits(inp["v_chunks"][i]), aux=acc_o) == ocache.SE_OK
+        s = oscore.score_window(c, inp["q_chunks"][i], inp["q_pos"][i].cpu().numpy(),
+                                [0] * shape.B, [ctx] * shape.B, [0] * shape.B, [ctx] * shape.B, True)
+        for (b, h), v in s.items():
+            acc_o[b, h, :ctx] += v
+        if ctx > shape.budget:
+            kg = pipe.keep.cpu().numpy()
+            keep = []
+            for b in range(shape.B):
+                kb = []
+                for h in range(shape.Hkv):
+                    ko = osel.topk_keep(acc_o[b, h, :ctx - shape.recent], 0, shape.heavy, 1,
+                                        ctx - shape.recent, ctx)
+                    ranking = {j: float(acc_o[b, h, j]) for j in range(ctx - shape.recent)}
+                    resynced += H.assert_keep_near(kg[b, h], ko, ranking, shape.heavy,
+                                                   range(ctx - shape.recent, ctx))
+                    kb.append(kg[b, h].astype(np.int64))     # follow the GPU (equal or a near-tie)
+                keep.append(kb)
+            assert ocache.compact(c, keep, [0] * shape.B, aux=acc_o) == ocache.SE_OK
+        H.assert_cache_equal(pc, c)
+        n = int(c.ctx_len[0])
+        np.testing.assert_allclose(pipe.acc[:, :, :n].cpu().double().numpy(), acc_o[:, :, :n],
+                                   rtol=2e-3, atol=1e-6)
+        acc_o[:, :, :n] = pipe.acc[:, :, :n].cpu().double().numpy()   # no drift between chunks
+    assert resident == min(shape.budget, shape.ctx)
+    return resynced
+
+
+def test_h2o_chunked_prefill_reduced(cuda_lib):
+    shape = W.h2o_decode(B=2, Hq=8, Hkv=2, ctx=1024, heavy=192, recent=64)
+    _h2o_chunked(cuda_lib, shape, 256)
+
+
+def test_h2o_chunked_prefill_ragged_pages(cuda_lib):
+    # budget and chunk not multiples of the page size
+    shape = W.h2o_decode(B=3, Hq=8, Hkv=2, ctx=600, heavy=101, recent=23)
+    _h2o_chunked(cuda_lib, shape, 120)
+
+
 # ---------------------------------------------------------------------------
 # Kara + prune
 # ---------------------------------------------------------------------------

@@ -35,7 +35,7 @@ def kv(**kw):
 def test_descriptor_checks(bad, code):
     d, _ = kv(**bad)
     assert L.se_quest_build_meta(d, FAKE, FAKE, None) == code
-    assert L.se_append_kv(d, FAKE, FAKE, None, 0, None, None, FAKE, 1 << 20, None) == code
+    assert L.se_append_kv(d, FAKE, FAKE, 1, None, 0, None, None, FAKE, 1 << 20, None) == code
 
 
 def test_null_pointers_rejected():
@@ -115,8 +115,18 @@ def test_static_scratch_variant_checks_size_before_anything():
 
 def test_append_meta_pointers_come_in_pairs():
     d, _ = kv()
-    assert L.se_append_kv(d, FAKE, FAKE, None, 0, FAKE, None, FAKE, 1 << 20, None) == \
+    assert L.se_append_kv(d, FAKE, FAKE, 1, None, 0, FAKE, None, FAKE, 1 << 20, None) == \
         se.SE_ERR_INVALID_ARG
+
+
+def test_append_token_count_checked_on_host():
+    d, raw = kv()
+    cap = raw.max_pages_per_seq * raw.page_size
+    for n in (-1, cap + 1):
+        assert L.se_append_kv(d, FAKE, FAKE, n, None, 0, None, None, FAKE, 1 << 20, None) == \
+            se.SE_ERR_INVALID_ARG
+    # zero tokens: nothing to launch
+    assert L.se_append_kv(d, FAKE, FAKE, 0, None, 0, None, None, FAKE, 1 << 20, None) == se.SE_OK
 
 
 def test_workspace_queries_grow_with_sizes():

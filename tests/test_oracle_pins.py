@@ -317,6 +317,150 @@ def test_h2o_no_eviction_when_budget_covers_context():
                 np.testing.assert_allclose(r["o"][(b, g)], ref, rtol=1e-12, atol=1e-14)
 
 
+def _h2o_chunked_tiny(heavy, recent, prompt=48):
+    shape = W.h2o_decode(B=2, Hq=4, Hkv=2, D=16, ctx=prompt, heavy=heavy, recent=recent,
+                         steps=1, dtype=torch.float32, name="h2o_chunked_tiny")
+    return shape, W.h2o_chunked_inputs(shape, 8, "cpu")
+
+
+def _chunk_group_probs(inp, i, b, g, G, K, k_pos):
+    """Library attention of chunk i's queries of group g over keys K (fp64)."""
+    tot = np.zeros(K.shape[0])
+    qpos = inp["q_pos"][i, b].numpy()
+    mask = k_pos[None, :] <= qpos[:, None]
+    for h in range(g * G, (g + 1) * G):
+        Q = inp["q_chunks"][i, b, :, h].double().numpy()
+        tot += sdpa_probs(Q, K, mask).sum(axis=0)
+    return tot
+
+
+def test_h2o_chunked_prefill_without_eviction_is_whole_prompt_scoring():
+    """Budget above the prompt: chunks only split the queries, so the running
+    scores are the causal column sums of the whole prompt (library SDPA)."""
+    shape, inp = _h2o_chunked_tiny(100, 8)
+    c = oc(inp["cache"])
+    acc = np.zeros(c.slot_map.shape)
+    for i in range(inp["q_chunks"].shape[0]):
+        r = pipelines.h2o_prefill_chunk(c, acc, inp["q_chunks"][i], inp["q_pos"][i].numpy(),
+                                        inp["k_chunks"][i], inp["v_chunks"][i], 100, 8)
+        assert r["keep"] is None
+    assert (c.ctx_len == shape.ctx).all() and (c.logical_len == shape.ctx).all()
+    n_ch = inp["q_chunks"].shape[0]
+    for b in range(c.B):
+        for g in range(c.Hkv):
+            slots = np.arange(shape.ctx)
+            assert list(c.slot_map[b, g, slots]) == list(range(shape.ctx))
+            K = values(cache._bits(inp["k_chunks"][:, b, :, g]).reshape(shape.ctx, shape.D))
+            assert (c.keys(b, g, slots) == K).all()
+            want = sum(_chunk_group_probs(inp, i, b, g, shape.G, K, slots) for i in range(n_ch))
+            np.testing.assert_allclose(acc[b, g, :shape.ctx], want, rtol=1e-12, atol=1e-14)
+
+
+def test_h2o_chunked_prefill_eviction_replayed_independently():
+    """With eviction: replay every chunk with library attention over the
+    entries resident at that chunk, keep per logical position a running score,
+    and pick the survivors by a full sort; the oracle must agree at every
+    chunk, keep the recent tokens and hold exactly heavy + recent entries."""
+    heavy, recent = 12, 4
+    shape, inp = _h2o_chunked_tiny(heavy, recent)
+    c = oc(inp["cache"])
+    before = c.copy()
+    acc = np.zeros(c.slot_map.shape)
+    G, chunk = shape.G, inp["q_chunks"].shape[2]
+    run = {(b, g): {} for b in range(c.B) for g in range(c.Hkv)}      # position -> score
+    keyv = {}                                                         # (b, g, position) -> key
+    for i in range(inp["q_chunks"].shape[0]):
+        for b in range(c.B):
+            for g in range(c.Hkv):
+                for j in range(chunk):
+                    p = i * chunk + j
+                    keyv[(b, g, p)] = values(cache._bits(inp["k_chunks"][i, b, j, g]))
+                    run[(b, g)][p] = 0.0
+                pos = np.array(sorted(run[(b, g)]))
+                K = np.stack([keyv[(b, g, int(p))] for p in pos])
+                probs = _chunk_group_probs(inp, i, b, g, G, K, pos)
+                for p, v in zip(pos, probs):
+                    run[(b, g)][int(p)] += v
+                if len(pos) > heavy + recent:
+                    old = pos[:-recent]
+                    top = sorted(old, key=lambda p: (-run[(b, g)][int(p)], p))[:heavy]
+                    survivors = set(int(p) for p in top) | set(int(p) for p in pos[-recent:])
+                    run[(b, g)] = {p: run[(b, g)][p] for p in survivors}
+        pipelines.h2o_prefill_chunk(c, acc, inp["q_chunks"][i], inp["q_pos"][i].numpy(),
+                                    inp["k_chunks"][i], inp["v_chunks"][i], heavy, recent)
+        _check_accounting(before, c)
+        for b in range(c.B):
+            n = int(c.ctx_len[b])
+            assert n == min(heavy + recent, (i + 1) * chunk)
+            for g in range(c.Hkv):
+                pos = c.slot_map[b, g, :n]
+                assert (np.diff(pos) > 0).all()
+                assert sorted(run[(b, g)]) == pos.tolist()
+                assert set(range((i + 1) * chunk - recent, (i + 1) * chunk)) <= set(pos.tolist())
+                want = np.array([run[(b, g)][int(p)] for p in pos])
+                np.testing.assert_allclose(acc[b, g, :n], want, rtol=1e-12, atol=1e-14)
+                for s, p in enumerate(pos):
+                    assert (c.keys(b, g, [s])[0] == keyv[(b, g, int(p))]).all()
+
+
+def test_append_tokens_one_sequence_equals_repeated_single_appends():
+    shape = tiny_shape(B=1, ctx=6, page_size=4)
+    c1 = oc(tiny_cache(shape, num_pages=12, max_ctx=30))
+    c2 = c1.copy()
+    rng = np.random.default_rng(3)
+    n = 11
+    kb = rng.integers(0, 2**32, size=(1, n, shape.Hkv, shape.D), dtype=np.uint32)
+    vb = rng.integers(0, 2**32, size=(1, n, shape.Hkv, shape.D), dtype=np.uint32)
+    a1 = np.ones(c1.slot_map.shape)
+    a2 = a1.copy()
+    assert cache.append_tokens(c1, kb, vb, aux=a1) == cache.SE_OK
+    for i in range(n):
+        assert cache.append(c2, kb[:, i], vb[:, i], aux=a2) == cache.SE_OK
+    for f in ("k", "v", "block_table", "slot_map", "ctx_len", "logical_len", "free_list",
+              "page_refcount"):
+        assert (getattr(c1, f) == getattr(c2, f)).all(), f
+    assert c1.free_top == c2.free_top
+    assert (a1 == a2).all()
+
+
+def test_append_tokens_pop_order_and_contents():
+    """Three sequences at ctx 22 (page 4) take 9 tokens each: blocks 6 and 7
+    are fresh, popped from the stack top in (sequence, block) order."""
+    shape = tiny_shape(B=3, ctx=22, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=48, max_ctx=32))
+    before = c.copy()
+    top = c.free_top
+    rng = np.random.default_rng(5)
+    kb = rng.integers(0, 2**32, size=(3, 9, shape.Hkv, shape.D), dtype=np.uint32)
+    assert cache.append_tokens(c, kb, kb + 1) == cache.SE_OK
+    assert c.free_top == top - 6
+    stack = before.free_list
+    for b in range(3):
+        assert c.block_table[b, 6] == stack[top - 1 - 2 * b]
+        assert c.block_table[b, 7] == stack[top - 2 - 2 * b]
+        assert (c.block_table[b, :6] == before.block_table[b, :6]).all()
+        for i in range(9):
+            s = 22 + i
+            assert (c.slot_map[b, :, s] == 22 + i).all()
+            (p,), (r,) = c.where(b, [s])
+            assert (c.k[p, :, r] == kb[b, i]).all() and (c.v[p, :, r] == kb[b, i] + 1).all()
+    assert (c.ctx_len == 31).all() and (c.logical_len == 31).all()
+    _check_accounting(before, c)
+
+
+def test_append_tokens_errors_change_nothing():
+    shape = tiny_shape(B=2, ctx=8, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=5, max_ctx=40))     # 4 pages used, 1 free
+    before = c.copy()
+    kb = np.zeros((2, 5, shape.Hkv, shape.D), dtype=np.uint32)
+    assert cache.append_tokens(c, kb, kb) == cache.SE_ERR_OUT_OF_PAGES
+    kb = np.zeros((2, 33, shape.Hkv, shape.D), dtype=np.uint32)
+    assert cache.append_tokens(c, kb, kb) == cache.SE_ERR_BOUNDS
+    for f in ("k", "block_table", "slot_map", "ctx_len", "free_list"):
+        assert (getattr(c, f) == getattr(before, f)).all()
+    assert c.free_top == before.free_top
+
+
 # ---------------------------------------------------------------------------
 # O6 Quest
 # ---------------------------------------------------------------------------
