@@ -8,20 +8,22 @@
 //
 //   pass 1 (rowstats)  S = Q_rows K_tile^T with the 256 rows of a chunk on
 //       TMEM lanes (two M=128 accumulators), N = 128 keys; each epilogue
-//       thread owns one row and keeps a base-2 running max / sum over its
-//       CTA's key range.  Partials per key split go to the workspace.
-//   rowinfo            the CUDA-core kernel merges the splits: lse2 per row
+//       thread owns one row and one 64-key half of every tile and keeps a
+//       base-2 running max / sum over its CTA's key range.  Partials per
+//       (key split, half) go to the workspace.
+//   rowinfo            the CUDA-core kernel merges the splits: -lse2 per row
 //       (plus the row's query position for causal masking).
 //   pass 2 (colsum)    S^T = K_tile Q_rows^T with the 128 keys of a tile on
 //       TMEM lanes (M=128), N = 256 rows; each epilogue thread owns one key
-//       and sums exp2(t - lse2_r) over the rows in registers -- no cross-
-//       thread reduction -- and writes its column sum.
+//       and one 128-row half and sums exp2(t - lse2_r) over its rows in
+//       registers; the two halves of a key meet once in shared memory.
 //
 // Both passes: one producer warp issues TMA loads (K pages as 16-row boxes
 // gathered through the block table, 128-byte swizzle; Q via a 4-D map over
 // [B][w][Hq][D]; key positions and row info as 1-D bulk copies), one warp
 // issues tcgen05.mma from shared-memory descriptors into double-buffered TMEM
-// accumulators, eight warps run the softmax epilogue from tcgen05.ld.  Every
+// accumulators, sixteen warps (four per SM sub-partition, so that exp2,
+// FMA and TMEM-load latencies overlap) run the epilogue from tcgen05.ld.  Every
 // mbarrier wait is bounded by %globaltimer: on expiry the CTA records
 // SE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -40,7 +42,7 @@ constexpr int kRowChunk = 256;      // rows per chunk (2 x M=128 in pass 1, N of
 constexpr int kKTileBytes = kKeyTile * kD * 2;   // 32 KB
 constexpr int kQChunkBytes = kRowChunk * kD * 2; // 64 KB
 constexpr int kStages1 = 4;         // K-tile ring depth, pass 1
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;       // epilogue warps (4 per SM sub-partition)
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
 
@@ -59,7 +61,7 @@ struct TcArgs {
   float* scores;
   int64_t scores_stride;
   float* part;      // [groups][RC*256][n_splits][2]
-  float2* rowinfo;  // [groups][RC*256] {lse2, qpos bits}
+  float2* rowinfo;  // [groups][RC*256] {-lse2, qpos bits}
   int n_splits, tiles_per_split, tiles_per_cta2;
   int32_t* status;
   float scale;      // log2(e) / sqrt(D)
@@ -233,36 +235,41 @@ SE_DEV bool active_row_chunks(const TcArgs& a, const TileGeom& tg, int b, int g,
   return true;
 }
 
-// One 64-column block of a row for the online base-2 softmax statistics
-// (m, l) of pass 1.  fast: every key of the tile is in range and visible.
-SE_DEV void rowstats_block(const uint32_t (&r)[64], bool fast, bool row_ok, int key0,
+// One block of N columns of a row for the online base-2 softmax statistics
+// (m, l) of pass 1.  fast: every key of the block is in range and visible.
+template <int N>
+SE_DEV void rowstats_block(const uint32_t (&r)[N], bool fast, bool row_ok, int key0,
                            const TileGeom& tg, bool causal, const int32_t* pos, int qpos,
                            float scale, float& m, float& l) {
   if (fast) {
     float c0 = __uint_as_float(r[0]), c1 = __uint_as_float(r[1]);
-    float c2 = __uint_as_float(r[2]), c3 = __uint_as_float(r[3]);
 #pragma unroll
-    for (int j = 4; j < 64; j += 4) {
-      c0 = fmaxf(c0, __uint_as_float(r[j])); c1 = fmaxf(c1, __uint_as_float(r[j + 1]));
-      c2 = fmaxf(c2, __uint_as_float(r[j + 2])); c3 = fmaxf(c3, __uint_as_float(r[j + 3]));
+    for (int j = 2; j < N; j += 4) {   // r[2..N-1] in pairs, two chains
+      c0 = tc::fmax3(c0, __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+      if (j + 2 < N) c1 = tc::fmax3(c1, __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
     }
-    const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * scale);
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const float mn = fmaxf(m, fmaxf(c0, c1) * scale);
+    const uint64_t sc2 = tc::f2(scale, scale), nm2 = tc::f2(-mn, -mn);
+    uint64_t s01 = 0, s23 = 0;   // (+0, +0) pairs
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      s0 += tc::ex2(fmaf(__uint_as_float(r[j]), scale, -mn));
-      s1 += tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -mn));
-      s2 += tc::ex2(fmaf(__uint_as_float(r[j + 2]), scale, -mn));
-      s3 += tc::exp2_poly(fmaf(__uint_as_float(r[j + 3]), scale, -mn));   // 1 in 4 on the FMA pipe
+    for (int j = 0; j < N; j += 4) {
+      float a0, a1, b0, b1;
+      tc::f2split(tc::ffma2(tc::f2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, nm2), a0, a1);
+      tc::f2split(tc::ffma2(tc::f2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), sc2, nm2), b0, b1);
+      s01 = tc::fadd2(s01, tc::f2(tc::ex2(a0), tc::ex2(a1)));
+      s23 = tc::fadd2(s23, tc::f2(tc::ex2(b0), tc::ex2(b1)));
     }
-    l = l * tc::ex2(m - mn) + ((s0 + s1) + (s2 + s3));
+    float x0, x1, y0, y1;
+    tc::f2split(s01, x0, x1);
+    tc::f2split(s23, y0, y1);
+    l = l * tc::ex2(m - mn) + ((x0 + x1) + (y0 + y1));
     m = mn;
     return;
   }
-  float v[64];
+  float v[N];
   float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 64; ++j) {
+  for (int j = 0; j < N; ++j) {
     const int key = key0 + j;
     bool vis = row_ok && key >= tg.lo && key < tg.hi;
     if (causal) vis = vis && pos[j] <= qpos;
@@ -274,7 +281,7 @@ SE_DEV void rowstats_block(const uint32_t (&r)[64], bool fast, bool row_ok, int 
     const float mn = fmaxf(m, cm);
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; j += 2) {
+    for (int j = 0; j < N; j += 2) {
       s0 += tc::ex2(v[j] - mn);
       s1 += tc::ex2(v[j + 1] - mn);
     }
@@ -284,26 +291,33 @@ SE_DEV void rowstats_block(const uint32_t (&r)[64], bool fast, bool row_ok, int 
 }
 
 // One 32-row block of a key's column sum in pass 2: adds
-// exp2(logit * scale - lse2) over the rows that see the key.  fast: every row
-// of the chunk sees it.
-SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const float* lse,
+// exp2(logit * scale - lse2) over the rows that see the key (nlse holds
+// -lse2 per row).  fast: every row of the chunk sees it.
+SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const float* nlse,
                          const int* qp, float scale, float& cs0, float& cs1, float& cs2,
                          float& cs3) {
   if (fast) {
+    const uint64_t sc2 = tc::f2(scale, scale);
+    uint64_t s01 = tc::f2(cs0, cs1), s23 = tc::f2(cs2, cs3);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(lse + j);
-      cs0 += tc::ex2(fmaf(__uint_as_float(r[j]), scale, -l4.x));
-      cs1 += tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -l4.y));
-      cs2 += tc::ex2(fmaf(__uint_as_float(r[j + 2]), scale, -l4.z));
-      cs3 += tc::exp2_poly(fmaf(__uint_as_float(r[j + 3]), scale, -l4.w));   // 1 in 4 on the FMA pipe
+      const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nlse + j);   // two pairs
+      float a0, a1, b0, b1;
+      tc::f2split(tc::ffma2(tc::f2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, nl.x),
+                  a0, a1);
+      tc::f2split(tc::ffma2(tc::f2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), sc2, nl.y),
+                  b0, b1);
+      s01 = tc::fadd2(s01, tc::f2(tc::ex2(a0), tc::ex2(a1)));
+      s23 = tc::fadd2(s23, tc::f2(tc::ex2(b0), tc::ex2(b1)));
     }
+    tc::f2split(s01, cs0, cs1);
+    tc::f2split(s23, cs2, cs3);
     return;
   }
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    float p0 = tc::ex2(fmaf(__uint_as_float(r[j]), scale, -lse[j]));
-    float p1 = tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, -lse[j + 1]));
+    float p0 = tc::ex2(fmaf(__uint_as_float(r[j]), scale, nlse[j]));
+    float p1 = tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, nlse[j + 1]));
     if (kpos > qp[j]) p0 = 0.f;
     if (kpos > qp[j + 1]) p1 = 0.f;
     cs0 += p0;
@@ -311,28 +325,43 @@ SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const flo
   }
 }
 
-// Column sum of one key over the 256 rows of a chunk held in TMEM at tb
-// (lane = key, columns = rows): eight 32-row blocks, each loaded while the
-// previous one is summed.
+// Column sum of one key over 32 NB rows held in TMEM at tb (lane = key,
+// columns = rows): NB 32-row blocks, each loaded while the previous one is
+// summed.
+template <int NB>
 SE_DEV void colsum_tile(uint32_t tb, bool fast, int kpos, const float* lse_s, const int* qp_s,
                         float scale, float& cs0, float& cs1, float& cs2, float& cs3) {
   uint32_t ra[32], rb[32];
   tc::tmem_ld32_async(tb, ra);
   tc::tmem_wait32(ra);
 #pragma unroll 1
-  for (int c = 0; c < 8; c += 2) {
+  for (int c = 0; c < NB; c += 2) {
     tc::tmem_ld32_async(tb + (c + 1) * 32, rb);
     colsum_block(ra, fast, kpos, lse_s + c * 32, qp_s + c * 32, scale, cs0, cs1, cs2, cs3);
     tc::tmem_wait32(rb);
-    if (c + 2 < 8) tc::tmem_ld32_async(tb + (c + 2) * 32, ra);
+    if (c + 2 < NB) tc::tmem_ld32_async(tb + (c + 2) * 32, ra);
     colsum_block(rb, fast, kpos, lse_s + (c + 1) * 32, qp_s + (c + 1) * 32, scale, cs0, cs1, cs2,
                  cs3);
-    if (c + 2 < 8) tc::tmem_wait32(ra);
+    if (c + 2 < NB) tc::tmem_wait32(ra);
+  }
+}
+
+// colsum_tile without the prefetch (one 32-row block in registers at a time),
+// for kernels whose warps are many enough to cover the load latency.
+template <int NB>
+SE_DEV void colsum_tile_seq(uint32_t tb, bool fast, int kpos, const float* lse_s, const int* qp_s,
+                            float scale, float& cs0, float& cs1, float& cs2, float& cs3) {
+#pragma unroll 1
+  for (int c = 0; c < NB; ++c) {
+    uint32_t r[32];
+    tc::tmem_ld32_async(tb + c * 32, r);
+    tc::tmem_wait32(r);
+    colsum_block(r, fast, kpos, lse_s + c * 32, qp_s + c * 32, scale, cs0, cs1, cs2, cs3);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 320 threads.
+// Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 576 threads.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -448,9 +477,11 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       tc::mbar_wait(done, 0, kTimeoutNs);
     }
   } else {
-    // ---------------- epilogue: one row per thread ----------------
+    // ---------------- epilogue: one row and column half per thread ----------------
+    // 16 warps: (row block mb, TMEM lane quarter, column half of each tile)
     const int e = warp - 2;
-    const int mb = e / 4;                 // row block (accumulator half)
+    const int mb = (e >> 2) & 1;
+    const int half = e >> 3;
     const int quarter = warp & 3;         // TMEM lane quarter this warp may read
     const int r = mb * 128 + quarter * 32 + lane;  // row in chunk
     const int row = rc * kRowChunk + r;
@@ -469,27 +500,27 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       }
       tc::tc_fence_after();
       const int tile = s_tiles[i];
-      const int key0 = tg.base + tile * kKeyTile;
-      const int32_t* pos = pos_s + s * kKeyTile;
-      // fast path: every key of the tile is in range and visible to this row
-      bool fast = row_ok && key0 >= tg.lo && key0 + kKeyTile <= tg.hi;
+      const int key0 = tg.base + tile * kKeyTile + half * 64;   // this warp's 64 columns
+      const int32_t* pos = pos_s + s * kKeyTile + half * 64;
+      // fast path: every key of the block is in range and visible to this row
+      bool fast = row_ok && key0 >= tg.lo && key0 + 64 <= tg.hi;
       if (a.causal) {
-        const int4 p4 = reinterpret_cast<const int4*>(pos)[lane];
-        int mx = max(max(p4.x, p4.y), max(p4.z, p4.w));
+        const int2 p2 = reinterpret_cast<const int2*>(pos)[lane];
+        int mx = max(p2.x, p2.y);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         fast = fast && mx <= qpos;
       }
       {
-        // two 64-column blocks; the second loads while the first is reduced
-        uint32_t ra[64], rb[64];
-        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128;
-        tc::tmem_ld64_async(tb, ra);
-        tc::tmem_wait64(ra);
-        tc::tmem_ld64_async(tb + 64, rb);
+        // two 32-column blocks; the second loads while the first is reduced
+        uint32_t ra[32], rb[32];
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + half * 64;
+        tc::tmem_ld32_async(tb, ra);
+        tc::tmem_wait32(ra);
+        tc::tmem_ld32_async(tb + 32, rb);
         rowstats_block(ra, fast, row_ok, key0, tg, a.causal, pos, qpos, a.scale, m, l);
-        tc::tmem_wait64(rb);
-        rowstats_block(rb, fast, row_ok, key0 + 64, tg, a.causal, pos + 64, qpos, a.scale, m, l);
+        tc::tmem_wait32(rb);
+        rowstats_block(rb, fast, row_ok, key0 + 32, tg, a.causal, pos + 32, qpos, a.scale, m, l);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -499,7 +530,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       }
     }
     if (row_ok) {
-      float* p = a.part + (((int64_t)bg * a.RC * kRowChunk + row) * a.n_splits + split) * 2;
+      float* p = a.part + (((int64_t)bg * a.RC * kRowChunk + row) * 2 * a.n_splits + 2 * split + half) * 2;
       p[0] = m;
       p[1] = l;
     }
@@ -512,7 +543,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// Row info: lse2 per row (+inf when the row sees nothing) and query position.
+// Row info: -lse2 per row (-inf when the row sees nothing) and query position.
 // grid (cdiv(RC*256, 256), B*Hkv)
 // ---------------------------------------------------------------------------
 __global__ void score_rowinfo_tc(TcArgs a) {
@@ -523,18 +554,19 @@ __global__ void score_rowinfo_tc(TcArgs a) {
   float lse = INFINITY;
   int qpos = 0x7fffffff;   // padded rows: lse = +inf already makes p = 0
   if (row < a.rows) {
-    const float* p = a.part + ((int64_t)bg * padded + row) * a.n_splits * 2;
+    // two slots per split (the column halves of its tiles)
+    const float* p = a.part + ((int64_t)bg * padded + row) * 2 * a.n_splits * 2;
     float M = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, p[2 * s]);
+    for (int s = 0; s < 2 * a.n_splits; ++s) M = fmaxf(M, p[2 * s]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int s = 0; s < a.n_splits; ++s) L += p[2 * s + 1] * exp2f(p[2 * s] - M);
+      for (int s = 0; s < 2 * a.n_splits; ++s) L += p[2 * s + 1] * exp2f(p[2 * s] - M);
     if (L > 0.f) lse = M + log2f(L);
     qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
   }
   // per 256-row chunk: 256 lse2 values, then 256 query positions
   float* chunk = reinterpret_cast<float*>(a.rowinfo + (int64_t)bg * padded + (row / kRowChunk) * kRowChunk);
-  chunk[row % kRowChunk] = lse;
+  chunk[row % kRowChunk] = -lse;   // stored negated: the FMA adds it
   chunk[kRowChunk + row % kRowChunk] = __int_as_float(qpos);
 }
 
@@ -542,8 +574,8 @@ __global__ void score_rowinfo_tc(TcArgs a) {
 // Pass 2: column sums.  grid (cdiv(n_tiles_max, tiles_per_cta2), B*Hkv).
 // Key tiles are taken in pairs (2p, 2p+1); for each row chunk rc the pair is
 // multiplied by the same Q chunk, tile 2p into TMEM buffer 0 and tile 2p+1
-// into buffer 1.  Epilogue warps 2-5 own even tiles, warps 6-9 odd tiles, so
-// each thread sums one key over every row chunk in registers.  When the rows
+// into buffer 1.  Half the epilogue warps own even tiles, half odd tiles; a
+// thread sums one key over its row half of every chunk in registers.  When the rows
 // fit one chunk the Q chunk stays resident and K tiles stream through four
 // stages; otherwise Q chunks stream through two stages (once per pair) and K
 // uses two stages.
@@ -571,6 +603,9 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   uint64_t* acc_full = bars + 18;         // [2]
   uint64_t* acc_free = bars + 20;         // [2]
   uint64_t* done = bars + 22;
+  uint64_t* hfull = bars + 23;            // [set][buf] the second row half's sums are in s_half
+  uint64_t* hempty = bars + 27;           // [set][buf] the first row half has read them
+  __shared__ float s_half[2][2][kKeyTile];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -591,7 +626,7 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     for (int s = 0; s < KS; ++s) {
       tc::mbar_init(&kfull[s], 1);
       tc::mbar_init(&kempty[s], 1);
-      tc::mbar_init(&pfree[s], 4);
+      tc::mbar_init(&pfree[s], kEpiWarps / 2);
     }
     for (int i = 0; i < QS; ++i) {
       tc::mbar_init(&qfull[i], 1);
@@ -600,7 +635,11 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_free[i], 4);
+      tc::mbar_init(&acc_free[i], kEpiWarps / 2);
+    }
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(&hfull[i], 4);
+      tc::mbar_init(&hempty[i], 4);
     }
     tc::mbar_init(done, 1);
     tc::fence_barrier_init();
@@ -720,8 +759,13 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       tc::mbar_wait(done, 0, kTimeoutNs);
     }
   } else {
-    // ---------------- epilogue: one key per thread, tiles of one parity ----------------
-    const int set = (warp - 2) / 4;       // 0: even tiles (buffer 0), 1: odd tiles
+    // ---------------- epilogue: one key and row half per thread ----------------
+    // 16 warps: (tile parity set: 0 even tiles / TMEM buffer 0, 1 odd tiles;
+    // TMEM lane quarter; row half of each chunk).  The second half hands its
+    // column sums to the first through s_half at the end of each pair.
+    const int e = warp - 2;
+    const int set = (e >> 2) & 1;
+    const int half = e >> 3;
     const int quarter = warp & 3;
     const int kl = quarter * 32 + lane;   // key within its tile
     int use = 0;
@@ -761,21 +805,20 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         }
         tc::tc_fence_after();
         if (ri == 0 && a.causal) kpos = pos_s[s * kKeyTile + kl];
-        const float* lse_s = reinterpret_cast<const float*>(info_s + qs * kRowChunk);
-        const int* qp_s = reinterpret_cast<const int*>(lse_s + kRowChunk);
-        // fast path: this key is visible to every row of the chunk
+        const float* lse_s = reinterpret_cast<const float*>(info_s + qs * kRowChunk) + half * 128;
+        const int* qp_s = reinterpret_cast<const int*>(info_s + qs * kRowChunk) + kRowChunk + half * 128;
+        // fast path: this key is visible to every row of the half chunk
         bool fast = !a.causal;
         if (a.causal) {
-          const int4 q4a = reinterpret_cast<const int4*>(qp_s)[lane * 2];
-          const int4 q4b = reinterpret_cast<const int4*>(qp_s)[lane * 2 + 1];
-          int mn = min(min(min(q4a.x, q4a.y), min(q4a.z, q4a.w)), min(min(q4b.x, q4b.y), min(q4b.z, q4b.w)));
+          const int4 q4 = reinterpret_cast<const int4*>(qp_s)[lane];
+          int mn = min(min(q4.x, q4.y), min(q4.z, q4.w));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
           fast = kpos <= mn;
         }
         float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-        colsum_tile(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256, fast, kpos, lse_s, qp_s,
-                    a.scale, cs0, cs1, cs2, cs3);
+        colsum_tile_seq<4>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128, fast,
+                           kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
         colsum += (cs0 + cs1) + (cs2 + cs3);
         tc::tc_fence_before();
         __syncwarp();
@@ -787,6 +830,26 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         use++;
       }
       if (stop) break;
+      // the two row halves meet: buffer p & 1 of this set, its (p >> 1)-th use
+      const int hb = set * 2 + (p & 1), k_use = p >> 1;
+      if (half == 1) {
+        const bool ok_e = k_use == 0 || tc::mbar_wait(&hempty[hb], (k_use - 1) & 1, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, ok_e)) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        s_half[set][p & 1][kl] = colsum;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&hfull[hb]);
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&hfull[hb], k_use & 1, kTimeoutNs))) {
+        record_timeout(a, &s_abort);
+        break;
+      }
+      colsum += s_half[set][p & 1][kl];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&hempty[hb]);
       const int key = tg.base + (t_begin + t) * kKeyTile + kl;
       if (key >= a.out_lo[b] && key < a.out_hi[b] && key >= tg.lo && key < tg.hi &&
           key < a.scores_stride) {
@@ -808,19 +871,6 @@ SE_DEV int group_tiles(const TcArgs& a, int bg) {
   return geom_ok(a, tg) ? tg.n_tiles : 0;
 }
 
-// Position of global tile index x: group and tile within it.
-SE_DEV void locate(const TcArgs& a, int x, int& bg, int& tile) {
-  bg = 0;
-  int base = 0;
-  const int groups = a.B * a.Hkv;
-  while (bg < groups) {
-    const int n = group_tiles(a, bg);
-    if (x < base + n) break;
-    base += n;
-    ++bg;
-  }
-  tile = x - base;
-}
 
 // ---------------------------------------------------------------------------
 // Pass 1, persistent form for one row chunk (RC == 1).  grid = the number of
@@ -830,10 +880,43 @@ SE_DEV void locate(const TcArgs& a, int x, int& bg, int& tile) {
 // CTA: part[(group * 256 + row) * C + c].  score_rowinfo_persistent merges the
 // slots of the CTAs whose ranges meet the group.
 // ---------------------------------------------------------------------------
-SE_DEV int total_tiles(const TcArgs& a) {
-  int total = 0;
-  for (int bg = 0; bg < a.B * a.Hkv; ++bg) total += group_tiles(a, bg);
-  return total;
+constexpr int kMaxGroupsP = 2048;   // groups the persistent passes index in shared memory
+
+// s_pre[x] = key tiles of groups 0 .. x-1, s_pre[groups] = all tiles.  Called
+// by every thread of the CTA (it synchronises the CTA).
+SE_DEV void group_prefix(const TcArgs& a, int* s_pre) {
+  const int groups = a.B * a.Hkv;
+  for (int x = threadIdx.x; x < groups; x += blockDim.x) s_pre[x + 1] = group_tiles(a, x);
+  if (threadIdx.x == 0) s_pre[0] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < groups; base += 32) {
+      const int i = base + lane;
+      int v = i < groups ? s_pre[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (i < groups) s_pre[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// Group holding global tile x (x < s_pre[groups]) and the tile within it.
+SE_DEV void locate_pre(const int* s_pre, int groups, int x, int& bg, int& tile) {
+  int lo = 0, hi = groups;            // largest g with s_pre[g] <= x
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  bg = lo;
+  while (bg < groups - 1 && s_pre[bg + 1] <= x) ++bg;   // skip empty groups
+  tile = x - s_pre[bg];
 }
 
 // The CTA whose range [c T / C, (c+1) T / C) holds tile x.
@@ -861,10 +944,13 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   __shared__ int s_abort;
   __shared__ int s_range[2];
 
+  __shared__ int s_pre[kMaxGroupsP + 1];
+  const int groups = a.B * a.Hkv;
+  group_prefix(a, s_pre);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    const int total = total_tiles(a);
+    const int total = s_pre[groups];
     s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
     s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
     for (int i = 0; i < KS; ++i) {
@@ -893,10 +979,10 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
       int bg = 0, tile = 0;
-      locate(a, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
       int cur = -1, gi = 0, issued = 0;
       for (int i = 0; i < n_my && !aborted(&s_abort); ++i) {
-        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
           if (gi > 0 && !tc::mbar_wait(q_done, (gi - 1) & 1, kTimeoutNs)) {
@@ -928,10 +1014,10 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     if (tc::elect_one()) {
       const uint32_t idesc = tc::idesc_bf16_f32(128, kKeyTile);
       int bg = 0, tile = 0;
-      locate(a, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
       int cur = -1, gi = 0;
       for (int i = 0; i < n_my && !aborted(&s_abort); ++i) {
-        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
         if (bg != cur) {
           if (gi > 0) tc::mma_commit(q_done);
           if (!tc::mbar_wait(q_full, gi & 1, kTimeoutNs)) {
@@ -969,21 +1055,23 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       tc::mbar_wait(done, 0, kTimeoutNs);
     }
   } else {
+    // 16 warps: (row block mb, TMEM lane quarter, column half of each tile)
     const int e = warp - 2;
-    const int mb = e / 4;
+    const int mb = (e >> 2) & 1;
+    const int half = e >> 3;
     const int quarter = warp & 3;
     const int r = mb * 128 + quarter * 32 + lane;   // row of the group
     const bool row_ok = r < a.rows;
     int bg = 0, tile = 0;
-    locate(a, x0, bg, tile);
+    if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
     int cur = -1, qpos = -1;
     float m = -INFINITY, l = 0.f;
     for (int i = 0; i < n_my; ++i) {
-      while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+      while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
       const int b = bg / a.Hkv;
       if (bg != cur) {
         if (cur >= 0 && row_ok) {
-          float* p = a.part + (((int64_t)cur * kRowChunk + r) * gridDim.x + blockIdx.x) * 2;
+          float* p = a.part + (((int64_t)cur * kRowChunk + r) * 2 * gridDim.x + 2 * blockIdx.x + half) * 2;
           p[0] = m;
           p[1] = l;
         }
@@ -1002,26 +1090,26 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       }
       tc::tc_fence_after();
       const TileGeom tg = TileGeom::make(a, b);
-      const int key0 = tg.base + tile * kKeyTile;
-      const int32_t* pos = pos_s + s * kKeyTile;
-      bool fast = row_ok && key0 >= tg.lo && key0 + kKeyTile <= tg.hi;
+      const int key0 = tg.base + tile * kKeyTile + half * 64;   // this warp's 64 columns
+      const int32_t* pos = pos_s + s * kKeyTile + half * 64;
+      bool fast = row_ok && key0 >= tg.lo && key0 + 64 <= tg.hi;
       if (a.causal) {
-        const int4 p4 = reinterpret_cast<const int4*>(pos)[lane];
-        int mx = max(max(p4.x, p4.y), max(p4.z, p4.w));
+        const int2 p2 = reinterpret_cast<const int2*>(pos)[lane];
+        int mx = max(p2.x, p2.y);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         fast = fast && mx <= qpos;
       }
       {
-        // two 64-column blocks; the second loads while the first is reduced
-        uint32_t ra[64], rb[64];
-        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128;
-        tc::tmem_ld64_async(tb, ra);
-        tc::tmem_wait64(ra);
-        tc::tmem_ld64_async(tb + 64, rb);
+        // two 32-column blocks; the second loads while the first is reduced
+        uint32_t ra[32], rb[32];
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + mb * 128 + half * 64;
+        tc::tmem_ld32_async(tb, ra);
+        tc::tmem_wait32(ra);
+        tc::tmem_ld32_async(tb + 32, rb);
         rowstats_block(ra, fast, row_ok, key0, tg, a.causal, pos, qpos, a.scale, m, l);
-        tc::tmem_wait64(rb);
-        rowstats_block(rb, fast, row_ok, key0 + 64, tg, a.causal, pos + 64, qpos, a.scale, m, l);
+        tc::tmem_wait32(rb);
+        rowstats_block(rb, fast, row_ok, key0 + 32, tg, a.causal, pos + 32, qpos, a.scale, m, l);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -1032,7 +1120,7 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       ++tile;
     }
     if (cur >= 0 && row_ok) {
-      float* p = a.part + (((int64_t)cur * kRowChunk + r) * gridDim.x + blockIdx.x) * 2;
+      float* p = a.part + (((int64_t)cur * kRowChunk + r) * 2 * gridDim.x + 2 * blockIdx.x + half) * 2;
       p[0] = m;
       p[1] = l;
     }
@@ -1049,33 +1137,27 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
 __global__ void score_rowinfo_persistent_tc(TcArgs a, int n_ctas) {
   const int bg = blockIdx.y, b = bg / a.Hkv;
   const int row = threadIdx.x;
-  __shared__ int s_first, s_last;
-  if (threadIdx.x == 0) {
-    int64_t T = 0, gstart = 0;
-    for (int x = 0; x < a.B * a.Hkv; ++x) {
-      const int n = group_tiles(a, x);
-      if (x < bg) gstart += n;
-      T += n;
-    }
-    const int n = group_tiles(a, bg);
-    s_first = (n > 0 && T > 0) ? cta_of(gstart, T, n_ctas) : 0;
-    s_last = (n > 0 && T > 0) ? cta_of(gstart + n - 1, T, n_ctas) : -1;
-  }
-  __syncthreads();
+  __shared__ int s_pre[kMaxGroupsP + 1];
+  group_prefix(a, s_pre);
+  const int64_t T = s_pre[a.B * a.Hkv], gstart = s_pre[bg];
+  const int n = s_pre[bg + 1] - s_pre[bg];
+  const int first = (n > 0 && T > 0) ? cta_of(gstart, T, n_ctas) : 0;
+  const int last = (n > 0 && T > 0) ? cta_of(gstart + n - 1, T, n_ctas) : -1;
   float lse = INFINITY;
   int qpos = 0x7fffffff;
   if (row < a.rows) {
-    const float* p = a.part + ((int64_t)bg * kRowChunk + row) * n_ctas * 2;
+    // two slots per CTA (the column halves of its tiles)
+    const float* p = a.part + ((int64_t)bg * kRowChunk + row) * 2 * n_ctas * 2;
     float M = -INFINITY;
-    for (int c = s_first; c <= s_last; ++c) M = fmaxf(M, p[2 * c]);
+    for (int c = 2 * first; c <= 2 * last + 1; ++c) M = fmaxf(M, p[2 * c]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int c = s_first; c <= s_last; ++c) L += p[2 * c + 1] * exp2f(p[2 * c] - M);
+      for (int c = 2 * first; c <= 2 * last + 1; ++c) L += p[2 * c + 1] * exp2f(p[2 * c] - M);
     if (L > 0.f) lse = M + log2f(L);
     qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
   }
   float* chunk = reinterpret_cast<float*>(a.rowinfo + (int64_t)bg * kRowChunk);
-  chunk[row] = lse;
+  chunk[row] = -lse;   // stored negated: the FMA adds it
   chunk[kRowChunk + row] = __int_as_float(qpos);
 }
 
@@ -1085,8 +1167,10 @@ __global__ void score_rowinfo_persistent_tc(TcArgs a, int n_ctas) {
 // global sequence of (group, key tile) pairs, so the last wave is full and the
 // pipeline runs across tiles of consecutive groups without refilling.  The Q
 // chunk and row info of a group are loaded when the group changes (after the
-// MMA and both epilogue sets are done with the previous ones).  Epilogue warps
-// 2-5 take the CTA's even local tiles (TMEM buffer 0), warps 6-9 the odd ones.
+// MMA and both epilogue sets are done with the previous ones).  One set of
+// eight epilogue warps takes the CTA's even local tiles (TMEM buffer 0), the
+// other the odd ones; within a set, the two row halves of a key meet in
+// shared memory.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
@@ -1108,28 +1192,37 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   uint64_t* acc_full = bars + 15;    // [2]
   uint64_t* acc_free = bars + 17;    // [2]
   uint64_t* done = bars + 19;
+  uint64_t* hfull = bars + 20;       // [set][buf] the second row half's sums are in s_half
+  uint64_t* hempty = bars + 24;      // [set][buf] the first row half has read them
+  __shared__ float s_half[2][2][kKeyTile];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_range[2];
 
+  __shared__ int s_pre[kMaxGroupsP + 1];
+  const int groups = a.B * a.Hkv;
+  group_prefix(a, s_pre);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    int total = 0;
-    for (int bg = 0; bg < a.B * a.Hkv; ++bg) total += group_tiles(a, bg);
+    const int total = s_pre[groups];
     s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
     s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
     for (int i = 0; i < KS; ++i) {
       tc::mbar_init(&kfull[i], 1);
       tc::mbar_init(&kempty[i], 1);
-      tc::mbar_init(&pfree[i], 4);
+      tc::mbar_init(&pfree[i], kEpiWarps / 2);
     }
     tc::mbar_init(qfull, 1);
     tc::mbar_init(qdone, 1);
     tc::mbar_init(ifree, kEpiWarps);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_free[i], 4);
+      tc::mbar_init(&acc_free[i], kEpiWarps / 2);
+    }
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(&hfull[i], 4);
+      tc::mbar_init(&hempty[i], 4);
     }
     tc::mbar_init(done, 1);
     tc::fence_barrier_init();
@@ -1147,10 +1240,10 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
       int bg = 0, tile = 0;
-      locate(a, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
       int cur = -1, gi = 0, issued = 0;
       for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
-        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
           if (gi > 0 && (!tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs) ||
@@ -1193,11 +1286,11 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     if (tc::elect_one()) {
       const uint32_t idesc = tc::idesc_bf16_f32(128, kRowChunk);
       int bg = 0, tile = 0;
-      locate(a, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
       int cur = -1, gi = 0;
       int uses[2] = {0, 0};
       for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
-        while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
         if (bg != cur) {
           if (gi > 0) tc::mma_commit(qdone);       // previous group's MMAs read its Q
           if (!tc::mbar_wait(qfull, gi & 1, kTimeoutNs)) {
@@ -1233,15 +1326,19 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       tc::mbar_wait(done, 0, kTimeoutNs);
     }
   } else {
-    // ---------------- epilogue: one key per thread ----------------
-    const int set = (warp - 2) / 4;
+    // ---------------- epilogue: one key per thread and row half ----------------
+    // 16 warps: (tile parity set, TMEM lane quarter, row half); the second
+    // half hands its partial sums to the first through s_half.
+    const int e = warp - 2;
+    const int set = (e >> 2) & 1;
+    const int half = e >> 3;
     const int quarter = warp & 3;
     const int kl = quarter * 32 + lane;
     int bg = 0, tile = 0;
-    locate(a, x0, bg, tile);
+    if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
     int cur = -1, gi = 0, use = 0;
     for (int lt = 0; lt < n_my; ++lt) {
-      while (tile >= group_tiles(a, bg)) { ++bg; tile = 0; }
+      while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
       if (bg != cur) {
         // leaving a group: both sets release its row info
         if (gi > 0) {
@@ -1266,30 +1363,51 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       }
       tc::tc_fence_after();
       const int kpos = a.causal ? pos_s[s * kKeyTile + kl] : 0;
-      const float* lse_s = reinterpret_cast<const float*>(info_s);
-      const int* qp_s = reinterpret_cast<const int*>(lse_s + kRowChunk);
+      const float* lse_s = reinterpret_cast<const float*>(info_s) + half * 128;
+      const int* qp_s = reinterpret_cast<const int*>(info_s) + kRowChunk + half * 128;
       bool fast = !a.causal;
       if (a.causal) {
-        const int4 q4a = reinterpret_cast<const int4*>(qp_s)[lane * 2];
-        const int4 q4b = reinterpret_cast<const int4*>(qp_s)[lane * 2 + 1];
-        int mn = min(min(min(q4a.x, q4a.y), min(q4a.z, q4a.w)), min(min(q4b.x, q4b.y), min(q4b.z, q4b.w)));
+        const int4 q4 = reinterpret_cast<const int4*>(qp_s)[lane];
+        int mn = min(min(q4.x, q4.y), min(q4.z, q4.w));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         fast = kpos <= mn;
       }
       float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-      colsum_tile(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256, fast, kpos, lse_s, qp_s,
-                  a.scale, cs0, cs1, cs2, cs3);
+      colsum_tile_seq<4>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128, fast,
+                         kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&acc_free[set]);
         tc::mbar_arrive(&pfree[s]);
       }
+      float colsum = (cs0 + cs1) + (cs2 + cs3);
+      const int hbuf = use & 1;              // s_half buffer of this tile
+      const int hb = set * 2 + hbuf;
+      const int k_use = use >> 1;           // earlier uses of this buffer
       ++use;
+      if (half == 1) {
+        const bool ok = k_use == 0 || tc::mbar_wait(&hempty[hb], (k_use - 1) & 1, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        s_half[set][hbuf][kl] = colsum;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&hfull[hb]);
+        ++tile;
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&hfull[hb], k_use & 1, kTimeoutNs))) {
+        record_timeout(a, &s_abort);
+        break;
+      }
+      colsum += s_half[set][hbuf][kl];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&hempty[hb]);
       const TileGeom tg = TileGeom::make(a, b);
       const int key = tg.base + tile * kKeyTile + kl;
-      const float colsum = (cs0 + cs1) + (cs2 + cs3);
       if (key >= a.out_lo[b] && key < a.out_hi[b] && key >= tg.lo && key < tg.hi &&
           key < a.scores_stride) {
         float* out = a.scores + (int64_t)bg * a.scores_stride + key;
@@ -1366,7 +1484,7 @@ constexpr int kMaxPersistentCTAs = 256;   // partial slots per row of the persis
 size_t score_tc_ws(const se_paged_kv* kv, int w, int n_max) {
   const TcPlan p = plan(kv, w, n_max);
   WsCarver c(nullptr);
-  const int slots = p.RC == 1 ? std::max(p.n_splits, kMaxPersistentCTAs) : p.n_splits;
+  const int slots = std::max(2 * p.n_splits, p.RC == 1 ? 2 * kMaxPersistentCTAs : 0);
   c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
   return c.bytes();
@@ -1412,7 +1530,7 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
   a.causal = causal; a.accumulate = accumulate; a.n_max = n_max;
   a.scores = scores; a.scores_stride = scores_stride;
   WsCarver c(ws);
-  const int slots = p.RC == 1 ? std::max(p.n_splits, kMaxPersistentCTAs) : p.n_splits;
+  const int slots = std::max(2 * p.n_splits, p.RC == 1 ? 2 * kMaxPersistentCTAs : 0);
   a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   a.rowinfo = c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
   a.n_splits = p.n_splits; a.tiles_per_split = p.tiles_per_split;
@@ -1435,7 +1553,7 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
     attrs = true;
   }
   const int groups = kv->B * kv->Hkv;
-  if (p.RC == 1) {
+  if (p.RC == 1 && groups <= kMaxGroupsP) {
     // one row chunk: persistent CTAs, one per SM, over the (group, tile) sequence
     static int n_sm = 0;
     if (n_sm == 0) {

@@ -71,7 +71,7 @@ def h2o_prefill_chunk(c: Cache, acc: np.ndarray, q_chunk, q_pos, k_chunk, v_chun
     """One chunk of H2O chunk-wise prefill eviction (SparseEngine "How it
     works": H2O evicts during prefill, chunk by chunk, on accumulated scores).
 
-    Reading (xviii): the chunk's keys and values are written first; its
+    Reading (xix): the chunk's keys and values are written first; its
     queries then attend causally to every resident entry (earlier survivors
     and the chunk itself) and their group-summed weights are added to the
     running scores (new entries start at 0); when more than heavy + recent
