@@ -41,7 +41,7 @@ EXPORTED = [
     "se_quest_build_meta", "se_quest_page_select", "se_quest_page_select_workspace_size",
     "se_sparse_decode_attn", "se_sparse_decode_attn_workspace_size",
     "se_sparse_decode_attn_static",
-    "se_append_kv", "se_append_kv_workspace_size",
+    "se_append_kv", "se_append_kv_workspace_size", "se_quest_decode_step",
     "se_status_string", "se_version",
 ]
 
@@ -102,6 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "se_append_kv": [P, c_void_p, c_void_p, c_int32, c_void_p, c_int64, c_void_p, c_void_p,
                          c_void_p, c_size_t, c_void_p],
         "se_append_kv_workspace_size": [P],
+        "se_quest_decode_step": [P, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                 c_void_p, c_void_p],
         "se_status_string": [c_int32],
         "se_version": [],
     }
@@ -278,6 +280,13 @@ def se_append_kv(kv, k_new, v_new, *, aux=None, kmin=None, kmax=None, workspace=
     _check("se_append_kv", _lib.se_append_kv(
         d, _ptr(k_new), _ptr(v_new), n_new, _ptr(aux), aux.shape[-1] if aux is not None else 0,
         _ptr(kmin), _ptr(kmax), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def se_quest_decode_step(kv, kmin, kmax, q, o, *, top_pages, page_idx=None, n_sel=None,
+                         stream=None):
+    _check("se_quest_decode_step", _lib.se_quest_decode_step(
+        ctypes.byref(kv), _ptr(kmin), _ptr(kmax), _ptr(q), top_pages, _ptr(o), _ptr(page_idx),
+        _ptr(n_sel), _stream(stream)))
 
 
 def workspace_sizes(kv, *, w=1, n_max=1, max_keep=0, max_blocks=1, max_entries=1) -> dict:

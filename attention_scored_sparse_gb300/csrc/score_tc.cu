@@ -1170,7 +1170,9 @@ __global__ void score_rowinfo_persistent_tc(TcArgs a, int n_ctas) {
 // MMA and both epilogue sets are done with the previous ones).  One set of
 // eight epilogue warps takes the CTA's even local tiles (TMEM buffer 0), the
 // other the odd ones; within a set, the two row halves of a key meet in
-// shared memory.
+// shared memory.  Each CTA walks its tile range backwards: pass 1 walked it
+// forwards, so the first tiles pass 2 needs are the ones pass 1 loaded last,
+// the most likely to be still in L2.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
@@ -1240,10 +1242,10 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
       int bg = 0, tile = 0;
-      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x1 - 1, bg, tile);
       int cur = -1, gi = 0, issued = 0;
       for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
-        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
+        while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
           if (gi > 0 && (!tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs) ||
@@ -1275,7 +1277,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         load_k_tile(a, &kmap, tg, b, g, tile, k_s + s * kKTileBytes,
                     a.causal ? pos_s + s * kKeyTile : nullptr, &kfull[s]);
         issued = lt + 1;
-        ++tile;
+        --tile;
       }
       for (int i = max(0, issued - KS); i < issued; ++i)
         tc::mbar_wait(&kfull[i % KS], (i / KS) & 1, kTimeoutNs);
@@ -1286,11 +1288,11 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     if (tc::elect_one()) {
       const uint32_t idesc = tc::idesc_bf16_f32(128, kRowChunk);
       int bg = 0, tile = 0;
-      if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
+      if (n_my > 0) locate_pre(s_pre, groups, x1 - 1, bg, tile);
       int cur = -1, gi = 0;
       int uses[2] = {0, 0};
       for (int lt = 0; lt < n_my && !aborted(&s_abort); ++lt) {
-        while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
+        while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
         if (bg != cur) {
           if (gi > 0) tc::mma_commit(qdone);       // previous group's MMAs read its Q
           if (!tc::mbar_wait(qfull, gi & 1, kTimeoutNs)) {
@@ -1320,7 +1322,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         tc::mma_commit(&kempty[s]);
         tc::mma_commit(&acc_full[buf]);
         uses[buf]++;
-        ++tile;
+        --tile;
       }
       tc::mma_commit(done);
       tc::mbar_wait(done, 0, kTimeoutNs);
@@ -1335,10 +1337,10 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     const int quarter = warp & 3;
     const int kl = quarter * 32 + lane;
     int bg = 0, tile = 0;
-    if (n_my > 0) locate_pre(s_pre, groups, x0, bg, tile);
+    if (n_my > 0) locate_pre(s_pre, groups, x1 - 1, bg, tile);
     int cur = -1, gi = 0, use = 0;
     for (int lt = 0; lt < n_my; ++lt) {
-      while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
+      while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
       if (bg != cur) {
         // leaving a group: both sets release its row info
         if (gi > 0) {
@@ -1352,7 +1354,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         cur = bg;
         ++gi;
       }
-      if ((lt & 1) != set) { ++tile; continue; }
+      if ((lt & 1) != set) { --tile; continue; }
       const int b = bg / a.Hkv;
       const int s = lt % KS;
       bool w_ok = tc::mbar_wait(&acc_full[set], use & 1, kTimeoutNs);
@@ -1396,7 +1398,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         s_half[set][hbuf][kl] = colsum;
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&hfull[hb]);
-        ++tile;
+        --tile;
         continue;
       }
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&hfull[hb], k_use & 1, kTimeoutNs))) {
@@ -1413,7 +1415,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         float* out = a.scores + (int64_t)bg * a.scores_stride + key;
         *out = a.accumulate ? *out + colsum : colsum;
       }
-      ++tile;
+      --tile;
     }
   }
   __syncthreads();

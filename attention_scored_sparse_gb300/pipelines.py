@@ -15,7 +15,8 @@ import torch
 from . import (SE_COMPACT_FRESH_PAGES, SE_COMPACT_MOVE_LAST, SE_SELECT_EVICT_ONE,
                SE_SELECT_KARA_CHUNK, SE_SELECT_TOPK, SE_VIEW_DENSE, SE_VIEW_PAGES, kv_desc,
                se_append_kv, se_compact_evict, se_prune_span, se_quest_build_meta,
-               se_quest_page_select, se_score_window, se_sparse_decode_attn, se_topk_select,
+               se_quest_decode_step, se_quest_page_select, se_score_window,
+               se_sparse_decode_attn, se_topk_select,
                workspace_sizes)
 
 
@@ -121,6 +122,11 @@ class QuestDecode(_Base):
     def step(self, q, o, stream=None):
         self.select(q, stream)
         self.decode(q, o, stream)
+
+    def step_fused(self, q, o, stream=None):
+        """The same step as one launch (bounds, selection and attention)."""
+        se_quest_decode_step(self.kv, self.kmin, self.kmax, q, o, top_pages=self.top,
+                             page_idx=self.page_idx, n_sel=self.n_sel, stream=stream)
 
 
 class H2O(_Base):

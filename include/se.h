@@ -260,6 +260,26 @@ se_status se_quest_page_select(const se_paged_kv* kv, const void* kmin, const vo
                                size_t workspace_bytes, void* stream);
 size_t se_quest_page_select_workspace_size(const se_paged_kv* kv, int32_t max_blocks);
 
+/*
+ * se_quest_decode_step -- one Quest decode step in a single launch
+ * (SparseEngine "What it is" / "How it works": Quest page selection, then
+ * attention over the selected pages).  Results equal se_quest_page_select
+ * followed by se_sparse_decode_attn over the page view: per (b, g) the page
+ * bound U over full pages 0 .. nb-2 (nb = ceil(ctx_len / page_size)), the
+ * top `top_pages` by (U desc, page asc) plus page nb-1, and single-query
+ * attention of q over the tokens of those pages.
+ * kmin, kmax [num_pages][Hkv][D] (from se_quest_build_meta or kept current by
+ * se_append_kv); q, o [B][Hq][D].  page_idx [B][Hkv][top_pages + 1] (optional)
+ * receives the selected pages ascending, -1 padded; n_sel [B] (optional) the
+ * count.  No workspace: each (b, g) runs on one cluster of 8 CTAs.
+ * Supports bf16, D = 128, Hq / Hkv in {1, 2, 4, 8}, top_pages <= 255 and up
+ * to 16384 full pages per sequence; otherwise SE_ERR_UNSUPPORTED (host) or
+ * SE_ERR_BOUNDS on the device status (longer context, bad page id).
+ */
+se_status se_quest_decode_step(const se_paged_kv* kv, const void* kmin, const void* kmax,
+                               const void* q, int32_t top_pages, void* o, int32_t* page_idx,
+                               int32_t* n_sel, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* 5. Decode attention over a view                                            */
 /* ------------------------------------------------------------------------ */

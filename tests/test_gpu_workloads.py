@@ -91,7 +91,7 @@ def test_snapkv_llama8b_full(cuda_lib):
 # ---------------------------------------------------------------------------
 
 
-def _quest(cuda_lib, shape, steps):
+def _quest(cuda_lib, shape, steps, fused=False):
     inp = W.quest_inputs(shape, "cuda")
     pc = inp["cache"]
     c = ocache.from_tensors(pc)
@@ -107,7 +107,8 @@ def _quest(cuda_lib, shape, steps):
     for t in steps:
         q = inp["q_steps"][t]
         o = torch.empty_like(q)
-        pipe.step(q, o)
+        pipe.page_idx.fill_(-7)
+        (pipe.step_fused if fused else pipe.step)(q, o)
         torch.cuda.synchronize()
         ref = opipe.quest_step(c, kmin, kmax, q, shape.top_pages)
         got = pipe.page_idx.cpu().numpy()
@@ -127,14 +128,25 @@ def _quest(cuda_lib, shape, steps):
     assert (pc.ctx_len.cpu() == shape.ctx).all()
 
 
-def test_quest_reduced(cuda_lib):
-    _quest(cuda_lib, W.quest_decode(ctx=16 * 700 + 5, top_pages=64, steps=3), range(3))
+@pytest.mark.parametrize("fused", [False, True])
+def test_quest_reduced(cuda_lib, fused):
+    _quest(cuda_lib, W.quest_decode(ctx=16 * 700 + 5, top_pages=64, steps=3), range(3), fused)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_quest_fused_small_contexts(cuda_lib, fused):
+    # fewer full pages than top_pages; a context inside the first page; G = 8
+    _quest(cuda_lib, W.quest_decode(B=3, ctx=16 * 9 + 3, top_pages=20, steps=2), range(2), fused)
+    _quest(cuda_lib, W.quest_decode(B=2, ctx=11, top_pages=4, steps=1), range(1), fused)
+    _quest(cuda_lib, W.quest_decode(B=2, Hq=32, Hkv=4, ctx=16 * 300, top_pages=33, steps=1),
+           range(1), fused)
 
 
 @pytest.mark.slow
-def test_quest_full(cuda_lib):
+@pytest.mark.parametrize("fused", [False, True])
+def test_quest_full(cuda_lib, fused):
     """2 x 131072 tokens, top 128 pages + current: steps 0 and 63 checked."""
-    _quest(cuda_lib, W.quest_decode(), [0, 63])
+    _quest(cuda_lib, W.quest_decode(), [0, 63], fused)
 
 
 # ---------------------------------------------------------------------------

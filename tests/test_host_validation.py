@@ -134,3 +134,21 @@ def test_workspace_queries_grow_with_sizes():
     assert L.se_score_window_workspace_size(d, 64, 8192) >= L.se_score_window_workspace_size(d, 64, 4096)
     assert L.se_compact_evict_workspace_size(d, 512) >= L.se_compact_evict_workspace_size(d, 64)
     assert L.se_sparse_decode_attn_workspace_size(d, 4096) >= L.se_sparse_decode_attn_workspace_size(d, 128)
+
+
+def test_quest_decode_step_host_checks():
+    d, _ = kv()
+    # null buffers, negative top
+    assert L.se_quest_decode_step(d, None, FAKE, FAKE, 8, FAKE, None, None, None) == \
+        se.SE_ERR_INVALID_ARG
+    assert L.se_quest_decode_step(d, FAKE, FAKE, FAKE, -1, FAKE, None, None, None) == \
+        se.SE_ERR_INVALID_ARG
+    # more than 255 top pages, or a layout the fused kernel does not cover
+    assert L.se_quest_decode_step(d, FAKE, FAKE, FAKE, 256, FAKE, None, None, None) == \
+        se.SE_ERR_UNSUPPORTED
+    d64, _ = kv(D=64)
+    assert L.se_quest_decode_step(d64, FAKE, FAKE, FAKE, 8, FAKE, None, None, None) == \
+        se.SE_ERR_UNSUPPORTED
+    df, _ = kv(dtype=se.SE_F32)
+    assert L.se_quest_decode_step(df, FAKE, FAKE, FAKE, 8, FAKE, None, None, None) == \
+        se.SE_ERR_UNSUPPORTED
