@@ -228,11 +228,11 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   }
 }
 
-// Commits block tables, lengths, refcounts and free-list pushes.  grid: B.
-__global__ void __launch_bounds__(1024) compact_finalize_pages_kernel(se_paged_kv kv, CompactWs w) {
+// Commits block tables, lengths, refcounts and free-list pushes of sequence
+// b (one CTA of 1024 threads).
+SE_DEV void commit_pages(const se_paged_kv& kv, const CompactWs& w, int b) {
   __shared__ int tmp[33];
-  if (w.ctrl->abort) return;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int pb = w.pb[b], nn = w.n_new[b], ob = w.old_blocks[b];
   const int top0 = w.ctrl->top0, total_new = w.ctrl->total_new;
   __shared__ int s_off, s_total;
@@ -284,20 +284,18 @@ __global__ void __launch_bounds__(1024) compact_finalize_pages_kernel(se_paged_k
   }
 }
 
-// Commits slot maps (and aux) from the staged values; slots past the new
-// length become -1 (aux 0).  grid: (slot chunks of 1024, Hkv, B).
-__global__ void __launch_bounds__(256) compact_finalize_slots_kernel(se_paged_kv kv, float* aux,
-                                                                     int64_t aux_stride,
-                                                                     CompactWs w) {
-  if (w.ctrl->abort) return;
-  const int h = blockIdx.y, b = blockIdx.z;
+// Commits slot maps (and aux) of (b, h), slots [chunk * 4096, +4096) from
+// the rewritten base, from the staged values; slots past the new length
+// become -1 (aux 0).
+SE_DEV void commit_slots(const se_paged_kv& kv, float* aux, int64_t aux_stride,
+                         const CompactWs& w, int b, int h, int chunk) {
   const int P = kv.page_size;
   const int base = w.pb[b] * P;
   const int nctx = w.new_ctx[b], octx = w.old_ctx[b];
   const int s_end = max(nctx, octx);
-  const int s0 = base + blockIdx.x * 1024;
+  const int s0 = base + chunk * 4096;
   if (s0 >= s_end) return;
-  const int s1 = min(s0 + 1024, s_end);
+  const int s1 = min(s0 + 4096, s_end);
   const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
   int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
   const int64_t tb = ((int64_t)b * kv.Hkv + h) * w.row;
@@ -311,6 +309,20 @@ __global__ void __launch_bounds__(256) compact_finalize_slots_kernel(se_paged_kv
       if (ar) ar[s] = 0.f;
     }
   }
+}
+
+// Commit of a compaction.  grid: (1 + slot chunks of 4096, Hkv, B), 1024
+// threads; CTA (0, 0, b) commits the pages of sequence b, CTA (1 + c, h, b)
+// chunk c of the slot map of (b, h).  Nothing runs after a planning error.
+__global__ void __launch_bounds__(1024) compact_commit_kernel(se_paged_kv kv, float* aux,
+                                                              int64_t aux_stride, CompactWs w) {
+  if (w.ctrl->abort) return;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (blockIdx.x == 0) {
+    if (h == 0) commit_pages(kv, w, b);
+    return;
+  }
+  commit_slots(kv, aux, aux_stride, w, b, h, blockIdx.x - 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -730,9 +742,8 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
     default:
       return SE_ERR_UNSUPPORTED;
   }
-  compact_finalize_pages_kernel<<<kv->B, 1024, 0, st>>>(*kv, w);
   const int max_span = kv->max_pages_per_seq * kv->page_size;
-  compact_finalize_slots_kernel<<<dim3(cdiv(max_span, 1024), kv->Hkv, kv->B), 256, 0, st>>>(
+  compact_commit_kernel<<<dim3(1 + cdiv(max_span, 4096), kv->Hkv, kv->B), 1024, 0, st>>>(
       *kv, aux, aux_stride, w);
   return se_last_launch_status();
 }

@@ -58,6 +58,10 @@ struct DecodeArgs {
   float* part;   // [B][Hkv][n_chunks][G][D + 2]
   float* logits; // [B][Hkv][max_entries][G] or null
   int max_entries;
+  void* out;          // o [B][Hq][D]
+  float* acc;         // H2O running scores or null
+  int64_t acc_stride;
+  int32_t* done;      // [B][Hkv] chunk CTAs finished (zeroed before the launch)
 };
 
 // Resident slot of view entry e of (b, g), or -1.
@@ -81,6 +85,60 @@ SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
   if (a.view == SE_VIEW_DENSE) return ctx;
   if (a.view == SE_VIEW_PAGES) return a.n_sel * a.kv.page_size;
   return a.n_sel;
+}
+
+// Merges the chunk partials of (b, g), writes o and updates the running
+// scores.  Run by the last chunk CTA of (b, g) to finish (128 threads).
+template <typename T, int D, int G>
+SE_DEV void merge_chunks(const DecodeArgs& a, int b, int g) {
+  __shared__ float s_M[G], s_invL[G];
+  T* out = static_cast<T*>(a.out);
+  float* acc = a.acc;
+  const int64_t acc_stride = a.acc_stride;
+  const se_paged_kv& kv = a.kv;
+  const float* part = a.part + ((int64_t)b * kv.Hkv + g) * a.n_chunks * G * (D + 2);
+  if (threadIdx.x < G) {
+    const int j = threadIdx.x;
+    float M = -INFINITY;
+    for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, part[(c * G + j) * (D + 2) + D]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int c = 0; c < a.n_chunks; ++c) {
+        const float* pc = part + (c * G + j) * (D + 2);
+        L = fmaf(pc[D + 1], ex2(pc[D] - M), L);
+      }
+    s_M[j] = M;
+    s_invL[j] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
+    const int j = x / D, d = x % D;
+    const float M = s_M[j];
+    float v = 0.f;
+    if (M != -INFINITY)
+      for (int c = 0; c < a.n_chunks; ++c) {
+        const float* pc = part + (c * G + j) * (D + 2);
+        v = fmaf(pc[d], ex2(pc[D] - M), v);
+      }
+    v *= s_invL[j];
+    T* op = out + ((int64_t)b * kv.Hq + g * G + j) * D + d;
+    if constexpr (sizeof(T) == 2) *op = __float2bfloat16_rn(v);
+    else *op = v;
+  }
+  if (acc != nullptr && a.logits != nullptr) {
+    const int ctx = kv.ctx_len[b];
+    const int n_view = min(view_entries(a, ctx), a.max_entries);
+    const float* lg = a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G;
+    float* ar = acc + ((int64_t)b * kv.Hkv + g) * acc_stride;
+    for (int e = threadIdx.x; e < n_view; e += blockDim.x) {
+      const int s = view_slot(a, b, g, e, ctx);
+      if (s < 0) continue;
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < G; ++j) ps += ex2(lg[(int64_t)e * G + j] - s_M[j]) * s_invL[j];
+      ar[s] += ps;
+    }
+  }
 }
 
 // grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps.
@@ -261,6 +319,19 @@ __global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) 
       part[j * (D + 2) + D + 1] = L;
     }
   }
+  // the last chunk CTA of (b, g) to finish merges all chunks (no extra launch):
+  // the barrier orders the CTA's partial before thread 0's device-scope fence
+  // and count; the last CTA's fence orders the count before its reads
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int last = atomicAdd(a.done + (int64_t)b * kv.Hkv + g, 1) == a.n_chunks - 1;
+    if (last) __threadfence();
+    s_last = last;
+  }
+  __syncthreads();
+  if (s_last) merge_chunks<T, D, G>(a, b, g);
 }
 
 
@@ -553,63 +624,25 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
       part[j * (D + 2) + D + 1] = L;
     }
   }
-}
-
-// grid: (Hkv, B); 128 threads.  Merges chunks, writes o, updates acc.
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a, T* out, float* acc,
-                                                             int64_t acc_stride) {
-  __shared__ float s_M[G], s_invL[G];
-  const int g = blockIdx.x, b = blockIdx.y;
-  const se_paged_kv& kv = a.kv;
-  const float* part = a.part + ((int64_t)b * kv.Hkv + g) * a.n_chunks * G * (D + 2);
-  if (threadIdx.x < G) {
-    const int j = threadIdx.x;
-    float M = -INFINITY;
-    for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, part[(c * G + j) * (D + 2) + D]);
-    float L = 0.f;
-    if (M != -INFINITY)
-      for (int c = 0; c < a.n_chunks; ++c) {
-        const float* pc = part + (c * G + j) * (D + 2);
-        L = fmaf(pc[D + 1], ex2(pc[D] - M), L);
-      }
-    s_M[j] = M;
-    s_invL[j] = L > 0.f ? 1.f / L : 0.f;
+  // the last chunk CTA of (b, g) to finish merges all chunks (no extra launch):
+  // the barrier orders the CTA's partial before thread 0's device-scope fence
+  // and count; the last CTA's fence orders the count before its reads
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int last = atomicAdd(a.done + (int64_t)b * kv.Hkv + g, 1) == a.n_chunks - 1;
+    if (last) __threadfence();
+    s_last = last;
   }
   __syncthreads();
-  for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
-    const int j = x / D, d = x % D;
-    const float M = s_M[j];
-    float v = 0.f;
-    if (M != -INFINITY)
-      for (int c = 0; c < a.n_chunks; ++c) {
-        const float* pc = part + (c * G + j) * (D + 2);
-        v = fmaf(pc[d], ex2(pc[D] - M), v);
-      }
-    v *= s_invL[j];
-    T* op = out + ((int64_t)b * kv.Hq + g * G + j) * D + d;
-    if constexpr (sizeof(T) == 2) *op = __float2bfloat16_rn(v);
-    else *op = v;
-  }
-  if (acc != nullptr && a.logits != nullptr) {
-    const int ctx = kv.ctx_len[b];
-    const int n_view = min(view_entries(a, ctx), a.max_entries);
-    const float* lg = a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G;
-    float* ar = acc + ((int64_t)b * kv.Hkv + g) * acc_stride;
-    for (int e = threadIdx.x; e < n_view; e += blockDim.x) {
-      const int s = view_slot(a, b, g, e, ctx);
-      if (s < 0) continue;
-      float ps = 0.f;
-#pragma unroll
-      for (int j = 0; j < G; ++j) ps += ex2(lg[(int64_t)e * G + j] - s_M[j]) * s_invL[j];
-      ar[s] += ps;
-    }
-  }
+  if (s_last) merge_chunks<T, D, G>(a, b, g);
 }
 
 struct DecodeWs {
   float* part;
   float* logits;
+  int32_t* done;
 };
 
 static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, int n_chunks, void* ws,
@@ -619,6 +652,7 @@ static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, int n_chunk
   const int G = kv->Hq / kv->Hkv;
   w.part = c.take<float>((size_t)kv->B * kv->Hkv * n_chunks * G * (kv->D + 2));
   w.logits = c.take<float>((size_t)kv->B * kv->Hkv * max_entries * G);
+  w.done = c.take<int32_t>((size_t)kv->B * kv->Hkv);
   *bytes = c.bytes();
   return w;
 }
@@ -636,8 +670,7 @@ static int pick_chunk(const se_paged_kv* kv, int max_entries) {
 }
 
 template <typename T, int D, int G>
-static void launch_decode_t(const DecodeArgs& a, void* o, float* acc, int64_t acc_stride,
-                            cudaStream_t st) {
+static void launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   using Gm = StagedGeom<T, D, G>;
   const dim3 grid(a.n_chunks, a.kv.Hkv, a.kv.B);
   bool staged = Gm::STAGES > 0;
@@ -652,18 +685,15 @@ static void launch_decode_t(const DecodeArgs& a, void* o, float* acc, int64_t ac
     if (staged) decode_partial_kernel<T, D, G><<<grid, 128, Gm::SMEM, st>>>(a);
   }
   if (!staged) decode_partial_regs_kernel<T, D, G><<<grid, 128, 0, st>>>(a);
-  decode_combine_kernel<T, D, G><<<dim3(a.kv.Hkv, a.kv.B), 128, 0, st>>>(a, static_cast<T*>(o),
-                                                                          acc, acc_stride);
 }
 
 template <typename T, int D>
-static se_status launch_decode_d(const DecodeArgs& a, int G, void* o, float* acc,
-                                 int64_t acc_stride, cudaStream_t st) {
+static se_status launch_decode_d(const DecodeArgs& a, int G, cudaStream_t st) {
   switch (G) {
-    case 1: launch_decode_t<T, D, 1>(a, o, acc, acc_stride, st); return SE_OK;
-    case 2: launch_decode_t<T, D, 2>(a, o, acc, acc_stride, st); return SE_OK;
-    case 4: launch_decode_t<T, D, 4>(a, o, acc, acc_stride, st); return SE_OK;
-    case 8: launch_decode_t<T, D, 8>(a, o, acc, acc_stride, st); return SE_OK;
+    case 1: launch_decode_t<T, D, 1>(a, st); return SE_OK;
+    case 2: launch_decode_t<T, D, 2>(a, st); return SE_OK;
+    case 4: launch_decode_t<T, D, 4>(a, st); return SE_OK;
+    case 8: launch_decode_t<T, D, 8>(a, st); return SE_OK;
     default: return SE_ERR_UNSUPPORTED;
   }
 }
@@ -697,13 +727,15 @@ extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q,
   DecodeWs w = carve_decode(kv, max_entries, n_chunks, workspace, &need);
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   DecodeArgs a{*kv, q, view, sel, sel_stride, n_sel, chunk, n_chunks, w.part,
-               acc_scores ? w.logits : nullptr, max_entries};
+               acc_scores ? w.logits : nullptr, max_entries, o, acc_scores, acc_stride, w.done};
   const int G = kv->Hq / kv->Hkv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (kv->dtype == SE_BF16 && kv->D == 128) s = launch_decode_d<__nv_bfloat16, 128>(a, G, o, acc_scores, acc_stride, st);
-  else if (kv->dtype == SE_BF16 && kv->D == 64) s = launch_decode_d<__nv_bfloat16, 64>(a, G, o, acc_scores, acc_stride, st);
-  else if (kv->dtype == SE_F32 && kv->D == 128) s = launch_decode_d<float, 128>(a, G, o, acc_scores, acc_stride, st);
-  else if (kv->dtype == SE_F32 && kv->D == 64) s = launch_decode_d<float, 64>(a, G, o, acc_scores, acc_stride, st);
+  if (cudaMemsetAsync(w.done, 0, sizeof(int32_t) * kv->B * kv->Hkv, st) != cudaSuccess)
+    return SE_ERR_CUDA;
+  if (kv->dtype == SE_BF16 && kv->D == 128) s = launch_decode_d<__nv_bfloat16, 128>(a, G, st);
+  else if (kv->dtype == SE_BF16 && kv->D == 64) s = launch_decode_d<__nv_bfloat16, 64>(a, G, st);
+  else if (kv->dtype == SE_F32 && kv->D == 128) s = launch_decode_d<float, 128>(a, G, st);
+  else if (kv->dtype == SE_F32 && kv->D == 64) s = launch_decode_d<float, 64>(a, G, st);
   else return SE_ERR_UNSUPPORTED;
   if (s != SE_OK) return s;
   return se_last_launch_status();

@@ -54,8 +54,8 @@ struct QfArgs {
 // three radix rounds of 11, 11 and 10 bits.  Returns the threshold key T and
 // how many keys equal to T are taken (the lowest-indexed ones).
 template <int ITEMS>
-SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, uint32_t* s_prefix,
-                          int* s_remaining, uint32_t& T, int& need_eq) {
+SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tmp, int* s_digit,
+                          int* s_rem, uint32_t& T, int& need_eq) {
   const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0;
   int remaining = kk;
@@ -71,33 +71,9 @@ SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, uint3
       for (int i = 0; i < ITEMS; ++i)
         if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
       __syncthreads();
-      if (tid < 32) {
-        const int per = nbins / 32;      // lane l owns bins [l per, (l+1) per)
-        int tot = 0;
-        for (int j = 0; j < per; ++j) tot += hist[tid * per + j];
-        int suf = tot;                   // inclusive suffix over lanes >= tid
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_down_sync(0xffffffffu, suf, o);
-          if (tid + o < 32) suf += y;
-        }
-        const int above = suf - tot;
-        if (above < remaining && suf >= remaining) {
-          int acc = above;
-          for (int j = per - 1; j >= 0; --j) {
-            const int cnt = hist[tid * per + j];
-            if (acc + cnt >= remaining) {
-              *s_prefix = prefix | ((uint32_t)(tid * per + j) << shift);
-              *s_remaining = remaining - acc;
-              break;
-            }
-            acc += cnt;
-          }
-        }
-      }
-      __syncthreads();
-      prefix = *s_prefix;
-      remaining = *s_remaining;
+      radix_find_digit(hist, nbins, remaining, tmp, s_digit, s_rem);
+      prefix |= (uint32_t)*s_digit << shift;
+      remaining = *s_rem;
       pmask |= dmask << shift;
       __syncthreads();
     }
@@ -109,11 +85,11 @@ SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, uint3
 // Selection flags for the k largest keys (ties: lower index, i.e. lower
 // thread / item first) and each selected key's rank in index order.
 template <int ITEMS>
-SE_DEV int block_select(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tmp,
-                        uint32_t* s_prefix, int* s_remaining, bool (&sel)[ITEMS], int* total) {
+SE_DEV int block_select(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tmp, int* s_digit,
+                        int* s_rem, bool (&sel)[ITEMS], int* total) {
   uint32_t T;
   int need_eq;
-  block_kth_key<ITEMS>(key, kk, hist, s_prefix, s_remaining, T, need_eq);
+  block_kth_key<ITEMS>(key, kk, hist, tmp, s_digit, s_rem, T, need_eq);
   int c_eq = 0;
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
@@ -143,13 +119,14 @@ struct QfSmem {
                                              // the selected ones' (phase 3)
   int hist[2048];
   int tmp[33];
-  uint32_t prefix;
-  int remaining;
+  int digit;
+  int rem;
   int loc_n;
   uint32_t loc_key[kQfMaxTop];               // local top, ascending page order
   int32_t loc_page[kQfMaxTop];
   uint32_t all_key[kQfCtas * kQfMaxTop];     // CTA 0: the gathered local tops
   int32_t all_page[kQfCtas * kQfMaxTop];
+  int peer_n[kQfCtas];                       // CTA 0: local list sizes
   int sel_n;                                 // CTA 0: final list (read by peers)
   int32_t sel_page[kQfMaxTop];
   int my_n;                                  // this CTA's share of the list
@@ -158,6 +135,7 @@ struct QfSmem {
   float hm[2 * kQfAttnWarps][G], hl[2 * kQfAttnWarps][G];
   float ho[2 * kQfAttnWarps][G][128];
   float cm[G], cl[G];                        // this CTA's merged partial
+  float all_m[kQfCtas * G], all_l[kQfCtas * G];  // CTA 0: every CTA's (m, l)
   float co[G][128];
 };
 
@@ -197,10 +175,13 @@ quest_fused_kernel(QfArgs a) {
     unpack8_bf16(u, qv[j]);
   }
   bool bad_page = false;
-  constexpr int kInFlight = 8;
-  for (int base = 0; base < n_loc; base += kInFlight * (kQfThreads / 16)) {
-    uint4 mnr[kInFlight], mxr[kInFlight];
-    bool ok[kInFlight];
+  // rounds of kInFlight pages per half-warp; the next round's rows load while
+  // the current round is reduced
+  constexpr int kInFlight = 8, kRound = kInFlight * (kQfThreads / 16);
+  uint4 cmn[kInFlight], cmx[kInFlight];
+  bool cok[kInFlight];
+  auto load_round = [&](int base, uint4 (&mn)[kInFlight], uint4 (&mx)[kInFlight],
+                        bool (&ok)[kInFlight]) {
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
       const int i = base + u * (kQfThreads / 16) + hw;
@@ -209,17 +190,28 @@ quest_fused_kernel(QfArgs a) {
       bad_page |= i < n_loc && !ok[u];
       if (ok[u]) {
         const int64_t off = ((int64_t)page * kv.Hkv + g) * D + t * V;
-        mnr[u] = ldg_nc_v4(a.kmin + off);
-        mxr[u] = ldg_nc_v4(a.kmax + off);
+        mn[u] = ldg_nc_v4(a.kmin + off);
+        mx[u] = ldg_nc_v4(a.kmax + off);
       }
+    }
+  };
+  if (n_loc > 0) load_round(0, cmn, cmx, cok);
+  for (int base = 0; base < n_loc; base += kRound) {
+    uint4 nmn[kInFlight], nmx[kInFlight];
+    bool nok[kInFlight];
+    if (base + kRound < n_loc) {
+      load_round(base + kRound, nmn, nmx, nok);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) nok[u] = false;
     }
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
       float acc = 0.f;
-      if (ok[u]) {
+      if (cok[u]) {
         float mn[V], mx[V];
-        unpack8_bf16(mnr[u], mn);
-        unpack8_bf16(mxr[u], mx);
+        unpack8_bf16(cmn[u], mn);
+        unpack8_bf16(cmx[u], mx);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
           float part = 0.f;
@@ -231,7 +223,13 @@ quest_fused_kernel(QfArgs a) {
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       const int i = base + u * (kQfThreads / 16) + hw;
-      if (ok[u] && t == 0) sm.key[i] = float_key(acc);
+      if (cok[u] && t == 0) sm.key[i] = float_key(acc);
+    }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      cmn[u] = nmn[u];
+      cmx[u] = nmx[u];
+      cok[u] = nok[u];
     }
   }
   if (bad_page) set_status(kv.status, SE_ERR_BOUNDS);
@@ -250,8 +248,8 @@ quest_fused_kernel(QfArgs a) {
     block_exclusive_scan(n_valid, sm.tmp, &valid_total);
     bool sel[kQfItems];
     int total;
-    int pos = block_select<kQfItems>(key, min(top, valid_total), sm.hist, sm.tmp, &sm.prefix,
-                                     &sm.remaining, sel, &total);
+    int pos = block_select<kQfItems>(key, min(top, valid_total), sm.hist, sm.tmp, &sm.digit,
+                                     &sm.rem, sel, &total);
 #pragma unroll
     for (int i = 0; i < kQfItems; ++i)
       if (sel[i]) {
@@ -265,15 +263,22 @@ quest_fused_kernel(QfArgs a) {
 
   // ---- phase 2b: CTA 0 selects among the local tops ----
   if (rank == 0) {
-    int n_all = 0;
+    // warp r copies CTA r's local list (eight warps, eight CTAs)
+    static_assert(kQfThreads / 32 == kQfCtas, "one warp per CTA of the cluster");
+    if (tid < kQfCtas) sm.peer_n[tid] = cluster.map_shared_rank(&sm, tid)->loc_n;
+    __syncthreads();
+    const int w = tid >> 5;
+    int off = 0, n_all = 0;
     for (int r = 0; r < kQfCtas; ++r) {
-      const QfSmem<G>* peer = cluster.map_shared_rank(&sm, r);
-      const int n = peer->loc_n;
-      for (int i = tid; i < n; i += kQfThreads) {
-        sm.all_key[n_all + i] = peer->loc_key[i];
-        sm.all_page[n_all + i] = peer->loc_page[i];
+      off += r < w ? sm.peer_n[r] : 0;
+      n_all += sm.peer_n[r];
+    }
+    {
+      const QfSmem<G>* peer = cluster.map_shared_rank(&sm, w);
+      for (int i = lane; i < sm.peer_n[w]; i += 32) {
+        sm.all_key[off + i] = peer->loc_key[i];
+        sm.all_page[off + i] = peer->loc_page[i];
       }
-      n_all += n;
     }
     __syncthreads();
     uint32_t key[kQfGather];
@@ -284,8 +289,8 @@ quest_fused_kernel(QfArgs a) {
     }
     bool sel[kQfGather];
     int total;
-    int pos = block_select<kQfGather>(key, min(top, n_all), sm.hist, sm.tmp, &sm.prefix,
-                                      &sm.remaining, sel, &total);
+    int pos = block_select<kQfGather>(key, min(top, n_all), sm.hist, sm.tmp, &sm.digit,
+                                      &sm.rem, sel, &total);
 #pragma unroll
     for (int i = 0; i < kQfGather; ++i)
       if (sel[i]) sm.sel_page[pos++] = sm.all_page[tid * kQfGather + i];
@@ -454,17 +459,27 @@ quest_fused_kernel(QfArgs a) {
   }
   cluster.sync();                                     // every partial complete
   if (rank == 0) {
+    if (tid < kQfCtas * G) {
+      const QfSmem<G>* peer = cluster.map_shared_rank(&sm, tid / G);
+      sm.all_m[tid] = peer->cm[tid % G];
+      sm.all_l[tid] = peer->cl[tid % G];
+    }
+    __syncthreads();
     for (int x = tid; x < G * D; x += kQfThreads) {
       const int j = x / D, d = x % D;
+      float ov[kQfCtas];
+#pragma unroll
+      for (int r = 0; r < kQfCtas; ++r) ov[r] = cluster.map_shared_rank(&sm, r)->co[j][d];
       float M = -INFINITY;
-      for (int r = 0; r < kQfCtas; ++r) M = fmaxf(M, cluster.map_shared_rank(&sm, r)->cm[j]);
+#pragma unroll
+      for (int r = 0; r < kQfCtas; ++r) M = fmaxf(M, sm.all_m[r * G + j]);
       float acc = 0.f, L = 0.f;
       if (M != -INFINITY)
+#pragma unroll
         for (int r = 0; r < kQfCtas; ++r) {
-          const QfSmem<G>* peer = cluster.map_shared_rank(&sm, r);
-          const float f = exp2f(peer->cm[j] - M);
-          acc = fmaf(peer->co[j][d], f, acc);
-          L = fmaf(peer->cl[j], f, L);
+          const float f = exp2f(sm.all_m[r * G + j] - M);
+          acc = fmaf(ov[r], f, acc);
+          L = fmaf(sm.all_l[r * G + j], f, L);
         }
       a.o[((int64_t)b * kv.Hq + g * G + j) * D + d] = __float2bfloat16(L > 0.f ? acc / L : 0.f);
     }

@@ -94,6 +94,37 @@ SE_DEV int block_exclusive_scan(int v, int* tmp, int* total) {
   return base + x - v;
 }
 
+// Radix-select step: hist[0 .. nbins) holds the candidate count per digit;
+// finds the digit that holds the `remaining`-th largest key (counting from
+// the top digit down) and how many keys of that digit are still needed.
+// Every thread calls it (nbins a multiple of blockDim.x, or below it); one
+// block scan replaces a serial walk over the bins.  Results in *s_digit,
+// *s_rem (shared), valid after the call.
+SE_DEV void radix_find_digit(const int* hist, int nbins, int remaining, int* tmp, int* s_digit,
+                             int* s_rem) {
+  const int per = nbins >= (int)blockDim.x ? nbins / (int)blockDim.x : 1;
+  const int b0 = threadIdx.x * per;
+  int c = 0;
+  for (int j = 0; j < per; ++j)
+    if (b0 + j < nbins) c += hist[b0 + j];
+  int total;
+  const int ex = block_exclusive_scan(c, tmp, &total);
+  const int above = total - ex - c;          // keys in higher digits than this thread's
+  if (c > 0 && above < remaining && above + c >= remaining) {
+    int acc = above;
+    for (int j = per - 1; j >= 0; --j) {
+      const int cnt = b0 + j < nbins ? hist[b0 + j] : 0;
+      if (acc + cnt >= remaining) {
+        *s_digit = b0 + j;
+        *s_rem = remaining - acc;
+        break;
+      }
+      acc += cnt;
+    }
+  }
+  __syncthreads();
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Bump allocator over a caller-provided workspace (host side).

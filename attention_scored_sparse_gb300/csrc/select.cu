@@ -42,8 +42,7 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   extern __shared__ float s_sc[];
   __shared__ int tmp[33];
   __shared__ int hist[2048];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
+  __shared__ int s_digit, s_rem;
   __shared__ int s_before_force;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int lo = a.cand_lo[b], hi = a.cand_hi[b];
@@ -109,34 +108,9 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
       for (int i = 0; i < ITEMS; ++i)
         if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
       __syncthreads();
-      if (tid < 32) {
-        // lane l owns bins [l*per, (l+1)*per); suffix sums from the top bin down
-        const int per = nbins / 32;
-        int tot = 0;
-        for (int j = 0; j < per; ++j) tot += hist[tid * per + j];
-        int suf = tot;  // inclusive suffix over lanes >= tid
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_down_sync(0xffffffffu, suf, o);
-          if (tid + o < 32) suf += y;
-        }
-        const int above = suf - tot;
-        if (above < remaining && suf >= remaining) {
-          int acc = above;
-          for (int j = per - 1; j >= 0; --j) {
-            const int cnt = hist[tid * per + j];
-            if (acc + cnt >= remaining) {
-              s_prefix = prefix | ((uint32_t)(tid * per + j) << shift);
-              s_remaining = remaining - acc;
-              break;
-            }
-            acc += cnt;
-          }
-        }
-      }
-      __syncthreads();
-      prefix = s_prefix;
-      remaining = s_remaining;
+      radix_find_digit(hist, nbins, remaining, tmp, &s_digit, &s_rem);
+      prefix |= (uint32_t)s_digit << shift;
+      remaining = s_rem;
       pmask |= dmask << shift;
       __syncthreads();
     }
@@ -207,8 +181,7 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
   __shared__ int tmp[33];
   __shared__ int hist[2048];
   __shared__ int s_cnt[4];        // forced-in-range, equal-to-T, selected, selected-before-force
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
+  __shared__ int s_digit, s_rem;
   const int rank = (int)cluster.block_rank();
   const int h = blockIdx.x / kClusterCTAs, b = blockIdx.y, tid = threadIdx.x;
   const int lo = a.cand_lo[b], hi = a.cand_hi[b];
@@ -289,33 +262,9 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
       for (int j = 0; j < 2; ++j)
         if (tid + j * 1024 < nbins) hist[tid + j * 1024] = tot_local[j];
       __syncthreads();
-      if (tid < 32) {
-        const int perl = nbins / 32;
-        int tot = 0;
-        for (int j = 0; j < perl; ++j) tot += hist[tid * perl + j];
-        int suf = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_down_sync(0xffffffffu, suf, o);
-          if (tid + o < 32) suf += y;
-        }
-        const int above = suf - tot;
-        if (above < remaining && suf >= remaining) {
-          int acc = above;
-          for (int j = perl - 1; j >= 0; --j) {
-            const int cnt = hist[tid * perl + j];
-            if (acc + cnt >= remaining) {
-              s_prefix = prefix | ((uint32_t)(tid * perl + j) << shift);
-              s_remaining = remaining - acc;
-              break;
-            }
-            acc += cnt;
-          }
-        }
-      }
-      __syncthreads();
-      prefix = s_prefix;
-      remaining = s_remaining;
+      radix_find_digit(hist, nbins, remaining, tmp, &s_digit, &s_rem);
+      prefix |= (uint32_t)s_digit << shift;
+      remaining = s_rem;
       pmask |= dmask << shift;
       __syncthreads();
     }

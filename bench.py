@@ -300,7 +300,7 @@ def run_snapkv(args, torch, rank, world):
     }
     roof = dict(bound="tensor", achieved=detail["score_tflops"], unit="TFLOP/s",
                 kernel="se_score_window", per_launch=f"{flops:.4g} FLOP (one QK^T sweep)")
-    launches = 3 + 1 + 3 + 2
+    launches = 3 + 1 + 4 + 1     # score, select, compaction, decode kernels per step
     cfg = {"workload": f"{shape.name}: B={B} x {shape.ctx} tokens, Hq={shape.Hq}/Hkv={Hkv}, "
                        f"d={D}, window {shape.window}, pool {shape.pool_kernel}, budget "
                        f"{shape.budget}", "l2": "inputs larger than L2 (KV cache 570 MB)"}
@@ -420,7 +420,7 @@ def run_quest(args, torch, rank, world):
                 kernel="quest_fused_kernel (bounds + select + attention)",
                 per_launch=f"{meta_bytes + kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
-                launches=1 + 4 + 2, metric="decode tokens/s", e2e=None,
+                launches=1 + 4 + 1, metric="decode tokens/s", e2e=None,
                 cfg={"workload": "quest_decode: B=2 x 131072 tokens, top 128 pages + current, "
                                  "32/8 heads, d=128, bf16",
                      "l2": "L2 flushed (256 MB write) before every timed step"},
@@ -487,7 +487,7 @@ def run_h2o(args, torch, rank, world):
     roof = dict(bound="hbm", achieved=detail["step_gbs"], unit="GB/s", kernel="h2o step",
                 per_launch=f"{kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
-                launches=2 + 2 + 1 + 2, metric="decode tokens/s", e2e=None,
+                launches=2 + 1 + 1 + 2, metric="decode tokens/s", e2e=None,
                 cfg={"workload": "h2o_decode: B=64, 4096-token prompt, budget 1024+128, "
                                  "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
                 dtype="bf16")
@@ -577,7 +577,7 @@ def run_kara(args, torch, rank, world):
     roof = dict(bound="hbm", achieved=detail["prune_gbs"], unit="GB/s", kernel="se_prune_span",
                 per_launch=f"{prune_bytes:.4g} B (moved entries, read + write)")
     return dict(tokens=shape.B * shape.ctx, ms=ms, wall=t_wall, clocks=clocks, detail=detail,
-                roof=roof, launches=3 + 1 + 3 + 5 + 2, e2e=None,
+                roof=roof, launches=3 + 1 + 4 + 5 + 1, e2e=None,
                 cfg={"workload": "kara_prune: B=128 x 16384 tokens, window 256 (32 protected), "
                                  "chunk budget 64, prune [2048,6144) keep 20%",
                      "l2": "inputs larger than L2"}, dtype="bf16")

@@ -116,7 +116,10 @@ def _quest(cuda_lib, shape, steps, fused=False):
         for (b, g), sel in ref["sel"].items():
             U = ref["bounds"][(b, g)]
             ranking = {i: float(U[i]) for i in range(nb - 1)}
-            d = H.assert_keep_near(got[b, g], sel, ranking, min(shape.top_pages, nb - 1), [nb - 1])
+            row = got[b, g]
+            n = len(sel)
+            assert (row[n:] == -1).all(), (b, g, row)     # -1 after the selected pages
+            d = H.assert_keep_near(row[:n], sel, ranking, min(shape.top_pages, nb - 1), [nb - 1])
             same[(b, g)] = d == 0
         og = o.double().cpu().numpy()
         for (b, g), ref_o in ref["o"].items():
