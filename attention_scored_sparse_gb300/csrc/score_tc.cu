@@ -11,8 +11,9 @@
 //       thread owns one row and one 64-key half of every tile and keeps a
 //       base-2 running max / sum over its CTA's key range.  Partials per
 //       (key split, half) go to the workspace.
-//   rowinfo            the CUDA-core kernel merges the splits: -lse2 per row
-//       (plus the row's query position for causal masking).
+//   rowinfo            the splits merge into -lse2 per row (plus the row's
+//       query position for causal masking): a CUDA-core kernel when the rows
+//       span several chunks, pass 2's epilogue itself in the persistent form.
 //   pass 2 (colsum)    S^T = K_tile Q_rows^T with the 128 keys of a tile on
 //       TMEM lanes (M=128), N = 256 rows; each epilogue thread owns one key
 //       and one 128-row half and sums exp2(t - lse2_r) over its rows in
@@ -876,9 +877,9 @@ SE_DEV int group_tiles(const TcArgs& a, int bg) {
 // Pass 1, persistent form for one row chunk (RC == 1).  grid = the number of
 // SMs; CTA c takes tiles [c T / C, (c+1) T / C) of the global (group, tile)
 // sequence.  Each epilogue thread keeps its row's running max / sum per group
-// and writes it, when the group ends in this CTA, to the partial slot of this
-// CTA: part[(group * 256 + row) * C + c].  score_rowinfo_persistent merges the
-// slots of the CTAs whose ranges meet the group.
+// and writes it, when the group ends in this CTA, to the partial slots of
+// this CTA: part[(group * 256 + row) * 2C + 2c + half].  The persistent pass 2
+// merges the slots of the CTAs whose ranges meet a group when it starts it.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsP = 2048;   // groups the persistent passes index in shared memory
 
@@ -1132,33 +1133,22 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-// Row info for the persistent passes: merges the partial slots of the CTAs
-// whose tile ranges meet the group.  grid (1, B*Hkv), 256 threads.
-__global__ void score_rowinfo_persistent_tc(TcArgs a, int n_ctas) {
-  const int bg = blockIdx.y, b = bg / a.Hkv;
-  const int row = threadIdx.x;
-  __shared__ int s_pre[kMaxGroupsP + 1];
-  group_prefix(a, s_pre);
-  const int64_t T = s_pre[a.B * a.Hkv], gstart = s_pre[bg];
+
+// lse2 of row r of group bg from pass 1's partial slots (two per CTA whose
+// tile range meets the group; n_ctas CTAs ran pass 1); +inf when the row saw
+// no key.
+SE_DEV float row_lse2(const TcArgs& a, const int* s_pre, int groups, int bg, int r, int n_ctas) {
+  const int64_t T = s_pre[groups], gstart = s_pre[bg];
   const int n = s_pre[bg + 1] - s_pre[bg];
-  const int first = (n > 0 && T > 0) ? cta_of(gstart, T, n_ctas) : 0;
-  const int last = (n > 0 && T > 0) ? cta_of(gstart + n - 1, T, n_ctas) : -1;
-  float lse = INFINITY;
-  int qpos = 0x7fffffff;
-  if (row < a.rows) {
-    // two slots per CTA (the column halves of its tiles)
-    const float* p = a.part + ((int64_t)bg * kRowChunk + row) * 2 * n_ctas * 2;
-    float M = -INFINITY;
-    for (int c = 2 * first; c <= 2 * last + 1; ++c) M = fmaxf(M, p[2 * c]);
-    float L = 0.f;
-    if (M != -INFINITY)
-      for (int c = 2 * first; c <= 2 * last + 1; ++c) L += p[2 * c + 1] * exp2f(p[2 * c] - M);
-    if (L > 0.f) lse = M + log2f(L);
-    qpos = a.q_pos[(int64_t)b * a.w + row / a.G];
-  }
-  float* chunk = reinterpret_cast<float*>(a.rowinfo + (int64_t)bg * kRowChunk);
-  chunk[row] = -lse;   // stored negated: the FMA adds it
-  chunk[kRowChunk + row] = __int_as_float(qpos);
+  if (n <= 0 || T <= 0) return INFINITY;
+  const int first = cta_of(gstart, T, n_ctas), last = cta_of(gstart + n - 1, T, n_ctas);
+  const float* p = a.part + ((int64_t)bg * kRowChunk + r) * 2 * n_ctas * 2;
+  float M = -INFINITY;
+  for (int c = 2 * first; c <= 2 * last + 1; ++c) M = fmaxf(M, p[2 * c]);
+  float L = 0.f;
+  if (M != -INFINITY)
+    for (int c = 2 * first; c <= 2 * last + 1; ++c) L += p[2 * c + 1] * exp2f(p[2 * c] - M);
+  return L > 0.f ? M + log2f(L) : INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -1190,12 +1180,13 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   uint64_t* pfree = bars + 8;        // [KS]
   uint64_t* qfull = bars + 12;
   uint64_t* qdone = bars + 13;       // MMA done with the group's Q
-  uint64_t* ifree = bars + 14;       // both epilogue sets done with the group's row info
+  uint64_t* ifree = bars + 14;       // every epilogue warp done with the group's row info
   uint64_t* acc_full = bars + 15;    // [2]
   uint64_t* acc_free = bars + 17;    // [2]
   uint64_t* done = bars + 19;
   uint64_t* hfull = bars + 20;       // [set][buf] the second row half's sums are in s_half
   uint64_t* hempty = bars + 24;      // [set][buf] the first row half has read them
+  uint64_t* ifull = bars + 28;       // the group's row info is in info_s
   __shared__ float s_half[2][2][kKeyTile];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -1218,6 +1209,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     tc::mbar_init(qfull, 1);
     tc::mbar_init(qdone, 1);
     tc::mbar_init(ifree, kEpiWarps);
+    tc::mbar_init(ifull, kRowChunk / 32);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
       tc::mbar_init(&acc_free[i], kEpiWarps / 2);
@@ -1248,21 +1240,13 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
-          if (gi > 0 && (!tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs) ||
-                         !tc::mbar_wait(ifree, (gi - 1) & 1, kTimeoutNs))) {
+          if (gi > 0 && !tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs)) {
             record_timeout(a, &s_abort);
             break;
           }
-          tc::mbar_arrive_expect_tx(qfull, kQChunkBytes + kRowChunk * 8);
-          const int qpc = kRowChunk / a.G;
-          (void)qpc;
+          tc::mbar_arrive_expect_tx(qfull, kQChunkBytes);
           tc::tma_load_4d(q_s, &qmap, qfull, 0, g * a.G, 0, b);
           tc::tma_load_4d(q_s + kQChunkBytes / 2, &qmap, qfull, 64, g * a.G, 0, b);
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-              ::"r"(tc::smem_u32(info_s)), "l"(a.rowinfo + (int64_t)bg * kRowChunk),
-              "r"(kRowChunk * 8), "r"(tc::smem_u32(qfull))
-              : "memory");
           cur = bg;
           ++gi;
         }
@@ -1342,12 +1326,34 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     for (int lt = 0; lt < n_my; ++lt) {
       while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
       if (bg != cur) {
-        // leaving a group: both sets release its row info
+        // leaving a group: every warp releases its row info, and the next
+        // group's info is written only once all of them have
+        bool ok = true;
         if (gi > 0) {
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(ifree);
+          ok = tc::mbar_wait(ifree, (gi - 1) & 1, kTimeoutNs);
         }
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(qfull, gi & 1, kTimeoutNs))) {
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_timeout(a, &s_abort);
+          break;
+        }
+        // row info of the new group (-lse2 and query position per row) from
+        // pass 1's partial slots; warps 2..9 write one row per lane
+        if (e < kRowChunk / 32) {
+          const int r = e * 32 + lane;
+          float nl = -INFINITY;
+          int qp = 0x7fffffff;
+          if (r < a.rows) {
+            nl = -row_lse2(a, s_pre, groups, bg, r, gridDim.x);
+            qp = a.q_pos[(int64_t)(bg / a.Hkv) * a.w + r / a.G];
+          }
+          reinterpret_cast<float*>(info_s)[r] = nl;
+          reinterpret_cast<int*>(info_s)[kRowChunk + r] = qp;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(ifull);
+        }
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(ifull, gi & 1, kTimeoutNs))) {
           record_timeout(a, &s_abort);
           break;
         }
@@ -1566,7 +1572,6 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
     }
     const int ctas = std::min(std::min(n_sm, kMaxPersistentCTAs), groups * p.n_tiles_max);
     score_rowstats_persistent_tc<<<ctas, kThreads, kSmem1, st>>>(kmap, qmap, a);
-    score_rowinfo_persistent_tc<<<dim3(1, groups), kRowChunk, 0, st>>>(a, ctas);
     score_colsum_persistent_tc<<<ctas, kThreads, kSmem2Resident, st>>>(kmap, qmap, a);
     return SE_OK;
   }
