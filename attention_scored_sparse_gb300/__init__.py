@@ -42,6 +42,9 @@ EXPORTED = [
     "se_sparse_decode_attn", "se_sparse_decode_attn_workspace_size",
     "se_sparse_decode_attn_static",
     "se_append_kv", "se_append_kv_workspace_size", "se_quest_decode_step",
+    "se_release_seqs", "se_release_seqs_workspace_size",
+    "se_chain_index_create", "se_chain_index_destroy", "se_chain_acquire", "se_chain_finish",
+    "se_chain_drop", "se_chain_count",
     "se_status_string", "se_version",
 ]
 
@@ -104,6 +107,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "se_append_kv_workspace_size": [P],
         "se_quest_decode_step": [P, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                  c_void_p, c_void_p],
+        "se_release_seqs": [P, c_void_p, c_void_p, c_size_t, c_void_p],
+        "se_release_seqs_workspace_size": [P],
+        "se_chain_index_create": [c_int32],
+        "se_chain_index_destroy": [c_void_p],
+        "se_chain_acquire": [c_void_p, c_void_p, c_int64, POINTER(c_int64), POINTER(c_int32),
+                             POINTER(c_int64), POINTER(c_int32)],
+        "se_chain_finish": [c_void_p, c_int64, c_void_p, c_int64],
+        "se_chain_drop": [c_void_p, c_int64, POINTER(c_int32)],
+        "se_chain_count": [c_void_p],
         "se_status_string": [c_int32],
         "se_version": [],
     }
@@ -114,6 +126,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             fn.restype = c_size_t
         elif name == "se_status_string":
             fn.restype = ctypes.c_char_p
+        elif name == "se_chain_index_create":
+            fn.restype = c_void_p
+        elif name == "se_chain_index_destroy":
+            fn.restype = None
         else:
             fn.restype = c_int32
     return lib
@@ -289,6 +305,65 @@ def se_quest_decode_step(kv, kmin, kmax, q, o, *, top_pages, page_idx=None, n_se
         _ptr(n_sel), _stream(stream)))
 
 
+def se_release_seqs(kv, mask, *, workspace=None, stream=None):
+    """mask: device int32 [B]; 1 = give back every page of that sequence."""
+    d = ctypes.byref(kv)
+    need = _lib.se_release_seqs_workspace_size(d)
+    ws = _ws(workspace, need, mask.device)
+    _check("se_release_seqs", _lib.se_release_seqs(d, _ptr(mask), _ptr(ws), ws.numel(),
+                                                   _stream(stream)))
+
+
+class ChainIndex:
+    """Host-side chain index (see se_chain_acquire in se.h): which cache row
+    holds which session, matched on logical token prefixes, idle chains
+    reclaimed least recently used first."""
+
+    def __init__(self, n_rows: int):
+        self._h = _lib.se_chain_index_create(n_rows)
+        if not self._h:
+            raise ValueError("could not create a chain index")
+
+    def close(self):
+        if self._h:
+            _lib.se_chain_index_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _tokens(tokens):
+        arr = (ctypes.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+        return arr, len(tokens)
+
+    def acquire(self, tokens):
+        """Returns (chain_id, row, reuse_len, reclaimed_row); SEError BUSY when
+        every row serves a request."""
+        arr, n = self._tokens(tokens)
+        cid, row, reuse, rec = c_int64(), c_int32(), c_int64(), c_int32()
+        _check("se_chain_acquire", _lib.se_chain_acquire(
+            self._h, ctypes.cast(arr, c_void_p), n, ctypes.byref(cid), ctypes.byref(row),
+            ctypes.byref(reuse), ctypes.byref(rec)))
+        return cid.value, row.value, reuse.value, rec.value
+
+    def finish(self, chain_id, tokens):
+        arr, n = self._tokens(tokens)
+        _check("se_chain_finish", _lib.se_chain_finish(self._h, chain_id,
+                                                       ctypes.cast(arr, c_void_p), n))
+
+    def drop(self, chain_id) -> int:
+        row = c_int32()
+        _check("se_chain_drop", _lib.se_chain_drop(self._h, chain_id, ctypes.byref(row)))
+        return row.value
+
+    def __len__(self):
+        return _lib.se_chain_count(self._h)
+
+
 def workspace_sizes(kv, *, w=1, n_max=1, max_keep=0, max_blocks=1, max_entries=1) -> dict:
     d = ctypes.byref(kv)
     return {
@@ -298,4 +373,5 @@ def workspace_sizes(kv, *, w=1, n_max=1, max_keep=0, max_blocks=1, max_entries=1
         "quest_page_select": _lib.se_quest_page_select_workspace_size(d, max_blocks),
         "sparse_decode_attn": _lib.se_sparse_decode_attn_workspace_size(d, max_entries),
         "append_kv": _lib.se_append_kv_workspace_size(d),
+        "release_seqs": _lib.se_release_seqs_workspace_size(d),
     }

@@ -699,6 +699,108 @@ __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
 
 __global__ void zero_int_kernel(int32_t* p) { *p = 0; }
 
+// ---------------------------------------------------------------------------
+// Release of whole sequences (reclaim of an idle chain's row)
+// ---------------------------------------------------------------------------
+
+struct ReleaseWs {
+  CompactCtrl* ctrl;   // abort, top0
+  int32_t* count;      // [B] pages each released sequence pushes
+};
+
+static ReleaseWs carve_release(const se_paged_kv* kv, void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  ReleaseWs w;
+  w.ctrl = c.take<CompactCtrl>(1);
+  w.count = c.take<int32_t>(kv->B);
+  *bytes = c.bytes();
+  return w;
+}
+
+SE_DEV bool release_pushes(const se_paged_kv& kv, int page) {
+  return page >= 0 && (kv.page_refcount == nullptr || kv.page_refcount[page] <= 1);
+}
+
+// grid: B, 1024 threads.  Counts the pages each released sequence pushes and
+// checks every page id before anything is written.  ctrl was zeroed.
+__global__ void __launch_bounds__(1024) release_count_kernel(se_paged_kv kv,
+                                                             const int32_t* __restrict__ mask,
+                                                             ReleaseWs w) {
+  __shared__ int s_cnt;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  if (b == 0 && threadIdx.x == 0) w.ctrl->top0 = *kv.free_top;
+  int cnt = 0;
+  if (mask[b] != 0) {
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    for (int blk = threadIdx.x; blk < kv.max_pages_per_seq; blk += blockDim.x) {
+      const int page = bt[blk];
+      if (page >= kv.num_pages) {
+        set_status(kv.status, SE_ERR_BOUNDS);
+        atomicExch(&w.ctrl->abort, 1);
+      } else if (release_pushes(kv, page)) {
+        cnt++;
+      }
+    }
+  }
+  if (cnt) atomicAdd(&s_cnt, cnt);
+  __syncthreads();
+  if (threadIdx.x == 0) w.count[b] = s_cnt;
+}
+
+// grid: B, 1024 threads.  Pushes (ascending sequence, then block), drops the
+// references of shared pages, clears block table, slot map and lengths.
+__global__ void __launch_bounds__(1024) release_apply_kernel(se_paged_kv kv,
+                                                             const int32_t* __restrict__ mask,
+                                                             ReleaseWs w) {
+  __shared__ int tmp[33];
+  __shared__ int s_off, s_total;
+  if (w.ctrl->abort) return;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  if (tid == 0) {
+    int off = 0, total = 0;
+    for (int bb = 0; bb < kv.B; ++bb) {
+      off += bb < b ? w.count[bb] : 0;
+      total += w.count[bb];
+    }
+    s_off = off;
+    s_total = total;
+  }
+  __syncthreads();
+  const int top0 = w.ctrl->top0;
+  if (b == 0 && tid == 0) {
+    if (top0 + s_total > kv.num_pages) set_status(kv.status, SE_ERR_BOUNDS);
+    else *kv.free_top = top0 + s_total;
+  }
+  if (mask[b] == 0 || top0 + s_total > kv.num_pages) return;
+  int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  int running = 0;
+  for (int c0 = 0; c0 < kv.max_pages_per_seq; c0 += blockDim.x) {
+    const int blk = c0 + tid;
+    const int page = blk < kv.max_pages_per_seq ? bt[blk] : -1;
+    const bool push = release_pushes(kv, page);
+    int total;
+    const int pos = block_exclusive_scan(push ? 1 : 0, tmp, &total);
+    if (push) {
+      kv.free_list[top0 + s_off + running + pos] = page;
+      if (kv.page_refcount) kv.page_refcount[page] = 0;
+    } else if (page >= 0) {
+      atomicSub(&kv.page_refcount[page], 1);   // shared: this sequence's reference only
+    }
+    if (blk < kv.max_pages_per_seq) bt[blk] = -1;
+    running += total;
+  }
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * kv.page_size;
+  int32_t* sm = kv.slot_map + (int64_t)b * kv.Hkv * smax;
+  for (int64_t x = tid; x < kv.Hkv * smax; x += blockDim.x) sm[x] = -1;
+  if (tid == 0) {
+    kv.ctx_len[b] = 0;
+    kv.logical_len[b] = 0;
+  }
+}
+
+
 }  // namespace se
 
 using namespace se;
@@ -835,4 +937,26 @@ extern "C" se_status se_prune_span(const se_paged_kv* kv, const int32_t* L, cons
   prune_plan_kernel<<<kv->B, 1024, 0, st>>>(*kv, L, R, mask, mask_stride, n_busy, w);
   return launch_compact(kv, w.keep, smax, w.n_keep, w.first, smax, aux, aux_stride, w.compact_ws,
                         w.compact_bytes, w.abort, st);
+}
+
+extern "C" size_t se_release_seqs_workspace_size(const se_paged_kv* kv) {
+  if (kv == nullptr) return 0;
+  size_t b = 0;
+  carve_release(kv, nullptr, &b);
+  return b;
+}
+
+extern "C" se_status se_release_seqs(const se_paged_kv* kv, const int32_t* mask, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (mask == nullptr || workspace == nullptr) return SE_ERR_INVALID_ARG;
+  size_t need = 0;
+  ReleaseWs w = carve_release(kv, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.ctrl, 0, sizeof(CompactCtrl), st) != cudaSuccess) return SE_ERR_CUDA;
+  release_count_kernel<<<kv->B, 1024, 0, st>>>(*kv, mask, w);
+  release_apply_kernel<<<kv->B, 1024, 0, st>>>(*kv, mask, w);
+  return se_last_launch_status();
 }

@@ -79,11 +79,18 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
   const int nb = cdiv(kv.ctx_len[b], P);
   const int half = threadIdx.x >> 4, t = threadIdx.x & 15;
   const int blk = blockIdx.x * 16 + half;
-  float qv[G][8];
+  // max(q kmax, q kmin) = max(q, 0) kmax + min(q, 0) kmin: two FMAs per term
+  float qp[G][8], qn[G][8];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const uint4 u = ldg_nc_v4(q + ((int64_t)b * kv.Hq + g * G + j) * kv.D + t * 8);
-    unpack8_bf16(u, qv[j]);
+    float qv[8];
+    unpack8_bf16(u, qv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      qp[j][i] = fmaxf(qv[i], 0.f);
+      qn[j][i] = fminf(qv[i], 0.f);
+    }
   }
   float acc = 0.f;
   const bool active = blk < nb - 1 && blk < u_stride;
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
     for (int j = 0; j < G; ++j) {
       float part = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) part += fmaxf(qv[j][i] * mx[i], qv[j][i] * mn[i]);
+      for (int i = 0; i < 8; ++i) part = fmaf(qn[j][i], mn[i], fmaf(qp[j][i], mx[i], part));
       acc += part;
     }
   }

@@ -168,11 +168,18 @@ quest_fused_kernel(QfArgs a) {
   for (int i = tid; i < n_loc; i += kQfThreads) sm.phys[i] = bt[c0 + i];
   for (int i = tid; i < kQfCap; i += kQfThreads) sm.key[i] = 0u;
   __syncthreads();
-  float qv[G][V];
+  // max(q kmax, q kmin) = max(q, 0) kmax + min(q, 0) kmin: two FMAs per term
+  float qp[G][V], qn[G][V];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const uint4 u = ldg_nc_v4(a.q + ((int64_t)b * kv.Hq + g * G + j) * D + t * V);
-    unpack8_bf16(u, qv[j]);
+    float qv[V];
+    unpack8_bf16(u, qv);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      qp[j][i] = fmaxf(qv[i], 0.f);
+      qn[j][i] = fminf(qv[i], 0.f);
+    }
   }
   bool bad_page = false;
   // rounds of kInFlight pages per half-warp; the next round's rows load while
@@ -216,7 +223,7 @@ quest_fused_kernel(QfArgs a) {
         for (int j = 0; j < G; ++j) {
           float part = 0.f;
 #pragma unroll
-          for (int i = 0; i < V; ++i) part += fmaxf(qv[j][i] * mx[i], qv[j][i] * mn[i]);
+          for (int i = 0; i < V; ++i) part = fmaf(qn[j][i], mn[i], fmaf(qp[j][i], mx[i], part));
           acc += part;
         }
       }

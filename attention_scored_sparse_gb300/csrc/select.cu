@@ -507,18 +507,27 @@ __global__ void __launch_bounds__(256) kara_chunk_kernel(SelectArgs a, int n_can
 // --------------------------------------------------------------------------
 // H2O evict-one: one warp per (b, h).
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) evict_one_kernel(SelectArgs a, const int32_t* ctx_len,
+// (v, pos) ranks below (bv, bpos): lower running score, ties to the higher
+// position (the mirror of the selection tie rule).
+SE_DEV bool evict_before(float v, int pos, float bv, int bpos, int bslot) {
+  return bslot < 0 || v < bv || (v == bv && pos > bpos);
+}
+
+// grid: B * Hkv, 128 threads (one CTA per (sequence, head)).  Each thread
+// scans every 128th slot with four loads in flight, then warp shuffles and
+// shared memory pick the minimum.
+__global__ void __launch_bounds__(128) evict_one_kernel(SelectArgs a, const int32_t* ctx_len,
                                                         const int32_t* logical_len,
                                                         const int32_t* slot_map, int64_t smax,
                                                         int budget, int recent) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int inst = blockIdx.x * 8 + warp;
-  if (inst >= a.B * a.Hkv) return;
+  __shared__ float s_v[4];
+  __shared__ int s_p[4], s_s[4];
+  const int inst = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = inst / a.Hkv, h = inst % a.Hkv;
   const int ctx = ctx_len[b];
   int32_t* out = a.keep + (int64_t)b * a.Hkv + h;
   if (ctx <= budget) {
-    if (lane == 0) *out = -1;
+    if (tid == 0) *out = -1;
     return;
   }
   const int recent_from = logical_len[b] - recent;
@@ -526,21 +535,39 @@ __global__ void __launch_bounds__(256) evict_one_kernel(SelectArgs a, const int3
   const int32_t* sm = slot_map + ((int64_t)b * a.Hkv + h) * smax;
   float best = INFINITY;
   int bpos = -1, bslot = -1;
-  for (int s = lane; s < ctx; s += 32) {
-    const int pos = sm[s];
-    if (pos < recent_from) {
-      const float v = acc[s];
-      if (bslot < 0 || v < best || (v == best && pos > bpos)) { best = v; bpos = pos; bslot = s; }
+  for (int s0 = tid; s0 < ctx; s0 += 4 * 128) {
+    int pos[4];
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sl = s0 + u * 128;
+      pos[u] = sl < ctx ? sm[sl] : INT_MAX;
+      v[u] = sl < ctx ? acc[sl] : 0.f;
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (pos[u] < recent_from && evict_before(v[u], pos[u], best, bpos, bslot)) {
+        best = v[u];
+        bpos = pos[u];
+        bslot = s0 + u * 128;
+      }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v = __shfl_xor_sync(0xffffffffu, best, o);
     const int p = __shfl_xor_sync(0xffffffffu, bpos, o);
-    const int s = __shfl_xor_sync(0xffffffffu, bslot, o);
-    if (s >= 0 && (bslot < 0 || v < best || (v == best && p > bpos))) { best = v; bpos = p; bslot = s; }
+    const int sl = __shfl_xor_sync(0xffffffffu, bslot, o);
+    if (sl >= 0 && evict_before(v, p, best, bpos, bslot)) { best = v; bpos = p; bslot = sl; }
   }
-  if (lane == 0) *out = bslot;
+  if (lane == 0) { s_v[warp] = best; s_p[warp] = bpos; s_s[warp] = bslot; }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < 4; ++w)
+      if (s_s[w] >= 0 && evict_before(s_v[w], s_p[w], best, bpos, bslot)) {
+        best = s_v[w]; bpos = s_p[w]; bslot = s_s[w];
+      }
+    *out = bslot;
+  }
 }
 
 template <int ITEMS>
@@ -646,8 +673,7 @@ extern "C" se_status se_topk_select(const se_paged_kv* kv, const float* scores,
   }
   if (p.mode == SE_SELECT_EVICT_ONE) {
     if (p.budget < 0 || p.recent < 0) return SE_ERR_INVALID_ARG;
-    const int blocks = cdiv(kv->B * kv->Hkv, 8);
-    evict_one_kernel<<<blocks, 256, 0, st>>>(a, kv->ctx_len, kv->logical_len, kv->slot_map,
+    evict_one_kernel<<<kv->B * kv->Hkv, 128, 0, st>>>(a, kv->ctx_len, kv->logical_len, kv->slot_map,
                                              (int64_t)kv->max_pages_per_seq * kv->page_size,
                                              p.budget, p.recent);
     return se_last_launch_status();

@@ -361,6 +361,49 @@ se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_n
                        void* workspace, size_t workspace_bytes, void* stream);
 size_t se_append_kv_workspace_size(const se_paged_kv* kv);
 
+/*
+ * se_release_seqs -- CacheManager "free" of whole sequences (SparseEngine
+ * "How it differs": an idle chain's row is reclaimed when capacity is
+ * needed).  Every sequence b with mask[b] != 0 (device int32 [B]) gives back
+ * all its pages: pushed onto the free list in ascending (sequence, block)
+ * order, except pages whose reference count is above one, which only lose
+ * this sequence's reference.  Counts are judged as they were before the
+ * call: release sequences that share pages in separate calls.  Block table
+ * and slot map rows become -1, ctx_len and logical_len 0.
+ * Device error (nothing written): SE_ERR_BOUNDS for a page id >= num_pages.
+ */
+se_status se_release_seqs(const se_paged_kv* kv, const int32_t* mask, void* workspace,
+                          size_t workspace_bytes, void* stream);
+size_t se_release_seqs_workspace_size(const se_paged_kv* kv);
+
+/*
+ * Chain index -- SparseEngine "How it differs" (Chain Cache): ties each
+ * session (chain_id) to the sequence row of the paged cache holding its
+ * retained KV and to its logical token prefix.  Host memory and host work
+ * only; every call on one index is serialised internally.
+ *   se_chain_acquire  for a request's tokens (host int32 [n_tokens]): resumes
+ *       the idle chain whose prefix is the longest prefix of the tokens (ties:
+ *       most recently used) -- *reuse_len = that prefix's length, prefill only
+ *       tokens[reuse_len:] -- or starts a chain on the lowest free row, or on
+ *       the row of the least recently used idle chain, which is dropped
+ *       (*reclaimed_row = that row, else -1: release its pages with
+ *       se_release_seqs first).  SE_ERR_BUSY when every row serves a request.
+ *   se_chain_finish   the request on chain_id ended; its logical prefix is now
+ *       tokens (prompt and generated tokens); the chain becomes idle.
+ *   se_chain_drop     forgets an idle chain; *row = its row (now free).
+ * Invalid handles, ids or busy chains: SE_ERR_INVALID_ARG.
+ */
+typedef struct se_chain_index se_chain_index;
+se_chain_index* se_chain_index_create(int32_t n_rows);
+void se_chain_index_destroy(se_chain_index* idx);
+se_status se_chain_acquire(se_chain_index* idx, const int32_t* tokens, int64_t n_tokens,
+                           int64_t* chain_id, int32_t* row, int64_t* reuse_len,
+                           int32_t* reclaimed_row);
+se_status se_chain_finish(se_chain_index* idx, int64_t chain_id, const int32_t* tokens,
+                          int64_t n_tokens);
+se_status se_chain_drop(se_chain_index* idx, int64_t chain_id, int32_t* row);
+int32_t se_chain_count(se_chain_index* idx);
+
 /* Human-readable name of a status code (static string). */
 const char* se_status_string(int32_t status);
 

@@ -349,6 +349,40 @@ def append_tokens(c: Cache, k_bits: np.ndarray, v_bits: np.ndarray,
     return SE_OK
 
 
+def release(c: Cache, mask: Sequence[int]) -> int:
+    """CacheManager "free" of whole sequences (SparseEngine "How it differs":
+    idle chains are reclaimed when capacity is needed).
+
+    Every sequence b with mask[b] != 0 gives back all its pages: in
+    ascending (sequence, block) order each page is pushed onto the free list,
+    except a page whose reference count is above one, which only loses this
+    sequence's reference (reading xvii).  Reading (xxiv): counts are judged
+    as they were before the call, so a page shared by two sequences released
+    in the same call loses both references and is pushed by neither; callers
+    release such sequences in separate calls.  The block table and slot map
+    of a released sequence become -1 and both lengths 0.
+    """
+    before = c.page_refcount.copy()
+    for b in range(c.B):
+        if not mask[b]:
+            continue
+        for blk in range(c.block_table.shape[1]):
+            page = int(c.block_table[b, blk])
+            if page < 0:
+                continue
+            if before[page] > 1:
+                c.page_refcount[page] -= 1
+            else:
+                c.page_refcount[page] = 0
+                c.free_list[c.free_top] = page
+                c.free_top += 1
+            c.block_table[b, blk] = -1
+        c.slot_map[b] = -1
+        c.ctx_len[b] = 0
+        c.logical_len[b] = 0
+    return SE_OK
+
+
 # ---------------------------------------------------------------------------
 # Prefix-span pruning (SparseEngine "How it differs")
 # ---------------------------------------------------------------------------

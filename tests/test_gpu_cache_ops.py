@@ -210,6 +210,26 @@ def test_append_chunk_beyond_capacity_changes_nothing(cuda_lib):
     assert torch.equal(pc.free_top, before.free_top)
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_release_matches_oracle(cuda_lib, seed):
+    """Whole sequences give their pages back (a reclaimed chain's row): free
+    list order, shared pages, cleared rows, bit for bit."""
+    se = cuda_lib
+    shape, pc = _cache(torch.bfloat16, 128, B=6, Hkv=2, ctx=70 + seed, max_ctx=96, tag=f"rel{seed}")
+    rng = np.random.default_rng(seed)
+    mask = rng.integers(0, 2, size=6).astype(np.int32)
+    mask[seed % 6] = 1
+    shared = int(pc.block_table[seed % 6, 1].item())
+    pc.page_refcount[shared] = 2
+    c = ocache.from_tensors(pc)
+    assert ocache.release(c, mask) == ocache.SE_OK
+    se.se_release_seqs(se.kv_desc(pc, shape.Hq), torch.tensor(mask, device="cuda"))
+    torch.cuda.synchronize()
+    assert H.status(pc) == 0
+    H.assert_cache_equal(pc, c)
+    np.testing.assert_array_equal(pc.page_refcount.cpu().numpy(), c.page_refcount)
+
+
 def test_append_out_of_pages(cuda_lib):
     se = cuda_lib
     shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=32, max_ctx=48, tag="apo")

@@ -152,3 +152,12 @@ def test_quest_decode_step_host_checks():
     df, _ = kv(dtype=se.SE_F32)
     assert L.se_quest_decode_step(df, FAKE, FAKE, FAKE, 8, FAKE, None, None, None) == \
         se.SE_ERR_UNSUPPORTED
+
+
+def test_release_seqs_host_checks():
+    d, _ = kv()
+    assert L.se_release_seqs(d, None, FAKE, 1 << 20, None) == se.SE_ERR_INVALID_ARG
+    assert L.se_release_seqs(d, FAKE, None, 1 << 20, None) == se.SE_ERR_INVALID_ARG
+    need = L.se_release_seqs_workspace_size(d)
+    assert need > 0
+    assert L.se_release_seqs(d, FAKE, FAKE, need - 1, None) == se.SE_ERR_INVALID_ARG

@@ -461,6 +461,41 @@ def test_append_tokens_errors_change_nothing():
     assert c.free_top == before.free_top
 
 
+def test_release_hand_worked_order_and_shared_page():
+    """Sequences 0 and 2 of three (page 4) are released: pages go back in
+    (sequence, block) order; a page held twice only loses a reference."""
+    shape = tiny_shape(B=3, ctx=9, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=16, max_ctx=12))
+    before = c.copy()
+    shared = int(c.block_table[2, 1])
+    c.page_refcount[shared] = 2                      # also held by someone else
+    top = c.free_top
+    assert cache.release(c, [1, 0, 1]) == cache.SE_OK
+    expect = [int(p) for p in before.block_table[0, :3]] + \
+        [int(before.block_table[2, 0]), int(before.block_table[2, 2])]
+    assert list(c.free_list[top:c.free_top]) == expect
+    assert c.page_refcount[shared] == 1 and shared not in c.free_list[:c.free_top]
+    for b in (0, 2):
+        assert (c.block_table[b] == -1).all() and (c.slot_map[b] == -1).all()
+        assert c.ctx_len[b] == 0 and c.logical_len[b] == 0
+    for f in ("block_table", "slot_map"):
+        assert (getattr(c, f)[1] == getattr(before, f)[1]).all()
+    assert c.ctx_len[1] == 9
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_release_conserves_pages(seed):
+    rng = np.random.default_rng(seed)
+    shape = tiny_shape(B=5, ctx=13, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=40, max_ctx=20))
+    before = c.copy()
+    mask = rng.integers(0, 2, size=5)
+    assert cache.release(c, mask) == cache.SE_OK
+    _check_accounting(before, c)
+    released = sum(int((before.block_table[b] >= 0).sum()) for b in range(5) if mask[b])
+    assert c.free_top == before.free_top + released
+
+
 # ---------------------------------------------------------------------------
 # O6 Quest
 # ---------------------------------------------------------------------------
