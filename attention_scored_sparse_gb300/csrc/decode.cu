@@ -346,6 +346,8 @@ SE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
       : "memory");
 }
 
+constexpr int kMaxChunk = 1024;   // view entries per CTA at most (see pick_chunk)
+
 template <typename T, int D, int G>
 struct StagedGeom {
   static constexpr int V = D / 16;                 // dims per lane
@@ -357,34 +359,32 @@ struct StagedGeom {
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
 };
 
-// Issues the copies of one stage (view entries [s0, s0 + SE)) of (b, g);
-// called by all 32 lanes of one warp.  Lane i resolves entry i of each group
-// of 32 (slot, page); a maximal run of entries that are consecutive rows of
-// one page becomes one K and one V copy, issued by the lane that starts it.
-// valid[u] records whether entry u has a row (read by the consumers after the
-// stage's barrier completes).  Lane 0 arrives on the barrier last.
+// Issues the copies of one stage (chunk entries [s0, s0 + SE)) of (b, g);
+// called by all 32 lanes of one warp.  rows[x] is the pool row (page * P +
+// row in page) of chunk entry x, -1 for none, resolved once per CTA.  A
+// maximal run of entries that are consecutive rows of one page becomes one K
+// and one V copy, issued by the lane that starts it.  valid[u] records
+// whether entry u has a row (read by the consumers after the stage's barrier
+// completes).  Lane 0 arrives on the barrier last.
 template <typename T, int D, int G>
-SE_DEV void issue_stage(const DecodeArgs& a, int b, int g, int ctx, int s0, int e_end,
+SE_DEV void issue_stage(const DecodeArgs& a, int g, int s0, int n_chunk, const int32_t* rows,
                         uint8_t* dst, uint64_t* bar, int8_t* valid, int lane) {
   using Gm = StagedGeom<T, D, G>;
   const se_paged_kv& kv = a.kv;
   const int P = kv.page_size;
-  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   const char* kp = static_cast<const char*>(kv.k_pool);
   const char* vp = static_cast<const char*>(kv.v_pool);
   uint32_t n_valid = 0;
 #pragma unroll
   for (int u0 = 0; u0 < Gm::SE; u0 += 32) {
     const int u = u0 + lane;
-    const int e = s0 + u;
-    int slot = (u < Gm::SE && e < e_end) ? view_slot(a, b, g, e, ctx) : -1;
-    int page = slot >= 0 ? bt[slot / P] : -1;
-    if (page < 0 || page >= kv.num_pages) slot = -1;
-    const bool ok = slot >= 0;
+    const int x = s0 + u;
+    const int prow = (u < Gm::SE && x < n_chunk) ? rows[x] : -1;
+    const bool ok = prow >= 0;
     if (u < Gm::SE) valid[u] = ok ? 1 : 0;
     // a run continues when this entry is the next row of the previous one's page
-    const int prev = __shfl_up_sync(0xffffffffu, slot, 1);
-    const bool cont = ok && lane > 0 && prev >= 0 && prev + 1 == slot && slot % P != 0;
+    const int prev = __shfl_up_sync(0xffffffffu, prow, 1);
+    const bool cont = ok && lane > 0 && prev >= 0 && prev + 1 == prow && prow % P != 0;
     const uint32_t okm = __ballot_sync(0xffffffffu, ok);
     const uint32_t starts = __ballot_sync(0xffffffffu, ok && !cont);
     n_valid += __popc(okm);
@@ -393,7 +393,7 @@ SE_DEV void issue_stage(const DecodeArgs& a, int b, int g, int ctx, int s0, int 
       const uint32_t stop = (starts | ~okm) & above;
       const int end = stop ? __ffs(stop) - 1 : 32;
       const int len = end - lane;
-      const int64_t off = (((int64_t)page * kv.Hkv + g) * P + slot % P) * Gm::RB;
+      const int64_t off = (((int64_t)(prow / P) * kv.Hkv + g) * P + prow % P) * Gm::RB;
       bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
       bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
     }
@@ -416,6 +416,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[4], empty[4];
   __shared__ int8_t s_valid[4][SE];
+  __shared__ int32_t s_rows[kMaxChunk];   // pool row of each chunk entry, -1 for none
   __shared__ float s_p[8][16];
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ int s_abort;
@@ -441,11 +442,23 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     }
     tc::fence_barrier_init();
   }
+  // resolve every entry of the chunk to its pool row once (view -> slot ->
+  // block table), so the stage producer only reads shared memory
+  const int n_chunk = max(e_end - e_begin, 0);
+  {
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    const int P = kv.page_size;
+    for (int x = threadIdx.x; x < n_chunk; x += blockDim.x) {
+      const int slot = view_slot(a, b, g, e_begin + x, ctx);
+      const int page = slot >= 0 ? bt[slot / P] : -1;
+      s_rows[x] = (page >= 0 && page < kv.num_pages) ? page * P + slot % P : -1;
+    }
+  }
   __syncthreads();
   const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
   if (producer)
     for (int i = 0; i < min(S - 1, n_it); ++i)
-      issue_stage<T, D, G>(a, b, g, ctx, e_begin + i * SE, e_end, stages + i * Gm::STAGE_BYTES,
+      issue_stage<T, D, G>(a, g, i * SE, n_chunk, s_rows, stages + i * Gm::STAGE_BYTES,
                            &full[i], s_valid[i], lane);
 
   const float qscale = kLog2e * rsqrtf((float)D);
@@ -475,8 +488,8 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
       const int ps = issued % S;
       const bool free_ok = issued < S || tc::mbar_wait(&empty[ps], ((issued / S) - 1) & 1, kLimit);
       if (__all_sync(full_mask, free_ok)) {
-        issue_stage<T, D, G>(a, b, g, ctx, e_begin + issued * SE, e_end,
-                             stages + ps * Gm::STAGE_BYTES, &full[ps], s_valid[ps], lane);
+        issue_stage<T, D, G>(a, g, issued * SE, n_chunk, s_rows, stages + ps * Gm::STAGE_BYTES,
+                             &full[ps], s_valid[ps], lane);
         ++issued;
       } else if (lane == 0) {
         set_status(kv.status, SE_ERR_TIMEOUT);

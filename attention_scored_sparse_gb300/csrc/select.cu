@@ -179,7 +179,8 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ float s_sc[];
   __shared__ int tmp[33];
-  __shared__ int hist[2048];
+  __shared__ int hist[2][2048];   // double-buffered: peers read round r while round r+1 fills the other
+  __shared__ int tot[2048];       // this round's histogram summed over the cluster
   __shared__ int s_cnt[4];        // forced-in-range, equal-to-T, selected, selected-before-force
   __shared__ int s_digit, s_rem;
   const int rank = (int)cluster.block_rank();
@@ -245,24 +246,26 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
       const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
       const int nbins = round == 2 ? 1024 : 2048;
       const uint32_t dmask = (uint32_t)nbins - 1u;
-      for (int i = tid; i < nbins; i += 1024) hist[i] = 0;
+      // buffer round & 1 was last read by peers two rounds ago; every peer
+      // has passed the previous round's cluster barrier since, after its reads
+      int* hb = hist[round & 1];
+      for (int i = tid; i < nbins; i += 1024) hb[i] = 0;
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i)
-        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hb[(key[i] >> shift) & dmask], 1);
       cluster.sync();                    // every CTA's histogram is complete
-      int tot_local[2] = {0, 0};
-      // each thread sums up to two bins over the cluster into registers
+      // each thread sums up to two bins over the cluster
       for (int j = 0; j < 2; ++j) {
         const int bin = tid + j * 1024;
-        if (bin < nbins)
-          for (int r = 0; r < kClusterCTAs; ++r) tot_local[j] += *cluster.map_shared_rank(&hist[bin], r);
+        if (bin < nbins) {
+          int sum = 0;
+          for (int r = 0; r < kClusterCTAs; ++r) sum += *cluster.map_shared_rank(&hb[bin], r);
+          tot[bin] = sum;
+        }
       }
-      cluster.sync();                    // peers have read my histogram
-      for (int j = 0; j < 2; ++j)
-        if (tid + j * 1024 < nbins) hist[tid + j * 1024] = tot_local[j];
       __syncthreads();
-      radix_find_digit(hist, nbins, remaining, tmp, &s_digit, &s_rem);
+      radix_find_digit(tot, nbins, remaining, tmp, &s_digit, &s_rem);
       prefix |= (uint32_t)s_digit << shift;
       remaining = s_rem;
       pmask |= dmask << shift;
