@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
         set_status(kv.status, SE_ERR_BOUNDS);
         atomicExch(&s_bad, 1);
       }
-      const int pb = fs / P;
+      // an empty rewrite (first_slot = ctx, nothing kept) leaves the sequence as it is
+      const int pb = (fs == ctx && nk == 0) ? cdiv(ctx, P) : fs / P;
       const int nctx = fs + nk;
       nn = ok ? max(cdiv(nctx, P) - pb, 0) : 0;
       w.pb[b] = pb;

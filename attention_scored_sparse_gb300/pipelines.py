@@ -233,6 +233,77 @@ class H2OChunkedPrefill(_Base):
         return resident
 
 
+class KaraSchedule(_Base):
+    """Kara periodic compression inside a decode loop, staggered over the batch.
+
+    Each step appends every sequence's token, attends over all resident
+    entries, and compresses the trailing window of the sequences whose window
+    just filled (bidirectional scores of the window's queries, Token2Chunk,
+    compaction from the window start); the other sequences get empty ranges
+    and are left untouched by every call.  The window's queries live in a
+    ring indexed by logical position modulo the window.  Lengths are tracked
+    on the host (they follow from the schedule), so no step reads the device."""
+
+    def __init__(self, cache, Hq, *, ctx, fills, window, protected, candidates, budget,
+                 chunk_coef, max_ctx):
+        super().__init__(cache, Hq)
+        B, dev = self.B, self.device
+        self.window, self.protected = window, protected
+        self.candidates, self.budget, self.coef = candidates, budget, chunk_coef
+        self.ctx = [ctx] * B                         # resident entries
+        self.logical = [ctx] * B                     # logical length
+        self.win_start = [ctx - f for f in fills]    # first slot of the window
+        self.scores = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
+        self.keep = torch.empty((B, self.Hkv, budget + protected), dtype=torch.int32, device=dev)
+        self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+        self.ranges = torch.empty((4, B), dtype=torch.int32, device=dev)
+        self.q_pos = torch.empty((B, window), dtype=torch.int32, device=dev)
+        self.max_ctx = max_ctx
+        sz = workspace_sizes(self.kv, w=window, n_max=window, max_keep=budget + protected,
+                             max_entries=max_ctx)
+        self.ws_score = self._ws(sz["score_window"])
+        self.ws_compact = self._ws(sz["compact_evict"])
+        self.ws_decode = self._ws(sz["sparse_decode_attn"])
+        self.ws_append = self._ws(sz["append_kv"])
+        self.compressions = 0
+
+    def step(self, q, k_new, v_new, o, q_ring, stream=None):
+        B, W = self.B, self.window
+        ring_slot = torch.tensor([lg % W for lg in self.logical], device=self.device)
+        q_ring[torch.arange(B, device=self.device), ring_slot] = q
+        se_append_kv(self.kv, k_new, v_new, workspace=self.ws_append, stream=stream)
+        for b in range(B):
+            self.ctx[b] += 1
+            self.logical[b] += 1
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.max_ctx,
+                              workspace=self.ws_decode, stream=stream)
+        due = [b for b in range(B) if self.ctx[b] - self.win_start[b] >= W]
+        if not due:
+            return due
+        win_lo = [self.ctx[b] - W if b in due else self.ctx[b] for b in range(B)]
+        prot_lo = [self.ctx[b] - self.protected if b in due else self.ctx[b] for b in range(B)]
+        rng = torch.tensor([win_lo, self.ctx, prot_lo, win_lo], dtype=torch.int32)
+        self.ranges.copy_(rng)
+        pos = torch.tensor([[self.logical[b] - W + i for i in range(W)] for b in range(B)],
+                           dtype=torch.int32)
+        self.q_pos.copy_(pos)
+        lo, hi, plo = self.ranges[0], self.ranges[1], self.ranges[2]
+        se_score_window(self.kv, q_ring, self.q_pos, lo, hi, lo, plo, causal=False,
+                        accumulate=False, n_max=W, scores=self.scores, workspace=self.ws_score,
+                        stream=stream)
+        se_topk_select(self.kv, self.scores, mode=SE_SELECT_KARA_CHUNK, cand_lo=lo, cand_hi=plo,
+                       force_lo=plo, force_hi=hi, keep_idx=self.keep, n_keep=self.n_keep,
+                       k=self.candidates, chunk_budget=self.budget, chunk_coef=self.coef,
+                       n_max=W - self.protected, stream=stream)
+        se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
+                         first_slot=self.ranges[3], max_keep=self.budget + self.protected,
+                         workspace=self.ws_compact, stream=stream)
+        for b in due:
+            self.ctx[b] = win_lo[b] + self.budget + self.protected
+        self.compressions += len(due)
+        return due
+
+
 class Kara(_Base):
     """Kara periodic compression of the trailing window (bidirectional scores
     of the compressible keys, Token2Chunk, compaction from the window start),

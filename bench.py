@@ -15,7 +15,8 @@ the restore sits outside the device-timed region (it does not touch K/V: the
 compaction writes only fresh pages).
 
 Other workloads (--workload): snapkv_tiny, quest_decode, h2o_decode,
-kara_prune -- each prints its own line with its own dominant kernel.
+kara_prune, kara_schedule -- each prints its own line with its own dominant
+kernel.
 
 --impl reference times the CPU oracle (the slow, plain fp64 reference) on a
 bounded sample of the same workload on the host cores.
@@ -195,6 +196,22 @@ def oracle_prepare(workload: str, groups: int):
             ocache.compact(c, r["keep"], r["first_slot"])
             ocache.prune(c, [shape.prune_L], [shape.prune_R], mask)
             return shape.ctx, time.perf_counter() - t0, desc
+        return run
+    if workload == "kara_schedule":
+        shape = W.kara_schedule(B=2)
+        inp = W.kara_schedule_inputs(shape, "cpu", steps=4)
+        c0 = ocache.from_tensors(inp["cache"])
+        # sequence 1 fills its window at the first step: one compression per call
+        win0 = [shape.ctx - shape.fill(0), shape.ctx - (shape.window - 1)]
+        desc = ("2 sequences (2304 resident tokens) for one decode step in which one of "
+                "them compresses its window")
+
+        def run():
+            c, ring, win = c0.copy(), inp["q_ring"].clone(), list(win0)
+            t0 = time.perf_counter()
+            opipe.kara_schedule_step(c, inp["q_steps"][0], inp["k_steps"][0],
+                                     inp["v_steps"][0], ring, win, shape)
+            return 2.0, time.perf_counter() - t0, desc
         return run
     raise ValueError(workload)
 
@@ -615,8 +632,60 @@ def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
     return units_per_rank * world / (ms * 1e-3)
 
 
+def run_kara_schedule(args, torch, rank, world):
+    import se_workloads as W
+    from attention_scored_sparse_gb300 import pipelines as P
+    n_steps = args.warmup + args.steps
+    shape = W.kara_schedule(steps=n_steps)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.kara_schedule_inputs(shape, dev)
+    fills = [shape.fill(b) for b in range(shape.B)]
+    pipe = P.KaraSchedule(inp["cache"], shape.Hq, ctx=shape.ctx, fills=fills,
+                          window=shape.window, protected=shape.protected,
+                          candidates=shape.candidates, budget=shape.budget,
+                          chunk_coef=shape.chunk_coef, max_ctx=shape.ctx + n_steps)
+    o = torch.empty_like(inp["q_steps"][0])
+    ring = inp["q_ring"]
+    ev = Events(torch, ["s0", "s1"])
+    it = [0]
+    resident = []                        # entries attended per step (for the GB/s)
+
+    def step(timed):
+        t = it[0]
+        it[0] += 1
+        resident.append(sum(pipe.ctx) + shape.B)
+        if timed: ev.mark("s0")
+        pipe.step(inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], o, ring)
+        if timed: ev.mark("s1")
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    c0 = pipe.compressions
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    if int(inp["cache"].status.item()) != 0:
+        raise RuntimeError(f"device status {int(inp['cache'].status.item())}")
+    ms = statistics.mean(ev.durations("s0", "s1"))
+    entry = 2 * shape.D * 2 * shape.Hkv
+    kv_bytes = statistics.mean(resident[args.warmup:]) * entry
+    detail = {"compressions_per_step": (pipe.compressions - c0) / args.steps,
+              "decode_gbs": kv_bytes / (ms * 1e-3) / 1e9}
+    roof = dict(bound="hbm", achieved=detail["decode_gbs"], unit="GB/s",
+                kernel="kara schedule step (append + decode + staggered compression)",
+                per_launch=f"{kv_bytes:.4g} B (resident K/V attended per step)")
+    return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
+                launches=2 + 1 + (3 + 1 + 3) * detail["compressions_per_step"],
+                metric="decode tokens/s", e2e=None,
+                cfg={"workload": "kara_schedule: B=128 decoding over 2304 resident tokens, "
+                                 "Kara window 256 (32 protected, 32 candidates, chunk budget 64) "
+                                 "compressed when full, staggered over the 160-step period; "
+                                 "32/8 heads, d=128, bf16",
+                     "l2": "inputs larger than L2 (1.2 GB attended per step)"},
+                dtype="bf16")
+
+
 RUNNERS = {"snapkv_llama8b": run_snapkv, "snapkv_tiny": run_snapkv, "quest_decode": run_quest,
-           "h2o_decode": run_h2o, "kara_prune": run_kara}
+           "h2o_decode": run_h2o, "kara_prune": run_kara, "kara_schedule": run_kara_schedule}
 
 
 def main():
@@ -641,7 +710,8 @@ def main():
         times = [r[1] for r in runs]
         desc = runs[0][2]
         value = sum(per) / sum(times)
-        unit = "KV tokens/s" if args.workload.startswith(("snapkv", "kara")) else "decode tokens/s"
+        unit = ("KV tokens/s" if args.workload.startswith("snapkv") or args.workload == "kara_prune"
+                else "decode tokens/s")
         line = {"impl": "reference", "metric": METRIC if unit == "KV tokens/s" else "decode tokens/s",
                 "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
@@ -680,7 +750,7 @@ def main():
                      "unit": r["roof"]["unit"], "frac": r["roof"]["achieved"] / peak,
                      "traffic": None, "kernel": r["roof"]["kernel"],
                      "per_launch": r["roof"]["per_launch"], "peak_source": src},
-        "clocks": r["clocks"], "gpu_launches": r["launches"] * args.steps, "detail": r["detail"],
+        "clocks": r["clocks"], "gpu_launches": int(round(r["launches"] * args.steps)), "detail": r["detail"],
         "wall_s_timed_region": r["wall"],
     }
     if r.get("e2e"):

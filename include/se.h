@@ -199,6 +199,8 @@ typedef enum { SE_COMPACT_FRESH_PAGES = 0, SE_COMPACT_MOVE_LAST = 1 } se_compact
  *   same order (a busy page loses one reference instead).  New ctx_len =
  *   first_slot + n_keep; slot_map follows the entries; positions past the new
  *   length become -1.  max_keep (host) bounds n_keep for grid sizing.
+ *   A sequence with first_slot[b] = ctx_len[b] and n_keep[b] = 0 is left
+ *   untouched (no page moves), so one call can compact a subset of sequences.
  * MOVE_LAST: keep_idx [B][Hkv] victim slot per head (-1 on every head = no
  *   eviction for that sequence): the last resident entry moves into the
  *   victim slot, ctx_len - 1, a page left empty is pushed to the free list.

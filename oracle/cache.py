@@ -167,6 +167,7 @@ def compact(c: Cache, keep: List[List[np.ndarray]], first_slot: Sequence[int],
     of sequence b: [0, first_slot) unchanged (those sharing the first
     rewritten page are copied into the fresh page at the same slot), then
     keep[b][h] in order.  Slots past the new length get position -1 (aux 0).
+    A sequence with first_slot = ctx_len and nothing kept is left untouched.
     On SE_ERR_OUT_OF_PAGES / SE_ERR_UNEVEN nothing changes.
     """
     P = c.page_size
@@ -179,7 +180,11 @@ def compact(c: Cache, keep: List[List[np.ndarray]], first_slot: Sequence[int],
         n_keep.append(counts.pop())
 
     # Page accounting: every pop (ascending b, then block) before any push.
-    first_block = [first_slot[b] // P for b in range(B)]
+    # Reading (xxv): a sequence whose rewrite is empty (first_slot = ctx_len,
+    # nothing kept) is left as it is -- no page moves.
+    untouched = [int(first_slot[b]) == int(c.ctx_len[b]) and n_keep[b] == 0 for b in range(B)]
+    first_block = [cdiv(int(c.ctx_len[b]), P) if untouched[b] else first_slot[b] // P
+                   for b in range(B)]
     new_ctx = [first_slot[b] + n_keep[b] for b in range(B)]
     n_new = [max(cdiv(new_ctx[b], P) - first_block[b], 0) for b in range(B)]
     old_blocks = [cdiv(int(c.ctx_len[b]), P) for b in range(B)]

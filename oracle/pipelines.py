@@ -133,3 +133,36 @@ def kara_compress(c: Cache, q_win, q_pos, shape, groups=None, seqs=None):
                 keep[b][h] = selection.kara_keep(s[(b, h)], win_lo[b], shape.candidates,
                                                  shape.budget, shape.chunk_coef, prot_lo[b], ctx[b])
     return dict(scores=s, keep=keep, first_slot=win_lo)
+
+
+def kara_schedule_step(c: Cache, q, k_new, v_new, q_ring, win_start, shape):
+    """One step of Kara compression inside a decode loop (KARA Method,
+    periodic compression of the trailing window; reading (xxvi): the window
+    compresses when the appended token fills it, after that step's attention;
+    its queries are those of its own positions, which the caller keeps in
+    q_ring at slot position % window).  Sequences whose window is not full
+    are left as they are.  win_start (list) is updated in place."""
+    B, W = c.B, shape.window
+    for b in range(B):
+        q_ring[b, int(c.logical_len[b]) % W] = q[b]
+    st = cache.append(c, cache._bits(k_new), cache._bits(v_new))
+    assert st == cache.SE_OK
+    o, _ = attention.decode_attention(c, to_f64(q), "dense")
+    ctx = [int(x) for x in c.ctx_len]
+    due = [b for b in range(B) if ctx[b] - win_start[b] >= W]
+    keep_all, scores = None, {}
+    if due:
+        win_lo = [ctx[b] - W if b in due else ctx[b] for b in range(B)]
+        prot_lo = [ctx[b] - shape.protected if b in due else ctx[b] for b in range(B)]
+        q_pos = np.array([[int(c.logical_len[b]) - W + i for i in range(W)] for b in range(B)])
+        groups = [(b, h) for b in due for h in range(c.Hkv)]
+        scores = scoring.score_window(c, q_ring, q_pos, win_lo, ctx, win_lo, prot_lo,
+                                      causal=False, groups=groups)
+        keep_all = [[np.array([], dtype=np.int64)] * c.Hkv for _ in range(B)]
+        for b in due:
+            keep_all[b] = [selection.kara_keep(scores[(b, h)], win_lo[b], shape.candidates,
+                                               shape.budget, shape.chunk_coef, prot_lo[b], ctx[b])
+                           for h in range(c.Hkv)]
+        st = cache.compact(c, keep_all, win_lo)
+        assert st == cache.SE_OK
+    return dict(o=o, due=due, keep=keep_all, scores=scores)

@@ -140,6 +140,23 @@ class Kara(Shape):
         return int(math.floor(self.prune_keep_frac * (self.prune_R - self.prune_L)))
 
 
+@dataclasses.dataclass
+class KaraSchedule(Kara):
+    """Kara compression inside a decode loop, staggered across the batch:
+    every sequence compresses its trailing window whenever it fills, and the
+    sequences start at different fills so that only a few compress per step."""
+    steps: int = 320
+
+    @property
+    def period(self) -> int:
+        """Decode steps between two compressions of one sequence."""
+        return self.window - (self.budget + self.protected)
+
+    def fill(self, b: int) -> int:
+        """Window fill of sequence b before the first step."""
+        return self.budget + self.protected + (b * self.period // self.B) % self.period
+
+
 def snapkv_tiny(**kw) -> SnapKV:
     """1 sequence, GQA 4 (4 query heads / 1 KV head), d=64, fp32, 512 tokens."""
     base = dict(name="snapkv_tiny", B=1, Hq=4, Hkv=1, D=64, page_size=16, ctx=512,
@@ -184,12 +201,24 @@ def kara_prune(**kw) -> Kara:
     return Kara(**base)
 
 
+def kara_schedule(**kw) -> KaraSchedule:
+    """128 sequences decoding 320 steps over 2048 + window tokens, 32/8 heads,
+    d=128, bf16; Kara window 256 (32 protected), candidates 32, chunk budget
+    64, compressions staggered over the 160-step period."""
+    base = dict(name="kara_schedule", B=128, Hq=32, Hkv=8, D=128, page_size=16, ctx=2304,
+                dtype=torch.bfloat16, window=256, protected=32, candidates=32, budget=64,
+                chunk_coef=0.01, steps=320)
+    base.update(kw)
+    return KaraSchedule(**base)
+
+
 WORKLOADS = {
     "snapkv_tiny": snapkv_tiny,
     "snapkv_llama8b": snapkv_llama8b,
     "quest_decode": quest_decode,
     "h2o_decode": h2o_decode,
     "kara_prune": kara_prune,
+    "kara_schedule": kara_schedule,
 }
 
 
@@ -423,6 +452,27 @@ def h2o_chunked_inputs(shape: H2O, chunk: int, device):
                "chunked", "v")
     pos = torch.arange(shape.ctx, dtype=torch.int32).view(n, 1, chunk).repeat(1, shape.B, 1)
     return dict(cache=cache, q_chunks=q, k_chunks=k, v_chunks=v, q_pos=pos.to(device))
+
+
+def kara_schedule_inputs(shape: KaraSchedule, device, *, steps: Optional[int] = None):
+    """ctx resident tokens per sequence; sequence b's uncompressed window is its
+    last shape.fill(b) slots.  q_ring holds the queries of the last `window`
+    logical positions (slot position % window); per-step q, k, v."""
+    P = shape.page_size
+    steps = shape.steps if steps is None else steps
+    max_ctx = shape.ctx + steps + P
+    per_seq = cdiv(max_ctx, P) + cdiv(shape.window, P) + 1
+    cache = build_paged_cache(shape, num_pages=per_seq * shape.B, max_ctx=max_ctx,
+                              device=device)
+    q_ring = normal((shape.B, shape.window, shape.Hq, shape.D), shape.dtype, device,
+                    shape.name, "q_ring")
+    q_steps = normal((steps, shape.B, shape.Hq, shape.D), shape.dtype, device, shape.name,
+                     "q_steps")
+    k_steps = normal((steps, shape.B, shape.Hkv, shape.D), shape.dtype, device, shape.name,
+                     "k_steps")
+    v_steps = normal((steps, shape.B, shape.Hkv, shape.D), shape.dtype, device, shape.name,
+                     "v_steps")
+    return dict(cache=cache, q_ring=q_ring, q_steps=q_steps, k_steps=k_steps, v_steps=v_steps)
 
 
 def kara_inputs(shape: Kara, device):

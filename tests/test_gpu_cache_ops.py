@@ -251,6 +251,29 @@ def _gpu_compact(se, shape, pc, keep, first):
                         max_keep=max(width, 1))
 
 
+def test_compact_subset_leaves_other_sequences_untouched(cuda_lib):
+    """One call compacts sequences 0 and 2; 1 and 3 (first slot = context,
+    nothing kept) must not move at all."""
+    se = cuda_lib
+    shape, pc = _cache(torch.bfloat16, 128, B=4, Hkv=2, ctx=150, tag="sub")
+    c = ocache.from_tensors(pc)
+    rng = np.random.default_rng(4)
+    keep, first = [], []
+    for b in range(4):
+        if b % 2 == 0:
+            kb = np.sort(rng.choice(np.arange(40, 150), 37, replace=False))
+            keep.append([kb, np.sort(rng.choice(np.arange(40, 150), 37, replace=False))])
+            first.append(40)
+        else:
+            keep.append([np.array([], dtype=np.int64)] * 2)
+            first.append(150)
+    assert ocache.compact(c, keep, first) == ocache.SE_OK
+    _gpu_compact(se, shape, pc, keep, first)
+    torch.cuda.synchronize()
+    assert H.status(pc) == 0
+    H.assert_cache_equal(pc, c)
+
+
 def _prune_case(se, seed, busy_pages=0):
     shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=200, spare=60, tag=f"pr{seed}")
     c = ocache.from_tensors(pc)

@@ -309,6 +309,48 @@ def test_h2o_chunked_prefill_ragged_pages(cuda_lib):
     _h2o_chunked(cuda_lib, shape, 120)
 
 
+def _kara_schedule(cuda_lib, shape, steps):
+    """Kara compression inside a decode loop, staggered over the batch, in
+    lock-step with the oracle: the cache bit for bit after every step, kept
+    sets of every compression, attention outputs."""
+    inp = W.kara_schedule_inputs(shape, "cuda", steps=steps)
+    pc = inp["cache"]
+    c = ocache.from_tensors(pc)
+    fills = [shape.fill(b) for b in range(shape.B)]
+    ring_g = inp["q_ring"].clone()
+    ring_o = inp["q_ring"].cpu().clone()
+    win_start = [shape.ctx - f for f in fills]
+    pipe = P.KaraSchedule(pc, shape.Hq, ctx=shape.ctx, fills=fills, window=shape.window,
+                          protected=shape.protected, candidates=shape.candidates,
+                          budget=shape.budget, chunk_coef=shape.chunk_coef,
+                          max_ctx=shape.ctx + steps)
+    n_due = 0
+    for t in range(steps):
+        o = torch.empty_like(inp["q_steps"][t])
+        due = pipe.step(inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], o, ring_g)
+        r = opipe.kara_schedule_step(c, inp["q_steps"][t].cpu(), inp["k_steps"][t].cpu(),
+                                     inp["v_steps"][t].cpu(), ring_o, win_start, shape)
+        torch.cuda.synchronize()
+        assert H.status(pc) == 0
+        assert due == r["due"], (t, due, r["due"])
+        n_due += len(due)
+        if due:
+            kg = pipe.keep.cpu().numpy()
+            for b in due:
+                for h in range(shape.Hkv):
+                    assert list(kg[b, h]) == list(r["keep"][b][h]), (t, b, h)
+        H.assert_cache_equal(pc, c)
+        _check_out(o, r["o"], shape.dtype, shape.G)
+    assert n_due >= shape.B
+    return n_due
+
+
+def test_kara_schedule_reduced(cuda_lib):
+    shape = W.kara_schedule(B=5, Hq=8, Hkv=2, ctx=300, window=64, protected=8, candidates=8,
+                            budget=16)
+    _kara_schedule(cuda_lib, shape, 90)
+
+
 # ---------------------------------------------------------------------------
 # Kara + prune
 # ---------------------------------------------------------------------------

@@ -496,6 +496,48 @@ def test_release_conserves_pages(seed):
     assert c.free_top == before.free_top + released
 
 
+def test_kara_schedule_steps_untouched_and_compressed_sequences():
+    """Staggered Kara compression in a decode loop: sequences whose window is
+    not full only gain the appended token; a full window is cut to budget +
+    protected entries (candidates kept, protected tail kept); attention output
+    equals library SDPA over the resident entries before compression."""
+    shape = W.kara_schedule(B=3, Hq=4, Hkv=2, D=16, ctx=40, window=16, protected=4,
+                            candidates=4, budget=6, steps=14, dtype=torch.float32,
+                            name="ks_tiny")
+    inp = W.kara_schedule_inputs(shape, "cpu")
+    c = oc(inp["cache"])
+    ring = inp["q_ring"].clone()
+    win_start = [shape.ctx - shape.fill(b) for b in range(3)]
+    seen_due = 0
+    for t in range(shape.steps):
+        before = c.copy()
+        r = pipelines.kara_schedule_step(c, inp["q_steps"][t], inp["k_steps"][t],
+                                         inp["v_steps"][t], ring, win_start, shape)
+        for b in range(3):
+            n0 = int(before.ctx_len[b])
+            if b in r["due"]:
+                seen_due += 1
+                lo = n0 + 1 - shape.window
+                assert c.ctx_len[b] == lo + shape.budget + shape.protected
+                for h in range(2):
+                    kept = r["keep"][b][h]
+                    assert len(kept) == shape.budget + shape.protected
+                    assert set(range(n0 + 1 - shape.protected, n0 + 1)) <= set(kept.tolist())
+            else:
+                assert c.ctx_len[b] == n0 + 1
+                assert (c.block_table[b, : before.block_table.shape[1]][before.block_table[b] >= 0]
+                        == before.block_table[b][before.block_table[b] >= 0]).all()
+            for g in range(2):
+                Q = inp["q_steps"][t][b, g * shape.G:(g + 1) * shape.G].double().numpy()
+                slots = np.arange(n0 + 1)
+                # the appended entry is resident in the cache as it was after append
+                cc = before.copy()
+                cache.append(cc, cache._bits(inp["k_steps"][t]), cache._bits(inp["v_steps"][t]))
+                ref = sdpa_out(Q, cc.keys(b, g, slots), cc.vals(b, g, slots))
+                np.testing.assert_allclose(r["o"][(b, g)], ref, rtol=1e-12, atol=1e-13)
+    assert seen_due >= 3
+
+
 # ---------------------------------------------------------------------------
 # O6 Quest
 # ---------------------------------------------------------------------------
@@ -638,6 +680,22 @@ def test_compact_out_of_pages_changes_nothing():
     keep = [[np.arange(0, 10)] * 2 for _ in range(2)]
     assert cache.compact(c, keep, [0, 0]) == cache.SE_ERR_OUT_OF_PAGES
     assert (c.block_table == before.block_table).all() and c.free_top == 1
+
+
+def test_compact_leaves_empty_rewrites_untouched():
+    """Sequence 1 (ctx 21, not a page multiple) asks for an empty rewrite:
+    nothing of it moves, while sequence 0 is compacted as usual."""
+    shape = tiny_shape(B=2, ctx=21, page_size=4)
+    c = oc(tiny_cache(shape, num_pages=30))
+    before = c.copy()
+    keep = [[np.array([9, 12, 20])] * 2, [np.array([], dtype=np.int64)] * 2]
+    assert cache.compact(c, keep, [8, 21]) == cache.SE_OK
+    assert (c.block_table[1] == before.block_table[1]).all()
+    assert (c.slot_map[1] == before.slot_map[1]).all() and c.ctx_len[1] == 21
+    assert c.ctx_len[0] == 11
+    # only sequence 0's pages moved: one fresh page popped, its 4 old ones pushed
+    assert c.free_top == before.free_top - 1 + 4
+    _check_accounting(before, c)
 
 
 def test_move_last_and_append():
