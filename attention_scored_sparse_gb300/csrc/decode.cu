@@ -470,12 +470,18 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) q[j][i] *= qscale;
   }
-  float m[G], o[G][V];
+  // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
+  constexpr int V2 = V / 2;
+  uint64_t q2[G][V2], o2[G][V2];
+  float m[G];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     m[j] = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < V; ++i) o[j][i] = 0.f;
+    for (int i = 0; i < V2; ++i) {
+      q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
+      o2[j][i] = 0;
+    }
   }
   float l_own = 0.f;
   float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
@@ -533,14 +539,20 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     if (lane == 0) tc::mbar_arrive(&empty[s]);   // rows are in registers now
     float part[16];
 #pragma unroll
-    for (int u = 0; u < E; ++u)
+    for (int u = 0; u < E; ++u) {
+      uint64_t k2[V2];
+#pragma unroll
+      for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[u][2 * i], kf[u][2 * i + 1]);
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        float acc = 0.f;
+        uint64_t acc2 = 0;
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[u][i], acc);
-        part[u * G + j] = acc;
+        for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
+        float lo, hi;
+        tc::f2split(acc2, lo, hi);
+        part[u * G + j] = lo + hi;
       }
+    }
 #pragma unroll
     for (int step = 0; step < 4; ++step) {
       const int off = 8 >> step;
@@ -580,17 +592,23 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     __syncwarp();
     if (grew) {
 #pragma unroll
-      for (int j = 0; j < G; ++j)
+      for (int j = 0; j < G; ++j) {
+        const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
 #pragma unroll
-        for (int i = 0; i < V; ++i) o[j][i] *= alpha[j];
+        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
+      }
     }
 #pragma unroll
     for (int u = 0; u < E; ++u) {
+      uint64_t v2[V2];
+#pragma unroll
+      for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[u][2 * i], vf[u][2 * i + 1]);
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const float pu = s_p[hw][u * G + j];
+        const uint64_t p2 = tc::f2(pu, pu);
 #pragma unroll
-        for (int i = 0; i < V; ++i) o[j][i] = fmaf(pu, vf[u][i], o[j][i]);
+        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
       }
     }
     __syncwarp();
@@ -614,7 +632,12 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
 #pragma unroll
   for (int j = 0; j < G; ++j)
 #pragma unroll
-    for (int i = 0; i < V; ++i) s_o[hw][j][t * V + i] = o[j][i];
+    for (int i = 0; i < V2; ++i) {
+      float lo, hi;
+      tc::f2split(o2[j][i], lo, hi);
+      s_o[hw][j][t * V + 2 * i] = lo;
+      s_o[hw][j][t * V + 2 * i + 1] = hi;
+    }
   __syncthreads();
   float* part = a.part + (((int64_t)b * kv.Hkv + g) * a.n_chunks + c) * G * (D + 2);
   for (int x = threadIdx.x; x < G * D; x += 128) {

@@ -241,23 +241,31 @@ class KaraSchedule(_Base):
     just filled (bidirectional scores of the window's queries, Token2Chunk,
     compaction from the window start); the other sequences get empty ranges
     and are left untouched by every call.  The window's queries live in a
-    ring indexed by logical position modulo the window.  Lengths are tracked
-    on the host (they follow from the schedule), so no step reads the device."""
+    ring indexed by logical position modulo the window.  Lengths follow from
+    the schedule and are tracked on the host; the per-step ranges reach the
+    device through pinned buffers with asynchronous copies, so no step waits
+    for the GPU."""
 
     def __init__(self, cache, Hq, *, ctx, fills, window, protected, candidates, budget,
-                 chunk_coef, max_ctx):
+                 chunk_coef, max_ctx, n_staging=8):
         super().__init__(cache, Hq)
         B, dev = self.B, self.device
         self.window, self.protected = window, protected
         self.candidates, self.budget, self.coef = candidates, budget, chunk_coef
-        self.ctx = [ctx] * B                         # resident entries
-        self.logical = [ctx] * B                     # logical length
+        self.ctx = [ctx] * B                         # resident entries (host mirror)
+        self.logical = [ctx] * B                     # logical length (host mirror)
         self.win_start = [ctx - f for f in fills]    # first slot of the window
         self.scores = torch.zeros((B, self.Hkv, self.max_slots), dtype=torch.float32, device=dev)
         self.keep = torch.empty((B, self.Hkv, budget + protected), dtype=torch.int32, device=dev)
         self.n_keep = torch.empty(B, dtype=torch.int32, device=dev)
-        self.ranges = torch.empty((4, B), dtype=torch.int32, device=dev)
-        self.q_pos = torch.empty((B, window), dtype=torch.int32, device=dev)
+        # device copies of the step's lengths: [logical, win_lo, ctx, prot_lo]
+        self.lens = torch.empty((4, B), dtype=torch.int32, device=dev)
+        self.staging = [torch.empty((4, B), dtype=torch.int32).pin_memory()
+                        for _ in range(n_staging)]
+        self.staged = [None] * n_staging             # event after each buffer's copy
+        self.n_steps = 0
+        self.rows = torch.arange(B, device=dev)
+        self.offs = torch.arange(window, dtype=torch.int32, device=dev) - window
         self.max_ctx = max_ctx
         sz = workspace_sizes(self.kv, w=window, n_max=window, max_keep=budget + protected,
                              max_entries=max_ctx)
@@ -267,28 +275,39 @@ class KaraSchedule(_Base):
         self.ws_append = self._ws(sz["append_kv"])
         self.compressions = 0
 
+    def _upload(self, rows, stream):
+        i = self.n_steps % len(self.staging)
+        if self.staged[i] is not None:
+            self.staged[i].synchronize()             # the copy that used it has run
+        buf = self.staging[i]
+        buf.copy_(torch.tensor(rows, dtype=torch.int32))
+        self.lens.copy_(buf, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+        self.staged[i] = ev
+
     def step(self, q, k_new, v_new, o, q_ring, stream=None):
         B, W = self.B, self.window
-        ring_slot = torch.tensor([lg % W for lg in self.logical], device=self.device)
-        q_ring[torch.arange(B, device=self.device), ring_slot] = q
+        due = [b for b in range(B) if self.ctx[b] + 1 - self.win_start[b] >= W]
+        win_lo = [self.ctx[b] + 1 - W if b in due else self.ctx[b] + 1 for b in range(B)]
+        ctx1 = [c + 1 for c in self.ctx]
+        prot_lo = [ctx1[b] - self.protected if b in due else ctx1[b] for b in range(B)]
+        self._upload([self.logical, win_lo, ctx1, prot_lo], stream)
+        self.n_steps += 1
+        # the new token's query goes to ring slot (its position % window)
+        q_ring[self.rows, (self.lens[0] % W).long()] = q
         se_append_kv(self.kv, k_new, v_new, workspace=self.ws_append, stream=stream)
+        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.max_ctx,
+                              workspace=self.ws_decode, stream=stream)
         for b in range(B):
             self.ctx[b] += 1
             self.logical[b] += 1
-        se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.max_ctx,
-                              workspace=self.ws_decode, stream=stream)
-        due = [b for b in range(B) if self.ctx[b] - self.win_start[b] >= W]
         if not due:
             return due
-        win_lo = [self.ctx[b] - W if b in due else self.ctx[b] for b in range(B)]
-        prot_lo = [self.ctx[b] - self.protected if b in due else self.ctx[b] for b in range(B)]
-        rng = torch.tensor([win_lo, self.ctx, prot_lo, win_lo], dtype=torch.int32)
-        self.ranges.copy_(rng)
-        pos = torch.tensor([[self.logical[b] - W + i for i in range(W)] for b in range(B)],
-                           dtype=torch.int32)
-        self.q_pos.copy_(pos)
-        lo, hi, plo = self.ranges[0], self.ranges[1], self.ranges[2]
-        se_score_window(self.kv, q_ring, self.q_pos, lo, hi, lo, plo, causal=False,
+        # positions of the window's queries: the last W before the new length
+        q_pos = (self.lens[0] + 1)[:, None] + self.offs[None, :]
+        lo, hi, plo = self.lens[1], self.lens[2], self.lens[3]
+        se_score_window(self.kv, q_ring, q_pos, lo, hi, lo, plo, causal=False,
                         accumulate=False, n_max=W, scores=self.scores, workspace=self.ws_score,
                         stream=stream)
         se_topk_select(self.kv, self.scores, mode=SE_SELECT_KARA_CHUNK, cand_lo=lo, cand_hi=plo,
@@ -296,7 +315,7 @@ class KaraSchedule(_Base):
                        k=self.candidates, chunk_budget=self.budget, chunk_coef=self.coef,
                        n_max=W - self.protected, stream=stream)
         se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
-                         first_slot=self.ranges[3], max_keep=self.budget + self.protected,
+                         first_slot=lo, max_keep=self.budget + self.protected,
                          workspace=self.ws_compact, stream=stream)
         for b in due:
             self.ctx[b] = win_lo[b] + self.budget + self.protected
