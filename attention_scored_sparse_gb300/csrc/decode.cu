@@ -346,6 +346,17 @@ SE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
       : "memory");
 }
 
+// V elements of a K or V row in shared memory, as fp32.
+template <typename T, int V>
+SE_DEV void load_row_smem(const T* r, float* f) {
+  if constexpr (sizeof(T) == 2 && V == 8) {
+    unpack8_bf16(*reinterpret_cast<const uint4*>(r), f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) f[i] = (float)r[i];
+  }
+}
+
 constexpr int kMaxChunk = 1024;   // view entries per CTA at most (see pick_chunk)
 
 template <typename T, int D, int G>
@@ -355,7 +366,9 @@ struct StagedGeom {
   static constexpr int SE = 8 * E;                 // entries per stage
   static constexpr int RB = D * (int)sizeof(T);    // bytes per K (or V) row
   static constexpr int STAGE_BYTES = SE * RB * 2;
-  static constexpr int STAGES = STAGE_BYTES <= 16384 ? 4 : (STAGE_BYTES <= 32768 ? 2 : 0);
+  // three 16 KB stages keep four CTAs (sixteen warps) on an SM with 127 registers a thread
+  static constexpr int STAGES =
+      STAGE_BYTES <= 8192 ? 4 : (STAGE_BYTES <= 16384 ? 3 : (STAGE_BYTES <= 32768 ? 2 : 0));
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
 };
 
@@ -513,36 +526,23 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
     const uint8_t* vst = kst + SE * RB;
     const int e0 = e_begin + it * SE + hw * E;
-    float kf[E][V], vf[E][V];
+    // K rows are read from the stage one entry at a time; V rows are read
+    // again after the probabilities are known (the stage is released after)
     bool valid[E];
-#pragma unroll
-    for (int u = 0; u < E; ++u) {
-      const int e = e0 + u;
-      valid[u] = s_valid[s][hw * E + u] != 0;
-      (void)e;
-      if (valid[u]) {
-        const T* kr = reinterpret_cast<const T*>(kst + (hw * E + u) * RB) + t * V;
-        const T* vr = reinterpret_cast<const T*>(vst + (hw * E + u) * RB) + t * V;
-        if constexpr (sizeof(T) == 2 && V == 8) {
-          unpack8_bf16(*reinterpret_cast<const uint4*>(kr), kf[u]);
-          unpack8_bf16(*reinterpret_cast<const uint4*>(vr), vf[u]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < V; ++i) { kf[u][i] = (float)kr[i]; vf[u][i] = (float)vr[i]; }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) { kf[u][i] = 0.f; vf[u][i] = 0.f; }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[s]);   // rows are in registers now
     float part[16];
 #pragma unroll
     for (int u = 0; u < E; ++u) {
+      valid[u] = s_valid[s][hw * E + u] != 0;
+      float kf[V];
+      if (valid[u]) {
+        load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + u) * RB) + t * V, kf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) kf[i] = 0.f;
+      }
       uint64_t k2[V2];
 #pragma unroll
-      for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[u][2 * i], kf[u][2 * i + 1]);
+      for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         uint64_t acc2 = 0;
@@ -600,9 +600,16 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < E; ++u) {
+      float vf[V];
+      if (valid[u]) {
+        load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + u) * RB) + t * V, vf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) vf[i] = 0.f;
+      }
       uint64_t v2[V2];
 #pragma unroll
-      for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[u][2 * i], vf[u][2 * i + 1]);
+      for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const float pu = s_p[hw][u * G + j];
@@ -612,6 +619,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with this stage's rows
   }
   // drain: after a timeout, copies of the last stages may still be in flight
   // (each earlier stage was waited on before its buffer was refilled)

@@ -294,14 +294,15 @@ SE_DEV void rowstats_block(const uint32_t (&r)[N], bool fast, bool row_ok, int k
 // One 32-row block of a key's column sum in pass 2: adds
 // exp2(logit * scale - lse2) over the rows that see the key (nlse holds
 // -lse2 per row).  fast: every row of the chunk sees it.
-SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const float* nlse,
+template <int N>
+SE_DEV void colsum_block(const uint32_t (&r)[N], bool fast, int kpos, const float* nlse,
                          const int* qp, float scale, float& cs0, float& cs1, float& cs2,
                          float& cs3) {
   if (fast) {
     const uint64_t sc2 = tc::f2(scale, scale);
     uint64_t s01 = tc::f2(cs0, cs1), s23 = tc::f2(cs2, cs3);
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
+    for (int j = 0; j < N; j += 4) {
       const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nlse + j);   // two pairs
       float a0, a1, b0, b1;
       tc::f2split(tc::ffma2(tc::f2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, nl.x),
@@ -316,7 +317,7 @@ SE_DEV void colsum_block(const uint32_t (&r)[32], bool fast, int kpos, const flo
     return;
   }
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     float p0 = tc::ex2(fmaf(__uint_as_float(r[j]), scale, nlse[j]));
     float p1 = tc::ex2(fmaf(__uint_as_float(r[j + 1]), scale, nlse[j + 1]));
     if (kpos > qp[j]) p0 = 0.f;
@@ -358,6 +359,28 @@ SE_DEV void colsum_tile_seq(uint32_t tb, bool fast, int kpos, const float* lse_s
     tc::tmem_ld32_async(tb + c * 32, r);
     tc::tmem_wait32(r);
     colsum_block(r, fast, kpos, lse_s + c * 32, qp_s + c * 32, scale, cs0, cs1, cs2, cs3);
+  }
+}
+
+// Column sum over 16 NB rows with 16-column TMEM loads, each block loaded
+// while the previous one is summed (the same registers as one 32-column
+// block, the load latency hidden inside the warp).
+template <int NB>
+SE_DEV void colsum_tile_pipe16(uint32_t tb, bool fast, int kpos, const float* lse_s,
+                               const int* qp_s, float scale, float& cs0, float& cs1, float& cs2,
+                               float& cs3) {
+  uint32_t ra[16], rb[16];
+  tc::tmem_ld16_async(tb, ra);
+  tc::tmem_wait16(ra);
+#pragma unroll 1
+  for (int c = 0; c < NB; c += 2) {
+    tc::tmem_ld16_async(tb + (c + 1) * 16, rb);
+    colsum_block<16>(ra, fast, kpos, lse_s + c * 16, qp_s + c * 16, scale, cs0, cs1, cs2, cs3);
+    tc::tmem_wait16(rb);
+    if (c + 2 < NB) tc::tmem_ld16_async(tb + (c + 2) * 16, ra);
+    colsum_block<16>(rb, fast, kpos, lse_s + (c + 1) * 16, qp_s + (c + 1) * 16, scale, cs0, cs1,
+                     cs2, cs3);
+    if (c + 2 < NB) tc::tmem_wait16(ra);
   }
 }
 
@@ -1382,8 +1405,8 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         fast = kpos <= mn;
       }
       float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-      colsum_tile_seq<4>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128, fast,
-                         kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
+      colsum_tile_pipe16<8>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128,
+                            fast, kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
