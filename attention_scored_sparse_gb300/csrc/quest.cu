@@ -64,9 +64,13 @@ __global__ void quest_meta_kernel(se_paged_kv kv, T* kmin, T* kmax) {
   }
 }
 
-// Page bound U for every full block.  grid: (cdiv(max_blocks, 16), Hkv, B),
-// 256 threads = 8 warps x 2 half-warps, one block per half-warp.
-// D = 128 bf16: lane t of the half-warp owns dims [8t, 8t+8).
+// Page bound U for every full block.  grid: (cdiv(max_blocks, 64), Hkv, B),
+// 256 threads = 8 warps x 2 half-warps; each half-warp takes four blocks
+// (16 apart, so a warp's block-table reads are contiguous) with all their
+// loads in flight together.  D = 128 bf16: lane t of the half-warp owns dims
+// [8t, 8t+8).
+constexpr int kBoundPages = 4;   // blocks per half-warp
+
 template <int G>
 __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
                                                                const __nv_bfloat16* __restrict__ kmin,
@@ -78,7 +82,15 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
   const int P = kv.page_size;
   const int nb = cdiv(kv.ctx_len[b], P);
   const int half = threadIdx.x >> 4, t = threadIdx.x & 15;
-  const int blk = blockIdx.x * 16 + half;
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  int blk[kBoundPages], page[kBoundPages];
+  bool act[kBoundPages];
+#pragma unroll
+  for (int u = 0; u < kBoundPages; ++u) {
+    blk[u] = blockIdx.x * 16 * kBoundPages + u * 16 + half;
+    act[u] = blk[u] < nb - 1 && blk[u] < u_stride;
+    page[u] = act[u] ? bt[blk[u]] : 0;
+  }
   // max(q kmax, q kmin) = max(q, 0) kmax + min(q, 0) kmin: two FMAs per term
   float qp[G][8], qn[G][8];
 #pragma unroll
@@ -92,25 +104,33 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
       qn[j][i] = fminf(qv[i], 0.f);
     }
   }
-  float acc = 0.f;
-  const bool active = blk < nb - 1 && blk < u_stride;
-  if (active) {
-    const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
-    const int64_t o = ((int64_t)page * kv.Hkv + g) * kv.D + t * 8;
-    float mn[8], mx[8];
-    unpack8_bf16(ldg_nc_v4(kmin + o), mn);
-    unpack8_bf16(ldg_nc_v4(kmax + o), mx);
+  uint4 mnr[kBoundPages], mxr[kBoundPages];
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-      float part = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) part = fmaf(qn[j][i], mn[i], fmaf(qp[j][i], mx[i], part));
-      acc += part;
+  for (int u = 0; u < kBoundPages; ++u)
+    if (act[u]) {
+      const int64_t o = ((int64_t)page[u] * kv.Hkv + g) * kv.D + t * 8;
+      mnr[u] = ldg_nc_v4(kmin + o);
+      mxr[u] = ldg_nc_v4(kmax + o);
     }
-  }
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (active && t == 0) U[((int64_t)b * kv.Hkv + g) * u_stride + blk] = acc;
+  for (int u = 0; u < kBoundPages; ++u) {
+    float acc = 0.f;
+    if (act[u]) {
+      float mn[8], mx[8];
+      unpack8_bf16(mnr[u], mn);
+      unpack8_bf16(mxr[u], mx);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part = fmaf(qn[j][i], mn[i], fmaf(qp[j][i], mx[i], part));
+        acc += part;
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (act[u] && t == 0) U[((int64_t)b * kv.Hkv + g) * u_stride + blk[u]] = acc;
+  }
 }
 
 // Generic bound (any D, fp32 or bf16): one thread per (block, group).
@@ -137,10 +157,10 @@ __global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const 
   U[((int64_t)b * kv.Hkv + g) * u_stride + blk] = acc;
 }
 
-// cand_hi = nblocks - 1, forced = [nblocks - 1, nblocks)
+// candidates [0, nblocks - 1), forced = [nblocks - 1, nblocks)
 __global__ void quest_ranges_kernel(const int32_t* ctx_len, int B, int P, int max_blocks,
-                                    int32_t* status, int32_t* cand_hi, int32_t* flo,
-                                    int32_t* fhi) {
+                                    int32_t* status, int32_t* cand_lo, int32_t* cand_hi,
+                                    int32_t* flo, int32_t* fhi) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   int nb = cdiv(ctx_len[b], P);
@@ -148,6 +168,7 @@ __global__ void quest_ranges_kernel(const int32_t* ctx_len, int B, int P, int ma
     set_status(status, SE_ERR_BOUNDS);
     nb = max_blocks;
   }
+  cand_lo[b] = 0;
   cand_hi[b] = max(nb - 1, 0);
   flo[b] = max(nb - 1, 0);
   fhi[b] = nb;
@@ -204,10 +225,6 @@ extern "C" size_t se_quest_page_select_workspace_size(const se_paged_kv* kv, int
   return b;
 }
 
-__global__ void se_fill_zero_i32(int32_t* p, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0;
-}
 
 extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmin,
                                           const void* kmax, const void* q, int32_t top_pages,
@@ -224,7 +241,7 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = kv->Hq / kv->Hkv;
-  dim3 grid(cdiv(max_blocks, 16), kv->Hkv, kv->B);
+  dim3 grid(cdiv(max_blocks, 16 * kBoundPages), kv->Hkv, kv->B);
   if (kv->dtype == SE_BF16 && kv->D == 128 && (G == 1 || G == 2 || G == 4 || G == 8)) {
     auto km = static_cast<const __nv_bfloat16*>(kmin);
     auto kx = static_cast<const __nv_bfloat16*>(kmax);
@@ -244,10 +261,9 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
           *kv, static_cast<const float*>(kmin), static_cast<const float*>(kmax),
           static_cast<const float*>(q), w.U, w.u_stride);
   }
-  se_fill_zero_i32<<<cdiv(kv->B, 256), 256, 0, st>>>(w.cand_lo, kv->B);
   quest_ranges_kernel<<<cdiv(kv->B, 256), 256, 0, st>>>(kv->ctx_len, kv->B, kv->page_size,
-                                                        max_blocks, kv->status, w.cand_hi, w.flo,
-                                                        w.fhi);
+                                                        max_blocks, kv->status, w.cand_lo,
+                                                        w.cand_hi, w.flo, w.fhi);
   s = launch_topk_select_pages(kv->B, kv->Hkv, w.U, w.u_stride, w.cand_lo, w.cand_hi, w.flo,
                                w.fhi, page_idx, top_pages + 1, n_sel, kv->status, top_pages,
                                max_blocks, st);

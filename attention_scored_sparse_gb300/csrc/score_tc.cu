@@ -362,28 +362,6 @@ SE_DEV void colsum_tile_seq(uint32_t tb, bool fast, int kpos, const float* lse_s
   }
 }
 
-// Column sum over 16 NB rows with 16-column TMEM loads, each block loaded
-// while the previous one is summed (the same registers as one 32-column
-// block, the load latency hidden inside the warp).
-template <int NB>
-SE_DEV void colsum_tile_pipe16(uint32_t tb, bool fast, int kpos, const float* lse_s,
-                               const int* qp_s, float scale, float& cs0, float& cs1, float& cs2,
-                               float& cs3) {
-  uint32_t ra[16], rb[16];
-  tc::tmem_ld16_async(tb, ra);
-  tc::tmem_wait16(ra);
-#pragma unroll 1
-  for (int c = 0; c < NB; c += 2) {
-    tc::tmem_ld16_async(tb + (c + 1) * 16, rb);
-    colsum_block<16>(ra, fast, kpos, lse_s + c * 16, qp_s + c * 16, scale, cs0, cs1, cs2, cs3);
-    tc::tmem_wait16(rb);
-    if (c + 2 < NB) tc::tmem_ld16_async(tb + (c + 2) * 16, ra);
-    colsum_block<16>(rb, fast, kpos, lse_s + (c + 1) * 16, qp_s + (c + 1) * 16, scale, cs0, cs1,
-                     cs2, cs3);
-    if (c + 2 < NB) tc::tmem_wait16(ra);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Pass 1: row statistics.  grid (n_splits, RC, B*Hkv), 576 threads.
 // ---------------------------------------------------------------------------
@@ -1405,8 +1383,8 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         fast = kpos <= mn;
       }
       float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-      colsum_tile_pipe16<8>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128,
-                            fast, kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
+      colsum_tile_seq<4>(tmem + ((uint32_t)(quarter * 32) << 16) + set * 256 + half * 128, fast,
+                         kpos, lse_s, qp_s, a.scale, cs0, cs1, cs2, cs3);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -437,7 +437,7 @@ def run_quest(args, torch, rank, world):
                 kernel="quest step (bound + top-k + decode attention)",
                 per_launch=f"{meta_bytes + kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
-                launches=4 + 1 + 1, metric="decode tokens/s", e2e=None,
+                launches=3 + 1 + 1, metric="decode tokens/s", e2e=None,
                 cfg={"workload": "quest_decode: B=2 x 131072 tokens, top 128 pages + current, "
                                  "32/8 heads, d=128, bf16",
                      "l2": "L2 flushed (256 MB write) before every timed step"},
