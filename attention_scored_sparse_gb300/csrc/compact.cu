@@ -69,6 +69,7 @@ static CompactWs carve_compact(const se_paged_kv* kv, int32_t max_keep, void* ws
 __global__ void __launch_bounds__(1024) compact_plan_kernel(
     se_paged_kv kv, const int32_t* __restrict__ n_keep, const int32_t* __restrict__ first_slot,
     int32_t max_keep, const int32_t* __restrict__ abort_in, CompactWs w) {
+  pdl_enter();
   __shared__ int tmp[33];
   __shared__ int s_bad;
   __shared__ int s_run_new;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
     se_paged_kv kv, const int32_t* __restrict__ keep_idx, int32_t keep_stride,
     const int32_t* __restrict__ first_slot, const float* __restrict__ aux, int64_t aux_stride,
     CompactWs w, int entries_per_cta) {
+  pdl_enter();
   if (w.ctrl->abort) return;
   const int h = blockIdx.y, b = blockIdx.z;
   const int P = kv.page_size;
@@ -317,6 +319,7 @@ SE_DEV void commit_slots(const se_paged_kv& kv, float* aux, int64_t aux_stride,
 // chunk c of the slot map of (b, h).  Nothing runs after a planning error.
 __global__ void __launch_bounds__(1024) compact_commit_kernel(se_paged_kv kv, float* aux,
                                                               int64_t aux_stride, CompactWs w) {
+  pdl_enter();
   if (w.ctrl->abort) return;
   const int h = blockIdx.y, b = blockIdx.z;
   if (blockIdx.x == 0) {
@@ -351,6 +354,7 @@ static MoveWs carve_move(const se_paged_kv* kv, void* ws, size_t* bytes) {
 __global__ void __launch_bounds__(1024) move_last_plan_kernel(se_paged_kv kv,
                                                               const int32_t* __restrict__ victim,
                                                               MoveWs w) {
+  pdl_enter();
   __shared__ int tmp[33];
   __shared__ int s_bad, s_run;
   const int tid = threadIdx.x;
@@ -399,6 +403,7 @@ __global__ void __launch_bounds__(256) move_last_apply_kernel(se_paged_kv kv,
                                                               const int32_t* __restrict__ victim,
                                                               float* aux, int64_t aux_stride,
                                                               MoveWs w) {
+  pdl_enter();
   if (w.ctrl->abort) return;
   const int b = blockIdx.x;
   if (!w.act[b]) return;
@@ -474,6 +479,7 @@ static AppendWs carve_append(const se_paged_kv* kv, void* ws, size_t* bytes) {
 // 1 CTA: bounds, fresh pages per sequence (blocks cdiv(ctx, P) ..
 // cdiv(ctx + n, P) - 1), pop ranks in ascending (b, block), capacity.
 __global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, int n, AppendWs w) {
+  pdl_enter();
   __shared__ int tmp[33];
   __shared__ int s_bad, s_run;
   const int tid = threadIdx.x;
@@ -519,6 +525,7 @@ __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
                                                            const void* __restrict__ v_new, int n,
                                                            float* aux, int64_t aux_stride,
                                                            void* kmin, void* kmax, AppendWs w) {
+  pdl_enter();
   if (w.ctrl->abort) return;
   const int b = blockIdx.y;
   const int P = kv.page_size;
@@ -631,6 +638,7 @@ __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
                                                           const uint8_t* __restrict__ mask,
                                                           int32_t mask_stride, int32_t* n_busy,
                                                           PruneWs w) {
+  pdl_enter();
   __shared__ int tmp[33];
   __shared__ int s_first, s_busy, s_count0, s_bad;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -698,7 +706,10 @@ __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
   }
 }
 
-__global__ void zero_int_kernel(int32_t* p) { *p = 0; }
+__global__ void zero_int_kernel(int32_t* p) {
+  pdl_enter();
+  *p = 0;
+}
 
 // ---------------------------------------------------------------------------
 // Release of whole sequences (reclaim of an idle chain's row)
@@ -727,6 +738,7 @@ SE_DEV bool release_pushes(const se_paged_kv& kv, int page) {
 __global__ void __launch_bounds__(1024) release_count_kernel(se_paged_kv kv,
                                                              const int32_t* __restrict__ mask,
                                                              ReleaseWs w) {
+  pdl_enter();
   __shared__ int s_cnt;
   const int b = blockIdx.x;
   if (threadIdx.x == 0) s_cnt = 0;
@@ -755,6 +767,7 @@ __global__ void __launch_bounds__(1024) release_count_kernel(se_paged_kv kv,
 __global__ void __launch_bounds__(1024) release_apply_kernel(se_paged_kv kv,
                                                              const int32_t* __restrict__ mask,
                                                              ReleaseWs w) {
+  pdl_enter();
   __shared__ int tmp[33];
   __shared__ int s_off, s_total;
   if (w.ctrl->abort) return;
@@ -818,7 +831,7 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
   size_t need = 0;
   CompactWs w = carve_compact(kv, max_keep, ws, aux != nullptr, &need);
   if (ws == nullptr || ws_bytes < need) return SE_ERR_INVALID_ARG;
-  compact_plan_kernel<<<1, 1024, 0, st>>>(*kv, n_keep, first_slot, max_keep, abort_in, w);
+  se_launch(compact_plan_kernel, 1, 1024, 0, st, *kv, n_keep, first_slot, max_keep, abort_in, w);
   const int row_bytes = kv->D * (int)elem_size(kv->dtype);
   const int chunks = row_bytes / 16;
   const int max_entries = max_keep + kv->page_size;
@@ -826,19 +839,19 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
   switch (chunks) {
     case 8: {
       const int epc = 4 * (256 / 8);
-      compact_gather_kernel<8><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+      se_launch(compact_gather_kernel<8>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
     }
     case 16: {
       const int epc = 4 * (256 / 16);
-      compact_gather_kernel<16><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+      se_launch(compact_gather_kernel<16>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
     }
     case 32: {
       const int epc = 4 * (256 / 32);
-      compact_gather_kernel<32><<<dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st>>>(
+      se_launch(compact_gather_kernel<32>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
     }
@@ -846,7 +859,7 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
       return SE_ERR_UNSUPPORTED;
   }
   const int max_span = kv->max_pages_per_seq * kv->page_size;
-  compact_commit_kernel<<<dim3(1 + cdiv(max_span, 4096), kv->Hkv, kv->B), 1024, 0, st>>>(
+  se_launch(compact_commit_kernel, dim3(1 + cdiv(max_span, 4096), kv->Hkv, kv->B), 1024, 0, st,
       *kv, aux, aux_stride, w);
   return se_last_launch_status();
 }
@@ -878,8 +891,8 @@ extern "C" se_status se_compact_evict(const se_paged_kv* kv, int32_t mode,
     size_t need = 0;
     MoveWs w = carve_move(kv, workspace, &need);
     if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
-    move_last_plan_kernel<<<1, 1024, 0, st>>>(*kv, keep_idx, w);
-    move_last_apply_kernel<<<kv->B, 256, 0, st>>>(*kv, keep_idx, aux, aux_stride, w);
+    se_launch(move_last_plan_kernel, 1, 1024, 0, st, *kv, keep_idx, w);
+    se_launch(move_last_apply_kernel, kv->B, 256, 0, st, *kv, keep_idx, aux, aux_stride, w);
     return se_last_launch_status();
   }
   return SE_ERR_INVALID_ARG;
@@ -907,9 +920,9 @@ extern "C" se_status se_append_kv(const se_paged_kv* kv, const void* k_new, cons
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   if (n_new == 0) return SE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  append_plan_kernel<<<1, 1024, 0, st>>>(*kv, n_new, w);
+  se_launch(append_plan_kernel, 1, 1024, 0, st, *kv, n_new, w);
   const dim3 grid(cdiv(n_new + kv->page_size - 1, kv->page_size), kv->B);
-  append_apply_kernel<<<grid, 256, 0, st>>>(*kv, k_new, v_new, n_new, aux, aux_stride, kmin, kmax,
+  se_launch(append_apply_kernel, grid, 256, 0, st, *kv, k_new, v_new, n_new, aux, aux_stride, kmin, kmax,
                                             w);
   return se_last_launch_status();
 }
@@ -934,8 +947,8 @@ extern "C" se_status se_prune_span(const se_paged_kv* kv, const int32_t* L, cons
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int32_t smax = kv->max_pages_per_seq * kv->page_size;
-  zero_int_kernel<<<1, 1, 0, st>>>(w.abort);
-  prune_plan_kernel<<<kv->B, 1024, 0, st>>>(*kv, L, R, mask, mask_stride, n_busy, w);
+  se_launch(zero_int_kernel, 1, 1, 0, st, w.abort);
+  se_launch(prune_plan_kernel, kv->B, 1024, 0, st, *kv, L, R, mask, mask_stride, n_busy, w);
   return launch_compact(kv, w.keep, smax, w.n_keep, w.first, smax, aux, aux_stride, w.compact_ws,
                         w.compact_bytes, w.abort, st);
 }
@@ -957,7 +970,7 @@ extern "C" se_status se_release_seqs(const se_paged_kv* kv, const int32_t* mask,
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.ctrl, 0, sizeof(CompactCtrl), st) != cudaSuccess) return SE_ERR_CUDA;
-  release_count_kernel<<<kv->B, 1024, 0, st>>>(*kv, mask, w);
-  release_apply_kernel<<<kv->B, 1024, 0, st>>>(*kv, mask, w);
+  se_launch(release_count_kernel, kv->B, 1024, 0, st, *kv, mask, w);
+  se_launch(release_apply_kernel, kv->B, 1024, 0, st, *kv, mask, w);
   return se_last_launch_status();
 }

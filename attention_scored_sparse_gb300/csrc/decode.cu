@@ -11,8 +11,11 @@
 // load), the group's G queries pre-scaled by log2(e)/sqrt(D) in registers, an
 // xor reduce-scatter of the partial dot products, one exponential per
 // (entry, head) and a base-2 online softmax.  Half-warp states merge in
-// shared memory; a second kernel merges the chunks and, for H2O, adds
-// sum_h p_{h,j} to the running scores from the logits the first kernel stored.
+// shared memory; the last chunk CTA of each (sequence, KV group) merges the
+// chunks and, for H2O, adds sum_h p_{h,j} to the running scores from the
+// logits the chunk CTAs stored.
+#include <algorithm>
+
 #include "tc_primitives.cuh"
 
 namespace se {
@@ -46,6 +49,18 @@ SE_DEV float ex2(float x) {
   return y;
 }
 
+// Work split.  The view entries of every (b, g) unit are padded to sp
+// slices of SE = 128 / G entries (one iteration of the 8 half-warps); the
+// ts = units x sp slices, in unit order, are cut into n_cta ranges, one per
+// CTA, in one of two ways:
+//   aligned (k_al > 0): each unit in k_al chunks of w_al slices (the last
+//     one shorter); a range never crosses a unit;
+//   stream (k_al == 0, "stream-K"): n_cta contiguous ranges of nearly equal
+//     length over all slices; a range that crosses a unit boundary makes one
+//     segment per unit.  Equal ranges keep every CTA busy to the end when
+//     the aligned chunks would leave a ragged last wave.
+// Every segment leaves a partial (m, l, o) that the last CTA to finish a
+// segment of the unit merges.
 struct DecodeArgs {
   se_paged_kv kv;
   const void* q;
@@ -53,16 +68,51 @@ struct DecodeArgs {
   const int32_t* sel;
   int32_t sel_stride;
   int32_t n_sel;
-  int chunk;     // view entries per CTA
-  int n_chunks;
-  float* part;   // [B][Hkv][n_chunks][G][D + 2]
-  float* logits; // [B][Hkv][max_entries][G] or null
+  int sp;          // slices per unit
+  int64_t ts;      // slices in all = units * sp
+  int n_cta;       // CTAs (ranges), 1 <= n_cta <= ts
+  int k_al;        // aligned split: chunks per unit, 0 for the stream split
+  int w_al;        // aligned split: slices per chunk
+  int max_parts;   // partial slots per unit
+  float* part;     // [units][max_parts][G][D + 2]
+  float* logits;   // [B][Hkv][max_entries][G] or null
   int max_entries;
   void* out;          // o [B][Hq][D]
   float* acc;         // H2O running scores or null
   int64_t acc_stride;
-  int32_t* done;      // [B][Hkv] chunk CTAs finished (zeroed before the launch)
+  int32_t* done;      // [units] segments finished (zeroed before the launch)
 };
+
+// Slices [start, end) of CTA c's range.
+SE_HD int64_t range_start(const DecodeArgs& a, int c) {
+  if (a.k_al > 0) {
+    const int64_t off = (int64_t)(c % a.k_al) * a.w_al;
+    return (int64_t)(c / a.k_al) * a.sp + (off < a.sp ? off : a.sp);
+  }
+  return (int64_t)c * a.ts / a.n_cta;
+}
+SE_HD int64_t range_end(const DecodeArgs& a, int c) {
+  if (a.k_al > 0) {
+    const int64_t off = (int64_t)(c % a.k_al + 1) * a.w_al;
+    return (int64_t)(c / a.k_al) * a.sp + (off < a.sp ? off : a.sp);
+  }
+  return (int64_t)(c + 1) * a.ts / a.n_cta;
+}
+// CTA whose stream range holds slice x.
+SE_HD int stream_owner(const DecodeArgs& a, int64_t x) {
+  return (int)(((x + 1) * a.n_cta - 1) / a.ts);
+}
+// The CTAs with a segment of unit u: first and count.
+SE_HD void unit_parts(const DecodeArgs& a, int u, int* first, int* n) {
+  if (a.k_al > 0) {
+    *first = u * a.k_al;
+    *n = a.k_al;
+    return;
+  }
+  const int64_t u0 = (int64_t)u * a.sp;
+  *first = stream_owner(a, u0);
+  *n = stream_owner(a, u0 + a.sp - 1) - *first + 1;
+}
 
 // Resident slot of view entry e of (b, g), or -1.
 SE_DEV int view_slot(const DecodeArgs& a, int b, int g, int e, int ctx) {
@@ -87,23 +137,24 @@ SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
   return a.n_sel;
 }
 
-// Merges the chunk partials of (b, g), writes o and updates the running
-// scores.  Run by the last chunk CTA of (b, g) to finish (128 threads).
+// Merges the n_parts partials of unit u = (b, g), writes o and updates the
+// running scores.  Run by the last CTA to finish a segment of u (128 threads).
 template <typename T, int D, int G>
-SE_DEV void merge_chunks(const DecodeArgs& a, int b, int g) {
+SE_DEV void merge_chunks(const DecodeArgs& a, int u, int n_parts) {
   __shared__ float s_M[G], s_invL[G];
   T* out = static_cast<T*>(a.out);
   float* acc = a.acc;
   const int64_t acc_stride = a.acc_stride;
   const se_paged_kv& kv = a.kv;
-  const float* part = a.part + ((int64_t)b * kv.Hkv + g) * a.n_chunks * G * (D + 2);
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+  const float* part = a.part + (int64_t)u * a.max_parts * G * (D + 2);
   if (threadIdx.x < G) {
     const int j = threadIdx.x;
     float M = -INFINITY;
-    for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, part[(c * G + j) * (D + 2) + D]);
+    for (int c = 0; c < n_parts; ++c) M = fmaxf(M, part[(c * G + j) * (D + 2) + D]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int c = 0; c < a.n_chunks; ++c) {
+      for (int c = 0; c < n_parts; ++c) {
         const float* pc = part + (c * G + j) * (D + 2);
         L = fmaf(pc[D + 1], ex2(pc[D] - M), L);
       }
@@ -116,7 +167,7 @@ SE_DEV void merge_chunks(const DecodeArgs& a, int b, int g) {
     const float M = s_M[j];
     float v = 0.f;
     if (M != -INFINITY)
-      for (int c = 0; c < a.n_chunks; ++c) {
+      for (int c = 0; c < n_parts; ++c) {
         const float* pc = part + (c * G + j) * (D + 2);
         v = fmaf(pc[d], ex2(pc[D] - M), v);
       }
@@ -126,179 +177,46 @@ SE_DEV void merge_chunks(const DecodeArgs& a, int b, int g) {
     else *op = v;
   }
   if (acc != nullptr && a.logits != nullptr) {
+    // four entries per thread per round, every load of a round issued before
+    // the first use, so a round costs one memory latency rather than four
     const int ctx = kv.ctx_len[b];
     const int n_view = min(view_entries(a, ctx), a.max_entries);
     const float* lg = a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G;
     float* ar = acc + ((int64_t)b * kv.Hkv + g) * acc_stride;
-    for (int e = threadIdx.x; e < n_view; e += blockDim.x) {
-      const int s = view_slot(a, b, g, e, ctx);
-      if (s < 0) continue;
-      float ps = 0.f;
+    constexpr int U = 4;
+    for (int e0 = threadIdx.x; e0 < n_view; e0 += U * blockDim.x) {
+      int sl[U];
+      float lv[U][G], old[U];
 #pragma unroll
-      for (int j = 0; j < G; ++j) ps += ex2(lg[(int64_t)e * G + j] - s_M[j]) * s_invL[j];
-      ar[s] += ps;
+      for (int k = 0; k < U; ++k) {
+        const int e = e0 + k * blockDim.x;
+        sl[k] = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
+#pragma unroll
+        for (int j = 0; j < G; ++j) lv[k][j] = sl[k] >= 0 ? __ldcg(lg + (int64_t)e * G + j) : 0.f;
+        old[k] = sl[k] >= 0 ? __ldcg(ar + sl[k]) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        float ps = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) ps += ex2(lv[k][j] - s_M[j]) * s_invL[j];
+        if (sl[k] >= 0) ar[sl[k]] = old[k] + ps;
+      }
     }
   }
 }
 
-// grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps.
-//
-// A half-warp takes E = 16/G consecutive view entries per iteration; lane t
-// owns dims [V t, V t + V) of K, V, q and o (V = D/16).  The E x G partial dot
-// products of a lane are reduced across the 16 lanes by a 4-step xor
-// reduce-scatter that leaves lane t with the complete logit of
-// (entry t / G, head t % G): 15 shuffles per iteration instead of 4 G per
-// entry.  Each lane then runs the base-2 online softmax for its own logit
-// (one exponential), the per-head maxima are exchanged among the lanes of a
-// head, the probabilities are all-gathered through shared memory, and every
-// lane accumulates p * v for its dims.  o is rescaled only when a head's
-// maximum grows.
+// End of a segment of unit u in CTA c: combines the 8 half-warp states
+// (s_m, s_l, s_o, written before the call and fenced by a barrier) into the
+// segment's partial, counts the segment and, in the last CTA to finish a
+// segment of u, merges u.  Ends with a barrier.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) {
-  constexpr int V = D / 16;        // dims per lane
-  constexpr int E = 16 / G;        // entries per half-warp iteration
-  static_assert(E * G == 16, "G must divide 16");
-  __shared__ float s_p[8][16];
-  __shared__ float s_m[8][G], s_l[8][G];
-  __shared__ float s_o[8][G][D];
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const se_paged_kv& kv = a.kv;
-  const int P = kv.page_size;
-  const int ctx = kv.ctx_len[b];
-  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
-  const int my_e = t / G, my_h = t % G;   // the logit this lane holds after the reduction
-  const int n_view = min(view_entries(a, ctx), a.max_entries);
-  const int e_begin = c * a.chunk;
-  const int e_end = min(e_begin + a.chunk, n_view);
-
-  const float qscale = kLog2e * rsqrtf((float)D);
-  float q[G][V];
-  const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-    load_row<T, V>(qb + (int64_t)j * D, q[j]);
-#pragma unroll
-    for (int i = 0; i < V; ++i) q[j][i] *= qscale;
-  }
-  float m[G], o[G][V];
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-    m[j] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < V; ++i) o[j][i] = 0.f;
-  }
-  float l_own = 0.f;                 // running sum of this lane's head, own entries
-  const T* kp = static_cast<const T*>(kv.k_pool);
-  const T* vp = static_cast<const T*>(kv.v_pool);
-  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-  float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
-  const unsigned full = 0xffffffffu;
-
-  for (int base = e_begin; base < e_end; base += 8 * E) {
-    const int e0 = base + hw * E;
-    float kf[E][V], vf[E][V];
-    bool valid[E];
-#pragma unroll
-    for (int u = 0; u < E; ++u) {
-      const int e = e0 + u;
-      const int slot = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
-      valid[u] = slot >= 0;
-      if (valid[u]) {
-        const int64_t off = (((int64_t)bt[slot / P] * kv.Hkv + g) * P + slot % P) * D + t * V;
-        load_row<T, V>(kp + off, kf[u]);
-        load_row<T, V>(vp + off, vf[u]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) { kf[u][i] = 0.f; vf[u][i] = 0.f; }
-      }
-    }
-    // partial dots, value index u * G + j
-    float part[16];
-#pragma unroll
-    for (int u = 0; u < E; ++u)
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[u][i], acc);
-        part[u * G + j] = acc;
-      }
-    // reduce-scatter: the lane keeps the upper half where its bit is set, so
-    // after 4 steps lane t holds value t
-#pragma unroll
-    for (int step = 0; step < 4; ++step) {
-      const int off = 8 >> step;
-      const int n = 8 >> step;
-      const bool upper = (t & off) != 0;
-#pragma unroll
-      for (int i = 0; i < n; ++i) {
-        const float lo = part[i], hi = part[i + n];
-        part[i] = (upper ? hi : lo) + __shfl_xor_sync(full, upper ? lo : hi, off);
-      }
-    }
-    bool ok = false;
-#pragma unroll
-    for (int u = 0; u < E; ++u) ok = (u == my_e) ? valid[u] : ok;
-    const float sv = ok ? part[0] : -INFINITY;
-    if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
-    // maximum of this head over the iteration's entries: lanes of one head
-    // differ in the bits above log2(G)
-    float tmax = sv;
-#pragma unroll
-    for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full, tmax, off));
-    float m_mine = m[0];             // running max of my head before this iteration
-#pragma unroll
-    for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
-    const float mn_mine = fmaxf(m_mine, tmax);
-    const float alpha_mine = (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
-    const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
-    l_own = fmaf(l_own, alpha_mine, p);
-    s_p[hw][t] = p;
-    // every lane needs every head's new maximum / rescale factor
-    bool grew = false;
-    float alpha[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const float mj = __shfl_sync(full, mn_mine, (threadIdx.x & 16) + j);
-      alpha[j] = __shfl_sync(full, alpha_mine, (threadIdx.x & 16) + j);
-      grew |= mj != m[j];
-      m[j] = mj;
-    }
-    __syncwarp();
-    if (grew) {
-#pragma unroll
-      for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int i = 0; i < V; ++i) o[j][i] *= alpha[j];
-    }
-#pragma unroll
-    for (int u = 0; u < E; ++u) {
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float pu = s_p[hw][u * G + j];
-#pragma unroll
-        for (int i = 0; i < V; ++i) o[j][i] = fmaf(pu, vf[u][i], o[j][i]);
-      }
-    }
-    __syncwarp();
-  }
-  // running sums of each head: lanes of a head add up their own entries
-  float lsum = l_own;
-#pragma unroll
-  for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full, lsum, off);
-  if (t < G) {
-    float mt = m[0];
-#pragma unroll
-    for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
-    s_m[hw][t] = mt;
-    s_l[hw][t] = lsum;
-  }
-#pragma unroll
-  for (int j = 0; j < G; ++j)
-#pragma unroll
-    for (int i = 0; i < V; ++i) s_o[hw][j][t * V + i] = o[j][i];
-  __syncthreads();
-  float* part = a.part + (((int64_t)b * kv.Hkv + g) * a.n_chunks + c) * G * (D + 2);
+SE_DEV void finish_segment(const DecodeArgs& a, int u, int c, float (*s_m)[G], float (*s_l)[G],
+                           float (*s_o)[G][D]) {
+  __shared__ int s_last;
+  int first, n_parts;
+  unit_parts(a, u, &first, &n_parts);
+  float* part = a.part + ((int64_t)u * a.max_parts + (c - first)) * G * (D + 2);
   for (int x = threadIdx.x; x < G * D; x += 128) {
     const int j = x / D, d = x % D;
     float M = -INFINITY;
@@ -319,21 +237,192 @@ __global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) 
       part[j * (D + 2) + D + 1] = L;
     }
   }
-  // the last chunk CTA of (b, g) to finish merges all chunks (no extra launch):
   // the barrier orders the CTA's partial before thread 0's device-scope fence
   // and count; the last CTA's fence orders the count before its reads
-  __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int last = atomicAdd(a.done + (int64_t)b * kv.Hkv + g, 1) == a.n_chunks - 1;
+    const int last = atomicAdd(a.done + u, 1) == n_parts - 1;
     if (last) __threadfence();
     s_last = last;
   }
   __syncthreads();
-  if (s_last) merge_chunks<T, D, G>(a, b, g);
+  if (s_last) merge_chunks<T, D, G>(a, u, n_parts);
+  __syncthreads();
 }
 
+// grid: n_cta; 128 threads = 8 half-warps.  Fallback for shapes whose stages
+// do not fit shared memory: K and V rows are loaded straight into registers.
+//
+// A half-warp takes E = 16/G consecutive view entries per iteration; lane t
+// owns dims [V t, V t + V) of K, V, q and o (V = D/16).  The E x G partial dot
+// products of a lane are reduced across the 16 lanes by a 4-step xor
+// reduce-scatter that leaves lane t with the complete logit of
+// (entry t / G, head t % G): 15 shuffles per iteration instead of 4 G per
+// entry.  Each lane then runs the base-2 online softmax for its own logit
+// (one exponential), the per-head maxima are exchanged among the lanes of a
+// head, the probabilities are all-gathered through shared memory, and every
+// lane accumulates p * v for its dims.  o is rescaled only when a head's
+// maximum grows.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) {
+  pdl_enter();
+  constexpr int V = D / 16;        // dims per lane
+  constexpr int E = 16 / G;        // entries per half-warp iteration
+  constexpr int SE = 8 * E;        // entries per slice
+  static_assert(E * G == 16, "G must divide 16");
+  __shared__ float s_p[8][16];
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ float s_o[8][G][D];
+  const int c = blockIdx.x;
+  const se_paged_kv& kv = a.kv;
+  const int P = kv.page_size;
+  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int my_e = t / G, my_h = t % G;   // the logit this lane holds after the reduction
+  const float qscale = kLog2e * rsqrtf((float)D);
+  const T* kp = static_cast<const T*>(kv.k_pool);
+  const T* vp = static_cast<const T*>(kv.v_pool);
+  const unsigned full = 0xffffffffu;
+  const int64_t x0 = range_start(a, c), x1 = range_end(a, c);
+
+  for (int64_t xs = x0; xs < x1;) {
+    const int u = (int)(xs / a.sp);
+    const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
+    const int b = u / kv.Hkv, g = u % kv.Hkv;
+    const int ctx = kv.ctx_len[b];
+    const int n_view = min(view_entries(a, ctx), a.max_entries);
+    const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
+    const int e_end = min((int)(xe - (int64_t)u * a.sp) * SE, n_view);
+
+    float q[G][V];
+    const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+      for (int i = 0; i < V; ++i) q[j][i] *= qscale;
+    }
+    float m[G], o[G][V];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < V; ++i) o[j][i] = 0.f;
+    }
+    float l_own = 0.f;                 // running sum of this lane's head, own entries
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    float* lg = a.logits ? a.logits + (int64_t)u * a.max_entries * G : nullptr;
+
+    for (int base = e_begin; base < e_end; base += SE) {
+      const int e0 = base + hw * E;
+      float kf[E][V], vf[E][V];
+      bool valid[E];
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) {
+        const int e = e0 + uu;
+        const int slot = e < e_end ? view_slot(a, b, g, e, ctx) : -1;
+        const int page = slot >= 0 ? bt[slot / P] : -1;
+        valid[uu] = page >= 0 && page < kv.num_pages;
+        if (valid[uu]) {
+          const int64_t off = (((int64_t)page * kv.Hkv + g) * P + slot % P) * D + t * V;
+          load_row<T, V>(kp + off, kf[uu]);
+          load_row<T, V>(vp + off, vf[uu]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) { kf[uu][i] = 0.f; vf[uu][i] = 0.f; }
+        }
+      }
+      // partial dots, value index uu * G + j
+      float part[16];
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu)
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc = fmaf(q[j][i], kf[uu][i], acc);
+          part[uu * G + j] = acc;
+        }
+      // reduce-scatter: the lane keeps the upper half where its bit is set, so
+      // after 4 steps lane t holds value t
+#pragma unroll
+      for (int step = 0; step < 4; ++step) {
+        const int off = 8 >> step;
+        const int n = 8 >> step;
+        const bool upper = (t & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float lo = part[i], hi = part[i + n];
+          part[i] = (upper ? hi : lo) + __shfl_xor_sync(full, upper ? lo : hi, off);
+        }
+      }
+      bool ok = false;
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) ok = (uu == my_e) ? valid[uu] : ok;
+      const float sv = ok ? part[0] : -INFINITY;
+      if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+      // maximum of this head over the iteration's entries: lanes of one head
+      // differ in the bits above log2(G)
+      float tmax = sv;
+#pragma unroll
+      for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full, tmax, off));
+      float m_mine = m[0];             // running max of my head before this iteration
+#pragma unroll
+      for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+      const float mn_mine = fmaxf(m_mine, tmax);
+      const float alpha_mine =
+          (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+      const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+      l_own = fmaf(l_own, alpha_mine, p);
+      s_p[hw][t] = p;
+      // every lane needs every head's new maximum / rescale factor
+      bool grew = false;
+      float alpha[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float mj = __shfl_sync(full, mn_mine, (threadIdx.x & 16) + j);
+        alpha[j] = __shfl_sync(full, alpha_mine, (threadIdx.x & 16) + j);
+        grew |= mj != m[j];
+        m[j] = mj;
+      }
+      __syncwarp();
+      if (grew) {
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+          for (int i = 0; i < V; ++i) o[j][i] *= alpha[j];
+      }
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pu = s_p[hw][uu * G + j];
+#pragma unroll
+          for (int i = 0; i < V; ++i) o[j][i] = fmaf(pu, vf[uu][i], o[j][i]);
+        }
+      }
+      __syncwarp();
+    }
+    // running sums of each head: lanes of a head add up their own entries
+    float lsum = l_own;
+#pragma unroll
+    for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full, lsum, off);
+    if (t < G) {
+      float mt = m[0];
+#pragma unroll
+      for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+      s_m[hw][t] = mt;
+      s_l[hw][t] = lsum;
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i) s_o[hw][j][t * V + i] = o[j][i];
+    __syncthreads();
+    finish_segment<T, D, G>(a, u, c, s_m, s_l, s_o);
+    xs = xe;
+  }
+}
 
 // Bulk copy global -> shared (the TMA engine, no tensor map), completing on
 // an mbarrier; the byte count is added to the barrier's expected total first.
@@ -357,7 +446,7 @@ SE_DEV void load_row_smem(const T* r, float* f) {
   }
 }
 
-constexpr int kMaxChunk = 1024;   // view entries per CTA at most (see pick_chunk)
+constexpr int kMaxChunk = 1024;   // view entries per CTA at most (see make_split)
 
 template <typename T, int D, int G>
 struct StagedGeom {
@@ -369,30 +458,33 @@ struct StagedGeom {
   // three 16 KB stages keep four CTAs (sixteen warps) on an SM with 127 registers a thread
   static constexpr int STAGES =
       STAGE_BYTES <= 8192 ? 4 : (STAGE_BYTES <= 16384 ? 3 : (STAGE_BYTES <= 32768 ? 2 : 0));
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 128;   // + alignment of the stages to 128 B
+  // CTAs an SM holds by shared memory (about 6 KB static besides SMEM),
+  // at most four; eight heads a group take two (their q and o fill the
+  // registers)
+  static constexpr int MIN_CTAS =
+      G >= 8 ? 2 : ((227 * 1024) / (SMEM + 6 * 1024) >= 4 ? 4 : 3);
 };
 
-// Issues the copies of one stage (chunk entries [s0, s0 + SE)) of (b, g);
-// called by all 32 lanes of one warp.  rows[x] is the pool row (page * P +
-// row in page) of chunk entry x, -1 for none, resolved once per CTA.  A
-// maximal run of entries that are consecutive rows of one page becomes one K
-// and one V copy, issued by the lane that starts it.  valid[u] records
-// whether entry u has a row (read by the consumers after the stage's barrier
-// completes).  Lane 0 arrives on the barrier last.
+// Issues the copies of one stage (segment entries [s0, s0 + SE)); called by
+// all 32 lanes of one warp.  rows[x] is the K/V row of segment entry x in the
+// pool ((page * Hkv + g) * P + row in page), -1 for none, resolved once per
+// CTA.  A maximal run of entries that are consecutive rows of one page
+// becomes one K and one V copy, issued by the lane that starts it.  valid[u]
+// records whether entry u has a row (read by the consumers after the stage's
+// barrier completes).  Lane 0 arrives on the barrier last.
 template <typename T, int D, int G>
-SE_DEV void issue_stage(const DecodeArgs& a, int g, int s0, int n_chunk, const int32_t* rows,
-                        uint8_t* dst, uint64_t* bar, int8_t* valid, int lane) {
+SE_DEV void issue_stage(const DecodeArgs& a, int s0, int n_seg, const int32_t* rows, uint8_t* dst,
+                        uint64_t* bar, int8_t* valid, int lane) {
   using Gm = StagedGeom<T, D, G>;
-  const se_paged_kv& kv = a.kv;
-  const int P = kv.page_size;
-  const char* kp = static_cast<const char*>(kv.k_pool);
-  const char* vp = static_cast<const char*>(kv.v_pool);
-  uint32_t n_valid = 0;
+  const int P = a.kv.page_size;
+  const char* kp = static_cast<const char*>(a.kv.k_pool);
+  const char* vp = static_cast<const char*>(a.kv.v_pool);
 #pragma unroll
   for (int u0 = 0; u0 < Gm::SE; u0 += 32) {
     const int u = u0 + lane;
     const int x = s0 + u;
-    const int prow = (u < Gm::SE && x < n_chunk) ? rows[x] : -1;
+    const int prow = (u < Gm::SE && x < n_seg) ? rows[x] : -1;
     const bool ok = prow >= 0;
     if (u < Gm::SE) valid[u] = ok ? 1 : 0;
     // a run continues when this entry is the next row of the previous one's page
@@ -400,52 +492,51 @@ SE_DEV void issue_stage(const DecodeArgs& a, int g, int s0, int n_chunk, const i
     const bool cont = ok && lane > 0 && prev >= 0 && prev + 1 == prow && prow % P != 0;
     const uint32_t okm = __ballot_sync(0xffffffffu, ok);
     const uint32_t starts = __ballot_sync(0xffffffffu, ok && !cont);
-    n_valid += __popc(okm);
     if (ok && !cont) {
       const uint32_t above = lane == 31 ? 0u : (~0u << (lane + 1));
       const uint32_t stop = (starts | ~okm) & above;
       const int end = stop ? __ffs(stop) - 1 : 32;
       const int len = end - lane;
-      const int64_t off = (((int64_t)(prow / P) * kv.Hkv + g) * P + prow % P) * Gm::RB;
+      const int64_t off = (int64_t)prow * Gm::RB;
       bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
       bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
     }
   }
   __syncwarp();
   if (lane == 0) tc::mbar_arrive(bar);
-  (void)n_valid;
 }
 
-// grid: (n_chunks, Hkv, B); 128 threads = 8 half-warps; dynamic smem
-// StagedGeom::SMEM.  Lane 0 of warp 0 keeps STAGES-1 stages of copies in
-// flight; every half-warp reads its E rows of each stage from shared memory
-// (16 lanes x 16 bytes = one 256-byte row, conflict-free) and runs the same
-// reduce-scatter / online-softmax arithmetic as the register kernel above.
+// grid: n_cta; 128 threads = 8 half-warps; dynamic smem StagedGeom::SMEM.
+// Warp 0 keeps STAGES-1 stages of copies in flight within a segment; every
+// half-warp reads its E rows of each stage from shared memory (16 lanes x 16
+// bytes = one 256-byte row, conflict-free) and runs the same reduce-scatter /
+// online-softmax arithmetic as the register kernel above.  Stage buffers and
+// barrier phases follow a count of the stages the CTA has issued, so they
+// carry over from one segment to the next; at a segment's end the stages are
+// idle and hold the half-warp states while they are combined.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_partial_kernel(DecodeArgs a) {
+  pdl_enter();
   using Gm = StagedGeom<T, D, G>;
   constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[4], empty[4];
   __shared__ int8_t s_valid[4][SE];
-  __shared__ int32_t s_rows[kMaxChunk];   // pool row of each chunk entry, -1 for none
+  __shared__ int32_t s_rows[kMaxChunk];   // K/V row of each entry of the CTA's range, -1 for none
   __shared__ float s_p[8][16];
   __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ int s_nseg[kMaxChunk / SE];   // viewed entries of each segment of the range
   __shared__ int s_abort;
   static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int c = blockIdx.x;
   const se_paged_kv& kv = a.kv;
-  const int ctx = kv.ctx_len[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
   const int my_e = t / G, my_h = t % G;
-  const int n_view = min(view_entries(a, ctx), a.max_entries);
-  const int e_begin = c * a.chunk;
-  const int e_end = min(e_begin + a.chunk, n_view);
-  const int n_it = e_end > e_begin ? cdiv(e_end - e_begin, SE) : 0;
   const unsigned full_mask = 0xffffffffu;
   constexpr uint64_t kLimit = 2000000000ull;
+  const int64_t x0 = range_start(a, c), x1 = range_end(a, c);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -455,232 +546,245 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
     }
     tc::fence_barrier_init();
   }
-  // resolve every entry of the chunk to its pool row once (view -> slot ->
-  // block table), so the stage producer only reads shared memory
-  const int n_chunk = max(e_end - e_begin, 0);
-  {
-    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  // resolve every entry of the range to its K/V row once (view -> slot ->
+  // block table), segment by segment, so the stage producer only reads
+  // shared memory; s_nseg keeps each segment's count of viewed entries
+  for (int64_t xs = x0, k = 0; xs < x1; ++k) {
+    const int u = (int)(xs / a.sp);
+    const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
+    const int b = u / kv.Hkv, g = u % kv.Hkv;
     const int P = kv.page_size;
-    for (int x = threadIdx.x; x < n_chunk; x += blockDim.x) {
-      const int slot = view_slot(a, b, g, e_begin + x, ctx);
+    const int ctx = kv.ctx_len[b];
+    const int n_view = min(view_entries(a, ctx), a.max_entries);
+    const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
+    const int n_all = (int)(xe - xs) * SE;
+    if (threadIdx.x == 0) s_nseg[k] = max(min(e_begin + n_all, n_view) - e_begin, 0);
+    int32_t* rows = s_rows + (int)(xs - x0) * SE;
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    for (int x = threadIdx.x; x < n_all; x += blockDim.x) {
+      const int e = e_begin + x;
+      const int slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
       const int page = slot >= 0 ? bt[slot / P] : -1;
-      s_rows[x] = (page >= 0 && page < kv.num_pages) ? page * P + slot % P : -1;
+      rows[x] = (page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
     }
+    xs = xe;
   }
   __syncthreads();
   const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
-  if (producer)
-    for (int i = 0; i < min(S - 1, n_it); ++i)
-      issue_stage<T, D, G>(a, g, i * SE, n_chunk, s_rows, stages + i * Gm::STAGE_BYTES,
-                           &full[i], s_valid[i], lane);
-
   const float qscale = kLog2e * rsqrtf((float)D);
-  float q[G][V];
-  const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-    load_row<T, V>(qb + (int64_t)j * D, q[j]);
-#pragma unroll
-    for (int i = 0; i < V; ++i) q[j][i] *= qscale;
-  }
-  // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
   constexpr int V2 = V / 2;
-  uint64_t q2[G][V2], o2[G][V2];
-  float m[G];
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-    m[j] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < V2; ++i) {
-      q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
-      o2[j][i] = 0;
-    }
-  }
-  float l_own = 0.f;
-  float* lg = a.logits ? a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G : nullptr;
-  int issued = min(S - 1, n_it);
+  int gi = 0;   // stages issued by this CTA (stage n uses buffer n % S)
+  int gc = 0;   // stages consumed
 
-  for (int it = 0; it < n_it; ++it) {
-    const int s = it % S;
-    if (producer && issued < n_it) {
-      // refill the stage consumed in the previous iteration
-      const int ps = issued % S;
-      const bool free_ok = issued < S || tc::mbar_wait(&empty[ps], ((issued / S) - 1) & 1, kLimit);
-      if (__all_sync(full_mask, free_ok)) {
-        issue_stage<T, D, G>(a, g, issued * SE, n_chunk, s_rows, stages + ps * Gm::STAGE_BYTES,
-                             &full[ps], s_valid[ps], lane);
-        ++issued;
-      } else if (lane == 0) {
-        set_status(kv.status, SE_ERR_TIMEOUT);
-        atomicExch(&s_abort, 1);
+  for (int64_t xs = x0, k = 0; xs < x1; ++k) {
+    const int u = (int)(xs / a.sp);
+    const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
+    const int b = u / kv.Hkv, g = u % kv.Hkv;
+    const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
+    const int n_seg = s_nseg[k];
+    const int n_it = cdiv(n_seg, SE);
+    const int32_t* rows = s_rows + (int)(xs - x0) * SE;
+    const int g0 = gi;   // stage count at the segment's start
+
+    // the first STAGES-1 stages; a buffer last used by an earlier segment is
+    // refilled only after its consumers have released it
+    if (producer) {
+      for (int i = 0; i < min(S - 1, n_it); ++i) {
+        const int n = g0 + i;
+        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
+        if (!__all_sync(full_mask, free_ok)) {
+          if (lane == 0) {
+            set_status(kv.status, SE_ERR_TIMEOUT);
+            atomicExch(&s_abort, 1);
+          }
+          break;
+        }
+        issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                             &full[n % S], s_valid[n % S], lane);
+        ++gi;
       }
     }
-    const bool ok_wait = tc::mbar_wait(&full[s], (it / S) & 1, kLimit);
-    if (!__all_sync(full_mask, ok_wait)) {
-      if (lane == 0) {
-        set_status(kv.status, SE_ERR_TIMEOUT);
-        atomicExch(&s_abort, 1);
-      }
-      break;
-    }
-    const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
-    const uint8_t* vst = kst + SE * RB;
-    const int e0 = e_begin + it * SE + hw * E;
-    // K rows are read from the stage one entry at a time; V rows are read
-    // again after the probabilities are known (the stage is released after)
-    bool valid[E];
-    float part[16];
-#pragma unroll
-    for (int u = 0; u < E; ++u) {
-      valid[u] = s_valid[s][hw * E + u] != 0;
-      float kf[V];
-      if (valid[u]) {
-        load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + u) * RB) + t * V, kf);
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) kf[i] = 0.f;
-      }
-      uint64_t k2[V2];
-#pragma unroll
-      for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        uint64_t acc2 = 0;
-#pragma unroll
-        for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
-        float lo, hi;
-        tc::f2split(acc2, lo, hi);
-        part[u * G + j] = lo + hi;
-      }
-    }
-#pragma unroll
-    for (int step = 0; step < 4; ++step) {
-      const int off = 8 >> step;
-      const int n = 8 >> step;
-      const bool upper = (t & off) != 0;
-#pragma unroll
-      for (int i = 0; i < n; ++i) {
-        const float lo = part[i], hi = part[i + n];
-        part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
-      }
-    }
-    bool ok = false;
-#pragma unroll
-    for (int u = 0; u < E; ++u) ok = (u == my_e) ? valid[u] : ok;
-    const float sv = ok ? part[0] : -INFINITY;
-    if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
-    float tmax = sv;
-#pragma unroll
-    for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
-    float m_mine = m[0];
-#pragma unroll
-    for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
-    const float mn_mine = fmaxf(m_mine, tmax);
-    const float alpha_mine = (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
-    const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
-    l_own = fmaf(l_own, alpha_mine, p);
-    s_p[hw][t] = p;
-    bool grew = false;
-    float alpha[G];
+
+    float q[G][V];
+    const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-      const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
-      alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
-      grew |= mj != m[j];
-      m[j] = mj;
+      load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+      for (int i = 0; i < V; ++i) q[j][i] *= qscale;
     }
-    __syncwarp();
-    if (grew) {
+    // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
+    uint64_t q2[G][V2], o2[G][V2];
+    float m[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < V2; ++i) {
+        q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
+        o2[j][i] = 0;
+      }
+    }
+    float l_own = 0.f;
+    float* lg = a.logits ? a.logits + (int64_t)u * a.max_entries * G : nullptr;
+
+    for (int it = 0; it < n_it; ++it) {
+      if (producer && gi - g0 < n_it) {
+        // refill the buffer consumed in the previous iteration
+        const int n = gi;
+        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
+        if (__all_sync(full_mask, free_ok)) {
+          issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                               &full[n % S], s_valid[n % S], lane);
+          ++gi;
+        } else if (lane == 0) {
+          set_status(kv.status, SE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+      }
+      const int s = gc % S;
+      const bool ok_wait = tc::mbar_wait(&full[s], (gc / S) & 1, kLimit);
+      if (!__all_sync(full_mask, ok_wait)) {
+        if (lane == 0) {
+          set_status(kv.status, SE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
+      const uint8_t* vst = kst + SE * RB;
+      const int e0 = e_begin + it * SE + hw * E;
+      // K rows are read from the stage one entry at a time; V rows are read
+      // again after the probabilities are known (the stage is released after)
+      bool valid[E];
+      float part[16];
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) {
+        valid[uu] = s_valid[s][hw * E + uu] != 0;
+        float kf[V];
+        if (valid[uu]) {
+          load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + uu) * RB) + t * V, kf);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) kf[i] = 0.f;
+        }
+        uint64_t k2[V2];
+#pragma unroll
+        for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          uint64_t acc2 = 0;
+#pragma unroll
+          for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
+          float lo, hi;
+          tc::f2split(acc2, lo, hi);
+          part[uu * G + j] = lo + hi;
+        }
+      }
+#pragma unroll
+      for (int step = 0; step < 4; ++step) {
+        const int off = 8 >> step;
+        const int n = 8 >> step;
+        const bool upper = (t & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float lo = part[i], hi = part[i + n];
+          part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
+        }
+      }
+      bool ok = false;
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) ok = (uu == my_e) ? valid[uu] : ok;
+      const float sv = ok ? part[0] : -INFINITY;
+      if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+      float tmax = sv;
+#pragma unroll
+      for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
+      float m_mine = m[0];
+#pragma unroll
+      for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+      const float mn_mine = fmaxf(m_mine, tmax);
+      const float alpha_mine =
+          (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+      const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+      l_own = fmaf(l_own, alpha_mine, p);
+      s_p[hw][t] = p;
+      bool grew = false;
+      float alpha[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
-#pragma unroll
-        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
+        const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
+        alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
+        grew |= mj != m[j];
+        m[j] = mj;
       }
-    }
+      __syncwarp();
+      if (grew) {
 #pragma unroll
-    for (int u = 0; u < E; ++u) {
-      float vf[V];
-      if (valid[u]) {
-        load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + u) * RB) + t * V, vf);
-      } else {
+        for (int j = 0; j < G; ++j) {
+          const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
 #pragma unroll
-        for (int i = 0; i < V; ++i) vf[i] = 0.f;
+          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
+        }
       }
-      uint64_t v2[V2];
 #pragma unroll
-      for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
+      for (int uu = 0; uu < E; ++uu) {
+        float vf[V];
+        if (valid[uu]) {
+          load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + uu) * RB) + t * V, vf);
+        } else {
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float pu = s_p[hw][u * G + j];
-        const uint64_t p2 = tc::f2(pu, pu);
+          for (int i = 0; i < V; ++i) vf[i] = 0.f;
+        }
+        uint64_t v2[V2];
 #pragma unroll
-        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
+        for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pu = s_p[hw][uu * G + j];
+          const uint64_t p2 = tc::f2(pu, pu);
+#pragma unroll
+          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
+        }
       }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with this stage's rows
+      ++gc;
     }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with this stage's rows
-  }
-  // drain: after a timeout, copies of the last stages may still be in flight
-  // (each earlier stage was waited on before its buffer was refilled)
-  if (producer && lane == 0)
-    for (int i = max(0, issued - S); i < issued; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
-  float lsum = l_own;
+    // drain: after a timeout, copies of the last stages may still be in flight
+    // (each earlier stage was waited on before its buffer was refilled)
+    if (producer && lane == 0)
+      for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
+    float lsum = l_own;
 #pragma unroll
-  for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
-  if (t < G) {
-    float mt = m[0];
+    for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
+    if (t < G) {
+      float mt = m[0];
 #pragma unroll
-    for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
-    s_m[hw][t] = mt;
-    s_l[hw][t] = lsum;
-  }
-  __syncthreads();   // every stage has been read: reuse the stage memory
-  float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
-#pragma unroll
-  for (int j = 0; j < G; ++j)
-#pragma unroll
-    for (int i = 0; i < V2; ++i) {
-      float lo, hi;
-      tc::f2split(o2[j][i], lo, hi);
-      s_o[hw][j][t * V + 2 * i] = lo;
-      s_o[hw][j][t * V + 2 * i + 1] = hi;
+      for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+      s_m[hw][t] = mt;
+      s_l[hw][t] = lsum;
     }
-  __syncthreads();
-  float* part = a.part + (((int64_t)b * kv.Hkv + g) * a.n_chunks + c) * G * (D + 2);
-  for (int x = threadIdx.x; x < G * D; x += 128) {
-    const int j = x / D, d = x % D;
-    float M = -INFINITY;
+    __syncthreads();   // every stage of the segment has been read: reuse the stage memory
+    float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w][j]);
-    float acc = 0.f, L = 0.f;
-    if (M != -INFINITY) {
+    for (int j = 0; j < G; ++j)
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float f = ex2(s_m[w][j] - M);
-        acc = fmaf(s_o[w][j][d], f, acc);
-        L = fmaf(s_l[w][j], f, L);
+      for (int i = 0; i < V2; ++i) {
+        float lo, hi;
+        tc::f2split(o2[j][i], lo, hi);
+        s_o[hw][j][t * V + 2 * i] = lo;
+        s_o[hw][j][t * V + 2 * i + 1] = hi;
       }
-    }
-    part[j * (D + 2) + d] = acc;
-    if (d == 0) {
-      part[j * (D + 2) + D] = M;
-      part[j * (D + 2) + D + 1] = L;
-    }
+    __syncthreads();
+    finish_segment<T, D, G>(a, u, c, s_m, s_l, s_o);
+    // the stage memory was written and read as plain shared memory; order
+    // that before the next segment's copies into it
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (s_abort) break;
+    xs = xe;
   }
-  // the last chunk CTA of (b, g) to finish merges all chunks (no extra launch):
-  // the barrier orders the CTA's partial before thread 0's device-scope fence
-  // and count; the last CTA's fence orders the count before its reads
-  __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int last = atomicAdd(a.done + (int64_t)b * kv.Hkv + g, 1) == a.n_chunks - 1;
-    if (last) __threadfence();
-    s_last = last;
-  }
-  __syncthreads();
-  if (s_last) merge_chunks<T, D, G>(a, b, g);
 }
 
 struct DecodeWs {
@@ -689,34 +793,72 @@ struct DecodeWs {
   int32_t* done;
 };
 
-static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, int n_chunks, void* ws,
-                             size_t* bytes) {
-  WsCarver c(ws);
-  DecodeWs w;
-  const int G = kv->Hq / kv->Hkv;
-  w.part = c.take<float>((size_t)kv->B * kv->Hkv * n_chunks * G * (kv->D + 2));
-  w.logits = c.take<float>((size_t)kv->B * kv->Hkv * max_entries * G);
-  w.done = c.take<int32_t>((size_t)kv->B * kv->Hkv);
-  *bytes = c.bytes();
-  return w;
+struct DecodeSplit {
+  int sp;          // slices per unit
+  int64_t ts;      // slices in all
+  int n_cta;
+  int k_al, w_al;  // aligned split (k_al = 0: stream split)
+  int max_parts;   // partial slots per unit
+};
+
+// CTA slots of the staged kernel on GB300: 152 SMs x 4 resident CTAs.
+constexpr int kCtaSlots = 152 * 4;
+
+// Aligned chunks: about four CTAs per SM, at least 128 entries (64 KB of
+// bf16 K/V at d = 128) per CTA so that set-up and the partial write stay
+// small next to the stream, at most kMaxChunk, evened out over the unit.
+// They are used when all of them run at once or when they make four waves or
+// more (a ragged last wave costs little then); otherwise the stream split
+// cuts the slices into whole waves of ranges, again of at most kMaxChunk and
+// at least 128 entries.  Depends on the shape only (the workspace size does).
+static DecodeSplit make_split(const se_paged_kv* kv, int max_entries) {
+  const int G = max(kv->Hq / max(kv->Hkv, 1), 1);
+  const int SE = max(128 / G, 1);
+  const int64_t units = std::max<int64_t>((int64_t)kv->B * kv->Hkv, 1);
+  const int me = max(max_entries, 1);
+  DecodeSplit d;
+  d.sp = cdiv(me, SE);
+  d.ts = units * d.sp;
+  int chunk = kMaxChunk;
+  while (chunk > 128 && units * cdiv(me, chunk) < kCtaSlots) chunk >>= 1;
+  chunk = min(chunk, cdiv(cdiv(me, cdiv(me, chunk)), 128) * 128);
+  const int w = max(chunk / SE, 1);
+  const int k = cdiv(d.sp, w);
+  const int64_t n_al = units * k;
+  if (n_al <= kCtaSlots || n_al >= 4 * kCtaSlots) {
+    d.n_cta = (int)n_al;
+    d.k_al = k;
+    d.w_al = w;
+    d.max_parts = k;
+    return d;
+  }
+  const int w_max = max(kMaxChunk / SE, 1), w_min = max(128 / SE, 1);
+  int64_t n = cdiv64(cdiv64(d.ts, w_max), kCtaSlots) * kCtaSlots;
+  if (d.ts / n < w_min) n = std::max<int64_t>(1, d.ts / w_min);
+  d.n_cta = (int)n;
+  d.k_al = 0;
+  d.w_al = 0;
+  d.max_parts = (int)cdiv64(d.sp, d.ts / n) + 1;
+  return d;
 }
 
-// Entries per CTA: about four CTAs per SM of the 152, at least 128 entries
-// (64 KB of K/V) per CTA so that per-CTA set-up and the partial write stay
-// small next to the stream, at most 1024.
-static int pick_chunk(const se_paged_kv* kv, int max_entries) {
-  const int64_t units = (int64_t)kv->B * kv->Hkv;
-  int chunk = 1024;
-  while (chunk > 128 && units * cdiv(max_entries, chunk) < 152 * 4) chunk >>= 1;
-  // same number of chunks, evened out (multiples of 128 entries)
-  const int n = cdiv(max(max_entries, 1), chunk);
-  return min(chunk, cdiv(cdiv(max(max_entries, 1), n), 128) * 128);
+static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, const DecodeSplit& sp,
+                             void* ws, size_t* bytes) {
+  WsCarver c(ws);
+  DecodeWs w;
+  const int G = max(kv->Hq / max(kv->Hkv, 1), 1);
+  const size_t units = (size_t)kv->B * kv->Hkv;
+  w.part = c.take<float>(units * sp.max_parts * G * (kv->D + 2));
+  w.logits = c.take<float>(units * max_entries * G);
+  w.done = c.take<int32_t>(units);
+  *bytes = c.bytes();
+  return w;
 }
 
 template <typename T, int D, int G>
 static void launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   using Gm = StagedGeom<T, D, G>;
-  const dim3 grid(a.n_chunks, a.kv.Hkv, a.kv.B);
+  const dim3 grid(a.n_cta);
   bool staged = Gm::STAGES > 0;
   if constexpr (Gm::STAGES > 0) {
     static bool attr = false;
@@ -726,9 +868,9 @@ static void launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
                                   Gm::SMEM) == cudaSuccess;
       staged = attr;
     }
-    if (staged) decode_partial_kernel<T, D, G><<<grid, 128, Gm::SMEM, st>>>(a);
+    if (staged) se_launch(decode_partial_kernel<T, D, G>, grid, 128, Gm::SMEM, st, a);
   }
-  if (!staged) decode_partial_regs_kernel<T, D, G><<<grid, 128, 0, st>>>(a);
+  if (!staged) se_launch(decode_partial_regs_kernel<T, D, G>, grid, 128, 0, st, a);
 }
 
 template <typename T, int D>
@@ -748,9 +890,8 @@ using namespace se;
 
 extern "C" size_t se_sparse_decode_attn_workspace_size(const se_paged_kv* kv, int32_t max_entries) {
   if (kv == nullptr || max_entries < 0) return 0;
-  const int chunk = pick_chunk(kv, max_entries);
   size_t b = 0;
-  carve_decode(kv, max_entries, cdiv(max(max_entries, 1), chunk), nullptr, &b);
+  carve_decode(kv, max_entries, make_split(kv, max_entries), nullptr, &b);
   return b;
 }
 
@@ -765,14 +906,19 @@ extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q,
   if (view != SE_VIEW_DENSE && (sel == nullptr || n_sel < 0 || sel_stride < n_sel))
     return SE_ERR_INVALID_ARG;
   if (view < SE_VIEW_DENSE || view > SE_VIEW_TOKENS) return SE_ERR_INVALID_ARG;
-  const int chunk = pick_chunk(kv, max_entries);
-  const int n_chunks = cdiv(max_entries, chunk);
-  size_t need = 0;
-  DecodeWs w = carve_decode(kv, max_entries, n_chunks, workspace, &need);
-  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
-  DecodeArgs a{*kv, q, view, sel, sel_stride, n_sel, chunk, n_chunks, w.part,
-               acc_scores ? w.logits : nullptr, max_entries, o, acc_scores, acc_stride, w.done};
   const int G = kv->Hq / kv->Hkv;
+  // K/V rows of the pool are indexed with 32-bit integers in the kernels
+  if ((int64_t)kv->num_pages * kv->Hkv * kv->page_size > INT32_MAX) return SE_ERR_UNSUPPORTED;
+  const DecodeSplit sp = make_split(kv, max_entries);
+  if ((sp.k_al > 0 ? sp.w_al : cdiv64(sp.ts, sp.n_cta)) * (128 / G) > kMaxChunk)
+    return SE_ERR_UNSUPPORTED;
+  size_t need = 0;
+  DecodeWs w = carve_decode(kv, max_entries, sp, workspace, &need);
+  if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
+  DecodeArgs a{*kv, q, view, sel, sel_stride, n_sel, sp.sp, sp.ts, sp.n_cta, sp.k_al, sp.w_al,
+               sp.max_parts,
+               w.part, acc_scores ? w.logits : nullptr, max_entries, o, acc_scores, acc_stride,
+               w.done};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.done, 0, sizeof(int32_t) * kv->B * kv->Hkv, st) != cudaSuccess)
     return SE_ERR_CUDA;

@@ -24,6 +24,7 @@ se_status launch_topk_select_pages(int B, int Hkv, const float* U, int64_t strid
 // grid: (blocks of a sequence, B); threads: Hkv * (row_bytes/16) <= 1024
 template <typename T>
 __global__ void quest_meta_kernel(se_paged_kv kv, T* kmin, T* kmax) {
+  pdl_enter();
   const int blk = blockIdx.x, b = blockIdx.y;
   const int P = kv.page_size;
   const int ctx = kv.ctx_len[b];
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
                                                                const __nv_bfloat16* __restrict__ q,
                                                                float* __restrict__ U,
                                                                int64_t u_stride) {
+  pdl_enter();
   const int g = blockIdx.y, b = blockIdx.z;
   const int P = kv.page_size;
   const int nb = cdiv(kv.ctx_len[b], P);
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
 template <typename T>
 __global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const T* kmax,
                                            const T* q, float* U, int64_t u_stride) {
+  pdl_enter();
   const int g = blockIdx.y, b = blockIdx.z;
   const int blk = blockIdx.x * blockDim.x + threadIdx.x;
   const int nb = cdiv(kv.ctx_len[b], kv.page_size);
@@ -161,6 +164,7 @@ __global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const 
 __global__ void quest_ranges_kernel(const int32_t* ctx_len, int B, int P, int max_blocks,
                                     int32_t* status, int32_t* cand_lo, int32_t* cand_hi,
                                     int32_t* flo, int32_t* fhi) {
+  pdl_enter();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   int nb = cdiv(ctx_len[b], P);
@@ -210,10 +214,10 @@ extern "C" se_status se_quest_build_meta(const se_paged_kv* kv, void* kmin, void
   if (threads > 1024) return SE_ERR_UNSUPPORTED;
   dim3 grid(kv->max_pages_per_seq, kv->B);
   if (kv->dtype == SE_BF16)
-    quest_meta_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+    se_launch(quest_meta_kernel<__nv_bfloat16>, grid, threads, 0, st,
         *kv, static_cast<__nv_bfloat16*>(kmin), static_cast<__nv_bfloat16*>(kmax));
   else
-    quest_meta_kernel<float><<<grid, threads, 0, st>>>(*kv, static_cast<float*>(kmin),
+    se_launch(quest_meta_kernel<float>, grid, threads, 0, st, *kv, static_cast<float*>(kmin),
                                                        static_cast<float*>(kmax));
   return se_last_launch_status();
 }
@@ -246,22 +250,22 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
     auto km = static_cast<const __nv_bfloat16*>(kmin);
     auto kx = static_cast<const __nv_bfloat16*>(kmax);
     auto qq = static_cast<const __nv_bfloat16*>(q);
-    if (G == 1) quest_bound_bf16_kernel<1><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 2) quest_bound_bf16_kernel<2><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 4) quest_bound_bf16_kernel<4><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 8) quest_bound_bf16_kernel<8><<<grid, 256, 0, st>>>(*kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 1) se_launch(quest_bound_bf16_kernel<1>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 2) se_launch(quest_bound_bf16_kernel<2>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 4) se_launch(quest_bound_bf16_kernel<4>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 8) se_launch(quest_bound_bf16_kernel<8>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
   } else {
     dim3 g2(cdiv(max_blocks, 128), kv->Hkv, kv->B);
     if (kv->dtype == SE_BF16)
-      quest_bound_generic_kernel<__nv_bfloat16><<<g2, 128, 0, st>>>(
+      se_launch(quest_bound_generic_kernel<__nv_bfloat16>, g2, 128, 0, st,
           *kv, static_cast<const __nv_bfloat16*>(kmin), static_cast<const __nv_bfloat16*>(kmax),
           static_cast<const __nv_bfloat16*>(q), w.U, w.u_stride);
     else
-      quest_bound_generic_kernel<float><<<g2, 128, 0, st>>>(
+      se_launch(quest_bound_generic_kernel<float>, g2, 128, 0, st,
           *kv, static_cast<const float*>(kmin), static_cast<const float*>(kmax),
           static_cast<const float*>(q), w.U, w.u_stride);
   }
-  quest_ranges_kernel<<<cdiv(kv->B, 256), 256, 0, st>>>(kv->ctx_len, kv->B, kv->page_size,
+  se_launch(quest_ranges_kernel, cdiv(kv->B, 256), 256, 0, st, kv->ctx_len, kv->B, kv->page_size,
                                                         max_blocks, kv->status, w.cand_lo,
                                                         w.cand_hi, w.flo, w.fhi);
   s = launch_topk_select_pages(kv->B, kv->Hkv, w.U, w.u_stride, w.cand_lo, w.cand_hi, w.flo,

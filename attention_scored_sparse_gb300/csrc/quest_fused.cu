@@ -142,6 +142,7 @@ struct QfSmem {
 template <int G>
 __global__ void __cluster_dims__(kQfCtas, 1, 1) __launch_bounds__(kQfThreads, 1)
 quest_fused_kernel(QfArgs a) {
+  pdl_enter();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int D = 128, V = 8, E = 16 / G;
@@ -504,7 +505,7 @@ se_status launch_fused(const QfArgs& a, cudaStream_t st) {
       return SE_ERR_CUDA;
     attr = true;
   }
-  quest_fused_kernel<G><<<dim3(kQfCtas * a.kv.Hkv, a.kv.B), kQfThreads, smem, st>>>(a);
+  se_launch(quest_fused_kernel<G>, dim3(kQfCtas * a.kv.Hkv, a.kv.B), kQfThreads, smem, st, a);
   return SE_OK;
 }
 

@@ -94,6 +94,7 @@ SE_DEV void load_k_tile(const ScoreArgs& a, int b, int g, int lo, int k0, int n,
 // grid: (row tiles, n_splits, B*Hkv), 256 threads: thread = (row tid/8, keys tid%8 + 8i)
 template <typename T>
 __global__ void __launch_bounds__(256) score_stats_simt(ScoreArgs a, int D) {
+  pdl_enter();
   extern __shared__ float smem[];
   float* sq = smem;                          // [32][D+1]
   float* sk = sq + kTile * (D + 1);          // [32][D+1]
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(256) score_stats_simt(ScoreArgs a, int D) {
 
 // lse2 per row from the split partials.  grid: (cdiv(rows,256), B*Hkv)
 __global__ void score_lse_kernel(ScoreArgs a) {
+  pdl_enter();
   const int bg = blockIdx.y;
   const int G = a.kv.Hq / a.kv.Hkv;
   const int rows = a.w * G;
@@ -172,6 +174,7 @@ __global__ void score_lse_kernel(ScoreArgs a) {
 // thread = (key tid%32, rows tid/32 + 8i)
 template <typename T>
 __global__ void __launch_bounds__(256) score_colsum_simt(ScoreArgs a, int D) {
+  pdl_enter();
   extern __shared__ float smem[];
   float* sq = smem;
   float* sk = sq + kTile * (D + 1);
@@ -253,13 +256,13 @@ se_status launch_score_simt(ScoreArgs a, void* ws, cudaStream_t st) {
   dim3 g1(cdiv(rows, kTile), a.n_splits, kv->B * kv->Hkv);
   dim3 g2(cdiv(a.n_max, kTile), 1, kv->B * kv->Hkv);
   if (kv->dtype == SE_BF16) {
-    score_stats_simt<__nv_bfloat16><<<g1, 256, smem, st>>>(a, D);
-    score_lse_kernel<<<dim3(cdiv(rows, 256), kv->B * kv->Hkv), 256, 0, st>>>(a);
-    score_colsum_simt<__nv_bfloat16><<<g2, 256, smem, st>>>(a, D);
+    se_launch(score_stats_simt<__nv_bfloat16>, g1, 256, smem, st, a, D);
+    se_launch(score_lse_kernel, dim3(cdiv(rows, 256), kv->B * kv->Hkv), 256, 0, st, a);
+    se_launch(score_colsum_simt<__nv_bfloat16>, g2, 256, smem, st, a, D);
   } else {
-    score_stats_simt<float><<<g1, 256, smem, st>>>(a, D);
-    score_lse_kernel<<<dim3(cdiv(rows, 256), kv->B * kv->Hkv), 256, 0, st>>>(a);
-    score_colsum_simt<float><<<g2, 256, smem, st>>>(a, D);
+    se_launch(score_stats_simt<float>, g1, 256, smem, st, a, D);
+    se_launch(score_lse_kernel, dim3(cdiv(rows, 256), kv->B * kv->Hkv), 256, 0, st, a);
+    se_launch(score_colsum_simt<float>, g2, 256, smem, st, a, D);
   }
   return SE_OK;
 }

@@ -368,6 +368,7 @@ SE_DEV void colsum_tile_seq(uint32_t tb, bool fast, int kpos, const float* lse_s
 __global__ void __launch_bounds__(kThreads, 1)
 score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   TcArgs a) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;                                   // 64 KB
@@ -549,6 +550,7 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 // grid (cdiv(RC*256, 256), B*Hkv)
 // ---------------------------------------------------------------------------
 __global__ void score_rowinfo_tc(TcArgs a) {
+  pdl_enter();
   const int bg = blockIdx.y, b = bg / a.Hkv;
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   const int padded = a.RC * kRowChunk;
@@ -585,6 +587,7 @@ __global__ void score_rowinfo_tc(TcArgs a) {
 __global__ void __launch_bounds__(kThreads, 1)
 score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                 TcArgs a) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int RC = a.RC;
@@ -927,6 +930,7 @@ SE_DEV int cta_of(int64_t x, int64_t T, int64_t C) { return (int)(((x + 1) * C -
 __global__ void __launch_bounds__(kThreads, 1)
 score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap qmap, TcArgs a) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int KS = kStages1;
@@ -1168,6 +1172,7 @@ SE_DEV float row_lse2(const TcArgs& a, const int* s_pre, int groups, int bg, int
 __global__ void __launch_bounds__(kThreads, 1)
 score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap qmap, TcArgs a) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int KS = 4;
@@ -1572,13 +1577,13 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
         return SE_ERR_CUDA;
     }
     const int ctas = std::min(std::min(n_sm, kMaxPersistentCTAs), groups * p.n_tiles_max);
-    score_rowstats_persistent_tc<<<ctas, kThreads, kSmem1, st>>>(kmap, qmap, a);
-    score_colsum_persistent_tc<<<ctas, kThreads, kSmem2Resident, st>>>(kmap, qmap, a);
+    se_launch(score_rowstats_persistent_tc, ctas, kThreads, kSmem1, st, kmap, qmap, a);
+    se_launch(score_colsum_persistent_tc, ctas, kThreads, kSmem2Resident, st, kmap, qmap, a);
     return SE_OK;
   }
-  score_rowstats_tc<<<dim3(p.n_splits, p.RC, groups), kThreads, kSmem1, st>>>(kmap, qmap, a);
-  score_rowinfo_tc<<<dim3(cdiv(p.RC * kRowChunk, 256), groups), 256, 0, st>>>(a);
-  score_colsum_tc<<<dim3(cdiv(p.n_tiles_max, p.tiles_per_cta2), groups), kThreads, kSmem2, st>>>(
+  se_launch(score_rowstats_tc, dim3(p.n_splits, p.RC, groups), kThreads, kSmem1, st, kmap, qmap, a);
+  se_launch(score_rowinfo_tc, dim3(cdiv(p.RC * kRowChunk, 256), groups), 256, 0, st, a);
+  se_launch(score_colsum_tc, dim3(cdiv(p.n_tiles_max, p.tiles_per_cta2), groups), kThreads, kSmem2, st,
       kmap, qmap, a);
   return SE_OK;
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "se.h"
 
 #define SE_DEV __device__ __forceinline__
@@ -14,6 +16,36 @@ namespace se {
 
 SE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 SE_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch.  Every kernel is launched with se_launch,
+// which lets it start while the kernel before it in the stream is still
+// finishing, and every kernel calls pdl_enter before it touches global
+// memory: the wait there returns once the previous kernel has completed and
+// its writes are visible, and the trigger then lets the next kernel of the
+// stream launch early in turn.  The launch latency and the ramp of the next
+// grid overlap the tail of the current one; the order of memory accesses is
+// that of plain stream order.  (Launched without the attribute, both
+// instructions do nothing.)
+SE_DEV void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... K, typename... A>
+inline cudaError_t se_launch(void (*kernel)(K...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // First-writer-wins device error word.
 SE_DEV void set_status(int32_t* status, int32_t code) {

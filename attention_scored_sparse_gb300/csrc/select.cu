@@ -39,6 +39,7 @@ SE_DEV int padded(int e) { return e + e / ITEMS; }
 // grid: (Hkv, B), 1024 threads, dynamic smem (1024*(ITEMS+1)+64) floats.
 template <int ITEMS>
 __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, int k) {
+  pdl_enter();
   extern __shared__ float s_sc[];
   __shared__ int tmp[33];
   __shared__ int hist[2048];
@@ -175,6 +176,7 @@ constexpr int kClusterCTAs = 4;
 template <int ITEMS>
 __global__ void __cluster_dims__(kClusterCTAs, 1, 1) __launch_bounds__(1024, 1)
 topk_cluster_kernel(SelectArgs a, int pool, int k) {
+  pdl_enter();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ float s_sc[];
@@ -376,6 +378,7 @@ SE_DEV int select_bit(const uint32_t* words, int j) {
 template <int IT>
 __global__ void __launch_bounds__(256) kara_chunk_kernel(SelectArgs a, int n_cand, int budget,
                                                          float coef) {
+  pdl_enter();
   __shared__ float s_sc[8][32 * IT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int inst = blockIdx.x * 8 + warp;
@@ -523,6 +526,7 @@ __global__ void __launch_bounds__(128) evict_one_kernel(SelectArgs a, const int3
                                                         const int32_t* logical_len,
                                                         const int32_t* slot_map, int64_t smax,
                                                         int budget, int recent) {
+  pdl_enter();
   __shared__ float s_v[4];
   __shared__ int s_p[4], s_s[4];
   const int inst = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -583,7 +587,7 @@ static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_
       return SE_ERR_CUDA;
     attr_set = true;
   }
-  topk_kernel<ITEMS><<<dim3(a.Hkv, a.B), 1024, smem, st>>>(a, pool, k);
+  se_launch(topk_kernel<ITEMS>, dim3(a.Hkv, a.B), 1024, smem, st, a, pool, k);
   return SE_OK;
 }
 
@@ -597,7 +601,7 @@ static se_status launch_topk_cluster_t(const SelectArgs& a, int pool, int k, cud
       return SE_ERR_CUDA;
     attr_set = true;
   }
-  topk_cluster_kernel<ITEMS><<<dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st>>>(a, pool, k);
+  se_launch(topk_cluster_kernel<ITEMS>, dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st, a, pool, k);
   return SE_OK;
 }
 
@@ -666,9 +670,9 @@ extern "C" se_status se_topk_select(const se_paged_kv* kv, const float* scores,
       return SE_ERR_INVALID_ARG;
     const int blocks = cdiv(kv->B * kv->Hkv, 8);
     if (p.n_max <= 256) {
-      kara_chunk_kernel<8><<<blocks, 256, 0, st>>>(a, p.k, p.chunk_budget, p.chunk_coef);
+      se_launch(kara_chunk_kernel<8>, blocks, 256, 0, st, a, p.k, p.chunk_budget, p.chunk_coef);
     } else if (p.n_max <= 512) {
-      kara_chunk_kernel<16><<<blocks, 256, 0, st>>>(a, p.k, p.chunk_budget, p.chunk_coef);
+      se_launch(kara_chunk_kernel<16>, blocks, 256, 0, st, a, p.k, p.chunk_budget, p.chunk_coef);
     } else {
       return SE_ERR_UNSUPPORTED;
     }
@@ -676,7 +680,7 @@ extern "C" se_status se_topk_select(const se_paged_kv* kv, const float* scores,
   }
   if (p.mode == SE_SELECT_EVICT_ONE) {
     if (p.budget < 0 || p.recent < 0) return SE_ERR_INVALID_ARG;
-    evict_one_kernel<<<kv->B * kv->Hkv, 128, 0, st>>>(a, kv->ctx_len, kv->logical_len, kv->slot_map,
+    se_launch(evict_one_kernel, kv->B * kv->Hkv, 128, 0, st, a, kv->ctx_len, kv->logical_len, kv->slot_map,
                                              (int64_t)kv->max_pages_per_seq * kv->page_size,
                                              p.budget, p.recent);
     return se_last_launch_status();
