@@ -51,11 +51,13 @@ struct QfArgs {
 };
 
 // k-th largest of the keys held by the CTA (ITEMS per thread, key 0 = absent):
-// three radix rounds of 11, 11 and 10 bits.  Returns the threshold key T and
-// how many keys equal to T are taken (the lowest-indexed ones).
+// up to three radix rounds of 11, 11 and 10 bits, fewer when every key under
+// the prefix found so far is taken.  Returns the threshold T on the digits
+// resolved (mask TM) and how many keys whose resolved digits equal T are
+// taken (the lowest-indexed ones).
 template <int ITEMS>
 SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tmp, int* s_digit,
-                          int* s_rem, uint32_t& T, int& need_eq) {
+                          int* s_rem, uint32_t& T, uint32_t& TM, int& need_eq) {
   const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0;
   int remaining = kk;
@@ -75,10 +77,13 @@ SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, int* 
       prefix |= (uint32_t)*s_digit << shift;
       remaining = *s_rem;
       pmask |= dmask << shift;
+      const bool whole_bin = hist[*s_digit] == remaining;
       __syncthreads();
+      if (whole_bin) break;
     }
   }
   T = kk > 0 ? prefix : 0xffffffffu;
+  TM = kk > 0 ? pmask : 0xffffffffu;
   need_eq = kk > 0 ? remaining : 0;
 }
 
@@ -87,12 +92,12 @@ SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, int* 
 template <int ITEMS>
 SE_DEV int block_select(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tmp, int* s_digit,
                         int* s_rem, bool (&sel)[ITEMS], int* total) {
-  uint32_t T;
+  uint32_t T, TM;
   int need_eq;
-  block_kth_key<ITEMS>(key, kk, hist, tmp, s_digit, s_rem, T, need_eq);
+  block_kth_key<ITEMS>(key, kk, hist, tmp, s_digit, s_rem, T, TM, need_eq);
   int c_eq = 0;
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
+  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && (key[i] & TM) == T) ? 1 : 0;
   int dummy;
   int eq_rank = block_exclusive_scan(c_eq, tmp, &dummy);
   int c_sel = 0;
@@ -100,9 +105,9 @@ SE_DEV int block_select(const uint32_t (&key)[ITEMS], int kk, int* hist, int* tm
   for (int i = 0; i < ITEMS; ++i) {
     sel[i] = false;
     if (key[i] != 0u) {
-      if (key[i] > T) {
+      if ((key[i] & TM) > T) {
         sel[i] = true;
-      } else if (key[i] == T) {
+      } else if ((key[i] & TM) == T) {
         sel[i] = eq_rank < need_eq;
         eq_rank++;
       }

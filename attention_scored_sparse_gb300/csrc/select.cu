@@ -93,8 +93,10 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   const int ncand = n - forced_in_total;
   const int kk = min(max(k, 0), ncand);
 
-  // 3 rounds of radix select (digits of 11, 11 and 10 bits, top first) for
-  // the kk-th largest key.  Wide digits spread scores that share an exponent.
+  // Up to 3 rounds of radix select (digits of 11, 11 and 10 bits, top first)
+  // for the kk-th largest key; a round whose threshold digit keeps every key
+  // under the prefix ends the search.  Wide digits spread scores that share
+  // an exponent.
   uint32_t prefix = 0, pmask = 0;
   int remaining = kk;
   if (kk > 0) {
@@ -113,15 +115,20 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
       prefix |= (uint32_t)s_digit << shift;
       remaining = s_rem;
       pmask |= dmask << shift;
+      // every key under this prefix is kept: its lower digits decide nothing
+      const bool whole_bin = hist[s_digit] == s_rem;
       __syncthreads();
+      if (whole_bin) break;
     }
   }
+  // keys are compared on the digits resolved so far
   const uint32_t T = kk > 0 ? prefix : 0xffffffffu;
+  const uint32_t TM = kk > 0 ? pmask : 0xffffffffu;
   const int need_eq = kk > 0 ? remaining : 0;
 
   int c_eq = 0;
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
+  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && (key[i] & TM) == T) ? 1 : 0;
   int dummy;
   int eq_rank = block_exclusive_scan(c_eq, tmp, &dummy);
   bool sel[ITEMS];
@@ -130,9 +137,9 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   for (int i = 0; i < ITEMS; ++i) {
     sel[i] = false;
     if (key[i] != 0u) {
-      if (key[i] > T) {
+      if ((key[i] & TM) > T) {
         sel[i] = true;
-      } else if (key[i] == T) {
+      } else if ((key[i] & TM) == T) {
         sel[i] = eq_rank < need_eq;
         eq_rank++;
       }
@@ -271,16 +278,22 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
       prefix |= (uint32_t)s_digit << shift;
       remaining = s_rem;
       pmask |= dmask << shift;
+      // every key under this prefix is kept: its lower digits decide nothing
+      // (tot is the same in every CTA of the cluster, so is the decision)
+      const bool whole_bin = tot[s_digit] == s_rem;
       __syncthreads();
+      if (whole_bin) break;
     }
   }
+  // keys are compared on the digits resolved so far
   const uint32_t T = kk > 0 ? prefix : 0xffffffffu;
+  const uint32_t TM = kk > 0 ? pmask : 0xffffffffu;
   const int need_eq = kk > 0 ? remaining : 0;
 
   // equal keys: cluster-wide rank in element order
   int c_eq = 0;
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && key[i] == T) ? 1 : 0;
+  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && (key[i] & TM) == T) ? 1 : 0;
   int my_eq_total;
   int eq_rank = block_exclusive_scan(c_eq, tmp, &my_eq_total);
   if (tid == 0) s_cnt[1] = my_eq_total;
@@ -292,9 +305,9 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
   for (int i = 0; i < ITEMS; ++i) {
     sel[i] = false;
     if (key[i] != 0u) {
-      if (key[i] > T) {
+      if ((key[i] & TM) > T) {
         sel[i] = true;
-      } else if (key[i] == T) {
+      } else if ((key[i] & TM) == T) {
         sel[i] = eq_rank < need_eq;
         eq_rank++;
       }
