@@ -241,64 +241,72 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
     }
   }
   if (n_forced_in) atomicAdd(&s_cnt[0], n_forced_in);
-  cluster.sync();
-  int forced_in_total = 0;
-  for (int r = 0; r < kClusterCTAs; ++r) forced_in_total += *cluster.map_shared_rank(&s_cnt[0], r);
-  const int ncand = n - forced_in_total;
-  const int kk = bad ? 0 : min(max(k, 0), ncand);
 
+  // Up to three radix rounds; the forced-in counts travel with round 0's
+  // barrier (the histogram does not depend on k).
   uint32_t prefix = 0, pmask = 0;
-  int remaining = kk;
-  if (kk > 0) {
+  int kk = 0, remaining = 0, bin_total = 0;
 #pragma unroll 1
-    for (int round = 0; round < 3; ++round) {
-      const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-      const int nbins = round == 2 ? 1024 : 2048;
-      const uint32_t dmask = (uint32_t)nbins - 1u;
-      // buffer round & 1 was last read by peers two rounds ago; every peer
-      // has passed the previous round's cluster barrier since, after its reads
-      int* hb = hist[round & 1];
-      for (int i = tid; i < nbins; i += 1024) hb[i] = 0;
-      __syncthreads();
+  for (int round = 0; round < 3; ++round) {
+    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+    const int nbins = round == 2 ? 1024 : 2048;
+    const uint32_t dmask = (uint32_t)nbins - 1u;
+    // buffer round & 1 was last read by peers two rounds ago; every peer
+    // has passed the previous round's cluster barrier since, after its reads
+    int* hb = hist[round & 1];
+    for (int i = tid; i < nbins; i += 1024) hb[i] = 0;
+    __syncthreads();
 #pragma unroll
-      for (int i = 0; i < ITEMS; ++i)
-        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hb[(key[i] >> shift) & dmask], 1);
-      cluster.sync();                    // every CTA's histogram is complete
-      // each thread sums up to two bins over the cluster
-      for (int j = 0; j < 2; ++j) {
-        const int bin = tid + j * 1024;
-        if (bin < nbins) {
-          int sum = 0;
-          for (int r = 0; r < kClusterCTAs; ++r) sum += *cluster.map_shared_rank(&hb[bin], r);
-          tot[bin] = sum;
-        }
-      }
-      __syncthreads();
-      radix_find_digit(tot, nbins, remaining, tmp, &s_digit, &s_rem);
-      prefix |= (uint32_t)s_digit << shift;
-      remaining = s_rem;
-      pmask |= dmask << shift;
-      // every key under this prefix is kept: its lower digits decide nothing
-      // (tot is the same in every CTA of the cluster, so is the decision)
-      const bool whole_bin = tot[s_digit] == s_rem;
-      __syncthreads();
-      if (whole_bin) break;
+    for (int i = 0; i < ITEMS; ++i)
+      if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hb[(key[i] >> shift) & dmask], 1);
+    cluster.sync();                    // every CTA's histogram (and round 0: count) is complete
+    if (round == 0) {
+      int forced_in_total = 0;
+      for (int r = 0; r < kClusterCTAs; ++r) forced_in_total += *cluster.map_shared_rank(&s_cnt[0], r);
+      kk = bad ? 0 : min(max(k, 0), n - forced_in_total);
+      remaining = kk;
+      if (kk == 0) break;              // same in every CTA
     }
+    // each thread sums up to two bins over the cluster
+    for (int j = 0; j < 2; ++j) {
+      const int bin = tid + j * 1024;
+      if (bin < nbins) {
+        int sum = 0;
+        for (int r = 0; r < kClusterCTAs; ++r) sum += *cluster.map_shared_rank(&hb[bin], r);
+        tot[bin] = sum;
+      }
+    }
+    __syncthreads();
+    radix_find_digit(tot, nbins, remaining, tmp, &s_digit, &s_rem);
+    prefix |= (uint32_t)s_digit << shift;
+    remaining = s_rem;
+    pmask |= dmask << shift;
+    bin_total = tot[s_digit];
+    __syncthreads();
+    // every key under this prefix is kept: its lower digits decide nothing
+    // (tot is the same in every CTA of the cluster, so is the decision)
+    if (bin_total == remaining) break;
   }
   // keys are compared on the digits resolved so far
   const uint32_t T = kk > 0 ? prefix : 0xffffffffu;
   const uint32_t TM = kk > 0 ? pmask : 0xffffffffu;
   const int need_eq = kk > 0 ? remaining : 0;
 
-  // equal keys: cluster-wide rank in element order
-  int c_eq = 0;
+  // keys equal to T on those digits: all of them are taken unless ties at
+  // the full key cut the threshold bin; only then do they need their
+  // cluster-wide rank in element order
+  const bool all_eq = kk == 0 || bin_total == need_eq;
+  int eq_rank = 0;
+  if (!all_eq) {
+    int c_eq = 0;
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && (key[i] & TM) == T) ? 1 : 0;
-  int my_eq_total;
-  int eq_rank = block_exclusive_scan(c_eq, tmp, &my_eq_total);
-  if (tid == 0) s_cnt[1] = my_eq_total;
-  cluster.sync();
-  for (int r = 0; r < rank; ++r) eq_rank += *cluster.map_shared_rank(&s_cnt[1], r);
+    for (int i = 0; i < ITEMS; ++i) c_eq += (key[i] != 0u && (key[i] & TM) == T) ? 1 : 0;
+    int my_eq_total;
+    eq_rank = block_exclusive_scan(c_eq, tmp, &my_eq_total);
+    if (tid == 0) s_cnt[1] = my_eq_total;
+    cluster.sync();
+    for (int r = 0; r < rank; ++r) eq_rank += *cluster.map_shared_rank(&s_cnt[1], r);
+  }
   bool sel[ITEMS];
   int c_sel = 0, c_sel_before_force = 0;
 #pragma unroll
@@ -308,7 +316,7 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
       if ((key[i] & TM) > T) {
         sel[i] = true;
       } else if ((key[i] & TM) == T) {
-        sel[i] = eq_rank < need_eq;
+        sel[i] = all_eq || eq_rank < need_eq;
         eq_rank++;
       }
     }
@@ -327,13 +335,12 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
     total_sel += cs;
     before_force += *cluster.map_shared_rank(&s_cnt[3], r);
   }
-  cluster.sync();                        // no CTA leaves while peers read its counters
-  if (bad) {
+  // peers may still read this CTA's counters: arrive now, wait before leaving
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  const bool fail = bad || total_sel + nf > a.keep_stride;   // same in every CTA
+  if (fail) {
     if (rank == 0 && tid == 0) set_status(a.status, SE_ERR_BOUNDS);
-    return;
-  }
-  if (total_sel + nf > a.keep_stride) {
-    if (rank == 0 && tid == 0) set_status(a.status, SE_ERR_BOUNDS);
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
   }
   int32_t* out = a.keep + ((int64_t)b * a.Hkv + h) * a.keep_stride;
@@ -350,6 +357,7 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
     for (int p = total_sel + nf + tid; p < a.keep_stride; p += 1024) out[p] = -1;
     if (h == 0 && tid == 0 && a.n_keep) a.n_keep[b] = total_sel + nf;
   }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // --------------------------------------------------------------------------
@@ -620,7 +628,7 @@ static se_status launch_topk_cluster_t(const SelectArgs& a, int pool, int k, cud
 
 se_status launch_topk(const SelectArgs& a, int pool, int k, int n_max, cudaStream_t st) {
   // long candidate ranges: four CTAs per (sequence, head) in a cluster
-  if (n_max > 2048) {
+  if (n_max > 8192) {
     const int items = cdiv(cdiv(n_max, kClusterCTAs) + 8, 1024);
     if (items <= 2) return launch_topk_cluster_t<2>(a, pool, k, st);
     if (items <= 4) return launch_topk_cluster_t<4>(a, pool, k, st);
