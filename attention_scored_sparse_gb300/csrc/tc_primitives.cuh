@@ -6,7 +6,6 @@
 #include <cuda.h>
 #include <stdint.h>
 
-#include "exp2_poly.cuh"
 #include "se_common.cuh"
 
 namespace se {
@@ -319,26 +318,6 @@ SE_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA pipe (for x <= ~0, finite): range reduction x = n + f with
-// n = round(x) taken from the low mantissa bits of x + 1.5*2^23, f in
-// [-1/2, 1/2]; 2^f from the degree-5 polynomial of exp2_poly.cuh (relative
-// error < 3e-7, comparable to ex2.approx); 2^n added to the exponent field.
-// Inputs below -126 give about 2^-126 instead of 0 (negligible next to any
-// sum it joins).  Used for part of the exponentials so the special-function
-// unit and the FMA pipe share the load.
-SE_DEV float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float j = x + 12582912.f;
-  const float n = j - 12582912.f;
-  const float f = x - n;
-  float p = fmaf(kExp2C5, f, kExp2C4);
-  p = fmaf(p, f, kExp2C3);
-  p = fmaf(p, f, kExp2C2);
-  p = fmaf(p, f, kExp2C1);
-  p = fmaf(p, f, kExp2C0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(j) << 23));
 }
 
 SE_DEV bool elect_one() {

@@ -222,6 +222,61 @@ def test_decode_attention_views_match_oracle(cuda_lib, dtype, D, G):
                 np.testing.assert_allclose(accg[b, g], expect, rtol=1e-4, atol=1e-6)
 
 
+def _aligned_ctas(units, max_entries):
+    """CTAs of the unit-aligned split of decode attention (chunks of at most
+    1024 entries, halved down to 128 while fewer than 152 x 4 CTAs)."""
+    chunk = 1024
+    while chunk > 128 and units * W.cdiv(max_entries, chunk) < 608:
+        chunk //= 2
+    return units * W.cdiv(max_entries, chunk)
+
+
+def test_decode_attention_stream_split_matches_oracle(cuda_lib):
+    """320 (sequence, head) units of up to 1153 entries: the unit-aligned
+    chunks would make 640 CTAs (1.05 waves), so the ranges are cut evenly over
+    all units and cross unit boundaries.  Ragged contexts, dense view with
+    running scores and a token view."""
+    se = cuda_lib
+    B, Hkv, G, D, me = 40, 8, 4, 128, 1153
+    assert 608 < _aligned_ctas(B * Hkv, me) < 4 * 608     # the shape takes the even split
+    dtype = torch.bfloat16
+    shape = W.Shape(name="dstream", B=B, Hq=Hkv * G, Hkv=Hkv, D=D, page_size=16, ctx=me, dtype=dtype)
+    pc = W.build_paged_cache(shape, num_pages=B * W.cdiv(me, 16) + 3, max_ctx=me, device="cuda",
+                             tag="dstream")
+    rng = np.random.default_rng(11)
+    ctx = rng.integers(1, me + 1, size=B).astype(np.int32)
+    ctx[:3] = [me, 1, 16]
+    pc.ctx_len.copy_(torch.from_numpy(ctx))
+    c = ocache.from_tensors(pc)
+    q = W.normal((B, shape.Hq, D), dtype, "cuda", "dstream", "q")
+    qv = q.double().cpu().numpy()
+    n_tok = 1100
+    sel_t = np.full((B, Hkv, n_tok), -1, dtype=np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            t = np.sort(rng.choice(int(ctx[b]), min(int(ctx[b]), 1000), replace=False))
+            sel_t[b, g, : len(t)] = t
+    stride = W.cdiv(me, 16) * 16
+    for view, sel, n_sel, oview in [(se.SE_VIEW_DENSE, None, 0, "dense"),
+                                    (se.SE_VIEW_TOKENS, sel_t, n_tok, "tokens")]:
+        acc = torch.zeros((B, Hkv, stride), device="cuda")
+        st = None if sel is None else torch.from_numpy(sel).cuda()
+        o = H.run_decode(pc, shape.Hq, q, view, st, n_sel, acc=acc)
+        torch.cuda.synchronize()
+        assert int(pc.status.item()) == 0
+        oo, ps = oattn.decode_attention(c, qv, oview, sel)
+        og = o.double().cpu().numpy()
+        accg = acc.cpu().double().numpy()
+        for b in range(B):
+            for g in range(Hkv):
+                err = np.abs(og[b, g * G:(g + 1) * G] - oo[(b, g)]).max()
+                assert err <= H.OUT_ATOL[dtype], (oview, b, g, err)
+                slots, p = ps[(b, g)]
+                expect = np.zeros(stride)
+                expect[slots] += p
+                np.testing.assert_allclose(accg[b, g], expect, rtol=1e-4, atol=1e-6)
+
+
 def test_decode_attention_special_cases(cuda_lib):
     se = cuda_lib
     shape = W.Shape(name="dsc", B=2, Hq=4, Hkv=1, D=128, page_size=16, ctx=40, dtype=torch.float32)
