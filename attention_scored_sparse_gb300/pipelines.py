@@ -13,7 +13,8 @@ from __future__ import annotations
 import torch
 
 from . import (SE_COMPACT_FRESH_PAGES, SE_COMPACT_MOVE_LAST, SE_SELECT_EVICT_ONE,
-               SE_SELECT_KARA_CHUNK, SE_SELECT_TOPK, SE_VIEW_DENSE, SE_VIEW_PAGES, kv_desc,
+               SE_SELECT_KARA_CHUNK, SE_SELECT_TOPK, SE_VIEW_DENSE, SE_VIEW_PAGES,
+               SE_VIEW_TOKENS, kv_desc,
                se_append_kv, se_compact_evict, se_prune_span, se_quest_build_meta,
                se_quest_decode_step, se_quest_page_select, se_score_window,
                se_sparse_decode_attn, se_topk_select,
@@ -39,6 +40,19 @@ class _Base:
         return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
 
 
+class _Snapshot:
+    """A cache's tensors with the block table and context lengths replaced by
+    other tensors (copies taken before compaction rewrites them)."""
+
+    def __init__(self, cache, block_table, ctx_len):
+        for n in ("k_pool", "v_pool", "slot_map", "logical_len", "free_list", "free_top",
+                  "status", "page_size"):
+            setattr(self, n, getattr(cache, n))
+        self.page_refcount = getattr(cache, "page_refcount", None)
+        self.block_table = block_table
+        self.ctx_len = ctx_len
+
+
 class SnapKV(_Base):
     """SnapKV after the last prompt chunk: causal window scores, avg-pool +
     top-k per KV head with the window forced, compaction into fresh pages,
@@ -59,6 +73,12 @@ class SnapKV(_Base):
         self.ws_score = self._ws(sz["score_window"])
         self.ws_compact = self._ws(sz["compact_evict"])
         self.ws_decode = self._ws(sz["sparse_decode_attn"])
+        # block table and context lengths as they were before compaction, so
+        # decode attention can read the kept entries while compaction moves them
+        self.bt_snap = torch.empty_like(cache.block_table)
+        self.ctx_snap = torch.empty_like(cache.ctx_len)
+        self.kv_snap = kv_desc(_Snapshot(cache, self.bt_snap, self.ctx_snap), Hq)
+        self.side = torch.cuda.Stream(device=dev)
 
     def score(self, q_win, q_pos, stream=None):
         se_score_window(self.kv, q_win, q_pos, self.zero, self.ctx_t, self.zero, self.scored_t,
@@ -80,11 +100,36 @@ class SnapKV(_Base):
         se_sparse_decode_attn(self.kv, q, view=SE_VIEW_DENSE, o=o, max_entries=self.budget,
                               workspace=self.ws_decode, stream=stream)
 
+    def decode_kept(self, q, o, stream=None):
+        """Decode attention over the kept entries where they lie before
+        compaction: the token view of keep_idx through the snapshot of the
+        block table and context lengths.  The same entries, in the same order,
+        as the dense view of the compacted cache."""
+        se_sparse_decode_attn(self.kv_snap, q, view=SE_VIEW_TOKENS, sel=self.keep,
+                              n_sel=self.budget, o=o, max_entries=self.budget,
+                              workspace=self.ws_decode, stream=stream)
+
+    def compact_decode(self, q, o, stream=None):
+        """Compaction and decode attention side by side: the block table and
+        context lengths are copied, decode attention runs on a second stream
+        over the kept entries in their old pages while compaction copies them
+        into fresh pages (it writes only pages it pops from the free list and
+        returns the old ones after the copy; nothing reuses them within the
+        step), and the stream waits for both.  ``stream`` is a
+        ``torch.cuda.Stream`` (default: the current stream)."""
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        with torch.cuda.stream(main):
+            self.bt_snap.copy_(self.cache.block_table)
+            self.ctx_snap.copy_(self.cache.ctx_len)
+        self.side.wait_stream(main)
+        self.decode_kept(q, o, self.side)
+        self.compact(main)
+        main.wait_stream(self.side)
+
     def step(self, q_win, q_pos, q_dec, o, stream=None):
         self.score(q_win, q_pos, stream)
         self.select(stream)
-        self.compact(stream)
-        self.decode(q_dec, o, stream)
+        self.compact_decode(q_dec, o, stream)
 
 
 class QuestDecode(_Base):

@@ -80,6 +80,37 @@ def test_snapkv_llama8b_reduced(cuda_lib):
     _snapkv(cuda_lib, W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512))
 
 
+def test_snapkv_step_decodes_beside_compaction(cuda_lib):
+    """The pipeline step runs decode attention on a second stream over the
+    kept entries in their old pages while compaction moves them: its output
+    equals, bit for bit, decode attention over the compacted cache, and the
+    compacted cache is the same as the one the separate calls leave."""
+    shape = W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512)
+    runs = []
+    for overlapped in (False, True):
+        inp = W.snapkv_inputs(shape, "cuda")
+        pc = inp["cache"]
+        pipe = P.SnapKV(pc, shape.Hq, ctx=shape.ctx, window=shape.window, budget=shape.budget,
+                        pool_kernel=shape.pool_kernel)
+        o = torch.full_like(inp["q_dec"], float("nan"))
+        if overlapped:
+            pipe.step(inp["q_win"], inp["q_pos"], inp["q_dec"], o)
+        else:
+            pipe.score(inp["q_win"], inp["q_pos"])
+            pipe.select()
+            pipe.compact()
+            pipe.decode(inp["q_dec"], o)
+        torch.cuda.synchronize()
+        assert H.status(pc) == 0
+        runs.append((o.clone(), {n: getattr(pc, n).clone() for n in
+                                 ("block_table", "slot_map", "ctx_len", "free_list", "free_top",
+                                  "k_pool", "v_pool")}))
+    (o_seq, c_seq), (o_ovl, c_ovl) = runs
+    assert torch.equal(o_seq, o_ovl)
+    for n in c_seq:
+        assert torch.equal(c_seq[n], c_ovl[n]), n
+
+
 @pytest.mark.slow
 def test_snapkv_llama8b_full(cuda_lib):
     """4 x 32768 tokens, 32/8 heads, budget 2048: full oracle (about 30 s)."""
