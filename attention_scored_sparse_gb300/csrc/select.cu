@@ -36,6 +36,71 @@ struct SelectArgs {
 template <int ITEMS>
 SE_DEV int padded(int e) { return e + e / ITEMS; }
 
+// Keys of this thread's ITEMS consecutive candidates e0 + i, i < ITEMS, from
+// the scores in shared memory (element e at padded index e - xbase; n_loaded
+// elements from xbase on): the sum over the pool window (neighbours outside
+// [0, n) are absent), as an order-preserving uint -- the window sum ranks
+// like the window mean.  Candidates at or past r_end get key 0, forced ones
+// (slot in [flo, fhi)) too; returns how many were forced.  HALO >= 0: the
+// window half-width at compile time, each window value read once; HALO < 0:
+// the half-width pool / 2 at run time.
+template <int ITEMS, int HALO>
+SE_DEV int pooled_keys(const float* s_sc, int e0, int r_end, int n, int xbase, int n_loaded,
+                       int pool, int lo, int flo, int fhi, bool bad, uint32_t (&key)[ITEMS]) {
+  int n_forced_in = 0;
+  if constexpr (HALO >= 0) {
+    float w[ITEMS + 2 * HALO];
+#pragma unroll
+    for (int i = 0; i < ITEMS + 2 * HALO; ++i) {
+      const int ee = e0 - HALO + i;
+      const bool in = !bad && ee >= 0 && ee < n && ee - xbase < n_loaded;
+      w[i] = in ? s_sc[padded<ITEMS>(ee - xbase)] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      const int e = e0 + i;
+      key[i] = 0u;
+      if (!bad && e < r_end) {
+        const int slot = lo + e;
+        if (slot >= flo && slot < fhi) {
+          n_forced_in++;
+        } else {
+          float acc = 0.f;
+#pragma unroll
+          for (int d = 0; d <= 2 * HALO; ++d) acc += w[i + d];
+          key[i] = float_key(acc);
+        }
+      }
+    }
+  } else {
+    const int halo = pool / 2;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      const int e = e0 + i;
+      key[i] = 0u;
+      if (!bad && e < r_end) {
+        const int slot = lo + e;
+        if (slot >= flo && slot < fhi) {
+          n_forced_in++;
+        } else {
+          float v;
+          if (pool > 1) {
+            v = 0.f;
+            for (int d = -halo; d <= halo; ++d) {
+              const int ee = e + d;
+              if (ee >= 0 && ee < n) v += s_sc[padded<ITEMS>(ee - xbase)];
+            }
+          } else {
+            v = s_sc[padded<ITEMS>(e - xbase)];
+          }
+          key[i] = float_key(v);
+        }
+      }
+    }
+  }
+  return n_forced_in;
+}
+
 // grid: (Hkv, B), 1024 threads, dynamic smem (1024*(ITEMS+1)+64) floats.
 template <int ITEMS>
 __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, int k) {
@@ -61,33 +126,8 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
   __syncthreads();
 
   uint32_t key[ITEMS];
-  const int r = pool / 2;
-  const float inv_div = (float)pool;
-  int n_forced_in = 0;
-#pragma unroll
-  for (int i = 0; i < ITEMS; ++i) {
-    const int e = tid * ITEMS + i;
-    key[i] = 0u;
-    if (e < n) {
-      const int slot = lo + e;
-      if (slot >= flo && slot < fhi) {
-        n_forced_in++;
-      } else {
-        float v;
-        if (pool > 1) {
-          float acc = 0.f;
-          for (int d = -r; d <= r; ++d) {
-            const int x = e + d;
-            if (x >= 0 && x < n) acc += s_sc[padded<ITEMS>(x)];
-          }
-          v = acc / inv_div;
-        } else {
-          v = s_sc[padded<ITEMS>(e)];
-        }
-        key[i] = float_key(v);
-      }
-    }
-  }
+  const int n_forced_in =
+      pooled_keys<ITEMS, -1>(s_sc, tid * ITEMS, n, n, 0, n, pool, lo, flo, fhi, false, key);
   int forced_in_total;
   block_exclusive_scan(n_forced_in, tmp, &forced_in_total);
   const int ncand = n - forced_in_total;
@@ -180,7 +220,7 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
 // --------------------------------------------------------------------------
 constexpr int kClusterCTAs = 4;
 
-template <int ITEMS>
+template <int ITEMS, int HALO>
 __global__ void __cluster_dims__(kClusterCTAs, 1, 1) __launch_bounds__(1024, 1)
 topk_cluster_kernel(SelectArgs a, int pool, int k) {
   pdl_enter();
@@ -214,32 +254,8 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
   __syncthreads();
 
   uint32_t key[ITEMS];
-  int n_forced_in = 0;
-#pragma unroll
-  for (int i = 0; i < ITEMS; ++i) {
-    const int e = r0 + tid * ITEMS + i;
-    key[i] = 0u;
-    if (!bad && e < r1) {
-      const int slot = lo + e;
-      if (slot >= flo && slot < fhi) {
-        n_forced_in++;
-      } else {
-        const int x = e - r0 + halo;
-        float v;
-        if (pool > 1) {
-          float acc = 0.f;
-          for (int d = -halo; d <= halo; ++d) {
-            const int ee = e + d;
-            if (ee >= 0 && ee < n) acc += s_sc[padded<ITEMS>(x + d)];
-          }
-          v = acc / (float)pool;
-        } else {
-          v = s_sc[padded<ITEMS>(x)];
-        }
-        key[i] = float_key(v);
-      }
-    }
-  }
+  const int n_forced_in = pooled_keys<ITEMS, HALO>(s_sc, r0 + tid * ITEMS, r1, n, r0 - halo, x1,
+                                                   pool, lo, flo, fhi, bad, key);
   if (n_forced_in) atomicAdd(&s_cnt[0], n_forced_in);
 
   // Up to three radix rounds; the forced-in counts travel with round 0's
@@ -612,18 +628,26 @@ static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_
   return SE_OK;
 }
 
-template <int ITEMS>
-static se_status launch_topk_cluster_t(const SelectArgs& a, int pool, int k, cudaStream_t st) {
+template <int ITEMS, int HALO>
+static se_status launch_topk_cluster_h(const SelectArgs& a, int pool, int k, cudaStream_t st) {
   const size_t smem = (size_t)(1024 * (ITEMS + 1) + 64) * sizeof(float);
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_cluster_kernel<ITEMS>,
+    if (cudaFuncSetAttribute(topk_cluster_kernel<ITEMS, HALO>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return SE_ERR_CUDA;
     attr_set = true;
   }
-  se_launch(topk_cluster_kernel<ITEMS>, dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st, a, pool, k);
+  se_launch(topk_cluster_kernel<ITEMS, HALO>, dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st, a,
+            pool, k);
   return SE_OK;
+}
+
+// the SnapKV pooling width (7) with its window unrolled; any other width at run time
+template <int ITEMS>
+static se_status launch_topk_cluster_t(const SelectArgs& a, int pool, int k, cudaStream_t st) {
+  if (pool == 7) return launch_topk_cluster_h<ITEMS, 3>(a, pool, k, st);
+  return launch_topk_cluster_h<ITEMS, -1>(a, pool, k, st);
 }
 
 se_status launch_topk(const SelectArgs& a, int pool, int k, int n_max, cudaStream_t st) {
