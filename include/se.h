@@ -168,7 +168,8 @@ typedef struct {
  *             n_keep[b] = their count (same for every head).
  *             EVICT_ONE: [B][Hkv] victim slot or -1; n_keep may be NULL.
  * TOPK ranks candidates by (avg-pooled score desc, slot asc) -- pooling over
- * [cand_lo, cand_hi) with zero padding -- and keeps the first k.
+ * [cand_lo, cand_hi) with zero padding -- and keeps the first k (the device
+ * ranks by the fp32 window sum, which orders as the mean does).
  * KARA_CHUNK keeps the top-k candidates, adds chunk interiors between
  * consecutive candidates by (chunk score desc, start asc) while they fit
  * chunk_budget, then tops up with the best remaining tokens to exactly
