@@ -5,15 +5,16 @@
 // slots of a list of blocks (Quest pages) or a list of slots.
 //
 // Bandwidth-bound design (each K/V byte is used by the G query heads of its
-// group and nothing else): split-K over the view ("chunks" of entries, one
-// CTA each, about four CTAs per SM), a half-warp per group of 16/G entries
-// with 16-byte row loads (a 256-byte bf16 row is one coalesced half-warp
-// load), the group's G queries pre-scaled by log2(e)/sqrt(D) in registers, an
-// xor reduce-scatter of the partial dot products, one exponential per
-// (entry, head) and a base-2 online softmax.  Half-warp states merge in
-// shared memory; the last chunk CTA of each (sequence, KV group) merges the
-// chunks and, for H2O, adds sum_h p_{h,j} to the running scores from the
-// logits the chunk CTAs stored.
+// group and nothing else): split-K over the view (ranges of entries, one
+// CTA each, four CTAs per SM; see the work split below), a half-warp per
+// group of 16/G entries with 16-byte row loads (a 256-byte bf16 row is one
+// coalesced half-warp load), the group's G queries pre-scaled by
+// log2(e)/sqrt(D) in registers, an xor reduce-scatter of the partial dot
+// products, one exponential per (entry, head) and a base-2 online softmax.
+// Half-warp states merge in shared memory into one partial per segment; the
+// last CTA to finish a segment of a (sequence, KV group) merges the partials
+// and, for H2O, adds sum_h p_{h,j} to the running scores from the logits the
+// CTAs stored.
 #include <algorithm>
 
 #include "tc_primitives.cuh"
@@ -861,13 +862,9 @@ static void launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   const dim3 grid(a.n_cta);
   bool staged = Gm::STAGES > 0;
   if constexpr (Gm::STAGES > 0) {
-    static bool attr = false;
-    if (!attr) {
-      attr = cudaFuncSetAttribute(decode_partial_kernel<T, D, G>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Gm::SMEM) == cudaSuccess;
-      staged = attr;
-    }
+    static std::atomic<uint64_t> attr{0};
+    staged = allow_smem(reinterpret_cast<const void*>(&decode_partial_kernel<T, D, G>), Gm::SMEM,
+                        attr);
     if (staged) se_launch(decode_partial_kernel<T, D, G>, grid, 128, Gm::SMEM, st, a);
   }
   if (!staged) se_launch(decode_partial_regs_kernel<T, D, G>, grid, 128, 0, st, a);

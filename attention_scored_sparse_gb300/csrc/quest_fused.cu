@@ -503,13 +503,9 @@ quest_fused_kernel(QfArgs a) {
 template <int G>
 se_status launch_fused(const QfArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(QfSmem<G>);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(quest_fused_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return SE_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (!allow_smem(reinterpret_cast<const void*>(&quest_fused_kernel<G>), (int)smem, attr))
+    return SE_ERR_CUDA;
   se_launch(quest_fused_kernel<G>, dim3(kQfCtas * a.kv.Hkv, a.kv.B), kQfThreads, smem, st, a);
   return SE_OK;
 }

@@ -1551,31 +1551,21 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
   a.tiles_per_cta2 = p.tiles_per_cta2;
   a.status = kv->status;
   a.scale = kLog2e / sqrtf((float)kD);
-  static bool attrs = false;
-  if (!attrs) {
-    if (cudaFuncSetAttribute(score_rowstats_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem1) != cudaSuccess ||
-        cudaFuncSetAttribute(score_colsum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem2) != cudaSuccess ||
-        cudaFuncSetAttribute(score_colsum_persistent_tc,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem2Resident) != cudaSuccess ||
-        cudaFuncSetAttribute(score_rowstats_persistent_tc,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem1) != cudaSuccess)
-      return SE_ERR_CUDA;
-    attrs = true;
-  }
+  static std::atomic<uint64_t> attr[4];
+  if (!allow_smem(reinterpret_cast<const void*>(&score_rowstats_tc), (int)kSmem1, attr[0]) ||
+      !allow_smem(reinterpret_cast<const void*>(&score_colsum_tc), (int)kSmem2, attr[1]) ||
+      !allow_smem(reinterpret_cast<const void*>(&score_colsum_persistent_tc), (int)kSmem2Resident,
+                  attr[2]) ||
+      !allow_smem(reinterpret_cast<const void*>(&score_rowstats_persistent_tc), (int)kSmem1,
+                  attr[3]))
+    return SE_ERR_CUDA;
   const int groups = kv->B * kv->Hkv;
   if (p.RC == 1 && groups <= kMaxGroupsP) {
     // one row chunk: persistent CTAs, one per SM, over the (group, tile) sequence
-    static int n_sm = 0;
-    if (n_sm == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return SE_ERR_CUDA;
-    }
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SE_ERR_CUDA;
     const int ctas = std::min(std::min(n_sm, kMaxPersistentCTAs), groups * p.n_tiles_max);
     se_launch(score_rowstats_persistent_tc, ctas, kThreads, kSmem1, st, kmap, qmap, a);
     se_launch(score_colsum_persistent_tc, ctas, kThreads, kSmem2Resident, st, kmap, qmap, a);

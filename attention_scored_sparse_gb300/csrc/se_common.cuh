@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "se.h"
@@ -45,6 +46,20 @@ inline cudaError_t se_launch(void (*kernel)(K...), dim3 grid, dim3 block, size_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+// Dynamic shared memory above 48 KB is allowed per kernel and per device:
+// sets the limit the first time `kernel` is launched on the current device.
+// `done` holds one bit per device (devices past 64 set it on every call).
+inline bool allow_smem(const void* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  if (bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return true;
 }
 
 // First-writer-wins device error word.

@@ -617,13 +617,9 @@ __global__ void __launch_bounds__(128) evict_one_kernel(SelectArgs a, const int3
 template <int ITEMS>
 static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_t st) {
   const size_t smem = (size_t)(1024 * (ITEMS + 1) + 64) * sizeof(float);
-  static bool attr_set = false;  // per device is enough here: set before first launch
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_kernel<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return SE_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (!allow_smem(reinterpret_cast<const void*>(&topk_kernel<ITEMS>), (int)smem, attr))
+    return SE_ERR_CUDA;
   se_launch(topk_kernel<ITEMS>, dim3(a.Hkv, a.B), 1024, smem, st, a, pool, k);
   return SE_OK;
 }
@@ -631,13 +627,9 @@ static se_status launch_topk_t(const SelectArgs& a, int pool, int k, cudaStream_
 template <int ITEMS, int HALO>
 static se_status launch_topk_cluster_h(const SelectArgs& a, int pool, int k, cudaStream_t st) {
   const size_t smem = (size_t)(1024 * (ITEMS + 1) + 64) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_cluster_kernel<ITEMS, HALO>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SE_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (!allow_smem(reinterpret_cast<const void*>(&topk_cluster_kernel<ITEMS, HALO>), (int)smem, attr))
+    return SE_ERR_CUDA;
   se_launch(topk_cluster_kernel<ITEMS, HALO>, dim3(kClusterCTAs * a.Hkv, a.B), 1024, smem, st, a,
             pool, k);
   return SE_OK;
