@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   char* kpw = static_cast<char*>(kv.k_pool);
   char* vpw = static_cast<char*>(kv.v_pool);
   constexpr int EPP = 256 / CHUNKS;  // entries per pass
-  constexpr int PASSES = 4;          // entries_per_cta == EPP * PASSES
+  constexpr int PASSES = 2;          // entries_per_cta == EPP * PASSES
   const int sub = threadIdx.x / CHUNKS, ch = threadIdx.x % CHUNKS;
   const int64_t tmp_base = ((int64_t)b * kv.Hkv + h) * w.row;
   // all loads of this thread first (PASSES x (K, V) 16-byte rows in flight), then the stores
@@ -835,22 +835,23 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
   const int row_bytes = kv->D * (int)elem_size(kv->dtype);
   const int chunks = row_bytes / 16;
   const int max_entries = max_keep + kv->page_size;
-  // entries per CTA = (256 / chunks) rows per pass x 4 passes
+  // entries per CTA = (256 / chunks) rows per pass x 2 passes (more, smaller CTAs measured
+  // faster than 4 or 8 passes for both the SnapKV compaction and the Kara prune)
   switch (chunks) {
     case 8: {
-      const int epc = 4 * (256 / 8);
+      const int epc = 2 * (256 / 8);
       se_launch(compact_gather_kernel<8>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
     }
     case 16: {
-      const int epc = 4 * (256 / 16);
+      const int epc = 2 * (256 / 16);
       se_launch(compact_gather_kernel<16>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
     }
     case 32: {
-      const int epc = 4 * (256 / 32);
+      const int epc = 2 * (256 / 32);
       se_launch(compact_gather_kernel<32>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
       break;
