@@ -172,6 +172,19 @@ def test_topk_with_pool_brute_force():
     assert list(keep) == sorted(ranked) + [60, 61, 62, 63]
 
 
+def test_topk_window_sum_ranks_as_window_mean():
+    """The device ranks pooled candidates by the zero-padded window sum; the
+    pages define the window mean.  Dividing by the fixed width keeps the order,
+    so the kept slots are the same (window sums taken here by convolution)."""
+    rng = np.random.default_rng(11)
+    for n, k, pool in [(200, 31, 7), (64, 10, 3), (129, 1, 5)]:
+        s = rng.random(n)
+        sums = np.convolve(s, np.ones(pool), mode="same")
+        ranked = sorted(range(n), key=lambda j: (-sums[j], j))[:k]
+        keep = selection.topk_keep(s, 0, k, pool, n, n)
+        assert list(keep) == sorted(ranked)
+
+
 def test_topk_all_equal_keeps_lowest_and_forced_overlap():
     keep = selection.topk_keep(np.ones(30), 0, 5, 1, 30, 32)
     assert list(keep) == [0, 1, 2, 3, 4, 30, 31]
