@@ -105,6 +105,15 @@ def test_compact_prune_decode_quest_argument_checks():
         se.SE_ERR_INVALID_ARG                              # more blocks than the table holds
 
 
+def test_decode_rejects_pools_past_32_bit_row_indices():
+    # K/V rows are indexed with 32-bit integers: a pool of 2^27 pages x 2 heads x 16
+    # rows is refused on the host, before any launch
+    d, _ = kv(num_pages=1 << 27)
+    dws = 1 << 30
+    assert L.se_sparse_decode_attn(d, FAKE, 0, None, 0, 0, 128, FAKE, None, 0, FAKE, dws, None) == \
+        se.SE_ERR_UNSUPPORTED
+
+
 def test_static_scratch_variant_checks_size_before_anything():
     d, _ = kv(B=64, Hkv=8, Hq=32)
     assert L.se_sparse_decode_attn_static(d, FAKE, 0, None, 0, 0, 1 << 22, FAKE, None, 0, None) == \
