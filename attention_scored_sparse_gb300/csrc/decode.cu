@@ -456,7 +456,7 @@ struct StagedGeom {
   static constexpr int SE = 8 * E;                 // entries per stage
   static constexpr int RB = D * (int)sizeof(T);    // bytes per K (or V) row
   static constexpr int STAGE_BYTES = SE * RB * 2;
-  // three 16 KB stages keep four CTAs (sixteen warps) on an SM with 127 registers a thread
+  // three 16 KB stages keep four CTAs (sixteen warps) on an SM at 128 registers a thread
   static constexpr int STAGES =
       STAGE_BYTES <= 8192 ? 4 : (STAGE_BYTES <= 16384 ? 3 : (STAGE_BYTES <= 32768 ? 2 : 0));
   static constexpr int SMEM = STAGES * STAGE_BYTES + 128;   // + alignment of the stages to 128 B
