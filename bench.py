@@ -5,8 +5,9 @@ Default workload (the headline metric "KV tokens scored+compacted/s"): the
 Llama-3.1-8B-shaped layer at the end of prefill -- 4 sequences x 32,768
 tokens, 32 query / 8 KV heads, d=128, bf16, SnapKV window of 64 queries,
 pooling 7, budget 2048 per KV head.  One step = the whole path on one batch:
-window scoring -> pooled top-k -> compaction into fresh pages -> decode
-attention over the retained view.  Inputs are synthetic (seeded N(0,1) with
+window scoring -> pooled top-k -> compaction into fresh pages and decode
+attention over the retained entries (the two side by side on two streams,
+as the pipeline runs them).  Inputs are synthetic (seeded N(0,1) with
 1% of keys offset by 3 sigma along a random direction) and resident in HBM;
 the KV cache (570 MB) is larger than L2, so no flush is needed between steps.
 Before each step the cache's metadata (block table, slot map, lengths, free
