@@ -788,6 +788,7 @@ def main():
     }
     if r.get("e2e"):
         e2e_ms, bi, bo = r["e2e"]
+        e2e_ms = max_over_ranks(e2e_ms, world, "cuda")     # the slowest rank, like the step time
         line["e2e"] = {"value": r["tokens"] * world / (e2e_ms * 1e-3), "unit": unit,
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
