@@ -200,13 +200,25 @@ class H2O(_Base):
         self.ws_append = self._ws(sz["append_kv"])
 
     def prefill(self, q_prompt, q_pos, stream=None):
+        self.prefill_score(q_prompt, q_pos, stream)
+        self.prefill_select(stream)
+        self.prefill_compact(stream)
+
+    def prefill_score(self, q_prompt, q_pos, stream=None):
+        """Causal scores of the whole prompt into the running scores."""
         se_score_window(self.kv, q_prompt, q_pos, self.zero, self.ctx_t, self.zero, self.ctx_t,
                         causal=True, accumulate=False, n_max=self.prompt, scores=self.acc,
                         workspace=self.ws_score, stream=stream)
+
+    def prefill_select(self, stream=None):
+        """Top ``heavy`` of the non-recent prompt plus the ``recent`` tokens."""
         se_topk_select(self.kv, self.acc, mode=SE_SELECT_TOPK, cand_lo=self.zero,
                        cand_hi=self.cand_t, force_lo=self.cand_t, force_hi=self.ctx_t,
                        keep_idx=self.keep, n_keep=self.n_keep, pool_kernel=1, k=self.heavy,
                        n_max=self.prompt - self.recent, stream=stream)
+
+    def prefill_compact(self, stream=None):
+        """Compaction of the kept entries from slot 0, scores moving along."""
         se_compact_evict(self.kv, SE_COMPACT_FRESH_PAGES, self.keep, n_keep=self.n_keep,
                          first_slot=self.zero, max_keep=self.budget, aux=self.acc,
                          workspace=self.ws_compact, stream=stream)

@@ -22,48 +22,84 @@ def to_f64(t) -> np.ndarray:
     return np.asarray(t, dtype=np.float64)
 
 
-def snapkv(c: Cache, q_win, q_pos, q_dec, shape):
-    """SnapKV after the last prompt chunk: score, pool + top-k, compact, decode."""
+def snapkv_select(c: Cache, q_win, q_pos, shape):
+    """SnapKV after the last prompt chunk, first half: window scores of the
+    scored prefix and the pooled top-k plus the window, per KV head."""
     B, ctx, w = c.B, int(c.ctx_len[0]), shape.window
     scored = ctx - w
     s = scoring.score_window(c, q_win, q_pos, [0] * B, [ctx] * B, [0] * B, [scored] * B,
                              causal=True)
     keep = [[selection.topk_keep(s[(b, h)], 0, shape.keep_topk, shape.pool_kernel, scored, ctx)
              for h in range(c.Hkv)] for b in range(B)]
-    st = cache.compact(c, keep, [0] * B)
+    return dict(scores=s, keep=keep)
+
+
+def snapkv_finish(c: Cache, keep, q_dec, groups=None):
+    """Second half: compaction of the kept entries from slot 0, then decode
+    attention of one query per head over the compacted cache."""
+    st = cache.compact(c, keep, [0] * c.B)
     assert st == cache.SE_OK
-    o, _ = attention.decode_attention(c, to_f64(q_dec), "dense")
-    return dict(scores=s, keep=keep, o=o)
+    o, _ = attention.decode_attention(c, to_f64(q_dec), "dense", groups=groups)
+    return o
 
 
-def quest_step(c: Cache, kmin, kmax, q, top_pages: int, groups=None):
-    """One Quest decode step: page bound, top pages + current page, attention."""
+def snapkv(c: Cache, q_win, q_pos, q_dec, shape):
+    """SnapKV after the last prompt chunk: score, pool + top-k, compact, decode."""
+    r = snapkv_select(c, q_win, q_pos, shape)
+    r["o"] = snapkv_finish(c, r["keep"], q_dec)
+    return r
+
+
+def quest_select(c: Cache, kmin, kmax, q, top_pages: int, groups=None):
+    """Quest page selection of one decode step: page bounds, top pages plus
+    the current page, per (sequence, KV group)."""
     qv = to_f64(q)
     pairs = groups if groups is not None else [(b, g) for b in range(c.B) for g in range(c.Hkv)]
     sel = {}
     bounds = {}
     for b, g in pairs:
         sel[(b, g)], bounds[(b, g)] = quest.select_pages(c, kmin, kmax, qv[b], top_pages, b, g)
+    return dict(sel=sel, bounds=bounds)
+
+
+def quest_attend(c: Cache, q, sel: dict):
+    """Decode attention of one Quest step over the pages ``sel[(b, g)]``."""
+    pairs = list(sel)
     selb = {b: {g: sel[(b, g)] for (bb, g) in sel if bb == b} for b in {p[0] for p in pairs}}
-    o, _ = attention.decode_attention(c, qv, "pages", selb, groups=pairs)
-    return dict(sel=sel, bounds=bounds, o=o)
+    o, _ = attention.decode_attention(c, to_f64(q), "pages", selb, groups=pairs)
+    return o
+
+
+def quest_step(c: Cache, kmin, kmax, q, top_pages: int, groups=None):
+    """One Quest decode step: page bound, top pages + current page, attention."""
+    r = quest_select(c, kmin, kmax, q, top_pages, groups)
+    r["o"] = quest_attend(c, q, r["sel"])
+    return r
+
+
+def h2o_prefill_select(c: Cache, q_prompt, q_pos, shape, acc: np.ndarray, groups=None):
+    """H2O at the end of prefill, reading (viii), first half: causal scores
+    of the whole prompt become the initial running scores; keep the top
+    ``heavy`` of the non-recent prefix plus the ``recent`` last tokens."""
+    B, ctx = c.B, int(c.ctx_len[0])
+    s = scoring.score_window(c, q_prompt, q_pos, [0] * B, [ctx] * B, [0] * B, [ctx] * B,
+                             causal=True, groups=groups)
+    for (b, h), v in s.items():
+        acc[b, h, :ctx] = v
+    keep = [[None] * c.Hkv for _ in range(B)]
+    for (b, h), v in s.items():
+        keep[b][h] = selection.topk_keep(v[: ctx - shape.recent], 0, shape.heavy, 1,
+                                         ctx - shape.recent, ctx)
+    return dict(scores=s, keep=keep)
 
 
 def h2o_prefill(c: Cache, q_prompt, q_pos, shape, acc: np.ndarray):
-    """H2O at the end of prefill, reading (viii): causal scores of the whole
-    prompt become the initial running scores; keep the top ``heavy`` of the
-    non-recent prefix plus the ``recent`` last tokens."""
-    B, ctx = c.B, int(c.ctx_len[0])
-    s = scoring.score_window(c, q_prompt, q_pos, [0] * B, [ctx] * B, [0] * B, [ctx] * B,
-                             causal=True)
-    for (b, h), v in s.items():
-        acc[b, h, :ctx] = v
-    keep = [[selection.topk_keep(s[(b, h)][: ctx - shape.recent], 0, shape.heavy, 1,
-                                 ctx - shape.recent, ctx)
-             for h in range(c.Hkv)] for b in range(B)]
-    st = cache.compact(c, keep, [0] * B, aux=acc)
+    """H2O at the end of prefill: scores, selection, compaction from slot 0
+    (the running scores move with their entries)."""
+    r = h2o_prefill_select(c, q_prompt, q_pos, shape, acc)
+    st = cache.compact(c, r["keep"], [0] * c.B, aux=acc)
     assert st == cache.SE_OK
-    return dict(scores=s, keep=keep)
+    return r
 
 
 def h2o_prefill_chunk(c: Cache, acc: np.ndarray, q_chunk, q_pos, k_chunk, v_chunk,
@@ -96,22 +132,39 @@ def h2o_prefill_chunk(c: Cache, acc: np.ndarray, q_chunk, q_pos, k_chunk, v_chun
     return dict(acc_pre=acc_pre, keep=keep)
 
 
-def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
-    """One H2O decode step: append, dense attention, add this step's
-    group-summed weights to the running scores, evict one if over budget."""
+def h2o_step_attend(c: Cache, acc: np.ndarray, q, k_new, v_new, groups=None):
+    """First half of an H2O decode step: append this step's key and value,
+    dense attention over the resident entries, and this step's group-summed
+    weights added to the running scores (the new entry starts at its own
+    weight).  ``groups`` limits the float work to those (sequence, KV head)
+    pairs; the append is done for every sequence."""
     kb, vb = cache._bits(k_new), cache._bits(v_new)
     st = cache.append(c, kb, vb, aux=acc)
     assert st == cache.SE_OK
-    o, psums = attention.decode_attention(c, to_f64(q), "dense")
+    o, psums = attention.decode_attention(c, to_f64(q), "dense", groups=groups)
     for (b, g), (slots, p) in psums.items():
         acc[b, g, slots] += p
-    acc_pre = acc.copy()
+    return o
+
+
+def h2o_victims(c: Cache, acc: np.ndarray, shape, seqs=None) -> np.ndarray:
+    """Evict-one choice per (sequence, KV head) after the scores are added
+    (-1: within budget); sequences outside ``seqs`` get -1."""
     victim = np.full((c.B, c.Hkv), -1, dtype=np.int64)
-    for b in range(c.B):
+    for b in (range(c.B) if seqs is None else seqs):
         recent_from = int(c.logical_len[b]) - shape.recent
         for g in range(c.Hkv):
             victim[b, g] = selection.h2o_victim(acc[b, g], c.slot_map[b, g], int(c.ctx_len[b]),
                                                 shape.budget, recent_from)
+    return victim
+
+
+def h2o_step(c: Cache, acc: np.ndarray, q, k_new, v_new, shape):
+    """One H2O decode step: append, dense attention, add this step's
+    group-summed weights to the running scores, evict one if over budget."""
+    o = h2o_step_attend(c, acc, q, k_new, v_new)
+    acc_pre = acc.copy()
+    victim = h2o_victims(c, acc, shape)
     st = cache.move_last(c, victim, aux=acc)
     assert st == cache.SE_OK
     return dict(o=o, victim=victim, acc_pre=acc_pre)

@@ -50,8 +50,9 @@ def random_keep(c: ocache.Cache, seed: int, first=None, frac=None):
     return keep, firsts
 
 
-def assert_cache_equal(pc, c: ocache.Cache, seqs=None, data=True):
-    """GPU cache tensors == oracle cache, bit for bit."""
+def assert_cache_equal(pc, c: ocache.Cache, seqs=None, data=True, data_seqs=None):
+    """GPU cache tensors == oracle cache, bit for bit.  Slot maps of ``seqs``
+    (every sequence by default), K/V bytes of ``data_seqs`` (default: seqs)."""
     np.testing.assert_array_equal(pc.block_table.cpu().numpy(), c.block_table)
     np.testing.assert_array_equal(pc.ctx_len.cpu().numpy(), c.ctx_len)
     np.testing.assert_array_equal(pc.logical_len.cpu().numpy(), c.logical_len)
@@ -64,7 +65,7 @@ def assert_cache_equal(pc, c: ocache.Cache, seqs=None, data=True):
     for b in bs:
         np.testing.assert_array_equal(sm[b], c.slot_map[b])
     if data:
-        for b in bs:
+        for b in (bs if data_seqs is None else data_seqs):
             ctx = int(c.ctx_len[b])
             if ctx == 0:
                 continue

@@ -41,11 +41,32 @@ def _check_out(o_gpu, oracle_o, dtype, G):
 # ---------------------------------------------------------------------------
 
 
+def _gpu_keep_after_ties(kg, ref_keep, rankings, k, forced):
+    """The GPU's kept sets, each checked against the oracle's: equal, or
+    different only at oracle near-ties of the k-th score (then the GPU's set
+    is an equally valid answer and the later stages follow it).  Returns the
+    kept lists and the number of (sequence, head) pairs that differed."""
+    keep, resynced = [], 0
+    for b in range(len(ref_keep)):
+        kb = []
+        for h in range(len(ref_keep[b])):
+            d = H.assert_keep_near(kg[b, h], ref_keep[b][h], rankings[(b, h)], k, forced)
+            resynced += d > 0
+            kb.append(np.asarray(kg[b, h], dtype=np.int64))
+        keep.append(kb)
+    return keep, resynced
+
+
 def _snapkv(cuda_lib, shape):
+    """Scores element-wise, kept sets under the tie rule, then compaction and
+    decode of the oracle on the kept sets the GPU chose (equal to the
+    oracle's or differing only at near-ties): the cache bit for bit and the
+    decode output always compared.  Returns the number of re-synchronised
+    (sequence, KV head) pairs."""
     inp = W.snapkv_inputs(shape, "cuda")
     pc = inp["cache"]
     c = ocache.from_tensors(pc)
-    ref = opipe.snapkv(c, inp["q_win"], inp["q_pos"].cpu().numpy(), inp["q_dec"], shape)
+    ref = opipe.snapkv_select(c, inp["q_win"], inp["q_pos"].cpu().numpy(), shape)
     pipe = P.SnapKV(pc, shape.Hq, ctx=shape.ctx, window=shape.window, budget=shape.budget,
                     pool_kernel=shape.pool_kernel)
     o = torch.empty_like(inp["q_dec"])
@@ -53,23 +74,19 @@ def _snapkv(cuda_lib, shape):
     pipe.select()
     torch.cuda.synchronize()
     _check_scores(pipe.scores, ref["scores"], [0] * shape.B, shape.dtype, shape.window, shape.G)
-    kg = pipe.keep.cpu().numpy()
-    diffs = 0
-    for b in range(shape.B):
-        for h in range(shape.Hkv):
-            s_o = ref["scores"][(b, h)]
-            ranking = H.pooled_scores(s_o, 0, shape.pool_kernel)
-            diffs += H.assert_keep_near(kg[b, h], ref["keep"][b][h], ranking, shape.keep_topk,
-                                        range(shape.scored, shape.ctx))
+    rankings = {(b, h): H.pooled_scores(ref["scores"][(b, h)], 0, shape.pool_kernel)
+                for b in range(shape.B) for h in range(shape.Hkv)}
+    keep, resynced = _gpu_keep_after_ties(pipe.keep.cpu().numpy(), ref["keep"], rankings,
+                                          shape.keep_topk, range(shape.scored, shape.ctx))
+    o_ref = opipe.snapkv_finish(c, keep, inp["q_dec"])
     pipe.compact()
     pipe.decode(inp["q_dec"], o)
     torch.cuda.synchronize()
     assert H.status(pc) == 0
-    if diffs == 0:
-        H.assert_cache_equal(pc, c)
-        _check_out(o, ref["o"], shape.dtype, shape.G)
+    H.assert_cache_equal(pc, c)
+    _check_out(o, o_ref, shape.dtype, shape.G)
     assert (pc.ctx_len.cpu() == shape.budget).all()
-    return diffs
+    return resynced
 
 
 def test_snapkv_tiny_workload(cuda_lib):
@@ -77,7 +94,7 @@ def test_snapkv_tiny_workload(cuda_lib):
 
 
 def test_snapkv_llama8b_reduced(cuda_lib):
-    _snapkv(cuda_lib, W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512))
+    assert _snapkv(cuda_lib, W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512)) <= 2
 
 
 def test_snapkv_step_decodes_beside_compaction(cuda_lib):
@@ -113,8 +130,9 @@ def test_snapkv_step_decodes_beside_compaction(cuda_lib):
 
 @pytest.mark.slow
 def test_snapkv_llama8b_full(cuda_lib):
-    """4 x 32768 tokens, 32/8 heads, budget 2048: full oracle (about 30 s)."""
-    _snapkv(cuda_lib, W.snapkv_llama8b())
+    """4 x 32768 tokens, 32/8 heads, budget 2048: full oracle (about 30 s).
+    At most a few (sequence, KV head) pairs may follow a near-tie."""
+    assert _snapkv(cuda_lib, W.snapkv_llama8b()) <= 4
 
 
 # ---------------------------------------------------------------------------
@@ -123,6 +141,9 @@ def test_snapkv_llama8b_full(cuda_lib):
 
 
 def _quest(cuda_lib, shape, steps, fused=False):
+    """Page bounds' metadata bit for bit; per step the selected pages under
+    the tie rule, then the oracle's attention over the pages the GPU chose
+    (the oracle's own or a near-tie alternative) for every (sequence, head)."""
     inp = W.quest_inputs(shape, "cuda")
     pc = inp["cache"]
     c = ocache.from_tensors(pc)
@@ -141,22 +162,18 @@ def _quest(cuda_lib, shape, steps, fused=False):
         pipe.page_idx.fill_(-7)
         (pipe.step_fused if fused else pipe.step)(q, o)
         torch.cuda.synchronize()
-        ref = opipe.quest_step(c, kmin, kmax, q, shape.top_pages)
+        ref = opipe.quest_select(c, kmin, kmax, q, shape.top_pages)
         got = pipe.page_idx.cpu().numpy()
-        same = {}
+        sel_gpu = {}
         for (b, g), sel in ref["sel"].items():
             U = ref["bounds"][(b, g)]
             ranking = {i: float(U[i]) for i in range(nb - 1)}
             row = got[b, g]
             n = len(sel)
             assert (row[n:] == -1).all(), (b, g, row)     # -1 after the selected pages
-            d = H.assert_keep_near(row[:n], sel, ranking, min(shape.top_pages, nb - 1), [nb - 1])
-            same[(b, g)] = d == 0
-        og = o.double().cpu().numpy()
-        for (b, g), ref_o in ref["o"].items():
-            if same[(b, g)]:
-                err = np.abs(og[b, g * shape.G:(g + 1) * shape.G] - ref_o).max()
-                assert err <= H.OUT_ATOL[shape.dtype]
+            H.assert_keep_near(row[:n], sel, ranking, min(shape.top_pages, nb - 1), [nb - 1])
+            sel_gpu[(b, g)] = np.asarray(row[:n], dtype=np.int64)
+        _check_out(o, opipe.quest_attend(c, q, sel_gpu), shape.dtype, shape.G)
     assert H.status(pc) == 0
     # Quest keeps the whole history resident
     assert (pc.ctx_len.cpu() == shape.ctx).all()
@@ -188,76 +205,109 @@ def test_quest_full(cuda_lib, fused):
 # ---------------------------------------------------------------------------
 
 
-def _h2o_lockstep(cuda_lib, shape, steps, check_every=1):
+def _h2o_lockstep(cuda_lib, shape, steps, seqs=None, data_every=1):
+    """H2O end to end in lock-step with the oracle.
+
+    Prompt: causal scores of the whole prompt (element-wise on the sampled
+    sequences ``seqs``, every sequence by default), the kept sets under the
+    tie rule, then the oracle's compaction on the kept sets the GPU chose --
+    its own or a near-tie alternative -- bit for bit over every sequence.
+    Decode: each step's output and running scores on the sampled sequences,
+    their victims under the tie rule (a near-tie re-synchronises the oracle
+    to the GPU's victim), and the cache's integer state (block table, slot
+    maps, lengths, free list) of every sequence after every step; K/V bytes
+    of the sampled sequences every step and of all every ``data_every``
+    steps.  Sequences outside the sample follow the GPU's kept sets and
+    victims, checked by their properties (count, order, forced range, the
+    recent boundary).  Returns the number of re-synchronised choices."""
     inp = W.h2o_inputs(shape, "cuda", steps=steps)
     pc = inp["cache"]
     c = ocache.from_tensors(pc)
+    B, Hkv, ctx = shape.B, shape.Hkv, shape.ctx
+    sampled = list(range(B)) if seqs is None else list(seqs)
+    groups = [(b, g) for b in sampled for g in range(Hkv)]
     acc_o = np.zeros(c.slot_map.shape)
-    ref = opipe.h2o_prefill(c, inp["q_prompt"], inp["q_pos"].cpu().numpy(), shape, acc_o)
-    pipe = P.H2O(pc, shape.Hq, prompt=shape.ctx, heavy=shape.heavy, recent=shape.recent)
-    pipe.prefill(inp["q_prompt"], inp["q_pos"])
+    ref = opipe.h2o_prefill_select(c, inp["q_prompt"], inp["q_pos"].cpu().numpy(), shape, acc_o,
+                                   groups=groups)
+    pipe = P.H2O(pc, shape.Hq, prompt=ctx, heavy=shape.heavy, recent=shape.recent)
+    pipe.prefill_score(inp["q_prompt"], inp["q_pos"])
+    torch.cuda.synchronize()
+    sg = pipe.acc[sampled].cpu().double().numpy()
+    for i, b in enumerate(sampled):
+        for g in range(Hkv):
+            H.assert_scores_close(sg[i, g, :ctx], ref["scores"][(b, g)], shape.dtype, ctx, shape.G)
+    pipe.prefill_select()
+    torch.cuda.synchronize()
+    kg = pipe.keep.cpu().numpy()
+    recent = range(ctx - shape.recent, ctx)
+    resynced = 0
+    keep = []
+    for b in range(B):
+        kb = []
+        for h in range(Hkv):
+            if b in sampled:
+                s_o = ref["scores"][(b, h)]
+                ranking = {j: float(s_o[j]) for j in range(ctx - shape.recent)}
+                resynced += H.assert_keep_near(kg[b, h], ref["keep"][b][h], ranking, shape.heavy,
+                                               recent) > 0
+            else:
+                row = [int(x) for x in kg[b, h]]
+                assert row == sorted(set(row)) and len(row) == shape.budget
+                assert set(recent) <= set(row) and 0 <= row[0]
+            kb.append(np.asarray(kg[b, h], dtype=np.int64))
+        keep.append(kb)
+    pipe.prefill_compact()
+    assert ocache.compact(c, keep, [0] * B, aux=acc_o) == ocache.SE_OK
     torch.cuda.synchronize()
     assert H.status(pc) == 0
-    kg = pipe.keep.cpu().numpy()
-    diverged = 0
-    for b in range(shape.B):
-        for h in range(shape.Hkv):
-            s_o = ref["scores"][(b, h)]
-            ranking = {j: float(s_o[j]) for j in range(shape.ctx - shape.recent)}
-            diverged += H.assert_keep_near(kg[b, h], ref["keep"][b][h], ranking, shape.heavy,
-                                           range(shape.ctx - shape.recent, shape.ctx))
-    if diverged:
-        pytest.skip("legitimate near-tie in the prompt selection; lock-step not comparable")
     H.assert_cache_equal(pc, c)
-    np.testing.assert_allclose(pipe.acc.cpu().double().numpy(), acc_o, rtol=1e-3, atol=1e-9)
+    np.testing.assert_allclose(pipe.acc[sampled].cpu().double().numpy(), acc_o[sampled],
+                               rtol=1e-3, atol=1e-9)
     for t in range(steps):
         o = torch.empty_like(inp["q_steps"][t])
         pipe.step(inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], o)
-        r = opipe.h2o_step(c, acc_o, inp["q_steps"][t], inp["k_steps"][t], inp["v_steps"][t], shape)
+        o_ref = opipe.h2o_step_attend(c, acc_o, inp["q_steps"][t], inp["k_steps"][t],
+                                      inp["v_steps"][t], groups=groups)
+        v_o = opipe.h2o_victims(c, acc_o, shape, seqs=sampled)
         torch.cuda.synchronize()
         assert H.status(pc) == 0
-        vg = pipe.victim.cpu().numpy()
-        if not (vg == r["victim"]).all():
-            # only a near-tie of the oracle's running scores may differ
-            for b, g in zip(*np.nonzero(vg != r["victim"])):
-                a = r["acc_pre"][b, g]
-                x, y = a[vg[b, g]], a[r["victim"][b, g]]
-                assert abs(x - y) <= H.TIE_REL * abs(y), (t, b, g, x, y)
-            return t        # lock-step cannot continue past a legitimate tie
-        if t % check_every == 0 or t == steps - 1:
-            H.assert_cache_equal(pc, c)
-            np.testing.assert_allclose(pipe.acc.cpu().double().numpy(), acc_o, rtol=1e-3, atol=1e-7)
-            _check_out(o, r["o"], shape.dtype, shape.G)
+        vg = pipe.victim.cpu().numpy().astype(np.int64)
+        for b in range(B):
+            n = int(c.ctx_len[b])
+            if b in sampled:
+                for g in np.nonzero(vg[b] != v_o[b])[0]:
+                    # only a near-tie of the oracle's running scores may differ
+                    x, y = acc_o[b, g, vg[b, g]], acc_o[b, g, v_o[b, g]]
+                    assert abs(x - y) <= H.TIE_REL * abs(y), (t, b, g, x, y)
+                    resynced += 1
+            elif n <= shape.budget:
+                assert (vg[b] == -1).all(), (t, b)
+            else:
+                assert ((vg[b] >= 0) & (vg[b] < n)).all(), (t, b, vg[b])
+                pos = c.slot_map[b, np.arange(Hkv), vg[b]]
+                assert (pos < int(c.logical_len[b]) - shape.recent).all(), (t, b)
+        assert ocache.move_last(c, vg, aux=acc_o) == ocache.SE_OK
+        full = (t + 1) % data_every == 0 or t == steps - 1
+        H.assert_cache_equal(pc, c, data_seqs=None if full else sampled)
+        np.testing.assert_allclose(pipe.acc[sampled].cpu().double().numpy(), acc_o[sampled],
+                                   rtol=1e-3, atol=1e-7)
+        _check_out(o, o_ref, shape.dtype, shape.G)
     assert (pc.ctx_len.cpu() == shape.budget).all()
-    return steps
+    return resynced
 
 
 def test_h2o_reduced_lockstep(cuda_lib):
     shape = W.h2o_decode(B=3, ctx=300, heavy=100, recent=20, steps=40)
-    _h2o_lockstep(cuda_lib, shape, 40)
+    assert _h2o_lockstep(cuda_lib, shape, 40) <= 2
 
 
-def test_h2o_full_prompt_scores_sampled(cuda_lib):
-    """Full H2O prompt (64 x 4096 causal, 32/8 heads): GPU scores of every
-    group, oracle on two sampled groups."""
+@pytest.mark.slow
+def test_h2o_full_end_to_end(cuda_lib):
+    """The full H2O workload: 64 x 4096-token prompts compressed to 1024 +
+    128, then 512 decode steps with evict-one; float results on sequences 0,
+    31 and 63, integer state of all 64 after every step."""
     shape = W.h2o_decode()
-    inp = W.h2o_inputs(shape, "cuda", steps=1)
-    pc = inp["cache"]
-    c = ocache.from_tensors(pc, seqs=[0, 63])
-    pipe = P.H2O(pc, shape.Hq, prompt=shape.ctx, heavy=shape.heavy, recent=shape.recent)
-    from attention_scored_sparse_gb300 import se_score_window
-    se_score_window(pipe.kv, inp["q_prompt"], inp["q_pos"], pipe.zero, pipe.ctx_t, pipe.zero,
-                    pipe.ctx_t, causal=True, accumulate=False, n_max=shape.ctx, scores=pipe.acc,
-                    workspace=pipe.ws_score)
-    torch.cuda.synchronize()
-    G = shape.G
-    q_pos = inp["q_pos"].cpu().numpy()
-    sg = pipe.acc.cpu().double().numpy()
-    for b, g in [(0, 0), (63, 7)]:
-        Q = opipe.to_f64(inp["q_prompt"][b, :, g * G:(g + 1) * G, :])
-        K = c.keys(b, g, np.arange(shape.ctx))
-        row = oscore.group_scores(Q, q_pos[b], K, c.slot_map[b, g, :shape.ctx], True)
-        H.assert_scores_close(sg[b, g, :shape.ctx], row, shape.dtype, shape.ctx, G)
+    assert _h2o_lockstep(cuda_lib, shape, shape.steps, seqs=[0, 31, 63], data_every=64) <= 8
 
 
 def test_h2o_full_decode_lockstep_from_generated_state(cuda_lib):

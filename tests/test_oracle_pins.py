@@ -229,6 +229,61 @@ def test_kara_contiguous_candidates_reduce_to_topk():
     assert list(keep) == sorted(ranked)
 
 
+def _kara_tiny():
+    shape = W.kara_prune(B=2, Hq=4, Hkv=2, D=16, page_size=4, ctx=64, window=16, protected=4,
+                         candidates=4, budget=6, prune_L=8, prune_R=24, dtype=torch.float32,
+                         name="kara_pin")
+    return shape, W.kara_inputs(shape, "cpu")
+
+
+def test_kara_compress_identical_keys_softmax_spans_the_whole_window():
+    # KARA Method 1: every window query attends to every window key, the
+    # protected tail included; only the compressible columns are scored.
+    # With one key vector per head each row gives 1/window to every window
+    # key, so each compressible score is G * w / window -- and G * w /
+    # (window - protected) if the protected keys were left out of the softmax.
+    shape, inp = _kara_tiny()
+    pc = inp["cache"]
+    _set_identical_keys(pc)
+    c = oc(pc)
+    r = pipelines.kara_compress(c, inp["q_win"], inp["q_pos"].numpy(), shape)
+    win_lo = shape.ctx - shape.window
+    assert r["first_slot"] == [win_lo] * shape.B
+    for (b, h), sv in r["scores"].items():
+        assert len(sv) == shape.compressible
+        np.testing.assert_allclose(sv, shape.G * shape.window / shape.window, rtol=1e-12)
+        # all scores tie: the candidates are the lowest compressible slots,
+        # contiguous, so no chunk has an interior and the top-up takes the
+        # next lowest slots; the protected tail follows
+        expect = list(range(win_lo, win_lo + shape.budget)) + \
+            list(range(shape.ctx - shape.protected, shape.ctx))
+        assert list(r["keep"][b][h]) == expect
+
+
+def test_kara_compress_scores_are_library_attention_over_the_window():
+    # column sums of torch SDPA probabilities (V = I) over the full window,
+    # no mask, restricted to the compressible columns; the kept set is
+    # Token2Chunk of those scores over [win_lo, ctx - protected) plus the tail
+    shape, inp = _kara_tiny()
+    c = oc(inp["cache"])
+    r = pipelines.kara_compress(c, inp["q_win"], inp["q_pos"].numpy(), shape)
+    win_lo, prot_lo = shape.ctx - shape.window, shape.ctx - shape.protected
+    for b in range(shape.B):
+        for g in range(shape.Hkv):
+            K = c.keys(b, g, range(win_lo, shape.ctx))
+            total = np.zeros(shape.window)
+            for h in range(g * shape.G, (g + 1) * shape.G):
+                total += sdpa_probs(inp["q_win"][b, :, h, :].double().numpy(), K).sum(axis=0)
+            want = total[: prot_lo - win_lo]
+            np.testing.assert_allclose(r["scores"][(b, g)], want, rtol=1e-12, atol=1e-15)
+            # the protected columns carry real probability mass, so leaving them
+            # out of the softmax would change every score above
+            assert total[prot_lo - win_lo:].sum() > 1e-3 * total.sum()
+            kept = selection.kara_keep(want, win_lo, shape.candidates, shape.budget,
+                                       shape.chunk_coef, prot_lo, shape.ctx)
+            assert list(r["keep"][b][g]) == list(kept)
+
+
 # ---------------------------------------------------------------------------
 # O5 H2O
 # ---------------------------------------------------------------------------
