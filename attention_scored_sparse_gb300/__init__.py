@@ -34,7 +34,7 @@ SE_VIEW_DENSE, SE_VIEW_PAGES, SE_VIEW_TOKENS = 0, 1, 2
 SE_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 EXPORTED = [
-    "se_score_window", "se_score_window_workspace_size",
+    "se_score_window", "se_score_window_workspace_size", "se_score_window_one_launch",
     "se_topk_select",
     "se_compact_evict", "se_compact_evict_workspace_size",
     "se_prune_span", "se_prune_span_workspace_size",
@@ -82,6 +82,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P = POINTER(se_paged_kv)
     sigs = {
         "se_score_window": [P, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                            c_int32, c_int32, c_int32, c_void_p, c_int64, c_void_p, c_size_t,
+                            c_void_p],
+        "se_score_window_one_launch": [P, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                             c_int32, c_int32, c_int32, c_void_p, c_int64, c_void_p, c_size_t,
                             c_void_p],
         "se_score_window_workspace_size": [P, c_int32, c_int32],
@@ -179,7 +182,9 @@ def kv_desc(cache, Hq: int) -> se_paged_kv:
 
 
 class Workspace:
-    """Caller-owned scratch memory (a torch uint8 tensor), grown on demand."""
+    """Caller-owned scratch memory (a torch uint8 tensor, zeroed when
+    allocated: the scoring call keeps a control block in it that must start
+    at zero), grown on demand."""
 
     def __init__(self, device="cuda"):
         self.device = device
@@ -187,13 +192,13 @@ class Workspace:
 
     def get(self, nbytes: int):
         if self.buf.numel() < nbytes:
-            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
 
 def _ws(ws, nbytes, device):
     if ws is None:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
     elif isinstance(ws, Workspace):
         ws = ws.get(nbytes)
     if ws.numel() < nbytes:
@@ -213,6 +218,19 @@ def se_score_window(kv, q_win, q_pos, attn_lo, attn_hi, out_lo, out_hi, *, causa
     need = _lib.se_score_window_workspace_size(d, w, n_max)
     ws = _ws(workspace, need, scores.device)
     _check("se_score_window", _lib.se_score_window(
+        d, _ptr(q_win), w, _ptr(q_pos), _ptr(attn_lo), _ptr(attn_hi), _ptr(out_lo), _ptr(out_hi),
+        int(causal), int(accumulate), n_max, _ptr(scores), scores.shape[-1], _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def se_score_window_one_launch(kv, q_win, q_pos, attn_lo, attn_hi, out_lo, out_hi, *, causal,
+                               accumulate, n_max, scores, workspace=None, stream=None):
+    """se_score_window with both sweeps in one cooperative launch (see se.h)."""
+    d = ctypes.byref(kv)
+    w = q_win.shape[1]
+    need = _lib.se_score_window_workspace_size(d, w, n_max)
+    ws = _ws(workspace, need, scores.device)
+    _check("se_score_window_one_launch", _lib.se_score_window_one_launch(
         d, _ptr(q_win), w, _ptr(q_pos), _ptr(attn_lo), _ptr(attn_hi), _ptr(out_lo), _ptr(out_hi),
         int(causal), int(accumulate), n_max, _ptr(scores), scores.shape[-1], _ptr(ws), ws.numel(),
         _stream(stream)))

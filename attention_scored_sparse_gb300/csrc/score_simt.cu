@@ -272,7 +272,8 @@ size_t score_tc_ws(const se_paged_kv* kv, int w, int n_max);
 se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const int32_t* q_pos,
                           const int32_t* attn_lo, const int32_t* attn_hi, const int32_t* out_lo,
                           const int32_t* out_hi, int causal, int accumulate, int n_max,
-                          float* scores, int64_t scores_stride, void* ws, cudaStream_t st);
+                          float* scores, int64_t scores_stride, void* ws, cudaStream_t st,
+                          int one_launch);
 
 }  // namespace se
 
@@ -286,12 +287,13 @@ extern "C" size_t se_score_window_workspace_size(const se_paged_kv* kv, int32_t 
   return score_simt_ws(kv, w, n_max, nullptr, nullptr);
 }
 
-extern "C" se_status se_score_window(const se_paged_kv* kv, const void* q_win, int32_t w,
-                                     const int32_t* q_pos, const int32_t* attn_lo,
-                                     const int32_t* attn_hi, const int32_t* out_lo,
-                                     const int32_t* out_hi, int32_t causal, int32_t accumulate,
-                                     int32_t n_max, float* scores, int64_t scores_stride,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
+static se_status score_window_impl(const se_paged_kv* kv, const void* q_win, int32_t w,
+                                   const int32_t* q_pos, const int32_t* attn_lo,
+                                   const int32_t* attn_hi, const int32_t* out_lo,
+                                   const int32_t* out_hi, int32_t causal, int32_t accumulate,
+                                   int32_t n_max, float* scores, int64_t scores_stride,
+                                   void* workspace, size_t workspace_bytes, void* stream,
+                                   int one_launch) {
   se_status s = se_check_kv(kv);
   if (s != SE_OK) return s;
   if (q_win == nullptr || q_pos == nullptr || attn_lo == nullptr || attn_hi == nullptr ||
@@ -302,7 +304,9 @@ extern "C" se_status se_score_window(const se_paged_kv* kv, const void* q_win, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (score_tc_supported(kv)) {
     s = launch_score_tc(kv, q_win, w, q_pos, attn_lo, attn_hi, out_lo, out_hi, causal, accumulate,
-                        n_max, scores, scores_stride, workspace, st);
+                        n_max, scores, scores_stride, workspace, st, one_launch);
+  } else if (one_launch) {
+    return SE_ERR_UNSUPPORTED;
   } else {
     ScoreArgs a{*kv, q_win, w, q_pos, attn_lo, attn_hi, out_lo, out_hi, causal, accumulate,
                 n_max, scores, scores_stride, nullptr, nullptr, 0, 0};
@@ -310,4 +314,27 @@ extern "C" se_status se_score_window(const se_paged_kv* kv, const void* q_win, i
   }
   if (s != SE_OK) return s;
   return se_last_launch_status();
+}
+
+extern "C" se_status se_score_window(const se_paged_kv* kv, const void* q_win, int32_t w,
+                                     const int32_t* q_pos, const int32_t* attn_lo,
+                                     const int32_t* attn_hi, const int32_t* out_lo,
+                                     const int32_t* out_hi, int32_t causal, int32_t accumulate,
+                                     int32_t n_max, float* scores, int64_t scores_stride,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return score_window_impl(kv, q_win, w, q_pos, attn_lo, attn_hi, out_lo, out_hi, causal,
+                           accumulate, n_max, scores, scores_stride, workspace, workspace_bytes,
+                           stream, 0);
+}
+
+extern "C" se_status se_score_window_one_launch(const se_paged_kv* kv, const void* q_win, int32_t w,
+                                                const int32_t* q_pos, const int32_t* attn_lo,
+                                                const int32_t* attn_hi, const int32_t* out_lo,
+                                                const int32_t* out_hi, int32_t causal,
+                                                int32_t accumulate, int32_t n_max, float* scores,
+                                                int64_t scores_stride, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  return score_window_impl(kv, q_win, w, q_pos, attn_lo, attn_hi, out_lo, out_hi, causal,
+                           accumulate, n_max, scores, scores_stride, workspace, workspace_bytes,
+                           stream, 1);
 }

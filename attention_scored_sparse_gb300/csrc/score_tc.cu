@@ -1495,19 +1495,35 @@ bool score_tc_supported(const se_paged_kv* kv) {
 
 constexpr int kMaxPersistentCTAs = 256;   // partial slots per row of the persistent pass 1
 
+size_t score_fused_ws(const se_paged_kv* kv, int w, int n_max);
+size_t score_fused_ctrl_bytes(const se_paged_kv* kv);
+bool score_fused_applicable(const se_paged_kv* kv, int w, int n_max, int n_sm, int smem_optin);
+se_status launch_score_fused(const se_paged_kv* kv, const CUtensorMap& kmap, const CUtensorMap& qmap,
+                             int w, const int32_t* q_pos, const int32_t* attn_lo,
+                             const int32_t* attn_hi, const int32_t* out_lo, const int32_t* out_hi,
+                             int causal, int accumulate, int n_max, float* scores,
+                             int64_t scores_stride, void* ws, int n_sm, cudaStream_t st);
+
+// Workspace: the one-launch scorer's control block first (it must stay zero
+// between calls, so the two-kernel forms carve their buffers after it), then
+// the larger of the two forms' buffers.
 size_t score_tc_ws(const se_paged_kv* kv, int w, int n_max) {
   const TcPlan p = plan(kv, w, n_max);
   WsCarver c(nullptr);
+  c.take<uint8_t>(score_fused_ctrl_bytes(kv));
   const int slots = std::max(2 * p.n_splits, p.RC == 1 ? 2 * kMaxPersistentCTAs : 0);
   c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
-  return c.bytes();
+  return std::max(c.bytes(), score_fused_ws(kv, w, n_max));
 }
 
+// one_launch: 0 -- the two- or three-launch forms; 1 -- both sweeps in one
+// cooperative launch (SE_ERR_UNSUPPORTED when the shape does not allow it).
 se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const int32_t* q_pos,
                           const int32_t* attn_lo, const int32_t* attn_hi, const int32_t* out_lo,
                           const int32_t* out_hi, int causal, int accumulate, int n_max,
-                          float* scores, int64_t scores_stride, void* ws, cudaStream_t st) {
+                          float* scores, int64_t scores_stride, void* ws, cudaStream_t st,
+                          int one_launch) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return SE_ERR_CUDA;
   const int G = kv->Hq / kv->Hkv;
@@ -1544,6 +1560,7 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
   a.causal = causal; a.accumulate = accumulate; a.n_max = n_max;
   a.scores = scores; a.scores_stride = scores_stride;
   WsCarver c(ws);
+  c.take<uint8_t>(score_fused_ctrl_bytes(kv));
   const int slots = std::max(2 * p.n_splits, p.RC == 1 ? 2 * kMaxPersistentCTAs : 0);
   a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   a.rowinfo = c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);
@@ -1560,12 +1577,19 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
                   attr[3]))
     return SE_ERR_CUDA;
   const int groups = kv->B * kv->Hkv;
+  int dev = 0, n_sm = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return SE_ERR_CUDA;
+  if (one_launch) {
+    // both passes in one cooperative launch, every key read from HBM once
+    if (!score_fused_applicable(kv, w, n_max, n_sm, optin)) return SE_ERR_UNSUPPORTED;
+    return launch_score_fused(kv, kmap, qmap, w, q_pos, attn_lo, attn_hi, out_lo, out_hi, causal,
+                              accumulate, n_max, scores, scores_stride, ws, n_sm, st);
+  }
   if (p.RC == 1 && groups <= kMaxGroupsP) {
     // one row chunk: persistent CTAs, one per SM, over the (group, tile) sequence
-    int dev = 0, n_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return SE_ERR_CUDA;
     const int ctas = std::min(std::min(n_sm, kMaxPersistentCTAs), groups * p.n_tiles_max);
     se_launch(score_rowstats_persistent_tc, ctas, kThreads, kSmem1, st, kmap, qmap, a);
     se_launch(score_colsum_persistent_tc, ctas, kThreads, kSmem2Resident, st, kmap, qmap, a);

@@ -37,7 +37,9 @@ class _Base:
         self.max_slots = cache.slot_map.shape[-1]
 
     def _ws(self, nbytes):
-        return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+        # zeroed: the scoring workspace starts with a control block that each
+        # call leaves at zero for the next
+        return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
 
 
 class _Snapshot:

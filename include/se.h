@@ -124,8 +124,22 @@ typedef struct {
  *   accumulate 1: add to scores; 0: overwrite
  *   n_max     host: upper bound of attn_hi[b] - attn_lo[b] over b (sizes the
  *             grid; entries past the real range are masked)
- *   workspace se_score_window_workspace_size(kv, w, n_max) bytes
+ *   workspace se_score_window_workspace_size(kv, w, n_max) bytes, zeroed
+ *             before its first use.  Its start is a control block (per
+ *             (sequence, KV head) counters of the one-launch form, below)
+ *             that every call leaves zero again, so a workspace is zeroed
+ *             once and reused; calls that share a workspace must not
+ *             overlap on the GPU.  Its first 8 bytes may hold a limit in
+ *             nanoseconds for the kernel's bounded waits (0: 2 s); a wait
+ *             that runs out sets SE_ERR_TIMEOUT in kv->status, records
+ *             where it was in bytes [12, 16) (nonzero; the caller reads and
+ *             clears it) and the launch winds down without writing further
+ *             scores.
  * A query that sees no key adds nothing.
+ *
+ * bf16 with D = 128 runs on the tensor cores: a sweep of row statistics,
+ * then a sweep of column sums (two or three launches, each key read twice);
+ * fp32 and D = 64 on the CUDA cores.
  */
 se_status se_score_window(const se_paged_kv* kv, const void* q_win, int32_t w,
                           const int32_t* q_pos, const int32_t* attn_lo,
@@ -134,6 +148,26 @@ se_status se_score_window(const se_paged_kv* kv, const void* q_win, int32_t w,
                           int32_t n_max, float* scores, int64_t scores_stride,
                           void* workspace, size_t workspace_bytes, void* stream);
 size_t se_score_window_workspace_size(const se_paged_kv* kv, int32_t w, int32_t n_max);
+
+/*
+ * se_score_window_one_launch -- the same scores as se_score_window (same
+ * arguments, same workspace size, same control block), with both sweeps in
+ * one cooperative launch of one CTA per SM: the keys are cut into waves that
+ * fit L2, the column sums of a wave follow its row statistics two waves
+ * later, and the rows' softmax denominators are merged across CTAs inside
+ * the launch, so every key is read from HBM once.  Needs bf16, D = 128,
+ * w * Hq / Hkv <= 256, B <= 128 and key ranges of at least eight 128-key
+ * tiles (n_max); otherwise returns SE_ERR_UNSUPPORTED without launching.
+ * The workspace's bytes [16, 20) count its calls (they tag each call's
+ * merged rows); bytes [64, 64 + 4 B Hkv) are per-(sequence, KV head) tile
+ * counters that every call leaves at zero.
+ */
+se_status se_score_window_one_launch(const se_paged_kv* kv, const void* q_win, int32_t w,
+                                     const int32_t* q_pos, const int32_t* attn_lo,
+                                     const int32_t* attn_hi, const int32_t* out_lo,
+                                     const int32_t* out_hi, int32_t causal, int32_t accumulate,
+                                     int32_t n_max, float* scores, int64_t scores_stride,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* 2. Selection                                                               */
