@@ -222,12 +222,70 @@ def oracle_runs(workload: str, groups: int, n: int):
     return [run() for _ in range(n)]
 
 
-def oracle_subprocess(workload: str, groups: int, n: int = 1):
-    """Oracle samples in a child process pinned to one BLAS / OpenMP thread."""
+_UNIT_STATE = {}
+
+
+def _oracle_unit_init(workload):
+    """Worker set-up: one sequence of the workload (seeded, the same for every
+    worker) in the oracle's cache form."""
+    import se_workloads as W
+    from oracle import cache as ocache
+    shape = W.WORKLOADS[workload](B=1)
+    inp = W.snapkv_inputs(shape, "cpu")
+    _UNIT_STATE.update(shape=shape, inp=inp, c=ocache.from_tensors(inp["cache"]),
+                       q_pos=inp["q_pos"].numpy())
+
+
+def _oracle_unit(h):
+    """One (sequence, KV head) unit of the SnapKV oracle: window scores,
+    pooled top-k, decode attention over the kept entries."""
+    from oracle import attention as oattn
+    from oracle import pipelines as opipe
+    from oracle import scoring as oscore
+    from oracle import selection as osel
+    st = _UNIT_STATE
+    shape, inp, c = st["shape"], st["inp"], st["c"]
+    h = h % shape.Hkv
+    s = oscore.score_window(c, inp["q_win"], st["q_pos"], [0], [shape.ctx], [0], [shape.scored],
+                            True, groups=[(0, h)])
+    keep = osel.topk_keep(s[(0, h)], 0, shape.keep_topk, shape.pool_kernel, shape.scored, shape.ctx)
+    G = shape.G
+    oattn.attend(opipe.to_f64(inp["q_dec"])[0, h * G:(h + 1) * G], c.keys(0, h, keep),
+                 c.vals(0, h, keep))
+    return h
+
+
+def oracle_all_cores(workload: str):
+    """The SnapKV oracle over as many (sequence, KV head) units as the
+    workload has, on all host cores (one single-threaded worker per core,
+    spawned); returns (token-equivalents, seconds, cores, description)."""
+    import multiprocessing as mp
+    import se_workloads as W
+    full = W.WORKLOADS[workload]()
+    cores = os.cpu_count() or 1
+    n_units = full.B * full.Hkv
+    workers = min(cores, n_units)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(processes=workers, initializer=_oracle_unit_init, initargs=(workload,)) as pool:
+        pool.map(_oracle_unit, range(workers), chunksize=1)            # warm the workers
+        t0 = time.perf_counter()
+        pool.map(_oracle_unit, range(n_units), chunksize=1)
+        dt = time.perf_counter() - t0
+    desc = (f"{n_units} (sequence, KV head) units of {full.ctx} tokens (the workload's count; "
+            f"each a head of one seeded sequence), one single-threaded worker per core on "
+            f"{workers} of {cores} host cores: score + pool/top-k + decode over the kept entries")
+    return full.B * full.ctx, dt, workers, desc
+
+
+def oracle_subprocess(workload: str, groups: int, n: int = 1, all_cores: bool = False):
+    """Oracle samples in a child process pinned to one BLAS / OpenMP thread
+    (all_cores: the whole SnapKV batch over a pool of such workers)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
+    call = (f"bench.oracle_all_cores({workload!r})" if all_cores
+            else f"bench.oracle_runs({workload!r}, {groups}, {n})")
     code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
-            f"print(json.dumps(bench.oracle_runs({workload!r}, {groups}, {n})))")
+            f"print(json.dumps({call}))")
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=1800)
     if r.returncode != 0:
@@ -260,7 +318,7 @@ class Events:
 def run_snapkv(args, torch, rank, world):
     import se_workloads as W
     from attention_scored_sparse_gb300 import pipelines as P
-    shape = W.WORKLOADS[args.workload]()
+    shape = W.WORKLOADS[args.workload](**batch_kw(args))
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.snapkv_inputs(shape, dev)
     pc = inp["cache"]
@@ -294,7 +352,7 @@ def run_snapkv(args, torch, rank, world):
         step(False)
     torch.cuda.synchronize()
     assert int(pc.status.item()) == 0
-    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True), lambda: step(False))
     score_ms = ev.durations("s0", "s1")
     sel_ms = ev.durations("s1", "s2")
     cd_ms = ev.durations("s2", "s3")
@@ -332,6 +390,9 @@ def run_snapkv(args, torch, rank, world):
         "compact_gbs": comp_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9,
         "decode_gbs": dec_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9,
     }
+    hbm = peaks()[0]["hbm_gbs"]
+    detail["compact_frac_of_hbm"] = detail["compact_gbs"] / hbm
+    detail["decode_frac_of_hbm"] = detail["decode_gbs"] / hbm
     # DRAM bytes of one se_score_window call on this workload, both passes
     # (dram__bytes_read.sum + dram__bytes_write.sum under ncu on GB300:
     # 276.2 + 3.3 MB and 278.7 + 5.9 MB), for the current scorer kernels
@@ -390,7 +451,7 @@ def run_e2e_snapkv(torch, pipe, inp, restore, steps):
 def run_quest(args, torch, rank, world):
     import se_workloads as W
     from attention_scored_sparse_gb300 import pipelines as P
-    shape = W.quest_decode()
+    shape = W.quest_decode(**batch_kw(args))
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.quest_inputs(shape, dev)
     pipe = P.QuestDecode(inp["cache"], shape.Hq, ctx=shape.ctx, top_pages=shape.top_pages)
@@ -451,7 +512,7 @@ def run_quest(args, torch, rank, world):
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
-    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True), lambda: step(False))
     fused = ev.durations("f0", "f1")
     sel = ev.durations("s0", "s1")
     dec = ev.durations("s1", "s2")
@@ -471,7 +532,7 @@ def run_quest(args, torch, rank, world):
                 per_launch=f"{meta_bytes + kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
                 launches=3 + 1 + 1, metric="decode tokens/s", e2e=None,
-                cfg={"workload": "quest_decode: B=2 x 131072 tokens, top 128 pages + current, "
+                cfg={"workload": f"quest_decode: B={shape.B} x 131072 tokens, top 128 pages + current, "
                                  "32/8 heads, d=128, bf16",
                      "l2": "L2 flushed (256 MB write) before every timed step"},
                 dtype="bf16")
@@ -480,7 +541,7 @@ def run_quest(args, torch, rank, world):
 def run_h2o(args, torch, rank, world):
     import se_workloads as W
     from attention_scored_sparse_gb300 import pipelines as P
-    shape = W.h2o_decode()
+    shape = W.h2o_decode(**batch_kw(args))
     dev = torch.device("cuda", torch.cuda.current_device())
     nsteps = max(args.steps + args.warmup + 2, 16)
     inp = W.h2o_inputs(shape, dev, steps=nsteps)
@@ -529,7 +590,7 @@ def run_h2o(args, torch, rank, world):
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
-    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True), lambda: step(False))
     ms = statistics.mean(ev.durations("s0", "s1"))
     kv_bytes = shape.B * shape.Hkv * (shape.budget + 1) * 2 * shape.D * 2
     detail = {"prefill_ms": prefill_ms, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9}
@@ -538,7 +599,7 @@ def run_h2o(args, torch, rank, world):
                 per_launch=f"{kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
                 launches=2 + 1 + 1 + 2, metric="decode tokens/s", e2e=None,
-                cfg={"workload": "h2o_decode: B=64, 4096-token prompt, budget 1024+128, "
+                cfg={"workload": f"h2o_decode: B={shape.B}, 4096-token prompt, budget 1024+128, "
                                  "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
                 dtype="bf16")
 
@@ -577,7 +638,7 @@ def time_h2o_chunked(torch, shape, chunk, dev, reps=3):
 def run_kara(args, torch, rank, world):
     import se_workloads as W
     from attention_scored_sparse_gb300 import pipelines as P
-    shape = W.kara_prune()
+    shape = W.kara_prune(**batch_kw(args))
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.kara_inputs(shape, dev)
     pc = inp["cache"]
@@ -611,7 +672,7 @@ def run_kara(args, torch, rank, world):
         step(False)
     torch.cuda.synchronize()
     assert int(pc.status.item()) == 0
-    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True))
+    t_wall, clocks = timed_loop(args, torch, rank, world, lambda: step(True), lambda: step(False))
     comp = ev.durations("s0", "s1")
     prn = ev.durations("s1", "s2")
     dec = ev.durations("s2", "s3")
@@ -628,22 +689,42 @@ def run_kara(args, torch, rank, world):
                 per_launch=f"{prune_bytes:.4g} B (moved entries, read + write)")
     return dict(tokens=shape.B * shape.ctx, ms=ms, wall=t_wall, clocks=clocks, detail=detail,
                 roof=roof, launches=3 + 1 + 3 + 5 + 1, e2e=None,
-                cfg={"workload": "kara_prune: B=128 x 16384 tokens, window 256 (32 protected), "
+                cfg={"workload": f"kara_prune: B={shape.B} x 16384 tokens, window 256 (32 protected), "
                                  "chunk budget 64, prune [2048,6144) keep 20%",
                      "l2": "inputs larger than L2"}, dtype="bf16")
 
 
-def timed_loop(args, torch, rank, world, fn):
+def batch_kw(args):
+    """--batch: a smaller batch of the same workload (profiling captures)."""
+    return {"B": args.batch} if getattr(args, "batch", None) else {}
+
+
+def timed_loop(args, torch, rank, world, fn, warm=None):
+    """Times args.steps calls of fn.  The clock sampler starts first; `warm`
+    (untimed steps) keeps the GPU busy for at least 0.3 s while it starts, so
+    that the clock record holds samples under load even for short runs."""
     import torch.distributed as dist
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as cs:
+        if warm is not None:
+            t_w = time.perf_counter()
+            while time.perf_counter() - t_w < 0.3:
+                for _ in range(8):
+                    warm()
+                torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             fn()
         torch.cuda.synchronize()
         t1 = time.perf_counter()
+        # a few more samples at the same load after the timed region
+        if warm is not None:
+            t_w = time.perf_counter()
+            while time.perf_counter() - t_w < 0.05:
+                warm()
+            torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     return t1 - t0, cs.summary()
@@ -669,7 +750,7 @@ def run_kara_schedule(args, torch, rank, world):
     import se_workloads as W
     from attention_scored_sparse_gb300 import pipelines as P
     n_steps = args.warmup + args.steps
-    shape = W.kara_schedule(steps=n_steps)
+    shape = W.kara_schedule(steps=n_steps, **batch_kw(args))
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.kara_schedule_inputs(shape, dev)
     fills = [shape.fill(b) for b in range(shape.B)]
@@ -709,12 +790,38 @@ def run_kara_schedule(args, torch, rank, world):
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
                 launches=2 + 1 + (3 + 1 + 3) * detail["compressions_per_step"],
                 metric="decode tokens/s", e2e=None,
-                cfg={"workload": "kara_schedule: B=128 decoding over 2304 resident tokens, "
+                cfg={"workload": f"kara_schedule: B={shape.B} decoding over 2304 resident tokens, "
                                  "Kara window 256 (32 protected, 32 candidates, chunk budget 64) "
                                  "compressed when full, staggered over the 160-step period; "
                                  "32/8 heads, d=128, bf16",
                      "l2": "inputs larger than L2 (1.2 GB attended per step)"},
                 dtype="bf16")
+
+
+def other_workloads(args, torch, rank, world):
+    """Step time and roofline fraction of the Quest, H2O and Kara workloads
+    (20 timed steps each after 3 warm-up steps), measured in this run."""
+    import copy
+    pk, src = peaks()
+    out = {}
+    for name in ("quest_decode", "h2o_decode", "kara_prune"):
+        a2 = copy.copy(args)
+        a2.workload, a2.steps, a2.warmup = name, 20, 3
+        try:
+            r = RUNNERS[name](a2, torch, rank, world)
+        except Exception as exc:  # reported, not hidden
+            out[name] = {"error": str(exc)[-300:]}
+            continue
+        peak = pk["bf16_tflops"] if r["roof"]["bound"] == "tensor" else pk["hbm_gbs"]
+        keep = {k: v for k, v in r["detail"].items() if k.endswith(("_ms", "_gbs"))}
+        out[name] = {"ms_per_step": r["ms"], "value": r["tokens"] / (r["ms"] * 1e-3),
+                     "unit": "KV tokens/s" if r.get("metric", METRIC) == METRIC else "decode tokens/s",
+                     "kernel": r["roof"]["kernel"], "achieved": r["roof"]["achieved"],
+                     "unit_roof": r["roof"]["unit"], "frac": r["roof"]["achieved"] / peak,
+                     "l2": r["cfg"].get("l2"), "detail": keep}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 RUNNERS = {"snapkv_llama8b": run_snapkv, "snapkv_tiny": run_snapkv, "quest_decode": run_quest,
@@ -730,6 +837,10 @@ def main():
     ap.add_argument("--workload", default="snapkv_llama8b", choices=sorted(RUNNERS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch decode steps eagerly")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences of the workload (default: the workload's own; for profiling)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the short runs of the other workloads reported in detail")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -791,11 +902,21 @@ def main():
         e2e_ms = max_over_ranks(e2e_ms, world, "cuda")     # the slowest rank, like the step time
         line["e2e"] = {"value": r["tokens"] * world / (e2e_ms * 1e-3), "unit": unit,
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    if world == 1 and args.workload == "snapkv_llama8b" and not args.no_others:
+        # short runs of the other workloads (their own inputs and step), for
+        # the decode / compaction / Quest fractions beside the headline
+        line["detail"]["other_workloads"] = other_workloads(args, torch, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             tokens, dt, desc = oracle_subprocess(args.workload, 2)[0]
-            line["cpu_baseline"] = {"value": tokens / dt, "unit": unit, "cores": 1,
-                                    "kind": "oracle", "sample": desc}
+            base = {"value": tokens / dt, "unit": unit, "cores": 1, "kind": "oracle",
+                    "sample": desc, "host_cores": os.cpu_count()}
+            if args.workload == "snapkv_llama8b":
+                tok_all, dt_all, cores, desc_all = oracle_subprocess(args.workload, 0, all_cores=True)
+                base = {"value": tok_all / dt_all, "unit": unit, "cores": cores, "kind": "oracle",
+                        "sample": desc_all, "host_cores": os.cpu_count(),
+                        "one_core": {"value": tokens / dt, "cores": 1, "sample": desc}}
+            line["cpu_baseline"] = base
         except Exception as exc:  # reported, not hidden
             line["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
     if rank == 0:
