@@ -81,7 +81,7 @@ struct DecodeArgs {
   void* out;          // o [B][Hq][D]
   float* acc;         // H2O running scores or null
   int64_t acc_stride;
-  int32_t* done;      // [units] segments finished (zeroed before the launch)
+  int32_t* done;      // [units] segments finished (zero at the launch; the last CTA of a unit resets it)
 };
 
 // Slices [start, end) of CTA c's range.
@@ -249,6 +249,9 @@ SE_DEV void finish_segment(const DecodeArgs& a, int u, int c, float (*s_m)[G], f
   }
   __syncthreads();
   if (s_last) merge_chunks<T, D, G>(a, u, n_parts);
+  // every segment of u has been counted: the counter is left at zero for
+  // the next call on this workspace
+  if (s_last && threadIdx.x == 0) a.done[u] = 0;
   __syncthreads();
 }
 
@@ -892,11 +895,15 @@ extern "C" size_t se_sparse_decode_attn_workspace_size(const se_paged_kv* kv, in
   return b;
 }
 
-extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
-                                           const int32_t* sel, int32_t sel_stride, int32_t n_sel,
-                                           int32_t max_entries, void* o, float* acc_scores,
-                                           int64_t acc_stride, void* workspace,
-                                           size_t workspace_bytes, void* stream) {
+// clear_counters: zero the per-unit segment counters before the launch (the
+// library's own scratch array, which no caller can re-zero after an error);
+// a caller's workspace is zero before its first use and every call that
+// completes leaves the counters zero.
+static se_status decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
+                             const int32_t* sel, int32_t sel_stride, int32_t n_sel,
+                             int32_t max_entries, void* o, float* acc_scores, int64_t acc_stride,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             bool clear_counters) {
   se_status s = se_check_kv(kv);
   if (s != SE_OK) return s;
   if (q == nullptr || o == nullptr || workspace == nullptr || max_entries < 1) return SE_ERR_INVALID_ARG;
@@ -917,7 +924,8 @@ extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q,
                w.part, acc_scores ? w.logits : nullptr, max_entries, o, acc_scores, acc_stride,
                w.done};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(w.done, 0, sizeof(int32_t) * kv->B * kv->Hkv, st) != cudaSuccess)
+  if (clear_counters &&
+      cudaMemsetAsync(w.done, 0, sizeof(int32_t) * kv->B * kv->Hkv, st) != cudaSuccess)
     return SE_ERR_CUDA;
   if (kv->dtype == SE_BF16 && kv->D == 128) s = launch_decode_d<__nv_bfloat16, 128>(a, G, st);
   else if (kv->dtype == SE_BF16 && kv->D == 64) s = launch_decode_d<__nv_bfloat16, 64>(a, G, st);
@@ -926,6 +934,15 @@ extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q,
   else return SE_ERR_UNSUPPORTED;
   if (s != SE_OK) return s;
   return se_last_launch_status();
+}
+
+extern "C" se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
+                                           const int32_t* sel, int32_t sel_stride, int32_t n_sel,
+                                           int32_t max_entries, void* o, float* acc_scores,
+                                           int64_t acc_stride, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  return decode_attn(kv, q, view, sel, sel_stride, n_sel, max_entries, o, acc_scores, acc_stride,
+                     workspace, workspace_bytes, stream, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -975,6 +992,6 @@ extern "C" se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const v
   void* scratch = nullptr;
   s = static_scratch(&scratch);
   if (s != SE_OK) return s;
-  return se_sparse_decode_attn(kv, q, view, sel, sel_stride, n_sel, max_entries, o, acc_scores,
-                               acc_stride, scratch, SE_DECODE_STATIC_SCRATCH_BYTES, stream);
+  return decode_attn(kv, q, view, sel, sel_stride, n_sel, max_entries, o, acc_scores, acc_stride,
+                     scratch, SE_DECODE_STATIC_SCRATCH_BYTES, stream, true);
 }

@@ -335,6 +335,11 @@ typedef enum { SE_VIEW_DENSE = 0, SE_VIEW_PAGES = 1, SE_VIEW_TOKENS = 2 } se_vie
  * acc_scores (optional) [B][Hkv][acc_stride] fp32: += sum_{h in g} of this
  * step's softmax weight of each viewed slot (H2O running scores).
  * max_entries (host) bounds the entries of one (b, g) view.
+ * workspace se_sparse_decode_attn_workspace_size(kv, max_entries) bytes,
+ * zeroed before its first use: it holds per-(b, g) counters of the CTAs that
+ * finished, which every call that completes leaves at zero again (zero it
+ * anew after a call that set a device error).  Calls that share a workspace
+ * must not overlap on the GPU.
  */
 se_status se_sparse_decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
                                 const int32_t* sel, int32_t sel_stride, int32_t n_sel,
