@@ -17,9 +17,13 @@
 // CTAs stored.
 #include <algorithm>
 
+#include <cooperative_groups.h>
+
 #include "tc_primitives.cuh"
 
 namespace se {
+
+namespace cg = cooperative_groups;
 
 template <typename T, int V>
 SE_DEV void load_row(const T* p, float* f) {
@@ -82,6 +86,7 @@ struct DecodeArgs {
   float* acc;         // H2O running scores or null
   int64_t acc_stride;
   int32_t* done;      // [units] segments finished (zero at the launch; the last CTA of a unit resets it)
+  int k_cl;           // cluster split: CTAs per unit (one cluster each); 0 for the kernels above
 };
 
 // Slices [start, end) of CTA c's range.
@@ -510,19 +515,282 @@ SE_DEV void issue_stage(const DecodeArgs& a, int s0, int n_seg, const int32_t* r
   if (lane == 0) tc::mbar_arrive(bar);
 }
 
+// Shared memory of the staged kernels: the stage ring and the per-half-warp
+// softmax states.
+template <int G, int SE>
+struct StageRing {
+  uint8_t* stages;       // STAGES buffers (K rows, then V rows), 128-byte aligned
+  uint64_t* full;        // [STAGES] the copies of a stage have landed
+  uint64_t* empty;       // [STAGES] the four warps are done with a stage
+  int8_t (*valid)[SE];   // [4][SE] whether entry x of a stage has a row
+  float (*p)[16];        // [8][16] probabilities of one iteration
+  float (*m)[G];         // [8][G] half-warp maxima
+  float (*l)[G];         // [8][G] half-warp sums
+  int* abort;            // a wait ran out
+};
+
+// K/V row in the pool ((page * Hkv + g) * P + row in page) of view entries
+// [e_begin, e_begin + n) of unit u, -1 for an entry past the view or without
+// a resident row, written to rows[0, n) by the CTA's threads.  In the dense
+// view the block-table reads do not wait for ctx_len (only the mask does).
+// Returns how many of the n entries lie in the view.
+SE_DEV int resolve_rows(const DecodeArgs& a, int u, int e_begin, int n, int32_t* rows) {
+  const se_paged_kv& kv = a.kv;
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+  const int P = kv.page_size;
+  const int ctx = kv.ctx_len[b];
+  const int n_view = min(view_entries(a, ctx), a.max_entries);
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  for (int x = threadIdx.x; x < n; x += blockDim.x) {
+    const int e = e_begin + x;
+    int slot, page;
+    if (a.view == SE_VIEW_DENSE) {
+      const int ip = e / P;
+      page = ip < kv.max_pages_per_seq ? bt[ip] : -1;
+      slot = e < n_view ? e : -1;
+    } else {
+      slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
+      page = slot >= 0 ? bt[slot / P] : -1;
+    }
+    rows[x] = (slot >= 0 && page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
+  }
+  return max(min(e_begin + n, n_view) - e_begin, 0);
+}
+
+// Streams view entries [e_begin, e_begin + n_seg) of unit u = (b, g), whose
+// K/V rows are rows[0, n_seg), through the stage ring.  Warp 0 keeps
+// STAGES-1 stages of copies in flight; every half-warp reads its E rows of
+// each stage from shared memory (16 lanes x 16 bytes = one 256-byte row,
+// conflict-free) and runs the reduce-scatter / online-softmax arithmetic of
+// the register kernel above.  gi / gc count the stages the CTA has issued /
+// consumed (stage n uses buffer n % STAGES), so buffers and barrier phases
+// carry over from one call to the next.  On return the 8 half-warp states
+// are in r.m, r.l and, as float [8][G][D], over the stage memory (every
+// stage is idle by then), and all threads have passed a barrier.  A wait
+// that runs out sets the status word and *r.abort and ends the stream; the
+// states are then meaningless but the call still returns normally.
+template <typename T, int D, int G>
+SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T, D, G>::SE>& r,
+                           int u, int e_begin, int n_seg, const int32_t* rows, int& gi, int& gc) {
+  using Gm = StagedGeom<T, D, G>;
+  constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
+  constexpr int V2 = V / 2;
+  constexpr uint64_t kLimit = 2000000000ull;
+  const se_paged_kv& kv = a.kv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int my_e = t / G, my_h = t % G;
+  const unsigned full_mask = 0xffffffffu;
+  const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
+  const float qscale = kLog2e * rsqrtf((float)D);
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+  const int n_it = cdiv(n_seg, SE);
+  const int g0 = gi;   // stage count at the segment's start
+  uint8_t* const stages = r.stages;
+
+  // the first STAGES-1 stages; a buffer last used by an earlier segment is
+  // refilled only after its consumers have released it
+  if (producer) {
+    for (int i = 0; i < min(S - 1, n_it); ++i) {
+      const int n = g0 + i;
+      const bool free_ok = n < S || tc::mbar_wait(&r.empty[n % S], ((n / S) - 1) & 1, kLimit);
+      if (!__all_sync(full_mask, free_ok)) {
+        if (lane == 0) {
+          set_status(kv.status, SE_ERR_TIMEOUT);
+          atomicExch(r.abort, 1);
+        }
+        break;
+      }
+      issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                           &r.full[n % S], r.valid[n % S], lane);
+      ++gi;
+    }
+  }
+
+  float q[G][V];
+  const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+    for (int i = 0; i < V; ++i) q[j][i] *= qscale;
+  }
+  // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
+  uint64_t q2[G][V2], o2[G][V2];
+  float m[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V2; ++i) {
+      q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
+      o2[j][i] = 0;
+    }
+  }
+  float l_own = 0.f;
+  float* lg = a.logits ? a.logits + (int64_t)u * a.max_entries * G : nullptr;
+
+  for (int it = 0; it < n_it; ++it) {
+    if (producer && gi - g0 < n_it) {
+      // refill the buffer consumed in the previous iteration
+      const int n = gi;
+      const bool free_ok = n < S || tc::mbar_wait(&r.empty[n % S], ((n / S) - 1) & 1, kLimit);
+      if (__all_sync(full_mask, free_ok)) {
+        issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                             &r.full[n % S], r.valid[n % S], lane);
+        ++gi;
+      } else if (lane == 0) {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(r.abort, 1);
+      }
+    }
+    const int s = gc % S;
+    const bool ok_wait = tc::mbar_wait(&r.full[s], (gc / S) & 1, kLimit);
+    if (!__all_sync(full_mask, ok_wait)) {
+      if (lane == 0) {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(r.abort, 1);
+      }
+      break;
+    }
+    const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
+    const uint8_t* vst = kst + SE * RB;
+    const int e0 = e_begin + it * SE + hw * E;
+    // K rows are read from the stage one entry at a time; V rows are read
+    // again after the probabilities are known (the stage is released after)
+    bool valid[E];
+    float part[16];
+#pragma unroll
+    for (int uu = 0; uu < E; ++uu) {
+      valid[uu] = r.valid[s][hw * E + uu] != 0;
+      float kf[V];
+      if (valid[uu]) {
+        load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + uu) * RB) + t * V, kf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) kf[i] = 0.f;
+      }
+      uint64_t k2[V2];
+#pragma unroll
+      for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        uint64_t acc2 = 0;
+#pragma unroll
+        for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
+        float lo, hi;
+        tc::f2split(acc2, lo, hi);
+        part[uu * G + j] = lo + hi;
+      }
+    }
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+      const int off = 8 >> step;
+      const int n = 8 >> step;
+      const bool upper = (t & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n; ++i) {
+        const float lo = part[i], hi = part[i + n];
+        part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
+      }
+    }
+    bool ok = false;
+#pragma unroll
+    for (int uu = 0; uu < E; ++uu) ok = (uu == my_e) ? valid[uu] : ok;
+    const float sv = ok ? part[0] : -INFINITY;
+    if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+    float tmax = sv;
+#pragma unroll
+    for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
+    float m_mine = m[0];
+#pragma unroll
+    for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+    const float mn_mine = fmaxf(m_mine, tmax);
+    const float alpha_mine =
+        (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+    const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+    l_own = fmaf(l_own, alpha_mine, p);
+    r.p[hw][t] = p;
+    bool grew = false;
+    float alpha[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
+      alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
+      grew |= mj != m[j];
+      m[j] = mj;
+    }
+    __syncwarp();
+    if (grew) {
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
+#pragma unroll
+        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
+      }
+    }
+#pragma unroll
+    for (int uu = 0; uu < E; ++uu) {
+      float vf[V];
+      if (valid[uu]) {
+        load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + uu) * RB) + t * V, vf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) vf[i] = 0.f;
+      }
+      uint64_t v2[V2];
+#pragma unroll
+      for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float pu = r.p[hw][uu * G + j];
+        const uint64_t p2 = tc::f2(pu, pu);
+#pragma unroll
+        for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&r.empty[s]);   // done with this stage's rows
+    ++gc;
+  }
+  // drain: after a timeout, copies of the last stages may still be in flight
+  // (each earlier stage was waited on before its buffer was refilled)
+  if (producer && lane == 0)
+    for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&r.full[i % S], (i / S) & 1, kLimit);
+  float lsum = l_own;
+#pragma unroll
+  for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
+  if (t < G) {
+    float mt = m[0];
+#pragma unroll
+    for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+    r.m[hw][t] = mt;
+    r.l[hw][t] = lsum;
+  }
+  __syncthreads();   // every stage of the segment has been read: reuse the stage memory
+  float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int i = 0; i < V2; ++i) {
+      float lo, hi;
+      tc::f2split(o2[j][i], lo, hi);
+      s_o[hw][j][t * V + 2 * i] = lo;
+      s_o[hw][j][t * V + 2 * i + 1] = hi;
+    }
+  __syncthreads();
+}
+
 // grid: n_cta; 128 threads = 8 half-warps; dynamic smem StagedGeom::SMEM.
-// Warp 0 keeps STAGES-1 stages of copies in flight within a segment; every
-// half-warp reads its E rows of each stage from shared memory (16 lanes x 16
-// bytes = one 256-byte row, conflict-free) and runs the same reduce-scatter /
-// online-softmax arithmetic as the register kernel above.  Stage buffers and
-// barrier phases follow a count of the stages the CTA has issued, so they
-// carry over from one segment to the next; at a segment's end the stages are
-// idle and hold the half-warp states while they are combined.
+// Every entry of the CTA's range is resolved to its K/V row up front; each
+// segment of the range is then streamed (stream_segment) and its half-warp
+// states are combined and counted (finish_segment), the last CTA of a unit
+// merging the unit's partials.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_partial_kernel(DecodeArgs a) {
   pdl_enter();
   using Gm = StagedGeom<T, D, G>;
-  constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
+  constexpr int SE = Gm::SE, S = Gm::STAGES;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[4], empty[4];
@@ -533,13 +801,8 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
   __shared__ int s_nseg[kMaxChunk / SE];   // viewed entries of each segment of the range
   __shared__ int s_abort;
   static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
+  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
   const int c = blockIdx.x;
-  const se_paged_kv& kv = a.kv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
-  const int my_e = t / G, my_h = t % G;
-  const unsigned full_mask = 0xffffffffu;
-  constexpr uint64_t kLimit = 2000000000ull;
   const int64_t x0 = range_start(a, c), x1 = range_end(a, c);
 
   if (threadIdx.x == 0) {
@@ -556,232 +819,19 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
   for (int64_t xs = x0, k = 0; xs < x1; ++k) {
     const int u = (int)(xs / a.sp);
     const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
-    const int b = u / kv.Hkv, g = u % kv.Hkv;
-    const int P = kv.page_size;
-    const int ctx = kv.ctx_len[b];
-    const int n_view = min(view_entries(a, ctx), a.max_entries);
     const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
-    const int n_all = (int)(xe - xs) * SE;
-    if (threadIdx.x == 0) s_nseg[k] = max(min(e_begin + n_all, n_view) - e_begin, 0);
-    int32_t* rows = s_rows + (int)(xs - x0) * SE;
-    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-    for (int x = threadIdx.x; x < n_all; x += blockDim.x) {
-      const int e = e_begin + x;
-      const int slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
-      const int page = slot >= 0 ? bt[slot / P] : -1;
-      rows[x] = (page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
-    }
+    const int n = resolve_rows(a, u, e_begin, (int)(xe - xs) * SE, s_rows + (int)(xs - x0) * SE);
+    if (threadIdx.x == 0) s_nseg[k] = n;
     xs = xe;
   }
   __syncthreads();
-  const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
-  const float qscale = kLog2e * rsqrtf((float)D);
-  constexpr int V2 = V / 2;
-  int gi = 0;   // stages issued by this CTA (stage n uses buffer n % S)
-  int gc = 0;   // stages consumed
-
+  int gi = 0, gc = 0;
   for (int64_t xs = x0, k = 0; xs < x1; ++k) {
     const int u = (int)(xs / a.sp);
     const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
-    const int b = u / kv.Hkv, g = u % kv.Hkv;
     const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
-    const int n_seg = s_nseg[k];
-    const int n_it = cdiv(n_seg, SE);
-    const int32_t* rows = s_rows + (int)(xs - x0) * SE;
-    const int g0 = gi;   // stage count at the segment's start
-
-    // the first STAGES-1 stages; a buffer last used by an earlier segment is
-    // refilled only after its consumers have released it
-    if (producer) {
-      for (int i = 0; i < min(S - 1, n_it); ++i) {
-        const int n = g0 + i;
-        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
-        if (!__all_sync(full_mask, free_ok)) {
-          if (lane == 0) {
-            set_status(kv.status, SE_ERR_TIMEOUT);
-            atomicExch(&s_abort, 1);
-          }
-          break;
-        }
-        issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
-                             &full[n % S], s_valid[n % S], lane);
-        ++gi;
-      }
-    }
-
-    float q[G][V];
-    const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      load_row<T, V>(qb + (int64_t)j * D, q[j]);
-#pragma unroll
-      for (int i = 0; i < V; ++i) q[j][i] *= qscale;
-    }
-    // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
-    uint64_t q2[G][V2], o2[G][V2];
-    float m[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      m[j] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < V2; ++i) {
-        q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
-        o2[j][i] = 0;
-      }
-    }
-    float l_own = 0.f;
-    float* lg = a.logits ? a.logits + (int64_t)u * a.max_entries * G : nullptr;
-
-    for (int it = 0; it < n_it; ++it) {
-      if (producer && gi - g0 < n_it) {
-        // refill the buffer consumed in the previous iteration
-        const int n = gi;
-        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
-        if (__all_sync(full_mask, free_ok)) {
-          issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
-                               &full[n % S], s_valid[n % S], lane);
-          ++gi;
-        } else if (lane == 0) {
-          set_status(kv.status, SE_ERR_TIMEOUT);
-          atomicExch(&s_abort, 1);
-        }
-      }
-      const int s = gc % S;
-      const bool ok_wait = tc::mbar_wait(&full[s], (gc / S) & 1, kLimit);
-      if (!__all_sync(full_mask, ok_wait)) {
-        if (lane == 0) {
-          set_status(kv.status, SE_ERR_TIMEOUT);
-          atomicExch(&s_abort, 1);
-        }
-        break;
-      }
-      const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
-      const uint8_t* vst = kst + SE * RB;
-      const int e0 = e_begin + it * SE + hw * E;
-      // K rows are read from the stage one entry at a time; V rows are read
-      // again after the probabilities are known (the stage is released after)
-      bool valid[E];
-      float part[16];
-#pragma unroll
-      for (int uu = 0; uu < E; ++uu) {
-        valid[uu] = s_valid[s][hw * E + uu] != 0;
-        float kf[V];
-        if (valid[uu]) {
-          load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + uu) * RB) + t * V, kf);
-        } else {
-#pragma unroll
-          for (int i = 0; i < V; ++i) kf[i] = 0.f;
-        }
-        uint64_t k2[V2];
-#pragma unroll
-        for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          uint64_t acc2 = 0;
-#pragma unroll
-          for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
-          float lo, hi;
-          tc::f2split(acc2, lo, hi);
-          part[uu * G + j] = lo + hi;
-        }
-      }
-#pragma unroll
-      for (int step = 0; step < 4; ++step) {
-        const int off = 8 >> step;
-        const int n = 8 >> step;
-        const bool upper = (t & off) != 0;
-#pragma unroll
-        for (int i = 0; i < n; ++i) {
-          const float lo = part[i], hi = part[i + n];
-          part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
-        }
-      }
-      bool ok = false;
-#pragma unroll
-      for (int uu = 0; uu < E; ++uu) ok = (uu == my_e) ? valid[uu] : ok;
-      const float sv = ok ? part[0] : -INFINITY;
-      if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
-      float tmax = sv;
-#pragma unroll
-      for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
-      float m_mine = m[0];
-#pragma unroll
-      for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
-      const float mn_mine = fmaxf(m_mine, tmax);
-      const float alpha_mine =
-          (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
-      const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
-      l_own = fmaf(l_own, alpha_mine, p);
-      s_p[hw][t] = p;
-      bool grew = false;
-      float alpha[G];
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
-        alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
-        grew |= mj != m[j];
-        m[j] = mj;
-      }
-      __syncwarp();
-      if (grew) {
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
-#pragma unroll
-          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
-        }
-      }
-#pragma unroll
-      for (int uu = 0; uu < E; ++uu) {
-        float vf[V];
-        if (valid[uu]) {
-          load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + uu) * RB) + t * V, vf);
-        } else {
-#pragma unroll
-          for (int i = 0; i < V; ++i) vf[i] = 0.f;
-        }
-        uint64_t v2[V2];
-#pragma unroll
-        for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          const float pu = s_p[hw][uu * G + j];
-          const uint64_t p2 = tc::f2(pu, pu);
-#pragma unroll
-          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with this stage's rows
-      ++gc;
-    }
-    // drain: after a timeout, copies of the last stages may still be in flight
-    // (each earlier stage was waited on before its buffer was refilled)
-    if (producer && lane == 0)
-      for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
-    float lsum = l_own;
-#pragma unroll
-    for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
-    if (t < G) {
-      float mt = m[0];
-#pragma unroll
-      for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
-      s_m[hw][t] = mt;
-      s_l[hw][t] = lsum;
-    }
-    __syncthreads();   // every stage of the segment has been read: reuse the stage memory
-    float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-      for (int i = 0; i < V2; ++i) {
-        float lo, hi;
-        tc::f2split(o2[j][i], lo, hi);
-        s_o[hw][j][t * V + 2 * i] = lo;
-        s_o[hw][j][t * V + 2 * i + 1] = hi;
-      }
-    __syncthreads();
-    finish_segment<T, D, G>(a, u, c, s_m, s_l, s_o);
+    stream_segment<T, D, G>(a, ring, u, e_begin, s_nseg[k], s_rows + (int)(xs - x0) * SE, gi, gc);
+    finish_segment<T, D, G>(a, u, c, s_m, s_l, reinterpret_cast<float (*)[G][D]>(stages));
     // the stage memory was written and read as plain shared memory; order
     // that before the next segment's copies into it
     tc::fence_proxy_async_smem();
@@ -789,6 +839,182 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
     if (s_abort) break;
     xs = xe;
   }
+}
+
+constexpr int kMaxCluster = 16;   // CTAs of a unit in the cluster split (non-portable above 8)
+
+// grid: units x k CTAs in clusters of k = a.k_cl (a power of two up to 16);
+// 128 threads; dynamic smem StagedGeom::SMEM.  Cluster u is unit u = (b, g);
+// its CTA of rank r streams slices [r sp / k, (r + 1) sp / k) of the unit and
+// combines its half-warp states into one partial (m, l, o) in its own shared
+// memory.  After a cluster barrier every CTA reads the k maxima and sums from
+// its peers' shared memory, merges its own G D / k elements of o from the
+// peers' partials (the partials of an element are summed in a fixed order,
+// so the result does not depend on timing), writes them, and for H2O adds
+// sum_h p_{h,j} to the running score of each of its own entries from the
+// logits it stored.  A second cluster barrier keeps every CTA's shared
+// memory alive until its peers have read it.  Every thread of every CTA
+// reaches both barriers, also after a stage wait has run out.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_cluster_kernel(DecodeArgs a) {
+  using Gm = StagedGeom<T, D, G>;
+  constexpr int SE = Gm::SE, S = Gm::STAGES;
+  constexpr int GD = G * D;
+  static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
+  static_assert(GD % kMaxCluster == 0, "o splits evenly over the cluster");
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[4], empty[4];
+  __shared__ int8_t s_valid[4][SE];
+  __shared__ int32_t s_rows[kMaxChunk];
+  __shared__ float s_p[8][16];
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ float s_pm[G], s_pl[G];                            // this CTA's partial: maxima, sums
+  __shared__ float s_cm[kMaxCluster][G], s_ce[kMaxCluster][G];  // the peers' maxima; their weights
+  __shared__ float s_M[G], s_invL[G];
+  __shared__ int s_abort;
+  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
+  cg::cluster_group cluster = cg::this_cluster();
+  const se_paged_kv& kv = a.kv;
+  const int k = a.k_cl;
+  const int rank = (int)cluster.block_rank();
+  const int u = blockIdx.x / k;
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 4);
+    }
+    tc::fence_barrier_init();
+  }
+  pdl_enter();
+  const int xs = (int)((int64_t)rank * a.sp / k), xe = (int)((int64_t)(rank + 1) * a.sp / k);
+  const int e_begin = xs * SE;
+  const int n_seg = resolve_rows(a, u, e_begin, (xe - xs) * SE, s_rows);
+  __syncthreads();
+  int gi = 0, gc = 0;
+  stream_segment<T, D, G>(a, ring, u, e_begin, n_seg, s_rows, gi, gc);
+
+  // the CTA's partial, in place over the first half-warp's o (each element
+  // is read and written by one thread)
+  float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
+  for (int x = threadIdx.x; x < GD; x += 128) {
+    const int j = x / D, d = x % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w][j]);
+    float acc = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float f = ex2(s_m[w][j] - M);
+        acc = fmaf(s_o[w][j][d], f, acc);
+        L = fmaf(s_l[w][j], f, L);
+      }
+    }
+    s_o[0][j][d] = acc;
+    if (d == 0) {
+      s_pm[j] = M;
+      s_pl[j] = L;
+    }
+  }
+  cluster.sync();   // every partial of the unit is in its CTA's shared memory
+
+  // this CTA's elements of o: tpe threads (adjacent lanes) per element, each
+  // summing cpt = k / tpe of the partials (every tpe-th one), then a fixed
+  // xor tree over the tpe lanes.  One round of peer reads fetches the
+  // maxima and sums and every o value the thread needs.
+  constexpr int NV = GD >= 128 ? GD / 128 : 1;   // o values per thread at most
+  const int per = GD / k;
+  int tpe = 1;
+  while (tpe < k && tpe * 2 * per <= 128) tpe <<= 1;
+  const int cpt = k / tpe, epr = 128 / tpe, rounds = cdiv(per, epr);
+  const int sub = threadIdx.x & (tpe - 1);
+  const float* po = &s_o[0][0][0];
+  float ov[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int x = (i / cpt) * epr + threadIdx.x / tpe;
+    ov[i] = (i < rounds * cpt && x < per)
+                ? *cluster.map_shared_rank(po + rank * per + x, sub + (i % cpt) * tpe)
+                : 0.f;
+  }
+  if (threadIdx.x < k * G) {
+    const int c = threadIdx.x / G, j = threadIdx.x % G;
+    s_cm[c][j] = *cluster.map_shared_rank(&s_pm[j], c);
+    s_ce[c][j] = *cluster.map_shared_rank(&s_pl[j], c);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int j = threadIdx.x;
+    float M = -INFINITY;
+    for (int c = 0; c < k; ++c) M = fmaxf(M, s_cm[c][j]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int c = 0; c < k; ++c) L = fmaf(s_ce[c][j], ex2(s_cm[c][j] - M), L);
+    s_M[j] = M;
+    s_invL[j] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x < k * G) {
+    const int c = threadIdx.x / G, j = threadIdx.x % G;
+    s_ce[c][j] = s_M[j] == -INFINITY ? 0.f : ex2(s_cm[c][j] - s_M[j]);
+  }
+  __syncthreads();
+  T* out = static_cast<T*>(a.out);
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int x = rd * epr + threadIdx.x / tpe;
+    const bool ok = x < per;
+    const int xg = rank * per + (ok ? x : 0);
+    const int j = xg / D, d = xg % D;
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (i / cpt == rd) v = fmaf(ov[i], s_ce[sub + (i % cpt) * tpe][j], v);
+    for (int off = 1; off < tpe; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (ok && sub == 0) {
+      v *= s_invL[j];
+      T* op = out + ((int64_t)b * kv.Hq + g * G + j) * D + d;
+      if constexpr (sizeof(T) == 2) *op = __float2bfloat16_rn(v);
+      else *op = v;
+    }
+  }
+  // the peers' shared memory is no longer read by this CTA
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
+  if (a.acc != nullptr && a.logits != nullptr) {
+    // the running scores of this CTA's own entries, from the logits it
+    // stored; four entries per thread per round, the loads of a round issued
+    // before the first use
+    const int ctx = kv.ctx_len[b];
+    const int e_end = e_begin + n_seg;
+    const float* lg = a.logits + (int64_t)u * a.max_entries * G;
+    float* ar = a.acc + (int64_t)u * a.acc_stride;
+    constexpr int U = 4;
+    for (int e00 = e_begin + threadIdx.x; e00 < e_end; e00 += U * 128) {
+      int sl[U];
+      float lv[U][G], old[U];
+#pragma unroll
+      for (int kk = 0; kk < U; ++kk) {
+        const int e = e00 + kk * 128;
+        sl[kk] = (e < e_end && s_rows[e - e_begin] >= 0) ? view_slot(a, b, g, e, ctx) : -1;
+#pragma unroll
+        for (int j = 0; j < G; ++j) lv[kk][j] = sl[kk] >= 0 ? __ldcg(lg + (int64_t)e * G + j) : 0.f;
+        old[kk] = sl[kk] >= 0 ? __ldcg(ar + sl[kk]) : 0.f;
+      }
+#pragma unroll
+      for (int kk = 0; kk < U; ++kk) {
+        float ps = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) ps += ex2(lv[kk][j] - s_M[j]) * s_invL[j];
+        if (sl[kk] >= 0) ar[sl[kk]] = old[kk] + ps;
+      }
+    }
+  }
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 struct DecodeWs {
@@ -803,6 +1029,7 @@ struct DecodeSplit {
   int n_cta;
   int k_al, w_al;  // aligned split (k_al = 0: stream split)
   int max_parts;   // partial slots per unit
+  int k_cl;        // cluster split: CTAs per unit, 0 where it does not apply
 };
 
 // CTA slots of the staged kernel on GB300: 152 SMs x 4 resident CTAs.
@@ -829,6 +1056,15 @@ static DecodeSplit make_split(const se_paged_kv* kv, int max_entries) {
   const int w = max(chunk / SE, 1);
   const int k = cdiv(d.sp, w);
   const int64_t n_al = units * k;
+  // cluster split: the fewest CTAs per unit (a power of two up to 16) that
+  // keep every CTA within kMaxChunk entries and give about four CTAs per SM
+  d.k_cl = 0;
+  const int64_t w_cl = max(kMaxChunk / SE, 1);
+  for (int kc = 1; kc <= kMaxCluster; kc *= 2) {
+    if (cdiv64(d.sp, kc) > w_cl) continue;
+    d.k_cl = kc;
+    if (units * kc >= kCtaSlots) break;
+  }
   if (n_al <= kCtaSlots || n_al >= 4 * kCtaSlots) {
     d.n_cta = (int)n_al;
     d.k_al = k;
@@ -859,16 +1095,61 @@ static DecodeWs carve_decode(const se_paged_kv* kv, int max_entries, const Decod
   return w;
 }
 
+// Whether clusters of k CTAs of `kernel` (128 threads, `smem` bytes of
+// dynamic shared memory) fit the current device; asked once per device and
+// cluster size.  known[dev] holds bit log2(k) once asked and bit 8 + log2(k)
+// when they fit.
+static bool cluster_fits(const void* kernel, int smem, int k, std::atomic<uint32_t>* known) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int bit = 0;
+  while ((1 << bit) < k) ++bit;
+  const uint32_t v = known[dev].load(std::memory_order_acquire);
+  if (v & (1u << bit)) return (v >> (8 + bit)) & 1u;
+  bool ok = k <= 8 ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (ok) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)k;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(k);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0;
+  }
+  if (!ok) (void)cudaGetLastError();   // a refused query is an answer, not a launch error
+  known[dev].fetch_or((1u << bit) | (ok ? 1u << (8 + bit) : 0u), std::memory_order_acq_rel);
+  return ok;
+}
+
 template <typename T, int D, int G>
 static void launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   using Gm = StagedGeom<T, D, G>;
   const dim3 grid(a.n_cta);
   bool staged = Gm::STAGES > 0;
   if constexpr (Gm::STAGES > 0) {
+    if (a.k_cl > 0) {
+      static std::atomic<uint64_t> attr_cl{0};
+      static std::atomic<uint32_t> known[64];
+      const void* kc = reinterpret_cast<const void*>(&decode_cluster_kernel<T, D, G>);
+      if (allow_smem(kc, Gm::SMEM, attr_cl) && cluster_fits(kc, Gm::SMEM, a.k_cl, known)) {
+        se_launch_cluster(decode_cluster_kernel<T, D, G>,
+                          dim3((unsigned)(a.kv.B * a.kv.Hkv * a.k_cl)), 128, Gm::SMEM, st, a.k_cl, a);
+        return;
+      }
+    }
+    DecodeArgs ak = a;
+    ak.k_cl = 0;
     static std::atomic<uint64_t> attr{0};
     staged = allow_smem(reinterpret_cast<const void*>(&decode_partial_kernel<T, D, G>), Gm::SMEM,
                         attr);
-    if (staged) se_launch(decode_partial_kernel<T, D, G>, grid, 128, Gm::SMEM, st, a);
+    if (staged) se_launch(decode_partial_kernel<T, D, G>, grid, 128, Gm::SMEM, st, ak);
   }
   if (!staged) se_launch(decode_partial_regs_kernel<T, D, G>, grid, 128, 0, st, a);
 }
@@ -922,7 +1203,7 @@ static se_status decode_attn(const se_paged_kv* kv, const void* q, int32_t view,
   DecodeArgs a{*kv, q, view, sel, sel_stride, n_sel, sp.sp, sp.ts, sp.n_cta, sp.k_al, sp.w_al,
                sp.max_parts,
                w.part, acc_scores ? w.logits : nullptr, max_entries, o, acc_scores, acc_stride,
-               w.done};
+               w.done, sp.k_cl};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (clear_counters &&
       cudaMemsetAsync(w.done, 0, sizeof(int32_t) * kv->B * kv->Hkv, st) != cudaSuccess)

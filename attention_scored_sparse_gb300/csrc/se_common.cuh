@@ -48,6 +48,28 @@ inline cudaError_t se_launch(void (*kernel)(K...), dim3 grid, dim3 block, size_t
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
 }
 
+// se_launch for a kernel whose CTAs form clusters of `cluster_x` along x
+// (the grid's x a multiple of it).
+template <typename... K, typename... A>
+inline cudaError_t se_launch_cluster(void (*kernel)(K...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, int cluster_x, A&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
 // Dynamic shared memory above 48 KB is allowed per kernel and per device:
 // sets the limit the first time `kernel` is launched on the current device.
 // `done` holds one bit per device (devices past 64 set it on every call).

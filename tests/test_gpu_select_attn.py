@@ -231,24 +231,56 @@ def _aligned_ctas(units, max_entries):
     return units * W.cdiv(max_entries, chunk)
 
 
-def test_decode_attention_stream_split_matches_oracle(cuda_lib):
-    """320 (sequence, head) units of up to 1153 entries: the unit-aligned
-    chunks would make 640 CTAs (1.05 waves), so the ranges are cut evenly over
-    all units and cross unit boundaries.  Ragged contexts, dense view with
-    running scores and a token view."""
+def _decode_split(units, max_entries, G):
+    """The work split decode attention takes for a shape: a cluster of k CTAs
+    per (sequence, KV head) unit (k a power of two up to 16, each CTA at most
+    1024 entries, the fewest k that give 152 x 4 CTAs), else split-K with a
+    merge through global memory, unit-aligned or cut evenly ("stream")."""
+    se_ = 128 // G
+    sp = W.cdiv(max_entries, se_)
+    k_cl, kc = 0, 1
+    while kc <= 16:
+        if W.cdiv(sp, kc) <= 1024 // se_:
+            k_cl = kc
+            if units * kc >= 608:
+                break
+        kc *= 2
+    if k_cl:
+        return ("cluster", k_cl)
+    n_al = _aligned_ctas(units, max_entries)
+    return ("aligned" if n_al <= 608 or n_al >= 4 * 608 else "stream", n_al)
+
+
+@pytest.mark.parametrize("B,Hkv,G,D,me,path", [
+    (80, 8, 4, 64, 600, ("cluster", 1)),
+    (40, 8, 4, 128, 1153, ("cluster", 2)),
+    (20, 8, 4, 64, 2000, ("cluster", 4)),
+    (10, 8, 4, 64, 3000, ("cluster", 8)),
+    (2, 2, 4, 128, 9000, ("cluster", 16)),
+    (4, 4, 8, 128, 5000, ("cluster", 16)),
+    (2, 2, 4, 128, 20000, ("stream", 628)),
+    (1, 2, 4, 128, 20000, ("aligned", 314)),
+])
+def test_decode_attention_splits_match_oracle(cuda_lib, B, Hkv, G, D, me, path):
+    """Every work split of decode attention against the oracle: clusters of
+    1 to 16 CTAs per unit merging through shared memory, and for views longer
+    than 16 x 1024 entries split-K with the merge in global memory (ranges
+    aligned to units, or cut evenly across unit boundaries).  Ragged contexts
+    (one of a single token, one of 16), dense view with running scores and a
+    token view."""
     se = cuda_lib
-    B, Hkv, G, D, me = 40, 8, 4, 128, 1153
-    assert 608 < _aligned_ctas(B * Hkv, me) < 4 * 608     # the shape takes the even split
+    assert _decode_split(B * Hkv, me, G) == path
     dtype = torch.bfloat16
-    shape = W.Shape(name="dstream", B=B, Hq=Hkv * G, Hkv=Hkv, D=D, page_size=16, ctx=me, dtype=dtype)
+    tag = f"dsplit{B}_{me}"
+    shape = W.Shape(name=tag, B=B, Hq=Hkv * G, Hkv=Hkv, D=D, page_size=16, ctx=me, dtype=dtype)
     pc = W.build_paged_cache(shape, num_pages=B * W.cdiv(me, 16) + 3, max_ctx=me, device="cuda",
-                             tag="dstream")
-    rng = np.random.default_rng(11)
+                             tag=tag)
+    rng = np.random.default_rng(me + B)
     ctx = rng.integers(1, me + 1, size=B).astype(np.int32)
-    ctx[:3] = [me, 1, 16]
+    ctx[:3] = [me, 1, 16][:B]
     pc.ctx_len.copy_(torch.from_numpy(ctx))
     c = ocache.from_tensors(pc)
-    q = W.normal((B, shape.Hq, D), dtype, "cuda", "dstream", "q")
+    q = W.normal((B, shape.Hq, D), dtype, "cuda", tag, "q")
     qv = q.double().cpu().numpy()
     n_tok = 1100
     sel_t = np.full((B, Hkv, n_tok), -1, dtype=np.int32)
@@ -275,6 +307,28 @@ def test_decode_attention_stream_split_matches_oracle(cuda_lib):
                 expect = np.zeros(stride)
                 expect[slots] += p
                 np.testing.assert_allclose(accg[b, g], expect, rtol=1e-4, atol=1e-6)
+
+
+def test_decode_attention_repeats_bit_for_bit(cuda_lib):
+    """The cluster merge sums the partials of an element in a fixed order and
+    the split-K merge in the order of the partial slots: repeated calls give
+    the same output and running scores bit for bit."""
+    se = cuda_lib
+    for B, Hkv, me in [(2, 2, 9000), (2, 2, 20000)]:
+        tag = f"drep{me}"
+        shape = W.Shape(name=tag, B=B, Hq=Hkv * 4, Hkv=Hkv, D=128, page_size=16, ctx=me,
+                        dtype=torch.bfloat16)
+        pc = W.build_paged_cache(shape, num_pages=B * W.cdiv(me, 16) + 3, max_ctx=me,
+                                 device="cuda", tag=tag)
+        q = W.normal((B, shape.Hq, 128), torch.bfloat16, "cuda", tag, "q")
+        outs = []
+        for _ in range(3):
+            acc = torch.zeros((B, Hkv, me), device="cuda")
+            outs.append((H.run_decode(pc, shape.Hq, q, se.SE_VIEW_DENSE, acc=acc), acc))
+        torch.cuda.synchronize()
+        assert int(pc.status.item()) == 0
+        for o, acc in outs[1:]:
+            assert torch.equal(o, outs[0][0]) and torch.equal(acc, outs[0][1])
 
 
 def test_decode_attention_special_cases(cuda_lib):
