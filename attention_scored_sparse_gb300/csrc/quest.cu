@@ -65,12 +65,43 @@ __global__ void quest_meta_kernel(se_paged_kv kv, T* kmin, T* kmax) {
   }
 }
 
-// Page bound U for every full block.  grid: (cdiv(max_blocks, 64), Hkv, B),
-// 256 threads = 8 warps x 2 half-warps; each half-warp takes four blocks
-// (16 apart, so a warp's block-table reads are contiguous) with all their
-// loads in flight together.  D = 128 bf16: lane t of the half-warp owns dims
-// [8t, 8t+8).
-constexpr int kBoundPages = 4;   // blocks per half-warp
+// Candidate and forced ranges of sequence b's top-k: candidates are the full
+// blocks [0, nb - 1), the current block nb - 1 is forced.  A sequence longer
+// than the bound buffer is reported and selected among its first max_blocks.
+struct QuestRanges {
+  int32_t* cand_lo;
+  int32_t* cand_hi;
+  int32_t* flo;
+  int32_t* fhi;
+};
+
+SE_DEV void write_ranges(const QuestRanges& r, int32_t* status, int b, int nb, int max_blocks) {
+  if (nb > max_blocks) {
+    set_status(status, SE_ERR_BOUNDS);
+    nb = max_blocks;
+  }
+  r.cand_lo[b] = 0;
+  r.cand_hi[b] = max(nb - 1, 0);
+  r.flo[b] = max(nb - 1, 0);
+  r.fhi[b] = nb;
+}
+
+// Page bound U for every full block; CTA (0, 0, b) also writes sequence b's
+// ranges.  grid: (cdiv(max_blocks, kBoundPages * 16 / hpc), Hkv / hpc, B),
+// 256 threads = 8 warps; warp w serves KV head blockIdx.y * hpc + w % hpc
+// (hpc = heads per CTA, min(Hkv, 8)), so the warps of a CTA read the kmin /
+// kmax rows of all hpc heads of a page together: hpc x 256 contiguous bytes
+// each, the heads of a physical page being adjacent in the metadata.  Each
+// half-warp takes kBoundPages blocks (16 / hpc apart, so a warp's
+// block-table reads are contiguous) with all their loads in flight together.
+// The block-table reads do not wait for ctx_len (only the mask does).
+// D = 128 bf16: lane t of the half-warp owns dims [8t, 8t+8).
+//
+// The sum over the group's heads is taken on the query side: with
+// kmax >= kmin, max(q kmax, q kmin) = max(q, 0) kmax + min(q, 0) kmin, so
+// U = sum_d (sum_h max(q_hd, 0)) kmax_d + (sum_h min(q_hd, 0)) kmin_d --
+// two FMAs per dimension whatever the group size, and 16 query registers.
+constexpr int kBoundPages = 8;   // blocks per half-warp
 
 template <int G>
 __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
@@ -78,23 +109,29 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
                                                                const __nv_bfloat16* __restrict__ kmax,
                                                                const __nv_bfloat16* __restrict__ q,
                                                                float* __restrict__ U,
-                                                               int64_t u_stride) {
+                                                               int64_t u_stride, int hpc,
+                                                               QuestRanges rg) {
   pdl_enter();
-  const int g = blockIdx.y, b = blockIdx.z;
+  const int b = blockIdx.z;
   const int P = kv.page_size;
-  const int nb = cdiv(kv.ctx_len[b], P);
-  const int half = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int warp = threadIdx.x >> 5, t = threadIdx.x & 15;
+  const int g = blockIdx.y * hpc + warp % hpc;
+  const int rows = 16 / hpc;                                  // half-warps per head
+  const int hi = (warp / hpc) * 2 + ((threadIdx.x >> 4) & 1);  // this half-warp among them
+  const int ctx = kv.ctx_len[b];
   const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   int blk[kBoundPages], page[kBoundPages];
-  bool act[kBoundPages];
 #pragma unroll
   for (int u = 0; u < kBoundPages; ++u) {
-    blk[u] = blockIdx.x * 16 * kBoundPages + u * 16 + half;
-    act[u] = blk[u] < nb - 1 && blk[u] < u_stride;
-    page[u] = act[u] ? bt[blk[u]] : 0;
+    blk[u] = blockIdx.x * rows * kBoundPages + u * rows + hi;
+    page[u] = blk[u] < u_stride ? bt[blk[u]] : -1;
   }
-  // max(q kmax, q kmin) = max(q, 0) kmax + min(q, 0) kmin: two FMAs per term
-  float qp[G][8], qn[G][8];
+  float qp[8], qn[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    qp[i] = 0.f;
+    qn[i] = 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const uint4 u = ldg_nc_v4(q + ((int64_t)b * kv.Hq + g * G + j) * kv.D + t * 8);
@@ -102,18 +139,24 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
     unpack8_bf16(u, qv);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      qp[j][i] = fmaxf(qv[i], 0.f);
-      qn[j][i] = fminf(qv[i], 0.f);
+      qp[i] += fmaxf(qv[i], 0.f);
+      qn[i] += fminf(qv[i], 0.f);
     }
   }
+  const int nb = cdiv(ctx, P);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    write_ranges(rg, kv.status, b, nb, (int)u_stride);
+  bool act[kBoundPages];
   uint4 mnr[kBoundPages], mxr[kBoundPages];
 #pragma unroll
-  for (int u = 0; u < kBoundPages; ++u)
+  for (int u = 0; u < kBoundPages; ++u) {
+    act[u] = blk[u] < nb - 1 && page[u] >= 0 && page[u] < kv.num_pages;
     if (act[u]) {
       const int64_t o = ((int64_t)page[u] * kv.Hkv + g) * kv.D + t * 8;
       mnr[u] = ldg_nc_v4(kmin + o);
       mxr[u] = ldg_nc_v4(kmax + o);
     }
+  }
 #pragma unroll
   for (int u = 0; u < kBoundPages; ++u) {
     float acc = 0.f;
@@ -122,12 +165,7 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
       unpack8_bf16(mnr[u], mn);
       unpack8_bf16(mxr[u], mx);
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float part = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) part = fmaf(qn[j][i], mn[i], fmaf(qp[j][i], mx[i], part));
-        acc += part;
-      }
+      for (int i = 0; i < 8; ++i) acc = fmaf(qn[i], mn[i], fmaf(qp[i], mx[i], acc));
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -135,17 +173,21 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
   }
 }
 
-// Generic bound (any D, fp32 or bf16): one thread per (block, group).
+// Generic bound (any D, fp32 or bf16): one thread per (block, group); CTA
+// (0, 0, b) also writes sequence b's ranges.
 template <typename T>
 __global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const T* kmax,
-                                           const T* q, float* U, int64_t u_stride) {
+                                           const T* q, float* U, int64_t u_stride, QuestRanges rg) {
   pdl_enter();
   const int g = blockIdx.y, b = blockIdx.z;
   const int blk = blockIdx.x * blockDim.x + threadIdx.x;
   const int nb = cdiv(kv.ctx_len[b], kv.page_size);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    write_ranges(rg, kv.status, b, nb, (int)u_stride);
   if (blk >= nb - 1 || blk >= u_stride) return;
   const int G = kv.Hq / kv.Hkv;
   const int page = kv.block_table[(int64_t)b * kv.max_pages_per_seq + blk];
+  if (page < 0 || page >= kv.num_pages) return;
   const int64_t o = ((int64_t)page * kv.Hkv + g) * kv.D;
   float acc = 0.f;
   for (int j = 0; j < G; ++j) {
@@ -158,24 +200,6 @@ __global__ void quest_bound_generic_kernel(se_paged_kv kv, const T* kmin, const 
     acc += part;
   }
   U[((int64_t)b * kv.Hkv + g) * u_stride + blk] = acc;
-}
-
-// candidates [0, nblocks - 1), forced = [nblocks - 1, nblocks)
-__global__ void quest_ranges_kernel(const int32_t* ctx_len, int B, int P, int max_blocks,
-                                    int32_t* status, int32_t* cand_lo, int32_t* cand_hi,
-                                    int32_t* flo, int32_t* fhi) {
-  pdl_enter();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  int nb = cdiv(ctx_len[b], P);
-  if (nb > max_blocks) {  // bound buffer too short: select among the first max_blocks
-    set_status(status, SE_ERR_BOUNDS);
-    nb = max_blocks;
-  }
-  cand_lo[b] = 0;
-  cand_hi[b] = max(nb - 1, 0);
-  flo[b] = max(nb - 1, 0);
-  fhi[b] = nb;
 }
 
 struct QuestWs {
@@ -245,29 +269,28 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = kv->Hq / kv->Hkv;
-  dim3 grid(cdiv(max_blocks, 16 * kBoundPages), kv->Hkv, kv->B);
-  if (kv->dtype == SE_BF16 && kv->D == 128 && (G == 1 || G == 2 || G == 4 || G == 8)) {
+  const QuestRanges rg{w.cand_lo, w.cand_hi, w.flo, w.fhi};
+  const int hpc = kv->Hkv % 8 == 0 ? 8 : (kv->Hkv < 8 && 8 % kv->Hkv == 0 ? kv->Hkv : 0);
+  if (kv->dtype == SE_BF16 && kv->D == 128 && hpc > 0 && (G == 1 || G == 2 || G == 4 || G == 8)) {
+    const dim3 grid(cdiv(max_blocks, 16 / hpc * kBoundPages), kv->Hkv / hpc, kv->B);
     auto km = static_cast<const __nv_bfloat16*>(kmin);
     auto kx = static_cast<const __nv_bfloat16*>(kmax);
     auto qq = static_cast<const __nv_bfloat16*>(q);
-    if (G == 1) se_launch(quest_bound_bf16_kernel<1>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 2) se_launch(quest_bound_bf16_kernel<2>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 4) se_launch(quest_bound_bf16_kernel<4>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
-    if (G == 8) se_launch(quest_bound_bf16_kernel<8>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride);
+    if (G == 1) se_launch(quest_bound_bf16_kernel<1>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 2) se_launch(quest_bound_bf16_kernel<2>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 4) se_launch(quest_bound_bf16_kernel<4>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 8) se_launch(quest_bound_bf16_kernel<8>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
   } else {
     dim3 g2(cdiv(max_blocks, 128), kv->Hkv, kv->B);
     if (kv->dtype == SE_BF16)
       se_launch(quest_bound_generic_kernel<__nv_bfloat16>, g2, 128, 0, st,
           *kv, static_cast<const __nv_bfloat16*>(kmin), static_cast<const __nv_bfloat16*>(kmax),
-          static_cast<const __nv_bfloat16*>(q), w.U, w.u_stride);
+          static_cast<const __nv_bfloat16*>(q), w.U, w.u_stride, rg);
     else
       se_launch(quest_bound_generic_kernel<float>, g2, 128, 0, st,
           *kv, static_cast<const float*>(kmin), static_cast<const float*>(kmax),
-          static_cast<const float*>(q), w.U, w.u_stride);
+          static_cast<const float*>(q), w.U, w.u_stride, rg);
   }
-  se_launch(quest_ranges_kernel, cdiv(kv->B, 256), 256, 0, st, kv->ctx_len, kv->B, kv->page_size,
-                                                        max_blocks, kv->status, w.cand_lo,
-                                                        w.cand_hi, w.flo, w.fhi);
   s = launch_topk_select_pages(kv->B, kv->Hkv, w.U, w.u_stride, w.cand_lo, w.cand_hi, w.flo,
                                w.fhi, page_idx, top_pages + 1, n_sel, kv->status, top_pages,
                                max_blocks, st);

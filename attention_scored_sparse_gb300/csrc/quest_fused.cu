@@ -69,9 +69,7 @@ SE_DEV void block_kth_key(const uint32_t (&key)[ITEMS], int kk, int* hist, int* 
       const uint32_t dmask = (uint32_t)nbins - 1u;
       for (int i = tid; i < nbins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i)
-        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+      hist_add_keys<ITEMS>(hist, key, shift, dmask, pmask, prefix);
       __syncthreads();
       radix_find_digit(hist, nbins, remaining, tmp, s_digit, s_rem);
       prefix |= (uint32_t)*s_digit << shift;

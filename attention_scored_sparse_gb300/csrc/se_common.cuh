@@ -163,6 +163,31 @@ SE_DEV int block_exclusive_scan(int v, int* tmp, int* total) {
   return base + x - v;
 }
 
+// Counts a thread's keys (ITEMS consecutive candidates) into hist: keys of
+// the digit `shift`/`dmask` whose higher digits equal `prefix` (mask
+// `pmask`), key 0 = absent.  Runs of one bin are added by one atomic: close
+// candidates tend to share a bin, and the lanes of a warp adding to one bin
+// at once would serialise.
+template <int ITEMS>
+SE_DEV void hist_add_keys(int* hist, const uint32_t (&key)[ITEMS], int shift, uint32_t dmask,
+                          uint32_t pmask, uint32_t prefix) {
+  uint32_t cur = 0xffffffffu;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    if (key[i] != 0u && (key[i] & pmask) == prefix) {
+      const uint32_t bin = (key[i] >> shift) & dmask;
+      if (bin != cur) {
+        if (cnt) atomicAdd(&hist[cur], cnt);
+        cur = bin;
+        cnt = 0;
+      }
+      ++cnt;
+    }
+  }
+  if (cnt) atomicAdd(&hist[cur], cnt);
+}
+
 // Radix-select step: hist[0 .. nbins) holds the candidate count per digit;
 // finds the digit that holds the `remaining`-th largest key (counting from
 // the top digit down) and how many keys of that digit are still needed.

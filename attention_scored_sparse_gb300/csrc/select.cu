@@ -121,7 +121,15 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
     return;
   }
   const float* row = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
-  for (int e = tid; e < n; e += 1024) s_sc[padded<ITEMS>(e)] = row[lo + e];
+  {
+    // every load of the thread in flight before the first store
+    float v[ITEMS];
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) v[i] = tid + i * 1024 < n ? row[lo + tid + i * 1024] : 0.f;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+      if (tid + i * 1024 < n) s_sc[padded<ITEMS>(tid + i * 1024)] = v[i];
+  }
   if (tid == 0) s_before_force = 0;
   __syncthreads();
 
@@ -147,9 +155,7 @@ __global__ void __launch_bounds__(1024, 1) topk_kernel(SelectArgs a, int pool, i
       const uint32_t dmask = (uint32_t)nbins - 1u;
       for (int i = tid; i < nbins; i += 1024) hist[i] = 0;
       __syncthreads();
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i)
-        if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+      hist_add_keys<ITEMS>(hist, key, shift, dmask, pmask, prefix);
       __syncthreads();
       radix_find_digit(hist, nbins, remaining, tmp, &s_digit, &s_rem);
       prefix |= (uint32_t)s_digit << shift;
@@ -246,9 +252,24 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
   const float* row = a.scores + ((int64_t)b * a.Hkv + h) * a.stride;
   // local smem index x <-> element r0 - halo + x
   const int x1 = bad ? 0 : (r1 + halo) - (r0 - halo);
-  for (int x = tid; x < x1; x += 1024) {
-    const int e = r0 - halo + x;
-    s_sc[padded<ITEMS>(x)] = (e >= 0 && e < n) ? row[lo + e] : 0.f;
+  // every load of the thread in flight before the first store; the range
+  // (at most 1024 ITEMS) and its two halos take at most ITEMS + 1 rounds
+  // when the halos add up to 1024 or less
+  if (2 * halo <= 1024) {
+    float v[ITEMS + 1];
+#pragma unroll
+    for (int i = 0; i <= ITEMS; ++i) {
+      const int x = tid + i * 1024, e = r0 - halo + x;
+      v[i] = (x < x1 && e >= 0 && e < n) ? row[lo + e] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i <= ITEMS; ++i)
+      if (tid + i * 1024 < x1) s_sc[padded<ITEMS>(tid + i * 1024)] = v[i];
+  } else {
+    for (int x = tid; x < x1; x += 1024) {
+      const int e = r0 - halo + x;
+      s_sc[padded<ITEMS>(x)] = (e >= 0 && e < n) ? row[lo + e] : 0.f;
+    }
   }
   if (tid < 4) s_cnt[tid] = 0;
   __syncthreads();
@@ -272,9 +293,7 @@ topk_cluster_kernel(SelectArgs a, int pool, int k) {
     int* hb = hist[round & 1];
     for (int i = tid; i < nbins; i += 1024) hb[i] = 0;
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i)
-      if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hb[(key[i] >> shift) & dmask], 1);
+    hist_add_keys<ITEMS>(hb, key, shift, dmask, pmask, prefix);
     cluster.sync();                    // every CTA's histogram (and round 0: count) is complete
     if (round == 0) {
       int forced_in_total = 0;
