@@ -37,6 +37,7 @@ EXPORTED = [
     "se_score_window", "se_score_window_workspace_size", "se_score_window_one_launch",
     "se_topk_select",
     "se_compact_evict", "se_compact_evict_workspace_size",
+    "se_compact_decode", "se_compact_decode_workspace_size",
     "se_prune_span", "se_prune_span_workspace_size",
     "se_quest_build_meta", "se_quest_page_select", "se_quest_page_select_workspace_size",
     "se_sparse_decode_attn", "se_sparse_decode_attn_workspace_size",
@@ -93,6 +94,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "se_compact_evict": [P, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                              c_int64, c_void_p, c_size_t, c_void_p],
         "se_compact_evict_workspace_size": [P, c_int32],
+        "se_compact_decode": [P, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_int64,
+                              c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p],
+        "se_compact_decode_workspace_size": [P, c_int32, c_int32],
         "se_prune_span": [P, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64,
                           c_void_p, c_size_t, c_void_p],
         "se_prune_span_workspace_size": [P],
@@ -258,6 +262,17 @@ def se_compact_evict(kv, mode, keep_idx, *, n_keep=None, first_slot=None, max_ke
         aux.shape[-1] if aux is not None else 0, _ptr(ws), ws.numel(), _stream(stream)))
 
 
+def se_compact_decode(kv, keep_idx, *, n_keep, first_slot, max_keep, q, o, max_entries,
+                      aux=None, workspace=None, stream=None):
+    d = ctypes.byref(kv)
+    need = _lib.se_compact_decode_workspace_size(d, max_keep, max_entries)
+    ws = _ws(workspace, need, keep_idx.device)
+    _check("se_compact_decode", _lib.se_compact_decode(
+        d, _ptr(keep_idx), keep_idx.shape[-1], _ptr(n_keep), _ptr(first_slot), max_keep, _ptr(aux),
+        aux.shape[-1] if aux is not None else 0, _ptr(q), _ptr(o), max_entries, _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
 def se_prune_span(kv, L, R, mask, *, n_busy=None, aux=None, workspace=None, stream=None):
     d = ctypes.byref(kv)
     need = _lib.se_prune_span_workspace_size(d)
@@ -387,6 +402,7 @@ def workspace_sizes(kv, *, w=1, n_max=1, max_keep=0, max_blocks=1, max_entries=1
     return {
         "score_window": _lib.se_score_window_workspace_size(d, w, n_max),
         "compact_evict": _lib.se_compact_evict_workspace_size(d, max_keep),
+        "compact_decode": _lib.se_compact_decode_workspace_size(d, max_keep, max_entries),
         "prune_span": _lib.se_prune_span_workspace_size(d),
         "quest_page_select": _lib.se_quest_page_select_workspace_size(d, max_blocks),
         "sparse_decode_attn": _lib.se_sparse_decode_attn_workspace_size(d, max_entries),

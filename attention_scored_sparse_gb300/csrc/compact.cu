@@ -13,53 +13,15 @@
 // pages are popped from the top of the free-list stack in ascending
 // (sequence, block) order and old pages pushed afterwards in the same order;
 // the same order makes block tables and the free list deterministic.
-#include "se_common.cuh"
+#include "compact_ws.cuh"
 
 namespace se {
 
-struct CompactCtrl {
-  int32_t abort;
-  int32_t top0;
-  int32_t total_new;
-  int32_t total_push;
-};
-
-struct CompactWs {
-  CompactCtrl* ctrl;
-  int32_t* pb;        // [B] first rewritten block
-  int32_t* n_new;     // [B] fresh pages
-  int32_t* old_blocks;// [B] blocks before the call
-  int32_t* new_ctx;   // [B]
-  int32_t* old_ctx;   // [B]
-  int32_t* off_new;   // [B] prefix of n_new
-  int32_t* push_count;// [B] old pages of the sequence that go back to the free list
-  int32_t* newpage;   // [B * max_pages_per_seq]
-  int32_t* slot_tmp;  // [B][Hkv][row]  new slot_map values from pb*P on
-  float* aux_tmp;     // [B][Hkv][row]
-  int64_t row;        // max_keep + page_size
-};
-
-static CompactWs carve_compact(const se_paged_kv* kv, int32_t max_keep, void* ws, bool aux,
-                               size_t* bytes) {
-  WsCarver c(ws);
-  CompactWs w;
-  const int B = kv->B;
-  w.ctrl = c.take<CompactCtrl>(1);
-  w.pb = c.take<int32_t>(B);
-  w.n_new = c.take<int32_t>(B);
-  w.old_blocks = c.take<int32_t>(B);
-  w.new_ctx = c.take<int32_t>(B);
-  w.old_ctx = c.take<int32_t>(B);
-  w.off_new = c.take<int32_t>(B);
-  w.push_count = c.take<int32_t>(B);
-  w.newpage = c.take<int32_t>((size_t)B * kv->max_pages_per_seq);
-  w.row = (int64_t)max_keep + kv->page_size;
-  w.slot_tmp = c.take<int32_t>((size_t)B * kv->Hkv * w.row);
-  w.aux_tmp = aux ? c.take<float>((size_t)B * kv->Hkv * w.row) : nullptr;
-  if (!aux) c.take<float>((size_t)B * kv->Hkv * w.row);  // size does not depend on aux
-  *bytes = c.bytes();
-  return w;
-}
+// compact_decode_kernel's launcher (decode.cu)
+se_status launch_compact_decode(const se_paged_kv* kv, const int32_t* keep, int32_t keep_stride,
+                                const int32_t* first_slot, const float* aux, int64_t aux_stride,
+                                const CompactWs& w, const void* q, void* o, int32_t max_entries,
+                                cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // FRESH_PAGES compaction
@@ -104,6 +66,7 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
       nn = ok ? max(cdiv(nctx, P) - pb, 0) : 0;
       w.pb[b] = pb;
       w.n_new[b] = nn;
+      w.push_count[b] = 0;   // counted by the gather
       w.old_blocks[b] = cdiv(ctx, P);
       w.new_ctx[b] = nctx;
       w.old_ctx[b] = ctx;
@@ -144,24 +107,7 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
   const int fs = first_slot[b];
   const int top0 = w.ctrl->top0;
   const int pop0 = top0 - 1 - w.off_new[b];   // free_list index of this sequence's first fresh page
-  if (blockIdx.x == 0 && h == 0) {
-    // record the fresh pages for the commit kernel, count the old pages that
-    // return to the free list (busy pages only lose a reference)
-    __shared__ int s_cnt;
-    if (threadIdx.x == 0) s_cnt = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < w.n_new[b]; i += blockDim.x)
-      w.newpage[w.off_new[b] + i] = kv.free_list[pop0 - i];
-    const int32_t* btb = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-    int cnt = 0;
-    for (int blk = pb + threadIdx.x; blk < w.old_blocks[b]; blk += blockDim.x) {
-      const int page = btb[blk];
-      cnt += (page >= 0 && (kv.page_refcount == nullptr || kv.page_refcount[page] <= 1)) ? 1 : 0;
-    }
-    if (cnt) atomicAdd(&s_cnt, cnt);
-    __syncthreads();
-    if (threadIdx.x == 0) w.push_count[b] = s_cnt;
-  }
+  if (blockIdx.x == 0 && h == 0) record_fresh_pages(kv, w, b);
   const int head = fs - pb * P;
   const int total = head + (w.new_ctx[b] - fs);
   const int e0 = blockIdx.x * entries_per_cta;
@@ -232,53 +178,71 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(
 }
 
 // Commits block tables, lengths, refcounts and free-list pushes of sequence
-// b (one CTA of 1024 threads).
+// b (one CTA).  Every thread takes kCommitItems consecutive blocks per round
+// with all their loads in flight, so a round costs one block scan; the scan
+// keeps the pushes in ascending block order.
+constexpr int kCommitItems = 4;
+
 SE_DEV void commit_pages(const se_paged_kv& kv, const CompactWs& w, int b) {
   __shared__ int tmp[33];
+  __shared__ int s_off, s_total;
   const int tid = threadIdx.x;
   const int pb = w.pb[b], nn = w.n_new[b], ob = w.old_blocks[b];
   const int top0 = w.ctrl->top0, total_new = w.ctrl->total_new;
-  __shared__ int s_off, s_total;
-  if (tid == 0) {
-    int off = 0, total = 0;
-    for (int bb = 0; bb < kv.B; ++bb) {
-      const int cnt = w.push_count[bb];
-      off += bb < b ? cnt : 0;
-      total += cnt;
+  // pushes of the sequences before b, and of all of them
+  {
+    int run = 0;
+    for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
+      const int bb = b0 + tid;
+      const int cnt = bb < kv.B ? w.push_count[bb] : 0;
+      int tot;
+      const int ex = block_exclusive_scan(cnt, tmp, &tot);
+      if (bb == b) s_off = run + ex;
+      run += tot;
     }
-    s_off = off;
-    s_total = total;
+    if (tid == 0) s_total = run;
   }
   __syncthreads();
   const int push_base = top0 - total_new + s_off;
+  const int off_new = w.off_new[b];
   int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   const int end = max(ob, pb + nn);
   int running = 0;
-  for (int c0 = pb; c0 < end; c0 += blockDim.x) {
-    const int blk = c0 + tid;
-    int old = -1;
-    bool busy = false, push = false;
-    if (blk < ob) {
-      old = bt[blk];
-      busy = old >= 0 && kv.page_refcount != nullptr && kv.page_refcount[old] > 1;
-      push = old >= 0 && !busy;
+  for (int c0 = pb; c0 < end; c0 += blockDim.x * kCommitItems) {
+    int old[kCommitItems], np[kCommitItems], rc[kCommitItems];
+#pragma unroll
+    for (int i = 0; i < kCommitItems; ++i) {
+      const int blk = c0 + tid * kCommitItems + i;
+      old[i] = blk < ob ? bt[blk] : -1;
+      np[i] = (blk < end && blk < pb + nn) ? w.newpage[off_new + blk - pb] : -1;
     }
+#pragma unroll
+    for (int i = 0; i < kCommitItems; ++i)
+      rc[i] = (old[i] >= 0 && kv.page_refcount != nullptr) ? kv.page_refcount[old[i]] : 1;
+    int n_push = 0;
+#pragma unroll
+    for (int i = 0; i < kCommitItems; ++i) n_push += (old[i] >= 0 && rc[i] <= 1) ? 1 : 0;
     int total;
-    const int pos = block_exclusive_scan(push ? 1 : 0, tmp, &total);
-    if (blk < end) {
-      if (blk < pb + nn) {
-        const int np = w.newpage[w.off_new[b] + blk - pb];
-        bt[blk] = np;
-        if (kv.page_refcount) kv.page_refcount[np] = 1;
-      } else {
-        bt[blk] = -1;
+    int pos = block_exclusive_scan(n_push, tmp, &total);
+#pragma unroll
+    for (int i = 0; i < kCommitItems; ++i) {
+      const int blk = c0 + tid * kCommitItems + i;
+      if (blk < end) {
+        bt[blk] = np[i];
+        if (np[i] >= 0 && kv.page_refcount) kv.page_refcount[np[i]] = 1;
+      }
+      if (old[i] >= 0) {
+        if (rc[i] <= 1) {
+          if (push_base + running + pos < kv.num_pages) {
+            kv.free_list[push_base + running + pos] = old[i];
+            if (kv.page_refcount) kv.page_refcount[old[i]] = 0;
+          }
+          ++pos;
+        } else {
+          atomicSub(&kv.page_refcount[old[i]], 1);
+        }
       }
     }
-    if (push && push_base + running + pos < kv.num_pages) {
-      kv.free_list[push_base + running + pos] = old;
-      if (kv.page_refcount) kv.page_refcount[old] = 0;
-    }
-    if (busy) atomicSub(&kv.page_refcount[old], 1);
     running += total;
   }
   if (tid == 0) {
@@ -823,15 +787,10 @@ using namespace se;
 // Host entry points
 // ---------------------------------------------------------------------------
 
-static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
-                                int32_t keep_stride, const int32_t* n_keep,
-                                const int32_t* first_slot, int32_t max_keep, float* aux,
-                                int64_t aux_stride, void* ws, size_t ws_bytes,
-                                const int32_t* abort_in, cudaStream_t st) {
-  size_t need = 0;
-  CompactWs w = carve_compact(kv, max_keep, ws, aux != nullptr, &need);
-  if (ws == nullptr || ws_bytes < need) return SE_ERR_INVALID_ARG;
-  se_launch(compact_plan_kernel, 1, 1024, 0, st, *kv, n_keep, first_slot, max_keep, abort_in, w);
+static se_status launch_compact_gather(const se_paged_kv* kv, const int32_t* keep_idx,
+                                       int32_t keep_stride, const int32_t* first_slot,
+                                       int32_t max_keep, float* aux, int64_t aux_stride,
+                                       const CompactWs& w, cudaStream_t st) {
   const int row_bytes = kv->D * (int)elem_size(kv->dtype);
   const int chunks = row_bytes / 16;
   const int max_entries = max_keep + kv->page_size;
@@ -842,26 +801,47 @@ static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
       const int epc = 2 * (256 / 8);
       se_launch(compact_gather_kernel<8>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
-      break;
+      return SE_OK;
     }
     case 16: {
       const int epc = 2 * (256 / 16);
       se_launch(compact_gather_kernel<16>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
-      break;
+      return SE_OK;
     }
     case 32: {
       const int epc = 2 * (256 / 32);
       se_launch(compact_gather_kernel<32>, dim3(cdiv(max_entries, epc), kv->Hkv, kv->B), 256, 0, st,
           *kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, epc);
-      break;
+      return SE_OK;
     }
     default:
       return SE_ERR_UNSUPPORTED;
   }
+}
+
+static void launch_compact_commit(const se_paged_kv* kv, float* aux, int64_t aux_stride,
+                                  const CompactWs& w, cudaStream_t st) {
   const int max_span = kv->max_pages_per_seq * kv->page_size;
   se_launch(compact_commit_kernel, dim3(1 + cdiv(max_span, 4096), kv->Hkv, kv->B), 1024, 0, st,
       *kv, aux, aux_stride, w);
+}
+
+static se_status launch_compact(const se_paged_kv* kv, const int32_t* keep_idx,
+                                int32_t keep_stride, const int32_t* n_keep,
+                                const int32_t* first_slot, int32_t max_keep, float* aux,
+                                int64_t aux_stride, void* ws, size_t ws_bytes,
+                                const int32_t* abort_in, cudaStream_t st) {
+  size_t need = 0;
+  CompactWs w = carve_compact(kv, max_keep, ws, aux != nullptr, &need);
+  if (ws == nullptr || ws_bytes < need) return SE_ERR_INVALID_ARG;
+  const int chunks = kv->D * (int)elem_size(kv->dtype) / 16;
+  if (chunks != 8 && chunks != 16 && chunks != 32) return SE_ERR_UNSUPPORTED;
+  se_launch(compact_plan_kernel, 1, 1024, 0, st, *kv, n_keep, first_slot, max_keep, abort_in, w);
+  se_status s = launch_compact_gather(kv, keep_idx, keep_stride, first_slot, max_keep, aux,
+                                      aux_stride, w, st);
+  if (s != SE_OK) return s;
+  launch_compact_commit(kv, aux, aux_stride, w, st);
   return se_last_launch_status();
 }
 
@@ -897,6 +877,56 @@ extern "C" se_status se_compact_evict(const se_paged_kv* kv, int32_t mode,
     return se_last_launch_status();
   }
   return SE_ERR_INVALID_ARG;
+}
+
+// Compaction and decode attention in one pass over the kept entries: the
+// compaction's plan, then compact_decode_kernel (gather + decode), then its
+// commit; shapes that kernel does not take run the plain compaction and then
+// decode attention over the dense view of the result.
+extern "C" size_t se_compact_decode_workspace_size(const se_paged_kv* kv, int32_t max_keep,
+                                                   int32_t max_entries) {
+  if (kv == nullptr || max_keep < 0 || max_entries < 1) return 0;
+  size_t a = 0;
+  carve_compact(kv, max_keep, nullptr, true, &a);
+  return align_up(a, 256) + se_sparse_decode_attn_workspace_size(kv, max_entries);
+}
+
+extern "C" se_status se_compact_decode(const se_paged_kv* kv, const int32_t* keep_idx,
+                                       int32_t keep_stride, const int32_t* n_keep,
+                                       const int32_t* first_slot, int32_t max_keep, float* aux,
+                                       int64_t aux_stride, const void* q, void* o,
+                                       int32_t max_entries, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  se_status s = se_check_kv(kv);
+  if (s != SE_OK) return s;
+  if (keep_idx == nullptr || n_keep == nullptr || first_slot == nullptr || q == nullptr ||
+      o == nullptr || workspace == nullptr || max_keep < 0 || keep_stride < max_keep ||
+      max_entries < 1)
+    return SE_ERR_INVALID_ARG;
+  if (workspace_bytes < se_compact_decode_workspace_size(kv, max_keep, max_entries))
+    return SE_ERR_INVALID_ARG;
+  const int chunks = kv->D * (int)elem_size(kv->dtype) / 16;
+  if (chunks != 8 && chunks != 16 && chunks != 32) return SE_ERR_UNSUPPORTED;
+  size_t ca = 0;
+  CompactWs w = carve_compact(kv, max_keep, workspace, aux != nullptr, &ca);
+  ca = align_up(ca, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  se_launch(compact_plan_kernel, 1, 1024, 0, st, *kv, n_keep, first_slot, max_keep,
+            (const int32_t*)nullptr, w);
+  s = launch_compact_decode(kv, keep_idx, keep_stride, first_slot, aux, aux_stride, w, q, o,
+                            max_entries, st);
+  if (s == SE_OK) {
+    launch_compact_commit(kv, aux, aux_stride, w, st);
+    return se_last_launch_status();
+  }
+  if (s != SE_ERR_UNSUPPORTED) return s;
+  s = launch_compact_gather(kv, keep_idx, keep_stride, first_slot, max_keep, aux, aux_stride, w, st);
+  if (s != SE_OK) return s;
+  launch_compact_commit(kv, aux, aux_stride, w, st);
+  s = se_last_launch_status();
+  if (s != SE_OK) return s;
+  return se_sparse_decode_attn(kv, q, SE_VIEW_DENSE, nullptr, 0, 0, max_entries, o, nullptr, 0,
+                               static_cast<char*>(workspace) + ca, workspace_bytes - ca, stream);
 }
 
 extern "C" size_t se_append_kv_workspace_size(const se_paged_kv* kv) {

@@ -19,6 +19,7 @@
 
 #include <cooperative_groups.h>
 
+#include "compact_ws.cuh"
 #include "tc_primitives.cuh"
 
 namespace se {
@@ -444,6 +445,19 @@ SE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
       : "memory");
 }
 
+// Bulk copy shared -> global (the TMA engine), tracked in the issuing
+// thread's bulk group; commit closes the group, wait_read waits until every
+// closed group of the thread has read its shared memory, wait_all until
+// every one has written global memory.
+SE_DEV void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(dst), "r"(tc::smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+SE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+SE_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+SE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // V elements of a K or V row in shared memory, as fp32.
 template <typename T, int V>
 SE_DEV void load_row_smem(const T* r, float* f) {
@@ -515,6 +529,38 @@ SE_DEV void issue_stage(const DecodeArgs& a, int s0, int n_seg, const int32_t* r
   if (lane == 0) tc::mbar_arrive(bar);
 }
 
+// Copies the rows of one landed stage out to the pool: entry x of the stage
+// (x < n) goes to K/V row dst[x] of the pool, none where dst[x] < 0.  Called
+// by all 32 lanes of one warp: a maximal run of consecutive destination rows
+// (within 32 entries) becomes one K and one V bulk store, issued by the lane
+// that starts it; every lane then closes its bulk group (empty for most).
+template <typename T, int D, int G>
+SE_DEV void store_stage(const DecodeArgs& a, const uint8_t* stage, const int32_t* dst, int n,
+                        int lane) {
+  using Gm = StagedGeom<T, D, G>;
+  char* kp = static_cast<char*>(a.kv.k_pool);
+  char* vp = static_cast<char*>(a.kv.v_pool);
+#pragma unroll
+  for (int x0 = 0; x0 < Gm::SE; x0 += 32) {
+    const int x = x0 + lane;
+    const int d = x < n ? dst[x] : -1;
+    const int prev = __shfl_up_sync(0xffffffffu, d, 1);
+    const bool ok = d >= 0;
+    const bool cont = ok && lane > 0 && prev >= 0 && prev + 1 == d;
+    const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+    const uint32_t starts = __ballot_sync(0xffffffffu, ok && !cont);
+    if (ok && !cont) {
+      const uint32_t above = lane == 31 ? 0u : (~0u << (lane + 1));
+      const uint32_t stop = (starts | ~okm) & above;
+      const int len = (stop ? __ffs(stop) - 1 : 32) - lane;
+      const uint32_t bytes = (uint32_t)(len * Gm::RB);
+      bulk_s2g(kp + (int64_t)d * Gm::RB, stage + x * Gm::RB, bytes);
+      bulk_s2g(vp + (int64_t)d * Gm::RB, stage + Gm::SE * Gm::RB + x * Gm::RB, bytes);
+    }
+  }
+  bulk_commit();
+}
+
 // Shared memory of the staged kernels: the stage ring and the per-half-warp
 // softmax states.
 template <int G, int SE>
@@ -569,9 +615,14 @@ SE_DEV int resolve_rows(const DecodeArgs& a, int u, int e_begin, int n, int32_t*
 // stage is idle by then), and all threads have passed a barrier.  A wait
 // that runs out sets the status word and *r.abort and ends the stream; the
 // states are then meaningless but the call still returns normally.
-template <typename T, int D, int G>
+// COPY: every landed stage is also copied out to the pool rows dst[0, n_seg)
+// (store_stage, by warp 0); a buffer is refilled, and the stage memory
+// reused, only after those stores have read it (every lane of warp 0 waits
+// for its own bulk groups).
+template <typename T, int D, int G, bool COPY = false>
 SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T, D, G>::SE>& r,
-                           int u, int e_begin, int n_seg, const int32_t* rows, int& gi, int& gc) {
+                           int u, int e_begin, int n_seg, const int32_t* rows, int& gi, int& gc,
+                           const int32_t* dst = nullptr) {
   using Gm = StagedGeom<T, D, G>;
   constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
   constexpr int V2 = V / 2;
@@ -600,6 +651,10 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
           atomicExch(r.abort, 1);
         }
         break;
+      }
+      if constexpr (COPY) {
+        bulk_wait_read();
+        __syncwarp();
       }
       issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
                            &r.full[n % S], r.valid[n % S], lane);
@@ -636,6 +691,10 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
       const int n = gi;
       const bool free_ok = n < S || tc::mbar_wait(&r.empty[n % S], ((n / S) - 1) & 1, kLimit);
       if (__all_sync(full_mask, free_ok)) {
+        if constexpr (COPY) {
+          bulk_wait_read();   // the stores of the buffer's last stage
+          __syncwarp();
+        }
         issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
                              &r.full[n % S], r.valid[n % S], lane);
         ++gi;
@@ -655,6 +714,9 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
     }
     const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
     const uint8_t* vst = kst + SE * RB;
+    if constexpr (COPY) {
+      if (warp == 0) store_stage<T, D, G>(a, kst, dst + it * SE, min(SE, n_seg - it * SE), lane);
+    }
     const int e0 = e_begin + it * SE + hw * E;
     // K rows are read from the stage one entry at a time; V rows are read
     // again after the probabilities are known (the stage is released after)
@@ -757,6 +819,9 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
   // (each earlier stage was waited on before its buffer was refilled)
   if (producer && lane == 0)
     for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&r.full[i % S], (i / S) & 1, kLimit);
+  if constexpr (COPY) {
+    if (producer) bulk_wait_read();   // the stage memory is reused below
+  }
   float lsum = l_own;
 #pragma unroll
   for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
@@ -843,62 +908,23 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
 
 constexpr int kMaxCluster = 16;   // CTAs of a unit in the cluster split (non-portable above 8)
 
-// grid: units x k CTAs in clusters of k = a.k_cl (a power of two up to 16);
-// 128 threads; dynamic smem StagedGeom::SMEM.  Cluster u is unit u = (b, g);
-// its CTA of rank r streams slices [r sp / k, (r + 1) sp / k) of the unit and
-// combines its half-warp states into one partial (m, l, o) in its own shared
-// memory.  After a cluster barrier every CTA reads the k maxima and sums from
-// its peers' shared memory, merges its own G D / k elements of o from the
-// peers' partials (the partials of an element are summed in a fixed order,
-// so the result does not depend on timing), writes them, and for H2O adds
-// sum_h p_{h,j} to the running score of each of its own entries from the
-// logits it stored.  A second cluster barrier keeps every CTA's shared
-// memory alive until its peers have read it.  Every thread of every CTA
-// reaches both barriers, also after a stage wait has run out.
+// The merge of a cluster split (decode_cluster_kernel): combines the CTA's
+// half-warp states (s_m, s_l, and o over the stage memory as left by
+// stream_segment) into its partial, in place over the first half-warp's o;
+// waits for the cluster; merges this CTA's G D / k elements of o from the
+// peers' partials and writes them; arrives on the cluster barrier that ends
+// the reads of the peers' shared memory (the caller waits on it before it
+// leaves).  Leaves the unit's maximum and 1 / sum of each head in s_M, s_invL.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_cluster_kernel(DecodeArgs a) {
-  using Gm = StagedGeom<T, D, G>;
-  constexpr int SE = Gm::SE, S = Gm::STAGES;
+SE_DEV void cluster_merge(const DecodeArgs& a, cg::cluster_group& cluster, int k, int rank, int b,
+                          int g, uint8_t* stages, float (*s_m)[G], float (*s_l)[G], float* s_M,
+                          float* s_invL) {
   constexpr int GD = G * D;
-  static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
   static_assert(GD % kMaxCluster == 0, "o splits evenly over the cluster");
-  extern __shared__ __align__(1024) uint8_t dsmem[];
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
-  __shared__ uint64_t full[4], empty[4];
-  __shared__ int8_t s_valid[4][SE];
-  __shared__ int32_t s_rows[kMaxChunk];
-  __shared__ float s_p[8][16];
-  __shared__ float s_m[8][G], s_l[8][G];
   __shared__ float s_pm[G], s_pl[G];                            // this CTA's partial: maxima, sums
   __shared__ float s_cm[kMaxCluster][G], s_ce[kMaxCluster][G];  // the peers' maxima; their weights
-  __shared__ float s_M[G], s_invL[G];
-  __shared__ int s_abort;
-  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
-  cg::cluster_group cluster = cg::this_cluster();
   const se_paged_kv& kv = a.kv;
-  const int k = a.k_cl;
-  const int rank = (int)cluster.block_rank();
-  const int u = blockIdx.x / k;
-  const int b = u / kv.Hkv, g = u % kv.Hkv;
-
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int i = 0; i < S; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 4);
-    }
-    tc::fence_barrier_init();
-  }
-  pdl_enter();
-  const int xs = (int)((int64_t)rank * a.sp / k), xe = (int)((int64_t)(rank + 1) * a.sp / k);
-  const int e_begin = xs * SE;
-  const int n_seg = resolve_rows(a, u, e_begin, (xe - xs) * SE, s_rows);
-  __syncthreads();
-  int gi = 0, gc = 0;
-  stream_segment<T, D, G>(a, ring, u, e_begin, n_seg, s_rows, gi, gc);
-
-  // the CTA's partial, in place over the first half-warp's o (each element
-  // is read and written by one thread)
+  // the CTA's partial (each element is read and written by one thread)
   float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
   for (int x = threadIdx.x; x < GD; x += 128) {
     const int j = x / D, d = x % D;
@@ -983,6 +1009,59 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_clu
   }
   // the peers' shared memory is no longer read by this CTA
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// grid: units x k CTAs in clusters of k = a.k_cl (a power of two up to 16);
+// 128 threads; dynamic smem StagedGeom::SMEM.  Cluster u is unit u = (b, g);
+// its CTA of rank r streams slices [r sp / k, (r + 1) sp / k) of the unit and
+// combines its half-warp states into one partial (m, l, o) in its own shared
+// memory.  After a cluster barrier every CTA reads the k maxima and sums from
+// its peers' shared memory, merges its own G D / k elements of o from the
+// peers' partials (the partials of an element are summed in a fixed order,
+// so the result does not depend on timing), writes them, and for H2O adds
+// sum_h p_{h,j} to the running score of each of its own entries from the
+// logits it stored.  A second cluster barrier keeps every CTA's shared
+// memory alive until its peers have read it.  Every thread of every CTA
+// reaches both barriers, also after a stage wait has run out.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_cluster_kernel(DecodeArgs a) {
+  using Gm = StagedGeom<T, D, G>;
+  constexpr int SE = Gm::SE, S = Gm::STAGES;
+  static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[4], empty[4];
+  __shared__ int8_t s_valid[4][SE];
+  __shared__ int32_t s_rows[kMaxChunk];
+  __shared__ float s_p[8][16];
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ int s_abort;
+  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
+  cg::cluster_group cluster = cg::this_cluster();
+  const se_paged_kv& kv = a.kv;
+  const int k = a.k_cl;
+  const int rank = (int)cluster.block_rank();
+  const int u = blockIdx.x / k;
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 4);
+    }
+    tc::fence_barrier_init();
+  }
+  pdl_enter();
+  const int xs = (int)((int64_t)rank * a.sp / k), xe = (int)((int64_t)(rank + 1) * a.sp / k);
+  const int e_begin = xs * SE;
+  const int n_seg = resolve_rows(a, u, e_begin, (xe - xs) * SE, s_rows);
+  __syncthreads();
+  int gi = 0, gc = 0;
+  stream_segment<T, D, G>(a, ring, u, e_begin, n_seg, s_rows, gi, gc);
+
+  __shared__ float s_M[G], s_invL[G];
+  cluster_merge<T, D, G>(a, cluster, k, rank, b, g, stages, s_m, s_l, s_M, s_invL);
 
   if (a.acc != nullptr && a.logits != nullptr) {
     // the running scores of this CTA's own entries, from the logits it
@@ -1013,6 +1092,145 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_clu
       }
     }
   }
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Compaction into fresh pages fused with decode attention over the result
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxChunkCD = 512;   // entries per CTA of the fused kernel
+
+struct CompactDecodeArgs {
+  DecodeArgs d;                // the cache before the call; the dense view of the result
+  const int32_t* keep;         // [B][Hkv][keep_stride] kept slots, ascending
+  int32_t keep_stride;
+  const int32_t* first_slot;   // [B]
+  const float* aux;            // [B][Hkv][aux_stride] values that move with the entries, or null
+  int64_t aux_stride;
+  CompactWs w;                 // the plan (compact_plan_kernel) and the staging for the commit
+};
+
+// Entries [e_begin, e_begin + n) of unit u in the compacted sequence: the K/V
+// row each is read from (its old page), the row it is written to (its fresh
+// page; -1 below the first rewritten block, where the entry stays), and the
+// staged slot-map / aux values of the rewritten ones -- the same sources,
+// destinations and checks as the gather kernel of a plain compaction.  A
+// sequence longer than the view (max_entries) is refused like a bad keep
+// index: status SE_ERR_BOUNDS, and the commit does not run.  Returns how many
+// of the n entries lie in the compacted sequence.
+SE_DEV int resolve_compact_rows(const CompactDecodeArgs& ca, int u, int e_begin, int n,
+                                int32_t* rows, int32_t* dst) {
+  const se_paged_kv& kv = ca.d.kv;
+  const CompactWs& w = ca.w;
+  const int b = u / kv.Hkv, h = u % kv.Hkv;
+  const int P = kv.page_size;
+  const int pb = w.pb[b], fs = ca.first_slot[b], nctx = w.new_ctx[b], octx = w.old_ctx[b];
+  const int pop0 = w.ctrl->top0 - 1 - w.off_new[b];
+  if (nctx > ca.d.max_entries) {
+    if (threadIdx.x == 0) {
+      set_status(kv.status, SE_ERR_BOUNDS);
+      atomicExch(&w.ctrl->abort, 1);
+    }
+    return 0;
+  }
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  const int32_t* keep = ca.keep + (int64_t)u * ca.keep_stride;
+  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+  const int64_t tb = (int64_t)u * w.row;
+  bool bad = false;
+  for (int x = threadIdx.x; x < n; x += blockDim.x) {
+    const int e = e_begin + x;
+    int src = -1, drow = -1;
+    if (e < nctx) {
+      if (e < pb * P) {
+        src = e;
+      } else {
+        src = e < fs ? e : keep[e - fs];
+        if (e >= fs && !(src >= fs && src < octx && (e == fs || src > keep[e - fs - 1]))) {
+          bad = true;
+          src = -1;
+        } else {
+          const int dp = kv.free_list[pop0 - (e / P - pb)];
+          if (dp < 0 || dp >= kv.num_pages) {
+            bad = true;
+            src = -1;
+          } else {
+            drow = (dp * kv.Hkv + h) * P + e % P;
+            w.slot_tmp[tb + (e - pb * P)] = kv.slot_map[(int64_t)u * smax + src];
+            if (ca.aux != nullptr && w.aux_tmp != nullptr)
+              w.aux_tmp[tb + (e - pb * P)] = ca.aux[(int64_t)u * ca.aux_stride + src];
+          }
+        }
+      }
+    }
+    const int page = src >= 0 ? bt[src / P] : -1;
+    if (src >= 0 && (page < 0 || page >= kv.num_pages)) bad = true;
+    const bool ok = src >= 0 && page >= 0 && page < kv.num_pages;
+    rows[x] = ok ? (page * kv.Hkv + h) * P + src % P : -1;
+    dst[x] = ok ? drow : -1;
+  }
+  if (bad) {
+    set_status(kv.status, SE_ERR_BOUNDS);
+    atomicExch(&w.ctrl->abort, 1);
+  }
+  return max(min(e_begin + n, nctx) - e_begin, 0);
+}
+
+// grid: units x k CTAs in clusters of k = d.k_cl; 128 threads; dynamic smem
+// StagedGeom::SMEM.  The cluster decode kernel over the dense view of the
+// compacted cache, reading every entry from where it lies before the call:
+// each landed stage of rewritten entries is also stored to the entries' rows
+// in their fresh pages, so the kept K/V cross HBM once on the way in and once
+// on the way out.  The CTAs of (b, head 0) record sequence b's fresh pages
+// for the commit.  After a planning error nothing is read or written (the
+// output is then undefined and the status word says why).
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS)
+compact_decode_kernel(CompactDecodeArgs ca) {
+  using Gm = StagedGeom<T, D, G>;
+  constexpr int SE = Gm::SE, S = Gm::STAGES;
+  static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
+  const DecodeArgs& a = ca.d;
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[4], empty[4];
+  __shared__ int8_t s_valid[4][SE];
+  __shared__ int32_t s_rows[kMaxChunkCD], s_dst[kMaxChunkCD];
+  __shared__ float s_p[8][16];
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ int s_abort;
+  __shared__ float s_M[G], s_invL[G];
+  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
+  cg::cluster_group cluster = cg::this_cluster();
+  const se_paged_kv& kv = a.kv;
+  const int k = a.k_cl;
+  const int rank = (int)cluster.block_rank();
+  const int u = blockIdx.x / k;
+  const int b = u / kv.Hkv, g = u % kv.Hkv;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 4);
+    }
+    tc::fence_barrier_init();
+  }
+  pdl_enter();
+  const bool planned = ca.w.ctrl->abort == 0;
+  const int xs = (int)((int64_t)rank * a.sp / k), xe = (int)((int64_t)(rank + 1) * a.sp / k);
+  const int e_begin = xs * SE;
+  const int n_seg = planned ? resolve_compact_rows(ca, u, e_begin, (xe - xs) * SE, s_rows, s_dst) : 0;
+  __syncthreads();
+  int gi = 0, gc = 0;
+  stream_segment<T, D, G, true>(a, ring, u, e_begin, n_seg, s_rows, gi, gc, s_dst);
+  // the cluster of (b, head 0) records sequence b's fresh pages, one share
+  // per CTA (after the stream, off its critical start)
+  if (planned && g == 0) record_fresh_pages(kv, ca.w, b, rank, k);
+  cluster_merge<T, D, G>(a, cluster, k, rank, b, g, stages, s_m, s_l, s_M, s_invL);
+  if (threadIdx.x < 32) bulk_wait_all();   // the copies have reached global memory
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -1163,6 +1381,78 @@ static se_status launch_decode_d(const DecodeArgs& a, int G, cudaStream_t st) {
     case 8: launch_decode_t<T, D, 8>(a, st); return SE_OK;
     default: return SE_ERR_UNSUPPORTED;
   }
+}
+
+template <typename T, int D, int G>
+static se_status launch_compact_decode_t(const CompactDecodeArgs& ca, cudaStream_t st) {
+  using Gm = StagedGeom<T, D, G>;
+  if constexpr (Gm::STAGES > 0) {
+    static std::atomic<uint64_t> attr{0};
+    static std::atomic<uint32_t> known[64];
+    const void* kf = reinterpret_cast<const void*>(&compact_decode_kernel<T, D, G>);
+    if (!allow_smem(kf, Gm::SMEM, attr) || !cluster_fits(kf, Gm::SMEM, ca.d.k_cl, known))
+      return SE_ERR_UNSUPPORTED;
+    se_launch_cluster(compact_decode_kernel<T, D, G>, dim3((unsigned)ca.d.n_cta), 128, Gm::SMEM, st,
+                      ca.d.k_cl, ca);
+    return SE_OK;
+  }
+  return SE_ERR_UNSUPPORTED;
+}
+
+template <typename T, int D>
+static se_status launch_compact_decode_d(const CompactDecodeArgs& ca, int G, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_compact_decode_t<T, D, 1>(ca, st);
+    case 2: return launch_compact_decode_t<T, D, 2>(ca, st);
+    case 4: return launch_compact_decode_t<T, D, 4>(ca, st);
+    case 8: return launch_compact_decode_t<T, D, 8>(ca, st);
+    default: return SE_ERR_UNSUPPORTED;
+  }
+}
+
+// Launches compact_decode_kernel between the plan and the commit of a
+// compaction into fresh pages when the shape takes it: a staged kernel for
+// the dtype, D and group size, a cluster of at most 16 CTAs of at most
+// kMaxChunkCD entries per (sequence, KV head), and clusters that fit the
+// device.  Returns SE_ERR_UNSUPPORTED, with nothing launched, otherwise.
+se_status launch_compact_decode(const se_paged_kv* kv, const int32_t* keep, int32_t keep_stride,
+                                const int32_t* first_slot, const float* aux, int64_t aux_stride,
+                                const CompactWs& w, const void* q, void* o, int32_t max_entries,
+                                cudaStream_t st) {
+  const int G = kv->Hq / kv->Hkv;
+  if (G < 1 || 128 % G != 0 || max_entries < 1) return SE_ERR_UNSUPPORTED;
+  if ((int64_t)kv->num_pages * kv->Hkv * kv->page_size > INT32_MAX) return SE_ERR_UNSUPPORTED;
+  const int SE = 128 / G;
+  const int64_t units = (int64_t)kv->B * kv->Hkv;
+  const int sp = cdiv(max_entries, SE);
+  int k = 0;
+  for (int kc = 1; kc <= kMaxCluster; kc *= 2) {
+    if (cdiv(sp, kc) * SE > kMaxChunkCD) continue;
+    k = kc;
+    if (units * kc >= kCtaSlots) break;
+  }
+  if (k == 0 || units * k > INT32_MAX) return SE_ERR_UNSUPPORTED;
+  CompactDecodeArgs ca{};
+  ca.d.kv = *kv;
+  ca.d.q = q;
+  ca.d.view = SE_VIEW_DENSE;
+  ca.d.sp = sp;
+  ca.d.ts = units * sp;
+  ca.d.n_cta = (int)(units * k);
+  ca.d.max_entries = max_entries;
+  ca.d.out = o;
+  ca.d.k_cl = k;
+  ca.keep = keep;
+  ca.keep_stride = keep_stride;
+  ca.first_slot = first_slot;
+  ca.aux = aux;
+  ca.aux_stride = aux_stride;
+  ca.w = w;
+  if (kv->dtype == SE_BF16 && kv->D == 128) return launch_compact_decode_d<__nv_bfloat16, 128>(ca, G, st);
+  if (kv->dtype == SE_BF16 && kv->D == 64) return launch_compact_decode_d<__nv_bfloat16, 64>(ca, G, st);
+  if (kv->dtype == SE_F32 && kv->D == 128) return launch_compact_decode_d<float, 128>(ca, G, st);
+  if (kv->dtype == SE_F32 && kv->D == 64) return launch_compact_decode_d<float, 64>(ca, G, st);
+  return SE_ERR_UNSUPPORTED;
 }
 
 }  // namespace se

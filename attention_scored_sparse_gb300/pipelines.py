@@ -15,7 +15,8 @@ import torch
 from . import (SE_COMPACT_FRESH_PAGES, SE_COMPACT_MOVE_LAST, SE_SELECT_EVICT_ONE,
                SE_SELECT_KARA_CHUNK, SE_SELECT_TOPK, SE_VIEW_DENSE, SE_VIEW_PAGES,
                SE_VIEW_TOKENS, kv_desc,
-               se_append_kv, se_compact_evict, se_prune_span, se_quest_build_meta,
+               se_append_kv, se_compact_decode, se_compact_evict, se_prune_span,
+               se_quest_build_meta,
                se_quest_decode_step, se_quest_page_select, se_score_window,
                se_sparse_decode_attn, se_topk_select,
                workspace_sizes)
@@ -75,6 +76,7 @@ class SnapKV(_Base):
         self.ws_score = self._ws(sz["score_window"])
         self.ws_compact = self._ws(sz["compact_evict"])
         self.ws_decode = self._ws(sz["sparse_decode_attn"])
+        self.ws_compact_decode = self._ws(sz["compact_decode"])
         # block table and context lengths as they were before compaction, so
         # decode attention can read the kept entries while compaction moves them
         self.bt_snap = torch.empty_like(cache.block_table)
@@ -127,6 +129,14 @@ class SnapKV(_Base):
         self.decode_kept(q, o, self.side)
         self.compact(main)
         main.wait_stream(self.side)
+
+    def compact_decode_fused(self, q, o, stream=None):
+        """Compaction and decode attention in one pass over the kept entries
+        (se_compact_decode): each kept K/V row is read once, copied into its
+        fresh page and attended there."""
+        se_compact_decode(self.kv, self.keep, n_keep=self.n_keep, first_slot=self.zero,
+                          max_keep=self.budget, q=q, o=o, max_entries=self.budget,
+                          workspace=self.ws_compact_decode, stream=stream)
 
     def step(self, q_win, q_pos, q_dec, o, stream=None):
         self.score(q_win, q_pos, stream)

@@ -252,6 +252,36 @@ se_status se_compact_evict(const se_paged_kv* kv, int32_t mode, const int32_t* k
 size_t se_compact_evict_workspace_size(const se_paged_kv* kv, int32_t max_keep);
 
 /*
+ * se_compact_decode -- SnapKV's step after the last prompt chunk (SparseEngine
+ * "How it works": physical eviction into fresh pages, then attention over the
+ * retained entries through the AttentionView) in one pass over the kept
+ * entries.  The cache ends as after se_compact_evict(FRESH_PAGES) with the
+ * same keep_idx, keep_stride, n_keep, first_slot, max_keep and aux, and
+ * o [B][Hq][D] (cache dtype) holds single-query attention of q [B][Hq][D]
+ * over every entry of the compacted sequences, as se_sparse_decode_attn with
+ * the dense view computes it after the compaction.  Each kept K/V row is
+ * read from HBM once: the kernel stages it in shared memory, copies it to its
+ * fresh page and attends over it there.
+ *
+ * max_entries (host) must be at least every compacted length first_slot[b] +
+ * n_keep[b]; a longer sequence is refused on the device (SE_ERR_BOUNDS, cache
+ * untouched).  Shapes the one-pass kernel does not take (more than 16 x 512
+ * entries per (sequence, KV head), or no cluster of that size fits) run the
+ * compaction and then the decode attention, with the same results.
+ * Workspace: se_compact_decode_workspace_size bytes, zeroed before its first
+ * use (the decode part keeps per-unit counters there that every completed
+ * call leaves at zero).  Device errors as se_compact_evict(FRESH_PAGES); after
+ * one, o is undefined.
+ */
+se_status se_compact_decode(const se_paged_kv* kv, const int32_t* keep_idx, int32_t keep_stride,
+                            const int32_t* n_keep, const int32_t* first_slot, int32_t max_keep,
+                            float* aux, int64_t aux_stride, const void* q, void* o,
+                            int32_t max_entries, void* workspace, size_t workspace_bytes,
+                            void* stream);
+size_t se_compact_decode_workspace_size(const se_paged_kv* kv, int32_t max_keep,
+                                        int32_t max_entries);
+
+/*
  * se_prune_span -- SparseEngine "How it differs": sparse prefix-cache pruning.
  * For each sequence, T = positions in [L[b], R[b]) and I = {t in T :
  * mask[b*mask_stride + t - L[b]] != 0}; the resident set of every head
