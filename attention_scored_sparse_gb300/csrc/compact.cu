@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(
 // Copies the surviving entries into the fresh pages (K, V) and stages their
 // slot_map / aux values.  grid: (entry chunks, Hkv, B).
 template <int CHUNKS>  // 16-byte chunks per entry row
-__global__ void __launch_bounds__(256) compact_gather_kernel(
+__global__ void __launch_bounds__(256, 8) compact_gather_kernel(
     se_paged_kv kv, const int32_t* __restrict__ keep_idx, int32_t keep_stride,
     const int32_t* __restrict__ first_slot, const float* __restrict__ aux, int64_t aux_stride,
     CompactWs w, int entries_per_cta) {
@@ -281,7 +281,7 @@ SE_DEV void commit_slots(const se_paged_kv& kv, float* aux, int64_t aux_stride,
 // Commit of a compaction.  grid: (1 + slot chunks of 4096, Hkv, B), 1024
 // threads; CTA (0, 0, b) commits the pages of sequence b, CTA (1 + c, h, b)
 // chunk c of the slot map of (b, h).  Nothing runs after a planning error.
-__global__ void __launch_bounds__(1024) compact_commit_kernel(se_paged_kv kv, float* aux,
+__global__ void __launch_bounds__(1024, 2) compact_commit_kernel(se_paged_kv kv, float* aux,
                                                               int64_t aux_stride, CompactWs w) {
   pdl_enter();
   if (w.ctrl->abort) return;

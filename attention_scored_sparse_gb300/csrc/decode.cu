@@ -847,15 +847,22 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
 }
 
 // grid: n_cta; 128 threads = 8 half-warps; dynamic smem StagedGeom::SMEM.
-// Every entry of the CTA's range is resolved to its K/V row up front; each
-// segment of the range is then streamed (stream_segment) and its half-warp
-// states are combined and counted (finish_segment), the last CTA of a unit
-// merging the unit's partials.
+// Warp 0 keeps STAGES-1 stages of copies in flight within a segment; every
+// half-warp reads its E rows of each stage from shared memory (16 lanes x 16
+// bytes = one 256-byte row, conflict-free) and runs the same reduce-scatter /
+// online-softmax arithmetic as the register kernel above.  Stage buffers and
+// barrier phases follow a count of the stages the CTA has issued, so they
+// carry over from one segment to the next; at a segment's end the stages are
+// idle and hold the half-warp states while they are combined.
+// The stream of a segment is the one stream_segment runs for the cluster
+// kernels, written out here: built from stream_segment, this kernel measured
+// about 5 % slower on the multi-wave grids it serves (same instructions,
+// scheduled differently by the compiler).
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_partial_kernel(DecodeArgs a) {
   pdl_enter();
   using Gm = StagedGeom<T, D, G>;
-  constexpr int SE = Gm::SE, S = Gm::STAGES;
+  constexpr int V = Gm::V, E = Gm::E, SE = Gm::SE, RB = Gm::RB, S = Gm::STAGES;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[4], empty[4];
@@ -866,8 +873,13 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
   __shared__ int s_nseg[kMaxChunk / SE];   // viewed entries of each segment of the range
   __shared__ int s_abort;
   static_assert(S * Gm::STAGE_BYTES >= 8 * G * D * 4, "merge buffer must fit the stages");
-  const StageRing<G, SE> ring{stages, full, empty, s_valid, s_p, s_m, s_l, &s_abort};
   const int c = blockIdx.x;
+  const se_paged_kv& kv = a.kv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int my_e = t / G, my_h = t % G;
+  const unsigned full_mask = 0xffffffffu;
+  constexpr uint64_t kLimit = 2000000000ull;
   const int64_t x0 = range_start(a, c), x1 = range_end(a, c);
 
   if (threadIdx.x == 0) {
@@ -884,19 +896,232 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
   for (int64_t xs = x0, k = 0; xs < x1; ++k) {
     const int u = (int)(xs / a.sp);
     const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
+    const int b = u / kv.Hkv, g = u % kv.Hkv;
+    const int P = kv.page_size;
+    const int ctx = kv.ctx_len[b];
+    const int n_view = min(view_entries(a, ctx), a.max_entries);
     const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
-    const int n = resolve_rows(a, u, e_begin, (int)(xe - xs) * SE, s_rows + (int)(xs - x0) * SE);
-    if (threadIdx.x == 0) s_nseg[k] = n;
+    const int n_all = (int)(xe - xs) * SE;
+    if (threadIdx.x == 0) s_nseg[k] = max(min(e_begin + n_all, n_view) - e_begin, 0);
+    int32_t* rows = s_rows + (int)(xs - x0) * SE;
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    for (int x = threadIdx.x; x < n_all; x += blockDim.x) {
+      const int e = e_begin + x;
+      const int slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
+      const int page = slot >= 0 ? bt[slot / P] : -1;
+      rows[x] = (page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
+    }
     xs = xe;
   }
   __syncthreads();
-  int gi = 0, gc = 0;
+  const bool producer = warp == 0;   // the whole warp issues, lane 0 arrives
+  const float qscale = kLog2e * rsqrtf((float)D);
+  constexpr int V2 = V / 2;
+  int gi = 0;   // stages issued by this CTA (stage n uses buffer n % S)
+  int gc = 0;   // stages consumed
+
   for (int64_t xs = x0, k = 0; xs < x1; ++k) {
     const int u = (int)(xs / a.sp);
     const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
+    const int b = u / kv.Hkv, g = u % kv.Hkv;
     const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
-    stream_segment<T, D, G>(a, ring, u, e_begin, s_nseg[k], s_rows + (int)(xs - x0) * SE, gi, gc);
-    finish_segment<T, D, G>(a, u, c, s_m, s_l, reinterpret_cast<float (*)[G][D]>(stages));
+    const int n_seg = s_nseg[k];
+    const int n_it = cdiv(n_seg, SE);
+    const int32_t* rows = s_rows + (int)(xs - x0) * SE;
+    const int g0 = gi;   // stage count at the segment's start
+
+    // the first STAGES-1 stages; a buffer last used by an earlier segment is
+    // refilled only after its consumers have released it
+    if (producer) {
+      for (int i = 0; i < min(S - 1, n_it); ++i) {
+        const int n = g0 + i;
+        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
+        if (!__all_sync(full_mask, free_ok)) {
+          if (lane == 0) {
+            set_status(kv.status, SE_ERR_TIMEOUT);
+            atomicExch(&s_abort, 1);
+          }
+          break;
+        }
+        issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                             &full[n % S], s_valid[n % S], lane);
+        ++gi;
+      }
+    }
+
+    float q[G][V];
+    const T* qb = static_cast<const T*>(a.q) + ((int64_t)b * kv.Hq + g * G) * D + t * V;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      load_row<T, V>(qb + (int64_t)j * D, q[j]);
+#pragma unroll
+      for (int i = 0; i < V; ++i) q[j][i] *= qscale;
+    }
+    // q and o as fp32 pairs: dot products and p * v updates run as paired FMAs
+    uint64_t q2[G][V2], o2[G][V2];
+    float m[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < V2; ++i) {
+        q2[j][i] = tc::f2(q[j][2 * i], q[j][2 * i + 1]);
+        o2[j][i] = 0;
+      }
+    }
+    float l_own = 0.f;
+    float* lg = a.logits ? a.logits + (int64_t)u * a.max_entries * G : nullptr;
+
+    for (int it = 0; it < n_it; ++it) {
+      if (producer && gi - g0 < n_it) {
+        // refill the buffer consumed in the previous iteration
+        const int n = gi;
+        const bool free_ok = n < S || tc::mbar_wait(&empty[n % S], ((n / S) - 1) & 1, kLimit);
+        if (__all_sync(full_mask, free_ok)) {
+          issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
+                               &full[n % S], s_valid[n % S], lane);
+          ++gi;
+        } else if (lane == 0) {
+          set_status(kv.status, SE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+      }
+      const int s = gc % S;
+      const bool ok_wait = tc::mbar_wait(&full[s], (gc / S) & 1, kLimit);
+      if (!__all_sync(full_mask, ok_wait)) {
+        if (lane == 0) {
+          set_status(kv.status, SE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      const uint8_t* kst = stages + s * Gm::STAGE_BYTES;
+      const uint8_t* vst = kst + SE * RB;
+      const int e0 = e_begin + it * SE + hw * E;
+      // K rows are read from the stage one entry at a time; V rows are read
+      // again after the probabilities are known (the stage is released after)
+      bool valid[E];
+      float part[16];
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) {
+        valid[uu] = s_valid[s][hw * E + uu] != 0;
+        float kf[V];
+        if (valid[uu]) {
+          load_row_smem<T, V>(reinterpret_cast<const T*>(kst + (hw * E + uu) * RB) + t * V, kf);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) kf[i] = 0.f;
+        }
+        uint64_t k2[V2];
+#pragma unroll
+        for (int i = 0; i < V2; ++i) k2[i] = tc::f2(kf[2 * i], kf[2 * i + 1]);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          uint64_t acc2 = 0;
+#pragma unroll
+          for (int i = 0; i < V2; ++i) acc2 = tc::ffma2(q2[j][i], k2[i], acc2);
+          float lo, hi;
+          tc::f2split(acc2, lo, hi);
+          part[uu * G + j] = lo + hi;
+        }
+      }
+#pragma unroll
+      for (int step = 0; step < 4; ++step) {
+        const int off = 8 >> step;
+        const int n = 8 >> step;
+        const bool upper = (t & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float lo = part[i], hi = part[i + n];
+          part[i] = (upper ? hi : lo) + __shfl_xor_sync(full_mask, upper ? lo : hi, off);
+        }
+      }
+      bool ok = false;
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) ok = (uu == my_e) ? valid[uu] : ok;
+      const float sv = ok ? part[0] : -INFINITY;
+      if (lg != nullptr && ok) lg[(int64_t)(e0 + my_e) * G + my_h] = sv;
+      float tmax = sv;
+#pragma unroll
+      for (int off = 8; off >= G; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(full_mask, tmax, off));
+      float m_mine = m[0];
+#pragma unroll
+      for (int j = 1; j < G; ++j) m_mine = (j == my_h) ? m[j] : m_mine;
+      const float mn_mine = fmaxf(m_mine, tmax);
+      const float alpha_mine =
+          (mn_mine == -INFINITY || mn_mine == m_mine) ? 1.f : ex2(m_mine - mn_mine);
+      const float p = (sv == -INFINITY) ? 0.f : ex2(sv - mn_mine);
+      l_own = fmaf(l_own, alpha_mine, p);
+      s_p[hw][t] = p;
+      bool grew = false;
+      float alpha[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float mj = __shfl_sync(full_mask, mn_mine, (threadIdx.x & 16) + j);
+        alpha[j] = __shfl_sync(full_mask, alpha_mine, (threadIdx.x & 16) + j);
+        grew |= mj != m[j];
+        m[j] = mj;
+      }
+      __syncwarp();
+      if (grew) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const uint64_t a2 = tc::f2(alpha[j], alpha[j]);
+#pragma unroll
+          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(o2[j][i], a2, 0);
+        }
+      }
+#pragma unroll
+      for (int uu = 0; uu < E; ++uu) {
+        float vf[V];
+        if (valid[uu]) {
+          load_row_smem<T, V>(reinterpret_cast<const T*>(vst + (hw * E + uu) * RB) + t * V, vf);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) vf[i] = 0.f;
+        }
+        uint64_t v2[V2];
+#pragma unroll
+        for (int i = 0; i < V2; ++i) v2[i] = tc::f2(vf[2 * i], vf[2 * i + 1]);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pu = s_p[hw][uu * G + j];
+          const uint64_t p2 = tc::f2(pu, pu);
+#pragma unroll
+          for (int i = 0; i < V2; ++i) o2[j][i] = tc::ffma2(p2, v2[i], o2[j][i]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with this stage's rows
+      ++gc;
+    }
+    // drain: after a timeout, copies of the last stages may still be in flight
+    // (each earlier stage was waited on before its buffer was refilled)
+    if (producer && lane == 0)
+      for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&full[i % S], (i / S) & 1, kLimit);
+    float lsum = l_own;
+#pragma unroll
+    for (int off = 8; off >= G; off >>= 1) lsum += __shfl_xor_sync(full_mask, lsum, off);
+    if (t < G) {
+      float mt = m[0];
+#pragma unroll
+      for (int j = 1; j < G; ++j) mt = (j == t) ? m[j] : mt;
+      s_m[hw][t] = mt;
+      s_l[hw][t] = lsum;
+    }
+    __syncthreads();   // every stage of the segment has been read: reuse the stage memory
+    float (*s_o)[G][D] = reinterpret_cast<float (*)[G][D]>(stages);
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+      for (int i = 0; i < V2; ++i) {
+        float lo, hi;
+        tc::f2split(o2[j][i], lo, hi);
+        s_o[hw][j][t * V + 2 * i] = lo;
+        s_o[hw][j][t * V + 2 * i + 1] = hi;
+      }
+    __syncthreads();
+    finish_segment<T, D, G>(a, u, c, s_m, s_l, s_o);
     // the stage memory was written and read as plain shared memory; order
     // that before the next segment's copies into it
     tc::fence_proxy_async_smem();
@@ -1274,14 +1499,17 @@ static DecodeSplit make_split(const se_paged_kv* kv, int max_entries) {
   const int w = max(chunk / SE, 1);
   const int k = cdiv(d.sp, w);
   const int64_t n_al = units * k;
-  // cluster split: the fewest CTAs per unit (a power of two up to 16) that
-  // keep every CTA within kMaxChunk entries and give about four CTAs per SM
+  // cluster split: the most CTAs per unit (a power of two up to 16) that
+  // keep every CTA within kMaxChunk entries and the grid within one wave of
+  // four CTAs per SM.  Grids of several waves keep the split-K forms: there
+  // the merge is a small share of the time, and clusters of 16 leave SMs of
+  // a GPC unused.
   d.k_cl = 0;
   const int64_t w_cl = max(kMaxChunk / SE, 1);
   for (int kc = 1; kc <= kMaxCluster; kc *= 2) {
     if (cdiv64(d.sp, kc) > w_cl) continue;
+    if (units * kc > kCtaSlots) break;
     d.k_cl = kc;
-    if (units * kc >= kCtaSlots) break;
   }
   if (n_al <= kCtaSlots || n_al >= 4 * kCtaSlots) {
     d.n_cta = (int)n_al;
@@ -1425,13 +1653,15 @@ se_status launch_compact_decode(const se_paged_kv* kv, const int32_t* keep, int3
   const int SE = 128 / G;
   const int64_t units = (int64_t)kv->B * kv->Hkv;
   const int sp = cdiv(max_entries, SE);
+  // the split of decode attention's cluster form (make_split), with at most
+  // kMaxChunkCD entries per CTA
   int k = 0;
   for (int kc = 1; kc <= kMaxCluster; kc *= 2) {
     if (cdiv(sp, kc) * SE > kMaxChunkCD) continue;
+    if (units * kc > kCtaSlots) break;
     k = kc;
-    if (units * kc >= kCtaSlots) break;
   }
-  if (k == 0 || units * k > INT32_MAX) return SE_ERR_UNSUPPORTED;
+  if (k == 0) return SE_ERR_UNSUPPORTED;
   CompactDecodeArgs ca{};
   ca.d.kv = *kv;
   ca.d.q = q;

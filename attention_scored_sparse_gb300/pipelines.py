@@ -141,7 +141,7 @@ class SnapKV(_Base):
     def step(self, q_win, q_pos, q_dec, o, stream=None):
         self.score(q_win, q_pos, stream)
         self.select(stream)
-        self.compact_decode(q_dec, o, stream)
+        self.compact_decode_fused(q_dec, o, stream)
 
 
 class QuestDecode(_Base):

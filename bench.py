@@ -335,9 +335,8 @@ def run_snapkv(args, torch, rank, world):
     stages = ["s0", "s1", "s2", "s3"]
     ev = Events(torch, stages)
 
-    # the step as the pipeline runs it: compaction and decode attention side
-    # by side (decode on a second stream over the kept entries in their old
-    # pages), joined before the step ends
+    # the step as the pipeline runs it: compaction and decode attention in
+    # one pass over the kept entries (se_compact_decode)
     def step(timed):
         restore()
         if timed: ev.mark("s0")
@@ -345,7 +344,7 @@ def run_snapkv(args, torch, rank, world):
         if timed: ev.mark("s1")
         pipe.select()
         if timed: ev.mark("s2")
-        pipe.compact_decode(inp["q_dec"], o)
+        pipe.compact_decode_fused(inp["q_dec"], o)
         if timed: ev.mark("s3")
 
     for _ in range(args.warmup):
@@ -391,6 +390,9 @@ def run_snapkv(args, torch, rank, world):
         "decode_gbs": dec_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9,
     }
     hbm = peaks()[0]["hbm_gbs"]
+    # the step's one pass over the kept entries: each read once, written once
+    detail["compact_and_decode_gbs"] = comp_bytes / (statistics.mean(cd_ms) * 1e-3) / 1e9
+    detail["compact_and_decode_frac_of_hbm"] = detail["compact_and_decode_gbs"] / hbm
     detail["compact_frac_of_hbm"] = detail["compact_gbs"] / hbm
     detail["decode_frac_of_hbm"] = detail["decode_gbs"] / hbm
     # DRAM bytes of one se_score_window call on this workload, both passes
@@ -399,7 +401,7 @@ def run_snapkv(args, torch, rank, world):
     roof = dict(bound="tensor", achieved=detail["score_tflops"], unit="TFLOP/s",
                 kernel="se_score_window", per_launch=f"{flops:.4g} FLOP (one QK^T sweep)",
                 traffic=(276.2 + 3.3 + 278.7 + 5.9) * 1e6 if shape.name == "snapkv_llama8b" else None)
-    launches = 2 + 1 + 3 + 1     # score, select, compaction, decode kernels per step
+    launches = 2 + 1 + 3         # score (2), select, compaction plan + compaction/decode + commit
     cfg = {"workload": f"{shape.name}: B={B} x {shape.ctx} tokens, Hq={shape.Hq}/Hkv={Hkv}, "
                        f"d={D}, window {shape.window}, pool {shape.pool_kernel}, budget "
                        f"{shape.budget}", "l2": "inputs larger than L2 (KV cache 570 MB)"}

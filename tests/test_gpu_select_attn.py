@@ -234,17 +234,18 @@ def _aligned_ctas(units, max_entries):
 def _decode_split(units, max_entries, G):
     """The work split decode attention takes for a shape: a cluster of k CTAs
     per (sequence, KV head) unit (k a power of two up to 16, each CTA at most
-    1024 entries, the fewest k that give 152 x 4 CTAs), else split-K with a
-    merge through global memory, unit-aligned or cut evenly ("stream")."""
+    1024 entries, the most k that keep the grid within 152 x 4 CTAs), else
+    split-K with a merge through global memory, unit-aligned or cut evenly
+    ("stream")."""
     se_ = 128 // G
     sp = W.cdiv(max_entries, se_)
-    k_cl, kc = 0, 1
-    while kc <= 16:
-        if W.cdiv(sp, kc) <= 1024 // se_:
-            k_cl = kc
-            if units * kc >= 608:
-                break
-        kc *= 2
+    k_cl = 0
+    for kc in (1, 2, 4, 8, 16):
+        if W.cdiv(sp, kc) > 1024 // se_:
+            continue
+        if units * kc > 608:
+            break
+        k_cl = kc
     if k_cl:
         return ("cluster", k_cl)
     n_al = _aligned_ctas(units, max_entries)
@@ -252,22 +253,23 @@ def _decode_split(units, max_entries, G):
 
 
 @pytest.mark.parametrize("B,Hkv,G,D,me,path", [
-    (80, 8, 4, 64, 600, ("cluster", 1)),
-    (40, 8, 4, 128, 1153, ("cluster", 2)),
-    (20, 8, 4, 64, 2000, ("cluster", 4)),
-    (10, 8, 4, 64, 3000, ("cluster", 8)),
+    (40, 8, 4, 64, 600, ("cluster", 1)),
+    (20, 8, 4, 128, 1153, ("cluster", 2)),
+    (10, 8, 4, 64, 3000, ("cluster", 4)),
+    (5, 8, 4, 64, 5000, ("cluster", 8)),
     (2, 2, 4, 128, 9000, ("cluster", 16)),
     (4, 4, 8, 128, 5000, ("cluster", 16)),
+    (40, 8, 4, 128, 1153, ("stream", 640)),
     (2, 2, 4, 128, 20000, ("stream", 628)),
     (1, 2, 4, 128, 20000, ("aligned", 314)),
 ])
 def test_decode_attention_splits_match_oracle(cuda_lib, B, Hkv, G, D, me, path):
     """Every work split of decode attention against the oracle: clusters of
-    1 to 16 CTAs per unit merging through shared memory, and for views longer
-    than 16 x 1024 entries split-K with the merge in global memory (ranges
-    aligned to units, or cut evenly across unit boundaries).  Ragged contexts
-    (one of a single token, one of 16), dense view with running scores and a
-    token view."""
+    1 to 16 CTAs per unit merging through shared memory, and for grids of
+    more than one wave or views longer than 16 x 1024 entries split-K with
+    the merge in global memory (ranges aligned to units, or cut evenly across
+    unit boundaries).  Ragged contexts (one of a single token, one of 16),
+    dense view with running scores and a token view."""
     se = cuda_lib
     assert _decode_split(B * Hkv, me, G) == path
     dtype = torch.bfloat16

@@ -97,11 +97,13 @@ def test_snapkv_llama8b_reduced(cuda_lib):
     assert _snapkv(cuda_lib, W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512)) <= 2
 
 
-def test_snapkv_step_decodes_beside_compaction(cuda_lib):
-    """The pipeline step runs decode attention on a second stream over the
-    kept entries in their old pages while compaction moves them: its output
-    equals, bit for bit, decode attention over the compacted cache, and the
-    compacted cache is the same as the one the separate calls leave."""
+@pytest.mark.parametrize("form", ["step", "two_streams"])
+def test_snapkv_step_decodes_beside_compaction(cuda_lib, form):
+    """The pipeline step (compaction and decode attention in one pass over the
+    kept entries), and the form that runs decode attention on a second stream
+    over the kept entries in their old pages while compaction moves them:
+    the output equals, bit for bit, decode attention over the compacted
+    cache, and the compacted cache is the one the separate calls leave."""
     shape = W.snapkv_llama8b(B=2, ctx=4096 + 37, window=64, budget=512)
     runs = []
     for overlapped in (False, True):
@@ -110,8 +112,12 @@ def test_snapkv_step_decodes_beside_compaction(cuda_lib):
         pipe = P.SnapKV(pc, shape.Hq, ctx=shape.ctx, window=shape.window, budget=shape.budget,
                         pool_kernel=shape.pool_kernel)
         o = torch.full_like(inp["q_dec"], float("nan"))
-        if overlapped:
+        if overlapped and form == "step":
             pipe.step(inp["q_win"], inp["q_pos"], inp["q_dec"], o)
+        elif overlapped:
+            pipe.score(inp["q_win"], inp["q_pos"])
+            pipe.select()
+            pipe.compact_decode(inp["q_dec"], o)
         else:
             pipe.score(inp["q_win"], inp["q_pos"])
             pipe.select()
