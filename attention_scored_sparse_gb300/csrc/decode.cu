@@ -434,30 +434,6 @@ __global__ void __launch_bounds__(128) decode_partial_regs_kernel(DecodeArgs a) 
   }
 }
 
-// Bulk copy global -> shared (the TMA engine, no tensor map), completing on
-// an mbarrier; the byte count is added to the barrier's expected total first.
-SE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
-               : "memory");
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-      : "memory");
-}
-
-// Bulk copy shared -> global (the TMA engine), tracked in the issuing
-// thread's bulk group; commit closes the group, wait_read waits until every
-// closed group of the thread has read its shared memory, wait_all until
-// every one has written global memory.
-SE_DEV void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(dst), "r"(tc::smem_u32(src)), "r"(bytes)
-               : "memory");
-}
-SE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-SE_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-SE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // V elements of a K or V row in shared memory, as fp32.
 template <typename T, int V>
 SE_DEV void load_row_smem(const T* r, float* f) {
@@ -521,8 +497,8 @@ SE_DEV void issue_stage(const DecodeArgs& a, int s0, int n_seg, const int32_t* r
       const int end = stop ? __ffs(stop) - 1 : 32;
       const int len = end - lane;
       const int64_t off = (int64_t)prow * Gm::RB;
-      bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
-      bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
+      tc::bulk_g2s(dst + u * Gm::RB, kp + off, (uint32_t)(len * Gm::RB), bar);
+      tc::bulk_g2s(dst + Gm::SE * Gm::RB + u * Gm::RB, vp + off, (uint32_t)(len * Gm::RB), bar);
     }
   }
   __syncwarp();
@@ -554,11 +530,11 @@ SE_DEV void store_stage(const DecodeArgs& a, const uint8_t* stage, const int32_t
       const uint32_t stop = (starts | ~okm) & above;
       const int len = (stop ? __ffs(stop) - 1 : 32) - lane;
       const uint32_t bytes = (uint32_t)(len * Gm::RB);
-      bulk_s2g(kp + (int64_t)d * Gm::RB, stage + x * Gm::RB, bytes);
-      bulk_s2g(vp + (int64_t)d * Gm::RB, stage + Gm::SE * Gm::RB + x * Gm::RB, bytes);
+      tc::bulk_s2g(kp + (int64_t)d * Gm::RB, stage + x * Gm::RB, bytes);
+      tc::bulk_s2g(vp + (int64_t)d * Gm::RB, stage + Gm::SE * Gm::RB + x * Gm::RB, bytes);
     }
   }
-  bulk_commit();
+  tc::bulk_commit();
 }
 
 // Shared memory of the staged kernels: the stage ring and the per-half-warp
@@ -653,7 +629,7 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
         break;
       }
       if constexpr (COPY) {
-        bulk_wait_read();
+        tc::bulk_wait_read();
         __syncwarp();
       }
       issue_stage<T, D, G>(a, i * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
@@ -692,7 +668,7 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
       const bool free_ok = n < S || tc::mbar_wait(&r.empty[n % S], ((n / S) - 1) & 1, kLimit);
       if (__all_sync(full_mask, free_ok)) {
         if constexpr (COPY) {
-          bulk_wait_read();   // the stores of the buffer's last stage
+          tc::bulk_wait_read();   // the stores of the buffer's last stage
           __syncwarp();
         }
         issue_stage<T, D, G>(a, (n - g0) * SE, n_seg, rows, stages + (n % S) * Gm::STAGE_BYTES,
@@ -820,7 +796,7 @@ SE_DEV void stream_segment(const DecodeArgs& a, const StageRing<G, StagedGeom<T,
   if (producer && lane == 0)
     for (int i = max(0, gi - S); i < gi; ++i) tc::mbar_wait(&r.full[i % S], (i / S) & 1, kLimit);
   if constexpr (COPY) {
-    if (producer) bulk_wait_read();   // the stage memory is reused below
+    if (producer) tc::bulk_wait_read();   // the stage memory is reused below
   }
   float lsum = l_own;
 #pragma unroll
@@ -1455,7 +1431,7 @@ compact_decode_kernel(CompactDecodeArgs ca) {
   // per CTA (after the stream, off its critical start)
   if (planned && g == 0) record_fresh_pages(kv, ca.w, b, rank, k);
   cluster_merge<T, D, G>(a, cluster, k, rank, b, g, stages, s_m, s_l, s_M, s_invL);
-  if (threadIdx.x < 32) bulk_wait_all();   // the copies have reached global memory
+  if (threadIdx.x < 32) tc::bulk_wait_all();   // the copies have reached global memory
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -10,7 +10,7 @@
 // kernel reads 2*D elements per (page, group) with one half-warp per page and
 // the group's queries held in registers, writes one float per page, and the
 // shared block radix top-k then picks the pages.
-#include "se_common.cuh"
+#include "tc_primitives.cuh"
 
 namespace se {
 
@@ -173,6 +173,157 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
   }
 }
 
+// Page bound over a ring of bulk-copied stages (bf16, D = 128): the same
+// bounds as quest_bound_bf16_kernel, with each CTA keeping copies in flight
+// across many pages.  grid: (cdiv(max_blocks, 8 SB), Hkv / hpc, B), 256
+// threads, dynamic smem kQbStages x 32 KB.  CTA (x, y, b) takes the blocks
+// [8 SB x, 8 SB (x + 1)) of sequence b (eight stages of SB = 64 / hpc
+// blocks) for heads [y hpc, (y + 1) hpc).  Warp 0 copies, per block, the kmin
+// rows of the hpc heads (hpc x 256 contiguous bytes) and their kmax rows into
+// a stage; two stages are in flight while the CTA computes a third.
+// Half-warp h serves head y hpc + h % hpc for the whole launch (its folded
+// query in 16 registers) and in round r of a stage the block (16 r + h) /
+// hpc.  CTA (0, 0, b) also writes sequence b's ranges.  Every wait is
+// bounded; one that runs out sets SE_ERR_TIMEOUT and the CTA drains its
+// copies and leaves.
+constexpr int kQbStages = 3;
+constexpr int kQbStageBytes = 32768;       // kmin half, then kmax half
+constexpr int kQbStagesPerCta = 8;
+constexpr int kQbMaxBlocks = kQbStagesPerCta * 64;
+
+template <int G>
+__global__ void __launch_bounds__(256, 2) quest_bound_ring_kernel(
+    se_paged_kv kv, const __nv_bfloat16* __restrict__ kmin, const __nv_bfloat16* __restrict__ kmax,
+    const __nv_bfloat16* __restrict__ q, float* __restrict__ U, int64_t u_stride, int hpc,
+    QuestRanges rg) {
+  extern __shared__ __align__(128) uint8_t qb_smem[];
+  __shared__ uint64_t full[kQbStages], empty[kQbStages];
+  __shared__ int32_t s_page[kQbMaxBlocks];
+  __shared__ int s_abort;
+  constexpr uint64_t kLimit = 2000000000ull;
+  const int b = blockIdx.z;
+  const int P = kv.page_size;
+  const int SB = 64 / hpc;                    // blocks per stage
+  const int x0 = blockIdx.x * SB * kQbStagesPerCta;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = threadIdx.x >> 4, t = threadIdx.x & 15;
+  const int hh = h % hpc, g = blockIdx.y * hpc + hh;
+  const uint32_t row_bytes = (uint32_t)hpc * 256u;   // hpc heads x 128 bf16
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(qb_smem) + 127) & ~uintptr_t(127));
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < kQbStages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 8);
+    }
+    tc::fence_barrier_init();
+  }
+  pdl_enter();
+  const int ctx = kv.ctx_len[b];
+  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+  // the CTA's block-table entries (these reads do not wait for ctx_len)
+  for (int i = threadIdx.x; i < SB * kQbStagesPerCta; i += blockDim.x)
+    s_page[i] = x0 + i < u_stride ? bt[x0 + i] : -1;
+  float qp[8], qn[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    qp[i] = 0.f;
+    qn[i] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const uint4 u = ldg_nc_v4(q + ((int64_t)b * kv.Hq + g * G + j) * kv.D + t * 8);
+    float qv[8];
+    unpack8_bf16(u, qv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      qp[i] += fmaxf(qv[i], 0.f);
+      qn[i] += fminf(qv[i], 0.f);
+    }
+  }
+  const int nb = cdiv(ctx, P);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    write_ranges(rg, kv.status, b, nb, (int)u_stride);
+  __syncthreads();
+  // full blocks [0, nb - 1) of this CTA, as a count from x0
+  const int n_blocks = max(min(min(nb - 1, (int)u_stride) - x0, SB * kQbStagesPerCta), 0);
+  const int n_stages = cdiv(n_blocks, SB);
+  const char* kmn = reinterpret_cast<const char*>(kmin);
+  const char* kmx = reinterpret_cast<const char*>(kmax);
+  const int64_t head0 = (int64_t)blockIdx.y * hpc * 256;   // byte offset of head y hpc in a page's rows
+
+  // copies of stage n: block j of the stage by lane j (and j + 32)
+  auto issue = [&](int n) {
+    uint8_t* st = stages + (n % kQbStages) * kQbStageBytes;
+    for (int j = lane; j < SB; j += 32) {
+      const int i = n * SB + j;
+      const int page = i < n_blocks ? s_page[i] : -1;
+      if (page >= 0 && page < kv.num_pages) {
+        const int64_t src = (int64_t)page * kv.Hkv * 256 + head0;
+        tc::bulk_g2s(st + j * row_bytes, kmn + src, row_bytes, &full[n % kQbStages]);
+        tc::bulk_g2s(st + kQbStageBytes / 2 + j * row_bytes, kmx + src, row_bytes,
+                     &full[n % kQbStages]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&full[n % kQbStages]);
+  };
+
+  int issued = 0;
+  if (warp == 0)
+    for (; issued < min(kQbStages - 1, n_stages); ++issued) issue(issued);
+  for (int n = 0; n < n_stages; ++n) {
+    if (warp == 0 && issued < n_stages) {
+      // refill the buffer released in the previous iteration
+      const int m = issued;
+      const bool ok = m < kQbStages ||
+                      tc::mbar_wait(&empty[m % kQbStages], ((m / kQbStages) - 1) & 1, kLimit);
+      if (__all_sync(0xffffffffu, ok)) {
+        issue(m);
+        ++issued;
+      } else if (lane == 0) {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(&s_abort, 1);
+      }
+    }
+    const bool landed = tc::mbar_wait(&full[n % kQbStages], (n / kQbStages) & 1, kLimit);
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (lane == 0) {
+        set_status(kv.status, SE_ERR_TIMEOUT);
+        atomicExch(&s_abort, 1);
+      }
+      break;
+    }
+    const uint8_t* st = stages + (n % kQbStages) * kQbStageBytes;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = (16 * r + h) / hpc;          // block of the stage
+      const int i = n * SB + j;
+      const int page = i < n_blocks ? s_page[i] : -1;
+      const bool act = page >= 0 && page < kv.num_pages;
+      float acc = 0.f;
+      if (act) {
+        const int off = j * row_bytes + hh * 256 + t * 16;
+        float mn[8], mx[8];
+        unpack8_bf16(*reinterpret_cast<const uint4*>(st + off), mn);
+        unpack8_bf16(*reinterpret_cast<const uint4*>(st + kQbStageBytes / 2 + off), mx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(qn[e], mn[e], fmaf(qp[e], mx[e], acc));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (act && t == 0) U[((int64_t)b * kv.Hkv + g) * u_stride + x0 + i] = acc;
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[n % kQbStages]);
+  }
+  // after a timeout, copies of issued stages may still be in flight
+  if (warp == 0 && lane == 0)
+    for (int m = max(0, issued - kQbStages); m < issued; ++m)
+      tc::mbar_wait(&full[m % kQbStages], (m / kQbStages) & 1, kLimit);
+}
+
 // Generic bound (any D, fp32 or bf16): one thread per (block, group); CTA
 // (0, 0, b) also writes sequence b's ranges.
 template <typename T>
@@ -224,6 +375,21 @@ static QuestWs carve_quest(const se_paged_kv* kv, int32_t max_blocks, void* ws, 
   return w;
 }
 
+// The ring kernel's shared memory above 48 KB, allowed once per device and
+// group size; false where the device refuses it (the bound then runs in the
+// register kernel).
+static bool ring_ready(int G) {
+  const int smem = kQbStages * kQbStageBytes + 128;
+  static std::atomic<uint64_t> a1{0}, a2{0}, a4{0}, a8{0};
+  switch (G) {
+    case 1: return allow_smem(reinterpret_cast<const void*>(&quest_bound_ring_kernel<1>), smem, a1);
+    case 2: return allow_smem(reinterpret_cast<const void*>(&quest_bound_ring_kernel<2>), smem, a2);
+    case 4: return allow_smem(reinterpret_cast<const void*>(&quest_bound_ring_kernel<4>), smem, a4);
+    case 8: return allow_smem(reinterpret_cast<const void*>(&quest_bound_ring_kernel<8>), smem, a8);
+    default: return false;
+  }
+}
+
 }  // namespace se
 
 using namespace se;
@@ -271,11 +437,20 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
   const int G = kv->Hq / kv->Hkv;
   const QuestRanges rg{w.cand_lo, w.cand_hi, w.flo, w.fhi};
   const int hpc = kv->Hkv % 8 == 0 ? 8 : (kv->Hkv < 8 && 8 % kv->Hkv == 0 ? kv->Hkv : 0);
-  if (kv->dtype == SE_BF16 && kv->D == 128 && hpc > 0 && (G == 1 || G == 2 || G == 4 || G == 8)) {
+  const bool bf16_128 = kv->dtype == SE_BF16 && kv->D == 128 && hpc > 0 &&
+                        (G == 1 || G == 2 || G == 4 || G == 8);
+  auto km = static_cast<const __nv_bfloat16*>(kmin);
+  auto kx = static_cast<const __nv_bfloat16*>(kmax);
+  auto qq = static_cast<const __nv_bfloat16*>(q);
+  if (bf16_128 && ring_ready(G)) {
+    const dim3 grid(cdiv(max_blocks, 64 / hpc * kQbStagesPerCta), kv->Hkv / hpc, kv->B);
+    const int smem = kQbStages * kQbStageBytes + 128;
+    if (G == 1) se_launch(quest_bound_ring_kernel<1>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 2) se_launch(quest_bound_ring_kernel<2>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 4) se_launch(quest_bound_ring_kernel<4>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 8) se_launch(quest_bound_ring_kernel<8>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+  } else if (bf16_128) {
     const dim3 grid(cdiv(max_blocks, 16 / hpc * kBoundPages), kv->Hkv / hpc, kv->B);
-    auto km = static_cast<const __nv_bfloat16*>(kmin);
-    auto kx = static_cast<const __nv_bfloat16*>(kmax);
-    auto qq = static_cast<const __nv_bfloat16*>(q);
     if (G == 1) se_launch(quest_bound_bf16_kernel<1>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
     if (G == 2) se_launch(quest_bound_bf16_kernel<2>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
     if (G == 4) se_launch(quest_bound_bf16_kernel<4>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
