@@ -175,10 +175,10 @@ __global__ void __launch_bounds__(256) quest_bound_bf16_kernel(se_paged_kv kv,
 
 // Page bound over a ring of bulk-copied stages (bf16, D = 128): the same
 // bounds as quest_bound_bf16_kernel, with each CTA keeping copies in flight
-// across many pages.  grid: (cdiv(max_blocks, 8 SB), Hkv / hpc, B), 256
+// across many pages.  grid: (cdiv(max_blocks, L), Hkv / hpc, B), 256
 // threads, dynamic smem kQbStages x 32 KB.  CTA (x, y, b) takes the blocks
-// [8 SB x, 8 SB (x + 1)) of sequence b (eight stages of SB = 64 / hpc
-// blocks) for heads [y hpc, (y + 1) hpc).  Warp 0 copies, per block, the kmin
+// [L x, L (x + 1)) of sequence b (L a multiple of SB = 64 / hpc blocks, at
+// most eight stages) for heads [y hpc, (y + 1) hpc).  Warp 0 copies, per block, the kmin
 // rows of the hpc heads (hpc x 256 contiguous bytes) and their kmax rows into
 // a stage; two stages are in flight while the CTA computes a third.
 // Half-warp h serves head y hpc + h % hpc for the whole launch (its folded
@@ -194,7 +194,7 @@ constexpr int kQbMaxBlocks = kQbStagesPerCta * 64;
 template <int G>
 __global__ void __launch_bounds__(256, 2) quest_bound_ring_kernel(
     se_paged_kv kv, const __nv_bfloat16* __restrict__ kmin, const __nv_bfloat16* __restrict__ kmax,
-    const __nv_bfloat16* __restrict__ q, float* __restrict__ U, int64_t u_stride, int hpc,
+    const __nv_bfloat16* __restrict__ q, float* __restrict__ U, int64_t u_stride, int hpc, int L,
     QuestRanges rg) {
   extern __shared__ __align__(128) uint8_t qb_smem[];
   __shared__ uint64_t full[kQbStages], empty[kQbStages];
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(256, 2) quest_bound_ring_kernel(
   const int b = blockIdx.z;
   const int P = kv.page_size;
   const int SB = 64 / hpc;                    // blocks per stage
-  const int x0 = blockIdx.x * SB * kQbStagesPerCta;
+  const int x0 = blockIdx.x * L;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = threadIdx.x >> 4, t = threadIdx.x & 15;
   const int hh = h % hpc, g = blockIdx.y * hpc + hh;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(256, 2) quest_bound_ring_kernel(
   const int ctx = kv.ctx_len[b];
   const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
   // the CTA's block-table entries (these reads do not wait for ctx_len)
-  for (int i = threadIdx.x; i < SB * kQbStagesPerCta; i += blockDim.x)
+  for (int i = threadIdx.x; i < L; i += blockDim.x)
     s_page[i] = x0 + i < u_stride ? bt[x0 + i] : -1;
   float qp[8], qn[8];
 #pragma unroll
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(256, 2) quest_bound_ring_kernel(
     write_ranges(rg, kv.status, b, nb, (int)u_stride);
   __syncthreads();
   // full blocks [0, nb - 1) of this CTA, as a count from x0
-  const int n_blocks = max(min(min(nb - 1, (int)u_stride) - x0, SB * kQbStagesPerCta), 0);
+  const int n_blocks = max(min(min(nb - 1, (int)u_stride) - x0, L), 0);
   const int n_stages = cdiv(n_blocks, SB);
   const char* kmn = reinterpret_cast<const char*>(kmin);
   const char* kmx = reinterpret_cast<const char*>(kmax);
@@ -443,12 +443,18 @@ extern "C" se_status se_quest_page_select(const se_paged_kv* kv, const void* kmi
   auto kx = static_cast<const __nv_bfloat16*>(kmax);
   auto qq = static_cast<const __nv_bfloat16*>(q);
   if (bf16_128 && ring_ready(G)) {
-    const dim3 grid(cdiv(max_blocks, 64 / hpc * kQbStagesPerCta), kv->Hkv / hpc, kv->B);
+    // one even wave of two CTAs per SM where the blocks allow it: L blocks
+    // per CTA, a multiple of a stage, at most eight stages
+    const int SB = 64 / hpc;
+    const int sets = kv->B * (kv->Hkv / hpc);
+    const int nx0 = max(cdiv(2 * 152, sets), cdiv(max_blocks, kQbMaxBlocks));
+    const int L = cdiv(cdiv(max_blocks, nx0), SB) * SB;
+    const dim3 grid(cdiv(max_blocks, L), kv->Hkv / hpc, kv->B);
     const int smem = kQbStages * kQbStageBytes + 128;
-    if (G == 1) se_launch(quest_bound_ring_kernel<1>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
-    if (G == 2) se_launch(quest_bound_ring_kernel<2>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
-    if (G == 4) se_launch(quest_bound_ring_kernel<4>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
-    if (G == 8) se_launch(quest_bound_ring_kernel<8>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
+    if (G == 1) se_launch(quest_bound_ring_kernel<1>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, L, rg);
+    if (G == 2) se_launch(quest_bound_ring_kernel<2>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, L, rg);
+    if (G == 4) se_launch(quest_bound_ring_kernel<4>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, L, rg);
+    if (G == 8) se_launch(quest_bound_ring_kernel<8>, grid, 256, smem, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, L, rg);
   } else if (bf16_128) {
     const dim3 grid(cdiv(max_blocks, 16 / hpc * kBoundPages), kv->Hkv / hpc, kv->B);
     if (G == 1) se_launch(quest_bound_bf16_kernel<1>, grid, 256, 0, st, *kv, km, kx, qq, w.U, w.u_stride, hpc, rg);
