@@ -144,6 +144,26 @@ SE_DEV int view_entries(const DecodeArgs& a, int ctx) {
   return a.n_sel;
 }
 
+// The G logits of one entry (G consecutive floats, 4 G-byte aligned: the
+// logits array is 256-byte aligned and holds G floats per entry) through
+// L2, as 16-, 8- or 4-byte loads; zeros when !ok.
+template <int G>
+SE_DEV void load_logits(const float* p, bool ok, float (&v)[G]) {
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < G; j += 4) {
+      const float4 f = ok ? __ldcg(reinterpret_cast<const float4*>(p + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 f = ok ? __ldcg(reinterpret_cast<const float2*>(p)) : make_float2(0.f, 0.f);
+    v[0] = f.x; v[1] = f.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < G; ++j) v[j] = ok ? __ldcg(p + j) : 0.f;
+  }
+}
+
 // Merges the n_parts partials of unit u = (b, g), writes o and updates the
 // running scores.  Run by the last CTA to finish a segment of u (128 threads).
 template <typename T, int D, int G>
@@ -184,13 +204,14 @@ SE_DEV void merge_chunks(const DecodeArgs& a, int u, int n_parts) {
     else *op = v;
   }
   if (acc != nullptr && a.logits != nullptr) {
-    // four entries per thread per round, every load of a round issued before
-    // the first use, so a round costs one memory latency rather than four
+    // eight entries per thread per round, every load of a round issued before
+    // the first use (an entry's G logits as vector loads), so a round costs
+    // one memory latency rather than eight
     const int ctx = kv.ctx_len[b];
     const int n_view = min(view_entries(a, ctx), a.max_entries);
     const float* lg = a.logits + ((int64_t)b * kv.Hkv + g) * a.max_entries * G;
     float* ar = acc + ((int64_t)b * kv.Hkv + g) * acc_stride;
-    constexpr int U = 4;
+    constexpr int U = 8;
     for (int e0 = threadIdx.x; e0 < n_view; e0 += U * blockDim.x) {
       int sl[U];
       float lv[U][G], old[U];
@@ -198,8 +219,7 @@ SE_DEV void merge_chunks(const DecodeArgs& a, int u, int n_parts) {
       for (int k = 0; k < U; ++k) {
         const int e = e0 + k * blockDim.x;
         sl[k] = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
-#pragma unroll
-        for (int j = 0; j < G; ++j) lv[k][j] = sl[k] >= 0 ? __ldcg(lg + (int64_t)e * G + j) : 0.f;
+        load_logits<G>(lg + (int64_t)e * G, sl[k] >= 0, lv[k]);
         old[k] = sl[k] >= 0 ? __ldcg(ar + sl[k]) : 0.f;
       }
 #pragma unroll
@@ -563,18 +583,35 @@ SE_DEV int resolve_rows(const DecodeArgs& a, int u, int e_begin, int n, int32_t*
   const int ctx = kv.ctx_len[b];
   const int n_view = min(view_entries(a, ctx), a.max_entries);
   const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-  for (int x = threadIdx.x; x < n; x += blockDim.x) {
-    const int e = e_begin + x;
-    int slot, page;
-    if (a.view == SE_VIEW_DENSE) {
-      const int ip = e / P;
-      page = ip < kv.max_pages_per_seq ? bt[ip] : -1;
-      slot = e < n_view ? e : -1;
-    } else {
-      slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
-      page = slot >= 0 ? bt[slot / P] : -1;
+  // four entries per thread per round, every load of a round issued before
+  // the first use
+  constexpr int R = 4;
+  for (int x0 = threadIdx.x; x0 < n; x0 += R * blockDim.x) {
+    int slot[R], page[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const int x = x0 + k * blockDim.x;
+      const int e = e_begin + x;
+      if (a.view == SE_VIEW_DENSE) {
+        const int ip = e / P;
+        page[k] = (x < n && ip < kv.max_pages_per_seq) ? bt[ip] : -1;
+        slot[k] = (x < n && e < n_view) ? e : -1;
+      } else {
+        slot[k] = (x < n && e < n_view) ? view_slot(a, b, g, e, ctx) : -1;
+      }
     }
-    rows[x] = (slot >= 0 && page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
+    if (a.view != SE_VIEW_DENSE) {
+#pragma unroll
+      for (int k = 0; k < R; ++k) page[k] = slot[k] >= 0 ? bt[slot[k] / P] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const int x = x0 + k * blockDim.x;
+      if (x < n)
+        rows[x] = (slot[k] >= 0 && page[k] >= 0 && page[k] < kv.num_pages)
+                      ? (page[k] * kv.Hkv + g) * P + slot[k] % P
+                      : -1;
+    }
   }
   return max(min(e_begin + n, n_view) - e_begin, 0);
 }
@@ -872,21 +909,9 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_par
   for (int64_t xs = x0, k = 0; xs < x1; ++k) {
     const int u = (int)(xs / a.sp);
     const int64_t xe = min(x1, (int64_t)(u + 1) * a.sp);
-    const int b = u / kv.Hkv, g = u % kv.Hkv;
-    const int P = kv.page_size;
-    const int ctx = kv.ctx_len[b];
-    const int n_view = min(view_entries(a, ctx), a.max_entries);
     const int e_begin = (int)(xs - (int64_t)u * a.sp) * SE;
-    const int n_all = (int)(xe - xs) * SE;
-    if (threadIdx.x == 0) s_nseg[k] = max(min(e_begin + n_all, n_view) - e_begin, 0);
-    int32_t* rows = s_rows + (int)(xs - x0) * SE;
-    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-    for (int x = threadIdx.x; x < n_all; x += blockDim.x) {
-      const int e = e_begin + x;
-      const int slot = e < n_view ? view_slot(a, b, g, e, ctx) : -1;
-      const int page = slot >= 0 ? bt[slot / P] : -1;
-      rows[x] = (page >= 0 && page < kv.num_pages) ? (page * kv.Hkv + g) * P + slot % P : -1;
-    }
+    const int n = resolve_rows(a, u, e_begin, (int)(xe - xs) * SE, s_rows + (int)(xs - x0) * SE);
+    if (threadIdx.x == 0) s_nseg[k] = n;
     xs = xe;
   }
   __syncthreads();
@@ -1280,8 +1305,7 @@ __global__ void __launch_bounds__(128, StagedGeom<T, D, G>::MIN_CTAS) decode_clu
       for (int kk = 0; kk < U; ++kk) {
         const int e = e00 + kk * 128;
         sl[kk] = (e < e_end && s_rows[e - e_begin] >= 0) ? view_slot(a, b, g, e, ctx) : -1;
-#pragma unroll
-        for (int j = 0; j < G; ++j) lv[kk][j] = sl[kk] >= 0 ? __ldcg(lg + (int64_t)e * G + j) : 0.f;
+        load_logits<G>(lg + (int64_t)e * G, sl[kk] >= 0, lv[kk]);
         old[kk] = sl[kk] >= 0 ? __ldcg(ar + sl[kk]) : 0.f;
       }
 #pragma unroll
