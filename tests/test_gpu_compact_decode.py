@@ -170,3 +170,43 @@ def test_compact_decode_refusals_leave_cache_unchanged(cuda_lib, case):
     assert H.status(pc) == want
     for name in ["block_table", "slot_map", "ctx_len", "free_list", "free_top", "page_refcount"]:
         assert torch.equal(getattr(pc, name), getattr(before, name)), name
+
+
+def test_compact_decode_reuses_its_workspace_after_a_refusal(cuda_lib):
+    """Three calls on one workspace (one max_keep, so one size): a compaction,
+    a refused one (a keep list out of order), and another compaction of the
+    result.  Nothing of the refused call (its abort flag, its page counts)
+    leaks into the next: the cache and output match the oracle after the
+    third call."""
+    se = cuda_lib
+    B, Hkv, W_ = 3, 2, 300
+    shape, pc, q = _cache(torch.bfloat16, 128, 4, B=B, Hkv=Hkv, ctx=300, spare=80, tag="cdws")
+    kv = se.kv_desc(pc, shape.Hq)
+    ws = torch.zeros(se._lib.se_compact_decode_workspace_size(kv, W_, 300), dtype=torch.uint8,
+                     device="cuda")
+
+    def call(keep, first, o):
+        kt = H.keep_tensor(keep, B, Hkv, W_, "cuda")
+        n_keep = torch.tensor([len(keep[b][0]) for b in range(B)], dtype=torch.int32, device="cuda")
+        fs = torch.tensor(first, dtype=torch.int32, device="cuda")
+        se.se_compact_decode(kv, kt, n_keep=n_keep, first_slot=fs, max_keep=W_, q=q, o=o,
+                             max_entries=300, workspace=ws)
+        torch.cuda.synchronize()
+
+    c = ocache.from_tensors(pc)
+    keep, first = H.random_keep(c, 21, first=[0, 40, 100], frac=0.6)
+    assert ocache.compact(c, keep, first) == ocache.SE_OK
+    call(keep, first, torch.empty_like(q))
+    assert H.status(pc) == 0
+    before = pc.clone()
+    call([[np.array([5, 3])] * Hkv for _ in range(B)], [0] * B, torch.empty_like(q))
+    assert H.status(pc) == se.SE_ERR_BOUNDS
+    for name in ["block_table", "slot_map", "ctx_len", "free_list", "free_top", "page_refcount"]:
+        assert torch.equal(getattr(pc, name), getattr(before, name)), name
+    pc.status.zero_()
+    keep2, first2 = H.random_keep(c, 22, frac=0.5)
+    assert ocache.compact(c, keep2, first2) == ocache.SE_OK
+    o2 = torch.full_like(q, float("nan"))
+    call(keep2, first2, o2)
+    assert H.status(pc) == 0
+    _check_against_oracle(pc, c, shape, q, o2)

@@ -174,6 +174,46 @@ def test_quest_meta_and_selection_match_oracle(cuda_lib, ctx, top):
                 assert (got[b, g, nsel:] == -1).all()
 
 
+@pytest.mark.parametrize("Hkv,G,dtype", [(1, 8, torch.bfloat16), (2, 4, torch.bfloat16),
+                                         (4, 2, torch.bfloat16), (8, 1, torch.bfloat16),
+                                         (2, 4, torch.float32)])
+def test_quest_selection_head_layouts_match_oracle(cuda_lib, Hkv, G, dtype):
+    """The page bound for every layout of KV heads over a CTA (1, 2, 4 or 8
+    heads of a page read together), group sizes 1 to 8, and the fp32 form;
+    contexts that end inside a page and span several CTA ranges."""
+    se = cuda_lib
+    ctx, top = 16 * 1500 + 9, 60
+    shape = W.quest_decode(B=2, ctx=ctx, top_pages=top, steps=1, Hq=Hkv * G, Hkv=Hkv, dtype=dtype)
+    inp = W.quest_inputs(shape, "cuda")
+    pc = inp["cache"]
+    pc.ctx_len.copy_(torch.tensor([ctx, ctx - 5000], dtype=torch.int32))
+    kv = se.kv_desc(pc, shape.Hq)
+    kmin = torch.empty_like(pc.k_pool[:, :, 0, :])
+    kmax = torch.empty_like(kmin)
+    se.se_quest_build_meta(kv, kmin, kmax)
+    c = ocache.from_tensors(pc)
+    omin, omax = oquest.build_meta(c)
+    nb_max = W.cdiv(ctx, 16)
+    q = inp["q_steps"][0]
+    page_idx = torch.full((2, Hkv, top + 1), -9, dtype=torch.int32, device="cuda")
+    n_sel = torch.zeros(2, dtype=torch.int32, device="cuda")
+    se.se_quest_page_select(kv, kmin, kmax, q, top_pages=top, max_blocks=nb_max,
+                            page_idx=page_idx, n_sel=n_sel)
+    torch.cuda.synchronize()
+    assert H.status(pc) == 0
+    qv = q.double().cpu().numpy()
+    got = page_idx.cpu().numpy()
+    for b in range(2):
+        nb = W.cdiv(int(c.ctx_len[b]), 16)
+        nsel = min(top, nb - 1) + 1
+        assert int(n_sel[b].item()) == nsel
+        for g in range(Hkv):
+            sel, U = oquest.select_pages(c, omin, omax, qv[b], top, b, g)
+            ranking = {i: float(U[i]) for i in range(nb - 1)}
+            H.assert_keep_near(got[b, g, :nsel], sel, ranking, min(top, nb - 1), [nb - 1])
+            assert (got[b, g, nsel:] == -1).all()
+
+
 # ---------------------------------------------------------------------------
 # decode attention
 # ---------------------------------------------------------------------------
