@@ -45,7 +45,7 @@ constexpr int kQChunkBytes = kRowChunk * kD * 2; // 64 KB
 constexpr int kStages1 = 4;         // K-tile ring depth, pass 1
 constexpr int kEpiWarps = 16;       // epilogue warps (4 per SM sub-partition)
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait (drains: always)
 
 struct TcArgs {
   int B, Hq, Hkv, G, w, P, rows, RC;  // RC: row chunks of 256
@@ -66,7 +66,25 @@ struct TcArgs {
   int n_splits, tiles_per_split, tiles_per_cta2;
   int32_t* status;
   float scale;      // log2(e) / sqrt(D)
+  const unsigned long long* limit;   // workspace bytes [0, 8): wait limit in ns, 0 = kTimeoutNs
+  unsigned int* diag;                // workspace bytes [12, 16): first wait that gave up
 };
+
+// Limit of the producer's waits that give up (SE_ERR_TIMEOUT).  The MMA
+// issuer's and the epilogue warps' waits keep kTimeoutNs (a runtime limit
+// there measured 1-3 % slower) and end through the abort of the producer
+// that feeds them; the drains (copies and MMAs in flight) always wait up to
+// kTimeoutNs.
+SE_DEV uint64_t wait_limit(const TcArgs& a) {
+  const uint64_t v = a.limit != nullptr ? *a.limit : 0ull;
+  return v != 0 ? v : kTimeoutNs;
+}
+
+// A producer wait: the limit is read only once a first try has failed.
+SE_DEV bool producer_wait(uint64_t* bar, uint32_t parity, const TcArgs& a) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  return tc::mbar_wait(bar, parity, wait_limit(a));
+}
 
 // Key-tile geometry of one (sequence, group): tiles start at the page that
 // holds attn_lo; tile t covers slots [base + 128 t, base + 128 t + 128).
@@ -138,6 +156,8 @@ SE_DEV bool aborted(const int* flag) { return *reinterpret_cast<const volatile i
 
 SE_DEV void record_timeout(const TcArgs& a, int* s_abort) {
   set_status(a.status, SE_ERR_TIMEOUT);
+  if (a.diag != nullptr)
+    atomicCAS(a.diag, 0u, 1u + ((threadIdx.x >> 5) << 8 | (blockIdx.x & 0xffffu) << 16));
   atomicExch(s_abort, 1);
 }
 
@@ -431,8 +451,8 @@ score_rowstats_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int s = i % kStages1;
         const uint32_t par = ((i / kStages1) & 1) ^ 1;
         if (i >= kStages1) {
-          if (!tc::mbar_wait(&empty[s], par, kTimeoutNs) ||
-              !tc::mbar_wait(&pos_free[s], par, kTimeoutNs)) {
+          if (!producer_wait(&empty[s], par, a) ||
+              !producer_wait(&pos_free[s], par, a)) {
             record_timeout(a, &s_abort);
             break;
           }
@@ -672,8 +692,8 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             for (int t = 2 * p; t < min(2 * p + 2, n_my); ++t) {
               const int s = t % KS;
               const uint32_t par = ((t / KS) & 1) ^ 1;
-              if (t >= KS && (!tc::mbar_wait(&kempty[s], par, kTimeoutNs) ||
-                              !tc::mbar_wait(&pfree[s], par, kTimeoutNs))) {
+              if (t >= KS && (!producer_wait(&kempty[s], par, a) ||
+                              !producer_wait(&pfree[s], par, a))) {
                 record_timeout(a, &s_abort);
                 stop = true;
                 break;
@@ -687,8 +707,8 @@ score_colsum_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           if (q_resident && q_issued > 0) continue;
           const int qs = q_issued % QS;
           const uint32_t par = ((q_issued / QS) & 1) ^ 1;
-          if (q_issued >= QS && (!tc::mbar_wait(&qempty[qs], par, kTimeoutNs) ||
-                                 !tc::mbar_wait(&ifree[qs], par, kTimeoutNs))) {
+          if (q_issued >= QS && (!producer_wait(&qempty[qs], par, a) ||
+                                 !producer_wait(&ifree[qs], par, a))) {
             record_timeout(a, &s_abort);
             stop = true;
             break;
@@ -991,7 +1011,7 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         while (tile >= s_pre[bg + 1] - s_pre[bg]) { ++bg; tile = 0; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
-          if (gi > 0 && !tc::mbar_wait(q_done, (gi - 1) & 1, kTimeoutNs)) {
+          if (gi > 0 && !producer_wait(q_done, (gi - 1) & 1, a)) {
             record_timeout(a, &s_abort);
             break;
           }
@@ -1001,8 +1021,8 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         }
         const int s = i % KS;
         const uint32_t par = ((i / KS) & 1) ^ 1;
-        if (i >= KS && (!tc::mbar_wait(&empty[s], par, kTimeoutNs) ||
-                        !tc::mbar_wait(&pos_free[s], par, kTimeoutNs))) {
+        if (i >= KS && (!producer_wait(&empty[s], par, a) ||
+                        !producer_wait(&pos_free[s], par, a))) {
           record_timeout(a, &s_abort);
           break;
         }
@@ -1246,7 +1266,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         while (tile < 0) { --bg; tile = s_pre[bg + 1] - s_pre[bg] - 1; }
         const int b = bg / a.Hkv, g = bg % a.Hkv;
         if (bg != cur) {
-          if (gi > 0 && !tc::mbar_wait(qdone, (gi - 1) & 1, kTimeoutNs)) {
+          if (gi > 0 && !producer_wait(qdone, (gi - 1) & 1, a)) {
             record_timeout(a, &s_abort);
             break;
           }
@@ -1258,8 +1278,8 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
         }
         const int s = lt % KS;
         const uint32_t par = ((lt / KS) & 1) ^ 1;
-        if (lt >= KS && (!tc::mbar_wait(&kempty[s], par, kTimeoutNs) ||
-                         !tc::mbar_wait(&pfree[s], par, kTimeoutNs))) {
+        if (lt >= KS && (!producer_wait(&kempty[s], par, a) ||
+                         !producer_wait(&pfree[s], par, a))) {
           record_timeout(a, &s_abort);
           break;
         }
@@ -1560,7 +1580,11 @@ se_status launch_score_tc(const se_paged_kv* kv, const void* q_win, int w, const
   a.causal = causal; a.accumulate = accumulate; a.n_max = n_max;
   a.scores = scores; a.scores_stride = scores_stride;
   WsCarver c(ws);
-  c.take<uint8_t>(score_fused_ctrl_bytes(kv));
+  // the control block at the start of the workspace: [0, 8) wait limit,
+  // [12, 16) the first wait that gave up
+  uint8_t* ctrl = c.take<uint8_t>(score_fused_ctrl_bytes(kv));
+  a.limit = reinterpret_cast<const unsigned long long*>(ctrl);
+  a.diag = reinterpret_cast<unsigned int*>(ctrl + 12);
   const int slots = std::max(2 * p.n_splits, p.RC == 1 ? 2 * kMaxPersistentCTAs : 0);
   a.part = c.take<float>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk * slots * 2);
   a.rowinfo = c.take<float2>((size_t)kv->B * kv->Hkv * p.RC * kRowChunk);

@@ -78,8 +78,17 @@ SE_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time (globaltimer), returning false; the caller then
-// records SE_ERR_TIMEOUT and winds down instead of spinning forever.
+// records SE_ERR_TIMEOUT and winds down instead of spinning forever.  A
+// limit below 1 us (a test's) is polled with the non-blocking test_wait:
+// try_wait may suspend the thread for longer than such a limit.
 SE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < 1000ull) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t n = 0;

@@ -130,11 +130,12 @@ typedef struct {
  *             that every call leaves zero again, so a workspace is zeroed
  *             once and reused; calls that share a workspace must not
  *             overlap on the GPU.  Its first 8 bytes may hold a limit in
- *             nanoseconds for the kernel's bounded waits (0: 2 s); a wait
- *             that runs out sets SE_ERR_TIMEOUT in kv->status, records
- *             where it was in bytes [12, 16) (nonzero; the caller reads and
- *             clears it) and the launch winds down without writing further
- *             scores.
+ *             nanoseconds for the kernels' bounded waits (0: 2 s; both the
+ *             tensor-core forms read it); a wait that runs out sets
+ *             SE_ERR_TIMEOUT in kv->status, records where it was in bytes
+ *             [12, 16) (nonzero; the caller reads and clears it) and the
+ *             launch winds down -- copies and MMAs in flight are still
+ *             waited for, up to 2 s -- without writing further scores.
  * A query that sees no key adds nothing.
  *
  * bf16 with D = 128 runs on the tensor cores: a sweep of row statistics,
@@ -265,9 +266,11 @@ size_t se_compact_evict_workspace_size(const se_paged_kv* kv, int32_t max_keep);
  *
  * max_entries (host) must be at least every compacted length first_slot[b] +
  * n_keep[b]; a longer sequence is refused on the device (SE_ERR_BOUNDS, cache
- * untouched).  Shapes the one-pass kernel does not take (more than 16 x 512
- * entries per (sequence, KV head), or no cluster of that size fits) run the
- * compaction and then the decode attention, with the same results.
+ * untouched).  The one-pass kernel runs one cluster of k CTAs per (sequence,
+ * KV head), k a power of two up to 16 with at most 512 entries per CTA and at
+ * most 152 x 4 CTAs in all; other shapes (and devices where such a cluster
+ * does not fit) run the compaction and then the decode attention, with the
+ * same results.
  * Workspace: se_compact_decode_workspace_size bytes, zeroed before its first
  * use (the decode part keeps per-unit counters there that every completed
  * call leaves at zero).  Device errors as se_compact_evict(FRESH_PAGES); after

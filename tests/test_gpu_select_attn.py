@@ -471,3 +471,53 @@ def test_score_window_accumulates(cuda_lib):
     c = ocache.from_tensors(pc)
     row = oscore.score_window(c, q_win, q_pos.cpu().numpy(), [0], [ctx], [0], [ctx], True)[(0, 0)]
     H.assert_scores_close(scores[0, 0].cpu().double().numpy(), 1.0 + 2 * row, torch.float32, w, G)
+
+
+@pytest.mark.parametrize("w", [64, 100])
+def test_score_window_wait_limit_runs_out(cuda_lib, w):
+    """The default (two-launch) tcgen05 scorer honours the wait limit in the
+    workspace's control block: with 1 ns the key producer's first wait for a
+    free stage gives up, the status word reads SE_ERR_TIMEOUT, the place is
+    recorded and the launch winds down (the drains still wait for copies and
+    MMAs in flight).  The next call on the same workspace (limit cleared,
+    status reset) gives the scores of a call on a fresh workspace bit for bit
+    and matches the oracle on a sampled group.  w = 64: one chunk of 256 rows
+    (persistent kernels); w = 100: two row chunks (the grid kernels).  16384
+    keys give every CTA more key tiles than its stage ring holds."""
+    se = cuda_lib
+    B, Hkv, G, ctx = 2, 4, 4, 16384
+    tag = f"sto{w}"
+    shape = W.Shape(name=tag, B=B, Hq=Hkv * G, Hkv=Hkv, D=128, page_size=16, ctx=ctx,
+                    dtype=torch.bfloat16)
+    pc = W.build_paged_cache(shape, num_pages=B * W.cdiv(ctx, 16) + 3, max_ctx=ctx, device="cuda",
+                             tag=tag)
+    q_win = W.normal((B, w, shape.Hq, 128), torch.bfloat16, "cuda", tag, "q")
+    q_pos = torch.arange(ctx - w, ctx, dtype=torch.int32).repeat(B, 1).cuda()
+    kv = se.kv_desc(pc, shape.Hq)
+    nbytes = se._lib.se_score_window_workspace_size(kv, w, ctx)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    z, n = H.ranges(B, 0, ctx)
+    lo, hi = H.ranges(B, 0, ctx - w)
+
+    def call(workspace):
+        out = torch.zeros((B, Hkv, ctx), device="cuda")
+        se.se_score_window(kv, q_win, q_pos, z, n, lo, hi, causal=True, accumulate=False,
+                           n_max=ctx, scores=out, workspace=workspace)
+        torch.cuda.synchronize()
+        return out
+
+    ws[:8].view(torch.int64).fill_(1)
+    call(ws)
+    assert H.status(pc) == se.SE_ERR_TIMEOUT
+    assert int(ws[12:16].view(torch.int32).item()) != 0
+    ws[:16].zero_()
+    pc.status.zero_()
+    again = call(ws)
+    assert H.status(pc) == 0
+    fresh = call(torch.zeros(nbytes, dtype=torch.uint8, device="cuda"))
+    assert torch.equal(again, fresh)
+    c = ocache.from_tensors(pc)
+    ref = oscore.score_window(c, q_win, q_pos.cpu().numpy(), [0] * B, [ctx] * B, [0] * B,
+                              [ctx - w] * B, True, groups=[(1, 3)])
+    H.assert_scores_close(again[1, 3, :ctx - w].cpu().double().numpy(), ref[(1, 3)],
+                          torch.bfloat16, w, G)
