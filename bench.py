@@ -410,41 +410,64 @@ def run_snapkv(args, torch, rank, world):
 
 
 def run_e2e_snapkv(torch, pipe, inp, restore, steps):
-    """Same metric through the public API with host-resident per-step inputs:
-    each step copies q_win, q_pos, q_dec from pinned host memory, runs the
-    pipeline step (captured once in a CUDA graph over the device input
-    buffers, as a serving loop would) and reads the decode output and the
-    kept indices back."""
+    """Same metric through the public API with host-resident per-step inputs,
+    as a serving loop runs it: the pipeline step is captured once per input
+    buffer in a CUDA graph (two device input buffers); while step i computes
+    from one buffer, a second stream copies the next step's q_win, q_pos,
+    q_dec from pinned host memory into the other, and after the step its
+    decode output and kept indices are read back.  Each timed step holds the
+    graph, one host-to-device copy of a step's inputs (the step's end waits
+    for it) and the device-to-host read of its own results; steps are
+    enqueued without host synchronisation between them."""
     hq = {k: inp[k].cpu().pin_memory() for k in ("q_win", "q_pos", "q_dec")}
-    dq = {k: torch.empty_like(inp[k]) for k in hq}
-    o = torch.empty_like(inp["q_dec"])
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    dq = [{k: torch.empty_like(inp[k]) for k in hq} for _ in range(2)]
+    outs = [torch.empty_like(inp["q_dec"]) for _ in range(2)]
+    ho = torch.empty(outs[0].shape, dtype=outs[0].dtype, pin_memory=True)
     hk = torch.empty(pipe.keep.shape, dtype=pipe.keep.dtype, pin_memory=True)
-    for k in hq:
-        dq[k].copy_(hq[k])
-    restore()
-    pipe.step(dq["q_win"], dq["q_pos"], dq["q_dec"], o)      # warm
+    for j in range(2):
+        for k in hq:
+            dq[j][k].copy_(hq[k])
+    graphs = []
+    for j in range(2):
+        restore()
+        pipe.step(dq[j]["q_win"], dq[j]["q_pos"], dq[j]["q_dec"], outs[j])      # warm
+        torch.cuda.synchronize()
+        restore()
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            pipe.step(dq[j]["q_win"], dq[j]["q_pos"], dq[j]["q_dec"], outs[j])
+        graphs.append(g_)
     torch.cuda.synchronize()
-    restore()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        pipe.step(dq["q_win"], dq["q_pos"], dq["q_dec"], o)
-    torch.cuda.synchronize()
-    total = []
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    # steps are enqueued back to back (no host synchronisation between them,
+    # as a serving loop runs); buffer 1 - j is refilled only after the step
+    # that read it last has ended
+    ev = []
+    ends = [None, None]
     for i in range(steps + 2):
+        j = i % 2
         restore()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for k in hq:
-            dq[k].copy_(hq[k], non_blocking=True)
-        graph.replay()
-        ho.copy_(o, non_blocking=True)
+        h2d = torch.cuda.Event()
+        e0.record(main)
+        if ends[1 - j] is not None:
+            side.wait_event(ends[1 - j])
+        side.wait_event(e0)
+        with torch.cuda.stream(side):
+            for k in hq:
+                dq[1 - j][k].copy_(hq[k], non_blocking=True)   # the next step's inputs
+            h2d.record(side)
+        graphs[j].replay()
+        ho.copy_(outs[j], non_blocking=True)
         hk.copy_(pipe.keep, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= 2:
-            total.append(e0.elapsed_time(e1))
+        main.wait_event(h2d)
+        e1.record(main)
+        ends[j] = e1
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    total = [x.elapsed_time(y) for x, y in ev[2:]]
     bi = sum(t.numel() * t.element_size() for t in hq.values())
     bo = ho.numel() * ho.element_size() + hk.numel() * hk.element_size()
     return statistics.mean(total), bi, bo
