@@ -299,122 +299,117 @@ __global__ void __launch_bounds__(1024, 2) compact_commit_kernel(se_paged_kv kv,
 
 struct MoveWs {
   CompactCtrl* ctrl;
-  int32_t* act;       // [B] 1 = evict one
-  int32_t* off_push;  // [B]
-  int32_t* ctx;       // [B] snapshot
 };
 
 static MoveWs carve_move(const se_paged_kv* kv, void* ws, size_t* bytes) {
   WsCarver c(ws);
   MoveWs w;
   w.ctrl = c.take<CompactCtrl>(1);
-  w.act = c.take<int32_t>(kv->B);
-  w.off_push = c.take<int32_t>(kv->B);
-  w.ctx = c.take<int32_t>(kv->B);
   *bytes = c.bytes();
   return w;
 }
 
-__global__ void __launch_bounds__(1024) move_last_plan_kernel(se_paged_kv kv,
-                                                              const int32_t* __restrict__ victim,
-                                                              MoveWs w) {
+// Move-last eviction in one launch.  grid: B, 256 threads (one warp per KV
+// head).  Every CTA validates the victims of every sequence (all heads evict
+// or none) and takes the free-list rank of its sequence's emptied page from a
+// scan over the sequences before it; a call with an invalid sequence changes
+// nothing.  CTA b moves the last entry of sequence b into each head's victim
+// slot and pushes the page the move empties; the last CTA to finish commits
+// the lengths and the free-list top, which every CTA read first.
+__global__ void __launch_bounds__(256) move_last_kernel(se_paged_kv kv,
+                                                        const int32_t* __restrict__ victim,
+                                                        float* aux, int64_t aux_stride, MoveWs w) {
   pdl_enter();
   __shared__ int tmp[33];
-  __shared__ int s_bad, s_run;
-  const int tid = threadIdx.x;
-  if (tid == 0) { s_bad = 0; s_run = 0; }
+  __shared__ int s_bad, s_off, s_act;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int P = kv.page_size;
+  const int top0 = *kv.free_top;
+  if (tid == 0) {
+    s_bad = 0;
+    s_off = 0;
+    s_act = 0;
+  }
   __syncthreads();
+  int run = 0;   // pages pushed by the sequences before the current chunk
   for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
-    const int b = b0 + tid;
+    const int bb = b0 + tid;
     int freed = 0;
-    if (b < kv.B) {
-      const int ctx = kv.ctx_len[b];
+    if (bb < kv.B) {
+      const int ctx = kv.ctx_len[bb];
       int n_neg = 0, n_ok = 0;
       for (int h = 0; h < kv.Hkv; ++h) {
-        const int v = victim[b * kv.Hkv + h];
+        const int v = victim[bb * kv.Hkv + h];
         n_neg += v < 0;
         n_ok += (v >= 0 && v < ctx);
       }
-      int act = 0;
-      if (n_neg == kv.Hkv) {
-        act = 0;
-      } else if (n_ok == kv.Hkv) {
-        act = 1;
-      } else {
+      if (n_neg != kv.Hkv && n_ok != kv.Hkv) {
         set_status(kv.status, n_neg > 0 ? SE_ERR_UNEVEN : SE_ERR_BOUNDS);
         atomicExch(&s_bad, 1);
       }
-      w.act[b] = act;
-      w.ctx[b] = ctx;
-      freed = act && ((ctx - 1) % kv.page_size == 0);
+      freed = (n_ok == kv.Hkv && (ctx - 1) % P == 0) ? 1 : 0;
+      if (bb == b) s_act = n_ok == kv.Hkv ? 1 : 0;
     }
     int total;
     const int ex = block_exclusive_scan(freed, tmp, &total);
-    if (b < kv.B) w.off_push[b] = s_run + ex;
-    __syncthreads();
-    if (tid == 0) s_run += total;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    w.ctrl->abort = s_bad;
-    w.ctrl->top0 = *kv.free_top;
-    w.ctrl->total_push = s_run;
-  }
-}
-
-// grid: B; one warp per KV head.
-__global__ void __launch_bounds__(256) move_last_apply_kernel(se_paged_kv kv,
-                                                              const int32_t* __restrict__ victim,
-                                                              float* aux, int64_t aux_stride,
-                                                              MoveWs w) {
-  pdl_enter();
-  if (w.ctrl->abort) return;
-  const int b = blockIdx.x;
-  if (!w.act[b]) return;
-  const int P = kv.page_size;
-  const int last = w.ctx[b] - 1;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int esz = (int)elem_size(kv.dtype);
-  const int64_t row_bytes = (int64_t)kv.D * esz;
-  const int chunks = (int)(row_bytes / 16);
-  const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
-  const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
-  const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
-  for (int h = warp; h < kv.Hkv; h += blockDim.x >> 5) {
-    const int v = victim[b * kv.Hkv + h];
-    if (v != last) {
-      const int64_t so = (int64_t)bt[last / P] * page_bytes + ((int64_t)h * P + last % P) * row_bytes;
-      const int64_t dof = (int64_t)bt[v / P] * page_bytes + ((int64_t)h * P + v % P) * row_bytes;
-      for (int c = lane; c < chunks; c += 32) {
-        const uint4 k4 = ldg_v4(static_cast<const char*>(kv.k_pool) + so + c * 16);
-        const uint4 v4 = ldg_v4(static_cast<const char*>(kv.v_pool) + so + c * 16);
-        stg_v4(static_cast<char*>(kv.k_pool) + dof + c * 16, k4);
-        stg_v4(static_cast<char*>(kv.v_pool) + dof + c * 16, v4);
-      }
-    }
-    if (lane == 0) {
-      int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
-      const int pos = sm[last];
-      sm[v] = pos;
-      sm[last] = -1;
-      if (aux != nullptr) {
-        float* ar = aux + ((int64_t)b * kv.Hkv + h) * aux_stride;
-        const float a = ar[last];
-        ar[v] = a;
-        ar[last] = 0.f;
-      }
-    }
+    if (bb == b) s_off = run + ex;
+    run += total;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    kv.ctx_len[b] = last;
-    if (last % P == 0) {
+  const bool bad = s_bad != 0;
+  if (!bad && s_act) {
+    const int last = kv.ctx_len[b] - 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int esz = (int)elem_size(kv.dtype);
+    const int64_t row_bytes = (int64_t)kv.D * esz;
+    const int chunks = (int)(row_bytes / 16);
+    const int64_t page_bytes = (int64_t)kv.Hkv * P * row_bytes;
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
+    for (int h = warp; h < kv.Hkv; h += blockDim.x >> 5) {
+      const int v = victim[b * kv.Hkv + h];
+      if (v != last) {
+        const int64_t so = (int64_t)bt[last / P] * page_bytes + ((int64_t)h * P + last % P) * row_bytes;
+        const int64_t dof = (int64_t)bt[v / P] * page_bytes + ((int64_t)h * P + v % P) * row_bytes;
+        for (int c = lane; c < chunks; c += 32) {
+          const uint4 k4 = ldg_v4(static_cast<const char*>(kv.k_pool) + so + c * 16);
+          const uint4 v4 = ldg_v4(static_cast<const char*>(kv.v_pool) + so + c * 16);
+          stg_v4(static_cast<char*>(kv.k_pool) + dof + c * 16, k4);
+          stg_v4(static_cast<char*>(kv.v_pool) + dof + c * 16, v4);
+        }
+      }
+      if (lane == 0) {
+        int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+        const int pos = sm[last];
+        sm[v] = pos;
+        sm[last] = -1;
+        if (aux != nullptr) {
+          float* ar = aux + ((int64_t)b * kv.Hkv + h) * aux_stride;
+          const float a = ar[last];
+          ar[v] = a;
+          ar[last] = 0.f;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && last % P == 0) {
       const int page = bt[last / P];
       kv.block_table[(int64_t)b * kv.max_pages_per_seq + last / P] = -1;
       if (kv.page_refcount) kv.page_refcount[page] = 0;
-      kv.free_list[w.ctrl->top0 + w.off_push[b]] = page;
+      kv.free_list[top0 + s_off] = page;
     }
-    if (b == 0) *kv.free_top = w.ctrl->top0 + w.ctrl->total_push;
+  }
+  if (finish_cta(&w.ctrl->done) && !bad) {
+    for (int bb = tid; bb < kv.B; bb += blockDim.x) {
+      const int ctx = kv.ctx_len[bb];
+      int n_ok = 0;
+      for (int h = 0; h < kv.Hkv; ++h) {
+        const int v = victim[bb * kv.Hkv + h];
+        n_ok += (v >= 0 && v < ctx);
+      }
+      if (n_ok == kv.Hkv) kv.ctx_len[bb] = ctx - 1;
+    }
+    if (tid == 0) *kv.free_top = top0 + run;
   }
 }
 
@@ -424,82 +419,31 @@ __global__ void __launch_bounds__(256) move_last_apply_kernel(se_paged_kv kv,
 
 struct AppendWs {
   CompactCtrl* ctrl;
-  int32_t* base;     // [B] pop rank of the sequence's first fresh page
-  int32_t* ctx;      // [B] snapshot
-  int32_t* logical;  // [B] snapshot
 };
 
 static AppendWs carve_append(const se_paged_kv* kv, void* ws, size_t* bytes) {
   WsCarver c(ws);
   AppendWs w;
   w.ctrl = c.take<CompactCtrl>(1);
-  w.base = c.take<int32_t>(kv->B);
-  w.ctx = c.take<int32_t>(kv->B);
-  w.logical = c.take<int32_t>(kv->B);
   *bytes = c.bytes();
   return w;
 }
 
-// 1 CTA: bounds, fresh pages per sequence (blocks cdiv(ctx, P) ..
-// cdiv(ctx + n, P) - 1), pop ranks in ascending (b, block), capacity.
-__global__ void __launch_bounds__(1024) append_plan_kernel(se_paged_kv kv, int n, AppendWs w) {
-  pdl_enter();
-  __shared__ int tmp[33];
-  __shared__ int s_bad, s_run;
-  const int tid = threadIdx.x;
+// Block blockIdx.x of the append of sequence b (see append_kernel); base:
+// pop rank of the sequence's first fresh page, top0: the free-list top
+// before the call.
+SE_DEV void append_fill_body(se_paged_kv kv, const void* __restrict__ k_new,
+                             const void* __restrict__ v_new, int n, float* aux, int64_t aux_stride,
+                             void* kmin, void* kmax, int b, int base, int top0) {
   const int P = kv.page_size;
-  if (tid == 0) { s_bad = 0; s_run = 0; }
-  __syncthreads();
-  const int top0 = *kv.free_top;
-  for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
-    const int b = b0 + tid;
-    int need = 0;
-    if (b < kv.B) {
-      const int ctx = kv.ctx_len[b];
-      if (ctx < 0 || (int64_t)ctx + n > (int64_t)kv.max_pages_per_seq * P) {
-        set_status(kv.status, SE_ERR_BOUNDS);
-        atomicExch(&s_bad, 1);
-      } else {
-        need = cdiv(ctx + n, P) - cdiv(ctx, P);
-      }
-      w.ctx[b] = ctx;
-      w.logical[b] = kv.logical_len[b];
-    }
-    int total;
-    const int ex = block_exclusive_scan(need, tmp, &total);
-    if (b < kv.B) w.base[b] = s_run + ex;
-    __syncthreads();
-    if (tid == 0) s_run += total;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    const bool bad = s_bad || s_run > top0;
-    if (!s_bad && s_run > top0) set_status(kv.status, SE_ERR_OUT_OF_PAGES);
-    w.ctrl->abort = bad ? 1 : 0;
-    w.ctrl->top0 = top0;
-    w.ctrl->total_new = s_run;
-  }
-}
-
-// grid: (cdiv(n + P - 1, P), B), 256 threads.  CTA (j, b) fills block
-// ctx / P + j of sequence b: K/V rows, slot map, aux, Quest bounds, and the
-// block-table entry of a fresh page.  CTA (0, b) commits the lengths.
-__global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
-                                                           const void* __restrict__ k_new,
-                                                           const void* __restrict__ v_new, int n,
-                                                           float* aux, int64_t aux_stride,
-                                                           void* kmin, void* kmax, AppendWs w) {
-  pdl_enter();
-  if (w.ctrl->abort) return;
-  const int b = blockIdx.y;
-  const int P = kv.page_size;
-  const int ctx = w.ctx[b];
+  const int ctx = kv.ctx_len[b];
+  const int logical = kv.logical_len[b];
   const int blk = ctx / P + blockIdx.x;
   const int s0 = max(ctx, blk * P), s1 = min(ctx + n, (blk + 1) * P);   // slots filled here
   const int64_t mps = kv.max_pages_per_seq;
   if (s0 < s1) {
     const bool fresh = blk * P >= ctx;   // the block held nothing before
-    const int page = fresh ? kv.free_list[w.ctrl->top0 - 1 - (w.base[b] + blk - cdiv(ctx, P))]
+    const int page = fresh ? kv.free_list[top0 - 1 - (base + blk - cdiv(ctx, P))]
                            : kv.block_table[b * mps + blk];
     const int esz = (int)elem_size(kv.dtype);
     const int64_t row_bytes = (int64_t)kv.D * esz;
@@ -550,7 +494,7 @@ __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
     const int64_t smax = mps * P;
     for (int x = threadIdx.x; x < (s1 - s0) * kv.Hkv; x += blockDim.x) {
       const int slot = s0 + x / kv.Hkv, h = x % kv.Hkv;
-      kv.slot_map[((int64_t)b * kv.Hkv + h) * smax + slot] = w.logical[b] + (slot - ctx);
+      kv.slot_map[((int64_t)b * kv.Hkv + h) * smax + slot] = logical + (slot - ctx);
       if (aux != nullptr) aux[((int64_t)b * kv.Hkv + h) * aux_stride + slot] = 0.f;
     }
     if (threadIdx.x == 0 && fresh) {
@@ -558,12 +502,67 @@ __global__ void __launch_bounds__(256) append_apply_kernel(se_paged_kv kv,
       if (kv.page_refcount) kv.page_refcount[page] = 1;
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    kv.ctx_len[b] = ctx + n;
-    kv.logical_len[b] = w.logical[b] + n;
-    if (b == 0) *kv.free_top = w.ctrl->top0 - w.ctrl->total_new;
+
+}
+
+// Append in one launch.  grid: (cdiv(n + P - 1, P), B), 256 threads.  Every
+// CTA checks the bounds of every sequence and the free-list capacity and
+// takes its sequence's pop rank (fresh pages in ascending (b, block) order)
+// from a scan over the sequences; a call that fails a check changes nothing.
+// CTA (j, b) fills block ctx / P + j of sequence b: K/V rows, slot map, aux,
+// Quest bounds, and the block-table entry of a fresh page.  The last CTA to
+// finish commits both lengths of every sequence and the free-list top, which
+// every CTA read first.
+__global__ void __launch_bounds__(256) append_kernel(se_paged_kv kv,
+                                                     const void* __restrict__ k_new,
+                                                     const void* __restrict__ v_new, int n,
+                                                     float* aux, int64_t aux_stride,
+                                                     void* kmin, void* kmax, AppendWs w) {
+  pdl_enter();
+  __shared__ int tmp[33];
+  __shared__ int s_bad, s_base;
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const int P = kv.page_size;
+  const int top0 = *kv.free_top;
+  if (tid == 0) {
+    s_bad = 0;
+    s_base = 0;
+  }
+  __syncthreads();
+  int run = 0;   // fresh pages of the sequences before the current chunk
+  for (int b0 = 0; b0 < kv.B; b0 += blockDim.x) {
+    const int bb = b0 + tid;
+    int need = 0;
+    if (bb < kv.B) {
+      const int c = kv.ctx_len[bb];
+      if (c < 0 || (int64_t)c + n > (int64_t)kv.max_pages_per_seq * P) {
+        set_status(kv.status, SE_ERR_BOUNDS);
+        atomicExch(&s_bad, 1);
+      } else {
+        need = cdiv(c + n, P) - cdiv(c, P);
+      }
+    }
+    int total;
+    const int ex = block_exclusive_scan(need, tmp, &total);
+    if (bb == b) s_base = run + ex;
+    run += total;
+  }
+  __syncthreads();
+  bool bad = s_bad != 0;
+  if (!bad && run > top0) {
+    if (tid == 0) set_status(kv.status, SE_ERR_OUT_OF_PAGES);
+    bad = true;
+  }
+  if (!bad) append_fill_body(kv, k_new, v_new, n, aux, aux_stride, kmin, kmax, b, s_base, top0);
+  if (finish_cta(&w.ctrl->done) && !bad) {
+    for (int bb = tid; bb < kv.B; bb += blockDim.x) {
+      kv.ctx_len[bb] += n;
+      kv.logical_len[bb] += n;
+    }
+    if (tid == 0) *kv.free_top = top0 - run;
   }
 }
+
 
 // ---------------------------------------------------------------------------
 // Prefix-span pruning plan
@@ -872,8 +871,7 @@ extern "C" se_status se_compact_evict(const se_paged_kv* kv, int32_t mode,
     size_t need = 0;
     MoveWs w = carve_move(kv, workspace, &need);
     if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
-    se_launch(move_last_plan_kernel, 1, 1024, 0, st, *kv, keep_idx, w);
-    se_launch(move_last_apply_kernel, kv->B, 256, 0, st, *kv, keep_idx, aux, aux_stride, w);
+    se_launch(move_last_kernel, kv->B, 256, 0, st, *kv, keep_idx, aux, aux_stride, w);
     return se_last_launch_status();
   }
   return SE_ERR_INVALID_ARG;
@@ -951,10 +949,9 @@ extern "C" se_status se_append_kv(const se_paged_kv* kv, const void* k_new, cons
   if (workspace_bytes < need) return SE_ERR_INVALID_ARG;
   if (n_new == 0) return SE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  se_launch(append_plan_kernel, 1, 1024, 0, st, *kv, n_new, w);
   const dim3 grid(cdiv(n_new + kv->page_size - 1, kv->page_size), kv->B);
-  se_launch(append_apply_kernel, grid, 256, 0, st, *kv, k_new, v_new, n_new, aux, aux_stride, kmin, kmax,
-                                            w);
+  se_launch(append_kernel, grid, 256, 0, st, *kv, k_new, v_new, n_new, aux, aux_stride, kmin, kmax,
+            w);
   return se_last_launch_status();
 }
 

@@ -11,7 +11,30 @@ struct CompactCtrl {
   int32_t top0;
   int32_t total_new;
   int32_t total_push;
+  int32_t done;        // CTAs finished (finish_cta); zero between calls
 };
+
+// Counts the calling CTA as finished -- after a barrier over its threads and
+// a device-scope fence, so that every read and write of the CTA precedes the
+// count -- and returns, in every thread, whether it was the last CTA of the
+// grid.  The last one resets the counter for the next call.  No CTA waits
+// for another.
+SE_DEV bool finish_cta(int32_t* done) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int n = (int)(gridDim.x * gridDim.y * gridDim.z);
+    const bool last = atomicAdd(done, 1) == n - 1;
+    if (last) {
+      __threadfence();
+      *done = 0;
+    }
+    s_last = last ? 1 : 0;
+  }
+  __syncthreads();
+  return s_last != 0;
+}
 
 struct CompactWs {
   CompactCtrl* ctrl;

@@ -244,6 +244,10 @@ typedef enum { SE_COMPACT_FRESH_PAGES = 0, SE_COMPACT_MOVE_LAST = 1 } se_compact
  * aux (optional) [B][Hkv][aux_stride] fp32 per-slot metadata moved with the
  * entries (H2O running scores); vacated slots get 0.
  * Device errors: SE_ERR_OUT_OF_PAGES, SE_ERR_UNEVEN, SE_ERR_BOUNDS.
+ * Workspace: se_compact_evict_workspace_size bytes, zeroed before its first
+ * use (MOVE_LAST keeps a count of finished CTAs there that every completed
+ * call leaves at zero); calls that share a workspace must not overlap on the
+ * GPU.
  */
 se_status se_compact_evict(const se_paged_kv* kv, int32_t mode, const int32_t* keep_idx,
                            int32_t keep_stride, const int32_t* n_keep,
@@ -430,6 +434,9 @@ se_status se_sparse_decode_attn_static(const se_paged_kv* kv, const void* q, int
  * Host errors: SE_ERR_INVALID_ARG (null buffers, n_new < 0, workspace too
  * small).  Device errors (nothing written): SE_ERR_BOUNDS (a sequence would
  * exceed max_pages_per_seq pages), SE_ERR_OUT_OF_PAGES.
+ * Workspace: se_append_kv_workspace_size bytes, zeroed before its first use
+ * (it holds a count of finished CTAs that every completed call leaves at
+ * zero); calls that share a workspace must not overlap on the GPU.
  */
 se_status se_append_kv(const se_paged_kv* kv, const void* k_new, const void* v_new,
                        int32_t n_new, float* aux, int64_t aux_stride, void* kmin, void* kmax,
