@@ -637,7 +637,7 @@ def run_h2o(args, torch, rank, world):
     roof = dict(bound="hbm", achieved=detail["step_gbs"], unit="GB/s", kernel="h2o step",
                 per_launch=f"{kv_bytes:.4g} B")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
-                launches=2 + 1 + 1 + 2, metric="decode tokens/s", e2e=None,
+                launches=1 + 1 + 1 + 1, metric="decode tokens/s", e2e=None,   # append, decode, evict-one, move-last
                 cfg={"workload": f"h2o_decode: B={shape.B}, 4096-token prompt, budget 1024+128, "
                                  "32/8 heads, d=128, bf16", "l2": "inputs larger than L2"},
                 dtype="bf16")
@@ -827,7 +827,7 @@ def run_kara_schedule(args, torch, rank, world):
                 kernel="kara schedule step (append + decode + staggered compression)",
                 per_launch=f"{kv_bytes:.4g} B (resident K/V attended per step)")
     return dict(tokens=shape.B, ms=ms, wall=t_wall, clocks=clocks, detail=detail, roof=roof,
-                launches=2 + 1 + (3 + 1 + 3) * detail["compressions_per_step"],
+                launches=1 + 1 + (3 + 1 + 3) * detail["compressions_per_step"],   # append, decode, compressions
                 metric="decode tokens/s", e2e=None,
                 cfg={"workload": f"kara_schedule: B={shape.B} decoding over 2304 resident tokens, "
                                  "Kara window 256 (32 protected, 32 candidates, chunk budget 64) "
