@@ -594,7 +594,15 @@ static PruneWs carve_prune(const se_paged_kv* kv, void* ws, size_t* bytes) {
   return w;
 }
 
+// Slots per thread and round of the prune plan's keep-list scan.
+constexpr int kPruneItems = 4;
+
 // grid: B, 1024 threads.  Builds per-head keep lists for R' = (R \ T) U I.
+// The first rewritten slot is the lowest slot of any head whose position is
+// at least L: each thread stops at its first such slot of a head (its slots
+// are visited in increasing order) and the warps meet in one shared minimum.
+// The keep lists come from one block scan per kPruneItems x 1024 slots, each
+// thread taking kPruneItems consecutive slots in order.
 __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
                                                           const int32_t* __restrict__ Lp,
                                                           const int32_t* __restrict__ Rp,
@@ -611,10 +619,19 @@ __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
   const int64_t smax = (int64_t)kv.max_pages_per_seq * P;
   if (tid == 0) { s_first = ctx; s_busy = 0; s_count0 = -1; s_bad = 0; }
   __syncthreads();
-  for (int h = 0; h < kv.Hkv; ++h) {
-    const int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
-    for (int s = tid; s < ctx; s += blockDim.x)
-      if (sm[s] >= L) atomicMin(&s_first, s);
+  {
+    int first = ctx;
+    for (int h = 0; h < kv.Hkv; ++h) {
+      const int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
+      for (int s = tid; s < min(ctx, first); s += blockDim.x)
+        if (sm[s] >= L) {
+          first = s;
+          break;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+    if ((tid & 31) == 0 && first < ctx) atomicMin(&s_first, first);
   }
   __syncthreads();
   const int fs = s_first;
@@ -629,27 +646,35 @@ __global__ void __launch_bounds__(1024) prune_plan_kernel(se_paged_kv kv,
     const int32_t* sm = kv.slot_map + ((int64_t)b * kv.Hkv + h) * smax;
     int32_t* keep = w.keep + ((int64_t)b * kv.Hkv + h) * smax;
     int running = 0;
-    for (int c0 = fs; c0 < ctx; c0 += blockDim.x) {
-      const int s = c0 + tid;
-      int k = 0;
-      if (s < ctx) {
-        const int pos = sm[s];
-        const bool in_T = pos >= L && pos < R;
+    for (int c0 = fs; c0 < ctx; c0 += blockDim.x * kPruneItems) {
+      const int s0 = c0 + tid * kPruneItems;
+      int pos[kPruneItems];
+#pragma unroll
+      for (int i = 0; i < kPruneItems; ++i) pos[i] = s0 + i < ctx ? sm[s0 + i] : -1;
+      bool k[kPruneItems];
+      int n = 0;
+#pragma unroll
+      for (int i = 0; i < kPruneItems; ++i) {
+        const int s = s0 + i;
         bool leaves = false;
-        if (in_T) {
-          if (pos - L >= mask_stride) {
+        if (s < ctx && pos[i] >= L && pos[i] < R) {
+          if (pos[i] - L >= mask_stride) {
             set_status(kv.status, SE_ERR_BOUNDS);
             atomicExch(w.abort, 1);
           }
-          const bool in_I = pos - L < mask_stride && mask[(int64_t)b * mask_stride + (pos - L)] != 0;
+          const bool in_I =
+              pos[i] - L < mask_stride && mask[(int64_t)b * mask_stride + (pos[i] - L)] != 0;
           const bool busy = kv.page_refcount != nullptr && kv.page_refcount[bt[s / P]] > 1;
           leaves = !in_I && !busy;
         }
-        k = leaves ? 0 : 1;
+        k[i] = s < ctx && !leaves;
+        n += k[i] ? 1 : 0;
       }
       int total;
-      const int ex = block_exclusive_scan(k, tmp, &total);
-      if (k) keep[running + ex] = s;
+      int at = running + block_exclusive_scan(n, tmp, &total);
+#pragma unroll
+      for (int i = 0; i < kPruneItems; ++i)
+        if (k[i]) keep[at++] = s0 + i;
       running += total;
     }
     if (tid == 0) {

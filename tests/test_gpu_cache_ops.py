@@ -313,6 +313,43 @@ def test_prune_span_matches_oracle(cuda_lib, busy):
     assert nb.cpu().tolist() == n_busy
 
 
+def test_prune_span_long_context_matches_oracle(cuda_lib):
+    """Contexts of several plan rounds (4601 slots; the plan scans 4096 a
+    round) with a ragged tail, heads that differ above slot 4000 (each keeps
+    its own 601 of the positions [4000, 5003)).  Sequence 0 prunes a span over
+    both rounds; sequence 1's span starts where the heads differ, so the first
+    rewritten slot is the lowest over the heads (everything in the span is kept,
+    so the heads stay even); sequence 2's span lies past every position and
+    leaves it as it is."""
+    se = cuda_lib
+    shape, pc = _cache(torch.bfloat16, 128, B=3, Hkv=2, ctx=5003, spare=300, tag="prl")
+    c = ocache.from_tensors(pc)
+    rng = np.random.default_rng(11)
+    keep = [[np.sort(rng.choice(np.arange(4000, 5003), 601, replace=False)) for _ in range(2)]
+            for _ in range(3)]
+    assert ocache.compact(c, keep, [4000] * 3) == ocache.SE_OK
+    _gpu_compact(se, shape, pc, keep, [4000] * 3)
+    torch.cuda.synchronize()
+    H.assert_cache_equal(pc, c)
+    firsts = [int(np.argmax(c.slot_map[1, h, :4601] >= 4300)) for h in range(2)]
+    assert firsts[0] != firsts[1]       # the heads reach the span at different slots
+    L, R = [100, 4300, 6000], [3900, 5003, 7000]
+    mask = np.zeros((3, 3800), dtype=np.uint8)
+    mask[0, rng.choice(3800, 760, replace=False)] = 1
+    mask[1, :] = 1
+    st, n_busy = ocache.prune(c, L, R, mask)
+    assert st == ocache.SE_OK
+    nb = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    se.se_prune_span(se.kv_desc(pc, shape.Hq), torch.tensor(L, dtype=torch.int32, device="cuda"),
+                     torch.tensor(R, dtype=torch.int32, device="cuda"),
+                     torch.from_numpy(mask).cuda(), n_busy=nb)
+    torch.cuda.synchronize()
+    assert H.status(pc) == 0
+    H.assert_cache_equal(pc, c)
+    assert nb.cpu().tolist() == n_busy
+    assert int(c.ctx_len[2]) == 4601
+
+
 def test_prune_uneven_heads_is_rejected(cuda_lib):
     se = cuda_lib
     shape, pc = _cache(torch.bfloat16, 128, B=1, Hkv=2, ctx=64, tag="pru")
