@@ -348,28 +348,9 @@ SE_DEV void colsum_block(const uint32_t (&r)[N], bool fast, int kpos, const floa
 }
 
 // Column sum of one key over 32 NB rows held in TMEM at tb (lane = key,
-// columns = rows): NB 32-row blocks, each loaded while the previous one is
-// summed.
-template <int NB>
-SE_DEV void colsum_tile(uint32_t tb, bool fast, int kpos, const float* lse_s, const int* qp_s,
-                        float scale, float& cs0, float& cs1, float& cs2, float& cs3) {
-  uint32_t ra[32], rb[32];
-  tc::tmem_ld32_async(tb, ra);
-  tc::tmem_wait32(ra);
-#pragma unroll 1
-  for (int c = 0; c < NB; c += 2) {
-    tc::tmem_ld32_async(tb + (c + 1) * 32, rb);
-    colsum_block(ra, fast, kpos, lse_s + c * 32, qp_s + c * 32, scale, cs0, cs1, cs2, cs3);
-    tc::tmem_wait32(rb);
-    if (c + 2 < NB) tc::tmem_ld32_async(tb + (c + 2) * 32, ra);
-    colsum_block(rb, fast, kpos, lse_s + (c + 1) * 32, qp_s + (c + 1) * 32, scale, cs0, cs1, cs2,
-                 cs3);
-    if (c + 2 < NB) tc::tmem_wait32(ra);
-  }
-}
-
-// colsum_tile without the prefetch (one 32-row block in registers at a time),
-// for kernels whose warps are many enough to cover the load latency.
+// columns = rows), one 32-row block in registers at a time: the epilogue's
+// sixteen warps cover the load latency (loading the next block while summing
+// the current one measured slower).
 template <int NB>
 SE_DEV void colsum_tile_seq(uint32_t tb, bool fast, int kpos, const float* lse_s, const int* qp_s,
                             float scale, float& cs0, float& cs1, float& cs2, float& cs3) {
