@@ -880,8 +880,8 @@ SE_DEV int group_tiles(const TcArgs& a, int bg) {
 
 // ---------------------------------------------------------------------------
 // Pass 1, persistent form for one row chunk (RC == 1).  grid = the number of
-// SMs; CTA c takes tiles [c T / C, (c+1) T / C) of the global (group, tile)
-// sequence.  Each epilogue thread keeps its row's running max / sum per group
+// SMs; CTA c takes an equal share of the global (group, tile) sequence, a
+// group change counted as kSwitchTiles tiles (cta_tiles).  Each epilogue thread keeps its row's running max / sum per group
 // and writes it, when the group ends in this CTA, to the partial slots of
 // this CTA: part[(group * 256 + row) * 2C + 2c + half].  The persistent pass 2
 // merges the slots of the CTAs whose ranges meet a group when it starts it.
@@ -925,8 +925,43 @@ SE_DEV void locate_pre(const int* s_pre, int groups, int x, int& bg, int& tile) 
   tile = x - s_pre[bg];
 }
 
-// The CTA whose range [c T / C, (c+1) T / C) holds tile x.
+// The CTA whose range [c T / C, (c+1) T / C) holds work coordinate x.
 SE_DEV int cta_of(int64_t x, int64_t T, int64_t C) { return (int)(((x + 1) * C - 1) / T); }
+
+// The persistent passes split work coordinates, not tiles, evenly over the
+// CTAs: tile t of group g sits at t + kSwitchTiles * g, so a CTA whose range
+// crosses into a new group takes kSwitchTiles fewer tiles.  The change costs
+// the CTA a Q load, a pipeline drain and refill and, in pass 2, the merge of
+// the group's row statistics: on the SnapKV shape (32 groups of 256 tiles
+// over 152 CTAs) 2 measured no gain, 4 and 6 cut the two passes by 4 and
+// 6 us, 8 no further.
+constexpr int kSwitchTiles = 6;
+
+SE_DEV int64_t work_total(const int* s_pre, int groups) {
+  return s_pre[groups] + (int64_t)kSwitchTiles * groups;
+}
+
+// Work coordinate of global tile x of group bg.
+SE_DEV int64_t work_of(int x, int bg) { return x + (int64_t)kSwitchTiles * bg; }
+
+// The first global tile whose work coordinate is at least X (all tiles, if
+// none): the first group whose last tile reaches X, from there.
+SE_DEV int tile_at_work(const int* s_pre, int groups, int64_t X) {
+  int lo = 0, hi = groups;   // smallest bg with work_of(last tile of bg) >= X, groups if none
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (work_of(s_pre[mid + 1] - 1, mid) >= X) hi = mid; else lo = mid + 1;
+  }
+  if (lo == groups) return s_pre[groups];
+  return (int)max((int64_t)s_pre[lo], X - (int64_t)kSwitchTiles * lo);
+}
+
+// The CTA's tile range [x0, x1) of the global (group, tile) sequence.
+SE_DEV void cta_tiles(const int* s_pre, int groups, int& x0, int& x1) {
+  const int64_t TW = work_total(s_pre, groups);
+  x0 = tile_at_work(s_pre, groups, (int64_t)blockIdx.x * TW / gridDim.x);
+  x1 = tile_at_work(s_pre, groups, (int64_t)(blockIdx.x + 1) * TW / gridDim.x);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
@@ -957,9 +992,7 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    const int total = s_pre[groups];
-    s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
-    s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    cta_tiles(s_pre, groups, s_range[0], s_range[1]);
     for (int i = 0; i < KS; ++i) {
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], 1);
@@ -1144,10 +1177,12 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
 // tile range meets the group; n_ctas CTAs ran pass 1); +inf when the row saw
 // no key.
 SE_DEV float row_lse2(const TcArgs& a, const int* s_pre, int groups, int bg, int r, int n_ctas) {
-  const int64_t T = s_pre[groups], gstart = s_pre[bg];
+  const int64_t TW = work_total(s_pre, groups);
+  const int gstart = s_pre[bg];
   const int n = s_pre[bg + 1] - s_pre[bg];
-  if (n <= 0 || T <= 0) return INFINITY;
-  const int first = cta_of(gstart, T, n_ctas), last = cta_of(gstart + n - 1, T, n_ctas);
+  if (n <= 0 || s_pre[groups] <= 0) return INFINITY;
+  const int first = cta_of(work_of(gstart, bg), TW, n_ctas);
+  const int last = cta_of(work_of(gstart + n - 1, bg), TW, n_ctas);
   const float* p = a.part + ((int64_t)bg * kRowChunk + r) * 2 * n_ctas * 2;
   float M = -INFINITY;
   for (int c = 2 * first; c <= 2 * last + 1; ++c) M = fmaxf(M, p[2 * c]);
@@ -1159,9 +1194,10 @@ SE_DEV float row_lse2(const TcArgs& a, const int* s_pre, int groups, int bg, int
 
 // ---------------------------------------------------------------------------
 // Pass 2, persistent form for one row chunk (RC == 1: w * G <= 256 rows).
-// grid = the number of SMs; CTA c takes an equal contiguous share of the
-// global sequence of (group, key tile) pairs, so the last wave is full and the
-// pipeline runs across tiles of consecutive groups without refilling.  The Q
+// grid = the number of SMs; CTA c takes the contiguous share of the global
+// sequence of (group, key tile) pairs that pass 1 took (cta_tiles), so the
+// last wave is full and the pipeline runs across tiles of consecutive groups
+// without refilling.  The Q
 // chunk and row info of a group are loaded when the group changes (after the
 // MMA and both epilogue sets are done with the previous ones).  One set of
 // eight epilogue warps takes the CTA's even local tiles (TMEM buffer 0), the
@@ -1205,9 +1241,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    const int total = s_pre[groups];
-    s_range[0] = (int)((int64_t)blockIdx.x * total / gridDim.x);
-    s_range[1] = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    cta_tiles(s_pre, groups, s_range[0], s_range[1]);
     for (int i = 0; i < KS; ++i) {
       tc::mbar_init(&kfull[i], 1);
       tc::mbar_init(&kempty[i], 1);
