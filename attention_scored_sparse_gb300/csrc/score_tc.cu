@@ -1209,7 +1209,12 @@ SE_DEV float row_lse2(const TcArgs& a, const int* s_pre, int groups, int bg, int
 __global__ void __launch_bounds__(kThreads, 1)
 score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap qmap, TcArgs a) {
-  pdl_enter();
+  // Of pass 1's output this kernel reads only the partial row statistics, in
+  // the epilogue warps; everything else it reads was written before pass 1
+  // started (pass 1 began with its own wait for those writers).  So only the
+  // epilogue waits for pass 1: the set-up, the Q and K loads and the first
+  // MMAs overlap pass 1's last CTAs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int KS = 4;
@@ -1356,6 +1361,7 @@ score_colsum_persistent_tc(const __grid_constant__ CUtensorMap kmap,
     // ---------------- epilogue: one key per thread and row half ----------------
     // 16 warps: (tile parity set, TMEM lane quarter, row half); the second
     // half hands its partial sums to the first through s_half.
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // pass 1's partial statistics
     const int e = warp - 2;
     const int set = (e >> 2) & 1;
     const int half = e >> 3;
