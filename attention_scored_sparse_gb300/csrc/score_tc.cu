@@ -1164,6 +1164,16 @@ score_rowstats_persistent_tc(const __grid_constant__ CUtensorMap kmap,
       p[0] = m;
       p[1] = l;
     }
+    // fewer tiles than CTAs: a CTA with an empty range may sit inside the
+    // span of the group that holds the next tile, and pass 2 merges the slots
+    // of every CTA in that span, so its slots of that group read as empty
+    if (n_my == 0 && x0 < s_pre[groups] && row_ok) {
+      int bg0 = 0, t0 = 0;
+      locate_pre(s_pre, groups, x0, bg0, t0);
+      float* p = a.part + (((int64_t)bg0 * kRowChunk + r) * 2 * gridDim.x + 2 * blockIdx.x + half) * 2;
+      p[0] = -INFINITY;
+      p[1] = 0.f;
+    }
   }
   __syncthreads();
   if (warp == 1) {

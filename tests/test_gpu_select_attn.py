@@ -473,6 +473,37 @@ def test_score_window_accumulates(cuda_lib):
     H.assert_scores_close(scores[0, 0].cpu().double().numpy(), 1.0 + 2 * row, torch.float32, w, G)
 
 
+def test_score_window_short_range_after_long_on_one_workspace(cuda_lib):
+    """One row chunk (the persistent kernels) with far fewer key tiles than
+    CTAs: 8 groups of 2 tiles (a 256-key range) under n_max = 4096, on a
+    workspace that a 4096-key call has just used.  Pass 2 merges the pass-1
+    slots of every CTA in a group's span, CTAs without tiles included; those
+    must read as empty, not as the earlier call's statistics."""
+    se = cuda_lib
+    B, Hkv, G, w, ctx = 1, 8, 4, 64, 4096
+    shape = W.Shape(name="scs", B=B, Hq=Hkv * G, Hkv=Hkv, D=128, page_size=16, ctx=ctx,
+                    dtype=torch.bfloat16)
+    pc = W.build_paged_cache(shape, num_pages=B * W.cdiv(ctx, 16) + 2, max_ctx=ctx, device="cuda",
+                             tag="scs")
+    q_win = W.normal((B, w, shape.Hq, 128), torch.bfloat16, "cuda", "scs", "q")
+    kv = se.kv_desc(pc, shape.Hq)
+    ws = torch.zeros(se._lib.se_score_window_workspace_size(kv, w, ctx), dtype=torch.uint8,
+                     device="cuda")
+    c = ocache.from_tensors(pc)
+    for n in (ctx, 256):
+        q_pos = torch.arange(n - w, n, dtype=torch.int32)[None].cuda()
+        z, hi = H.ranges(B, 0, n)
+        out = torch.full((B, Hkv, ctx), -5.0, device="cuda")
+        se.se_score_window(kv, q_win, q_pos, z, hi, z, hi, causal=True, accumulate=False,
+                           n_max=ctx, scores=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert H.status(pc) == 0
+        ref = oscore.score_window(c, q_win, q_pos.cpu().numpy(), [0], [n], [0], [n], True)
+        sg = out.cpu().double().numpy()
+        for (b, g), row in ref.items():
+            H.assert_scores_close(sg[b, g, :n], row, torch.bfloat16, w, G)
+
+
 @pytest.mark.parametrize("w", [64, 100])
 def test_score_window_wait_limit_runs_out(cuda_lib, w):
     """The default (two-launch) tcgen05 scorer honours the wait limit in the
