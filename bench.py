@@ -395,12 +395,12 @@ def run_snapkv(args, torch, rank, world):
     detail["compact_and_decode_frac_of_hbm"] = detail["compact_and_decode_gbs"] / hbm
     detail["compact_frac_of_hbm"] = detail["compact_gbs"] / hbm
     detail["decode_frac_of_hbm"] = detail["decode_gbs"] / hbm
-    # DRAM bytes of one se_score_window call on this workload, both passes
-    # (dram__bytes_read.sum + dram__bytes_write.sum under ncu on GB300:
-    # 275.99 + 3.33 MB and 278.70 + 2.75 MB), for the current scorer kernels
+    # DRAM bytes of one se_score_window call: none measured on the current
+    # scorer kernels (the last ncu capture, 275.99 + 3.33 MB and 278.70 +
+    # 2.75 MB for the two passes, predates a change to pass 1)
     roof = dict(bound="tensor", achieved=detail["score_tflops"], unit="TFLOP/s",
                 kernel="se_score_window", per_launch=f"{flops:.4g} FLOP (one QK^T sweep)",
-                traffic=(275.99 + 3.33 + 278.70 + 2.75) * 1e6 if shape.name == "snapkv_llama8b" else None)
+                traffic=None)
     launches = 2 + 1 + 3         # score (2), select, compaction plan + compaction/decode + commit
     cfg = {"workload": f"{shape.name}: B={B} x {shape.ctx} tokens, Hq={shape.Hq}/Hkv={Hkv}, "
                        f"d={D}, window {shape.window}, pool {shape.pool_kernel}, budget "
